@@ -1,0 +1,220 @@
+/*
+ * kvq.h -- C ABI of the GB300 (sm_103a) quantized paged-KV attention library.
+ *
+ * The library implements the hot path described on three pages about
+ * vLLM's quantized KV cache (prhub.com.cn summaries of vLLM pull requests):
+ *
+ *   [P1] vllm PR 39445 "CPU 后端新增 FP8 KV 缓存量化支持": an fp8 KV cache;
+ *        entry points cpu_attn_reshape_and_cache / cpu_attention_with_kv_cache
+ *        that take kv_cache_dtype, k_scale and v_scale (Breakdown items 1-4).
+ *   [P2] vllm PR 50194 "修复 CPU FP8 注意力调度器临时缓冲区大小计算错误":
+ *        get_scheduler_metadata must size its tiles and scratch from the KV
+ *        cache element size, not the query's (Motivation, Key source snippet).
+ *   [P3] vllm PR 38378 "为 Triton 注意力后端引入 KV 缓存按令牌头 INT8/FP8 量化":
+ *        int8 / fp8 per-(token, head) dynamic absmax scales stored inline in a
+ *        padded head row (Breakdown item 3, Risks).
+ *
+ * Conventions for every call:
+ *   - Device pointers point to memory of the CUDA device that is current on
+ *     the calling thread; host pointers are named *_host.
+ *   - `stream` is a cudaStream_t passed as void* (NULL = legacy default
+ *     stream).  Kernels are enqueued on it; calls do not synchronise, so a
+ *     kernel fault surfaces at the caller's next stream synchronisation.
+ *   - The caller owns every buffer it passes.  The library owns only the
+ *     kvq_sched_t objects it creates (freed with kvq_sched_destroy).  No call
+ *     except kvq_get_scheduler_metadata allocates device memory.
+ *   - Every call returns KVQ_OK (0) or a negative KVQ_E_* status; no call
+ *     throws, exits or prints.  Arguments are checked on the host before any
+ *     launch; a call that returns an error has enqueued nothing.
+ *   - bf16 tensors are IEEE bfloat16 bit patterns (uint16), little endian.
+ */
+#ifndef KVQ_H_
+#define KVQ_H_
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+/* ---- status codes ---------------------------------------------------- */
+#define KVQ_OK 0
+#define KVQ_E_INVALID_ARG (-1)      /* a pointer, size, stride or value is invalid */
+#define KVQ_E_UNSUPPORTED (-2)      /* dtype / head_dim / GQA ratio not built      */
+#define KVQ_E_SCHED_MISMATCH (-3)   /* sched built for other dtype/heads/head_dim  */
+#define KVQ_E_WORKSPACE_TOO_SMALL (-4)
+#define KVQ_E_CUDA (-5)             /* a CUDA runtime call or launch failed        */
+#define KVQ_E_NO_MEMORY (-6)        /* host or device allocation failed            */
+
+/* ---- KV cache data types -------------------------------------------------
+ * 0..2 keep the kv_cache_dtype indices printed in [P2]'s source snippet
+ * ("0 = kAuto, 1 = kFp8E4M3, 2 = kFp8E5M2"); 3 and 4 are [P3]'s modes.
+ *
+ *   KVQ_AUTO                 bf16 cache, row = 2*D bytes (no quantisation)
+ *   KVQ_FP8_E4M3             OCP E4M3FN codes, per-tensor scale, row = D bytes
+ *   KVQ_FP8_E5M2             OCP E5M2 codes, per-tensor scale, row = D bytes
+ *   KVQ_INT8_PER_TOKEN_HEAD  int8 codes + inline fp32 scale, row = D+16 bytes
+ *   KVQ_FP8_PER_TOKEN_HEAD   E4M3FN codes + inline fp32 scale, row = D+16 bytes
+ *
+ * Per-token-head row layout: [D codes][scale: little-endian fp32][12 zero
+ * bytes]; the 16-byte pad keeps every row 16-byte aligned.
+ */
+typedef enum {
+  KVQ_AUTO = 0,
+  KVQ_FP8_E4M3 = 1,
+  KVQ_FP8_E5M2 = 2,
+  KVQ_INT8_PER_TOKEN_HEAD = 3,
+  KVQ_FP8_PER_TOKEN_HEAD = 4
+} kvq_dtype_t;
+
+/* Opaque schedule (work list + sizes), owned by the library. */
+typedef struct kvq_sched kvq_sched_t;
+
+/* Parse a kv_cache_dtype string.  Accepts "auto" (the default of [P2]
+ * Breakdown item 2), "fp8" (alias of fp8_e4m3), "fp8_e4m3", "fp8_e5m2",
+ * "int8_per_token_head", "fp8_per_token_head".  s == NULL or "" reads as
+ * "auto".  Unknown strings: KVQ_E_INVALID_ARG. */
+int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out);
+
+/* Bytes of one (token, kv_head) cache row: 2*D (AUTO), D (per-tensor fp8)
+ * or D+16 (per-token-head).  head_dim must be a positive multiple of 16. */
+int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
+
+/* reshape_and_cache -- quantise new K/V tokens into the paged caches.
+ * [P1] Breakdown item 1 (the reshape kernel writing the fp8 cache) and
+ * Key files (cpu_attn_reshape_and_cache); [P3] Breakdown item 3
+ * (_reshape_cache_per_token_head: dynamic per-(token, head) absmax scale).
+ *
+ *   key, value        device bf16 [num_tokens, num_heads_kv, head_dim]; heads
+ *                     and dims contiguous; token stride given in elements
+ *                     (key_stride_tok, value_stride_tok >= Hkv*D, multiples
+ *                     of 8); base pointers 16-byte aligned.
+ *   key_cache,        device uint8 [num_blocks, block_size, num_heads_kv, row]
+ *   value_cache       with row = kvq_cache_row_bytes(dtype, head_dim);
+ *                     16-byte aligned.
+ *   slot_mapping      device int64 [num_tokens]: token t goes to block
+ *                     slot/block_size, position slot%block_size.  Slots < 0
+ *                     or >= num_blocks*block_size are skipped (nothing is
+ *                     written for that token).
+ *   dtype             any kvq_dtype_t.
+ *   k_scale, v_scale  per-tensor scales (fp8_e4m3 / fp8_e5m2): code =
+ *                     fp8(x / scale) with a correctly rounded fp32 division,
+ *                     round-to-nearest-even and saturation to +-448 (e4m3) /
+ *                     +-57344 (e5m2).  Must be finite and > 0 for those
+ *                     dtypes; ignored otherwise.
+ * Per-token-head: s = amax/qmax in fp32 (qmax 127 for int8, 448 for fp8),
+ * code = Q(x / s) (int8: round half to even, clamp [-128,127]); s == 0 gives
+ * zero codes.  Inputs must be finite.  num_tokens == 0 is a no-op. */
+int kvq_reshape_and_cache(const void* key, const void* value,
+                          int64_t num_tokens, int64_t key_stride_tok,
+                          int64_t value_stride_tok, int num_heads_kv,
+                          int head_dim, void* key_cache, void* value_cache,
+                          int64_t num_blocks, int block_size,
+                          const int64_t* slot_mapping, kvq_dtype_t dtype,
+                          float k_scale, float v_scale, void* stream);
+
+/* get_scheduler_metadata -- plan one attention call (host only).
+ * [P2] Breakdown item 1 and Key source snippet: the scheduler takes
+ * kv_cache_dtype so that its tile and scratch sizes come from the KV cache
+ * element size that the kernels use.
+ *
+ *   num_req                 requests in the batch (>= 0)
+ *   heads_q, heads_kv       heads_q % heads_kv == 0, heads_q/heads_kv <= 16
+ *   head_dim                64, 128 or 256
+ *   seq_lens_host           host int32 [num_req]: kv length L of each request
+ *   query_start_loc_host    host int32 [num_req+1], non-decreasing, [0] == 0;
+ *                           request r has Q = qsl[r+1]-qsl[r] <= L queries,
+ *                           the last Q positions of its L-token context.
+ *   causal, window          window > 0 keeps keys with p - j < window (the
+ *                           query's own position included); window <= 0 is
+ *                           off.  A window needs causal != 0.
+ *   dtype                   the KV cache dtype the attention call will read.
+ *   out                     receives a new schedule (free: kvq_sched_destroy)
+ *   workspace_bytes         receives the scratch size the attention call
+ *                           needs (may be 0); must not be NULL.
+ * The schedule holds a host copy and one device copy of its work list, made
+ * on the current device (a blocking upload).  Decoding requests (Q * heads
+ * per kv head <= 16) are split along the KV axis across CTAs. */
+int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
+                               int head_dim, const int32_t* seq_lens_host,
+                               const int32_t* query_start_loc_host, int causal,
+                               int window, kvq_dtype_t dtype,
+                               kvq_sched_t** out, size_t* workspace_bytes);
+
+/* attention_with_kv_cache -- varlen causal GQA attention over the paged
+ * caches, dequantisation fused into the tiles, online softmax.
+ * [P1] Breakdown items 2-3 (tile GEMMs with fused fp8 dequantisation,
+ * cpu_attention_with_kv_cache) and Risks (scale folding); [P2] Key source
+ * snippet (causal, window_size, soft_cap, paged blocks); [P3] Breakdown
+ * item 3 (_prepare_kv_tile: per-token-head dequantisation in the tile).
+ *
+ *   sched                   from kvq_get_scheduler_metadata with the same
+ *                           heads, head_dim, dtype, causal and window; else
+ *                           KVQ_E_SCHED_MISMATCH.
+ *   q                       device bf16 [sum Q, heads_q, head_dim], contiguous,
+ *                           16-byte aligned.
+ *   key_cache, value_cache  as written by kvq_reshape_and_cache.
+ *   query_start_loc,        device int32 copies of the arrays given to the
+ *   seq_lens                scheduler (same values).
+ *   block_table             device int32 [num_req, block_table_stride]:
+ *                           logical block i of request r lives in physical
+ *                           block block_table[r*stride + i].  Entries outside
+ *                           [0, num_blocks) read as empty (masked) keys.
+ *   block_size, num_blocks  cache geometry; block_size a multiple of 16.
+ *   sm_scale                score scale (typically 1/sqrt(head_dim)).
+ *   soft_cap                > 0: z <- soft_cap * tanh(z / soft_cap) after
+ *                           sm_scale; <= 0: off.
+ *   k_scale, v_scale        per-tensor scales (per-tensor fp8 only), folded
+ *                           into the scores and the output.
+ *   out                     device bf16 [sum Q, heads_q, head_dim].
+ *   workspace               device scratch of >= the scheduler's
+ *                           workspace_bytes (256-byte aligned; may be NULL
+ *                           when that is 0).  Calls sharing one workspace
+ *                           must be ordered on one stream.
+ * Query row i of a request sits at position L - Q + i; key j is visible iff
+ * (!causal || j <= p) and (window <= 0 || p - j < window). */
+int kvq_attention_with_kv_cache(const kvq_sched_t* sched, const void* q,
+                                const void* key_cache, const void* value_cache,
+                                const int32_t* query_start_loc,
+                                const int32_t* seq_lens,
+                                const int32_t* block_table,
+                                int block_table_stride, int block_size,
+                                int64_t num_blocks, float sm_scale, int causal,
+                                int window, float soft_cap, float k_scale,
+                                float v_scale, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream);
+
+/* Free a schedule (NULL is a no-op).  Its device work list is released
+ * with cudaFree, which waits for the device: call it after the attention
+ * calls that use it have been enqueued. */
+void kvq_sched_destroy(kvq_sched_t* sched);
+
+/* Summary of a schedule, for tests and benchmarks. */
+typedef struct {
+  int num_req, heads_q, heads_kv, head_dim;
+  int dtype;                 /* kvq_dtype_t the schedule was built for     */
+  int kv_elem_bytes;         /* bytes per cached K/V element (1 or 2)      */
+  int row_bytes;             /* bytes per (token, kv_head) cache row       */
+  int causal, window;
+  int64_t num_rowtile_items; /* work items of the split-KV row-tile kernel */
+  int64_t num_split_items;   /* of those, items that write partials        */
+  int64_t num_merge_items;   /* (request, kv_head) groups to merge         */
+  int64_t num_prefill_items; /* 128-row tiles of the tensor-core kernel    */
+  int64_t max_splits;        /* most KV splits of one row tile             */
+  int64_t total_query_tokens;
+  size_t workspace_bytes;
+  size_t rowtile_smem_bytes; /* dynamic shared memory per row-tile CTA     */
+  size_t prefill_smem_bytes; /* dynamic shared memory per prefill CTA      */
+} kvq_sched_info_t;
+
+int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
+
+/* Short English description of a status code (static storage). */
+const char* kvq_status_string(int status);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* KVQ_H_ */
