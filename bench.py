@@ -1,0 +1,468 @@
+"""Benchmark of the quantized paged-KV attention path on GB300.
+
+One step = one serving step over a batch: reshape_and_cache of the step's
+new tokens (the last query_len tokens of every request) into the fp8 /
+int8 paged cache, then attention_with_kv_cache over the whole cache (the
+split-KV row-tile kernel, the split merge, and the tensor-core prefill
+kernel where the batch has prefills).  The cache holding the earlier
+context is written once before timing (state, not per-step input).
+
+Default workload: the decode batch -- 64 requests, query_len 1, kv_len ~
+U[1024, 4096], 32 query heads over 8 kv heads, head_dim 128, block 16,
+fp8_e4m3 per-tensor scales.  Metric: decode KV GB/s = the K and V cache
+bytes the step's attention must read, divided by the step time.
+
+Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on a
+bounded sample of the same workload instead.  Under torchrun each rank
+runs an independent replica (replicas only: the path has no exchange).
+"""
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+sys.path.insert(0, ROOT)
+
+L2_FLUSH_BYTES = 512 << 20
+FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+
+def _peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    try:
+        with open(path) as f:
+            d = json.load(f)
+        return d, "measured"
+    except (OSError, ValueError):
+        return dict(FALLBACK_PEAKS), "fallback"
+
+
+class ClockSampler:
+    """nvidia-smi clock / throttle samples while the GPU is under load."""
+
+    FIELDS = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, gpu_index: int):
+        self.gpu_index = gpu_index
+        self.proc = None
+        self.lines = []
+        self._t = None
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", "-i", str(self.gpu_index), f"--query-gpu={self.FIELDS}",
+                 "--format=csv,noheader,nounits", "-lms", "100"],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+        except OSError:
+            self.proc = None
+            return
+        self._t = threading.Thread(target=self._read, daemon=True)
+        self._t.start()
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self) -> dict:
+        if self.proc is None:
+            return {"sm_mhz": None, "sm_max_mhz": None, "reasons": ["nvidia-smi unavailable"],
+                    "samples": 0}
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except subprocess.TimeoutExpired:
+            self.proc.kill()
+        if self._t:
+            self._t.join(timeout=2)
+        sm, smax, reasons = [], [], set()
+        names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
+        for line in self.lines:
+            parts = [p.strip() for p in line.split(",")]
+            if len(parts) < 9:
+                continue
+            try:
+                sm.append(float(parts[1]))
+                smax.append(float(parts[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, parts[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        return {"sm_mhz": statistics.median(sm) if sm else None,
+                "sm_max_mhz": max(smax) if smax else None,
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def _dist():
+    """(rank, world, local_rank); initialises a process group under torchrun
+    only for the start/stop barriers and the max-over-ranks time."""
+    world = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    if world > 1:
+        import torch.distributed as dist
+        import torch
+        backend = "nccl" if torch.cuda.is_available() else "gloo"
+        if backend == "nccl":
+            torch.cuda.set_device(local)
+        dist.init_process_group(backend)
+    return rank, world, local
+
+
+def _barrier(world):
+    if world > 1:
+        import torch.distributed as dist
+        dist.barrier()
+
+
+def _max_over_ranks(x: float, world: int) -> float:
+    if world == 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    t = torch.tensor([x], dtype=torch.float64, device=dev)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def kv_bytes_read(wl) -> int:
+    """Algorithmic K+V cache bytes the attention reads: every key visible to
+    some query of its request, once (the window bounds it)."""
+    row = {"fp8_e4m3": wl.head_dim, "fp8_e5m2": wl.head_dim,
+           "int8_per_token_head": wl.head_dim + 4,
+           "fp8_per_token_head": wl.head_dim + 4}[wl.kv_cache_dtype]
+    total = 0
+    for Q, L in zip(wl.query_lens, wl.seq_lens):
+        if Q == 0:
+            continue
+        lo = max(0, L - Q - wl.window + 1) if wl.window > 0 else 0
+        total += (L - lo) * wl.heads_kv * row * 2
+    return total
+
+
+def attention_flops(wl) -> int:
+    """Algorithmic FLOPs: 4 * D per visible (query, key) pair and q head."""
+    total = 0
+    for Q, L in zip(wl.query_lens, wl.seq_lens):
+        for i in range(Q):
+            p = L - Q + i
+            hi = p + 1 if wl.causal else L
+            lo = max(0, p - wl.window + 1) if wl.window > 0 else 0
+            total += (hi - lo)
+    return total * wl.heads_q * 4 * wl.head_dim
+
+
+def run_gpu(args, rank, world, local):
+    import numpy as np
+    import torch
+    from int8_kv_cache_reshape_gb300 import workloads as W
+    from int8_kv_cache_reshape_gb300 import kvq
+
+    dev = torch.device(f"cuda:{local}")
+    torch.cuda.set_device(dev)
+    wl = W.config(args.workload, args.kv_cache_dtype)
+    new = wl.new_token_mask()
+    row = kvq.cache_row_bytes(wl.kv_cache_dtype, wl.head_dim)
+    shape = (wl.num_blocks, wl.block_size, wl.heads_kv, row)
+    kc = torch.empty(shape, dtype=torch.uint8, device=dev)
+    vc = torch.empty(shape, dtype=torch.uint8, device=dev)
+    key, value = wl.key.to(dev), wl.value.to(dev)
+    slots = wl.slot_mapping.to(dev)
+    # State: the earlier context's K/V are already in the cache.
+    kvq.reshape_and_cache(key, value, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+    # Per-step inputs: the new tokens' K/V, their slots, q, lengths, table.
+    new_idx = torch.nonzero(new).flatten()
+    nkey = wl.key[new_idx].contiguous()
+    nval = wl.value[new_idx].contiguous()
+    nslot = wl.slot_mapping[new_idx].contiguous()
+    d_nkey, d_nval, d_nslot = nkey.to(dev), nval.to(dev), nslot.to(dev)
+    q = wl.q.to(dev)
+    qsl = wl.query_start_loc.to(dev)
+    sl = wl.seq_lens_t.to(dev)
+    bt = wl.block_table.to(dev)
+    out = torch.empty(wl.q.shape, dtype=torch.bfloat16, device=dev)
+    sl_host = wl.seq_lens_t.numpy()
+    qsl_host = wl.query_start_loc.numpy()
+    t0 = time.perf_counter()
+    sched = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                       sl_host, qsl_host, wl.causal, wl.window,
+                                       wl.kv_cache_dtype)
+    sched_ms = (time.perf_counter() - t0) * 1e3
+    info = sched.info()
+    ws = torch.empty(max(1, sched.workspace_bytes), dtype=torch.uint8, device=dev)
+    flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
+    stream = torch.cuda.current_stream(dev)
+
+    def step():
+        kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
+                              wl.v_scale, stream)
+        kvq.attention_with_kv_cache(sched, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
+                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
+                                    wl.kv_cache_dtype, wl.heads_kv, stream)
+
+    launches_per_step = 1 + info["num_kernel_launches"]
+    for _ in range(args.warmup):
+        flush.zero_()
+        step()
+    torch.cuda.synchronize()
+
+    clocks = ClockSampler(local)
+    clocks.start()
+    # keep the GPU under the same load briefly so the sampler sees it
+    t_end = time.perf_counter() + args.clock_window
+    while time.perf_counter() < t_end:
+        flush.zero_()
+        step()
+        torch.cuda.synchronize()
+
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
+           torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    _barrier(world)
+    torch.cuda.synchronize()
+    for i in range(args.steps):
+        flush.zero_()           # L2 flush between steps, outside the timed events
+        a, b, c = ev[i]
+        a.record(stream)
+        kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
+                              wl.v_scale, stream)
+        b.record(stream)
+        kvq.attention_with_kv_cache(sched, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
+                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
+                                    wl.kv_cache_dtype, wl.heads_kv, stream)
+        c.record(stream)
+    torch.cuda.synchronize()
+    _barrier(world)
+    clk = clocks.stop()
+    step_ms = [a.elapsed_time(c) for a, b, c in ev]
+    attn_ms = [b.elapsed_time(c) for a, b, c in ev]
+    cache_ms = [a.elapsed_time(b) for a, b, c in ev]
+    total_ms = _max_over_ranks(sum(step_ms), world)
+    ms_per_step = total_ms / args.steps
+    attn_avg = sum(attn_ms) / len(attn_ms)
+
+    kvb = kv_bytes_read(wl)
+    flops = attention_flops(wl)
+    decode_metric = is_decode_metric(args.workload)
+    if decode_metric:
+        metric, unit = "decode KV GB/s", "GB/s"
+        value = world * kvb / (ms_per_step * 1e-3) / 1e9
+    else:
+        metric, unit = "prefill TFLOP/s", "TFLOP/s"
+        value = world * flops / (ms_per_step * 1e-3) / 1e12
+
+    # ---- end to end: host buffers through the public API -------------------
+    pin = lambda t: t.pin_memory()
+    h_q, h_nkey, h_nval, h_nslot = pin(wl.q), pin(nkey), pin(nval), pin(nslot)
+    h_qsl, h_sl, h_bt = pin(wl.query_start_loc), pin(wl.seq_lens_t), pin(wl.block_table)
+    h_out = torch.empty(wl.q.shape, dtype=torch.bfloat16).pin_memory()
+    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nkey, h_nval, h_nslot, h_qsl, h_sl, h_bt))
+    d2h = h_out.numel() * h_out.element_size()
+
+    def e2e_step():
+        q.copy_(h_q, non_blocking=True)
+        d_nkey.copy_(h_nkey, non_blocking=True)
+        d_nval.copy_(h_nval, non_blocking=True)
+        d_nslot.copy_(h_nslot, non_blocking=True)
+        qsl.copy_(h_qsl, non_blocking=True)
+        sl.copy_(h_sl, non_blocking=True)
+        bt.copy_(h_bt, non_blocking=True)
+        s2 = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                        sl_host, qsl_host, wl.causal, wl.window,
+                                        wl.kv_cache_dtype)
+        kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
+                              wl.v_scale, stream)
+        kvq.attention_with_kv_cache(s2, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
+                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
+                                    wl.kv_cache_dtype, wl.heads_kv, stream)
+        h_out.copy_(out, non_blocking=True)
+        torch.cuda.current_stream().synchronize()
+        s2.close()
+
+    for _ in range(3):
+        e2e_step()
+    e2e_times = []
+    for _ in range(args.steps):
+        flush.zero_()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        e2e_step()
+        e2e_times.append(time.perf_counter() - t0)
+    e2e_s = _max_over_ranks(sum(e2e_times), world) / args.steps
+    e2e_value = world * (kvb if decode_metric else flops) / e2e_s / (1e9 if decode_metric else 1e12)
+
+    peaks, peaks_src = _peaks()
+    roofline = {"bound": "hbm" if decode_metric else "tensor",
+                "kernel": "split-KV row-tile attention (+ split merge)",
+                "unit": "GB/s" if decode_metric else "TFLOP/s", "traffic": None,
+                "peak_source": peaks_src}
+    if decode_metric:
+        achieved = kvb / (attn_avg * 1e-3) / 1e9
+        roofline.update(achieved=achieved, peak=peaks["hbm_gbs"],
+                        frac=achieved / peaks["hbm_gbs"])
+    else:
+        achieved = flops / (attn_avg * 1e-3) / 1e12
+        roofline.update(achieved=achieved, peak=peaks["bf16_tflops"],
+                        frac=achieved / peaks["bf16_tflops"])
+
+    res = {
+        "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": ms_per_step, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None,
+        "dtype": f"{wl.kv_cache_dtype} cache, f16 mma / f32 accumulate",
+        "data": "synthetic (seeded, torch.Generator cpu, seed 1000 + workload index)",
+        "config": {"workload": wl.name, "num_req": wl.num_req, "heads_q": wl.heads_q,
+                   "heads_kv": wl.heads_kv, "head_dim": wl.head_dim,
+                   "block_size": wl.block_size, "kv_cache_dtype": wl.kv_cache_dtype,
+                   "kv_tokens": int(sum(wl.seq_lens)), "query_tokens": wl.num_query_tokens,
+                   "l2": f"flushed between steps ({L2_FLUSH_BYTES >> 20} MB write)",
+                   "parallelism": f"replicas x{world}"},
+        "kv_bytes_per_step": kvb, "flops_per_step": flops,
+        "tokens_per_s": world * wl.num_query_tokens / (ms_per_step * 1e-3),
+        "attention_ms": attn_avg, "cache_write_ms": sum(cache_ms) / len(cache_ms),
+        "scheduler_host_ms": sched_ms, "schedule": info,
+        "roofline": roofline,
+        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
+                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
+                "includes": "H2D of step inputs, scheduler, cache write, attention, D2H of out"},
+        "gpu_launches": args.steps * launches_per_step,
+        "clocks": clk,
+    }
+    return res, wl
+
+
+class OracleStep:
+    """The oracle (as it stands) on a bounded sample of the step: the first
+    `nreq` requests -- cache write of their new tokens, then attention of
+    their queries over all heads.  Their earlier context is written once in
+    setup (untimed)."""
+
+    def __init__(self, wl, nreq: int):
+        import numpy as np
+        import oracle
+        from int8_kv_cache_reshape_gb300 import workloads as W
+        sys.path.insert(0, os.path.join(ROOT, "tests"))
+        from _harness import ORACLE_DT, cache_shape
+        self.oracle, self.W, self.np = oracle, W, np
+        self.wl = wl
+        self.dt = ORACLE_DT[wl.kv_cache_dtype]
+        self.reqs = list(range(min(nreq, wl.num_req)))
+        req = wl.token_req.numpy()
+        new = wl.new_token_mask().numpy()
+        pos = wl.token_pos.numpy()
+        L = wl.seq_lens_t.numpy()[req]
+        Q = np.array(wl.query_lens)[req]
+        in_sample = np.isin(req, self.reqs)
+        if wl.window > 0:
+            in_sample &= pos >= (L - Q - wl.window + 1)
+        self.kc = np.zeros(cache_shape(wl), np.uint8)
+        self.vc = np.zeros(cache_shape(wl), np.uint8)
+        self.kb, self.vb = W.bf16_bits(wl.key), W.bf16_bits(wl.value)
+        self.qb = W.bf16_bits(wl.q)
+        slots = wl.slot_mapping.numpy()
+        old = np.where(in_sample & ~new, slots, -1)
+        oracle.reshape_and_cache(self.kb, self.vb, self.kc, self.vc, old, self.dt, wl.k_scale,
+                                 wl.v_scale, wl.block_size)
+        self.fresh = np.where(in_sample & new, slots, -1)
+        qsl = wl.query_start_loc.numpy()
+        self.toks = np.concatenate([np.arange(qsl[r], qsl[r + 1]) for r in self.reqs])
+        self.sub = W.Workload(**{**wl.__dict__})
+        self.sub.query_lens = [wl.query_lens[r] for r in self.reqs]
+        self.sub.seq_lens = [wl.seq_lens[r] for r in self.reqs]
+        self.cores = oracle.num_threads()
+        self.sample = (f"first {len(self.reqs)} of {wl.num_req} requests: cache write of their "
+                       f"new tokens + attention of their {self.sub.num_query_tokens} query "
+                       f"tokens over all {wl.heads_q} heads")
+
+    def step(self) -> float:
+        wl = self.wl
+        t0 = time.perf_counter()
+        self.oracle.reshape_and_cache(self.kb, self.vb, self.kc, self.vc, self.fresh, self.dt,
+                                      wl.k_scale, wl.v_scale, wl.block_size)
+        self.oracle.attention(self.qb, self.kc, self.vc, wl.query_start_loc, wl.seq_lens_t,
+                              wl.block_table, wl.heads_kv, wl.block_size, self.dt, wl.sm_scale,
+                              wl.causal, wl.window, wl.soft_cap, wl.k_scale, wl.v_scale,
+                              tokens=self.toks)
+        return time.perf_counter() - t0
+
+    def work(self, decode_metric: bool) -> float:
+        return kv_bytes_read(self.sub) if decode_metric else attention_flops(self.sub)
+
+
+def is_decode_metric(index: int) -> bool:
+    return index in (1, 2, 5)
+
+
+def run_reference(args, rank, world):
+    from int8_kv_cache_reshape_gb300 import workloads as W
+    if rank != 0:
+        return None
+    wl = W.config(args.workload, args.kv_cache_dtype)
+    decode_metric = is_decode_metric(args.workload)
+    ref = OracleStep(wl, args.ref_requests)
+    for _ in range(args.warmup):
+        ref.step()
+    times = [ref.step() for _ in range(args.steps)]
+    s = sum(times) / len(times)
+    value = ref.work(decode_metric) / s / (1e9 if decode_metric else 1e12)
+    unit = "GB/s" if decode_metric else "TFLOP/s"
+    return {
+        "impl": "reference", "metric": "decode KV GB/s" if decode_metric else "prefill TFLOP/s",
+        "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
+        "warmup": args.warmup, "ms_per_step": s * 1e3, "higher_is_better": True,
+        "scaling": "weak", "vs_baseline": None, "dtype": "f64 (oracle)",
+        "data": "synthetic (seeded)", "config": {"workload": wl.name, "sample": ref.sample},
+        "cpu_baseline": {"value": value, "unit": unit, "cores": ref.cores, "kind": "oracle",
+                         "sample": ref.sample},
+        "e2e": {"value": value, "unit": unit, "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0},
+    }
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=50)
+    ap.add_argument("--warmup", type=int, default=5)
+    ap.add_argument("--impl", choices=["kvq", "reference"], default="kvq")
+    ap.add_argument("--workload", type=int, default=2, choices=[1, 2, 3, 4, 5])
+    ap.add_argument("--kv-cache-dtype", default=None)
+    ap.add_argument("--clock-window", type=float, default=1.5,
+                    help="seconds of untimed load before the timed steps, for clock samples")
+    ap.add_argument("--ref-requests", type=int, default=16)
+    ap.add_argument("--cpu-requests", type=int, default=16)
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    if args.warmup < 3:
+        args.warmup = 3
+    rank, world, local = _dist()
+    if args.impl == "reference":
+        res = run_reference(args, rank, world)
+        if rank == 0:
+            print(json.dumps(res))
+        return
+    res, wl = run_gpu(args, rank, world, local)
+    if rank == 0:
+        if not args.no_cpu_baseline:
+            decode_metric = is_decode_metric(args.workload)
+            ref = OracleStep(wl, args.cpu_requests)
+            secs = ref.step()
+            res["cpu_baseline"] = {
+                "value": ref.work(decode_metric) / secs / (1e9 if decode_metric else 1e12),
+                "unit": res["unit"], "cores": ref.cores, "kind": "oracle", "seconds": secs,
+                "sample": ref.sample}
+        print(json.dumps(res))
+
+
+if __name__ == "__main__":
+    main()

@@ -38,6 +38,14 @@
 extern "C" {
 #endif
 
+/* Symbols of the ABI are exported even when the library is built with
+ * hidden default visibility. */
+#if defined(__GNUC__)
+#define KVQ_API __attribute__((visibility("default")))
+#else
+#define KVQ_API
+#endif
+
 /* ---- status codes ---------------------------------------------------- */
 #define KVQ_OK 0
 #define KVQ_E_INVALID_ARG (-1)      /* a pointer, size, stride or value is invalid */
@@ -75,11 +83,11 @@ typedef struct kvq_sched kvq_sched_t;
  * Breakdown item 2), "fp8" (alias of fp8_e4m3), "fp8_e4m3", "fp8_e5m2",
  * "int8_per_token_head", "fp8_per_token_head".  s == NULL or "" reads as
  * "auto".  Unknown strings: KVQ_E_INVALID_ARG. */
-int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out);
+KVQ_API int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out);
 
 /* Bytes of one (token, kv_head) cache row: 2*D (AUTO), D (per-tensor fp8)
  * or D+16 (per-token-head).  head_dim must be a positive multiple of 16. */
-int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
+KVQ_API int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
 
 /* reshape_and_cache -- quantise new K/V tokens into the paged caches.
  * [P1] Breakdown item 1 (the reshape kernel writing the fp8 cache) and
@@ -106,7 +114,7 @@ int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
  * Per-token-head: s = amax/qmax in fp32 (qmax 127 for int8, 448 for fp8),
  * code = Q(x / s) (int8: round half to even, clamp [-128,127]); s == 0 gives
  * zero codes.  Inputs must be finite.  num_tokens == 0 is a no-op. */
-int kvq_reshape_and_cache(const void* key, const void* value,
+KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
                           int64_t num_tokens, int64_t key_stride_tok,
                           int64_t value_stride_tok, int num_heads_kv,
                           int head_dim, void* key_cache, void* value_cache,
@@ -136,7 +144,7 @@ int kvq_reshape_and_cache(const void* key, const void* value,
  * The schedule holds a host copy and one device copy of its work list, made
  * on the current device (a blocking upload).  Decoding requests (Q * heads
  * per kv head <= 16) are split along the KV axis across CTAs. */
-int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
+KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
                                int head_dim, const int32_t* seq_lens_host,
                                const int32_t* query_start_loc_host, int causal,
                                int window, kvq_dtype_t dtype,
@@ -149,9 +157,12 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  * snippet (causal, window_size, soft_cap, paged blocks); [P3] Breakdown
  * item 3 (_prepare_kv_tile: per-token-head dequantisation in the tile).
  *
- *   sched                   from kvq_get_scheduler_metadata with the same
- *                           heads, head_dim, dtype, causal and window; else
- *                           KVQ_E_SCHED_MISMATCH.
+ *   sched                   from kvq_get_scheduler_metadata.
+ *   heads_q, heads_kv,      what the caller believes the caches and q hold;
+ *   head_dim, dtype         they, causal and window must equal the values
+ *                           the schedule was built for, else
+ *                           KVQ_E_SCHED_MISMATCH.  (The bug of [P2]: tiles
+ *                           sized for one KV element size, run on another.)
  *   q                       device bf16 [sum Q, heads_q, head_dim], contiguous,
  *                           16-byte aligned.
  *   key_cache, value_cache  as written by kvq_reshape_and_cache.
@@ -174,7 +185,9 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  *                           must be ordered on one stream.
  * Query row i of a request sits at position L - Q + i; key j is visible iff
  * (!causal || j <= p) and (window <= 0 || p - j < window). */
-int kvq_attention_with_kv_cache(const kvq_sched_t* sched, const void* q,
+KVQ_API int kvq_attention_with_kv_cache(const kvq_sched_t* sched, int heads_q,
+                                int heads_kv, int head_dim, kvq_dtype_t dtype,
+                                const void* q,
                                 const void* key_cache, const void* value_cache,
                                 const int32_t* query_start_loc,
                                 const int32_t* seq_lens,
@@ -188,7 +201,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* sched, const void* q,
 /* Free a schedule (NULL is a no-op).  Its device work list is released
  * with cudaFree, which waits for the device: call it after the attention
  * calls that use it have been enqueued. */
-void kvq_sched_destroy(kvq_sched_t* sched);
+KVQ_API void kvq_sched_destroy(kvq_sched_t* sched);
 
 /* Summary of a schedule, for tests and benchmarks. */
 typedef struct {
@@ -206,12 +219,13 @@ typedef struct {
   size_t workspace_bytes;
   size_t rowtile_smem_bytes; /* dynamic shared memory per row-tile CTA     */
   size_t prefill_smem_bytes; /* dynamic shared memory per prefill CTA      */
+  int64_t num_kernel_launches; /* kernels one attention call launches      */
 } kvq_sched_info_t;
 
-int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
+KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
 
 /* Short English description of a status code (static storage). */
-const char* kvq_status_string(int status);
+KVQ_API const char* kvq_status_string(int status);
 
 #ifdef __cplusplus
 }

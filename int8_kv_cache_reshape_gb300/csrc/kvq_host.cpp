@@ -1,0 +1,390 @@
+// kvq_host.cpp -- the C ABI: argument checks, dtype parsing, the scheduler
+// (get_scheduler_metadata) and the attention dispatch.
+//
+// vllm PR 50194 page, Breakdown item 1 and Key source snippet: the
+// scheduler is given kv_cache_dtype (parsed to the enum 0 = auto,
+// 1 = fp8_e4m3, 2 = fp8_e5m2) so that tile and scratch sizes follow the KV
+// cache element size.  Here every size comes from kvq_internal.h's constexpr
+// geometry, and the attention call refuses a schedule built for another
+// dtype, head count or head size.
+#include <cuda_runtime.h>
+
+#include <algorithm>
+#include <cmath>
+#include <cstdlib>
+#include <cstring>
+#include <mutex>
+#include <new>
+#include <vector>
+
+#include "kvq_internal.h"
+
+using kvq::MergeItem;
+using kvq::RowtileItem;
+
+struct kvq_sched {
+  int num_req, heads_q, heads_kv, head_dim, dtype, causal, window, group;
+  int device;
+  int64_t total_q;
+  // Row-tile items: [0, n1) use one 8-row n-tile, [n1, n1 + n2) use two.
+  std::vector<RowtileItem> items;
+  int64_t n_tiles1, n_tiles2, n_split;
+  int64_t max_splits;
+  std::vector<MergeItem> merges;
+  int64_t partial_rows;
+  size_t workspace_bytes;
+  void* d_buf;  // device copy: items, then merges
+  size_t d_items_off, d_merges_off;
+};
+
+namespace {
+
+bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+int sm_count() {
+  int dev = 0, sms = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) return 0;
+  if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess) return 0;
+  return sms;
+}
+
+int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
+
+// SM count assumed when planning without a device (GB300: 152 SMs).
+constexpr int kDefaultSmCount = 152;
+
+}  // namespace
+
+extern "C" {
+
+const char* kvq_status_string(int status) {
+  switch (status) {
+    case KVQ_OK: return "ok";
+    case KVQ_E_INVALID_ARG: return "invalid argument";
+    case KVQ_E_UNSUPPORTED: return "unsupported dtype, head_dim or shape";
+    case KVQ_E_SCHED_MISMATCH: return "schedule built for another dtype, head count, head_dim, causal or window";
+    case KVQ_E_WORKSPACE_TOO_SMALL: return "workspace smaller than the schedule requires";
+    case KVQ_E_CUDA: return "CUDA runtime error";
+    case KVQ_E_NO_MEMORY: return "allocation failed";
+    default: return "unknown status";
+  }
+}
+
+int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out) {
+  if (!out) return KVQ_E_INVALID_ARG;
+  if (!s || !*s || !std::strcmp(s, "auto")) { *out = KVQ_AUTO; return KVQ_OK; }
+  if (!std::strcmp(s, "fp8") || !std::strcmp(s, "fp8_e4m3")) { *out = KVQ_FP8_E4M3; return KVQ_OK; }
+  if (!std::strcmp(s, "fp8_e5m2")) { *out = KVQ_FP8_E5M2; return KVQ_OK; }
+  if (!std::strcmp(s, "int8_per_token_head")) { *out = KVQ_INT8_PER_TOKEN_HEAD; return KVQ_OK; }
+  if (!std::strcmp(s, "fp8_per_token_head")) { *out = KVQ_FP8_PER_TOKEN_HEAD; return KVQ_OK; }
+  return KVQ_E_INVALID_ARG;
+}
+
+int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out) {
+  if (!out || !kvq::is_valid_dtype(dtype) || head_dim <= 0 || head_dim % 16)
+    return KVQ_E_INVALID_ARG;
+  *out = (size_t)kvq::row_bytes(dtype, head_dim);
+  return KVQ_OK;
+}
+
+int kvq_reshape_and_cache(const void* key, const void* value, int64_t num_tokens,
+                          int64_t key_stride_tok, int64_t value_stride_tok, int num_heads_kv,
+                          int head_dim, void* key_cache, void* value_cache, int64_t num_blocks,
+                          int block_size, const int64_t* slot_mapping, kvq_dtype_t dtype,
+                          float k_scale, float v_scale, void* stream) {
+  if (!kvq::is_valid_dtype(dtype)) return KVQ_E_INVALID_ARG;
+  if (!kvq::head_dim_supported(head_dim)) return KVQ_E_UNSUPPORTED;
+  if (num_tokens < 0 || num_heads_kv <= 0 || num_blocks < 0 || block_size <= 0)
+    return KVQ_E_INVALID_ARG;
+  if (num_tokens == 0) return KVQ_OK;
+  if (!key || !value || !key_cache || !value_cache || !slot_mapping) return KVQ_E_INVALID_ARG;
+  const int64_t min_stride = (int64_t)num_heads_kv * head_dim;
+  if (key_stride_tok < min_stride || value_stride_tok < min_stride || key_stride_tok % 8 ||
+      value_stride_tok % 8)
+    return KVQ_E_INVALID_ARG;
+  if (!aligned(key, 16) || !aligned(value, 16) || !aligned(key_cache, 16) ||
+      !aligned(value_cache, 16) || !aligned(slot_mapping, 8))
+    return KVQ_E_INVALID_ARG;
+  if (dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2) {
+    if (!(std::isfinite(k_scale) && k_scale > 0.0f && std::isfinite(v_scale) && v_scale > 0.0f))
+      return KVQ_E_INVALID_ARG;
+  }
+  return kvq::launch_reshape_and_cache(key, value, num_tokens, key_stride_tok, value_stride_tok,
+                                       num_heads_kv, head_dim, key_cache, value_cache, num_blocks,
+                                       block_size, slot_mapping, dtype, k_scale, v_scale, stream);
+}
+
+void kvq_sched_destroy(kvq_sched_t* s) {
+  if (!s) return;
+  if (s->d_buf) {
+    int cur = -1;
+    cudaGetDevice(&cur);
+    if (cur != s->device) cudaSetDevice(s->device);
+    cudaFree(s->d_buf);
+    if (cur != s->device && cur >= 0) cudaSetDevice(cur);
+  }
+  delete s;
+}
+
+int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_dim,
+                               const int32_t* seq_lens_host, const int32_t* query_start_loc_host,
+                               int causal, int window, kvq_dtype_t dtype, kvq_sched_t** out,
+                               size_t* workspace_bytes) {
+  if (!out || !workspace_bytes) return KVQ_E_INVALID_ARG;
+  *out = nullptr;
+  *workspace_bytes = 0;
+  if (num_req < 0 || heads_kv <= 0 || heads_q <= 0) return KVQ_E_INVALID_ARG;
+  if (num_req > 0 && (!seq_lens_host || !query_start_loc_host)) return KVQ_E_INVALID_ARG;
+  if (!kvq::is_valid_dtype(dtype)) return KVQ_E_INVALID_ARG;
+  if (heads_q % heads_kv) return KVQ_E_UNSUPPORTED;
+  if (!kvq::head_dim_supported(head_dim) || !kvq::attention_dtype_supported(dtype))
+    return KVQ_E_UNSUPPORTED;
+  if (window > 0 && !causal) return KVQ_E_INVALID_ARG;
+  if (num_req > 0 && query_start_loc_host[0] != 0) return KVQ_E_INVALID_ARG;
+  for (int r = 0; r < num_req; ++r) {
+    const int64_t Q = (int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r];
+    if (Q < 0 || seq_lens_host[r] < 0 || Q > seq_lens_host[r]) return KVQ_E_INVALID_ARG;
+  }
+
+  kvq_sched* s = new (std::nothrow) kvq_sched();
+  if (!s) return KVQ_E_NO_MEMORY;
+  s->num_req = num_req;
+  s->heads_q = heads_q;
+  s->heads_kv = heads_kv;
+  s->head_dim = head_dim;
+  s->dtype = dtype;
+  s->causal = causal ? 1 : 0;
+  s->window = window > 0 ? window : 0;
+  s->group = heads_q / heads_kv;
+  s->total_q = num_req > 0 ? query_start_loc_host[num_req] : 0;
+  s->d_buf = nullptr;
+  // Without a usable CUDA device the plan is still built (host-only: its
+  // attention calls return KVQ_E_CUDA), so that planning can be inspected
+  // on machines without a GPU.
+  bool have_device = cudaGetDevice(&s->device) == cudaSuccess;
+  if (!have_device) {
+    cudaGetLastError();
+    s->device = -1;
+  }
+  const int G = s->group;
+
+  // 1) Row tiles: the packed rows (q_index * G + g) of each (request,
+  //    kv_head) in tiles of up to 16, each with the KV chunk range its rows
+  //    can see.
+  struct Tile {
+    RowtileItem it;
+    int64_t chunks;
+  };
+  std::vector<Tile> tiles;
+  int64_t total_chunks = 0;
+  for (int r = 0; r < num_req; ++r) {
+    const int64_t L = seq_lens_host[r];
+    const int64_t Q = (int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r];
+    if (Q == 0) continue;
+    const int64_t rows = Q * G;
+    for (int64_t row0 = 0; row0 < rows; row0 += kvq::kRowtileMaxRows) {
+      const int64_t nrows = std::min<int64_t>(kvq::kRowtileMaxRows, rows - row0);
+      const int64_t p_min = L - Q + row0 / G;
+      const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
+      const int64_t kv_hi = s->causal ? p_max + 1 : L;
+      const int64_t kv_lo = s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0;
+      const int64_t c_lo = kv_lo / kvq::kChunkTokens;
+      const int64_t c_hi = ceil_div(kv_hi, kvq::kChunkTokens);
+      for (int h = 0; h < heads_kv; ++h) {
+        Tile t;
+        t.it.req = r;
+        t.it.kv_head = h;
+        t.it.row0 = (int32_t)row0;
+        t.it.nrows = (int32_t)nrows;
+        t.it.chunk_lo = (int32_t)c_lo;
+        t.it.chunk_hi = (int32_t)c_hi;
+        t.it.part = -1;
+        t.it.pad = 0;
+        t.chunks = c_hi - c_lo;
+        total_chunks += t.chunks;
+        tiles.push_back(t);
+      }
+    }
+  }
+
+  // 2) KV splits: aim for a few waves of CTAs over the SMs; no split
+  //    smaller than kMinChunksPerSplit.  KVQ_NUM_SPLITS (benchmarks and
+  //    tests) forces a split count per tile.
+  const int sms = have_device ? std::max(1, sm_count()) : kDefaultSmCount;
+  const int64_t target_ctas = (int64_t)sms * 3 * 4;
+  int64_t per_split = std::max<int64_t>(kvq::kMinChunksPerSplit, ceil_div(total_chunks, target_ctas));
+  int64_t forced = 0;
+  if (const char* env = std::getenv("KVQ_NUM_SPLITS")) forced = std::atoll(env);
+
+  std::vector<RowtileItem> one, two;
+  s->partial_rows = 0;
+  s->max_splits = 0;
+  s->n_split = 0;
+  std::stable_sort(tiles.begin(), tiles.end(),
+                   [](const Tile& a, const Tile& b) { return a.chunks > b.chunks; });
+  for (const Tile& t : tiles) {
+    int64_t ns = forced > 0 ? forced : ceil_div(t.chunks, per_split);
+    ns = std::max<int64_t>(1, std::min<int64_t>(ns, t.chunks));
+    s->max_splits = std::max(s->max_splits, ns);
+    auto& dst = t.it.nrows <= 8 ? one : two;
+    if (ns == 1) {
+      dst.push_back(t.it);
+      continue;
+    }
+    MergeItem m;
+    m.req = t.it.req;
+    m.kv_head = t.it.kv_head;
+    m.row0 = t.it.row0;
+    m.nrows = t.it.nrows;
+    m.part = (int32_t)s->partial_rows;
+    m.nsplits = (int32_t)ns;
+    m.pad0 = m.pad1 = 0;
+    s->merges.push_back(m);
+    for (int64_t k = 0; k < ns; ++k) {
+      RowtileItem it = t.it;
+      it.chunk_lo = (int32_t)(t.it.chunk_lo + t.chunks * k / ns);
+      it.chunk_hi = (int32_t)(t.it.chunk_lo + t.chunks * (k + 1) / ns);
+      it.part = (int32_t)(s->partial_rows + k * t.it.nrows);
+      dst.push_back(it);
+      ++s->n_split;
+    }
+    s->partial_rows += ns * t.it.nrows;
+  }
+  s->n_tiles1 = (int64_t)one.size();
+  s->n_tiles2 = (int64_t)two.size();
+  s->items = std::move(one);
+  s->items.insert(s->items.end(), two.begin(), two.end());
+  s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
+
+  // 3) Device copy of the work list (one allocation, blocking upload).
+  const size_t items_bytes = s->items.size() * sizeof(RowtileItem);
+  const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
+  s->d_items_off = 0;
+  s->d_merges_off = kvq::align256(items_bytes);
+  const size_t total = s->d_merges_off + merges_bytes;
+  if (total > 0 && have_device) {
+    if (cudaMalloc(&s->d_buf, total) != cudaSuccess) {
+      cudaGetLastError();
+      delete s;
+      return KVQ_E_NO_MEMORY;
+    }
+    bool ok = true;
+    if (items_bytes)
+      ok &= cudaMemcpy(static_cast<char*>(s->d_buf) + s->d_items_off, s->items.data(),
+                       items_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (merges_bytes)
+      ok &= cudaMemcpy(static_cast<char*>(s->d_buf) + s->d_merges_off, s->merges.data(),
+                       merges_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (!ok) {
+      kvq_sched_destroy(s);
+      return KVQ_E_CUDA;
+    }
+  }
+  *workspace_bytes = s->workspace_bytes;
+  *out = s;
+  return KVQ_OK;
+}
+
+int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
+  if (!s || !out) return KVQ_E_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->num_req = s->num_req;
+  out->heads_q = s->heads_q;
+  out->heads_kv = s->heads_kv;
+  out->head_dim = s->head_dim;
+  out->dtype = s->dtype;
+  out->kv_elem_bytes = kvq::kv_elem_bytes(s->dtype);
+  out->row_bytes = kvq::row_bytes(s->dtype, s->head_dim);
+  out->causal = s->causal;
+  out->window = s->window;
+  out->num_rowtile_items = (int64_t)s->items.size();
+  out->num_split_items = s->n_split;
+  out->num_merge_items = (int64_t)s->merges.size();
+  out->num_prefill_items = 0;
+  out->max_splits = s->max_splits;
+  out->total_query_tokens = s->total_q;
+  out->workspace_bytes = s->workspace_bytes;
+  out->rowtile_smem_bytes = kvq::rowtile_smem_bytes(s->dtype, s->head_dim);
+  out->prefill_smem_bytes = 0;
+  out->num_kernel_launches = (s->n_tiles1 > 0) + (s->n_tiles2 > 0) + (!s->merges.empty());
+  return KVQ_OK;
+}
+
+int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv, int head_dim,
+                                kvq_dtype_t dtype, const void* q, const void* key_cache,
+                                const void* value_cache, const int32_t* query_start_loc,
+                                const int32_t* seq_lens, const int32_t* block_table,
+                                int block_table_stride, int block_size, int64_t num_blocks,
+                                float sm_scale, int causal, int window, float soft_cap,
+                                float k_scale, float v_scale, void* out, void* workspace,
+                                size_t workspace_bytes, void* stream) {
+  if (!s) return KVQ_E_INVALID_ARG;
+  if (heads_q != s->heads_q || heads_kv != s->heads_kv || head_dim != s->head_dim ||
+      (int)dtype != s->dtype || (causal ? 1 : 0) != s->causal ||
+      (window > 0 ? window : 0) != s->window)
+    return KVQ_E_SCHED_MISMATCH;
+  if (s->items.empty()) return KVQ_OK;
+  if (!s->d_buf) return KVQ_E_CUDA;  // planned without a device
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
+  if (cur != s->device) return KVQ_E_INVALID_ARG;
+  if (!q || !key_cache || !value_cache || !query_start_loc || !seq_lens || !block_table || !out)
+    return KVQ_E_INVALID_ARG;
+  if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(out, 16) || !aligned(block_table, 4))
+    return KVQ_E_INVALID_ARG;
+  if (block_size <= 0 || block_size % kvq::kChunkTokens) return KVQ_E_UNSUPPORTED;
+  if (num_blocks <= 0 || block_table_stride <= 0) return KVQ_E_INVALID_ARG;
+  // The table must hold every logical block the schedule reads.
+  for (const RowtileItem& it : s->items) {
+    const int64_t last_block = ((int64_t)it.chunk_hi * kvq::kChunkTokens - 1) / block_size;
+    if (last_block >= block_table_stride) return KVQ_E_INVALID_ARG;
+  }
+  if (!std::isfinite(sm_scale) || !std::isfinite(soft_cap)) return KVQ_E_INVALID_ARG;
+  if (dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2) {
+    if (!(std::isfinite(k_scale) && std::isfinite(v_scale))) return KVQ_E_INVALID_ARG;
+  }
+  if (workspace_bytes < s->workspace_bytes) return KVQ_E_WORKSPACE_TOO_SMALL;
+  if (s->workspace_bytes > 0 && (!workspace || !aligned(workspace, 256)))
+    return KVQ_E_INVALID_ARG;
+
+  kvq::AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.key_cache = static_cast<const uint8_t*>(key_cache);
+  p.value_cache = static_cast<const uint8_t*>(value_cache);
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.block_table = block_table;
+  p.out = static_cast<uint16_t*>(out);
+  p.part_o = static_cast<float*>(workspace);
+  p.part_lse = s->workspace_bytes
+                   ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
+                                              kvq::workspace_o_bytes(s->partial_rows, head_dim))
+                   : nullptr;
+  p.items = reinterpret_cast<const RowtileItem*>(static_cast<char*>(s->d_buf) + s->d_items_off);
+  p.merges = reinterpret_cast<const MergeItem*>(static_cast<char*>(s->d_buf) + s->d_merges_off);
+  p.num_blocks = num_blocks;
+  p.block_table_stride = block_table_stride;
+  p.block_size = block_size;
+  p.heads_q = heads_q;
+  p.heads_kv = heads_kv;
+  p.group = s->group;
+  p.causal = s->causal;
+  p.window = s->window;
+  p.sm_scale = sm_scale;
+  p.soft_cap = soft_cap > 0.0f ? soft_cap : 0.0f;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+
+  int rc = KVQ_OK;
+  if (s->n_tiles1 > 0)
+    rc = kvq::launch_rowtile(p, s->dtype, head_dim, 1, 0, s->n_tiles1, stream);
+  if (rc == KVQ_OK && s->n_tiles2 > 0)
+    rc = kvq::launch_rowtile(p, s->dtype, head_dim, 2, s->n_tiles1, s->n_tiles2, stream);
+  if (rc == KVQ_OK && !s->merges.empty())
+    rc = kvq::launch_merge(p, head_dim, (int64_t)s->merges.size(), stream);
+  return rc;
+}
+
+}  // extern "C"

@@ -1,0 +1,152 @@
+// kvq_internal.h -- definitions shared by the host scheduler and the kernels.
+//
+// The tile geometry lives here, in one set of constexpr functions of the KV
+// cache dtype and head_dim.  The scheduler sizes shared memory and scratch
+// from these functions and the kernels are instantiated from the same ones,
+// so the two cannot disagree about the KV element size -- the failure of
+// the vllm PR 50194 page (Motivation: tiles chosen from one element size,
+// scratch sized for another, out-of-bounds writes during a large prefill).
+#pragma once
+
+#include <cstddef>
+#include <cstdint>
+
+#include "../../include/kvq.h"
+
+#ifdef __CUDACC__
+#define KVQ_HD __host__ __device__
+#else
+#define KVQ_HD
+#endif
+
+namespace kvq {
+
+// ---- cache rows --------------------------------------------------------
+KVQ_HD constexpr bool is_per_token_head(int dtype) {
+  return dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD;
+}
+KVQ_HD constexpr bool is_valid_dtype(int dtype) { return dtype >= 0 && dtype <= 4; }
+// Bytes of one cached K or V element (the KV element size).
+KVQ_HD constexpr int kv_elem_bytes(int dtype) { return dtype == KVQ_AUTO ? 2 : 1; }
+// Bytes of one (token, kv_head) row: codes plus, per-token-head, a 16-byte
+// tail holding the fp32 scale and 12 zero bytes.
+KVQ_HD constexpr int row_bytes(int dtype, int head_dim) {
+  return head_dim * kv_elem_bytes(dtype) + (is_per_token_head(dtype) ? 16 : 0);
+}
+KVQ_HD constexpr bool head_dim_supported(int d) { return d == 64 || d == 128 || d == 256; }
+// Dtypes with built attention kernels (bf16 "auto" cache: not yet).
+KVQ_HD constexpr bool attention_dtype_supported(int dtype) {
+  return dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2 ||
+         dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD;
+}
+
+// ---- split-KV row-tile kernel ---------------------------------------------
+// A work item is up to 16 packed (query token, head) rows of one kv head,
+// over a range of 16-token KV chunks; a CTA of 4 warps shares the range.
+constexpr int kChunkTokens = 16;
+constexpr int kRowtileWarps = 4;
+constexpr int kRowtileThreads = 32 * kRowtileWarps;
+constexpr int kRowtileMaxRows = 16;
+
+// Bytes one warp stages per chunk: 16 K rows + 16 V rows of codes, plus
+// the scale tails of the K and V rows for per-token-head dtypes (one 16-byte
+// slot per lane).
+KVQ_HD constexpr int rowtile_chunk_bytes(int dtype, int head_dim) {
+  return 2 * kChunkTokens * head_dim * kv_elem_bytes(dtype) +
+         (is_per_token_head(dtype) ? 32 * 16 : 0);
+}
+// Pipeline depth: enough chunks in flight per warp to cover HBM latency,
+// fewer when a chunk is large.
+KVQ_HD constexpr int rowtile_stages(int dtype, int head_dim) {
+  return rowtile_chunk_bytes(dtype, head_dim) >= 8192 ? 3 : 4;
+}
+KVQ_HD constexpr size_t rowtile_pipeline_smem(int dtype, int head_dim) {
+  return (size_t)kRowtileWarps * rowtile_stages(dtype, head_dim) *
+         rowtile_chunk_bytes(dtype, head_dim);
+}
+// Cross-warp combine at the end reuses the pipeline buffers: per warp,
+// 16 rows x head_dim fp32 partial outputs, plus (m, l) per row.
+KVQ_HD constexpr size_t rowtile_combine_smem(int head_dim) {
+  return (size_t)kRowtileWarps * kRowtileMaxRows * (head_dim + 2) * 4;
+}
+KVQ_HD constexpr size_t rowtile_smem_bytes(int dtype, int head_dim) {
+  return rowtile_pipeline_smem(dtype, head_dim) > rowtile_combine_smem(head_dim)
+             ? rowtile_pipeline_smem(dtype, head_dim)
+             : rowtile_combine_smem(head_dim);
+}
+// Smallest KV split worth a CTA (chunks): below this the merge costs more
+// than the parallelism gains.
+constexpr int kMinChunksPerSplit = 8;
+
+// One row-tile work item (32 bytes, read once per CTA).
+struct RowtileItem {
+  int32_t req;       // request index
+  int32_t kv_head;   // kv head
+  int32_t row0;      // first packed row: row = q_index * G + (head % G)
+  int32_t nrows;     // rows in the tile, 1..16
+  int32_t chunk_lo;  // first 16-token KV chunk
+  int32_t chunk_hi;  // one past the last chunk
+  int32_t part;      // -1: write `out`; else first partial row in workspace
+  int32_t pad;
+};
+static_assert(sizeof(RowtileItem) == 32, "RowtileItem layout");
+
+// One merge item: the partial rows of a tile that was split along KV.
+struct MergeItem {
+  int32_t req, kv_head, row0, nrows;
+  int32_t part;      // partial row of (split 0, row 0); split s row n at
+                     // part + s * nrows + n
+  int32_t nsplits;
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(MergeItem) == 32, "MergeItem layout");
+
+// Workspace layout: partial outputs [P][head_dim] fp32, then partial
+// log2-sum-exp [P] fp32, each 256-byte aligned.
+KVQ_HD constexpr size_t align256(size_t x) { return (x + 255) & ~(size_t)255; }
+KVQ_HD constexpr size_t workspace_o_bytes(int64_t partial_rows, int head_dim) {
+  return align256((size_t)partial_rows * head_dim * 4);
+}
+KVQ_HD constexpr size_t workspace_bytes(int64_t partial_rows, int head_dim) {
+  return partial_rows == 0 ? 0
+                           : workspace_o_bytes(partial_rows, head_dim) +
+                                 align256((size_t)partial_rows * 4);
+}
+
+// Kernel arguments of the attention kernels (passed by value).
+struct AttnParams {
+  const uint16_t* q;           // bf16 [sum Q, Hq, D]
+  const uint8_t* key_cache;    // [NB, B, Hkv, row]
+  const uint8_t* value_cache;
+  const int32_t* query_start_loc;
+  const int32_t* seq_lens;
+  const int32_t* block_table;
+  uint16_t* out;               // bf16 [sum Q, Hq, D]
+  float* part_o;               // [P, D]
+  float* part_lse;             // [P]
+  const RowtileItem* items;
+  const MergeItem* merges;
+  int64_t num_blocks;
+  int block_table_stride;
+  int block_size;
+  int heads_q, heads_kv, group;  // group = Hq / Hkv
+  int causal, window;
+  float sm_scale, soft_cap, k_scale, v_scale;
+};
+
+}  // namespace kvq
+
+// Launchers (defined in the .cu files; return KVQ_OK or KVQ_E_CUDA).
+namespace kvq {
+int launch_reshape_and_cache(const void* key, const void* value,
+                             int64_t num_tokens, int64_t key_stride,
+                             int64_t value_stride, int num_heads_kv,
+                             int head_dim, void* key_cache, void* value_cache,
+                             int64_t num_blocks, int block_size,
+                             const int64_t* slot_mapping, int dtype,
+                             float k_scale, float v_scale, void* stream);
+int launch_rowtile(const AttnParams& p, int dtype, int head_dim, int ntiles,
+                   int64_t item_offset, int64_t num_items, void* stream);
+int launch_merge(const AttnParams& p, int head_dim, int64_t num_items,
+                 void* stream);
+}  // namespace kvq

@@ -1,0 +1,197 @@
+"""ctypes binding of libkvq.so (include/kvq.h) -- argument marshalling only.
+
+Every function here turns tensors into pointers and sizes and calls the C
+ABI of the same name; all computation runs in the library's CUDA kernels.
+Importing this module loads the library and raises if it was not built
+(``python -m int8_kv_cache_reshape_gb300.build`` or ``__graft_entry__.build()``):
+there is no fallback.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+import re
+
+_HERE = os.path.dirname(os.path.abspath(__file__))
+LIB_PATH = os.path.join(_HERE, "libkvq.so")
+HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
+
+OK = 0
+E_INVALID_ARG, E_UNSUPPORTED, E_SCHED_MISMATCH = -1, -2, -3
+E_WORKSPACE_TOO_SMALL, E_CUDA, E_NO_MEMORY = -4, -5, -6
+
+DTYPES = {"auto": 0, "fp8_e4m3": 1, "fp8_e5m2": 2, "int8_per_token_head": 3,
+          "fp8_per_token_head": 4}
+
+
+class KvqError(RuntimeError):
+    def __init__(self, status: int, what: str):
+        self.status = status
+        super().__init__(f"{what}: {status_string(status)} ({status})")
+
+
+if not os.path.exists(LIB_PATH):
+    raise ImportError(f"libkvq.so is not built ({LIB_PATH}); run "
+                      "int8_kv_cache_reshape_gb300.build.build() first")
+
+lib = ctypes.CDLL(LIB_PATH)
+
+
+class SchedInfo(ctypes.Structure):
+    _fields_ = [("num_req", ctypes.c_int), ("heads_q", ctypes.c_int),
+                ("heads_kv", ctypes.c_int), ("head_dim", ctypes.c_int),
+                ("dtype", ctypes.c_int), ("kv_elem_bytes", ctypes.c_int),
+                ("row_bytes", ctypes.c_int), ("causal", ctypes.c_int),
+                ("window", ctypes.c_int),
+                ("num_rowtile_items", ctypes.c_int64),
+                ("num_split_items", ctypes.c_int64),
+                ("num_merge_items", ctypes.c_int64),
+                ("num_prefill_items", ctypes.c_int64),
+                ("max_splits", ctypes.c_int64),
+                ("total_query_tokens", ctypes.c_int64),
+                ("workspace_bytes", ctypes.c_size_t),
+                ("rowtile_smem_bytes", ctypes.c_size_t),
+                ("prefill_smem_bytes", ctypes.c_size_t),
+                ("num_kernel_launches", ctypes.c_int64)]
+
+    def as_dict(self):
+        return {k: getattr(self, k) for k, _ in self._fields_}
+
+
+_c = ctypes
+_p = ctypes.c_void_p
+lib.kvq_status_string.restype = _c.c_char_p
+lib.kvq_status_string.argtypes = [_c.c_int]
+lib.kvq_parse_kv_cache_dtype.restype = _c.c_int
+lib.kvq_parse_kv_cache_dtype.argtypes = [_c.c_char_p, _c.POINTER(_c.c_int)]
+lib.kvq_cache_row_bytes.restype = _c.c_int
+lib.kvq_cache_row_bytes.argtypes = [_c.c_int, _c.c_int, _c.POINTER(_c.c_size_t)]
+lib.kvq_reshape_and_cache.restype = _c.c_int
+lib.kvq_reshape_and_cache.argtypes = [
+    _p, _p, _c.c_int64, _c.c_int64, _c.c_int64, _c.c_int, _c.c_int, _p, _p,
+    _c.c_int64, _c.c_int, _p, _c.c_int, _c.c_float, _c.c_float, _p]
+lib.kvq_get_scheduler_metadata.restype = _c.c_int
+lib.kvq_get_scheduler_metadata.argtypes = [
+    _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _c.c_int, _c.c_int,
+    _c.c_int, _c.POINTER(_p), _c.POINTER(_c.c_size_t)]
+lib.kvq_attention_with_kv_cache.restype = _c.c_int
+lib.kvq_attention_with_kv_cache.argtypes = [
+    _p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _p, _p, _p, _p,
+    _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
+    _c.c_float, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
+lib.kvq_sched_destroy.restype = None
+lib.kvq_sched_destroy.argtypes = [_p]
+lib.kvq_sched_get_info.restype = _c.c_int
+lib.kvq_sched_get_info.argtypes = [_p, _c.POINTER(SchedInfo)]
+
+
+def declared_functions() -> list:
+    """Names of the functions include/kvq.h declares."""
+    text = open(HEADER).read()
+    text = re.sub(r"/\*.*?\*/", "", text, flags=re.S)
+    return sorted(set(re.findall(r"\b(kvq_\w+)\s*\(", text)))
+
+
+def status_string(status: int) -> str:
+    return lib.kvq_status_string(int(status)).decode()
+
+
+def _check(rc: int, what: str) -> None:
+    if rc != OK:
+        raise KvqError(rc, what)
+
+
+def _ptr(t):
+    return None if t is None else _p(t.data_ptr())
+
+
+def _stream(stream):
+    if stream is None:
+        import torch
+        stream = torch.cuda.current_stream()
+    return _p(getattr(stream, "cuda_stream", stream))
+
+
+def parse_kv_cache_dtype(s) -> int:
+    out = _c.c_int()
+    _check(lib.kvq_parse_kv_cache_dtype(None if s is None else s.encode(), _c.byref(out)),
+           "kvq_parse_kv_cache_dtype")
+    return out.value
+
+
+def cache_row_bytes(kv_cache_dtype, head_dim: int) -> int:
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    out = _c.c_size_t()
+    _check(lib.kvq_cache_row_bytes(dt, head_dim, _c.byref(out)), "kvq_cache_row_bytes")
+    return out.value
+
+
+def reshape_and_cache(key, value, key_cache, value_cache, slot_mapping, kv_cache_dtype,
+                      k_scale: float = 1.0, v_scale: float = 1.0, stream=None) -> None:
+    """key/value: bf16 [T, Hkv, D] (token stride may exceed Hkv*D);
+    caches: uint8 [NB, B, Hkv, row]; slot_mapping: int64 [T]."""
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    T, H, D = key.shape
+    nb, bs = key_cache.shape[0], key_cache.shape[1]
+    _check(lib.kvq_reshape_and_cache(
+        _ptr(key), _ptr(value), T, key.stride(0), value.stride(0), H, D,
+        _ptr(key_cache), _ptr(value_cache), nb, bs, _ptr(slot_mapping), dt,
+        float(k_scale), float(v_scale), _stream(stream)), "kvq_reshape_and_cache")
+
+
+class Sched:
+    """Owns one kvq_sched_t (freed on close / garbage collection)."""
+
+    def __init__(self, handle, workspace_bytes: int):
+        self.handle = handle
+        self.workspace_bytes = workspace_bytes
+
+    def info(self) -> dict:
+        inf = SchedInfo()
+        _check(lib.kvq_sched_get_info(self.handle, _c.byref(inf)), "kvq_sched_get_info")
+        return inf.as_dict()
+
+    def close(self):
+        if self.handle is not None:
+            lib.kvq_sched_destroy(self.handle)
+            self.handle = None
+
+    def __del__(self):
+        self.close()
+
+
+def get_scheduler_metadata(num_req: int, heads_q: int, heads_kv: int, head_dim: int,
+                           seq_lens, query_start_loc, causal: bool, window: int,
+                           kv_cache_dtype) -> Sched:
+    """seq_lens / query_start_loc: host int32 tensors or arrays."""
+    import numpy as np
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    sl = np.ascontiguousarray(np.asarray(seq_lens), dtype=np.int32)
+    qsl = np.ascontiguousarray(np.asarray(query_start_loc), dtype=np.int32)
+    h = _p()
+    ws = _c.c_size_t()
+    _check(lib.kvq_get_scheduler_metadata(
+        num_req, heads_q, heads_kv, head_dim, _p(sl.ctypes.data), _p(qsl.ctypes.data),
+        int(bool(causal)), int(window), dt, _c.byref(h), _c.byref(ws)),
+        "kvq_get_scheduler_metadata")
+    return Sched(h, ws.value)
+
+
+def attention_with_kv_cache(sched: Sched, q, key_cache, value_cache, query_start_loc,
+                            seq_lens, block_table, sm_scale: float, causal: bool,
+                            window: int, soft_cap: float, k_scale: float, v_scale: float,
+                            out, workspace, kv_cache_dtype, heads_kv: int, stream=None,
+                            num_blocks=None) -> None:
+    """q / out: bf16 [sum Q, Hq, D]; caches uint8 [NB, B, Hkv, row];
+    block_table int32 [R, max_blocks]; query_start_loc / seq_lens device
+    int32; workspace: a uint8 device tensor of >= sched.workspace_bytes."""
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    _, Hq, D = q.shape
+    nb = key_cache.shape[0] if num_blocks is None else num_blocks
+    ws_bytes = 0 if workspace is None else workspace.numel() * workspace.element_size()
+    _check(lib.kvq_attention_with_kv_cache(
+        sched.handle, Hq, heads_kv, D, dt, _ptr(q), _ptr(key_cache), _ptr(value_cache),
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), block_table.stride(0),
+        key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
+        float(soft_cap), float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
+        ws_bytes, _stream(stream)), "kvq_attention_with_kv_cache")

@@ -24,6 +24,7 @@ from __future__ import annotations
 
 import ctypes
 import os
+import platform
 import subprocess
 import threading
 
@@ -31,7 +32,7 @@ import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
 _SRC = os.path.join(_HERE, "kvq_oracle.c")
-_BUILD_DIR = os.path.join(_HERE, "_build")
+_BUILD_DIR = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkvq_oracle.so")
 
 AUTO, FP8_E4M3, FP8_E5M2, INT8_PER_TOKEN_HEAD, FP8_PER_TOKEN_HEAD = range(5)

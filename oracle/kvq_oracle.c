@@ -238,6 +238,9 @@ int kvo_reshape_and_cache(const uint16_t* key, const uint16_t* value,
                           int dtype, float k_scale, float v_scale) {
   int64_t row = kvo_row_bytes(dtype, head_dim);
   if (row < 0) return -1;
+  /* Tokens are independent (each slot is written by one token; a slot
+   * named twice has no defined winner, here or in any parallel writer). */
+#pragma omp parallel for schedule(dynamic, 64)
   for (int64_t t = 0; t < num_tokens; ++t) {
     int64_t slot = slot_mapping[t];
     int64_t blk, off;

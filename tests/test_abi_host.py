@@ -1,0 +1,167 @@
+"""Host-side tests of the C ABI (no GPU): the library loads and exports
+every function include/kvq.h declares; dtype parsing, row sizes, argument
+checks and the scheduler's plan (built host-only when no device is present).
+
+The scheduler and its checks restate the vllm PR 50194 page (Breakdown
+item 1, Key source snippet): the plan is sized from the KV cache dtype, and
+a runtime that disagrees with the plan is refused.
+"""
+import ctypes
+import subprocess
+
+import numpy as np
+import pytest
+
+from int8_kv_cache_reshape_gb300 import build as kbuild
+
+kbuild.build()
+from int8_kv_cache_reshape_gb300 import kvq  # noqa: E402
+
+
+def test_every_declared_function_is_exported():
+    names = kvq.declared_functions()
+    assert {"kvq_reshape_and_cache", "kvq_get_scheduler_metadata",
+            "kvq_attention_with_kv_cache", "kvq_sched_destroy"} <= set(names)
+    for n in names:
+        assert hasattr(kvq.lib, n), n
+    out = subprocess.run(["nm", "-D", "--defined-only", kvq.LIB_PATH],
+                         capture_output=True, text=True, check=True).stdout
+    exported = {line.split()[-1] for line in out.splitlines() if " T " in line}
+    assert set(names) <= exported
+    # nothing but the ABI is exported
+    assert {n for n in exported if n.startswith("kvq")} == set(names)
+
+
+@pytest.mark.parametrize("s,want", [("auto", 0), (None, 0), ("", 0), ("fp8", 1),
+                                    ("fp8_e4m3", 1), ("fp8_e5m2", 2),
+                                    ("int8_per_token_head", 3), ("fp8_per_token_head", 4)])
+def test_parse_dtype(s, want):
+    assert kvq.parse_kv_cache_dtype(s) == want
+
+
+def test_parse_dtype_rejects_unknown():
+    with pytest.raises(kvq.KvqError) as e:
+        kvq.parse_kv_cache_dtype("fp8_e3m4")
+    assert e.value.status == kvq.E_INVALID_ARG
+
+
+def test_row_bytes():
+    assert kvq.cache_row_bytes("auto", 128) == 256
+    assert kvq.cache_row_bytes("fp8_e4m3", 128) == 128
+    assert kvq.cache_row_bytes("fp8_e5m2", 256) == 256
+    assert kvq.cache_row_bytes("int8_per_token_head", 128) == 144
+    assert kvq.cache_row_bytes("fp8_per_token_head", 64) == 80
+    with pytest.raises(kvq.KvqError):
+        kvq.cache_row_bytes("fp8_e4m3", 100)
+
+
+def test_status_strings():
+    for s in (0, -1, -2, -3, -4, -5, -6):
+        assert kvq.status_string(s) and kvq.status_string(s) != "unknown status"
+    assert kvq.status_string(-99) == "unknown status"
+
+
+def _rac(**kw):
+    """Call kvq_reshape_and_cache with fake (never dereferenced) pointers;
+    only argument checks that fail before any launch are exercised."""
+    a = dict(key=256, value=512, T=4, ks=256, vs=256, H=2, D=128, kc=1024,
+             vc=2048, nb=4, bs=16, slots=4096, dt=1, k=1.0, v=1.0)
+    a.update(kw)
+    return kvq.lib.kvq_reshape_and_cache(
+        ctypes.c_void_p(a["key"]), ctypes.c_void_p(a["value"]), a["T"], a["ks"], a["vs"],
+        a["H"], a["D"], ctypes.c_void_p(a["kc"]), ctypes.c_void_p(a["vc"]), a["nb"], a["bs"],
+        ctypes.c_void_p(a["slots"]), a["dt"], a["k"], a["v"], None)
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(D=96), kvq.E_UNSUPPORTED), (dict(dt=9), kvq.E_INVALID_ARG),
+    (dict(T=-1), kvq.E_INVALID_ARG), (dict(key=0), kvq.E_INVALID_ARG),
+    (dict(ks=255), kvq.E_INVALID_ARG), (dict(ks=100), kvq.E_INVALID_ARG),
+    (dict(key=264), kvq.E_INVALID_ARG), (dict(kc=1032), kvq.E_INVALID_ARG),
+    (dict(k=0.0), kvq.E_INVALID_ARG), (dict(v=float("nan")), kvq.E_INVALID_ARG),
+    (dict(k=float("inf")), kvq.E_INVALID_ARG), (dict(H=0), kvq.E_INVALID_ARG),
+    (dict(T=0), kvq.OK),
+])
+def test_reshape_and_cache_argument_checks(kw, want):
+    assert _rac(**kw) == want
+
+
+def _sched(seq_lens, query_lens, hq=32, hkv=8, D=128, dtype="fp8_e4m3", causal=True,
+           window=0):
+    qsl = np.concatenate([[0], np.cumsum(query_lens)]).astype(np.int32)
+    return kvq.get_scheduler_metadata(len(seq_lens), hq, hkv, D, np.array(seq_lens, np.int32),
+                                      qsl, causal, window, dtype)
+
+
+def test_scheduler_decode_plan_covers_every_chunk(monkeypatch):
+    monkeypatch.delenv("KVQ_NUM_SPLITS", raising=False)
+    rng = np.random.default_rng(0)
+    L = rng.integers(1024, 4097, 64)
+    s = _sched(L, [1] * 64)
+    info = s.info()
+    assert info["kv_elem_bytes"] == 1 and info["row_bytes"] == 128
+    assert info["total_query_tokens"] == 64
+    assert info["num_rowtile_items"] >= 64 * 8
+    assert info["num_merge_items"] <= 64 * 8
+    # partial rows: 4 rows (G = 4) per split item
+    assert info["workspace_bytes"] >= info["num_split_items"] * 4 * (128 + 1) * 4
+    s.close()
+
+
+def test_scheduler_sizes_follow_kv_element_size():
+    """The vllm PR 50194 page's bug: scratch sized from the query's element
+    size instead of the cache's.  The plan's row size and shared memory
+    follow the cache dtype."""
+    a = _sched([300], [1], dtype="fp8_e4m3").info()
+    b = _sched([300], [1], dtype="int8_per_token_head").info()
+    assert a["row_bytes"] == 128 and b["row_bytes"] == 144
+    assert a["kv_elem_bytes"] == b["kv_elem_bytes"] == 1
+    assert b["rowtile_smem_bytes"] > a["rowtile_smem_bytes"]
+    d = _sched([300], [1], D=256).info()
+    assert d["rowtile_smem_bytes"] <= 227 * 1024
+
+
+def test_forced_splits(monkeypatch):
+    monkeypatch.setenv("KVQ_NUM_SPLITS", "5")
+    info = _sched([1000, 37], [1, 1]).info()
+    assert info["max_splits"] == 5
+    assert info["num_merge_items"] == 2 * 8
+    monkeypatch.setenv("KVQ_NUM_SPLITS", "1")
+    info = _sched([1000, 37], [1, 1]).info()
+    assert info["num_merge_items"] == 0 and info["workspace_bytes"] == 0
+
+
+@pytest.mark.parametrize("kw,want", [
+    (dict(hq=30, hkv=8), kvq.E_UNSUPPORTED), (dict(D=96), kvq.E_UNSUPPORTED),
+    (dict(dtype="auto"), kvq.E_UNSUPPORTED), (dict(causal=False, window=8), kvq.E_INVALID_ARG),
+])
+def test_scheduler_rejects(kw, want):
+    with pytest.raises(kvq.KvqError) as e:
+        _sched([10, 20], [1, 2], **kw)
+    assert e.value.status == want
+
+
+def test_scheduler_rejects_more_queries_than_keys():
+    with pytest.raises(kvq.KvqError) as e:
+        _sched([3], [4])
+    assert e.value.status == kvq.E_INVALID_ARG
+
+
+def test_empty_batch_and_zero_query_requests():
+    s = _sched([], [])
+    assert s.info()["num_rowtile_items"] == 0 and s.workspace_bytes == 0
+    s = _sched([40, 0], [0, 0])
+    assert s.info()["num_rowtile_items"] == 0
+
+
+def test_attention_refuses_mismatched_schedule():
+    s = _sched([64], [1], dtype="fp8_e4m3")
+    f = kvq.lib.kvq_attention_with_kv_cache
+    args = lambda hq, hkv, D, dt, causal=1, window=0: (
+        s.handle, hq, hkv, D, dt, *([ctypes.c_void_p(256)] * 6), 4, 16, 8, 0.1, causal,
+        window, 0.0, 1.0, 1.0, ctypes.c_void_p(256), None, 0, None)
+    assert f(*args(32, 8, 128, 3)) == kvq.E_SCHED_MISMATCH     # other dtype
+    assert f(*args(32, 8, 64, 1)) == kvq.E_SCHED_MISMATCH      # other head_dim
+    assert f(*args(16, 8, 128, 1)) == kvq.E_SCHED_MISMATCH     # other heads
+    assert f(*args(32, 8, 128, 1, causal=0)) == kvq.E_SCHED_MISMATCH
+    assert f(*args(32, 8, 128, 1, window=5)) == kvq.E_SCHED_MISMATCH
