@@ -42,6 +42,12 @@ __device__ __forceinline__ uint32_t enc_int8(float y) {
   return (uint32_t)v & 0xFFu;
 }
 
+__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
+  uint32_t r;
+  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
+  return r;
+}
+
 // ---- code pairs -> f16x2 (exact) ---------------------------------------------
 // `pair` holds two codes: bits 0-7 -> low half, bits 8-15 -> high half.
 __device__ __forceinline__ uint32_t e4m3x2_to_f16x2(uint32_t pair) {
@@ -72,10 +78,29 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t pair) {
   else return e4m3x2_to_f16x2(pair);
 }
 
-__device__ __forceinline__ uint32_t prmt(uint32_t a, uint32_t b, uint32_t sel) {
-  uint32_t r;
-  asm("prmt.b32 %0, %1, %2, %3;" : "=r"(r) : "r"(a), "r"(b), "r"(sel));
-  return r;
+// Four codes (one 32-bit word) -> two f16x2: lo gets bytes 0-1, hi bytes
+// 2-3.  The word is split into its 16-bit halves inside the asm block.
+template <int DT>
+__device__ __forceinline__ void word_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
+  if constexpr (DT == KVQ_FP8_E5M2) {
+    // E5M2 code = upper byte of the f16: place each byte above a zero byte.
+    lo = prmt(w, 0u, 0x1404u);
+    hi = prmt(w, 0u, 0x3424u);
+  } else if constexpr (DT == KVQ_INT8_PER_TOKEN_HEAD) {
+    // bias to unsigned, put each byte under the f16 exponent of 1024 (0x64),
+    // subtract 1024 + 128.
+    const uint32_t u = w ^ 0x80808080u;
+    const uint32_t a = prmt(u, 0x64646464u, 0x7170u);
+    const uint32_t b = prmt(u, 0x64646464u, 0x7372u);
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(lo) : "r"(a), "r"(0x64806480u));
+    asm("sub.rn.f16x2 %0, %1, %2;" : "=r"(hi) : "r"(b), "r"(0x64806480u));
+  } else {
+    asm("{\n\t.reg .b16 l16, h16;\n\t"
+        "mov.b32 {l16, h16}, %2;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %0, l16;\n\t"
+        "cvt.rn.f16x2.e4m3x2 %1, h16;\n\t}"
+        : "=r"(lo), "=r"(hi) : "r"(w));
+  }
 }
 
 __device__ __forceinline__ uint32_t pack_f16x2(float lo, float hi) {

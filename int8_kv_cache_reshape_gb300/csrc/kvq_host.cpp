@@ -33,8 +33,8 @@ struct kvq_sched {
   std::vector<MergeItem> merges;
   int64_t partial_rows;
   size_t workspace_bytes;
-  void* d_buf;  // device copy: items, then merges
-  size_t d_items_off, d_merges_off;
+  void* d_buf;  // device copy: items, merges, then merge counters
+  size_t d_items_off, d_merges_off, d_counters_off;
 };
 
 namespace {
@@ -199,7 +199,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         t.it.chunk_lo = (int32_t)c_lo;
         t.it.chunk_hi = (int32_t)c_hi;
         t.it.part = -1;
-        t.it.pad = 0;
+        t.it.merge = -1;
         t.chunks = c_hi - c_lo;
         total_chunks += t.chunks;
         tiles.push_back(t);
@@ -245,6 +245,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
       it.chunk_lo = (int32_t)(t.it.chunk_lo + t.chunks * k / ns);
       it.chunk_hi = (int32_t)(t.it.chunk_lo + t.chunks * (k + 1) / ns);
       it.part = (int32_t)(s->partial_rows + k * t.it.nrows);
+      it.merge = (int32_t)(s->merges.size() - 1);
       dst.push_back(it);
       ++s->n_split;
     }
@@ -261,7 +262,9 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
   s->d_items_off = 0;
   s->d_merges_off = kvq::align256(items_bytes);
-  const size_t total = s->d_merges_off + merges_bytes;
+  s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
+  const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
+  const size_t total = s->d_counters_off + counters_bytes;
   if (total > 0 && have_device) {
     if (cudaMalloc(&s->d_buf, total) != cudaSuccess) {
       cudaGetLastError();
@@ -275,6 +278,9 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     if (merges_bytes)
       ok &= cudaMemcpy(static_cast<char*>(s->d_buf) + s->d_merges_off, s->merges.data(),
                        merges_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (counters_bytes)
+      ok &= cudaMemset(static_cast<char*>(s->d_buf) + s->d_counters_off, 0, counters_bytes) ==
+            cudaSuccess;
     if (!ok) {
       kvq_sched_destroy(s);
       return KVQ_E_CUDA;
@@ -306,7 +312,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->workspace_bytes = s->workspace_bytes;
   out->rowtile_smem_bytes = kvq::rowtile_smem_bytes(s->dtype, s->head_dim);
   out->prefill_smem_bytes = 0;
-  out->num_kernel_launches = (s->n_tiles1 > 0) + (s->n_tiles2 > 0) + (!s->merges.empty());
+  out->num_kernel_launches = (s->n_tiles1 > 0) + (s->n_tiles2 > 0);
   return KVQ_OK;
 }
 
@@ -364,6 +370,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
                    : nullptr;
   p.items = reinterpret_cast<const RowtileItem*>(static_cast<char*>(s->d_buf) + s->d_items_off);
   p.merges = reinterpret_cast<const MergeItem*>(static_cast<char*>(s->d_buf) + s->d_merges_off);
+  p.merge_counters = reinterpret_cast<int32_t*>(static_cast<char*>(s->d_buf) + s->d_counters_off);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;
   p.block_size = block_size;
@@ -382,8 +389,6 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     rc = kvq::launch_rowtile(p, s->dtype, head_dim, 1, 0, s->n_tiles1, stream);
   if (rc == KVQ_OK && s->n_tiles2 > 0)
     rc = kvq::launch_rowtile(p, s->dtype, head_dim, 2, s->n_tiles1, s->n_tiles2, stream);
-  if (rc == KVQ_OK && !s->merges.empty())
-    rc = kvq::launch_merge(p, head_dim, (int64_t)s->merges.size(), stream);
   return rc;
 }
 

@@ -55,10 +55,15 @@ KVQ_HD constexpr int rowtile_chunk_bytes(int dtype, int head_dim) {
   return 2 * kChunkTokens * head_dim * kv_elem_bytes(dtype) +
          (is_per_token_head(dtype) ? 32 * 16 : 0);
 }
-// Pipeline depth: enough chunks in flight per warp to cover HBM latency,
-// fewer when a chunk is large.
+// Pipeline depth: enough chunks in flight per warp to cover HBM latency
+// (with 12-16 warps per SM, 2-3 chunks each), fewer when a chunk is large.
 KVQ_HD constexpr int rowtile_stages(int dtype, int head_dim) {
-  return rowtile_chunk_bytes(dtype, head_dim) >= 8192 ? 3 : 4;
+  return rowtile_chunk_bytes(dtype, head_dim) >= 4096 ? 3 : 4;
+}
+// Resident CTAs per SM the kernel is compiled for (register budget):
+// 4 for the common decode tiles, fewer for wider tiles.
+KVQ_HD constexpr int rowtile_min_ctas(int dtype, int head_dim, int ntiles) {
+  return head_dim >= 256 ? 2 : (ntiles == 1 ? 4 : 3);
 }
 KVQ_HD constexpr size_t rowtile_pipeline_smem(int dtype, int head_dim) {
   return (size_t)kRowtileWarps * rowtile_stages(dtype, head_dim) *
@@ -87,7 +92,7 @@ struct RowtileItem {
   int32_t chunk_lo;  // first 16-token KV chunk
   int32_t chunk_hi;  // one past the last chunk
   int32_t part;      // -1: write `out`; else first partial row in workspace
-  int32_t pad;
+  int32_t merge;     // merge item of a split tile (-1: not split)
 };
 static_assert(sizeof(RowtileItem) == 32, "RowtileItem layout");
 
@@ -126,6 +131,7 @@ struct AttnParams {
   float* part_lse;             // [P]
   const RowtileItem* items;
   const MergeItem* merges;
+  int32_t* merge_counters;     // one per merge item, zero between calls
   int64_t num_blocks;
   int block_table_stride;
   int block_size;
@@ -147,6 +153,4 @@ int launch_reshape_and_cache(const void* key, const void* value,
                              float k_scale, float v_scale, void* stream);
 int launch_rowtile(const AttnParams& p, int dtype, int head_dim, int ntiles,
                    int64_t item_offset, int64_t num_items, void* stream);
-int launch_merge(const AttnParams& p, int head_dim, int64_t num_items,
-                 void* stream);
 }  // namespace kvq
