@@ -198,6 +198,33 @@ KVQ_API int kvq_attention_with_kv_cache(const kvq_sched_t* sched, int heads_q,
                                 float v_scale, void* out, void* workspace,
                                 size_t workspace_bytes, void* stream);
 
+/* attention_with_kv_cache_static_scratch -- the same attention for callers
+ * that cannot allocate device memory (no cudaMalloc in their context: a
+ * serving loop whose device heap is owned by a memory pool or allocator
+ * hook).  It takes no workspace: the split-KV partials go to a fixed
+ * KVQ_STATIC_SCRATCH_BYTES array of device memory that the library reserves
+ * on every device it is loaded on, held until the process exits.  There is
+ * no counterpart on the pages this library follows; it is an interface
+ * addition.
+ *   Arguments, layouts, ownership and checks are those of
+ *   kvq_attention_with_kv_cache without workspace / workspace_bytes.  A
+ *   schedule needing more scratch than KVQ_STATIC_SCRATCH_BYTES
+ *   (kvq_sched_get_info's workspace_bytes) is refused with
+ *   KVQ_E_WORKSPACE_TOO_SMALL before anything is enqueued.
+ *   The call allocates nothing.  The first call on each device looks up the
+ *   array's device address (cudaGetSymbolAddress); make that first call
+ *   before any stream capture.
+ *   All calls on a device share the one array and it keeps the last call's
+ *   contents: calls that may overlap on the GPU (other streams, other host
+ *   threads) race on it; order them on one stream. */
+#define KVQ_STATIC_SCRATCH_BYTES (16u << 20)
+KVQ_API int kvq_attention_with_kv_cache_static_scratch(
+    const kvq_sched_t* sched, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype,
+    const void* q, const void* key_cache, const void* value_cache,
+    const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,
+    int block_table_stride, int block_size, int64_t num_blocks, float sm_scale, int causal,
+    int window, float soft_cap, float k_scale, float v_scale, void* out, void* stream);
+
 /* Free a schedule (NULL is a no-op).  Its device work list is released
  * with cudaFree, which waits for the device: call it after the attention
  * calls that use it have been enqueued. */

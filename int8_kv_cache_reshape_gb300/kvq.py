@@ -79,6 +79,12 @@ lib.kvq_attention_with_kv_cache.argtypes = [
     _p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _p, _p, _p, _p,
     _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
     _c.c_float, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
+lib.kvq_attention_with_kv_cache_static_scratch.restype = _c.c_int
+lib.kvq_attention_with_kv_cache_static_scratch.argtypes = [
+    _p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _p, _p, _p, _p,
+    _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
+    _c.c_float, _c.c_float, _c.c_float, _p, _p]
+STATIC_SCRATCH_BYTES = 16 << 20
 lib.kvq_sched_destroy.restype = None
 lib.kvq_sched_destroy.argtypes = [_p]
 lib.kvq_sched_get_info.restype = _c.c_int
@@ -195,3 +201,24 @@ def attention_with_kv_cache(sched: Sched, q, key_cache, value_cache, query_start
         key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
         float(soft_cap), float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
         ws_bytes, _stream(stream)), "kvq_attention_with_kv_cache")
+
+
+def attention_with_kv_cache_static_scratch(sched: Sched, q, key_cache, value_cache,
+                                           query_start_loc, seq_lens, block_table,
+                                           sm_scale: float, causal: bool, window: int,
+                                           soft_cap: float, k_scale: float, v_scale: float,
+                                           out, kv_cache_dtype, heads_kv: int, stream=None,
+                                           num_blocks=None) -> None:
+    """attention_with_kv_cache without a workspace argument: the library's
+    fixed device scratch (STATIC_SCRATCH_BYTES) holds the split partials.
+    For callers that cannot allocate device memory; calls must not overlap
+    on the GPU."""
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    _, Hq, D = q.shape
+    nb = key_cache.shape[0] if num_blocks is None else num_blocks
+    _check(lib.kvq_attention_with_kv_cache_static_scratch(
+        sched.handle, Hq, heads_kv, D, dt, _ptr(q), _ptr(key_cache), _ptr(value_cache),
+        _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), block_table.stride(0),
+        key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
+        float(soft_cap), float(k_scale), float(v_scale), _ptr(out), _stream(stream)),
+        "kvq_attention_with_kv_cache_static_scratch")
