@@ -128,7 +128,7 @@ KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
  * element size that the kernels use.
  *
  *   num_req                 requests in the batch (>= 0)
- *   heads_q, heads_kv       heads_q % heads_kv == 0, heads_q/heads_kv <= 16
+ *   heads_q, heads_kv       heads_q % heads_kv == 0
  *   head_dim                64, 128 or 256
  *   seq_lens_host           host int32 [num_req]: kv length L of each request
  *   query_start_loc_host    host int32 [num_req+1], non-decreasing, [0] == 0;
@@ -141,9 +141,11 @@ KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
  *   out                     receives a new schedule (free: kvq_sched_destroy)
  *   workspace_bytes         receives the scratch size the attention call
  *                           needs (may be 0); must not be NULL.
- * The schedule holds a host copy and one device copy of its work list, made
- * on the current device (a blocking upload).  Decoding requests (Q * heads
- * per kv head <= 16) are split along the KV axis across CTAs. */
+ * The schedule holds a host copy and one device copy of its plan, made on
+ * the current device (a blocking upload).  The rows of each (request, kv
+ * head) form tiles of up to 16 (query, head) rows; the tiles' 16-token KV
+ * chunks are cut into equal contiguous segments, one per warp, so long
+ * contexts are split along the KV axis and merged. */
 KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
                                int head_dim, const int32_t* seq_lens_host,
                                const int32_t* query_start_loc_host, int causal,
@@ -172,7 +174,8 @@ KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  *                           logical block i of request r lives in physical
  *                           block block_table[r*stride + i].  Entries outside
  *                           [0, num_blocks) read as empty (masked) keys.
- *   block_size, num_blocks  cache geometry; block_size a multiple of 16.
+ *   block_size, num_blocks  cache geometry; block_size a multiple of 16,
+ *                           num_blocks * block_size < 2^31.
  *   sm_scale                score scale (typically 1/sqrt(head_dim)).
  *   soft_cap                > 0: z <- soft_cap * tanh(z / soft_cap) after
  *                           sm_scale; <= 0: off.
@@ -233,20 +236,20 @@ KVQ_API void kvq_sched_destroy(kvq_sched_t* sched);
 /* Summary of a schedule, for tests and benchmarks. */
 typedef struct {
   int num_req, heads_q, heads_kv, head_dim;
-  int dtype;                 /* kvq_dtype_t the schedule was built for     */
-  int kv_elem_bytes;         /* bytes per cached K/V element (1 or 2)      */
-  int row_bytes;             /* bytes per (token, kv_head) cache row       */
+  int dtype;                   /* kvq_dtype_t the schedule was built for      */
+  int kv_elem_bytes;           /* bytes per cached K/V element (1 or 2)       */
+  int row_bytes;               /* bytes per (token, kv_head) cache row        */
   int causal, window;
-  int64_t num_rowtile_items; /* work items of the split-KV row-tile kernel */
-  int64_t num_split_items;   /* of those, items that write partials        */
-  int64_t num_merge_items;   /* (request, kv_head) groups to merge         */
-  int64_t num_prefill_items; /* 128-row tiles of the tensor-core kernel    */
-  int64_t max_splits;        /* most KV splits of one row tile             */
+  int64_t num_tiles;           /* row tiles: <= 16 (query, head) rows of a kv head */
+  int64_t num_pieces;          /* tile pieces (a tile cut among warps)        */
+  int64_t num_merge_items;     /* tiles cut into more than one piece          */
+  int64_t num_chunks;          /* 16-token KV chunks streamed in total        */
+  int64_t num_decode_warps;    /* warps the chunk sequence is cut among       */
+  int64_t max_splits;          /* most pieces of one tile                     */
   int64_t total_query_tokens;
   size_t workspace_bytes;
-  size_t rowtile_smem_bytes; /* dynamic shared memory per row-tile CTA     */
-  size_t prefill_smem_bytes; /* dynamic shared memory per prefill CTA      */
-  int64_t num_kernel_launches; /* kernels one attention call launches      */
+  size_t decode_smem_bytes;    /* dynamic shared memory per decode CTA        */
+  int64_t num_kernel_launches; /* kernels one attention call launches         */
 } kvq_sched_info_t;
 
 KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);

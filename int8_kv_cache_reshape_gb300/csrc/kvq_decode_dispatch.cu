@@ -1,0 +1,21 @@
+// kvq_decode_dispatch.cu -- head_dim dispatch of the split-KV decode kernels
+// (one translation unit per head_dim holds the instances).
+#include "kvq_internal.h"
+
+namespace kvq {
+
+int launch_decode_d64(const AttnParams&, int, int, void*);
+int launch_decode_d128(const AttnParams&, int, int, void*);
+int launch_decode_d256(const AttnParams&, int, int, void*);
+
+int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream) {
+  if (p.num_chunks <= 0) return KVQ_OK;
+  switch (head_dim) {
+    case 64: return launch_decode_d64(p, dtype, ntiles, stream);
+    case 128: return launch_decode_d128(p, dtype, ntiles, stream);
+    case 256: return launch_decode_d256(p, dtype, ntiles, stream);
+    default: return KVQ_E_UNSUPPORTED;
+  }
+}
+
+}  // namespace kvq

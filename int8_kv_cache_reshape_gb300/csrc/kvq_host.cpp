@@ -13,28 +13,36 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
-#include <mutex>
 #include <new>
 #include <vector>
 
 #include "kvq_internal.h"
 
+using kvq::ChunkRef;
+using kvq::DecodePiece;
 using kvq::MergeItem;
-using kvq::RowtileItem;
+
+// One launch of the split-KV decode kernel: the tiles with one 8-row n-tile
+// (class 0) or two (class 1).
+struct DecodeLaunch {
+  int64_t chunk_off = 0;   // first entry of the launch's flat chunk sequence
+  int64_t num_chunks = 0;  // its length
+  int num_warps = 0;       // warps the sequence is cut among
+};
 
 struct kvq_sched {
   int num_req, heads_q, heads_kv, head_dim, dtype, causal, window, group;
   int device;
   int64_t total_q;
-  // Row-tile items: [0, n1) use one 8-row n-tile, [n1, n1 + n2) use two.
-  std::vector<RowtileItem> items;
-  int64_t n_tiles1, n_tiles2, n_split;
-  int64_t max_splits;
+  std::vector<DecodePiece> pieces;
+  std::vector<ChunkRef> chunks;
   std::vector<MergeItem> merges;
-  int64_t partial_rows;
+  DecodeLaunch launch[2];
+  int64_t num_tiles, max_splits, partial_rows;
+  int32_t max_chunk;  // highest 16-token chunk index any tile reads
   size_t workspace_bytes;
-  void* d_buf;  // device copy: items, merges, then merge counters
-  size_t d_items_off, d_merges_off, d_counters_off;
+  void* d_buf;  // device copy: pieces, chunks, merges, merge counters
+  size_t d_pieces_off, d_chunks_off, d_merges_off, d_counters_off;
 };
 
 namespace {
@@ -52,6 +60,13 @@ int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
 // SM count assumed when planning without a device (GB300: 152 SMs).
 constexpr int kDefaultSmCount = 152;
+
+// A row tile: packed rows [row0, row0 + nrows) of one (request, kv head)
+// and the 16-token chunks [c_lo, c_hi) those rows can see.
+struct Tile {
+  int req, kv_head, row0, nrows;
+  int64_t c_lo, c_hi, any_lo, any_hi;
+};
 
 }  // namespace
 
@@ -114,6 +129,7 @@ int kvq_reshape_and_cache(const void* key, const void* value, int64_t num_tokens
                                        block_size, slot_mapping, dtype, k_scale, v_scale, stream);
 }
 
+
 void kvq_sched_destroy(kvq_sched_t* s) {
   if (!s) return;
   if (s->d_buf) {
@@ -161,7 +177,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   // Without a usable CUDA device the plan is still built (host-only: its
   // attention calls return KVQ_E_CUDA), so that planning can be inspected
   // on machines without a GPU.
-  bool have_device = cudaGetDevice(&s->device) == cudaSuccess;
+  const bool have_device = cudaGetDevice(&s->device) == cudaSuccess;
   if (!have_device) {
     cudaGetLastError();
     s->device = -1;
@@ -169,101 +185,121 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   const int G = s->group;
 
   // 1) Row tiles: the packed rows (q_index * G + g) of each (request,
-  //    kv_head) in tiles of up to 16, each with the KV chunk range its rows
-  //    can see.
-  struct Tile {
-    RowtileItem it;
-    int64_t chunks;
-  };
-  std::vector<Tile> tiles;
-  int64_t total_chunks = 0;
+  //    kv_head) in tiles of up to 16, each with the chunks its rows can see,
+  //    in (request, kv head) order so neighbouring warps read neighbouring
+  //    rows of the same cache blocks.  Tiles of up to 8 rows use one MMA
+  //    n-tile (class 0), larger ones two (class 1).
+  std::vector<Tile> tiles[2];
+  s->max_chunk = 0;
   for (int r = 0; r < num_req; ++r) {
     const int64_t L = seq_lens_host[r];
     const int64_t Q = (int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r];
     if (Q == 0) continue;
     const int64_t rows = Q * G;
-    for (int64_t row0 = 0; row0 < rows; row0 += kvq::kRowtileMaxRows) {
-      const int64_t nrows = std::min<int64_t>(kvq::kRowtileMaxRows, rows - row0);
-      const int64_t p_min = L - Q + row0 / G;
-      const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
-      const int64_t kv_hi = s->causal ? p_max + 1 : L;
-      const int64_t kv_lo = s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0;
-      const int64_t c_lo = kv_lo / kvq::kChunkTokens;
-      const int64_t c_hi = ceil_div(kv_hi, kvq::kChunkTokens);
-      for (int h = 0; h < heads_kv; ++h) {
+    for (int h = 0; h < heads_kv; ++h) {
+      for (int64_t row0 = 0; row0 < rows; row0 += kvq::kTileMaxRows) {
+        const int64_t nrows = std::min<int64_t>(kvq::kTileMaxRows, rows - row0);
+        const int64_t p_min = L - Q + row0 / G;
+        const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
         Tile t;
-        t.it.req = r;
-        t.it.kv_head = h;
-        t.it.row0 = (int32_t)row0;
-        t.it.nrows = (int32_t)nrows;
-        t.it.chunk_lo = (int32_t)c_lo;
-        t.it.chunk_hi = (int32_t)c_hi;
-        t.it.part = -1;
-        t.it.merge = -1;
-        t.chunks = c_hi - c_lo;
-        total_chunks += t.chunks;
-        tiles.push_back(t);
+        t.req = r;
+        t.kv_head = h;
+        t.row0 = (int)row0;
+        t.nrows = (int)nrows;
+        t.any_hi = s->causal ? p_max + 1 : L;
+        t.any_lo = s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0;
+        t.c_lo = t.any_lo / kvq::kChunkTokens;
+        t.c_hi = ceil_div(t.any_hi, kvq::kChunkTokens);
+        s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)(t.c_hi - 1));
+        tiles[nrows > 8 ? 1 : 0].push_back(t);
       }
     }
   }
+  s->num_tiles = (int64_t)(tiles[0].size() + tiles[1].size());
 
-  // 2) KV splits: aim for a few waves of CTAs over the SMs; no split
-  //    smaller than kMinChunksPerSplit.  KVQ_NUM_SPLITS (benchmarks and
-  //    tests) forces a split count per tile.
+  // 2) Stream decomposition: per class, lay the tiles' chunks end to end and
+  //    cut the sequence into equal contiguous segments, one per warp.  A
+  //    tile cut by a segment boundary becomes several pieces whose partial
+  //    rows are merged.  KVQ_DECODE_WARPS (tests, benchmarks) forces the
+  //    warp count.
   const int sms = have_device ? std::max(1, sm_count()) : kDefaultSmCount;
-  const int64_t target_ctas = (int64_t)sms * 3 * 4;
-  int64_t per_split = std::max<int64_t>(kvq::kMinChunksPerSplit, ceil_div(total_chunks, target_ctas));
   int64_t forced = 0;
-  if (const char* env = std::getenv("KVQ_NUM_SPLITS")) forced = std::atoll(env);
-
-  std::vector<RowtileItem> one, two;
+  if (const char* env = std::getenv("KVQ_DECODE_WARPS")) forced = std::atoll(env);
   s->partial_rows = 0;
   s->max_splits = 0;
-  s->n_split = 0;
-  std::stable_sort(tiles.begin(), tiles.end(),
-                   [](const Tile& a, const Tile& b) { return a.chunks > b.chunks; });
-  for (const Tile& t : tiles) {
-    int64_t ns = forced > 0 ? forced : ceil_div(t.chunks, per_split);
-    ns = std::max<int64_t>(1, std::min<int64_t>(ns, t.chunks));
-    s->max_splits = std::max(s->max_splits, ns);
-    auto& dst = t.it.nrows <= 8 ? one : two;
-    if (ns == 1) {
-      dst.push_back(t.it);
-      continue;
+  for (int cls = 0; cls < 2; ++cls) {
+    DecodeLaunch& dl = s->launch[cls];
+    dl.chunk_off = (int64_t)s->chunks.size();
+    int64_t T = 0;
+    for (const Tile& t : tiles[cls]) T += t.c_hi - t.c_lo;
+    dl.num_chunks = T;
+    if (T == 0) continue;
+    const int64_t max_ctas = (int64_t)sms * kvq::decode_min_ctas(dtype, head_dim, cls + 1);
+    int64_t ctas = std::min<int64_t>(max_ctas, std::max<int64_t>(1, ceil_div(T, kvq::kDecodeWarps * kvq::kMinChunksPerWarp)));
+    if (forced > 0) ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(forced, kvq::kDecodeWarps), ceil_div(T, kvq::kDecodeWarps)));
+    const int64_t W = ctas * kvq::kDecodeWarps;
+    dl.num_warps = (int)W;
+    auto seg_start = [&](int64_t w) { return w * T / W; };
+    int64_t F = 0;  // flat position of the current tile's first chunk
+    for (const Tile& t : tiles[cls]) {
+      const int64_t nt = t.c_hi - t.c_lo;
+      // Warps whose segments overlap [F, F + nt).
+      int64_t w0 = (F * W) / T;
+      while (w0 > 0 && seg_start(w0) > F) --w0;
+      while (seg_start(w0 + 1) <= F) ++w0;
+      std::vector<std::pair<int64_t, int64_t>> cuts;  // [lo, hi) flat ranges
+      for (int64_t w = w0; w < W && seg_start(w) < F + nt; ++w) {
+        const int64_t lo = std::max<int64_t>(F, seg_start(w));
+        const int64_t hi = std::min<int64_t>(F + nt, seg_start(w + 1));
+        if (hi > lo) cuts.push_back({lo, hi});
+      }
+      const int64_t np = (int64_t)cuts.size();
+      s->max_splits = std::max(s->max_splits, np);
+      int32_t merge = -1;
+      int64_t part0 = -1;
+      if (np > 1) {
+        MergeItem m;
+        m.req = t.req;
+        m.kv_head = t.kv_head;
+        m.row0 = t.row0;
+        m.nrows = t.nrows;
+        m.part = (int32_t)s->partial_rows;
+        m.nsplits = (int32_t)np;
+        m.pad0 = m.pad1 = 0;
+        merge = (int32_t)s->merges.size();
+        s->merges.push_back(m);
+        part0 = s->partial_rows;
+        s->partial_rows += np * t.nrows;
+      }
+      for (int64_t k = 0; k < np; ++k) {
+        DecodePiece pc;
+        pc.req = t.req;
+        pc.kv_head = t.kv_head;
+        pc.row0 = t.row0;
+        pc.nrows = t.nrows;
+        pc.part = np > 1 ? (int32_t)(part0 + k * t.nrows) : -1;
+        pc.merge = merge;
+        pc.any_lo = (int32_t)t.any_lo;
+        pc.any_hi = (int32_t)t.any_hi;
+        const int32_t idx = (int32_t)s->pieces.size();
+        s->pieces.push_back(pc);
+        for (int64_t f = cuts[k].first; f < cuts[k].second; ++f)
+          s->chunks.push_back(ChunkRef{idx, (int32_t)(t.c_lo + (f - F))});
+      }
+      F += nt;
     }
-    MergeItem m;
-    m.req = t.it.req;
-    m.kv_head = t.it.kv_head;
-    m.row0 = t.it.row0;
-    m.nrows = t.it.nrows;
-    m.part = (int32_t)s->partial_rows;
-    m.nsplits = (int32_t)ns;
-    m.pad0 = m.pad1 = 0;
-    s->merges.push_back(m);
-    for (int64_t k = 0; k < ns; ++k) {
-      RowtileItem it = t.it;
-      it.chunk_lo = (int32_t)(t.it.chunk_lo + t.chunks * k / ns);
-      it.chunk_hi = (int32_t)(t.it.chunk_lo + t.chunks * (k + 1) / ns);
-      it.part = (int32_t)(s->partial_rows + k * t.it.nrows);
-      it.merge = (int32_t)(s->merges.size() - 1);
-      dst.push_back(it);
-      ++s->n_split;
-    }
-    s->partial_rows += ns * t.it.nrows;
   }
-  s->n_tiles1 = (int64_t)one.size();
-  s->n_tiles2 = (int64_t)two.size();
-  s->items = std::move(one);
-  s->items.insert(s->items.end(), two.begin(), two.end());
   s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
 
-  // 3) Device copy of the work list (one allocation, blocking upload).
-  const size_t items_bytes = s->items.size() * sizeof(RowtileItem);
+  // 3) Device copy of the plan (one allocation, blocking upload).
+  const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
+  const size_t chunks_bytes = s->chunks.size() * sizeof(ChunkRef);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
-  s->d_items_off = 0;
-  s->d_merges_off = kvq::align256(items_bytes);
-  s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
   const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
+  s->d_pieces_off = 0;
+  s->d_chunks_off = kvq::align256(pieces_bytes);
+  s->d_merges_off = s->d_chunks_off + kvq::align256(chunks_bytes);
+  s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
   const size_t total = s->d_counters_off + counters_bytes;
   if (total > 0 && have_device) {
     if (cudaMalloc(&s->d_buf, total) != cudaSuccess) {
@@ -271,16 +307,19 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
       delete s;
       return KVQ_E_NO_MEMORY;
     }
+    char* b = static_cast<char*>(s->d_buf);
     bool ok = true;
-    if (items_bytes)
-      ok &= cudaMemcpy(static_cast<char*>(s->d_buf) + s->d_items_off, s->items.data(),
-                       items_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+    if (pieces_bytes)
+      ok &= cudaMemcpy(b + s->d_pieces_off, s->pieces.data(), pieces_bytes,
+                       cudaMemcpyHostToDevice) == cudaSuccess;
+    if (chunks_bytes)
+      ok &= cudaMemcpy(b + s->d_chunks_off, s->chunks.data(), chunks_bytes,
+                       cudaMemcpyHostToDevice) == cudaSuccess;
     if (merges_bytes)
-      ok &= cudaMemcpy(static_cast<char*>(s->d_buf) + s->d_merges_off, s->merges.data(),
-                       merges_bytes, cudaMemcpyHostToDevice) == cudaSuccess;
+      ok &= cudaMemcpy(b + s->d_merges_off, s->merges.data(), merges_bytes,
+                       cudaMemcpyHostToDevice) == cudaSuccess;
     if (counters_bytes)
-      ok &= cudaMemset(static_cast<char*>(s->d_buf) + s->d_counters_off, 0, counters_bytes) ==
-            cudaSuccess;
+      ok &= cudaMemset(b + s->d_counters_off, 0, counters_bytes) == cudaSuccess;
     if (!ok) {
       kvq_sched_destroy(s);
       return KVQ_E_CUDA;
@@ -303,16 +342,16 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->row_bytes = kvq::row_bytes(s->dtype, s->head_dim);
   out->causal = s->causal;
   out->window = s->window;
-  out->num_rowtile_items = (int64_t)s->items.size();
-  out->num_split_items = s->n_split;
+  out->num_tiles = s->num_tiles;
+  out->num_pieces = (int64_t)s->pieces.size();
   out->num_merge_items = (int64_t)s->merges.size();
-  out->num_prefill_items = 0;
+  out->num_chunks = (int64_t)s->chunks.size();
+  out->num_decode_warps = (int64_t)s->launch[0].num_warps + s->launch[1].num_warps;
   out->max_splits = s->max_splits;
   out->total_query_tokens = s->total_q;
   out->workspace_bytes = s->workspace_bytes;
-  out->rowtile_smem_bytes = kvq::rowtile_smem_bytes(s->dtype, s->head_dim);
-  out->prefill_smem_bytes = 0;
-  out->num_kernel_launches = (s->n_tiles1 > 0) + (s->n_tiles2 > 0);
+  out->decode_smem_bytes = kvq::decode_smem_bytes(s->dtype, s->head_dim);
+  out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0);
   return KVQ_OK;
 }
 
@@ -329,7 +368,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
       (int)dtype != s->dtype || (causal ? 1 : 0) != s->causal ||
       (window > 0 ? window : 0) != s->window)
     return KVQ_E_SCHED_MISMATCH;
-  if (s->items.empty()) return KVQ_OK;
+  if (s->chunks.empty()) return KVQ_OK;
   if (!s->d_buf) return KVQ_E_CUDA;  // planned without a device
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
@@ -341,11 +380,11 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     return KVQ_E_INVALID_ARG;
   if (block_size <= 0 || block_size % kvq::kChunkTokens) return KVQ_E_UNSUPPORTED;
   if (num_blocks <= 0 || block_table_stride <= 0) return KVQ_E_INVALID_ARG;
+  // Cache slots are addressed with 32-bit indices.
+  if (num_blocks * (int64_t)block_size >= ((int64_t)1 << 31)) return KVQ_E_UNSUPPORTED;
   // The table must hold every logical block the schedule reads.
-  for (const RowtileItem& it : s->items) {
-    const int64_t last_block = ((int64_t)it.chunk_hi * kvq::kChunkTokens - 1) / block_size;
-    if (last_block >= block_table_stride) return KVQ_E_INVALID_ARG;
-  }
+  const int64_t last_block = ((int64_t)s->max_chunk * kvq::kChunkTokens) / block_size;
+  if (last_block >= block_table_stride) return KVQ_E_INVALID_ARG;
   if (!std::isfinite(sm_scale) || !std::isfinite(soft_cap)) return KVQ_E_INVALID_ARG;
   if (dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2) {
     if (!(std::isfinite(k_scale) && std::isfinite(v_scale))) return KVQ_E_INVALID_ARG;
@@ -368,9 +407,10 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
                    ? reinterpret_cast<float*>(static_cast<char*>(workspace) +
                                               kvq::workspace_o_bytes(s->partial_rows, head_dim))
                    : nullptr;
-  p.items = reinterpret_cast<const RowtileItem*>(static_cast<char*>(s->d_buf) + s->d_items_off);
-  p.merges = reinterpret_cast<const MergeItem*>(static_cast<char*>(s->d_buf) + s->d_merges_off);
-  p.merge_counters = reinterpret_cast<int32_t*>(static_cast<char*>(s->d_buf) + s->d_counters_off);
+  char* b = static_cast<char*>(s->d_buf);
+  p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off);
+  p.merges = reinterpret_cast<const MergeItem*>(b + s->d_merges_off);
+  p.merge_counters = reinterpret_cast<int32_t*>(b + s->d_counters_off);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;
   p.block_size = block_size;
@@ -384,12 +424,16 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.k_scale = k_scale;
   p.v_scale = v_scale;
 
-  int rc = KVQ_OK;
-  if (s->n_tiles1 > 0)
-    rc = kvq::launch_rowtile(p, s->dtype, head_dim, 1, 0, s->n_tiles1, stream);
-  if (rc == KVQ_OK && s->n_tiles2 > 0)
-    rc = kvq::launch_rowtile(p, s->dtype, head_dim, 2, s->n_tiles1, s->n_tiles2, stream);
-  return rc;
+  for (int cls = 0; cls < 2; ++cls) {
+    const DecodeLaunch& dl = s->launch[cls];
+    if (dl.num_chunks == 0) continue;
+    p.chunks = reinterpret_cast<const ChunkRef*>(b + s->d_chunks_off) + dl.chunk_off;
+    p.num_chunks = dl.num_chunks;
+    p.num_warps = dl.num_warps;
+    const int rc = kvq::launch_decode(p, s->dtype, head_dim, cls + 1, stream);
+    if (rc != KVQ_OK) return rc;
+  }
+  return KVQ_OK;
 }
 
 }  // extern "C"

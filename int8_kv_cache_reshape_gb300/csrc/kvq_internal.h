@@ -40,61 +40,56 @@ KVQ_HD constexpr bool attention_dtype_supported(int dtype) {
          dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD;
 }
 
-// ---- split-KV row-tile kernel ---------------------------------------------
-// A work item is up to 16 packed (query token, head) rows of one kv head,
-// over a range of 16-token KV chunks; a CTA of 4 warps shares the range.
+// ---- split-KV decode kernel (stream decomposition) -------------------------
+// A row tile is up to 16 packed (query token, head) rows of one kv head with
+// the range of 16-token KV chunks its rows can see.  The tiles' chunks are
+// laid end to end and the sequence is cut into equal contiguous segments,
+// one per warp; a tile cut by a segment boundary becomes several pieces whose
+// partial results are merged.  The 4 warps of a CTA are independent.
 constexpr int kChunkTokens = 16;
-constexpr int kRowtileWarps = 4;
-constexpr int kRowtileThreads = 32 * kRowtileWarps;
-constexpr int kRowtileMaxRows = 16;
+constexpr int kDecodeWarps = 4;
+constexpr int kDecodeThreads = 32 * kDecodeWarps;
+constexpr int kTileMaxRows = 16;
+constexpr int kRecordRing = 32;       // per-warp ring of chunk records (16 B each)
+constexpr int kMinChunksPerWarp = 8;  // smallest segment worth a warp
 
-// Bytes one warp stages per chunk: 16 K rows + 16 V rows of codes, plus
-// the scale tails of the K and V rows for per-token-head dtypes (one 16-byte
-// slot per lane).
-KVQ_HD constexpr int rowtile_chunk_bytes(int dtype, int head_dim) {
+// Bytes of one 16-token chunk of K and V codes (plus the per-token-head
+// scale tails) -- what a warp loads per step, straight into registers.
+KVQ_HD constexpr int decode_chunk_bytes(int dtype, int head_dim) {
   return 2 * kChunkTokens * head_dim * kv_elem_bytes(dtype) +
          (is_per_token_head(dtype) ? 32 * 16 : 0);
 }
-// Pipeline depth: enough chunks in flight per warp to cover HBM latency
-// (with 12-16 warps per SM, 2-3 chunks each), fewer when a chunk is large.
-KVQ_HD constexpr int rowtile_stages(int dtype, int head_dim) {
-  return rowtile_chunk_bytes(dtype, head_dim) >= 4096 ? 3 : 4;
-}
-// Resident CTAs per SM the kernel is compiled for (register budget):
-// 4 for the common decode tiles, fewer for wider tiles.
-KVQ_HD constexpr int rowtile_min_ctas(int dtype, int head_dim, int ntiles) {
+// Resident CTAs per SM the kernel is compiled for (register budget).
+KVQ_HD constexpr int decode_min_ctas(int dtype, int head_dim, int ntiles) {
   return head_dim >= 256 ? 2 : (ntiles == 1 ? 4 : 3);
 }
-KVQ_HD constexpr size_t rowtile_pipeline_smem(int dtype, int head_dim) {
-  return (size_t)kRowtileWarps * rowtile_stages(dtype, head_dim) *
-         rowtile_chunk_bytes(dtype, head_dim);
+// Shared memory: only each warp's ring of chunk records.
+KVQ_HD constexpr size_t decode_warp_smem(int dtype, int head_dim) {
+  return (size_t)kRecordRing * 16;
 }
-// Cross-warp combine at the end reuses the pipeline buffers: per warp,
-// 16 rows x head_dim fp32 partial outputs, plus (m, l) per row.
-KVQ_HD constexpr size_t rowtile_combine_smem(int head_dim) {
-  return (size_t)kRowtileWarps * kRowtileMaxRows * (head_dim + 2) * 4;
+KVQ_HD constexpr size_t decode_smem_bytes(int dtype, int head_dim) {
+  return (size_t)kDecodeWarps * decode_warp_smem(dtype, head_dim);
 }
-KVQ_HD constexpr size_t rowtile_smem_bytes(int dtype, int head_dim) {
-  return rowtile_pipeline_smem(dtype, head_dim) > rowtile_combine_smem(head_dim)
-             ? rowtile_pipeline_smem(dtype, head_dim)
-             : rowtile_combine_smem(head_dim);
-}
-// Smallest KV split worth a CTA (chunks): below this the merge costs more
-// than the parallelism gains.
-constexpr int kMinChunksPerSplit = 8;
 
-// One row-tile work item (32 bytes, read once per CTA).
-struct RowtileItem {
+// One piece of a row tile (32 bytes).
+struct DecodePiece {
   int32_t req;       // request index
   int32_t kv_head;   // kv head
   int32_t row0;      // first packed row: row = q_index * G + (head % G)
   int32_t nrows;     // rows in the tile, 1..16
-  int32_t chunk_lo;  // first 16-token KV chunk
-  int32_t chunk_hi;  // one past the last chunk
   int32_t part;      // -1: write `out`; else first partial row in workspace
   int32_t merge;     // merge item of a split tile (-1: not split)
+  int32_t any_lo;    // keys some row of the tile can see: [any_lo, any_hi)
+  int32_t any_hi;
 };
-static_assert(sizeof(RowtileItem) == 32, "RowtileItem layout");
+static_assert(sizeof(DecodePiece) == 32, "DecodePiece layout");
+
+// One entry of the flat chunk sequence: which piece, which 16-token chunk.
+struct ChunkRef {
+  int32_t piece;
+  int32_t chunk;
+};
+static_assert(sizeof(ChunkRef) == 8, "ChunkRef layout");
 
 // One merge item: the partial rows of a tile that was split along KV.
 struct MergeItem {
@@ -129,7 +124,10 @@ struct AttnParams {
   uint16_t* out;               // bf16 [sum Q, Hq, D]
   float* part_o;               // [P, D]
   float* part_lse;             // [P]
-  const RowtileItem* items;
+  const DecodePiece* pieces;
+  const ChunkRef* chunks;      // this launch's flat chunk sequence
+  int64_t num_chunks;          // its length
+  int num_warps;               // warps it is cut among (grid * kDecodeWarps)
   const MergeItem* merges;
   int32_t* merge_counters;     // one per merge item, zero between calls
   int64_t num_blocks;
@@ -151,6 +149,5 @@ int launch_reshape_and_cache(const void* key, const void* value,
                              int64_t num_blocks, int block_size,
                              const int64_t* slot_mapping, int dtype,
                              float k_scale, float v_scale, void* stream);
-int launch_rowtile(const AttnParams& p, int dtype, int head_dim, int ntiles,
-                   int64_t item_offset, int64_t num_items, void* stream);
+int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream);
 }  // namespace kvq

@@ -43,15 +43,15 @@ class SchedInfo(ctypes.Structure):
                 ("dtype", ctypes.c_int), ("kv_elem_bytes", ctypes.c_int),
                 ("row_bytes", ctypes.c_int), ("causal", ctypes.c_int),
                 ("window", ctypes.c_int),
-                ("num_rowtile_items", ctypes.c_int64),
-                ("num_split_items", ctypes.c_int64),
+                ("num_tiles", ctypes.c_int64),
+                ("num_pieces", ctypes.c_int64),
                 ("num_merge_items", ctypes.c_int64),
-                ("num_prefill_items", ctypes.c_int64),
+                ("num_chunks", ctypes.c_int64),
+                ("num_decode_warps", ctypes.c_int64),
                 ("max_splits", ctypes.c_int64),
                 ("total_query_tokens", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t),
-                ("rowtile_smem_bytes", ctypes.c_size_t),
-                ("prefill_smem_bytes", ctypes.c_size_t),
+                ("decode_smem_bytes", ctypes.c_size_t),
                 ("num_kernel_launches", ctypes.c_int64)]
 
     def as_dict(self):

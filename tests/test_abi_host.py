@@ -94,17 +94,25 @@ def _sched(seq_lens, query_lens, hq=32, hkv=8, D=128, dtype="fp8_e4m3", causal=T
 
 
 def test_scheduler_decode_plan_covers_every_chunk(monkeypatch):
-    monkeypatch.delenv("KVQ_NUM_SPLITS", raising=False)
+    """Stream decomposition: every (request, kv head) tile's 16-token chunks
+    are streamed exactly once, cut among the warps; each warp boundary cuts
+    at most one tile."""
+    monkeypatch.delenv("KVQ_DECODE_WARPS", raising=False)
     rng = np.random.default_rng(0)
     L = rng.integers(1024, 4097, 64)
     s = _sched(L, [1] * 64)
     info = s.info()
     assert info["kv_elem_bytes"] == 1 and info["row_bytes"] == 128
     assert info["total_query_tokens"] == 64
-    assert info["num_rowtile_items"] >= 64 * 8
-    assert info["num_merge_items"] <= 64 * 8
-    # partial rows: 4 rows (G = 4) per split item
-    assert info["workspace_bytes"] >= info["num_split_items"] * 4 * (128 + 1) * 4
+    assert info["num_tiles"] == 64 * 8
+    assert info["num_chunks"] == int(np.sum(-(-L // 16))) * 8
+    assert info["num_decode_warps"] == 152 * 4 * 4        # all SMs, 4 CTAs of 4 warps
+    assert info["num_pieces"] <= info["num_tiles"] + info["num_decode_warps"] - 1
+    assert info["num_merge_items"] <= info["num_tiles"]
+    assert info["num_kernel_launches"] == 1
+    # every cut tile keeps one partial row per (piece, row): 4 rows (G = 4)
+    split_pieces = info["num_pieces"] - (info["num_tiles"] - info["num_merge_items"])
+    assert info["workspace_bytes"] >= split_pieces * 4 * (128 + 1) * 4
     s.close()
 
 
@@ -116,19 +124,29 @@ def test_scheduler_sizes_follow_kv_element_size():
     b = _sched([300], [1], dtype="int8_per_token_head").info()
     assert a["row_bytes"] == 128 and b["row_bytes"] == 144
     assert a["kv_elem_bytes"] == b["kv_elem_bytes"] == 1
-    assert b["rowtile_smem_bytes"] > a["rowtile_smem_bytes"]
-    d = _sched([300], [1], D=256).info()
-    assert d["rowtile_smem_bytes"] <= 227 * 1024
+    assert b["decode_smem_bytes"] > a["decode_smem_bytes"]
+    for dt in ("fp8_e4m3", "int8_per_token_head"):
+        for D in (64, 128, 256):
+            assert _sched([300], [1], dtype=dt, D=D).info()["decode_smem_bytes"] <= 227 * 1024
 
 
-def test_forced_splits(monkeypatch):
-    monkeypatch.setenv("KVQ_NUM_SPLITS", "5")
+def test_forced_warp_counts(monkeypatch):
+    T = 8 * (63 + 3)                      # chunks of L = 1000 and L = 37, 8 kv heads
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "4")
     info = _sched([1000, 37], [1, 1]).info()
-    assert info["max_splits"] == 5
-    assert info["num_merge_items"] == 2 * 8
-    monkeypatch.setenv("KVQ_NUM_SPLITS", "1")
+    assert info["num_decode_warps"] == 4 and info["num_chunks"] == T
+    assert info["max_splits"] <= 2
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "100000")   # one chunk per warp
     info = _sched([1000, 37], [1, 1]).info()
-    assert info["num_merge_items"] == 0 and info["workspace_bytes"] == 0
+    assert info["num_decode_warps"] == T
+    assert info["max_splits"] == 63 and info["num_merge_items"] == 16
+    assert info["num_pieces"] == T
+
+
+def test_prefill_rows_make_wider_tiles():
+    info = _sched([100, 50], [40, 1], hq=32, hkv=8).info()   # 160 rows + 4 rows per kv head
+    assert info["num_tiles"] == 8 * (10 + 1)
+    assert info["num_kernel_launches"] == 2                   # 16-row and 8-row tiles
 
 
 @pytest.mark.parametrize("kw,want", [
@@ -149,9 +167,9 @@ def test_scheduler_rejects_more_queries_than_keys():
 
 def test_empty_batch_and_zero_query_requests():
     s = _sched([], [])
-    assert s.info()["num_rowtile_items"] == 0 and s.workspace_bytes == 0
+    assert s.info()["num_tiles"] == 0 and s.workspace_bytes == 0
     s = _sched([40, 0], [0, 0])
-    assert s.info()["num_rowtile_items"] == 0
+    assert s.info()["num_tiles"] == 0 and s.info()["num_kernel_launches"] == 0
 
 
 def test_attention_refuses_mismatched_schedule():

@@ -18,12 +18,12 @@ from _harness import (GpuRun, assert_attention_close, oracle_attention, oracle_c
 pytestmark = pytest.mark.gpu
 
 
-def _check(wl, splits=None, monkeypatch=None, tokens=None):
+def _check(wl, warps=None, monkeypatch=None, tokens=None):
     if monkeypatch is not None:
-        if splits is None:
-            monkeypatch.delenv("KVQ_NUM_SPLITS", raising=False)
+        if warps is None:
+            monkeypatch.delenv("KVQ_DECODE_WARPS", raising=False)
         else:
-            monkeypatch.setenv("KVQ_NUM_SPLITS", str(splits))
+            monkeypatch.setenv("KVQ_DECODE_WARPS", str(warps))
     g = GpuRun(wl).write_cache().attention()
     kc, vc = oracle_cache(wl)
     ref = oracle_attention(wl, kc, vc, tokens=tokens)
@@ -68,12 +68,22 @@ def test_non_causal(cuda_device):
     _check(wl)
 
 
-@pytest.mark.parametrize("splits", [1, 2, 3, 7, 64])
-def test_forced_kv_splits(cuda_device, monkeypatch, splits):
-    wl = W.custom("splits", [1, 1, 2], [1000, 129, 300], 32, 8, 128, 16, "int8_per_token_head",
-                  302, token_scale_range=(0.1, 10.0), window=200 if splits == 7 else 0)
-    e, g = _check(wl, splits=splits, monkeypatch=monkeypatch)
-    assert g.sched_info["max_splits"] == min(splits, 63)   # 63 chunks in the longest tile
+@pytest.mark.parametrize("warps", [4, 12, 40, 400, 100000])
+def test_forced_warp_counts(cuda_device, monkeypatch, warps):
+    """Few warps: each streams many pieces of many tiles; many warps: tiles
+    are cut into many pieces and merged (one chunk per warp at the end)."""
+    wl = W.custom("splits", [1, 1, 2, 1], [1000, 129, 300, 16], 32, 8, 128, 16,
+                  "int8_per_token_head", 302, token_scale_range=(0.1, 10.0),
+                  window=200 if warps == 40 else 0)
+    e, g = _check(wl, warps=warps, monkeypatch=monkeypatch)
+    assert g.sched_info["num_decode_warps"] <= max(warps, 4)
+
+
+@pytest.mark.parametrize("warps", [4, 100000])
+def test_forced_warp_counts_prefill_rows(cuda_device, monkeypatch, warps):
+    wl = W.custom("rows-split", [37, 1, 9], [300, 600, 9], 16, 2, 128, 16, "fp8_e4m3", 309,
+                  window=100)
+    _check(wl, warps=warps, monkeypatch=monkeypatch)
 
 
 def test_block_permutation_is_bit_identical(cuda_device):

@@ -35,7 +35,7 @@ def _run_static(g, sched):
 
 @pytest.mark.parametrize("dtype", ["fp8_e4m3", "int8_per_token_head"])
 def test_static_scratch_matches_workspace_entry_point(cuda_device, monkeypatch, dtype):
-    monkeypatch.setenv("KVQ_NUM_SPLITS", "5")     # make sure the scratch is used
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "64")  # tiles cut among warps: scratch is used
     wl = W.custom("noalloc", [1, 1, 2, 1], [900, 333, 640, 1500], 32, 8, 128, 16, dtype, 77,
                   token_scale_range=(0.1, 10.0) if "per_token" in dtype else None)
     g = GpuRun(wl).write_cache().attention()         # workspace entry point
@@ -56,7 +56,7 @@ def test_static_scratch_matches_workspace_entry_point(cuda_device, monkeypatch, 
 
 
 def test_static_scratch_refuses_oversized_schedule(cuda_device, monkeypatch):
-    monkeypatch.setenv("KVQ_NUM_SPLITS", "64")
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "100000")   # one chunk per warp: huge scratch
     k = kvq()
     L = np.full(64, 2048, np.int32)
     qsl = np.arange(65, dtype=np.int32)
