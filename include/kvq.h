@@ -249,6 +249,7 @@ typedef struct {
   int64_t total_query_tokens;
   size_t workspace_bytes;
   size_t decode_smem_bytes;    /* dynamic shared memory per decode CTA        */
+  size_t decode_chunk_bytes;   /* K+V bytes a warp streams per 16-token chunk */
   int64_t num_kernel_launches; /* kernels one attention call launches         */
 } kvq_sched_info_t;
 

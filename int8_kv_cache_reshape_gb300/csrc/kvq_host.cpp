@@ -351,6 +351,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->total_query_tokens = s->total_q;
   out->workspace_bytes = s->workspace_bytes;
   out->decode_smem_bytes = kvq::decode_smem_bytes(s->dtype, s->head_dim);
+  out->decode_chunk_bytes = (size_t)kvq::decode_chunk_bytes(s->dtype, s->head_dim);
   out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0);
   return KVQ_OK;
 }

@@ -52,6 +52,7 @@ class SchedInfo(ctypes.Structure):
                 ("total_query_tokens", ctypes.c_int64),
                 ("workspace_bytes", ctypes.c_size_t),
                 ("decode_smem_bytes", ctypes.c_size_t),
+                ("decode_chunk_bytes", ctypes.c_size_t),
                 ("num_kernel_launches", ctypes.c_int64)]
 
     def as_dict(self):

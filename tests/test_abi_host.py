@@ -124,7 +124,9 @@ def test_scheduler_sizes_follow_kv_element_size():
     b = _sched([300], [1], dtype="int8_per_token_head").info()
     assert a["row_bytes"] == 128 and b["row_bytes"] == 144
     assert a["kv_elem_bytes"] == b["kv_elem_bytes"] == 1
-    assert b["decode_smem_bytes"] > a["decode_smem_bytes"]
+    # bytes streamed per 16-token chunk: 2 * 16 * (D codes) [+ scale tails]
+    assert a["decode_chunk_bytes"] == 2 * 16 * 128
+    assert b["decode_chunk_bytes"] == 2 * 16 * 128 + 32 * 16
     for dt in ("fp8_e4m3", "int8_per_token_head"):
         for D in (64, 128, 256):
             assert _sched([300], [1], dtype=dt, D=D).info()["decode_smem_bytes"] <= 227 * 1024
