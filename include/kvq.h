@@ -54,6 +54,7 @@ extern "C" {
 #define KVQ_E_WORKSPACE_TOO_SMALL (-4)
 #define KVQ_E_CUDA (-5)             /* a CUDA runtime call or launch failed        */
 #define KVQ_E_NO_MEMORY (-6)        /* host or device allocation failed            */
+#define KVQ_E_TIMEOUT (-7)          /* a kernel gave up a bounded wait (see below) */
 
 /* ---- KV cache data types -------------------------------------------------
  * 0..2 keep the kv_cache_dtype indices printed in [P2]'s source snippet
@@ -142,10 +143,11 @@ KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
  *   workspace_bytes         receives the scratch size the attention call
  *                           needs (may be 0); must not be NULL.
  * The schedule holds a host copy and one device copy of its plan, made on
- * the current device (a blocking upload).  The rows of each (request, kv
- * head) form tiles of up to 16 (query, head) rows; the tiles' 16-token KV
+ * the current device (a blocking upload).  Requests with at most 16
+ * (query, head) rows per kv head (decodes) form row tiles whose 16-token KV
  * chunks are cut into equal contiguous segments, one per warp, so long
- * contexts are split along the KV axis and merged. */
+ * contexts are split along the KV axis and merged.  Requests with more rows
+ * (prefills) form 128-row tiles for the tensor-core prefill kernel. */
 KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
                                int head_dim, const int32_t* seq_lens_host,
                                const int32_t* query_start_loc_host, int causal,
@@ -250,10 +252,19 @@ typedef struct {
   size_t workspace_bytes;
   size_t decode_smem_bytes;    /* dynamic shared memory per decode CTA        */
   size_t decode_chunk_bytes;   /* K+V bytes a warp streams per 16-token chunk */
+  int64_t num_prefill_tiles;   /* 128-row tiles of the tensor-core prefill    */
+  size_t prefill_smem_bytes;   /* dynamic shared memory per prefill CTA       */
   int64_t num_kernel_launches; /* kernels one attention call launches         */
 } kvq_sched_info_t;
 
 KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
+
+/* Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
+ * kernel run with this schedule gave up waiting for the tensor core (a
+ * bounded wait of about a second; the kernel then released its tensor
+ * memory and returned without writing its tile), else KVQ_OK.  Blocks until
+ * the device is idle. */
+KVQ_API int kvq_sched_check_device(const kvq_sched_t* sched);
 
 /* Short English description of a status code (static storage). */
 KVQ_API const char* kvq_status_string(int status);

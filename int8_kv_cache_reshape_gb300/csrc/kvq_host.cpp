@@ -21,6 +21,7 @@
 using kvq::ChunkRef;
 using kvq::DecodePiece;
 using kvq::MergeItem;
+using kvq::PrefillTile;
 
 // One launch of the split-KV decode kernel: the tiles with one 8-row n-tile
 // (class 0) or two (class 1).
@@ -37,12 +38,13 @@ struct kvq_sched {
   std::vector<DecodePiece> pieces;
   std::vector<ChunkRef> chunks;
   std::vector<MergeItem> merges;
+  std::vector<PrefillTile> prefill;
   DecodeLaunch launch[2];
   int64_t num_tiles, max_splits, partial_rows;
   int32_t max_chunk;  // highest 16-token chunk index any tile reads
   size_t workspace_bytes;
-  void* d_buf;  // device copy: pieces, chunks, merges, merge counters
-  size_t d_pieces_off, d_chunks_off, d_merges_off, d_counters_off;
+  void* d_buf;  // device copy: pieces, chunks, merges, merge counters, prefill tiles, error word
+  size_t d_pieces_off, d_chunks_off, d_merges_off, d_counters_off, d_prefill_off, d_error_off;
 };
 
 namespace {
@@ -81,6 +83,7 @@ const char* kvq_status_string(int status) {
     case KVQ_E_WORKSPACE_TOO_SMALL: return "workspace smaller than the schedule requires";
     case KVQ_E_CUDA: return "CUDA runtime error";
     case KVQ_E_NO_MEMORY: return "allocation failed";
+    case KVQ_E_TIMEOUT: return "a kernel's bounded wait for the tensor core timed out";
     default: return "unknown status";
   }
 }
@@ -196,6 +199,27 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     const int64_t Q = (int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r];
     if (Q == 0) continue;
     const int64_t rows = Q * G;
+    if (rows > kvq::kTileMaxRows) {
+      // Prefill: 128-row tiles on the tensor cores.
+      for (int h = 0; h < heads_kv; ++h) {
+        for (int64_t row0 = 0; row0 < rows; row0 += kvq::kPrefillRows) {
+          const int64_t nrows = std::min<int64_t>(kvq::kPrefillRows, rows - row0);
+          const int64_t p_min = L - Q + row0 / G;
+          const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
+          PrefillTile pt;
+          pt.req = r;
+          pt.kv_head = h;
+          pt.row0 = (int32_t)row0;
+          pt.nrows = (int32_t)nrows;
+          pt.kv_hi = (int32_t)(s->causal ? p_max + 1 : L);
+          pt.kv_lo = (int32_t)(s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0);
+          pt.pad0 = pt.pad1 = 0;
+          s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)((pt.kv_hi - 1) / kvq::kChunkTokens));
+          s->prefill.push_back(pt);
+        }
+      }
+      continue;
+    }
     for (int h = 0; h < heads_kv; ++h) {
       for (int64_t row0 = 0; row0 < rows; row0 += kvq::kTileMaxRows) {
         const int64_t nrows = std::min<int64_t>(kvq::kTileMaxRows, rows - row0);
@@ -216,6 +240,11 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     }
   }
   s->num_tiles = (int64_t)(tiles[0].size() + tiles[1].size());
+  // Longest prefill tiles first, so the tail of the grid is short tiles.
+  std::stable_sort(s->prefill.begin(), s->prefill.end(),
+                   [](const PrefillTile& a, const PrefillTile& b) {
+                     return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
+                   });
 
   // 2) Stream decomposition: per class, lay the tiles' chunks end to end and
   //    cut the sequence into equal contiguous segments, one per warp.  A
@@ -296,12 +325,15 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   const size_t chunks_bytes = s->chunks.size() * sizeof(ChunkRef);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
   const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
+  const size_t prefill_bytes = s->prefill.size() * sizeof(PrefillTile);
   s->d_pieces_off = 0;
   s->d_chunks_off = kvq::align256(pieces_bytes);
   s->d_merges_off = s->d_chunks_off + kvq::align256(chunks_bytes);
   s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
-  const size_t total = s->d_counters_off + counters_bytes;
-  if (total > 0 && have_device) {
+  s->d_prefill_off = s->d_counters_off + kvq::align256(counters_bytes);
+  s->d_error_off = s->d_prefill_off + kvq::align256(prefill_bytes);
+  const size_t total = s->d_error_off + sizeof(int32_t);
+  if (have_device) {
     if (cudaMalloc(&s->d_buf, total) != cudaSuccess) {
       cudaGetLastError();
       delete s;
@@ -318,8 +350,13 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     if (merges_bytes)
       ok &= cudaMemcpy(b + s->d_merges_off, s->merges.data(), merges_bytes,
                        cudaMemcpyHostToDevice) == cudaSuccess;
+    if (prefill_bytes)
+      ok &= cudaMemcpy(b + s->d_prefill_off, s->prefill.data(), prefill_bytes,
+                       cudaMemcpyHostToDevice) == cudaSuccess;
+    // Merge counters and the error word start at zero.
     if (counters_bytes)
       ok &= cudaMemset(b + s->d_counters_off, 0, counters_bytes) == cudaSuccess;
+    ok &= cudaMemset(b + s->d_error_off, 0, sizeof(int32_t)) == cudaSuccess;
     if (!ok) {
       kvq_sched_destroy(s);
       return KVQ_E_CUDA;
@@ -352,8 +389,29 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->workspace_bytes = s->workspace_bytes;
   out->decode_smem_bytes = kvq::decode_smem_bytes(s->dtype, s->head_dim);
   out->decode_chunk_bytes = (size_t)kvq::decode_chunk_bytes(s->dtype, s->head_dim);
-  out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0);
+  out->num_prefill_tiles = (int64_t)s->prefill.size();
+  out->prefill_smem_bytes = kvq::prefill_smem_bytes(s->head_dim);
+  out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0) +
+                             (!s->prefill.empty());
   return KVQ_OK;
+}
+
+int kvq_sched_check_device(const kvq_sched_t* s) {
+  if (!s) return KVQ_E_INVALID_ARG;
+  if (!s->d_buf) return KVQ_OK;
+  int cur = -1;
+  if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
+  if (cur != s->device && cudaSetDevice(s->device) != cudaSuccess) return KVQ_E_CUDA;
+  int32_t flag = 0;
+  char* err = static_cast<char*>(s->d_buf) + s->d_error_off;
+  int rc = KVQ_OK;
+  if (cudaMemcpy(&flag, err, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess) rc = KVQ_E_CUDA;
+  else if (flag != 0) {
+    rc = KVQ_E_TIMEOUT;
+    cudaMemset(err, 0, sizeof(flag));
+  }
+  if (cur != s->device) cudaSetDevice(cur);
+  return rc;
 }
 
 int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv, int head_dim,
@@ -369,7 +427,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
       (int)dtype != s->dtype || (causal ? 1 : 0) != s->causal ||
       (window > 0 ? window : 0) != s->window)
     return KVQ_E_SCHED_MISMATCH;
-  if (s->chunks.empty()) return KVQ_OK;
+  if (s->chunks.empty() && s->prefill.empty()) return KVQ_OK;
   if (!s->d_buf) return KVQ_E_CUDA;  // planned without a device
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
@@ -412,6 +470,8 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off);
   p.merges = reinterpret_cast<const MergeItem*>(b + s->d_merges_off);
   p.merge_counters = reinterpret_cast<int32_t*>(b + s->d_counters_off);
+  p.prefill_tiles = reinterpret_cast<const PrefillTile*>(b + s->d_prefill_off);
+  p.error_flag = reinterpret_cast<int32_t*>(b + s->d_error_off);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;
   p.block_size = block_size;
@@ -425,6 +485,10 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.k_scale = k_scale;
   p.v_scale = v_scale;
 
+  if (!s->prefill.empty()) {
+    const int rc = kvq::launch_prefill(p, s->dtype, head_dim, (int64_t)s->prefill.size(), stream);
+    if (rc != KVQ_OK) return rc;
+  }
   for (int cls = 0; cls < 2; ++cls) {
     const DecodeLaunch& dl = s->launch[cls];
     if (dl.num_chunks == 0) continue;

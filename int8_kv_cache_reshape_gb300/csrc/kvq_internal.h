@@ -71,6 +71,30 @@ KVQ_HD constexpr size_t decode_smem_bytes(int dtype, int head_dim) {
   return (size_t)kDecodeWarps * decode_warp_smem(dtype, head_dim);
 }
 
+// ---- tensor-core prefill kernel -----------------------------------------
+// A prefill tile is 128 packed (query token, head) rows of one kv head; its
+// keys stream through in tiles of 64.  Requests whose rows per kv head
+// exceed kTileMaxRows go to this kernel.
+constexpr int kPrefillRows = 128;
+constexpr int kPrefillKeys = 64;
+// Tensor-memory columns: O (head_dim fp32) + S (64 fp32), a power of two.
+KVQ_HD constexpr int prefill_tmem_cols(int head_dim) {
+  return head_dim + kPrefillKeys <= 128 ? 128 : (head_dim + kPrefillKeys <= 256 ? 256 : 512);
+}
+// Shared memory: Q (128 x D bf16), K (64 x D), V^T (D x 64), P (128 x 64),
+// key / value scales, key-valid flags, barriers; +1 KB for 1024 alignment.
+KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
+  return (size_t)kPrefillRows * head_dim * 2 + 2 * (size_t)kPrefillKeys * head_dim * 2 +
+         (size_t)kPrefillRows * kPrefillKeys * 2 + kPrefillKeys * (4 + 4 + 1) + 32 + 1024;
+}
+
+struct PrefillTile {
+  int32_t req, kv_head, row0, nrows;
+  int32_t kv_lo, kv_hi;  // keys some row of the tile can see
+  int32_t pad0, pad1;
+};
+static_assert(sizeof(PrefillTile) == 32, "PrefillTile layout");
+
 // One piece of a row tile (32 bytes).
 struct DecodePiece {
   int32_t req;       // request index
@@ -130,6 +154,8 @@ struct AttnParams {
   int num_warps;               // warps it is cut among (grid * kDecodeWarps)
   const MergeItem* merges;
   int32_t* merge_counters;     // one per merge item, zero between calls
+  const PrefillTile* prefill_tiles;
+  int32_t* error_flag;         // set by a kernel whose bounded wait timed out
   int64_t num_blocks;
   int block_table_stride;
   int block_size;
@@ -150,4 +176,5 @@ int launch_reshape_and_cache(const void* key, const void* value,
                              const int64_t* slot_mapping, int dtype,
                              float k_scale, float v_scale, void* stream);
 int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream);
+int launch_prefill(const AttnParams& p, int dtype, int head_dim, int64_t num_tiles, void* stream);
 }  // namespace kvq

@@ -1,0 +1,8 @@
+// kvq_prefill_d256.cu -- tensor-core prefill kernels for head_dim 256.
+#include "kvq_prefill.cuh"
+
+namespace kvq {
+int launch_prefill_d256(const AttnParams& p, int dtype, int64_t num_tiles, void* stream) {
+  return launch_prefill_d<256>(p, dtype, num_tiles, static_cast<cudaStream_t>(stream));
+}
+}  // namespace kvq

@@ -18,7 +18,7 @@ HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 
 OK = 0
 E_INVALID_ARG, E_UNSUPPORTED, E_SCHED_MISMATCH = -1, -2, -3
-E_WORKSPACE_TOO_SMALL, E_CUDA, E_NO_MEMORY = -4, -5, -6
+E_WORKSPACE_TOO_SMALL, E_CUDA, E_NO_MEMORY, E_TIMEOUT = -4, -5, -6, -7
 
 DTYPES = {"auto": 0, "fp8_e4m3": 1, "fp8_e5m2": 2, "int8_per_token_head": 3,
           "fp8_per_token_head": 4}
@@ -53,6 +53,8 @@ class SchedInfo(ctypes.Structure):
                 ("workspace_bytes", ctypes.c_size_t),
                 ("decode_smem_bytes", ctypes.c_size_t),
                 ("decode_chunk_bytes", ctypes.c_size_t),
+                ("num_prefill_tiles", ctypes.c_int64),
+                ("prefill_smem_bytes", ctypes.c_size_t),
                 ("num_kernel_launches", ctypes.c_int64)]
 
     def as_dict(self):
@@ -88,6 +90,8 @@ lib.kvq_attention_with_kv_cache_static_scratch.argtypes = [
 STATIC_SCRATCH_BYTES = 16 << 20
 lib.kvq_sched_destroy.restype = None
 lib.kvq_sched_destroy.argtypes = [_p]
+lib.kvq_sched_check_device.restype = _c.c_int
+lib.kvq_sched_check_device.argtypes = [_p]
 lib.kvq_sched_get_info.restype = _c.c_int
 lib.kvq_sched_get_info.argtypes = [_p, _c.POINTER(SchedInfo)]
 
@@ -157,6 +161,11 @@ class Sched:
         inf = SchedInfo()
         _check(lib.kvq_sched_get_info(self.handle, _c.byref(inf)), "kvq_sched_get_info")
         return inf.as_dict()
+
+    def check_device(self) -> None:
+        """Raise KvqError(E_TIMEOUT) if a kernel run with this schedule gave
+        up a bounded wait; synchronizes the device."""
+        _check(lib.kvq_sched_check_device(self.handle), "kvq_sched_check_device")
 
     def close(self):
         if self.handle is not None:

@@ -81,6 +81,8 @@ def _load():
             c.c_int, c.c_int, c.c_int, c.c_int, p, p, p, c.c_int, c.c_int, p,
             p, p, c.c_int, c.c_double, c.c_int, c.c_int, c.c_double,
             c.c_float, c.c_float, p, c.c_int64, p]
+        lib.kvo_attention_fp32_bound.restype = c.c_int
+        lib.kvo_attention_fp32_bound.argtypes = lib.kvo_attention.argtypes
         lib.kvo_attention_probs.restype = c.c_int64
         lib.kvo_attention_probs.argtypes = [
             c.c_int, c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, p, p,
@@ -157,6 +159,27 @@ def attention(q_bits: np.ndarray, key_cache: np.ndarray,
               v_scale: float, tokens=None) -> np.ndarray:
     """float32 [n, Hq, D] attention output for the listed query tokens
     (all tokens when ``tokens`` is None)."""
+    return _attention_call("kvo_attention", q_bits, key_cache, value_cache, query_start_loc,
+                           seq_lens, block_table, heads_kv, block_size, dtype, sm_scale, causal,
+                           window, soft_cap, k_scale, v_scale, tokens)
+
+
+def attention_fp32_bound(q_bits: np.ndarray, key_cache: np.ndarray,
+                         value_cache: np.ndarray, query_start_loc, seq_lens, block_table,
+                         heads_kv: int, block_size: int, dtype: int, sm_scale: float,
+                         causal: bool, window: int, soft_cap: float, k_scale: float,
+                         v_scale: float, tokens=None) -> np.ndarray:
+    """float32 [n, Hq, D]: first-order bound on how far a binary32
+    evaluation (binary32 scores and sums, 11-bit softmax weights) of the
+    attention may land from the exact result (kvo_attention_fp32_bound)."""
+    return _attention_call("kvo_attention_fp32_bound", q_bits, key_cache, value_cache,
+                           query_start_loc, seq_lens, block_table, heads_kv, block_size, dtype,
+                           sm_scale, causal, window, soft_cap, k_scale, v_scale, tokens)
+
+
+def _attention_call(fn, q_bits, key_cache, value_cache, query_start_loc, seq_lens, block_table,
+                    heads_kv, block_size, dtype, sm_scale, causal, window, soft_cap, k_scale,
+                    v_scale, tokens):
     q_bits = _c(q_bits, np.uint16)
     qsl = _c(query_start_loc, np.int32)
     sl = _c(seq_lens, np.int32)
@@ -167,14 +190,14 @@ def attention(q_bits: np.ndarray, key_cache: np.ndarray,
     tok = None if tokens is None else _c(tokens, np.int64)
     n = int(qsl[-1]) if tok is None else tok.size
     out = np.zeros((n, Hq, D), dtype=np.float32)
-    rc = _load().kvo_attention(
+    rc = getattr(_load(), fn)(
         len(sl), Hq, heads_kv, D, _ptr(q_bits), _ptr(key_cache),
         _ptr(value_cache), block_size, dtype, _ptr(qsl), _ptr(sl), _ptr(bt),
         bt.shape[1], float(sm_scale), int(bool(causal)), int(window),
         float(soft_cap), float(k_scale), float(v_scale), _ptr(tok),
         0 if tok is None else tok.size, _ptr(out))
     if rc != 0:
-        raise ValueError("oracle attention rejected its arguments")
+        raise ValueError(f"oracle {fn} rejected its arguments")
     return out
 
 

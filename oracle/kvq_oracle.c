@@ -481,6 +481,124 @@ int64_t kvo_attention_probs(int num_req, int heads_q, int heads_kv,
   return row_probs(&a, token, head_q, probs, max_seq_len(&a));
 }
 
+/* ------------------------------------------------------------------ */
+/* Forward error bound of a binary32 evaluation (test tolerance)       */
+/* ------------------------------------------------------------------ */
+
+/* First-order bound on |o_fp32 - o| for one output element when the
+ * attention above is evaluated the way a GPU kernel does it: scores
+ * s_j = sm_scale * (q . k_j) accumulated in binary32 (any order, up to
+ * 2^-23 relative error per operation, so truncating accumulators are
+ * covered), softmax weights rounded to a format with an 11-bit significand
+ * (binary16: relative error <= 2^-11), and the weighted sums of values and
+ * weights accumulated in binary32.
+ *
+ *   s_j -> s_j + e_j,  |e_j| <= gamma_{D+4} * A_j  (+ 2^-20 * cap with a soft
+ *   cap: tanh evaluated to a few ulp; the cap's derivative is <= 1), where
+ *   A_j = sm_scale * sum_d |q_d| |k_jd| and gamma_n = n 2^-23 / (1 - n 2^-23);
+ *   a score perturbation moves the output by sum_j w_j (v_j - o) e_j to
+ *   first order (softmax derivative), and the weight / sum rounding by at
+ *   most (2^-11 + gamma_{2n+8}) sum_j w_j |v_j| over the n visible keys,
+ *   plus 2^-25 sum_j |v_j| / sum_j p_j for weights that fall below the
+ *   binary16 normal range (absolute error 2^-25 with the largest unnormalised
+ *   weight p at 1).
+ *
+ * The bound is the sum of those two terms; it is zero only where nothing
+ * is visible.  Used by the tests to widen the stated tolerance by what
+ * binary32 arithmetic itself cannot avoid on inputs with outliers. */
+static double gamma_n(double n) {
+  const double u = 1.0 / 8388608.0; /* 2^-23 */
+  return n * u / (1.0 - n * u);
+}
+
+static int row_bound(const attn_args* a, int64_t tok, int hq, float* out,
+                     double* probs, double* err, int64_t cap) {
+  int64_t L = row_probs(a, tok, hq, probs, cap);
+  int r = request_of(a, tok);
+  int D = a->head_dim, G = a->heads_q / a->heads_kv, hk = hq / G;
+  const uint16_t* qrow = a->q + (tok * a->heads_q + hq) * (int64_t)D;
+  int64_t n = 0;
+  if (L < 0) return -1;
+  for (int64_t j = 0; j < L; ++j) {
+    const uint8_t* krow;
+    double A = 0.0;
+    err[j] = 0.0;
+    if (probs[j] == 0.0) continue;
+    ++n;
+    krow = cache_row(a, a->key_cache, r, j, hk);
+    for (int d = 0; d < D; ++d)
+      A += fabs(kvo_bf16_to_double(qrow[d]) * dequant(a->dtype, krow, d, D, a->k_scale));
+    err[j] = gamma_n(D + 4) * A * fabs(a->sm_scale);
+    if (a->soft_cap > 0.0) err[j] += a->soft_cap / 1048576.0; /* 2^-20 cap */
+  }
+  /* sum_j p_j with the largest p at 1: the softmax normaliser of the
+   * unnormalised weights a kernel rounds */
+  double lsum = 0.0, pmax = 0.0;
+  for (int64_t j = 0; j < L; ++j)
+    if (probs[j] > pmax) pmax = probs[j];
+  for (int64_t j = 0; j < L; ++j) lsum += probs[j] / (pmax > 0.0 ? pmax : 1.0);
+  for (int d = 0; d < D; ++d) {
+    double o = 0.0, e_score = 0.0, wv = 0.0, v_abs = 0.0;
+    for (int64_t j = 0; j < L; ++j) {
+      if (probs[j] == 0.0) continue;
+      o += probs[j] * dequant(a->dtype, cache_row(a, a->value_cache, r, j, hk), d, D, a->v_scale);
+    }
+    for (int64_t j = 0; j < L; ++j) {
+      double v;
+      if (probs[j] == 0.0) continue;
+      v = dequant(a->dtype, cache_row(a, a->value_cache, r, j, hk), d, D, a->v_scale);
+      e_score += probs[j] * fabs(v - o) * err[j];
+      wv += probs[j] * fabs(v);
+      v_abs += fabs(v);
+    }
+    out[d] = (float)(e_score + (1.0 / 2048.0 + gamma_n(2.0 * (double)n + 8.0)) * wv +
+                     v_abs / 33554432.0 / (lsum > 0.0 ? lsum : 1.0));
+  }
+  return 0;
+}
+
+/* The bound above for the listed query tokens, all q heads (layout and
+ * arguments as kvo_attention). */
+int kvo_attention_fp32_bound(int num_req, int heads_q, int heads_kv, int head_dim,
+                             const uint16_t* q, const uint8_t* key_cache,
+                             const uint8_t* value_cache, int block_size, int dtype,
+                             const int32_t* query_start_loc, const int32_t* seq_lens,
+                             const int32_t* block_table, int block_table_stride,
+                             double sm_scale, int causal, int window, double soft_cap,
+                             float k_scale, float v_scale, const int64_t* tokens,
+                             int64_t n_tokens, float* out) {
+  attn_args a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache,
+                          value_cache, block_size, dtype, query_start_loc,
+                          seq_lens, block_table, block_table_stride, sm_scale,
+                          causal, window, soft_cap, k_scale, v_scale);
+  int64_t cap = max_seq_len(&a);
+  int64_t n = tokens ? n_tokens : query_start_loc[num_req];
+  int64_t work = n * heads_q;
+  int failed = 0;
+  if (heads_kv <= 0 || heads_q % heads_kv != 0 || kvo_row_bytes(dtype, head_dim) < 0)
+    return -1;
+#pragma omp parallel
+  {
+    double* probs = (double*)malloc(sizeof(double) * (size_t)cap);
+    double* err = (double*)malloc(sizeof(double) * (size_t)cap);
+#pragma omp for schedule(dynamic, 1)
+    for (int64_t w = 0; w < work; ++w) {
+      int64_t i = w / heads_q;
+      int hq = (int)(w % heads_q);
+      int64_t tok = tokens ? tokens[i] : i;
+      if (!probs || !err ||
+          row_bound(&a, tok, hq, out + (i * heads_q + hq) * (int64_t)head_dim, probs, err,
+                    cap) != 0) {
+#pragma omp atomic write
+        failed = 1;
+      }
+    }
+    free(probs);
+    free(err);
+  }
+  return failed ? -1 : 0;
+}
+
 /* Threads the OpenMP loops use (reported with CPU timings). */
 int kvo_num_threads(void) {
 #ifdef _OPENMP

@@ -56,7 +56,7 @@ def test_row_bytes():
 
 
 def test_status_strings():
-    for s in (0, -1, -2, -3, -4, -5, -6):
+    for s in (0, -1, -2, -3, -4, -5, -6, -7):
         assert kvq.status_string(s) and kvq.status_string(s) != "unknown status"
     assert kvq.status_string(-99) == "unknown status"
 
@@ -145,10 +145,23 @@ def test_forced_warp_counts(monkeypatch):
     assert info["num_pieces"] == T
 
 
-def test_prefill_rows_make_wider_tiles():
+def test_prefill_rows_make_tensor_core_tiles():
     info = _sched([100, 50], [40, 1], hq=32, hkv=8).info()   # 160 rows + 4 rows per kv head
-    assert info["num_tiles"] == 8 * (10 + 1)
-    assert info["num_kernel_launches"] == 2                   # 16-row and 8-row tiles
+    assert info["num_prefill_tiles"] == 8 * 2                 # 128 + 32 rows per kv head
+    assert info["num_tiles"] == 8                             # the decode's 4-row tiles
+    assert info["num_kernel_launches"] == 2                   # prefill + one decode class
+    assert info["prefill_smem_bytes"] > 0
+
+
+def test_prefill_tiles_and_decode_boundary():
+    # 16 rows per kv head stays a decode tile; 17 rows become a prefill tile.
+    info = _sched([64, 64], [8, 9], hq=16, hkv=8).info()      # G=2: 16 and 18 rows
+    assert info["num_prefill_tiles"] == 8
+    assert info["num_tiles"] == 8
+    assert info["num_kernel_launches"] == 2
+    info = _sched([64], [64], hq=8, hkv=8).info()             # only prefill
+    assert info["num_prefill_tiles"] == 8 and info["num_tiles"] == 0
+    assert info["num_kernel_launches"] == 1 and info["workspace_bytes"] == 0
 
 
 @pytest.mark.parametrize("kw,want", [

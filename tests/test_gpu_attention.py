@@ -12,7 +12,7 @@ import torch
 
 from int8_kv_cache_reshape_gb300 import workloads as W
 
-from _harness import (GpuRun, assert_attention_close, oracle_attention, oracle_cache,
+from _harness import (GpuRun, assert_attention_close, oracle_cache, oracle_reference,
                       visible_window_mask)
 
 pytestmark = pytest.mark.gpu
@@ -26,8 +26,8 @@ def _check(wl, warps=None, monkeypatch=None, tokens=None):
             monkeypatch.setenv("KVQ_DECODE_WARPS", str(warps))
     g = GpuRun(wl).write_cache().attention()
     kc, vc = oracle_cache(wl)
-    ref = oracle_attention(wl, kc, vc, tokens=tokens)
-    return assert_attention_close(g.out_f32(tokens), ref, wl.name), g
+    ref, bnd = oracle_reference(wl, kc, vc, tokens=tokens)
+    return assert_attention_close(g.out_f32(tokens), ref, wl.name, bnd), g
 
 
 def test_config1_tiny(cuda_device):
@@ -127,7 +127,8 @@ def test_unwritten_pages_outside_window_are_ignored(cuda_device):
     mask = visible_window_mask(wl, range(wl.num_req))
     g = GpuRun(wl, write_mask=mask).write_cache().attention()
     kc, vc = oracle_cache(wl, write_mask=mask)
-    assert_attention_close(g.out_f32(), oracle_attention(wl, kc, vc), "unwritten")
+    ref, bnd = oracle_reference(wl, kc, vc)
+    assert_attention_close(g.out_f32(), ref, "unwritten", bnd)
 
 
 @pytest.mark.parametrize("index,dtype", [(2, None), (3, None), (4, "int8_per_token_head"),
@@ -148,6 +149,6 @@ def test_full_size_sampled(cuda_device, index, dtype):
                            + [int(span[-1])]))
     mask = visible_window_mask(wl, reqs)
     kc, vc = oracle_cache(wl, write_mask=mask)
-    ref = oracle_attention(wl, kc, vc, tokens=np.array(toks))
-    assert_attention_close(g.out_f32(toks), ref, wl.name)
+    ref, bnd = oracle_reference(wl, kc, vc, tokens=np.array(toks))
+    assert_attention_close(g.out_f32(toks), ref, wl.name, bnd)
     assert torch.isfinite(g.out.float()).all()
