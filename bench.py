@@ -303,8 +303,13 @@ def run_gpu(args, rank, world, local):
     e2e_value = world * (kvb if decode_metric else flops) / e2e_s / (1e9 if decode_metric else 1e12)
 
     peaks, peaks_src = _peaks()
-    roofline = {"bound": "hbm" if decode_metric else "tensor",
-                "kernel": "split-KV row-tile attention (+ split merge)",
+    if info["num_prefill_tiles"] and info["num_tiles"]:
+        kernel = "tcgen05 prefill + split-KV decode (one attention call)"
+    elif info["num_prefill_tiles"]:
+        kernel = "tcgen05 prefill attention"
+    else:
+        kernel = "split-KV decode attention (+ split merge)"
+    roofline = {"bound": "hbm" if decode_metric else "tensor", "kernel": kernel,
                 "unit": "GB/s" if decode_metric else "TFLOP/s", "traffic": None,
                 "peak_source": peaks_src}
     if decode_metric:

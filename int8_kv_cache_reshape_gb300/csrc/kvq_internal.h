@@ -76,16 +76,22 @@ KVQ_HD constexpr size_t decode_smem_bytes(int dtype, int head_dim) {
 // keys stream through in tiles of 64.  Requests whose rows per kv head
 // exceed kTileMaxRows go to this kernel.
 constexpr int kPrefillRows = 128;
-constexpr int kPrefillKeys = 64;
-// Tensor-memory columns: O (head_dim fp32) + S (64 fp32), a power of two.
-KVQ_HD constexpr int prefill_tmem_cols(int head_dim) {
-  return head_dim + kPrefillKeys <= 128 ? 128 : (head_dim + kPrefillKeys <= 256 ? 256 : 512);
-}
-// Shared memory: Q (128 x D bf16), K (64 x D), V^T (D x 64), P (128 x 64),
-// key / value scales, key-valid flags, barriers; +1 KB for 1024 alignment.
+constexpr int kPrefillStages = 2;        // K / V^T tiles in flight
+constexpr int kPrefillThreads = 384;     // 1 MMA warp, 4 softmax warps, 7 converter warps
+constexpr int kPrefillConvThreads = 224;
+// Keys per KV tile: 128, or 64 at head_dim 256 (shared memory).
+KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
+// Tensor-memory columns: O (head_dim fp32) + two S buffers; always 512.
+KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
+// Shared memory: Q (128 x D f16), 2 x K (keys x D f16), 2 x V^T (D x keys
+// f16), P (128 x keys f16), 2 x key / value scales and key-valid flags,
+// the 128 rows' Q scales, barriers; +1 KB for 1024-byte alignment.
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
-  return (size_t)kPrefillRows * head_dim * 2 + 2 * (size_t)kPrefillKeys * head_dim * 2 +
-         (size_t)kPrefillRows * kPrefillKeys * 2 + kPrefillKeys * (4 + 4 + 1) + 32 + 1024;
+  return (size_t)kPrefillRows * head_dim * 2 +
+         2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
+         (size_t)kPrefillRows * prefill_keys(head_dim) * 2 +
+         (size_t)kPrefillStages * prefill_keys(head_dim) * (4 + 4 + 1) + kPrefillRows * 4 + 128 +
+         1024;
 }
 
 struct PrefillTile {
