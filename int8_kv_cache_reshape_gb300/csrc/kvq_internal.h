@@ -81,15 +81,16 @@ constexpr int kPrefillThreads = 384;     // 1 MMA warp, 4 softmax warps, 7 conve
 constexpr int kPrefillConvThreads = 224;
 // Keys per KV tile: 128, or 64 at head_dim 256 (shared memory).
 KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
-// Tensor-memory columns: O (head_dim fp32) + two S buffers; always 512.
+// Tensor-memory columns: O (head_dim fp32), two S buffers (keys fp32 each,
+// P in f16 pairs over the first half), Q (head_dim / 2 columns of f16
+// pairs); always 512.
 KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
-// Shared memory: Q (128 x D f16), 2 x K (keys x D f16), 2 x V^T (D x keys
-// f16), P (128 x keys f16), 2 x key / value scales and key-valid flags,
-// the 128 rows' Q scales, barriers; +1 KB for 1024-byte alignment.
+// Shared memory: 2 x K and 2 x V (keys x D f16 each), 2 x key / value
+// scales and key-valid flags, the 128 rows' Q scales, barriers; +1 KB for
+// 1024-byte alignment.  Q is staged through the K ring before it moves to
+// tensor memory.
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
-  return (size_t)kPrefillRows * head_dim * 2 +
-         2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
-         (size_t)kPrefillRows * prefill_keys(head_dim) * 2 +
+  return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
          (size_t)kPrefillStages * prefill_keys(head_dim) * (4 + 4 + 1) + kPrefillRows * 4 + 128 +
          1024;
 }

@@ -1,5 +1,6 @@
 // kvq_prefill.cuh -- prefill attention over the quantised paged cache on the
-// 5th-generation tensor cores (tcgen05, accumulators in tensor memory).
+// 5th-generation tensor cores (tcgen05, operands and accumulators in tensor
+// memory).
 //
 // What it computes is the attention of kvq_decode.cuh (same masks, soft cap,
 // scales) for tiles of 128 packed (query token, head) rows of one kv head:
@@ -11,21 +12,28 @@
 //
 // GB300 design: one CTA of 12 warps per 128-row tile, warp-specialised and
 // pipelined through mbarriers.
-//   * Converter warps (1-3, 8-11): stream the key and value codes of the
-//     paged cache (16-byte loads, a whole 32-byte sector per key row and
-//     load pair), convert them exactly to f16 (every e4m3 / e5m2 / int8
-//     value is an f16 value) and store K (keys x D) and V^T (D x keys) in the
-//     128-byte-swizzled K-major layout the tensor core reads, into a 2-stage
-//     ring; per-token-head scales and key-valid flags go beside them.
-//   * Warp 0, one thread: issues S(j+1) = Q K(j+1)^T into the free one of
-//     two tensor-memory S buffers while the softmax works on S(j), then
-//     O += P(j) V(j) once P(j) is in shared memory; commits free the ring.
-//   * Softmax warps (4-7): thread t owns row t (tensor-memory lane t).  It
-//     reads its row of S twice (maximum, then weights), applies scales,
-//     soft cap and masks, keeps a lazy reference maximum (moved only when a
-//     score exceeds it by 2^8; weights are lifted by 2^6, so P <= 2^14),
-//     writes its row of P in f16 and, when the reference moved, rescales its
-//     row of O in tensor memory.  At the end it reads O and writes bf16.
+//   * Tensor memory (512 columns): O (D fp32 columns), two S buffers (keys
+//     fp32 columns each; P(j) is written as f16 pairs over the first half of
+//     S(j)'s buffer), and Q (D/2 columns of f16 pairs).  Both MMAs take A
+//     from tensor memory: S = Q K^T and O += P V read only K and V from
+//     shared memory.
+//   * Converter warps (1-3, 8-11): a thread takes (key, 32 dims) pieces; one
+//     block-table lookup serves the key's K and V rows (the caches share a
+//     layout); it loads 32 codes of each (one 32-byte sector), converts them
+//     exactly to f16 (every e4m3 / e5m2 / int8 value is an f16 value) and
+//     stores both as key-major rows in the 128-byte swizzle into a 2-stage
+//     ring.  K is read by the tensor core K-major, V MN-major, so neither
+//     needs a transpose.  The next tile's codes are loaded while the current
+//     tile is consumed.  Per-token-head scales and key-valid flags go beside.
+//   * Warp 0, one thread: issues S(j+1) as soon as K(j+1) is in and P(j-1)
+//     has been consumed, and O += P(j) V(j) as soon as P(j) and V(j) are in,
+//     whichever comes first; commits free the ring and signal the softmax.
+//   * Softmax warps (4-7): thread t owns row t (tensor-memory lane t).  A
+//     maximum pass over its row of S, then a weights pass that writes P in
+//     f16 straight into tensor memory.  The reference maximum is lazy (moved
+//     only when a score exceeds it by 2^8; weights are lifted by 2^6, so
+//     P <= 2^14); only when it moves does the thread wait for P(j-1) V(j-1)
+//     and rescale its row of O.  At the end it reads O and writes bf16.
 //   * Q enters as f16 exactly: each row is scaled by a power of two that puts
 //     its largest |q| in [2^14, 2^15) (a bf16 significand fits in f16's);
 //     the scale, sm_scale, log2(e) and k_scale (per tensor) or the key's
@@ -59,27 +67,33 @@ struct PrefillGeom {
   static constexpr int kStages = kPrefillStages;
   static constexpr bool kPth = is_per_token_head(DT);
   static constexpr int kRow = row_bytes(DT, D);
-  static constexpr int kOffQ = 0;                                   // kM x D f16
-  static constexpr int kOffK = kOffQ + kM * D * 2;                  // stages x kN x D f16
-  static constexpr int kOffV = kOffK + kStages * kN * D * 2;        // stages x D x kN f16
-  static constexpr int kOffP = kOffV + kStages * D * kN * 2;        // kM x kN f16
-  static constexpr int kOffSk = kOffP + kM * kN * 2;                // stages x kN f32
+  static constexpr int kTileBytes = kN * D * 2;                     // one K or V tile (f16)
+  static constexpr int kOffK = 0;                                   // stages x K tile
+  static constexpr int kOffV = kOffK + kStages * kTileBytes;        // stages x V tile
+  static constexpr int kOffSk = kOffV + kStages * kTileBytes;       // stages x kN f32
   static constexpr int kOffSv = kOffSk + kStages * kN * 4;          // stages x kN f32
   static constexpr int kOffValid = kOffSv + kStages * kN * 4;       // stages x kN bytes
   static constexpr int kOffQScale = kOffValid + kStages * kN;       // kM f32: 2^-sh of each Q row
   static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
   static constexpr int kBytes = kOffBar + 128;
-  static constexpr int kColO = 0;   // O: D fp32 columns
-  static constexpr int kColS = D;   // S buffers: kN fp32 columns each
+  static constexpr int kOffQStage = kOffK;  // Q (kM x D f16, swizzled) staged over the K ring
+  static constexpr int kOffOStage = kOffK;  // O (kM x D bf16) staged over the K ring at the end
+  static constexpr int kColO = 0;                 // O: D fp32 columns
+  static constexpr int kColS = D;                 // S buffers: kN fp32 columns each
+  static constexpr int kColQ = D + 2 * kN;        // Q: D/2 columns of f16 pairs
   static constexpr int kTmemCols = prefill_tmem_cols(D);
-  static_assert(D + 2 * kN <= kTmemCols, "tensor memory: O + 2 S buffers");
-  static_assert(kOffK % 1024 == 0 && kOffV % 1024 == 0 && kOffP % 1024 == 0, "1024-byte tiles");
-  static_assert((kN * D * 2) % 1024 == 0, "stage tiles stay 1024-byte aligned");
+  static_assert(kColQ + D / 2 <= kTmemCols, "tensor memory: O + 2 S buffers + Q");
+  static_assert(kM * D * 2 <= kStages * kTileBytes, "Q / O staging fits the K ring");
+  static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0, "1024-byte tiles");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
   // barrier slots (8 bytes each)
+  // One P barrier per S buffer: P(j+1) may be ready before PV(j) is
+  // issued.  A parity wait is unambiguous only while the waiter is at most
+  // one phase behind, so the epilogue (which may be several PVs ahead of
+  // the last phase it saw) waits on a one-shot barrier for the last PV.
   static constexpr int kBarKFull = 0, kBarVFull = 2, kBarKvEmpty = 4, kBarSFull = 6, kBarPFull = 8,
-                       kBarODone = 9, kBarDrain = 10, kNumBars = 11;
+                       kBarODone = 10, kBarOFinal = 11, kBarDrain = 12, kNumBars = 13;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
   static constexpr int kOffBadTile = kOffAbort + 4;             // stages x i32
@@ -89,6 +103,13 @@ struct PrefillGeom {
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
   asm volatile("st.shared.v4.u32 [%0], {%1,%2,%3,%4};" :: "r"(addr), "r"(v.x), "r"(v.y), "r"(v.z),
                "r"(v.w) : "memory");
+}
+
+__device__ __forceinline__ uint4 lds128(uint32_t addr) {
+  uint4 v;
+  asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
+               : "r"(addr));
+  return v;
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -111,9 +132,11 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, vol
 
 // 8 codes (two words) -> 8 f16 (four f16x2 words), exact.
 template <int DT>
-__device__ __forceinline__ void codes8_to_f16(uint32_t w0, uint32_t w1, uint32_t (&h)[4]) {
-  dev::word_to_f16x2x2<DT>(w0, h[0], h[1]);
-  dev::word_to_f16x2x2<DT>(w1, h[2], h[3]);
+__device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
+  uint4 h;
+  dev::word_to_f16x2x2<DT>(w0, h.x, h.y);
+  dev::word_to_f16x2x2<DT>(w1, h.z, h.w);
+  return h;
 }
 
 template <int DT, int D>
@@ -146,10 +169,11 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
       tc::mbar_init(bar(Geo::kBarVFull + s), Geo::kConv);
       tc::mbar_init(bar(Geo::kBarKvEmpty + s), 1);
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
+      tc::mbar_init(bar(Geo::kBarPFull + s), 128);
       bad_tile[s] = -1;
     }
-    tc::mbar_init(bar(Geo::kBarPFull), 128);
     tc::mbar_init(bar(Geo::kBarODone), 1);
+    tc::mbar_init(bar(Geo::kBarOFinal), 1);
     tc::mbar_init(bar(Geo::kBarDrain), 1);
     *abort_flag = 0u;
     tc::mbar_fence_init();
@@ -159,11 +183,83 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
     tc::tmem_relinquish();
   }
 
-  // ---- Q tile -> shared memory, all warps: lanes_per_row lanes hold one
-  // row (16 bytes each, coalesced); the row's largest exponent comes from a
-  // shuffle reduction over those lanes, and the row is scaled by the power of
-  // two that puts its largest |q| in [2^14, 2^15) (exact in f16: a bf16
-  // significand fits in f16's).
+  // ---- converter state (used by warps 1-3, 8-11)
+  const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
+  const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
+  const int64_t row_stride = (int64_t)p.heads_kv * Geo::kRow;
+  const uint8_t* kcache = p.key_cache + (int64_t)t.kv_head * Geo::kRow;
+  const uint8_t* vcache = p.value_cache + (int64_t)t.kv_head * Geo::kRow;
+  float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
+  float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
+  uint8_t* kvalid = sm + Geo::kOffValid;
+  // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
+  // floor((2^32 - 1) / B)) is q or q - 1 for every 32-bit j.
+  const uint32_t bsz = (uint32_t)p.block_size;
+  const uint32_t bdiv = 0xFFFFFFFFu / bsz;
+  // Byte offset of logical key j's row in either cache, or -1 when its
+  // block is missing.
+  auto key_off = [&](int j) -> int64_t {
+    uint32_t q = __umulhi((uint32_t)j, bdiv);
+    uint32_t r = (uint32_t)j - q * bsz;
+    if (r >= bsz) {
+      ++q;
+      r -= bsz;
+    }
+    const int blk = btab[q];
+    if (blk < 0 || (int64_t)blk >= p.num_blocks) return -1;
+    return ((int64_t)blk * bsz + r) * row_stride;
+  };
+  // A unit is (key n, 32 dims pc); 8 consecutive threads take 8
+  // consecutive keys, so the swizzled 16-byte stores hit 8 bank groups.
+  constexpr int kUnits = kN * (D / 32);
+  constexpr int kSlots = (kUnits + Geo::kConv - 1) / Geo::kConv;
+  uint4 kraw[kSlots][2], vraw[kSlots][2];  // the next tile's codes
+  float kscale[kSlots], vscale[kSlots];
+  uint32_t kdead = 0, kmiss = 0;  // per slot: key in range without a block / no row
+  auto load_tile = [&](int j) {
+    const int kv0 = kv_first + j * kN;
+    kdead = kmiss = 0;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int u = ctid + i * Geo::kConv;
+      kraw[i][0] = kraw[i][1] = vraw[i][0] = vraw[i][1] = make_uint4(0, 0, 0, 0);
+      kscale[i] = vscale[i] = 0.0f;
+      if (u < kUnits) {
+        const int n = u % kN, pc = u / kN;
+        const int jj = kv0 + n;
+        const bool in_range = jj >= t.kv_lo && jj < t.kv_hi;
+        const int64_t off = in_range ? key_off(jj) : -1;
+        if (off >= 0) {
+          const uint8_t* kr = kcache + off;
+          const uint8_t* vr = vcache + off;
+          kraw[i][0] = *reinterpret_cast<const uint4*>(kr + 32 * pc);
+          kraw[i][1] = *reinterpret_cast<const uint4*>(kr + 32 * pc + 16);
+          vraw[i][0] = *reinterpret_cast<const uint4*>(vr + 32 * pc);
+          vraw[i][1] = *reinterpret_cast<const uint4*>(vr + 32 * pc + 16);
+          if constexpr (Geo::kPth) {
+            if (pc == 0) {
+              kscale[i] = *reinterpret_cast<const float*>(kr + D);
+              vscale[i] = *reinterpret_cast<const float*>(vr + D);
+            }
+          }
+        } else {
+          kmiss |= 1u << i;
+          if (in_range) kdead |= 1u << i;
+        }
+      }
+    }
+  };
+  auto store_rows = [&](uint32_t tile, const uint4 (&c)[2], int n, int pc) {
+    sts128(tile + tc::sw128_offset(kN, n, 32 * pc), codes8_to_f16<DT>(c[0].x, c[0].y));
+    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 8), codes8_to_f16<DT>(c[0].z, c[0].w));
+    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 16), codes8_to_f16<DT>(c[1].x, c[1].y));
+    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 24), codes8_to_f16<DT>(c[1].z, c[1].w));
+  };
+
+  // ---- Q tile -> staging (swizzled rows), all warps: lanes_per_row lanes
+  // hold one row (16 bytes each, coalesced); the row's largest exponent
+  // comes from a shuffle reduction over those lanes, and the row is scaled
+  // by the power of two that puts its largest |q| in [2^14, 2^15).
   {
     constexpr int kLpr = D / 8;            // lanes per row
     constexpr int kRps = 32 / kLpr;        // rows per warp step
@@ -201,67 +297,100 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
         o.y = dev::pack_f16x2(dev::bf16_lo(w[1]) * up, dev::bf16_hi(w[1]) * up);
         o.z = dev::pack_f16x2(dev::bf16_lo(w[2]) * up, dev::bf16_hi(w[2]) * up);
         o.w = dev::pack_f16x2(dev::bf16_lo(w[3]) * up, dev::bf16_hi(w[3]) * up);
-        sts128(base + Geo::kOffQ + tc::sw128_offset(kM, m, 8 * c), o);
+        sts128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 8 * c), o);
         if (c == 0) qscale[m] = ldexpf(1.0f, -sh);
       }
     }
-    tc::fence_async_smem();
   }
+  __syncthreads();
+  tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffTmemSlot);
   const bool is_softmax = warp >= 4 && warp < 8;
   const int m = tid - 128;  // row (softmax warps)
   const bool row_valid = is_softmax && m < t.nrows;
   const int R = t.row0 + (row_valid ? m : 0);
+  const uint32_t lane_base = (uint32_t)(((warp - 4) & 3) * 32) << 16;
+  if (is_softmax) {
+    // The softmax warps move Q rows (their own lanes) into tensor memory.
+#pragma unroll
+    for (int c0 = 0; c0 < D / 2; c0 += 16) {
+      uint32_t w[16];
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const uint4 x = lds128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 2 * c0 + 8 * q));
+        w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
+      }
+      tc::tmem_st16(tmem + Geo::kColQ + lane_base + c0, w);
+    }
+    tc::tmem_wait_st();
+  }
   tc::fence_before_sync();
-  __syncthreads();
+  __syncthreads();  // Q is in tensor memory; the staging area is free
   tc::fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffTmemSlot);
 
   if (warp == 0) {
     // ======================= MMA issuer ========================================
     if (tid == 0 && T > 0) {
       constexpr uint32_t idesc_s = tc::idesc_f16(kM, kN);
-      constexpr uint32_t idesc_o = tc::idesc_f16(kM, D);
+      constexpr uint32_t idesc_o = tc::idesc_f16(kM, D) | tc::kBMajorMN;
       auto issue_s = [&](int j) {
         const int st = j & 1;
-        const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN);
-        const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * kN * D * 2);
+        const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes);
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
           const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
-          tc::mma_bf16(tmem_s, tc::desc_sw128(base + Geo::kOffQ + aoff), tc::desc_sw128(kbase + boff),
-                       idesc_s, kk > 0 ? 1u : 0u);
+          tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
+                     tc::desc_sw128(kbase + boff), idesc_s, kk > 0 ? 1u : 0u);
         }
         tc::mma_commit(bar(Geo::kBarSFull + st));
       };
-      bool ok = wait_or_abort(bar(Geo::kBarKFull + 0), 0u, abort_flag);
-      if (ok) {
-        tc::fence_after_sync();
-        issue_s(0);
-      }
-      for (int j = 0; ok && j < T; ++j) {
+      auto issue_pv = [&](int j) {
         const int st = j & 1;
-        if (j + 1 < T) {
-          ok = wait_or_abort(bar(Geo::kBarKFull + ((j + 1) & 1)), (uint32_t)(((j + 1) >> 1) & 1),
-                             abort_flag);
-          if (!ok) break;
-          tc::fence_after_sync();
-          issue_s(j + 1);
-        }
-        ok = wait_or_abort(bar(Geo::kBarPFull), (uint32_t)(j & 1), abort_flag) &&
-             wait_or_abort(bar(Geo::kBarVFull + st), (uint32_t)((j >> 1) & 1), abort_flag);
-        if (!ok) break;
-        tc::fence_after_sync();
-        const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * D * kN * 2);
+        const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes);
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk) {
-          const uint32_t aoff = (kk >> 2) * (kM * 128) + (kk & 3) * 32;
-          const uint32_t boff = (kk >> 2) * (D * 128) + (kk & 3) * 32;
-          tc::mma_bf16(tmem + Geo::kColO, tc::desc_sw128(base + Geo::kOffP + aoff),
-                       tc::desc_sw128(vbase + boff), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-        }
+        for (int kk = 0; kk < kN / 16; ++kk)
+          tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
+                     tc::desc_sw128_mn(vbase + (uint32_t)(kk * 2048), kN * 128, 1024), idesc_o,
+                     (j > 0 || kk > 0) ? 1u : 0u);
         tc::mma_commit(bar(Geo::kBarODone));
         tc::mma_commit(bar(Geo::kBarKvEmpty + st));
+        if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
+      };
+      // S(j) needs K(j) and PV(j-2) issued (P(j-2) shares its buffer; the
+      // tensor core runs one thread's MMAs in order).  PV(j) needs P(j) and
+      // V(j).  Issue whichever is ready.
+      int ns = 0, npv = 0;
+      bool ok = true;
+      long long t_idle = clock64();
+      while (npv < T) {
+        bool progressed = false;
+        if (ns < T && ns <= npv + 1 &&
+            tc::mbar_try_wait(bar(Geo::kBarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1))) {
+          tc::fence_after_sync();
+          issue_s(ns);
+          ++ns;
+          progressed = true;
+        }
+        if (npv < ns && tc::mbar_try_wait(bar(Geo::kBarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
+            tc::mbar_try_wait(bar(Geo::kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+          tc::fence_after_sync();
+          issue_pv(npv);
+          ++npv;
+          progressed = true;
+        }
+        if (progressed) {
+          t_idle = clock64();
+        } else {
+          if (*abort_flag) {
+            ok = false;
+            break;
+          }
+          if (clock64() - t_idle > 2000000000LL) {
+            *abort_flag = 1u;
+            ok = false;
+            break;
+          }
+        }
       }
       if (!ok) {
         // Drain whatever was issued before the tensor memory is freed.
@@ -272,115 +401,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
     __syncwarp();
   } else if (!is_softmax) {
     // ======================= converters ========================================
-    const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
-    const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
-    const int64_t row_stride = (int64_t)p.heads_kv * Geo::kRow;
-    const uint8_t* kcache = p.key_cache + (int64_t)t.kv_head * Geo::kRow;
-    const uint8_t* vcache = p.value_cache + (int64_t)t.kv_head * Geo::kRow;
-    float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
-    float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
-    uint8_t* kvalid = sm + Geo::kOffValid;
-    // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
-    // floor((2^32 - 1) / B)) is q or q - 1 for every 32-bit j.
-    const uint32_t bsz = (uint32_t)p.block_size;
-    const uint32_t bdiv = 0xFFFFFFFFu / bsz;
-    // Row of logical key j (j >= 0), or nullptr when its block is missing.
-    // Keys j .. j + k within one 8-aligned group share a block (block sizes
-    // are multiples of 16), so their rows are consecutive slots.
-    auto key_row = [&](const uint8_t* cache, int j) -> const uint8_t* {
-      uint32_t q = __umulhi((uint32_t)j, bdiv);
-      uint32_t r = (uint32_t)j - q * bsz;
-      if (r >= bsz) {
-        ++q;
-        r -= bsz;
-      }
-      const int blk = btab[q];
-      if (blk < 0 || (int64_t)blk >= p.num_blocks) return nullptr;
-      return cache + ((int64_t)blk * bsz + r) * row_stride;
-    };
-    constexpr int kKUnits = kN * (D / 32);        // key x 32-code pieces
-    constexpr int kVUnits = (kN / 8) * (D / 16);  // 8 keys x 16 dims
-    constexpr int kKSlots = (kKUnits + Geo::kConv - 1) / Geo::kConv;
-    constexpr int kVSlots = (kVUnits + Geo::kConv - 1) / Geo::kConv;
-    // Codes of the next tile, loaded while the current one is in use.
-    uint4 kraw[kKSlots][2];
-    uint4 vraw[kVSlots][8];
-    float kscale[kKSlots];
-    float vscale[kVSlots][8];
-    uint32_t kdead = 0;  // bit i: K slot i's key has no row (in range, no block)
-    uint32_t kmiss = 0;  // bit i: K slot i's key has no row at all
-    auto load_tile = [&](int j) {
-      const int kv0 = kv_first + j * kN;
-      kdead = kmiss = 0;
-#pragma unroll
-      for (int i = 0; i < kKSlots; ++i) {
-        const int u = ctid + i * Geo::kConv;
-        kraw[i][0] = kraw[i][1] = make_uint4(0, 0, 0, 0);
-        kscale[i] = 0.0f;
-        if (u < kKUnits) {
-          const int n = u % kN, pc = u / kN;
-          const int jj = kv0 + n;
-          const bool in_range = jj >= t.kv_lo && jj < t.kv_hi;
-          const uint8_t* row = in_range ? key_row(kcache, jj) : nullptr;
-          if (row) {
-            kraw[i][0] = *reinterpret_cast<const uint4*>(row + 32 * pc);
-            kraw[i][1] = *reinterpret_cast<const uint4*>(row + 32 * pc + 16);
-            if constexpr (Geo::kPth)
-              if (pc == 0) kscale[i] = *reinterpret_cast<const float*>(row + D);
-          } else {
-            kmiss |= 1u << i;
-            if (in_range) kdead |= 1u << i;
-          }
-        }
-      }
-#pragma unroll
-      for (int i = 0; i < kVSlots; ++i) {
-        const int u = ctid + i * Geo::kConv;
-#pragma unroll
-        for (int k = 0; k < 8; ++k) {
-          vraw[i][k] = make_uint4(0, 0, 0, 0);
-          vscale[i][k] = 0.0f;
-        }
-        if (u < kVUnits) {
-          const int kg = u % (kN / 8), d16 = u / (kN / 8);
-          const int j8 = kv0 + 8 * kg;  // 8-aligned: one block for all 8 keys
-          const uint8_t* row0 =
-              (j8 + 8 > t.kv_lo && j8 < t.kv_hi) ? key_row(vcache, j8) : nullptr;
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            if (row0 && j8 + k >= t.kv_lo && j8 + k < t.kv_hi) {
-              const uint8_t* row = row0 + (int64_t)k * row_stride;
-              vraw[i][k] = *reinterpret_cast<const uint4*>(row + 16 * d16);
-              if constexpr (Geo::kPth)
-                if (d16 == 0) vscale[i][k] = *reinterpret_cast<const float*>(row + D);
-            }
-          }
-        }
-      }
-    };
     if (T > 0) load_tile(0);
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
       if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarKvEmpty + st),
                                                             (uint32_t)(((j >> 1) - 1) & 1), abort_flag)))
         break;
-      // ---- K: thread -> (key n, 32 codes); 8 consecutive threads take 8
-      // consecutive keys, so the swizzled 16-byte stores hit 8 bank groups.
-      const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * kN * D * 2);
+      const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes);
+      const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes);
 #pragma unroll
-      for (int i = 0; i < kKSlots; ++i) {
+      for (int i = 0; i < kSlots; ++i) {
         const int u = ctid + i * Geo::kConv;
-        if (u < kKUnits) {
+        if (u < kUnits) {
           const int n = u % kN, pc = u / kN;
-          uint32_t h[4];
-          codes8_to_f16<DT>(kraw[i][0].x, kraw[i][0].y, h);
-          sts128(kbase + tc::sw128_offset(kN, n, 32 * pc), make_uint4(h[0], h[1], h[2], h[3]));
-          codes8_to_f16<DT>(kraw[i][0].z, kraw[i][0].w, h);
-          sts128(kbase + tc::sw128_offset(kN, n, 32 * pc + 8), make_uint4(h[0], h[1], h[2], h[3]));
-          codes8_to_f16<DT>(kraw[i][1].x, kraw[i][1].y, h);
-          sts128(kbase + tc::sw128_offset(kN, n, 32 * pc + 16), make_uint4(h[0], h[1], h[2], h[3]));
-          codes8_to_f16<DT>(kraw[i][1].z, kraw[i][1].w, h);
-          sts128(kbase + tc::sw128_offset(kN, n, 32 * pc + 24), make_uint4(h[0], h[1], h[2], h[3]));
+          store_rows(kbase, kraw[i], n, pc);
           if (pc == 0) {
             kvalid[st * kN + n] = (kmiss >> i) & 1u ? 0 : 1;
             if constexpr (Geo::kPth) sk[st * kN + n] = kscale[i];
@@ -390,36 +424,14 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
       }
       tc::fence_async_smem();
       mbar_arrive(bar(Geo::kBarKFull + st));
-      // ---- V^T: thread -> (8 keys, 16 dims); threads with consecutive key
-      // groups share dims, so the stores of one row hit distinct bank groups.
-      const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * D * kN * 2);
 #pragma unroll
-      for (int i = 0; i < kVSlots; ++i) {
+      for (int i = 0; i < kSlots; ++i) {
         const int u = ctid + i * Geo::kConv;
-        if (u < kVUnits) {
-          const int kg = u % (kN / 8), d16 = u / (kN / 8);
-          uint32_t x[8][8];  // key k: 16 dims as 8 f16x2 words
-#pragma unroll
-          for (int k = 0; k < 8; ++k) {
-            uint32_t h[4];
-            codes8_to_f16<DT>(vraw[i][k].x, vraw[i][k].y, h);
-            x[k][0] = h[0]; x[k][1] = h[1]; x[k][2] = h[2]; x[k][3] = h[3];
-            codes8_to_f16<DT>(vraw[i][k].z, vraw[i][k].w, h);
-            x[k][4] = h[0]; x[k][5] = h[1]; x[k][6] = h[2]; x[k][7] = h[3];
-            if constexpr (Geo::kPth)
-              if (d16 == 0) sv[st * kN + 8 * kg + k] = vscale[i][k];
-          }
-          // Row d of V^T holds keys 8kg .. 8kg+7: the d-th half of each word.
-#pragma unroll
-          for (int w = 0; w < 8; ++w)
-#pragma unroll
-            for (int hh = 0; hh < 2; ++hh) {
-              const uint32_t sel = hh ? 0x7632u : 0x5410u;
-              const uint4 out =
-                  make_uint4(dev::prmt(x[0][w], x[1][w], sel), dev::prmt(x[2][w], x[3][w], sel),
-                             dev::prmt(x[4][w], x[5][w], sel), dev::prmt(x[6][w], x[7][w], sel));
-              sts128(vbase + tc::sw128_offset(D, 16 * d16 + 2 * w + hh, 8 * kg), out);
-            }
+        if (u < kUnits) {
+          const int n = u % kN, pc = u / kN;
+          store_rows(vbase, vraw[i], n, pc);
+          if constexpr (Geo::kPth)
+            if (pc == 0) sv[st * kN + n] = vscale[i];
         }
       }
       tc::fence_async_smem();
@@ -429,7 +441,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
     __syncwarp();
   } else {
     // ======================= softmax ===========================================
-    const uint32_t lane_base = (uint32_t)((warp - 4) * 32) << 16;
     const float* sk = reinterpret_cast<const float*>(sm + Geo::kOffSk);
     const float* sv = reinterpret_cast<const float*>(sm + Geo::kOffSv);
     const uint8_t* kvalid = sm + Geo::kOffValid;
@@ -455,7 +466,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
       ok = wait_or_abort(bar(Geo::kBarSFull + st), (uint32_t)((j >> 1) & 1), abort_flag) &&
            wait_or_abort(bar(Geo::kBarKFull + st), (uint32_t)((j >> 1) & 1), abort_flag) &&
            (!Geo::kPth || wait_or_abort(bar(Geo::kBarVFull + st), (uint32_t)((j >> 1) & 1), abort_flag));
-      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory loads are collective
+      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory accesses are collective
       if (!ok) break;
       tc::fence_after_sync();
       const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN) + lane_base;
@@ -463,8 +474,57 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
       // tile, or the tile has a key without a block.
       const bool full =
           __all_sync(0xffffffffu, kv0 >= row_lo && kv0 + kN <= row_hi) && bad_tile[st] != j;
-      // Value-scale reference (per-token-head): the largest exponent so far.
+      // r: the raw score (per-token-head: times the key's scale), -inf when
+      // masked; r * score_mul is the score in log2 units without a cap.
+      auto raw_pair = [&](auto full_c, uint32_t b0, uint32_t b1, int n, float& r0, float& r1) {
+        r0 = __uint_as_float(b0);
+        r1 = __uint_as_float(b1);
+        if constexpr (Geo::kPth) {
+          const float2 k2 = *reinterpret_cast<const float2*>(sk + st * kN + n);
+          r0 *= k2.x;
+          r1 *= k2.y;
+        }
+        if constexpr (!decltype(full_c)::value) {
+          const int jj = kv0 + n;
+          r0 = kvalid[st * kN + n] && jj >= row_lo && jj < row_hi ? r0 : -INFINITY;
+          r1 = kvalid[st * kN + n + 1] && jj + 1 >= row_lo && jj + 1 < row_hi ? r1 : -INFINITY;
+        }
+      };
+      // The score in log2 units from r.  Under a cap, masked r stays masked
+      // (a capped -inf would be finite).
+      auto score = [&](auto cap_c, float r) -> float {
+        if constexpr (decltype(cap_c)::value)
+          return r == -INFINITY ? -INFINITY : cap_l2 * tanhf(r * score_mul * inv_cap);
+        else
+          return r * score_mul;
+      };
+      // ---- pass 1: the row's maximum over this tile
+      auto max_pass = [&](auto full_c) -> float {
+        float mr = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < kN; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tmem_s + c0, v);
+          tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; e += 2) {
+            float r0, r1;
+            raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
+            mr = fmaxf(mr, fmaxf(r0, r1));
+          }
+        }
+        return mr;
+      };
+      const float mr = full ? max_pass(std::true_type{}) : max_pass(std::false_type{});
+      // the score is monotonic in r (score_mul > 0, tanh increasing)
+      const float mx = cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
       float alpha = 1.0f;  // factor for O (score reference and value reference)
+      if (mx > m_ref + 8.0f) {
+        alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
+        l_sum *= alpha;
+        m_ref = mx;
+      }
+      // Value-scale reference (per-token-head): the largest exponent so far.
       float v_mul = 1.0f;  // 2^-ev
       if constexpr (Geo::kPth) {
         float smax = 0.0f;
@@ -477,132 +537,87 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
           int e;
           (void)frexpf(smax, &e);  // smax < 2^e
           if (e > ev) {
-            if (ev > -1000) alpha = ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
+            if (ev > -1000) alpha *= ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
             ev = e;
           }
         }
         v_mul = ldexpf(1.0f, -ev);
       }
-      // Weights against the current reference: P = 2^(z - m_ref + 6) <= 2^14
-      // while no score exceeds m_ref + 8 (the 2^6 lifts small weights clear
-      // of the f16 subnormal range; l carries the same factor).  Specialised
-      // on a tile every row sees whole (no masks) and on the soft cap.
-      uint32_t pw[kN / 2];
-      float lsum_tile = 0.0f, mx = -INFINITY;
-      auto weights = [&](auto full_c, auto cap_c) {
-        constexpr bool kFull = decltype(full_c)::value, kCap = decltype(cap_c)::value;
-        const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
-        float mr = -INFINITY;  // max of r (r * score_mul is the score without a cap)
-        lsum_tile = 0.0f;
-        constexpr int kBatch = kN >= 128 ? 32 : 64;  // columns per tensor-memory wait (registers)
+      // ---- pass 2: P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs, written over
+      // the first half of S(j)'s columns (columns already read).  The 2^6
+      // lifts small weights clear of the f16 subnormal range; l carries the
+      // same factor.
+      const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
+      float lsum_tile = 0.0f;
+      auto weight_pass = [&](auto full_c, auto cap_c) {
 #pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += kBatch) {
-          uint32_t v[kBatch];
-#pragma unroll
-          for (int c = 0; c < kBatch; c += 32)
-            tc::tmem_ld32(tmem_s + c0 + c, *reinterpret_cast<uint32_t(*)[32]>(v + c));
+        for (int c0 = 0; c0 < kN; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tmem_s + c0, v);
           tc::tmem_wait_ld();
+          uint32_t pw[16];
 #pragma unroll
-          for (int e = 0; e < kBatch; e += 2) {
-            const int n = c0 + e;
-            float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
-            if constexpr (Geo::kPth) {
-              const float2 k2 = *reinterpret_cast<const float2*>(sk + st * kN + n);
-              r0 *= k2.x;
-              r1 *= k2.y;
-            }
-            bool vis0 = true, vis1 = true;
-            if constexpr (!kFull) {
-              const int jj = kv0 + n;
-              vis0 = kvalid[st * kN + n] && jj >= row_lo && jj < row_hi;
-              vis1 = kvalid[st * kN + n + 1] && jj + 1 >= row_lo && jj + 1 < row_hi;
-              if constexpr (!kCap) {
-                r0 = vis0 ? r0 : -INFINITY;
-                r1 = vis1 ? r1 : -INFINITY;
-              }
-            }
+          for (int e = 0; e < 32; e += 2) {
+            float r0, r1;
+            raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
             float p0, p1;
-            if constexpr (kCap) {
-              // the cap first, then the mask (a capped -inf would be finite)
-              float z0 = cap_l2 * tanhf(r0 * score_mul * inv_cap);
-              float z1 = cap_l2 * tanhf(r1 * score_mul * inv_cap);
-              z0 = vis0 ? z0 : -INFINITY;
-              z1 = vis1 ? z1 : -INFINITY;
-              mr = fmaxf(mr, fmaxf(z0, z1));
-              p0 = dev::fast_exp2(z0 - ref);
-              p1 = dev::fast_exp2(z1 - ref);
+            if constexpr (decltype(cap_c)::value) {
+              p0 = dev::fast_exp2(score(cap_c, r0) - ref);
+              p1 = dev::fast_exp2(score(cap_c, r1) - ref);
             } else {
-              mr = fmaxf(mr, fmaxf(r0, r1));
               p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
               p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
             }
             lsum_tile += p0 + p1;
             if constexpr (Geo::kPth) {
-              const float2 v2 = *reinterpret_cast<const float2*>(sv + st * kN + n);
+              const float2 v2 = *reinterpret_cast<const float2*>(sv + st * kN + c0 + e);
               p0 *= v2.x * v_mul;
               p1 *= v2.y * v_mul;
             }
-            pw[n / 2] = dev::pack_f16x2(p0, p1);
+            pw[e / 2] = dev::pack_f16x2(p0, p1);
           }
-        }
-        mx = kCap ? mr : mr * score_mul;  // score_mul > 0
-      };
-      auto run_weights = [&]() {
-        if (cap > 0.0f) {
-          if (full) weights(std::true_type{}, std::true_type{});
-          else weights(std::false_type{}, std::true_type{});
-        } else {
-          if (full) weights(std::true_type{}, std::false_type{});
-          else weights(std::false_type{}, std::false_type{});
+          tc::tmem_st16(tmem_s + c0 / 2, pw);
         }
       };
-      run_weights();
-      // A score above the reference by more than 2^8 moves it (lazily); the
-      // warp then recomputes its weights against the new reference.
-      if (__any_sync(0xffffffffu, mx > m_ref + 8.0f)) {
-        if (mx > m_ref + 8.0f) {
-          const float a = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
-          alpha *= a;
-          l_sum *= a;
-          m_ref = mx;
-        }
-        run_weights();
+      if (cap > 0.0f) {
+        if (full) weight_pass(std::true_type{}, std::true_type{});
+        else weight_pass(std::false_type{}, std::true_type{});
+      } else {
+        if (full) weight_pass(std::true_type{}, std::false_type{});
+        else weight_pass(std::false_type{}, std::false_type{});
       }
       l_sum += lsum_tile;
-      // PV(j-1) must be complete: it reads the P buffer and accumulates O.
-      if (j > 0) {
-        ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarODone), (uint32_t)((j - 1) & 1), abort_flag));
+      // A moved reference rescales O: PV(j-1) must be complete first.  (S(j)
+      // being complete implies PV(j-2) is, and PV(j) waits for this tile's
+      // P, so the barrier is at completion j-1 or j: the wait is exact.)
+      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+        ok = __all_sync(0xffffffffu,
+                        wait_or_abort(bar(Geo::kBarODone), (uint32_t)((j - 1) & 1), abort_flag));
         if (!ok) break;
         tc::fence_after_sync();
-        if (__any_sync(0xffffffffu, alpha != 1.0f)) {
 #pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t v[32];
-            tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
-            tc::tmem_wait_ld();
+        for (int c0 = 0; c0 < D; c0 += 32) {
+          uint32_t v[32];
+          tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
+          tc::tmem_wait_ld();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tc::tmem_st32(tmem + Geo::kColO + lane_base + c0, v);
-          }
-          tc::tmem_wait_st();
+          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+          tc::tmem_st32(tmem + Geo::kColO + lane_base + c0, v);
         }
       }
-#pragma unroll
-      for (int c0 = 0; c0 < kN; c0 += 8)
-        sts128(base + Geo::kOffP + tc::sw128_offset(kM, m, c0),
-               make_uint4(pw[c0 / 2], pw[c0 / 2 + 1], pw[c0 / 2 + 2], pw[c0 / 2 + 3]));
-      tc::fence_async_smem();
+      tc::tmem_wait_st();
       tc::fence_before_sync();
-      mbar_arrive(bar(Geo::kBarPFull));
+      mbar_arrive(bar(Geo::kBarPFull + st));
     }
     // ---- epilogue: O / l -> bf16 -------------------------------------------
     if (ok && T > 0)
-      ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarODone), (uint32_t)((T - 1) & 1), abort_flag));
+      ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarOFinal), 0u, abort_flag));
     // ok is warp-uniform here: the whole warp reads O (tcgen05.ld is a
-    // warp-collective instruction), only valid rows are stored.
+    // warp-collective instruction).  Each thread writes its row in bf16 to
+    // the (now idle) K ring, row-major with the 16-byte chunks of row m
+    // rotated by m mod 8; all warps then copy the tile out coalesced.
     if (ok) {
-      uint16_t* dst =
-          row_valid ? p.out + ((int64_t)(q0 + R / G) * p.heads_q + t.kv_head * G + R % G) * D : nullptr;
+      const uint32_t orow = base + Geo::kOffOStage + (uint32_t)(m * D * 2);
       if (T > 0) {
         tc::fence_after_sync();
         const float sc = (l_sum > 0.0f ? 1.0f / l_sum : 0.0f) *
@@ -612,23 +627,21 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
           uint32_t v[32];
           tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
           tc::tmem_wait_ld();
-          if (row_valid) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 o;
-              o.x = dev::pack_bf16x2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
-              o.y = dev::pack_bf16x2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
-              o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
-              o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
-              *reinterpret_cast<uint4*>(dst + c0 + e) = o;
-            }
+          for (int e = 0; e < 32; e += 8) {
+            uint4 o;
+            o.x = dev::pack_bf16x2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
+            o.y = dev::pack_bf16x2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
+            o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
+            o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
+            const int c = (c0 + e) / 8;
+            sts128(orow + (uint32_t)(((c ^ (m & 7)) << 4)), o);
           }
-          __syncwarp();
         }
-      } else if (row_valid) {
+      } else {
         // No key tile at all (an empty key range): the output row is zero.
 #pragma unroll 1
-        for (int c = 0; c < D; c += 8) *reinterpret_cast<uint4*>(dst + c) = make_uint4(0, 0, 0, 0);
+        for (int c = 0; c < D / 8; ++c) sts128(orow + (uint32_t)(c << 4), make_uint4(0, 0, 0, 0));
       }
     }
     // Order this warp's tensor-memory accesses before the teardown barrier.
@@ -637,10 +650,24 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
   }
 
   __syncthreads();
-  if (tid == 0 && *abort_flag) atomicExch(p.error_flag, 1);
+  const bool aborted = *abort_flag != 0u;
+  if (tid == 0 && aborted) atomicExch(p.error_flag, 1);
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Geo::kTmemCols);
+  }
+  // ---- O tile -> global, coalesced: lanes_per_row lanes write one row.
+  if (!aborted) {
+    constexpr int kLpr = D / 8;
+    constexpr int kRps = 32 / kLpr;
+    const int lane = tid & 31;
+    const int sub = lane / kLpr, c = lane % kLpr;
+    for (int r = warp * kRps + sub; r < t.nrows; r += (Geo::kThreads / 32) * kRps) {
+      const uint4 o = lds128(base + Geo::kOffOStage + (uint32_t)(r * D * 2 + ((c ^ (r & 7)) << 4)));
+      const int Rr = t.row0 + r;
+      *reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D +
+                                8 * c) = o;
+    }
   }
 }
 
