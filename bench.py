@@ -19,6 +19,7 @@ runs an independent replica (replicas only: the path has no exchange).
 from __future__ import annotations
 
 import argparse
+import hashlib
 import json
 import math
 import os
@@ -33,6 +34,32 @@ sys.path.insert(0, ROOT)
 
 L2_FLUSH_BYTES = 512 << 20
 FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustained": 1700.0}
+
+# DRAM bytes (read + write) per launch of the dominant kernel, from the ncu
+# captures summarised in profiles/; valid only while the kernel's sources
+# hash as they did when captured.
+PROFILED_TRAFFIC = {
+    2: {"bytes": 362.000896e6 + 5.402624e6, "profile": "profiles/splitkv_decode_decode_batch.md",
+         "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
+         "sha1": "664bb511280f94baf86230fc1ce898ccd6ae1bfd"},
+    3: {"bytes": 37.86496e6 + 0.621312e6, "profile": "profiles/prefill_attention_large_prefill.md",
+         "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
+         "sha1": "00bd3b7830be0bd10aed6852eec66d560f95127c"},
+}
+
+
+def profiled_traffic(workload: int):
+    """The captured DRAM traffic of this workload's dominant kernel, or None
+    when there is no capture or the kernel changed since."""
+    entry = PROFILED_TRAFFIC.get(workload)
+    if entry is None:
+        return None
+    m = hashlib.sha1()
+    csrc = os.path.join(os.path.dirname(os.path.abspath(__file__)), "int8_kv_cache_reshape_gb300", "csrc")
+    for f in entry["sources"]:
+        with open(os.path.join(csrc, f), "rb") as fh:
+            m.update(fh.read())
+    return entry["bytes"] if m.hexdigest() == entry["sha1"] else None
 
 
 def _peaks():
@@ -310,7 +337,8 @@ def run_gpu(args, rank, world, local):
     else:
         kernel = "split-KV decode attention (+ split merge)"
     roofline = {"bound": "hbm" if decode_metric else "tensor", "kernel": kernel,
-                "unit": "GB/s" if decode_metric else "TFLOP/s", "traffic": None,
+                "unit": "GB/s" if decode_metric else "TFLOP/s",
+                "traffic": profiled_traffic(args.workload) if args.kv_cache_dtype is None else None,
                 "peak_source": peaks_src}
     if decode_metric:
         achieved = kvb / (attn_avg * 1e-3) / 1e9
