@@ -7,6 +7,8 @@
 // cache element size.  Here every size comes from kvq_internal.h's constexpr
 // geometry, and the attention call refuses a schedule built for another
 // dtype, head count or head size.
+#include <cuda.h>
+#include <cudaTypedefs.h>
 #include <cuda_runtime.h>
 
 #include <algorithm>
@@ -50,6 +52,36 @@ struct kvq_sched {
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// The driver's tensor-map encoder, fetched once through the runtime (no
+// link against the driver library).
+PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = []() -> PFN_cuTensorMapEncodeTiled_v12000 {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault, &q) !=
+            cudaSuccess ||
+        q != cudaDriverEntryPointSuccess)
+      return nullptr;
+    return reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  }();
+  return fn;
+}
+
+// Maps of one cache for the prefill's bulk tensor copies: {row bytes, kv
+// heads, slots} with boxes {box0, 1, 16}.
+bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t row, int heads_kv, int64_t slots,
+                      uint32_t box0) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)heads_kv, (cuuint64_t)slots};
+  const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)row * (cuuint64_t)heads_kv};
+  const cuuint32_t box[3] = {box0, 1u, 16u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box, estr,
+             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
+             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
 
 int sm_count() {
   int dev = 0, sms = 0;
@@ -486,7 +518,17 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.v_scale = v_scale;
 
   if (!s->prefill.empty()) {
-    const int rc = kvq::launch_prefill(p, s->dtype, head_dim, (int64_t)s->prefill.size(), stream);
+    kvq::PrefillMaps maps;
+    std::memset(&maps, 0, sizeof(maps));
+    const int64_t row = kvq::row_bytes(s->dtype, head_dim);
+    const int64_t slots = num_blocks * (int64_t)block_size;
+    bool ok = encode_cache_map(&maps.k, key_cache, row, heads_kv, slots, (uint32_t)head_dim) &&
+              encode_cache_map(&maps.v, value_cache, row, heads_kv, slots, (uint32_t)head_dim);
+    if (ok && kvq::is_per_token_head(s->dtype))
+      ok = encode_cache_map(&maps.ks, key_cache, row, heads_kv, slots, 16u) &&
+           encode_cache_map(&maps.vs, value_cache, row, heads_kv, slots, 16u);
+    if (!ok) return KVQ_E_CUDA;
+    const int rc = kvq::launch_prefill(p, maps, s->dtype, head_dim, (int64_t)s->prefill.size(), stream);
     if (rc != KVQ_OK) return rc;
   }
   for (int cls = 0; cls < 2; ++cls) {

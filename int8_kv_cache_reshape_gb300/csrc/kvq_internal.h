@@ -11,6 +11,8 @@
 #include <cstddef>
 #include <cstdint>
 
+#include <cuda.h>  // CUtensorMap
+
 #include "../../include/kvq.h"
 
 #ifdef __CUDACC__
@@ -85,15 +87,25 @@ KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 
 // P in f16 pairs over the first half), Q (head_dim / 2 columns of f16
 // pairs); always 512.
 KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
-// Shared memory: 2 x K and 2 x V (keys x D f16 each), 2 x key / value
-// scales and key-valid flags, the 128 rows' Q scales, barriers; +1 KB for
-// 1024-byte alignment.  Q is staged through the K ring before it moves to
-// tensor memory.
+// Shared memory: 2 x K and 2 x V (keys x D f16 each); 2 x the K and V codes
+// (keys x D bytes each, as the tensor-memory-access unit delivers them) and
+// their 16-byte scale tails (per-token-head); 2 x key / value scales and
+// key-valid flags; the 128 rows' Q scales; barriers; +1 KB for 1024-byte
+// alignment.  Q and O are staged through the K ring.
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
   return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
-         (size_t)kPrefillStages * prefill_keys(head_dim) * (4 + 4 + 1) + kPrefillRows * 4 + 128 +
+         2 * (size_t)kPrefillStages * prefill_keys(head_dim) * (head_dim + 16) +
+         (size_t)kPrefillStages * prefill_keys(head_dim) * (4 + 4 + 1) + kPrefillRows * 4 + 192 +
          1024;
 }
+
+// Tensor maps of the paged caches for the prefill's bulk tensor copies: a
+// cache is a rank-3 byte tensor {row bytes, kv heads, slots}; the code maps
+// copy boxes of {head_dim, 1, 16 slots}, the scale-tail maps {16, 1, 16}
+// starting at byte head_dim (per-token-head only).
+struct alignas(64) PrefillMaps {
+  CUtensorMap k, v, ks, vs;
+};
 
 struct PrefillTile {
   int32_t req, kv_head, row0, nrows;
@@ -183,5 +195,6 @@ int launch_reshape_and_cache(const void* key, const void* value,
                              const int64_t* slot_mapping, int dtype,
                              float k_scale, float v_scale, void* stream);
 int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream);
-int launch_prefill(const AttnParams& p, int dtype, int head_dim, int64_t num_tiles, void* stream);
+int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
+                   int64_t num_tiles, void* stream);
 }  // namespace kvq

@@ -70,12 +70,16 @@ struct PrefillGeom {
   static constexpr int kTileBytes = kN * D * 2;                     // one K or V tile (f16)
   static constexpr int kOffK = 0;                                   // stages x K tile
   static constexpr int kOffV = kOffK + kStages * kTileBytes;        // stages x V tile
-  static constexpr int kOffSk = kOffV + kStages * kTileBytes;       // stages x kN f32
+  static constexpr int kOffCodeK = kOffV + kStages * kTileBytes;   // stages x kN x D code bytes
+  static constexpr int kOffCodeV = kOffCodeK + kStages * kN * D;    // stages x kN x D code bytes
+  static constexpr int kOffTailK = kOffCodeV + kStages * kN * D;    // stages x kN x 16 (scale tails)
+  static constexpr int kOffTailV = kOffTailK + kStages * kN * 16;   // stages x kN x 16
+  static constexpr int kOffSk = kOffTailV + kStages * kN * 16;      // stages x kN f32
   static constexpr int kOffSv = kOffSk + kStages * kN * 4;          // stages x kN f32
   static constexpr int kOffValid = kOffSv + kStages * kN * 4;       // stages x kN bytes
   static constexpr int kOffQScale = kOffValid + kStages * kN;       // kM f32: 2^-sh of each Q row
   static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
-  static constexpr int kBytes = kOffBar + 128;
+  static constexpr int kBytes = kOffBar + 192;
   static constexpr int kOffQStage = kOffK;  // Q (kM x D f16, swizzled) staged over the K ring
   static constexpr int kOffOStage = kOffK;  // O (kM x D bf16) staged over the K ring at the end
   static constexpr int kColO = 0;                 // O: D fp32 columns
@@ -84,7 +88,9 @@ struct PrefillGeom {
   static constexpr int kTmemCols = prefill_tmem_cols(D);
   static_assert(kColQ + D / 2 <= kTmemCols, "tensor memory: O + 2 S buffers + Q");
   static_assert(kM * D * 2 <= kStages * kTileBytes, "Q / O staging fits the K ring");
-  static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0, "1024-byte tiles");
+  static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0 && kOffCodeK % 1024 == 0 &&
+                    kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
+                "1024-byte operand tiles, 128-byte copy destinations");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
   // barrier slots (8 bytes each)
@@ -93,11 +99,14 @@ struct PrefillGeom {
   // one phase behind, so the epilogue (which may be several PVs ahead of
   // the last phase it saw) waits on a one-shot barrier for the last PV.
   static constexpr int kBarKFull = 0, kBarVFull = 2, kBarKvEmpty = 4, kBarSFull = 6, kBarPFull = 8,
-                       kBarODone = 10, kBarOFinal = 11, kBarDrain = 12, kNumBars = 13;
+                       kBarODone = 10, kBarOFinal = 11, kBarDrain = 12, kBarCodes = 13, kBarCodesFree = 15,
+                       kNumBars = 17;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
   static constexpr int kOffBadTile = kOffAbort + 4;             // stages x i32
-  static_assert(kOffBadTile + 4 * kStages <= kBytes, "flag space");
+  static constexpr int kOffChunkValid = kOffBadTile + 4 * kStages;  // stages x u32: 16-key chunks copied
+  static_assert(kOffChunkValid + 4 * kStages <= kBytes, "flag space");
+  static_assert(kN / 16 <= 32, "chunk mask");
 };
 
 __device__ __forceinline__ void sts128(uint32_t addr, uint4 v) {
@@ -110,6 +119,31 @@ __device__ __forceinline__ uint4 lds128(uint32_t addr) {
   asm volatile("ld.shared.v4.u32 {%0,%1,%2,%3}, [%4];" : "=r"(v.x), "=r"(v.y), "=r"(v.z), "=r"(v.w)
                : "r"(addr));
   return v;
+}
+
+// One lane of the (converged) warp, the same one on every lane's view.
+__device__ __forceinline__ bool elect_one() {
+  uint32_t pred;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "elect.sync _|p, 0xffffffff;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(pred));
+  return pred != 0;
+}
+
+// Bulk tensor copy of a {x, y, z} box of a rank-3 tensor map into shared
+// memory, completing on an mbarrier's transaction count.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y, int z,
+                                            uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1, {%2, %3, %4}], [%5];"
+      :: "r"(dst), "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar) : "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.release.cta.shared::cta.b64 _, [%0], %1;" :: "r"(bar), "r"(bytes)
+               : "memory");
 }
 
 __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
@@ -140,7 +174,8 @@ __device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
 }
 
 template <int DT, int D>
-__global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(const AttnParams p) {
+__global__ void __launch_bounds__(kPrefillThreads, 1)
+    prefill_attention_kernel(const AttnParams p, const __grid_constant__ PrefillMaps maps) {
   using Geo = PrefillGeom<DT, D>;
   constexpr int kM = Geo::kM, kN = Geo::kN;
   extern __shared__ uint8_t smem_raw[];
@@ -170,6 +205,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
       tc::mbar_init(bar(Geo::kBarKvEmpty + s), 1);
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
       tc::mbar_init(bar(Geo::kBarPFull + s), 128);
+      tc::mbar_init(bar(Geo::kBarCodes + s), 1);
+      tc::mbar_init(bar(Geo::kBarCodesFree + s), Geo::kConv);
       bad_tile[s] = -1;
     }
     tc::mbar_init(bar(Geo::kBarODone), 1);
@@ -183,78 +220,101 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
     tc::tmem_relinquish();
   }
 
-  // ---- converter state (used by warps 1-3, 8-11)
+  // ---- converter state (warps 1-3, 8-11); converter 0 also issues the bulk
+  // tensor copies of each tile's codes.
+  const bool is_conv = (warp >= 1 && warp < 4) || warp >= 8;
   const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
   const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
-  const int64_t row_stride = (int64_t)p.heads_kv * Geo::kRow;
-  const uint8_t* kcache = p.key_cache + (int64_t)t.kv_head * Geo::kRow;
-  const uint8_t* vcache = p.value_cache + (int64_t)t.kv_head * Geo::kRow;
   float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
   float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
   uint8_t* kvalid = sm + Geo::kOffValid;
+  volatile uint32_t* chunk_valid = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffChunkValid);
   // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
   // floor((2^32 - 1) / B)) is q or q - 1 for every 32-bit j.
   const uint32_t bsz = (uint32_t)p.block_size;
   const uint32_t bdiv = 0xFFFFFFFFu / bsz;
-  // Byte offset of logical key j's row in either cache, or -1 when its
-  // block is missing.
-  auto key_off = [&](int j) -> int64_t {
-    uint32_t q = __umulhi((uint32_t)j, bdiv);
-    uint32_t r = (uint32_t)j - q * bsz;
-    if (r >= bsz) {
-      ++q;
-      r -= bsz;
-    }
-    const int blk = btab[q];
-    if (blk < 0 || (int64_t)blk >= p.num_blocks) return -1;
-    return ((int64_t)blk * bsz + r) * row_stride;
-  };
-  // A unit is (key n, 32 dims pc); 8 consecutive threads take 8
-  // consecutive keys, so the swizzled 16-byte stores hit 8 bank groups.
-  constexpr int kUnits = kN * (D / 32);
-  constexpr int kSlots = (kUnits + Geo::kConv - 1) / Geo::kConv;
-  uint4 kraw[kSlots][2], vraw[kSlots][2];  // the next tile's codes
-  float kscale[kSlots], vscale[kSlots];
-  uint32_t kdead = 0, kmiss = 0;  // per slot: key in range without a block / no row
-  auto load_tile = [&](int j) {
+  // Tile j's 16-key chunks: their table entries are loaded one tile ahead
+  // (fetch_chunks, whose loads nobody waits for until the copies are issued),
+  // then resolved to first slots and a mask of the chunks with a key in the
+  // tile's range and a block (resolve_chunks).
+  constexpr int kChunks = kN / 16;
+  auto fetch_chunks = [&](int j, int (&blk)[kChunks], uint32_t (&off)[kChunks]) {
     const int kv0 = kv_first + j * kN;
-    kdead = kmiss = 0;
 #pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      const int u = ctid + i * Geo::kConv;
-      kraw[i][0] = kraw[i][1] = vraw[i][0] = vraw[i][1] = make_uint4(0, 0, 0, 0);
-      kscale[i] = vscale[i] = 0.0f;
-      if (u < kUnits) {
-        const int n = u % kN, pc = u / kN;
-        const int jj = kv0 + n;
-        const bool in_range = jj >= t.kv_lo && jj < t.kv_hi;
-        const int64_t off = in_range ? key_off(jj) : -1;
-        if (off >= 0) {
-          const uint8_t* kr = kcache + off;
-          const uint8_t* vr = vcache + off;
-          kraw[i][0] = *reinterpret_cast<const uint4*>(kr + 32 * pc);
-          kraw[i][1] = *reinterpret_cast<const uint4*>(kr + 32 * pc + 16);
-          vraw[i][0] = *reinterpret_cast<const uint4*>(vr + 32 * pc);
-          vraw[i][1] = *reinterpret_cast<const uint4*>(vr + 32 * pc + 16);
-          if constexpr (Geo::kPth) {
-            if (pc == 0) {
-              kscale[i] = *reinterpret_cast<const float*>(kr + D);
-              vscale[i] = *reinterpret_cast<const float*>(vr + D);
-            }
-          }
-        } else {
-          kmiss |= 1u << i;
-          if (in_range) kdead |= 1u << i;
+    for (int c = 0; c < kChunks; ++c) {
+      const int j0 = kv0 + 16 * c;
+      blk[c] = -1;
+      off[c] = 0;
+      if (j0 + 16 > t.kv_lo && j0 < t.kv_hi) {
+        uint32_t q = __umulhi((uint32_t)j0, bdiv);
+        uint32_t r = (uint32_t)j0 - q * bsz;
+        if (r >= bsz) {
+          ++q;
+          r -= bsz;
+        }
+        blk[c] = btab[q];
+        off[c] = r;
+      }
+    }
+  };
+  auto resolve_chunks = [&](const int (&blk)[kChunks], const uint32_t (&off)[kChunks],
+                            int (&slot0)[kChunks], uint32_t& valid) {
+    valid = 0;
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      slot0[c] = 0;
+      if (blk[c] >= 0 && (int64_t)blk[c] < p.num_blocks) {
+        valid |= 1u << c;
+        slot0[c] = blk[c] * (int)bsz + (int)off[c];  // < num_blocks * block_size < 2^31
+      }
+    }
+  };
+  // Copies of those chunks into code stage j & 1: K and V codes and, per
+  // token-head, the scale tails; one arrival with the byte count.
+  auto issue_codes = [&](int j, const int (&slot0)[kChunks], uint32_t valid, bool leader) {
+    const int st = j & 1;
+    constexpr uint32_t kChunkBytes = 2u * 16u * D + (Geo::kPth ? 2u * 16u * 16u : 0u);
+    const uint32_t cb = bar(Geo::kBarCodes + st);
+    if (leader) {
+      chunk_valid[st] = valid;
+      mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * kChunkBytes);
+    }
+#pragma unroll
+    for (int c = 0; c < kChunks; ++c) {
+      if (leader && ((valid >> c) & 1u)) {
+        const uint32_t off = (uint32_t)(st * kN + 16 * c);
+        tma_load_3d(base + Geo::kOffCodeK + off * D, &maps.k, 0, t.kv_head, slot0[c], cb);
+        tma_load_3d(base + Geo::kOffCodeV + off * D, &maps.v, 0, t.kv_head, slot0[c], cb);
+        if constexpr (Geo::kPth) {
+          tma_load_3d(base + Geo::kOffTailK + off * 16, &maps.ks, D, t.kv_head, slot0[c], cb);
+          tma_load_3d(base + Geo::kOffTailV + off * 16, &maps.vs, D, t.kv_head, slot0[c], cb);
         }
       }
     }
   };
-  auto store_rows = [&](uint32_t tile, const uint4 (&c)[2], int n, int pc) {
-    sts128(tile + tc::sw128_offset(kN, n, 32 * pc), codes8_to_f16<DT>(c[0].x, c[0].y));
-    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 8), codes8_to_f16<DT>(c[0].z, c[0].w));
-    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 16), codes8_to_f16<DT>(c[1].x, c[1].y));
-    sts128(tile + tc::sw128_offset(kN, n, 32 * pc + 24), codes8_to_f16<DT>(c[1].z, c[1].w));
+  // The MMA thread issues the copies: tiles 0 and 1 now, then tile j + 2 once
+  // every converter has released code stage j & 1; the table entries of the
+  // next tile to copy are read ahead.
+  int nt = 0;  // tiles whose copies are issued
+  int nx_blk[kChunks];
+  uint32_t nx_off[kChunks];
+  // Run by the whole of warp 0 (uniform state); the leader issues.
+  auto issue_next = [&](bool leader) {  // copies of tile nt (entries fetched), fetch tile nt + 1
+    int slot0[kChunks];
+    uint32_t valid;
+    resolve_chunks(nx_blk, nx_off, slot0, valid);
+    issue_codes(nt, slot0, valid, leader);
+    ++nt;
+    if (nt < T) fetch_chunks(nt, nx_blk, nx_off);
   };
+  __syncthreads();  // barriers initialised
+  if (warp == 0 && T > 0) {
+    const bool leader = elect_one();
+    fetch_chunks(0, nx_blk, nx_off);
+    issue_next(leader);
+    if (nt < T) issue_next(leader);
+    __syncwarp();
+  }
 
   // ---- Q tile -> staging (swizzled rows), all warps: lanes_per_row lanes
   // hold one row (16 bytes each, coalesced); the row's largest exponent
@@ -330,49 +390,67 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
 
   if (warp == 0) {
     // ======================= MMA issuer ========================================
-    if (tid == 0 && T > 0) {
+    // The whole warp runs the loop with warp-uniform state (descriptors and
+    // counters stay in the uniform datapath); one elected lane issues.
+    if (T > 0) {
+      const bool leader = elect_one();
       constexpr uint32_t idesc_s = tc::idesc_f16(kM, kN);
       constexpr uint32_t idesc_o = tc::idesc_f16(kM, D) | tc::kBMajorMN;
       auto issue_s = [&](int j) {
         const int st = j & 1;
-        const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes);
+        // (descriptor start addresses are in 16-byte units in the low bits)
+        const uint64_t d0 = tc::desc_sw128(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes));
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
-          tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
-                     tc::desc_sw128(kbase + boff), idesc_s, kk > 0 ? 1u : 0u);
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
+            tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
+                       d0 + (uint64_t)(boff >> 4), idesc_s, kk > 0 ? 1u : 0u);
+          }
+          tc::mma_commit(bar(Geo::kBarSFull + st));
         }
-        tc::mma_commit(bar(Geo::kBarSFull + st));
+        __syncwarp();
       };
       auto issue_pv = [&](int j) {
         const int st = j & 1;
-        const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes);
+        const uint64_t d0 =
+            tc::desc_sw128_mn(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), kN * 128, 1024);
+        if (leader) {
 #pragma unroll
-        for (int kk = 0; kk < kN / 16; ++kk)
-          tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
-                     tc::desc_sw128_mn(vbase + (uint32_t)(kk * 2048), kN * 128, 1024), idesc_o,
-                     (j > 0 || kk > 0) ? 1u : 0u);
-        tc::mma_commit(bar(Geo::kBarODone));
-        tc::mma_commit(bar(Geo::kBarKvEmpty + st));
-        if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
+          for (int kk = 0; kk < kN / 16; ++kk)
+            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
+                       d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          tc::mma_commit(bar(Geo::kBarODone));
+          tc::mma_commit(bar(Geo::kBarKvEmpty + st));
+          if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
+        }
+        __syncwarp();
       };
       // S(j) needs K(j) and PV(j-2) issued (P(j-2) shares its buffer; the
       // tensor core runs one thread's MMAs in order).  PV(j) needs P(j) and
-      // V(j).  Issue whichever is ready.
+      // V(j).  Issue whichever is ready: non-blocking tests (this warp polls
+      // several barriers), lane 0's results decide for the warp.
+      auto ready = [&](bool cond, uint32_t b, uint32_t parity) -> bool {
+        const bool r = cond && tc::mbar_test_wait(b, parity);
+        return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
+      };
       int ns = 0, npv = 0;
       bool ok = true;
       long long t_idle = clock64();
       while (npv < T) {
         bool progressed = false;
-        if (ns < T && ns <= npv + 1 &&
-            tc::mbar_try_wait(bar(Geo::kBarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1))) {
+        if (ready(nt < T, bar(Geo::kBarCodesFree + (nt & 1)), (uint32_t)(((nt >> 1) - 1) & 1))) {
+          issue_next(leader);
+          progressed = true;
+        }
+        if (ready(ns < T && ns <= npv + 1, bar(Geo::kBarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1))) {
           tc::fence_after_sync();
           issue_s(ns);
           ++ns;
           progressed = true;
         }
-        if (npv < ns && tc::mbar_try_wait(bar(Geo::kBarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
-            tc::mbar_try_wait(bar(Geo::kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+        if (ready(npv < ns, bar(Geo::kBarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
+            ready(true, bar(Geo::kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
           tc::fence_after_sync();
           issue_pv(npv);
           ++npv;
@@ -381,62 +459,102 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
         if (progressed) {
           t_idle = clock64();
         } else {
-          if (*abort_flag) {
-            ok = false;
-            break;
-          }
-          if (clock64() - t_idle > 2000000000LL) {
-            *abort_flag = 1u;
+          const bool give_up = __shfl_sync(0xffffffffu, (*abort_flag != 0u) ? 1 : 0, 0) != 0;
+          const bool timeout = __shfl_sync(0xffffffffu, (clock64() - t_idle > 2000000000LL) ? 1 : 0, 0) != 0;
+          if (give_up || timeout) {
+            if (timeout && leader) *abort_flag = 1u;
             ok = false;
             break;
           }
         }
       }
-      if (!ok) {
-        // Drain whatever was issued before the tensor memory is freed.
+      if (!ok && leader) {
+        // Drain whatever was issued before the tensor memory is freed, and
+        // let the last copies (at most two tiles in flight) land.
         tc::mma_commit(bar(Geo::kBarDrain));
         (void)tc::mbar_wait(bar(Geo::kBarDrain), 0u, 200000000LL);
+        for (int j = nt >= 2 ? nt - 2 : 0; j < nt; ++j)
+          (void)tc::mbar_wait(bar(Geo::kBarCodes + (j & 1)), (uint32_t)((j >> 1) & 1), 200000000LL);
       }
     }
     __syncwarp();
   } else if (!is_softmax) {
     // ======================= converters ========================================
-    if (T > 0) load_tile(0);
+    // A unit is (key n, 16 codes pc): consecutive threads take consecutive
+    // 16-byte pieces of a code row (conflict-free reads).  The two 16-byte f16
+    // chunks go out in the order that keeps the 8 lanes of a quarter-warp on
+    // 8 bank groups (lanes in odd 64-dim blocks store their odd chunk first).
+    // A unit's offsets do not change from tile to tile.
+    constexpr int kPieces = D / 16;
+    constexpr int kUnits = kN * kPieces;
+    constexpr int kSlots = (kUnits + Geo::kConv - 1) / Geo::kConv;
+    uint32_t code_off[kSlots], st_first[kSlots], st_second[kSlots];
+    int unit_key[kSlots];
+    uint32_t odd_mask = 0;
+#pragma unroll
+    for (int i = 0; i < kSlots; ++i) {
+      const int u = min(ctid + i * Geo::kConv, kUnits - 1);
+      const int n = u / kPieces, pc = u % kPieces;
+      const bool odd = (pc >> 2) & 1;
+      const uint32_t a_lo = tc::sw128_offset(kN, n, 16 * pc), a_hi = tc::sw128_offset(kN, n, 16 * pc + 8);
+      code_off[i] = (uint32_t)(n * D + 16 * pc);
+      st_first[i] = odd ? a_hi : a_lo;
+      st_second[i] = odd ? a_lo : a_hi;
+      unit_key[i] = n;
+      odd_mask |= (odd ? 1u : 0u) << i;
+    }
+    auto convert = [&](int j, uint32_t tile, uint32_t codes, bool whole) {
+      const int kv0 = kv_first + j * kN;
+      const uint32_t valid = chunk_valid[j & 1];
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        if (ctid + i * Geo::kConv < kUnits) {
+          uint4 c = make_uint4(0, 0, 0, 0);
+          const int n = unit_key[i];
+          if (whole || (((valid >> (n >> 4)) & 1u) && kv0 + n >= t.kv_lo && kv0 + n < t.kv_hi))
+            c = lds128(codes + code_off[i]);
+          const bool odd = (odd_mask >> i) & 1u;
+          sts128(tile + st_first[i], codes8_to_f16<DT>(odd ? c.z : c.x, odd ? c.w : c.y));
+          sts128(tile + st_second[i], codes8_to_f16<DT>(odd ? c.x : c.z, odd ? c.y : c.w));
+        }
+      }
+    };
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
+      const int kv0 = kv_first + j * kN;
+      if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodes + st), (uint32_t)((j >> 1) & 1),
+                                                 abort_flag)))
+        break;
       if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarKvEmpty + st),
                                                             (uint32_t)(((j >> 1) - 1) & 1), abort_flag)))
         break;
-      const uint32_t kbase = base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes);
-      const uint32_t vbase = base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes);
-#pragma unroll
-      for (int i = 0; i < kSlots; ++i) {
-        const int u = ctid + i * Geo::kConv;
-        if (u < kUnits) {
-          const int n = u % kN, pc = u / kN;
-          store_rows(kbase, kraw[i], n, pc);
-          if (pc == 0) {
-            kvalid[st * kN + n] = (kmiss >> i) & 1u ? 0 : 1;
-            if constexpr (Geo::kPth) sk[st * kN + n] = kscale[i];
-            if ((kdead >> i) & 1u) bad_tile[st] = j;
-          }
+      const uint32_t valid = chunk_valid[st];
+      // every key of the tile in range and copied: no per-unit checks
+      const bool whole = valid == (1u << kChunks) - 1u && kv0 >= t.kv_lo && kv0 + kN <= t.kv_hi;
+      // per-key flags and scales: one thread per key
+      for (int n = ctid; n < kN; n += Geo::kConv) {
+        const int jj = kv0 + n;
+        const bool in_range = jj >= t.kv_lo && jj < t.kv_hi;
+        const bool live = in_range && ((valid >> (n >> 4)) & 1u);
+        kvalid[st * kN + n] = live ? 1 : 0;
+        if (in_range && !live) bad_tile[st] = j;
+        if constexpr (Geo::kPth) {
+          const uint32_t off = (uint32_t)((st * kN + n) * 16);
+          sk[st * kN + n] = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
+          sv[st * kN + n] = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
         }
       }
+      convert(j, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
+              base + Geo::kOffCodeK + (uint32_t)(st * kN * D), whole);
       tc::fence_async_smem();
       mbar_arrive(bar(Geo::kBarKFull + st));
-#pragma unroll
-      for (int i = 0; i < kSlots; ++i) {
-        const int u = ctid + i * Geo::kConv;
-        if (u < kUnits) {
-          const int n = u % kN, pc = u / kN;
-          store_rows(vbase, vraw[i], n, pc);
-          if constexpr (Geo::kPth)
-            if (pc == 0) sv[st * kN + n] = vscale[i];
-        }
-      }
+      convert(j, base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes),
+              base + Geo::kOffCodeV + (uint32_t)(st * kN * D), whole);
       tc::fence_async_smem();
       mbar_arrive(bar(Geo::kBarVFull + st));
-      if (j + 1 < T) load_tile(j + 1);
+      // This thread is done with code stage st: the MMA thread refills it
+      // with tile j + 2 once every converter is.
+      mbar_arrive(bar(Geo::kBarCodesFree + st));
     }
     __syncwarp();
   } else {
@@ -672,25 +790,27 @@ __global__ void __launch_bounds__(kPrefillThreads, 1) prefill_attention_kernel(c
 }
 
 template <int DT, int D>
-int launch_prefill_instance(const AttnParams& p, int64_t num_tiles, cudaStream_t stream) {
+int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_t num_tiles,
+                            cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes(D);
   auto kern = prefill_attention_kernel<DT, D>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
-  kern<<<(unsigned)num_tiles, kPrefillThreads, smem, stream>>>(p);
+  kern<<<(unsigned)num_tiles, kPrefillThreads, smem, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 
 template <int D>
-int launch_prefill_d(const AttnParams& p, int dtype, int64_t num_tiles, cudaStream_t stream) {
+int launch_prefill_d(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+                     cudaStream_t stream) {
   switch (dtype) {
-    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D>(p, num_tiles, stream);
-    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D>(p, num_tiles, stream);
+    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D>(p, maps, num_tiles, stream);
+    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D>(p, maps, num_tiles, stream);
     case KVQ_INT8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D>(p, num_tiles, stream);
+      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
     case KVQ_FP8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D>(p, num_tiles, stream);
+      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
     default:
       return KVQ_E_UNSUPPORTED;
   }

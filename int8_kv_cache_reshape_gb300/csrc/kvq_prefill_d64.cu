@@ -2,7 +2,8 @@
 #include "kvq_prefill.cuh"
 
 namespace kvq {
-int launch_prefill_d64(const AttnParams& p, int dtype, int64_t num_tiles, void* stream) {
-  return launch_prefill_d<64>(p, dtype, num_tiles, static_cast<cudaStream_t>(stream));
+int launch_prefill_d64(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+                       void* stream) {
+  return launch_prefill_d<64>(p, maps, dtype, num_tiles, static_cast<cudaStream_t>(stream));
 }
 }  // namespace kvq
