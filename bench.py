@@ -41,10 +41,10 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 PROFILED_TRAFFIC = {
     2: {"bytes": 362.000896e6 + 5.402624e6, "profile": "profiles/splitkv_decode_decode_batch.md",
          "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "664bb511280f94baf86230fc1ce898ccd6ae1bfd"},
-    3: {"bytes": 37.86496e6 + 0.621312e6, "profile": "profiles/prefill_attention_large_prefill.md",
+         "sha1": "a7763bcf8af7b2995e0506000ed312235a4528e0"},
+    3: {"bytes": 37.85984e6 + 0.655616e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "00bd3b7830be0bd10aed6852eec66d560f95127c"},
+         "sha1": "b30d5205b969c9f064d5c2e2966d28410256f597"},
 }
 
 

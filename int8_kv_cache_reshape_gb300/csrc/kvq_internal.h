@@ -88,7 +88,7 @@ KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 
 // pairs); always 512.
 KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
 // Shared memory: 2 x K and 2 x V (keys x D f16 each); 2 x the K and V codes
-// (keys x D bytes each, as the tensor-memory-access unit delivers them) and
+// (keys x D bytes each, as the bulk tensor copies deliver them) and
 // their 16-byte scale tails (per-token-head); 2 x key / value scales and
 // key-valid flags; the 128 rows' Q scales; barriers; +1 KB for 1024-byte
 // alignment.  Q and O are staged through the K ring.
