@@ -143,7 +143,8 @@ KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
  *   workspace_bytes         receives the scratch size the attention call
  *                           needs (may be 0); must not be NULL.
  * The schedule holds a host copy and one device copy of its plan, made on
- * the current device (a blocking upload).  Requests with at most 16
+ * the current device (one blocking upload from pinned staging into a pooled
+ * device buffer).  Requests with at most 16
  * (query, head) rows per kv head (decodes) form row tiles whose 16-token KV
  * chunks are cut into equal contiguous segments, one per warp, so long
  * contexts are split along the KV axis and merged.  Requests with more rows
@@ -230,9 +231,11 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
     int block_table_stride, int block_size, int64_t num_blocks, float sm_scale, int causal,
     int window, float soft_cap, float k_scale, float v_scale, void* out, void* stream);
 
-/* Free a schedule (NULL is a no-op).  Its device work list is released
- * with cudaFree, which waits for the device: call it after the attention
- * calls that use it have been enqueued. */
+/* Free a schedule (NULL is a no-op).  Its device work list goes back to a
+ * small library pool that later schedules on the same device reuse (no
+ * cudaFree / cudaMalloc per step), so destroy a schedule only once the
+ * attention calls that use it have completed on the device, as for any
+ * memory the caller frees. */
 KVQ_API void kvq_sched_destroy(kvq_sched_t* sched);
 
 /* Summary of a schedule, for tests and benchmarks. */

@@ -132,7 +132,8 @@ splitkv_decode_kernel(const AttnParams p) {
   const int gw = blockIdx.x * kDecodeWarps + warp;
   const int64_t seg0 = (int64_t)gw * p.num_chunks / p.num_warps;
   const int n = (int)((int64_t)(gw + 1) * p.num_chunks / p.num_warps - seg0);
-  const ChunkRef* refs = p.chunks + seg0;
+  // The piece of each position: the warp's first piece comes from the
+  // schedule; a lane's cursor only moves forward as its positions grow.
   uint4* records = reinterpret_cast<uint4*>(smem + warp * Geo::kWarpSmem);
 
   const uint8_t* kbase = p.key_cache;
@@ -157,27 +158,34 @@ splitkv_decode_kernel(const AttnParams p) {
   // 0-15 for 16 positions at a time in three steps a few chunks apart so
   // that the dependent loads (chunk ref -> piece -> block table) overlap
   // with the streaming.
-  ChunkRef f_ref = {-1, 0};
+  int f_piece = -1, f_chunk = 0;
+  int cur_piece = n > 0 ? p.warp_piece[gw] : 0;
   int4 f_pc = make_int4(0, 0, 0, 0);  // req, kv_head, any_lo, any_hi
   int f_blk = -1;
   auto fill_load_ref = [&](int pos) {
-    f_ref.piece = -1;
-    if (lane < 16 && pos + lane < n) f_ref = refs[pos + lane];
+    f_piece = -1;
+    if (lane < 16 && pos + lane < n) {
+      const int64_t flat = seg0 + pos + lane;
+      while (cur_piece + 1 < p.num_pieces && (int64_t)__ldg(&p.pieces[cur_piece + 1].flat0) <= flat)
+        ++cur_piece;
+      f_piece = cur_piece;
+      f_chunk = __ldg(&p.pieces[cur_piece].chunk0) + (int)(flat - __ldg(&p.pieces[cur_piece].flat0));
+    }
   };
   auto fill_load_piece = [&]() {
-    if (f_ref.piece >= 0) {
-      const DecodePiece* pc = p.pieces + f_ref.piece;
+    if (f_piece >= 0) {
+      const DecodePiece* pc = p.pieces + f_piece;
       f_pc = make_int4(pc->req, pc->kv_head, pc->any_lo, pc->any_hi);
     }
   };
   auto fill_load_block = [&]() {
     f_blk = -1;
-    if (f_ref.piece >= 0)
-      f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_ref.chunk / cpb];
+    if (f_piece >= 0)
+      f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_chunk / cpb];
   };
   auto fill_store = [&](int pos) {
     if (lane < 16 && pos + lane < n) {
-      const int chunk = f_ref.chunk;
+      const int chunk = f_chunk;
       const int tok0 = chunk * kChunkTokens;
       const bool ok = f_blk >= 0 && (int64_t)f_blk < p.num_blocks;
       const int slot0 = ok ? f_blk * p.block_size + (chunk % cpb) * kChunkTokens : -1;
@@ -185,7 +193,7 @@ splitkv_decode_kernel(const AttnParams p) {
       const int hi = min(max(f_pc.w - tok0, 0), kChunkTokens);
       const uint32_t live = ok ? (((1u << hi) - 1u) & ~((1u << lo) - 1u)) : 0u;
       records[(pos + lane) % kRecordRing] =
-          make_uint4((uint32_t)slot0, (uint32_t)tok0, (uint32_t)f_ref.piece,
+          make_uint4((uint32_t)slot0, (uint32_t)tok0, (uint32_t)f_piece,
                      live | ((uint32_t)f_pc.y << 16));
     }
   };

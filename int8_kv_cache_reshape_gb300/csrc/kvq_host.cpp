@@ -15,12 +15,12 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <mutex>
 #include <new>
 #include <vector>
 
 #include "kvq_internal.h"
 
-using kvq::ChunkRef;
 using kvq::DecodePiece;
 using kvq::MergeItem;
 using kvq::PrefillTile;
@@ -28,8 +28,10 @@ using kvq::PrefillTile;
 // One launch of the split-KV decode kernel: the tiles with one 8-row n-tile
 // (class 0) or two (class 1).
 struct DecodeLaunch {
-  int64_t chunk_off = 0;   // first entry of the launch's flat chunk sequence
-  int64_t num_chunks = 0;  // its length
+  int64_t piece_off = 0;   // the launch's first piece
+  int64_t num_pieces = 0;
+  int64_t warp_off = 0;    // its first entry of the per-warp first-piece table
+  int64_t num_chunks = 0;  // length of its flat chunk sequence
   int num_warps = 0;       // warps the sequence is cut among
 };
 
@@ -38,20 +40,78 @@ struct kvq_sched {
   int device;
   int64_t total_q;
   std::vector<DecodePiece> pieces;
-  std::vector<ChunkRef> chunks;
+  std::vector<int32_t> warp_piece;  // per launch, per warp: the piece of its first chunk
   std::vector<MergeItem> merges;
   std::vector<PrefillTile> prefill;
   DecodeLaunch launch[2];
   int64_t num_tiles, max_splits, partial_rows;
   int32_t max_chunk;  // highest 16-token chunk index any tile reads
   size_t workspace_bytes;
-  void* d_buf;  // device copy: pieces, chunks, merges, merge counters, prefill tiles, error word
-  size_t d_pieces_off, d_chunks_off, d_merges_off, d_counters_off, d_prefill_off, d_error_off;
+  void* d_buf;  // device copy: pieces, warp table, merges, merge counters, prefill tiles, error word
+  size_t d_buf_bytes;
+  size_t d_pieces_off, d_warps_off, d_merges_off, d_counters_off, d_prefill_off, d_error_off;
 };
 
 namespace {
 
 bool aligned(const void* p, size_t a) { return (reinterpret_cast<uintptr_t>(p) % a) == 0; }
+
+// Device buffers of destroyed schedules, kept for the next schedules (a
+// serving loop plans every step; cudaMalloc / cudaFree there would cost more
+// than the planning).  Bounded; sizes are powers of two from 64 KiB.
+struct PooledBuf {
+  int device;
+  size_t bytes;
+  void* ptr;
+};
+std::mutex g_pool_mutex;
+std::vector<PooledBuf> g_pool;
+constexpr size_t kPoolMax = 16;
+
+size_t pool_size_class(size_t bytes) {
+  size_t c = 64 * 1024;
+  while (c < bytes) c <<= 1;
+  return c;
+}
+
+void* pool_get(int device, size_t bytes, size_t* got) {
+  const size_t want = pool_size_class(bytes);
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    for (size_t i = 0; i < g_pool.size(); ++i) {
+      if (g_pool[i].device == device && g_pool[i].bytes >= want) {
+        void* p = g_pool[i].ptr;
+        *got = g_pool[i].bytes;
+        g_pool.erase(g_pool.begin() + (std::ptrdiff_t)i);
+        return p;
+      }
+    }
+  }
+  void* p = nullptr;
+  if (cudaMalloc(&p, want) != cudaSuccess) {
+    cudaGetLastError();
+    return nullptr;
+  }
+  *got = want;
+  return p;
+}
+
+// Pinned host staging for the plan's upload (the upload is synchronous, so
+// one buffer serves every call in turn).
+std::mutex g_stage_mutex;
+void* g_stage = nullptr;
+size_t g_stage_bytes = 0;
+
+void pool_put(int device, void* ptr, size_t bytes) {
+  {
+    std::lock_guard<std::mutex> lock(g_pool_mutex);
+    if (g_pool.size() < kPoolMax) {
+      g_pool.push_back(PooledBuf{device, bytes, ptr});
+      return;
+    }
+  }
+  cudaFree(ptr);
+}
 
 // The driver's tensor-map encoder, fetched once through the runtime (no
 // link against the driver library).
@@ -167,13 +227,7 @@ int kvq_reshape_and_cache(const void* key, const void* value, int64_t num_tokens
 
 void kvq_sched_destroy(kvq_sched_t* s) {
   if (!s) return;
-  if (s->d_buf) {
-    int cur = -1;
-    cudaGetDevice(&cur);
-    if (cur != s->device) cudaSetDevice(s->device);
-    cudaFree(s->d_buf);
-    if (cur != s->device && cur >= 0) cudaSetDevice(cur);
-  }
+  if (s->d_buf) pool_put(s->device, s->d_buf, s->d_buf_bytes);
   delete s;
 }
 
@@ -288,9 +342,18 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   if (const char* env = std::getenv("KVQ_DECODE_WARPS")) forced = std::atoll(env);
   s->partial_rows = 0;
   s->max_splits = 0;
+  struct Cut {
+    int64_t warp, lo, hi;
+  };
+  std::vector<int64_t> seg;
+  std::vector<Cut> cuts;
+  cuts.reserve(64);
+  s->pieces.reserve(tiles[0].size() + tiles[1].size() + 2 * 4096);
+  s->merges.reserve(tiles[0].size() + tiles[1].size());
   for (int cls = 0; cls < 2; ++cls) {
     DecodeLaunch& dl = s->launch[cls];
-    dl.chunk_off = (int64_t)s->chunks.size();
+    dl.piece_off = (int64_t)s->pieces.size();
+    dl.warp_off = (int64_t)s->warp_piece.size();
     int64_t T = 0;
     for (const Tile& t : tiles[cls]) T += t.c_hi - t.c_lo;
     dl.num_chunks = T;
@@ -300,19 +363,33 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     if (forced > 0) ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(forced, kvq::kDecodeWarps), ceil_div(T, kvq::kDecodeWarps)));
     const int64_t W = ctas * kvq::kDecodeWarps;
     dl.num_warps = (int)W;
-    auto seg_start = [&](int64_t w) { return w * T / W; };
+    s->warp_piece.resize((size_t)(dl.warp_off + W), 0);
+    // Segment starts floor(w T / W), incrementally (no divides in the loop).
+    seg.resize((size_t)W + 1);
+    {
+      const int64_t qt = T / W, rt = T % W;
+      int64_t q = 0, r = 0;
+      for (int64_t w = 0; w <= W; ++w) {
+        seg[(size_t)w] = q;
+        q += qt;
+        r += rt;
+        if (r >= W) {
+          r -= W;
+          ++q;
+        }
+      }
+    }
+    // Tiles and warps in one pass: w is the warp whose segment holds F.
     int64_t F = 0;  // flat position of the current tile's first chunk
+    int64_t w = 0;
     for (const Tile& t : tiles[cls]) {
       const int64_t nt = t.c_hi - t.c_lo;
-      // Warps whose segments overlap [F, F + nt).
-      int64_t w0 = (F * W) / T;
-      while (w0 > 0 && seg_start(w0) > F) --w0;
-      while (seg_start(w0 + 1) <= F) ++w0;
-      std::vector<std::pair<int64_t, int64_t>> cuts;  // [lo, hi) flat ranges
-      for (int64_t w = w0; w < W && seg_start(w) < F + nt; ++w) {
-        const int64_t lo = std::max<int64_t>(F, seg_start(w));
-        const int64_t hi = std::min<int64_t>(F + nt, seg_start(w + 1));
-        if (hi > lo) cuts.push_back({lo, hi});
+      while (w + 1 < W && seg[(size_t)w + 1] <= F) ++w;
+      cuts.clear();  // (warp, [lo, hi)) per piece
+      for (int64_t ww = w; ww < W && seg[(size_t)ww] < F + nt; ++ww) {
+        const int64_t lo = std::max<int64_t>(F, seg[(size_t)ww]);
+        const int64_t hi = std::min<int64_t>(F + nt, seg[(size_t)ww + 1]);
+        if (hi > lo) cuts.push_back(Cut{ww, lo, hi});
       }
       const int64_t np = (int64_t)cuts.size();
       s->max_splits = std::max(s->max_splits, np);
@@ -333,6 +410,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         s->partial_rows += np * t.nrows;
       }
       for (int64_t k = 0; k < np; ++k) {
+        const Cut& cu = cuts[(size_t)k];
         DecodePiece pc;
         pc.req = t.req;
         pc.kv_head = t.kv_head;
@@ -342,54 +420,64 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         pc.merge = merge;
         pc.any_lo = (int32_t)t.any_lo;
         pc.any_hi = (int32_t)t.any_hi;
-        const int32_t idx = (int32_t)s->pieces.size();
+        pc.flat0 = (int32_t)cu.lo;
+        pc.chunk0 = (int32_t)(t.c_lo + (cu.lo - F));
+        pc.pad0 = pc.pad1 = 0;
+        // A warp whose segment starts inside this tile starts with this piece.
+        if (seg[(size_t)cu.warp] >= F)
+          s->warp_piece[(size_t)(dl.warp_off + cu.warp)] =
+              (int32_t)((int64_t)s->pieces.size() - dl.piece_off);
         s->pieces.push_back(pc);
-        for (int64_t f = cuts[k].first; f < cuts[k].second; ++f)
-          s->chunks.push_back(ChunkRef{idx, (int32_t)(t.c_lo + (f - F))});
       }
       F += nt;
     }
+    dl.num_pieces = (int64_t)s->pieces.size() - dl.piece_off;
   }
   s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
 
-  // 3) Device copy of the plan (one allocation, blocking upload).
+  // 3) Device copy of the plan: one image (pieces, per-warp first pieces,
+  //    merge items, zeroed merge counters, prefill tiles, zeroed error word),
+  //    one blocking upload into a pooled device buffer.
   const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
-  const size_t chunks_bytes = s->chunks.size() * sizeof(ChunkRef);
+  const size_t warps_bytes = s->warp_piece.size() * sizeof(int32_t);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
   const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
   const size_t prefill_bytes = s->prefill.size() * sizeof(PrefillTile);
   s->d_pieces_off = 0;
-  s->d_chunks_off = kvq::align256(pieces_bytes);
-  s->d_merges_off = s->d_chunks_off + kvq::align256(chunks_bytes);
+  s->d_warps_off = kvq::align256(pieces_bytes);
+  s->d_merges_off = s->d_warps_off + kvq::align256(warps_bytes);
   s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
   s->d_prefill_off = s->d_counters_off + kvq::align256(counters_bytes);
   s->d_error_off = s->d_prefill_off + kvq::align256(prefill_bytes);
   const size_t total = s->d_error_off + sizeof(int32_t);
   if (have_device) {
-    if (cudaMalloc(&s->d_buf, total) != cudaSuccess) {
-      cudaGetLastError();
+    s->d_buf = pool_get(s->device, total, &s->d_buf_bytes);
+    if (!s->d_buf) {
       delete s;
       return KVQ_E_NO_MEMORY;
     }
-    char* b = static_cast<char*>(s->d_buf);
-    bool ok = true;
-    if (pieces_bytes)
-      ok &= cudaMemcpy(b + s->d_pieces_off, s->pieces.data(), pieces_bytes,
-                       cudaMemcpyHostToDevice) == cudaSuccess;
-    if (chunks_bytes)
-      ok &= cudaMemcpy(b + s->d_chunks_off, s->chunks.data(), chunks_bytes,
-                       cudaMemcpyHostToDevice) == cudaSuccess;
-    if (merges_bytes)
-      ok &= cudaMemcpy(b + s->d_merges_off, s->merges.data(), merges_bytes,
-                       cudaMemcpyHostToDevice) == cudaSuccess;
-    if (prefill_bytes)
-      ok &= cudaMemcpy(b + s->d_prefill_off, s->prefill.data(), prefill_bytes,
-                       cudaMemcpyHostToDevice) == cudaSuccess;
-    // Merge counters and the error word start at zero.
-    if (counters_bytes)
-      ok &= cudaMemset(b + s->d_counters_off, 0, counters_bytes) == cudaSuccess;
-    ok &= cudaMemset(b + s->d_error_off, 0, sizeof(int32_t)) == cudaSuccess;
-    if (!ok) {
+    std::lock_guard<std::mutex> lock(g_stage_mutex);
+    if (g_stage_bytes < total) {
+      if (g_stage) cudaFreeHost(g_stage);
+      g_stage = nullptr;
+      g_stage_bytes = 0;
+      const size_t want = pool_size_class(total);
+      if (cudaHostAlloc(&g_stage, want, cudaHostAllocDefault) == cudaSuccess) g_stage_bytes = want;
+      else cudaGetLastError();
+    }
+    std::vector<char> pageable;  // fallback when pinned memory is not available
+    char* image = static_cast<char*>(g_stage);
+    if (!image) {
+      pageable.resize(total);
+      image = pageable.data();
+    }
+    std::memset(image, 0, total);  // merge counters and the error word start at zero
+    if (pieces_bytes) std::memcpy(image + s->d_pieces_off, s->pieces.data(), pieces_bytes);
+    if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_piece.data(), warps_bytes);
+    if (merges_bytes) std::memcpy(image + s->d_merges_off, s->merges.data(), merges_bytes);
+    if (prefill_bytes) std::memcpy(image + s->d_prefill_off, s->prefill.data(), prefill_bytes);
+    if (cudaMemcpy(s->d_buf, image, total, cudaMemcpyHostToDevice) != cudaSuccess) {
+      cudaGetLastError();
       kvq_sched_destroy(s);
       return KVQ_E_CUDA;
     }
@@ -414,7 +502,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->num_tiles = s->num_tiles;
   out->num_pieces = (int64_t)s->pieces.size();
   out->num_merge_items = (int64_t)s->merges.size();
-  out->num_chunks = (int64_t)s->chunks.size();
+  out->num_chunks = s->launch[0].num_chunks + s->launch[1].num_chunks;
   out->num_decode_warps = (int64_t)s->launch[0].num_warps + s->launch[1].num_warps;
   out->max_splits = s->max_splits;
   out->total_query_tokens = s->total_q;
@@ -459,7 +547,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
       (int)dtype != s->dtype || (causal ? 1 : 0) != s->causal ||
       (window > 0 ? window : 0) != s->window)
     return KVQ_E_SCHED_MISMATCH;
-  if (s->chunks.empty() && s->prefill.empty()) return KVQ_OK;
+  if (s->launch[0].num_chunks + s->launch[1].num_chunks == 0 && s->prefill.empty()) return KVQ_OK;
   if (!s->d_buf) return KVQ_E_CUDA;  // planned without a device
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
@@ -534,7 +622,9 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   for (int cls = 0; cls < 2; ++cls) {
     const DecodeLaunch& dl = s->launch[cls];
     if (dl.num_chunks == 0) continue;
-    p.chunks = reinterpret_cast<const ChunkRef*>(b + s->d_chunks_off) + dl.chunk_off;
+    p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off) + dl.piece_off;
+    p.num_pieces = (int32_t)dl.num_pieces;
+    p.warp_piece = reinterpret_cast<const int32_t*>(b + s->d_warps_off) + dl.warp_off;
     p.num_chunks = dl.num_chunks;
     p.num_warps = dl.num_warps;
     const int rc = kvq::launch_decode(p, s->dtype, head_dim, cls + 1, stream);

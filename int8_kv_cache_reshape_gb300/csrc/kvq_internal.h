@@ -124,15 +124,11 @@ struct DecodePiece {
   int32_t merge;     // merge item of a split tile (-1: not split)
   int32_t any_lo;    // keys some row of the tile can see: [any_lo, any_hi)
   int32_t any_hi;
+  int32_t flat0;     // position of the piece's first chunk in its launch's flat sequence
+  int32_t chunk0;    // that chunk's 16-token index in the request
+  int32_t pad0, pad1;
 };
-static_assert(sizeof(DecodePiece) == 32, "DecodePiece layout");
-
-// One entry of the flat chunk sequence: which piece, which 16-token chunk.
-struct ChunkRef {
-  int32_t piece;
-  int32_t chunk;
-};
-static_assert(sizeof(ChunkRef) == 8, "ChunkRef layout");
+static_assert(sizeof(DecodePiece) == 48, "DecodePiece layout");
 
 // One merge item: the partial rows of a tile that was split along KV.
 struct MergeItem {
@@ -167,9 +163,10 @@ struct AttnParams {
   uint16_t* out;               // bf16 [sum Q, Hq, D]
   float* part_o;               // [P, D]
   float* part_lse;             // [P]
-  const DecodePiece* pieces;
-  const ChunkRef* chunks;      // this launch's flat chunk sequence
-  int64_t num_chunks;          // its length
+  const DecodePiece* pieces;   // this launch's pieces, in flat order
+  int32_t num_pieces;
+  const int32_t* warp_piece;   // per warp: the piece holding its first chunk
+  int64_t num_chunks;          // length of the launch's flat chunk sequence
   int num_warps;               // warps it is cut among (grid * kDecodeWarps)
   const MergeItem* merges;
   int32_t* merge_counters;     // one per merge item, zero between calls
