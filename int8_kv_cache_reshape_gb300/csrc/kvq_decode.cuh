@@ -508,7 +508,7 @@ splitkv_decode_kernel(const AttnParams p) {
       for (int e = 0; e < 4; ++e) {
         const float sk = (e < 2) ? sk0 : sk1;
         float v = (s[t][e] + s2[t][e]) * score_mul * sk;
-        if (cap > 0.0f) v = cap_l2 * tanhf(v * inv_cap);
+        if (cap > 0.0f) v = cap_l2 * dev::tanh_exp(v * inv_cap);
         if (!full) {
           const int tok = tok0 + g + 8 * (e >> 1);
           const int col = e & 1;

@@ -168,5 +168,16 @@ __device__ __forceinline__ float fast_exp2(float x) {
   return r;
 }
 
+// tanh(x) = 1 - 2 / (1 + e^(2x)), with e^(2x) = 2^(2 x log2 e): one exp2 and
+// one reciprocal.  The absolute error stays within a few 2^-23 over the whole
+// range (the result is needed to an absolute, not relative, accuracy: the
+// soft cap multiplies it by the cap); +-inf give +-1.
+__device__ __forceinline__ float tanh_exp(float x) {
+  const float e = fast_exp2(x * 2.8853900817779268f);  // 2 log2(e)
+  float r;
+  asm("rcp.approx.ftz.f32 %0, %1;" : "=f"(r) : "f"(1.0f + e));
+  return fmaf(-2.0f, r, 1.0f);
+}
+
 }  // namespace dev
 }  // namespace kvq

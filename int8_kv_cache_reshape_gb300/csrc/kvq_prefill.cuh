@@ -612,7 +612,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // (a capped -inf would be finite).
       auto score = [&](auto cap_c, float r) -> float {
         if constexpr (decltype(cap_c)::value)
-          return r == -INFINITY ? -INFINITY : cap_l2 * tanhf(r * score_mul * inv_cap);
+          return r == -INFINITY ? -INFINITY : cap_l2 * dev::tanh_exp(r * score_mul * inv_cap);
         else
           return r * score_mul;
       };
