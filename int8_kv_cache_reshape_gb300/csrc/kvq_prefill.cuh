@@ -633,15 +633,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         return mr;
       };
-      const float mr = full ? max_pass(std::true_type{}) : max_pass(std::false_type{});
-      // the score is monotonic in r (score_mul > 0, tanh increasing)
-      const float mx = cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
       float alpha = 1.0f;  // factor for O (score reference and value reference)
-      if (mx > m_ref + 8.0f) {
-        alpha = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
-        l_sum *= alpha;
-        m_ref = mx;
-      }
       // Value-scale reference (per-token-head): the largest exponent so far.
       float v_mul = 1.0f;  // 2^-ev
       if constexpr (Geo::kPth) {
@@ -655,54 +647,119 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
           int e;
           (void)frexpf(smax, &e);  // smax < 2^e
           if (e > ev) {
-            if (ev > -1000) alpha *= ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
+            if (ev > -1000) alpha = ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
             ev = e;
           }
         }
         v_mul = ldexpf(1.0f, -ev);
       }
-      // ---- pass 2: P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs, written over
-      // the first half of S(j)'s columns (columns already read).  The 2^6
-      // lifts small weights clear of the f16 subnormal range; l carries the
-      // same factor.
-      const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
-      float lsum_tile = 0.0f;
-      auto weight_pass = [&](auto full_c, auto cap_c) {
-#pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(tmem_s + c0, v);
-          tc::tmem_wait_ld();
-          uint32_t pw[16];
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float r0, r1;
-            raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
-            float p0, p1;
-            if constexpr (decltype(cap_c)::value) {
-              p0 = dev::fast_exp2(score(cap_c, r0) - ref);
-              p1 = dev::fast_exp2(score(cap_c, r1) - ref);
-            } else {
-              p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
-              p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
-            }
-            lsum_tile += p0 + p1;
-            if constexpr (Geo::kPth) {
-              const float2 v2 = *reinterpret_cast<const float2*>(sv + st * kN + c0 + e);
-              p0 *= v2.x * v_mul;
-              p1 *= v2.y * v_mul;
-            }
-            pw[e / 2] = dev::pack_f16x2(p0, p1);
-          }
-          tc::tmem_st16(tmem_s + c0 / 2, pw);
+      // A tile maximum above m_ref + 8 moves the reference (lazily).
+      auto move_ref = [&](float mx) {
+        if (mx > m_ref + 8.0f) {
+          const float a = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
+          alpha *= a;
+          l_sum *= a;
+          m_ref = mx;
         }
       };
-      if (cap > 0.0f) {
-        if (full) weight_pass(std::true_type{}, std::true_type{});
-        else weight_pass(std::false_type{}, std::true_type{});
+      // P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs: the 2^6 lifts small
+      // weights clear of the f16 subnormal range; l carries the same factor.
+      float lsum_tile = 0.0f;
+      // weights of 32 scores (raw bits) from column c0, against `ref`
+      auto weights32 = [&](auto full_c, auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float r0, r1;
+          raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
+          float p0, p1;
+          if constexpr (decltype(cap_c)::value) {
+            p0 = dev::fast_exp2(score(cap_c, r0) - ref);
+            p1 = dev::fast_exp2(score(cap_c, r1) - ref);
+          } else {
+            p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
+            p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
+          }
+          lsum_tile += p0 + p1;
+          if constexpr (Geo::kPth) {
+            const float2 v2 = *reinterpret_cast<const float2*>(sv + st * kN + c0 + e);
+            p0 *= v2.x * v_mul;
+            p1 *= v2.y * v_mul;
+          }
+          pw[e / 2] = dev::pack_f16x2(p0, p1);
+        }
+      };
+      auto max32 = [&](auto full_c, const uint32_t* v, int c0) -> float {
+        float mr = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 32; e += 2) {
+          float r0, r1;
+          raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
+          mr = fmaxf(mr, fmaxf(r0, r1));
+        }
+        return mr;
+      };
+      // the score is monotonic in r (score_mul > 0, tanh increasing)
+      auto to_score = [&](float mr) {
+        return cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
+      };
+      if constexpr (kN <= 64) {
+        // One pass: the row of S stays in registers; weights against the
+        // current reference, recomputed only when the tile moves it.
+        uint32_t v[kN];
+#pragma unroll
+        for (int c0 = 0; c0 < kN; c0 += 32)
+          tc::tmem_ld32(tmem_s + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+        tc::tmem_wait_ld();
+        uint32_t pw[kN / 2];
+        auto all_weights = [&](float ref) {
+          lsum_tile = 0.0f;
+          auto run = [&](auto full_c, auto cap_c) {
+#pragma unroll
+            for (int c0 = 0; c0 < kN; c0 += 32) weights32(full_c, cap_c, v + c0, c0, ref, pw + c0 / 2);
+          };
+          if (cap > 0.0f) {
+            if (full) run(std::true_type{}, std::true_type{});
+            else run(std::false_type{}, std::true_type{});
+          } else {
+            if (full) run(std::true_type{}, std::false_type{});
+            else run(std::false_type{}, std::false_type{});
+          }
+        };
+        float mr = -INFINITY;
+#pragma unroll
+        for (int c0 = 0; c0 < kN; c0 += 32)
+          mr = fmaxf(mr, full ? max32(std::true_type{}, v + c0, c0) : max32(std::false_type{}, v + c0, c0));
+        const float mx = to_score(mr);
+        if (__any_sync(0xffffffffu, mx > m_ref + 8.0f)) move_ref(mx);
+        all_weights(m_ref == -INFINITY ? 0.0f : m_ref - 6.0f);
+#pragma unroll
+        for (int c0 = 0; c0 < kN; c0 += 32)
+          tc::tmem_st16(tmem_s + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(pw + c0 / 2));
       } else {
-        if (full) weight_pass(std::true_type{}, std::false_type{});
-        else weight_pass(std::false_type{}, std::false_type{});
+        // Two passes over tensor memory (registers for 128 scores and their
+        // weights would spill): the maximum, then the weights, written over
+        // the first half of S(j)'s columns (columns already read).
+        const float mr = full ? max_pass(std::true_type{}) : max_pass(std::false_type{});
+        move_ref(to_score(mr));
+        const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
+        auto weight_pass = [&](auto full_c, auto cap_c) {
+#pragma unroll
+          for (int c0 = 0; c0 < kN; c0 += 32) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem_s + c0, v);
+            tc::tmem_wait_ld();
+            uint32_t pw[16];
+            weights32(full_c, cap_c, v, c0, ref, pw);
+            tc::tmem_st16(tmem_s + c0 / 2, pw);
+          }
+        };
+        if (cap > 0.0f) {
+          if (full) weight_pass(std::true_type{}, std::true_type{});
+          else weight_pass(std::false_type{}, std::true_type{});
+        } else {
+          if (full) weight_pass(std::true_type{}, std::false_type{});
+          else weight_pass(std::false_type{}, std::false_type{});
+        }
       }
       l_sum += lsum_tile;
       // A moved reference rescales O: PV(j-1) must be complete first.  (S(j)
