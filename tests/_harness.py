@@ -43,29 +43,60 @@ def cache_shape(wl):
     return (wl.num_blocks, wl.block_size, wl.heads_kv, row)
 
 
+GUARD_BYTES = 4096   # canary band on each side of every buffer the library writes
+GUARD_BYTE = 0xA5
+
+
+class Guarded:
+    """A device buffer with 4 KB canary bands on both sides; `check` fails if
+    a kernel wrote outside the buffer.  Used for the caches, the output and
+    the attention workspace.  The body starts 4096 bytes into a fresh
+    allocation, so it keeps the allocator's alignment."""
+
+    def __init__(self, shape, dtype, fill, device):
+        n = int(np.prod(shape)) * torch.empty((), dtype=dtype).element_size()
+        self.raw = torch.full((n + 2 * GUARD_BYTES,), GUARD_BYTE, dtype=torch.uint8, device=device)
+        body = self.raw[GUARD_BYTES:GUARD_BYTES + n]
+        self.t = body.view(dtype).view(shape) if n else torch.empty(shape, dtype=dtype, device=device)
+        if n:
+            self.t.fill_(fill)
+
+    def check(self, what):
+        lo = self.raw[:GUARD_BYTES]
+        hi = self.raw[self.raw.numel() - GUARD_BYTES:]
+        assert bool((lo == GUARD_BYTE).all()) and bool((hi == GUARD_BYTE).all()), \
+            f"{what}: a kernel wrote outside the buffer"
+
+
 class GpuRun:
     """Device tensors and results of one workload run through the library."""
 
     def __init__(self, wl, device="cuda:0", write_mask=None):
         self.wl = wl
         dev = torch.device(device)
+        self.dev = dev
         self.key = wl.key.to(dev)
         self.value = wl.value.to(dev)
         slots = wl.slot_mapping.clone()
         if write_mask is not None:
             slots[~write_mask] = -1
         self.slots = slots.to(dev)
-        self.kc = torch.full(cache_shape(wl), FILL, dtype=torch.uint8, device=dev)
-        self.vc = torch.full(cache_shape(wl), FILL, dtype=torch.uint8, device=dev)
+        self._kc = Guarded(cache_shape(wl), torch.uint8, FILL, dev)
+        self._vc = Guarded(cache_shape(wl), torch.uint8, FILL, dev)
+        self.kc, self.vc = self._kc.t, self._vc.t
         self.q = wl.q.to(dev)
         self.qsl = wl.query_start_loc.to(dev)
         self.sl = wl.seq_lens_t.to(dev)
         self.bt = wl.block_table.to(dev)
-        self.out = torch.full(wl.q.shape, float("nan"), dtype=torch.bfloat16, device=dev)
+        self._out = Guarded(tuple(wl.q.shape), torch.bfloat16, float("nan"), dev)
+        self.out = self._out.t
 
     def write_cache(self):
         kvq().reshape_and_cache(self.key, self.value, self.kc, self.vc, self.slots,
                                 self.wl.kv_cache_dtype, self.wl.k_scale, self.wl.v_scale)
+        torch.cuda.synchronize()
+        self._kc.check("key cache")
+        self._vc.check("value cache")
         return self
 
     def attention(self):
@@ -74,13 +105,16 @@ class GpuRun:
         sched = k.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
                                          wl.seq_lens_t.numpy(), wl.query_start_loc.numpy(),
                                          wl.causal, wl.window, wl.kv_cache_dtype)
-        ws = torch.empty(max(sched.workspace_bytes, 1), dtype=torch.uint8,
-                         device=self.q.device)
+        ws = Guarded((max(sched.workspace_bytes, 1),), torch.uint8, 0, self.q.device)
         k.attention_with_kv_cache(sched, self.q, self.kc, self.vc, self.qsl, self.sl, self.bt,
                                   wl.sm_scale, wl.causal, wl.window, wl.soft_cap, wl.k_scale,
-                                  wl.v_scale, self.out, ws, wl.kv_cache_dtype, wl.heads_kv)
+                                  wl.v_scale, self.out, ws.t, wl.kv_cache_dtype, wl.heads_kv)
         torch.cuda.synchronize()
         sched.check_device()   # no kernel gave up a bounded wait
+        ws.check("workspace")
+        self._out.check("output")
+        self._kc.check("key cache (read only)")
+        self._vc.check("value cache (read only)")
         self.sched_info = sched.info()
         sched.close()
         return self

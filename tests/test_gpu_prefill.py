@@ -11,10 +11,13 @@ that start inside a key tile, soft caps, mixed prefill + decode batches and
 rows that see no written key.  Tolerances: see tests/_harness.py.
 """
 import pytest
+import torch
 
+import oracle
 from int8_kv_cache_reshape_gb300 import workloads as W
 
-from _harness import GpuRun, assert_attention_close, oracle_cache, oracle_reference
+from _harness import (GpuRun, _oracle_args, assert_attention_close, oracle_cache,
+                      oracle_reference)
 
 pytestmark = pytest.mark.gpu
 
@@ -89,3 +92,68 @@ def test_prefill_rows_without_blocks(cuda_device):
     ref, bnd = oracle_reference(wl, kc, vc, tokens=range(64, 104))
     assert_attention_close(g.out_f32(range(64, 104)), ref, "holes", bnd)
     assert float(abs(g.out_f32(range(64))).max()) == 0.0
+
+
+@pytest.mark.parametrize("dtype", ["int8_per_token_head", "fp8_per_token_head"])
+def test_prefill_large_blocks_window_per_token_head(cuda_device, dtype):
+    """block_size 2176 (vllm PR 50194 page, Key source snippet) with a
+    sliding window and per-token-head scales at D = 256: the 16-key copies
+    of codes and of their scale tails cross a block boundary mid-tile."""
+    wl = W.custom(f"pf-B2176-win-{dtype}", [300, 90, 1], [2400, 2176, 4500], 16, 4, 256, 2176,
+                  dtype, 416, window=700, token_scale_range=(0.1, 10.0), outlier_p=0.01)
+    e, g = _check(wl)
+    assert g.sched_info["num_prefill_tiles"] > 0 and g.sched_info["num_tiles"] > 0
+
+
+def _without_block(bt, sl, block_size, req, blk):
+    """Block table and sequence lengths with block `blk` of request `req`
+    taken out of its table and its sequence one block shorter.  When every
+    query of the request sees that block whole (no window, the block ends at
+    or before L - Q), the keys that remain keep their causal relation to
+    every query, so on the same caches this is what a table hole at `blk`
+    must give."""
+    bt, sl = bt.clone(), sl.clone()
+    row = bt[req].tolist()
+    bt[req] = torch.tensor(row[:blk] + row[blk + 1:] + [row[0]], dtype=bt.dtype)
+    sl[req] -= block_size
+    return bt, sl
+
+
+@pytest.mark.parametrize("dtype,D", [("fp8_e4m3", 128), ("int8_per_token_head", 256),
+                                     ("fp8_e5m2", 64)])
+def test_table_hole_mid_sequence(cuda_device, dtype, D):
+    """A -1 in the middle of a block table masks that block's keys, for a
+    prefill request (the hole inside one key tile) and a decode request of
+    the same batch; the rest of each row matches the oracle without them."""
+    wl = W.custom(f"hole-{dtype}-{D}", [120, 1], [700, 900], 16, 4, D, 16, dtype, 417,
+                  token_scale_range=_pth(dtype))
+    g0 = GpuRun(wl).write_cache()
+    holes = {0: 9, 1: 30}                       # keys 144..159 and 480..495
+    for r, blk in holes.items():
+        assert (blk + 1) * wl.block_size <= wl.seq_lens[r] - wl.query_lens[r]
+        g0.bt[r, blk] = -1
+    g = g0.attention()
+    assert g.sched_info["num_prefill_tiles"] > 0 and g.sched_info["num_tiles"] > 0
+    kc, vc = oracle_cache(wl)
+    bt, sl = wl.block_table, wl.seq_lens_t
+    for r, blk in holes.items():
+        bt, sl = _without_block(bt, sl, wl.block_size, r, blk)
+    args = list(_oracle_args(wl, kc, vc))
+    args[4], args[5] = sl, bt
+    ref = oracle.attention(*args)
+    bnd = oracle.attention_fp32_bound(*args)
+    assert_attention_close(g.out_f32(), ref, "table hole", bnd)
+
+
+def test_reruns_are_bit_identical(cuda_device, monkeypatch):
+    """Two calls on the same inputs give the same bits: the split-KV merge
+    order is fixed by the schedule, not by which piece arrives last."""
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "96")
+    wl = W.custom("rerun", [1, 200, 1, 33], [3000, 500, 1200, 40], 32, 8, 128, 16,
+                  "fp8_per_token_head", 418, token_scale_range=(0.1, 10.0))
+    g = GpuRun(wl).write_cache()
+    a = g.attention().out.clone()
+    g.out.fill_(float("nan"))
+    b = g.attention().out.clone()
+    assert g.sched_info["num_merge_items"] > 0
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))

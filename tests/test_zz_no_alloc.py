@@ -75,3 +75,24 @@ def test_static_scratch_refuses_oversized_schedule(cuda_device, monkeypatch):
                                                  "fp8_e4m3", 8)
     assert e.value.status == k.E_WORKSPACE_TOO_SMALL
     sched.close()
+
+
+def test_static_scratch_with_prefill_rows(cuda_device, monkeypatch):
+    """A batch with prefill tiles and cut decode tiles: both kernels run
+    from the static-scratch entry point and match the workspace one."""
+    monkeypatch.setenv("KVQ_DECODE_WARPS", "48")
+    wl = W.custom("noalloc-mixed", [1, 150, 1, 40], [1800, 400, 700, 40], 32, 8, 128, 16,
+                  "int8_per_token_head", 78, token_scale_range=(0.1, 10.0))
+    g = GpuRun(wl).write_cache().attention()
+    assert g.sched_info["num_prefill_tiles"] > 0 and g.sched_info["num_merge_items"] > 0
+    ref = g.out_f32()
+    k = kvq()
+    sched = k.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                     wl.seq_lens_t.numpy(), wl.query_start_loc.numpy(),
+                                     wl.causal, wl.window, wl.kv_cache_dtype)
+    out = _run_static(g, sched)
+    sched.check_device()
+    sched.close()
+    got = out.float().cpu().numpy()
+    assert_attention_close(got, ref, "static scratch, mixed batch")
+    assert np.array_equal(got, ref)      # same kernels, same schedule: same bits
