@@ -76,8 +76,12 @@ struct PrefillGeom {
   static constexpr int kOffTailV = kOffTailK + kStages * kN * 16;   // stages x kN x 16
   static constexpr int kOffSk = kOffTailV + kStages * kN * 16;      // stages x kN f32
   static constexpr int kOffSv = kOffSk + kStages * kN * 4;          // stages x kN f32
-  static constexpr int kOffValid = kOffSv + kStages * kN * 4;       // stages x kN bytes
-  static constexpr int kOffQScale = kOffValid + kStages * kN;       // kM f32: 2^-sh of each Q row
+  // Per stage, for the softmax: the tile's 16-key chunk mask and, per
+  // converter warp, the largest value scale of its keys (bits of a float >= 0).
+  static constexpr int kOffTileInfo = kOffSv + kStages * kN * 4;    // stages x kN bytes reserved
+  static constexpr int kOffSMask = kOffTileInfo;                     // stages x u32
+  static constexpr int kOffVMax = kOffTileInfo + 4 * kStages;       // stages x 8 u32
+  static constexpr int kOffQScale = kOffTileInfo + kStages * kN;    // kM f32: 2^-sh of each Q row
   static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
   static constexpr int kBytes = kOffBar + 192;
   static constexpr int kOffQStage = kOffK;  // Q (kM x D f16, swizzled) staged over the K ring
@@ -92,6 +96,7 @@ struct PrefillGeom {
                     kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
                 "1024-byte operand tiles, 128-byte copy destinations");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
+  static_assert(4 * kStages + 32 * kStages <= kStages * kN && kConv / 32 <= 8, "tile info space");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
   // barrier slots (8 bytes each)
   // One P barrier per S buffer: P(j+1) may be ready before PV(j) is
@@ -103,8 +108,7 @@ struct PrefillGeom {
                        kNumBars = 17;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
-  static constexpr int kOffBadTile = kOffAbort + 4;             // stages x i32
-  static constexpr int kOffChunkValid = kOffBadTile + 4 * kStages;  // stages x u32: 16-key chunks copied
+  static constexpr int kOffChunkValid = kOffAbort + 4;          // stages x u32: 16-key chunks copied
   static_assert(kOffChunkValid + 4 * kStages <= kBytes, "flag space");
   static_assert(kN / 16 <= 32, "chunk mask");
 };
@@ -196,7 +200,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const uint32_t bars = base + Geo::kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffAbort);
-  volatile int32_t* bad_tile = reinterpret_cast<volatile int32_t*>(sm + Geo::kOffBadTile);
 
   if (tid == 0) {
     for (int s = 0; s < Geo::kStages; ++s) {
@@ -207,7 +210,6 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       tc::mbar_init(bar(Geo::kBarPFull + s), 128);
       tc::mbar_init(bar(Geo::kBarCodes + s), 1);
       tc::mbar_init(bar(Geo::kBarCodesFree + s), Geo::kConv);
-      bad_tile[s] = -1;
     }
     tc::mbar_init(bar(Geo::kBarODone), 1);
     tc::mbar_init(bar(Geo::kBarOFinal), 1);
@@ -227,7 +229,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
   float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
   float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
-  uint8_t* kvalid = sm + Geo::kOffValid;
+  uint32_t* smask = reinterpret_cast<uint32_t*>(sm + Geo::kOffSMask);
+  uint32_t* vmaxw = reinterpret_cast<uint32_t*>(sm + Geo::kOffVMax);
   volatile uint32_t* chunk_valid = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffChunkValid);
   // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
   // floor((2^32 - 1) / B)) is q or q - 1 for every 32-bit j.
@@ -307,42 +310,56 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     ++nt;
     if (nt < T) fetch_chunks(nt, nx_blk, nx_off);
   };
-  __syncthreads();  // barriers initialised
-  if (warp == 0 && T > 0) {
-    const bool leader = elect_one();
-    fetch_chunks(0, nx_blk, nx_off);
-    issue_next(leader);
-    if (nt < T) issue_next(leader);
-    __syncwarp();
-  }
-
   // ---- Q tile -> staging (swizzled rows), all warps: lanes_per_row lanes
   // hold one row (16 bytes each, coalesced); the row's largest exponent
   // comes from a shuffle reduction over those lanes, and the row is scaled
-  // by the power of two that puts its largest |q| in [2^14, 2^15).
-  {
-    constexpr int kLpr = D / 8;            // lanes per row
-    constexpr int kRps = 32 / kLpr;        // rows per warp step
-    constexpr int kWarps = Geo::kThreads / 32;
-    constexpr int kSteps = (kM / kRps + kWarps - 1) / kWarps;
-    const int lane = tid & 31;
-    const int sub = lane / kLpr, c = lane % kLpr;
-    float* qscale = reinterpret_cast<float*>(sm + Geo::kOffQScale);
-    uint4 v[kSteps];
+  // by the power of two that puts its largest |q| in [2^14, 2^15).  The
+  // loads are issued first: their latency overlaps the table reads and the
+  // first copies.
+  constexpr int kLpr = D / 8;            // lanes per row
+  constexpr int kRps = 32 / kLpr;        // rows per warp step
+  constexpr int kQWarps = Geo::kThreads / 32;
+  constexpr int kQSteps = (kM / kRps + kQWarps - 1) / kQWarps;
+  const int q_sub = (tid & 31) / kLpr, q_c = (tid & 31) % kLpr;
+  uint4 qv[kQSteps];
 #pragma unroll
-    for (int i = 0; i < kSteps; ++i) {  // all loads first
-      const int m = (warp + i * kWarps) * kRps + sub;
-      v[i] = make_uint4(0, 0, 0, 0);
-      if (m < t.nrows) {
-        const int R = t.row0 + m;
-        v[i] = *reinterpret_cast<const uint4*>(
-            p.q + ((int64_t)(q0 + R / G) * p.heads_q + t.kv_head * G + R % G) * D + 8 * c);
-      }
+  for (int i = 0; i < kQSteps; ++i) {
+    const int m = (warp + i * kQWarps) * kRps + q_sub;
+    qv[i] = make_uint4(0, 0, 0, 0);
+    if (m < t.nrows) {
+      const int R = t.row0 + m;
+      qv[i] = *reinterpret_cast<const uint4*>(
+          p.q + ((int64_t)(q0 + R / G) * p.heads_q + t.kv_head * G + R % G) * D + 8 * q_c);
     }
+  }
+  int blk1[kChunks];
+  uint32_t off1[kChunks];
+  if (warp == 0 && T > 0) {
+    fetch_chunks(0, nx_blk, nx_off);
+    if (T > 1) fetch_chunks(1, blk1, off1);
+  }
+  __syncthreads();  // barriers initialised
+  if (warp == 0 && T > 0) {
+    const bool leader = elect_one();
+    int slot0[kChunks];
+    uint32_t valid;
+    resolve_chunks(nx_blk, nx_off, slot0, valid);
+    issue_codes(0, slot0, valid, leader);
+    nt = 1;
+    if (T > 1) {
+      resolve_chunks(blk1, off1, slot0, valid);
+      issue_codes(1, slot0, valid, leader);
+      nt = 2;
+      if (nt < T) fetch_chunks(nt, nx_blk, nx_off);
+    }
+    __syncwarp();
+  }
+  {
+    float* qscale = reinterpret_cast<float*>(sm + Geo::kOffQScale);
 #pragma unroll
-    for (int i = 0; i < kSteps; ++i) {
-      const int m = (warp + i * kWarps) * kRps + sub;
-      const uint32_t w[4] = {v[i].x, v[i].y, v[i].z, v[i].w};
+    for (int i = 0; i < kQSteps; ++i) {
+      const int m = (warp + i * kQWarps) * kRps + q_sub;
+      const uint32_t w[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
       int emax = 0;
 #pragma unroll
       for (int k = 0; k < 4; ++k) emax = max(emax, (int)max((w[k] >> 7) & 0xFFu, (w[k] >> 23) & 0xFFu));
@@ -357,8 +374,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         o.y = dev::pack_f16x2(dev::bf16_lo(w[1]) * up, dev::bf16_hi(w[1]) * up);
         o.z = dev::pack_f16x2(dev::bf16_lo(w[2]) * up, dev::bf16_hi(w[2]) * up);
         o.w = dev::pack_f16x2(dev::bf16_lo(w[3]) * up, dev::bf16_hi(w[3]) * up);
-        sts128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 8 * c), o);
-        if (c == 0) qscale[m] = ldexpf(1.0f, -sh);
+        sts128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 8 * q_c), o);
+        if (q_c == 0) qscale[m] = ldexpf(1.0f, -sh);
       }
     }
   }
@@ -531,18 +548,26 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       const uint32_t valid = chunk_valid[st];
       // every key of the tile in range and copied: no per-unit checks
       const bool whole = valid == (1u << kChunks) - 1u && kv0 >= t.kv_lo && kv0 + kN <= t.kv_hi;
-      // per-key flags and scales: one thread per key
-      for (int n = ctid; n < kN; n += Geo::kConv) {
-        const int jj = kv0 + n;
-        const bool in_range = jj >= t.kv_lo && jj < t.kv_hi;
-        const bool live = in_range && ((valid >> (n >> 4)) & 1u);
-        kvalid[st * kN + n] = live ? 1 : 0;
-        if (in_range && !live) bad_tile[st] = j;
-        if constexpr (Geo::kPth) {
+      // The softmax's copy of the chunk mask: the issuer rewrites
+      // chunk_valid[st] for tile j + 2 before the softmax is done with j,
+      // while this copy is rewritten only after P(j) V(j) has completed.
+      if (ctid == 0) smask[st] = valid;
+      if constexpr (Geo::kPth) {
+        // Per-key scales, one thread per key (0 for a key without a copied
+        // row); each converter warp publishes the largest value scale it saw.
+        float vmax = 0.0f;
+        for (int n = ctid; n < kN; n += Geo::kConv) {
+          const int jj = kv0 + n;
+          const bool live = jj >= t.kv_lo && jj < t.kv_hi && ((valid >> (n >> 4)) & 1u);
           const uint32_t off = (uint32_t)((st * kN + n) * 16);
-          sk[st * kN + n] = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
-          sv[st * kN + n] = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
+          const float ks = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
+          const float vs = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
+          sk[st * kN + n] = ks;
+          sv[st * kN + n] = vs;
+          vmax = fmaxf(vmax, vs);  // stays >= 0 (a NaN or negative scale is ignored)
         }
+        const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
+        if ((ctid & 31) == 0) vmaxw[st * 8 + (ctid >> 5)] = wmax;
       }
       convert(j, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
               base + Geo::kOffCodeK + (uint32_t)(st * kN * D), whole);
@@ -561,7 +586,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     // ======================= softmax ===========================================
     const float* sk = reinterpret_cast<const float*>(sm + Geo::kOffSk);
     const float* sv = reinterpret_cast<const float*>(sm + Geo::kOffSv);
-    const uint8_t* kvalid = sm + Geo::kOffValid;
+    const uint32_t* smask = reinterpret_cast<const uint32_t*>(sm + Geo::kOffSMask);
+    const uint32_t* vmaxw = reinterpret_cast<const uint32_t*>(sm + Geo::kOffVMax);
+    constexpr uint32_t kAllChunks = (kChunks >= 32) ? 0xFFFFFFFFu : ((1u << kChunks) - 1u);
+    constexpr int kVMaxSlots = (kN + 31) / 32;  // converter warps that hold keys
     const int pos = L - Q + R / G;
     const int W = p.window;
     const int row_hi = row_valid ? (p.causal ? pos + 1 : L) : 0;  // padding rows see nothing
@@ -574,6 +602,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         p.sm_scale * q_unscale * (cap > 0.0f ? 1.0f : log2e) * (Geo::kPth ? 1.0f : p.k_scale);
     const float cap_l2 = cap * log2e;
     const float inv_cap = cap > 0.0f ? 1.0f / cap : 0.0f;
+    // m_ref: the reference maximum, an integer (log2 units) once set, so
+    // that moving it scales weights, O and l by exact powers of two.
     float m_ref = -INFINITY, l_sum = 0.0f;
     int ev = -1000;  // exponent of the value-scale reference (per-token-head)
     bool ok = true;
@@ -588,61 +618,20 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if (!ok) break;
       tc::fence_after_sync();
       const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN) + lane_base;
-      // Masks are needed when some row of the warp does not see the whole
-      // tile, or the tile has a key without a block.
-      const bool full =
-          __all_sync(0xffffffffu, kv0 >= row_lo && kv0 + kN <= row_hi) && bad_tile[st] != j;
-      // r: the raw score (per-token-head: times the key's scale), -inf when
-      // masked; r * score_mul is the score in log2 units without a cap.
-      auto raw_pair = [&](auto full_c, uint32_t b0, uint32_t b1, int n, float& r0, float& r1) {
-        r0 = __uint_as_float(b0);
-        r1 = __uint_as_float(b1);
-        if constexpr (Geo::kPth) {
-          const float2 k2 = *reinterpret_cast<const float2*>(sk + st * kN + n);
-          r0 *= k2.x;
-          r1 *= k2.y;
-        }
-        if constexpr (!decltype(full_c)::value) {
-          const int jj = kv0 + n;
-          r0 = kvalid[st * kN + n] && jj >= row_lo && jj < row_hi ? r0 : -INFINITY;
-          r1 = kvalid[st * kN + n + 1] && jj + 1 >= row_lo && jj + 1 < row_hi ? r1 : -INFINITY;
-        }
-      };
-      // The score in log2 units from r.  Under a cap, masked r stays masked
-      // (a capped -inf would be finite).
-      auto score = [&](auto cap_c, float r) -> float {
-        if constexpr (decltype(cap_c)::value)
-          return r == -INFINITY ? -INFINITY : cap_l2 * dev::tanh_exp(r * score_mul * inv_cap);
-        else
-          return r * score_mul;
-      };
-      // ---- pass 1: the row's maximum over this tile
-      auto max_pass = [&](auto full_c) -> float {
-        float mr = -INFINITY;
-#pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(tmem_s + c0, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; e += 2) {
-            float r0, r1;
-            raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
-            mr = fmaxf(mr, fmaxf(r0, r1));
-          }
-        }
-        return mr;
-      };
+      // Visible keys n of this row: lo_n <= n < hi_n, in a 16-key chunk
+      // that was copied.  Masks are needed unless every row of the warp
+      // sees the whole tile and every chunk is in.
+      const uint32_t cmask = smask[st];
+      const int lo_n = row_lo - kv0, hi_n = row_hi - kv0;
+      const bool full = __all_sync(0xffffffffu, lo_n <= 0 && hi_n >= kN) && cmask == kAllChunks;
       float alpha = 1.0f;  // factor for O (score reference and value reference)
       // Value-scale reference (per-token-head): the largest exponent so far.
       float v_mul = 1.0f;  // 2^-ev
       if constexpr (Geo::kPth) {
-        float smax = 0.0f;
+        uint32_t mb = 0;
 #pragma unroll
-        for (int n = 0; n < kN; n += 4) {
-          const float4 s4 = *reinterpret_cast<const float4*>(sv + st * kN + n);
-          smax = fmaxf(fmaxf(smax, fmaxf(s4.x, s4.y)), fmaxf(s4.z, s4.w));
-        }
+        for (int w = 0; w < kVMaxSlots; ++w) mb = max(mb, vmaxw[st * 8 + w]);
+        const float smax = __uint_as_float(mb);
         if (smax > 0.0f) {
           int e;
           (void)frexpf(smax, &e);  // smax < 2^e
@@ -653,24 +642,49 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
         v_mul = ldexpf(1.0f, -ev);
       }
-      // A tile maximum above m_ref + 8 moves the reference (lazily).
-      auto move_ref = [&](float mx) {
-        if (mx > m_ref + 8.0f) {
-          const float a = m_ref == -INFINITY ? 0.0f : exp2f(m_ref - mx);
-          alpha *= a;
-          l_sum *= a;
-          m_ref = mx;
+      // The score in log2 units from r (the raw score, times the key's scale
+      // per token-head; -inf when masked).  Under a cap, masked r stays
+      // masked (a capped -inf would be finite).
+      auto score = [&](auto cap_c, float r) -> float {
+        if constexpr (decltype(cap_c)::value)
+          return r == -INFINITY ? -INFINITY : cap_l2 * dev::tanh_exp(r * score_mul * inv_cap);
+        else
+          return r * score_mul;
+      };
+      // 64 scores from column c0: r in place, the row's maximum of r.
+      auto raw64 = [&](auto full_c, uint32_t* v, int c0) -> float {
+        const float* skp = sk + st * kN + c0;
+        const int lo = lo_n - c0, hi = hi_n - c0;
+        const uint32_t cm = cmask >> (c0 >> 4);
+        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+#pragma unroll
+        for (int e = 0; e < 64; e += 2) {
+          float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
+          if constexpr (Geo::kPth) {
+            const float2 k2 = *reinterpret_cast<const float2*>(skp + e);
+            r0 *= k2.x;
+            r1 *= k2.y;
+          }
+          if constexpr (!decltype(full_c)::value) {
+            const bool in = (cm >> (e >> 4)) & 1u;
+            r0 = in && e >= lo && e < hi ? r0 : -INFINITY;
+            r1 = in && e + 1 >= lo && e + 1 < hi ? r1 : -INFINITY;
+          }
+          v[e] = __float_as_uint(r0);
+          v[e + 1] = __float_as_uint(r1);
+          mx4[(e >> 1) & 3] = fmaxf(mx4[(e >> 1) & 3], fmaxf(r0, r1));
         }
+        return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
       };
       // P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs: the 2^6 lifts small
       // weights clear of the f16 subnormal range; l carries the same factor.
       float lsum_tile = 0.0f;
-      // weights of 32 scores (raw bits) from column c0, against `ref`
-      auto weights32 = [&](auto full_c, auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
+      auto weights64 = [&](auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
+        const float* svp = sv + st * kN + c0;
+        float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float r0, r1;
-          raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
+        for (int e = 0; e < 64; e += 2) {
+          const float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
           float p0, p1;
           if constexpr (decltype(cap_c)::value) {
             p0 = dev::fast_exp2(score(cap_c, r0) - ref);
@@ -679,86 +693,65 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
             p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
           }
-          lsum_tile += p0 + p1;
+          ls0 += p0;
+          ls1 += p1;
           if constexpr (Geo::kPth) {
-            const float2 v2 = *reinterpret_cast<const float2*>(sv + st * kN + c0 + e);
+            const float2 v2 = *reinterpret_cast<const float2*>(svp + e);
             p0 *= v2.x * v_mul;
             p1 *= v2.y * v_mul;
           }
           pw[e / 2] = dev::pack_f16x2(p0, p1);
         }
+        lsum_tile += ls0 + ls1;
       };
-      auto max32 = [&](auto full_c, const uint32_t* v, int c0) -> float {
-        float mr = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 32; e += 2) {
-          float r0, r1;
-          raw_pair(full_c, v[e], v[e + 1], c0 + e, r0, r1);
-          mr = fmaxf(mr, fmaxf(r0, r1));
-        }
-        return mr;
-      };
-      // the score is monotonic in r (score_mul > 0, tanh increasing)
-      auto to_score = [&](float mr) {
-        return cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
-      };
-      if constexpr (kN <= 64) {
-        // One pass: the row of S stays in registers; weights against the
-        // current reference, recomputed only when the tile moves it.
-        uint32_t v[kN];
-#pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += 32)
-          tc::tmem_ld32(tmem_s + c0, *reinterpret_cast<uint32_t(*)[32]>(v + c0));
+      // One pass over the row, 64 scores per tensor-memory round trip: the
+      // round's maximum, then its weights against the reference, written
+      // as f16 pairs over columns of S(j) already read.  A round maximum
+      // more than 2^8 above the reference moves it (lazily) to the next
+      // integer at or above; weights already written in this tile are then
+      // scaled by the same power of two.
+#pragma unroll 1
+      for (int c0 = 0; c0 < kN; c0 += 64) {
+        uint32_t v[64];
+        tc::tmem_ld32(tmem_s + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+        tc::tmem_ld32(tmem_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tc::tmem_wait_ld();
-        uint32_t pw[kN / 2];
-        auto all_weights = [&](float ref) {
-          lsum_tile = 0.0f;
-          auto run = [&](auto full_c, auto cap_c) {
-#pragma unroll
-            for (int c0 = 0; c0 < kN; c0 += 32) weights32(full_c, cap_c, v + c0, c0, ref, pw + c0 / 2);
-          };
-          if (cap > 0.0f) {
-            if (full) run(std::true_type{}, std::true_type{});
-            else run(std::false_type{}, std::true_type{});
-          } else {
-            if (full) run(std::true_type{}, std::false_type{});
-            else run(std::false_type{}, std::false_type{});
-          }
-        };
-        float mr = -INFINITY;
-#pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += 32)
-          mr = fmaxf(mr, full ? max32(std::true_type{}, v + c0, c0) : max32(std::false_type{}, v + c0, c0));
-        const float mx = to_score(mr);
-        if (__any_sync(0xffffffffu, mx > m_ref + 8.0f)) move_ref(mx);
-        all_weights(m_ref == -INFINITY ? 0.0f : m_ref - 6.0f);
-#pragma unroll
-        for (int c0 = 0; c0 < kN; c0 += 32)
-          tc::tmem_st16(tmem_s + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(pw + c0 / 2));
-      } else {
-        // Two passes over tensor memory (registers for 128 scores and their
-        // weights would spill): the maximum, then the weights, written over
-        // the first half of S(j)'s columns (columns already read).
-        const float mr = full ? max_pass(std::true_type{}) : max_pass(std::false_type{});
-        move_ref(to_score(mr));
+        const float mr = full ? raw64(std::true_type{}, v, c0) : raw64(std::false_type{}, v, c0);
+        // the score is monotonic in r (score_mul > 0, tanh increasing)
+        const float mx = cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
+        float a = 1.0f;
+        if (mx > m_ref + 8.0f) {
+          const float nref = ceilf(mx);
+          if (m_ref != -INFINITY) a = ldexpf(1.0f, (int)fmaxf(m_ref - nref, -200.0f));
+          m_ref = nref;
+          alpha *= a;
+          l_sum *= a;
+          lsum_tile *= a;
+        }
         const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
-        auto weight_pass = [&](auto full_c, auto cap_c) {
-#pragma unroll
-          for (int c0 = 0; c0 < kN; c0 += 32) {
-            uint32_t v[32];
-            tc::tmem_ld32(tmem_s + c0, v);
+        uint32_t pw[32];
+        if (cap > 0.0f)
+          weights64(std::true_type{}, v, c0, ref, pw);
+        else
+          weights64(std::false_type{}, v, c0, ref, pw);
+        tc::tmem_st16(tmem_s + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(pw));
+        tc::tmem_st16(tmem_s + c0 / 2 + 16, *reinterpret_cast<uint32_t(*)[16]>(pw + 16));
+        if (c0 > 0 && __any_sync(0xffffffffu, a != 1.0f)) {
+          // Weights of the earlier rounds (columns [0, c0 / 2)) against the
+          // new reference: a power-of-two scaling, exact unless subnormal.
+          tc::tmem_wait_st();
+#pragma unroll 1
+          for (int c = 0; c < c0 / 2; c += 32) {
+            uint32_t w[32];
+            tc::tmem_ld32(tmem_s + c, w);
             tc::tmem_wait_ld();
-            uint32_t pw[16];
-            weights32(full_c, cap_c, v, c0, ref, pw);
-            tc::tmem_st16(tmem_s + c0 / 2, pw);
+#pragma unroll
+            for (int e = 0; e < 32; ++e) {
+              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+              w[e] = dev::pack_f16x2(f.x * a, f.y * a);
+            }
+            tc::tmem_st32(tmem_s + c, w);
           }
-        };
-        if (cap > 0.0f) {
-          if (full) weight_pass(std::true_type{}, std::true_type{});
-          else weight_pass(std::false_type{}, std::true_type{});
-        } else {
-          if (full) weight_pass(std::true_type{}, std::false_type{});
-          else weight_pass(std::false_type{}, std::false_type{});
         }
       }
       l_sum += lsum_tile;
