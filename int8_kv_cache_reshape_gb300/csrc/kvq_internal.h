@@ -79,23 +79,29 @@ KVQ_HD constexpr size_t decode_smem_bytes(int dtype, int head_dim) {
 // exceed kTileMaxRows go to this kernel.
 constexpr int kPrefillRows = 128;
 constexpr int kPrefillStages = 2;        // K / V^T tiles in flight
-constexpr int kPrefillThreads = 384;     // 1 MMA warp, 4 softmax warps, 7 converter warps
-constexpr int kPrefillConvThreads = 224;
+constexpr int kPrefillThreads = 384;     // 1 MMA, 4 softmax, 6 converter warps, 1 copy warp
+constexpr int kPrefillConvThreads = 192;
 // Keys per KV tile: 128, or 64 at head_dim 256 (shared memory).
 KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 // Tensor-memory columns: O (head_dim fp32), two S buffers (keys fp32 each,
 // P in f16 pairs over the first half), Q (head_dim / 2 columns of f16
 // pairs); always 512.
 KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
+// Side-data slots of the prefill (per-key scales, chunk mask, largest value
+// scale): tile j uses slot j % 4, so the converters may run two tiles
+// ahead of the softmax.
+constexpr int kPrefillSideSlots = 4;
 // Shared memory: 2 x K and 2 x V (keys x D f16 each); 2 x the K and V codes
-// (keys x D bytes each, as the bulk tensor copies deliver them) and
-// their 16-byte scale tails (per-token-head); 2 x key / value scales and
-// key-valid flags; the 128 rows' Q scales; barriers; +1 KB for 1024-byte
-// alignment.  Q and O are staged through the K ring.
+// (keys x D bytes each, as the bulk tensor copies deliver them) and their
+// 16-byte scale tails (per-token-head); 4 x the tile's key / value scales;
+// 4 x the tile's chunk mask and per-warp largest value scales (144 bytes);
+// the 128 rows' Q scales; barriers and flags (256 bytes); +1 KB for
+// 1024-byte alignment.
+// Q and O are staged through the K ring.
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
   return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
          2 * (size_t)kPrefillStages * prefill_keys(head_dim) * (head_dim + 16) +
-         (size_t)kPrefillStages * prefill_keys(head_dim) * (4 + 4 + 1) + kPrefillRows * 4 + 192 +
+         (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillRows * 4 + 256 +
          1024;
 }
 

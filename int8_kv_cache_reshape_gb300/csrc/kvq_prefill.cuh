@@ -74,16 +74,17 @@ struct PrefillGeom {
   static constexpr int kOffCodeV = kOffCodeK + kStages * kN * D;    // stages x kN x D code bytes
   static constexpr int kOffTailK = kOffCodeV + kStages * kN * D;    // stages x kN x 16 (scale tails)
   static constexpr int kOffTailV = kOffTailK + kStages * kN * 16;   // stages x kN x 16
-  static constexpr int kOffSk = kOffTailV + kStages * kN * 16;      // stages x kN f32
-  static constexpr int kOffSv = kOffSk + kStages * kN * 4;          // stages x kN f32
-  // Per stage, for the softmax: the tile's 16-key chunk mask and, per
-  // converter warp, the largest value scale of its keys (bits of a float >= 0).
-  static constexpr int kOffTileInfo = kOffSv + kStages * kN * 4;    // stages x kN bytes reserved
-  static constexpr int kOffSMask = kOffTileInfo;                     // stages x u32
-  static constexpr int kOffVMax = kOffTileInfo + 4 * kStages;       // stages x 8 u32
-  static constexpr int kOffQScale = kOffTileInfo + kStages * kN;    // kM f32: 2^-sh of each Q row
+  // Side data of tile j, for the softmax, in slot j % kSide: per-key scales,
+  // the 16-key chunk mask and, per converter warp, the largest value scale
+  // of its keys (bits of a float >= 0).
+  static constexpr int kSide = kPrefillSideSlots;
+  static constexpr int kOffSk = kOffTailV + kStages * kN * 16;      // kSide x kN f32
+  static constexpr int kOffSv = kOffSk + kSide * kN * 4;            // kSide x kN f32
+  static constexpr int kOffSMask = kOffSv + kSide * kN * 4;         // kSide x u32
+  static constexpr int kOffVMax = kOffSMask + 4 * kSide;            // kSide x 8 u32
+  static constexpr int kOffQScale = kOffVMax + 32 * kSide;          // kM f32: 2^-sh of each Q row
   static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
-  static constexpr int kBytes = kOffBar + 192;
+  static constexpr int kBytes = kOffBar + 256;
   static constexpr int kOffQStage = kOffK;  // Q (kM x D f16, swizzled) staged over the K ring
   static constexpr int kOffOStage = kOffK;  // O (kM x D bf16) staged over the K ring at the end
   static constexpr int kColO = 0;                 // O: D fp32 columns
@@ -96,16 +97,19 @@ struct PrefillGeom {
                     kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
                 "1024-byte operand tiles, 128-byte copy destinations");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
-  static_assert(4 * kStages + 32 * kStages <= kStages * kN && kConv / 32 <= 8, "tile info space");
+  static_assert(kConv / 32 <= 8 && kSide == 4, "side data space");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
-  // barrier slots (8 bytes each)
-  // One P barrier per S buffer: P(j+1) may be ready before PV(j) is
-  // issued.  A parity wait is unambiguous only while the waiter is at most
-  // one phase behind, so the epilogue (which may be several PVs ahead of
-  // the last phase it saw) waits on a one-shot barrier for the last PV.
-  static constexpr int kBarKFull = 0, kBarVFull = 2, kBarKvEmpty = 4, kBarSFull = 6, kBarPFull = 8,
-                       kBarODone = 10, kBarOFinal = 11, kBarDrain = 12, kBarCodes = 13, kBarCodesFree = 15,
-                       kNumBars = 17;
+  // barrier slots (8 bytes each).  K and V travel separately: the K codes
+  // of tile j + 2 are copied once K(j) is converted, K(j + 2) is converted
+  // once S(j) is complete, V(j + 2) once P(j) V(j) is.  One P barrier per
+  // S buffer: P(j+1) may be ready before PV(j) is issued.  A parity wait is
+  // unambiguous only while the waiter is at most one phase behind, so the
+  // epilogue (which may be several PVs ahead of the last phase it saw)
+  // waits on a one-shot barrier for the last PV, and the side data (which
+  // the converters may write two tiles ahead) has four slots.
+  static constexpr int kBarCodesK = 0, kBarCodesV = 2, kBarCodesKFree = 4, kBarCodesVFree = 6,
+                       kBarKFull = 8, kBarVFull = 10, kBarVEmpty = 12, kBarSFull = 14, kBarPFull = 16,
+                       kBarSide = 18, kBarODone = 22, kBarOFinal = 23, kBarDrain = 24, kNumBars = 25;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
   static constexpr int kOffChunkValid = kOffAbort + 4;          // stages x u32: 16-key chunks copied
@@ -203,14 +207,17 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   if (tid == 0) {
     for (int s = 0; s < Geo::kStages; ++s) {
+      tc::mbar_init(bar(Geo::kBarCodesK + s), 1);
+      tc::mbar_init(bar(Geo::kBarCodesV + s), 1);
+      tc::mbar_init(bar(Geo::kBarCodesKFree + s), Geo::kConv);
+      tc::mbar_init(bar(Geo::kBarCodesVFree + s), Geo::kConv);
       tc::mbar_init(bar(Geo::kBarKFull + s), Geo::kConv);
       tc::mbar_init(bar(Geo::kBarVFull + s), Geo::kConv);
-      tc::mbar_init(bar(Geo::kBarKvEmpty + s), 1);
+      tc::mbar_init(bar(Geo::kBarVEmpty + s), 1);
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
       tc::mbar_init(bar(Geo::kBarPFull + s), 128);
-      tc::mbar_init(bar(Geo::kBarCodes + s), 1);
-      tc::mbar_init(bar(Geo::kBarCodesFree + s), Geo::kConv);
     }
+    for (int s = 0; s < Geo::kSide; ++s) tc::mbar_init(bar(Geo::kBarSide + s), Geo::kConv);
     tc::mbar_init(bar(Geo::kBarODone), 1);
     tc::mbar_init(bar(Geo::kBarOFinal), 1);
     tc::mbar_init(bar(Geo::kBarDrain), 1);
@@ -224,7 +231,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   // ---- converter state (warps 1-3, 8-11); converter 0 also issues the bulk
   // tensor copies of each tile's codes.
-  const bool is_conv = (warp >= 1 && warp < 4) || warp >= 8;
+  constexpr int kCopyWarp = 11;  // issues the bulk tensor copies
+  const bool is_conv = (warp >= 1 && warp < 4) || (warp >= 8 && warp < kCopyWarp);
   const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
   const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
   float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
@@ -272,43 +280,80 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       }
     }
   };
-  // Copies of those chunks into code stage j & 1: K and V codes and, per
-  // token-head, the scale tails; one arrival with the byte count.
-  auto issue_codes = [&](int j, const int (&slot0)[kChunks], uint32_t valid, bool leader) {
+  // Copies of those chunks into code stage j & 1, in two groups with a
+  // barrier each: the K codes (and, per token-head, both scale tails), and
+  // the V codes.  The chunk list of each stage stays in registers (static
+  // indices, selected by the uniform stage) for the V group.
+  int kept_slot[2][kChunks];
+  uint32_t kept_valid[2] = {0u, 0u};
+  auto issue_k = [&](int j, const int (&slot0)[kChunks], uint32_t valid, bool leader) {
     const int st = j & 1;
-    constexpr uint32_t kChunkBytes = 2u * 16u * D + (Geo::kPth ? 2u * 16u * 16u : 0u);
-    const uint32_t cb = bar(Geo::kBarCodes + st);
+    constexpr uint32_t kChunkBytes = 16u * D + (Geo::kPth ? 2u * 16u * 16u : 0u);
+    const uint32_t cb = bar(Geo::kBarCodesK + st);
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      if (s2 == st) {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) kept_slot[s2][c] = slot0[c];
+        kept_valid[s2] = valid;
+      }
+    }
     if (leader) {
       chunk_valid[st] = valid;
       mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * kChunkBytes);
-    }
 #pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      if (leader && ((valid >> c) & 1u)) {
-        const uint32_t off = (uint32_t)(st * kN + 16 * c);
-        tma_load_3d(base + Geo::kOffCodeK + off * D, &maps.k, 0, t.kv_head, slot0[c], cb);
-        tma_load_3d(base + Geo::kOffCodeV + off * D, &maps.v, 0, t.kv_head, slot0[c], cb);
-        if constexpr (Geo::kPth) {
-          tma_load_3d(base + Geo::kOffTailK + off * 16, &maps.ks, D, t.kv_head, slot0[c], cb);
-          tma_load_3d(base + Geo::kOffTailV + off * 16, &maps.vs, D, t.kv_head, slot0[c], cb);
+      for (int c = 0; c < kChunks; ++c) {
+        if ((valid >> c) & 1u) {
+          const uint32_t off = (uint32_t)(st * kN + 16 * c);
+          tma_load_3d(base + Geo::kOffCodeK + off * D, &maps.k, 0, t.kv_head, slot0[c], cb);
+          if constexpr (Geo::kPth) {
+            tma_load_3d(base + Geo::kOffTailK + off * 16, &maps.ks, D, t.kv_head, slot0[c], cb);
+            tma_load_3d(base + Geo::kOffTailV + off * 16, &maps.vs, D, t.kv_head, slot0[c], cb);
+          }
         }
       }
     }
   };
-  // The MMA thread issues the copies: tiles 0 and 1 now, then tile j + 2 once
-  // every converter has released code stage j & 1; the table entries of the
-  // next tile to copy are read ahead.
-  int nt = 0;  // tiles whose copies are issued
+  auto issue_v = [&](int j, bool leader) {
+    const int st = j & 1;
+    const uint32_t cb = bar(Geo::kBarCodesV + st);
+    int slot0[kChunks];
+    uint32_t valid = 0;
+#pragma unroll
+    for (int s2 = 0; s2 < 2; ++s2) {
+      if (s2 == st) {
+#pragma unroll
+        for (int c = 0; c < kChunks; ++c) slot0[c] = kept_slot[s2][c];
+        valid = kept_valid[s2];
+      }
+    }
+    if (leader) {
+      mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * 16u * D);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        if ((valid >> c) & 1u) {
+          const uint32_t off = (uint32_t)(st * kN + 16 * c);
+          tma_load_3d(base + Geo::kOffCodeV + off * D, &maps.v, 0, t.kv_head, slot0[c], cb);
+        }
+      }
+    }
+  };
+  // The MMA warp issues the copies: tiles 0 and 1 now; then the K group of
+  // tile j + 2 once every converter has released the K codes of stage j & 1
+  // (and the V group of tile j is out: the chunk list is per stage), the V
+  // group once the V codes are released.  The table entries of the next
+  // tile to copy are read ahead.
+  int nk = 0, nv = 0;  // tiles whose K / V copies are issued
   int nx_blk[kChunks];
   uint32_t nx_off[kChunks];
   // Run by the whole of warp 0 (uniform state); the leader issues.
-  auto issue_next = [&](bool leader) {  // copies of tile nt (entries fetched), fetch tile nt + 1
+  auto issue_next_k = [&](bool leader) {  // K copies of tile nk (entries fetched), fetch tile nk + 1
     int slot0[kChunks];
     uint32_t valid;
     resolve_chunks(nx_blk, nx_off, slot0, valid);
-    issue_codes(nt, slot0, valid, leader);
-    ++nt;
-    if (nt < T) fetch_chunks(nt, nx_blk, nx_off);
+    issue_k(nk, slot0, valid, leader);
+    ++nk;
+    if (nk < T) fetch_chunks(nk, nx_blk, nx_off);
   };
   // ---- Q tile -> staging (swizzled rows), all warps: lanes_per_row lanes
   // hold one row (16 bytes each, coalesced); the row's largest exponent
@@ -334,23 +379,25 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   }
   int blk1[kChunks];
   uint32_t off1[kChunks];
-  if (warp == 0 && T > 0) {
+  if (warp == kCopyWarp && T > 0) {
     fetch_chunks(0, nx_blk, nx_off);
     if (T > 1) fetch_chunks(1, blk1, off1);
   }
   __syncthreads();  // barriers initialised
-  if (warp == 0 && T > 0) {
+  if (warp == kCopyWarp && T > 0) {
     const bool leader = elect_one();
     int slot0[kChunks];
     uint32_t valid;
     resolve_chunks(nx_blk, nx_off, slot0, valid);
-    issue_codes(0, slot0, valid, leader);
-    nt = 1;
+    issue_k(0, slot0, valid, leader);
+    issue_v(0, leader);
+    nk = nv = 1;
     if (T > 1) {
       resolve_chunks(blk1, off1, slot0, valid);
-      issue_codes(1, slot0, valid, leader);
-      nt = 2;
-      if (nt < T) fetch_chunks(nt, nx_blk, nx_off);
+      issue_k(1, slot0, valid, leader);
+      issue_v(1, leader);
+      nk = nv = 2;
+      if (nk < T) fetch_chunks(nk, nx_blk, nx_off);
     }
     __syncwarp();
   }
@@ -408,8 +455,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
   if (warp == 0) {
     // ======================= MMA issuer ========================================
     // The whole warp runs the loop with warp-uniform state (descriptors and
-    // counters stay in the uniform datapath); one elected lane issues.
+    // counters stay in the uniform datapath); one elected lane issues every
+    // MMA (the tensor core runs one thread's MMAs in order).
     if (T > 0) {
+      const int lane = tid & 31;
       const bool leader = elect_one();
       constexpr uint32_t idesc_s = tc::idesc_f16(kM, kN);
       constexpr uint32_t idesc_o = tc::idesc_f16(kM, D) | tc::kBMajorMN;
@@ -438,44 +487,43 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
                        d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
           tc::mma_commit(bar(Geo::kBarODone));
-          tc::mma_commit(bar(Geo::kBarKvEmpty + st));
+          tc::mma_commit(bar(Geo::kBarVEmpty + st));
           if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
         }
         __syncwarp();
       };
       // S(j) needs K(j) and PV(j-2) issued (P(j-2) shares its buffer; the
       // tensor core runs one thread's MMAs in order).  PV(j) needs P(j) and
-      // V(j).  Issue whichever is ready: non-blocking tests (this warp polls
-      // several barriers), lane 0's results decide for the warp.
-      auto ready = [&](bool cond, uint32_t b, uint32_t parity) -> bool {
-        const bool r = cond && tc::mbar_test_wait(b, parity);
-        return __shfl_sync(0xffffffffu, r ? 1 : 0, 0) != 0;
-      };
+      // V(j).  One warp-wide non-blocking test per pass (lane 0: K(ns) in,
+      // lane 1: P(npv), lane 2: V(npv)) and one ballot decide for the warp;
+      // everything ready is issued, PV first.
       int ns = 0, npv = 0;
       bool ok = true;
       long long t_idle = clock64();
       while (npv < T) {
-        bool progressed = false;
-        if (ready(nt < T, bar(Geo::kBarCodesFree + (nt & 1)), (uint32_t)(((nt >> 1) - 1) & 1))) {
-          issue_next(leader);
-          progressed = true;
+        uint32_t tb = bar(Geo::kBarKFull + (ns & 1)), tp = (uint32_t)((ns >> 1) & 1);
+        bool cond = ns < T && ns <= npv + 1;
+        if (lane == 1 || lane == 2) {
+          tb = bar((lane == 1 ? Geo::kBarPFull : Geo::kBarVFull) + (npv & 1));
+          tp = (uint32_t)((npv >> 1) & 1);
+          cond = npv < ns;
         }
-        if (ready(ns < T && ns <= npv + 1, bar(Geo::kBarKFull + (ns & 1)), (uint32_t)((ns >> 1) & 1))) {
-          tc::fence_after_sync();
-          issue_s(ns);
-          ++ns;
-          progressed = true;
-        }
-        if (ready(npv < ns, bar(Geo::kBarPFull + (npv & 1)), (uint32_t)((npv >> 1) & 1)) &&
-            ready(true, bar(Geo::kBarVFull + (npv & 1)), (uint32_t)((npv >> 1) & 1))) {
+        const bool r = tc::mbar_test_wait(tb, tp) && cond;
+        const uint32_t rb = __ballot_sync(0xffffffffu, r);
+        __syncwarp();  // orders the testing lanes' acquires before the leader's issues
+        if ((rb & 6u) == 6u) {
           tc::fence_after_sync();
           issue_pv(npv);
           ++npv;
-          progressed = true;
         }
-        if (progressed) {
+        if (rb & 1u) {
+          tc::fence_after_sync();
+          issue_s(ns);
+          ++ns;
+        }
+        if ((rb & 1u) || (rb & 6u) == 6u) {
           t_idle = clock64();
-        } else {
+        } else if (clock64() - t_idle > 20000) {  // idle a while: look for an abort
           const bool give_up = __shfl_sync(0xffffffffu, (*abort_flag != 0u) ? 1 : 0, 0) != 0;
           const bool timeout = __shfl_sync(0xffffffffu, (clock64() - t_idle > 2000000000LL) ? 1 : 0, 0) != 0;
           if (give_up || timeout) {
@@ -486,16 +534,48 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
       if (!ok && leader) {
-        // Drain whatever was issued before the tensor memory is freed, and
-        // let the last copies (at most two tiles in flight) land.
+        // Drain whatever was issued before the tensor memory is freed.
         tc::mma_commit(bar(Geo::kBarDrain));
         (void)tc::mbar_wait(bar(Geo::kBarDrain), 0u, 200000000LL);
-        for (int j = nt >= 2 ? nt - 2 : 0; j < nt; ++j)
-          (void)tc::mbar_wait(bar(Geo::kBarCodes + (j & 1)), (uint32_t)((j >> 1) & 1), 200000000LL);
       }
     }
     __syncwarp();
-  } else if (!is_softmax) {
+  } else if (warp == kCopyWarp) {
+    // ======================= copy producer =====================================
+    // Tiles 0 and 1 went out before Q was staged.  Step i copies the K codes
+    // of tile i + 1 (once K(i - 1) is converted) and then the V codes of
+    // tile i (once V(i - 2) is), the order in which the converters release
+    // them.
+    if (T > 2) {
+      const bool leader = elect_one();
+      bool ok = true;
+      for (int i = 1; i < T; ++i) {
+        if (i + 1 < T) {
+          const int j = i + 1;
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesKFree + (j & 1)),
+                                                      (uint32_t)(((j >> 1) - 1) & 1), abort_flag));
+          if (!ok) break;
+          issue_next_k(leader);
+        }
+        if (i >= 2) {
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesVFree + (i & 1)),
+                                                      (uint32_t)(((i >> 1) - 1) & 1), abort_flag));
+          if (!ok) break;
+          issue_v(i, leader);
+          ++nv;
+        }
+      }
+      if (!ok && leader) {
+        // Let the last copies (at most two tiles of each group in flight)
+        // land before the shared memory is released.
+        for (int j = nk >= 2 ? nk - 2 : 0; j < nk; ++j)
+          (void)tc::mbar_wait(bar(Geo::kBarCodesK + (j & 1)), (uint32_t)((j >> 1) & 1), 200000000LL);
+        for (int j = nv >= 2 ? nv - 2 : 0; j < nv; ++j)
+          (void)tc::mbar_wait(bar(Geo::kBarCodesV + (j & 1)), (uint32_t)((j >> 1) & 1), 200000000LL);
+      }
+    }
+    __syncwarp();
+  } else if (is_conv) {
     // ======================= converters ========================================
     // A unit is (key n, 16 codes pc): consecutive threads take consecutive
     // 16-byte pieces of a code row (conflict-free reads).  The two 16-byte f16
@@ -520,9 +600,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       unit_key[i] = n;
       odd_mask |= (odd ? 1u : 0u) << i;
     }
-    auto convert = [&](int j, uint32_t tile, uint32_t codes, bool whole) {
+    auto convert = [&](int j, uint32_t tile, uint32_t codes, uint32_t valid, bool whole) {
       const int kv0 = kv_first + j * kN;
-      const uint32_t valid = chunk_valid[j & 1];
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
         if (ctid + i * Geo::kConv < kUnits) {
@@ -536,50 +615,70 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
         }
       }
     };
-    for (int j = 0; j < T; ++j) {
-      const int st = j & 1;
-      const int kv0 = kv_first + j * kN;
-      if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodes + st), (uint32_t)((j >> 1) & 1),
-                                                 abort_flag)))
-        break;
-      if (j >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarKvEmpty + st),
-                                                            (uint32_t)(((j >> 1) - 1) & 1), abort_flag)))
-        break;
-      const uint32_t valid = chunk_valid[st];
-      // every key of the tile in range and copied: no per-unit checks
-      const bool whole = valid == (1u << kChunks) - 1u && kv0 >= t.kv_lo && kv0 + kN <= t.kv_hi;
-      // The softmax's copy of the chunk mask: the issuer rewrites
-      // chunk_valid[st] for tile j + 2 before the softmax is done with j,
-      // while this copy is rewritten only after P(j) V(j) has completed.
-      if (ctid == 0) smask[st] = valid;
-      if constexpr (Geo::kPth) {
-        // Per-key scales, one thread per key (0 for a key without a copied
-        // row); each converter warp publishes the largest value scale it saw.
-        float vmax = 0.0f;
-        for (int n = ctid; n < kN; n += Geo::kConv) {
-          const int jj = kv0 + n;
-          const bool live = jj >= t.kv_lo && jj < t.kv_hi && ((valid >> (n >> 4)) & 1u);
-          const uint32_t off = (uint32_t)((st * kN + n) * 16);
-          const float ks = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
-          const float vs = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
-          sk[st * kN + n] = ks;
-          sv[st * kN + n] = vs;
-          vmax = fmaxf(vmax, vs);  // stays >= 0 (a NaN or negative scale is ignored)
+    // Step i converts K(i), then V(i - 1): K(i) needs S(i - 2) complete
+    // (its buffer), V(i - 1) needs P(i - 3) V(i - 3) complete, which the
+    // tensor core finishes later.  The chunk mask of a tile is read with its
+    // K codes and kept for its V codes (the issuer rewrites it for tile
+    // i + 2 once K(i) is converted).
+    uint32_t valid_k = 0, valid_v = 0;
+    bool whole_k = false, whole_v = false;
+    for (int i = 0; i <= T; ++i) {
+      if (i < T) {
+        const int st = i & 1, sd = i & (Geo::kSide - 1);
+        const int kv0 = kv_first + i * kN;
+        if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesK + st), (uint32_t)((i >> 1) & 1),
+                                                   abort_flag)))
+          break;
+        if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSFull + st),
+                                                              (uint32_t)(((i >> 1) - 1) & 1), abort_flag)))
+          break;
+        valid_k = chunk_valid[st];
+        // every key of the tile in range and copied: no per-unit checks
+        whole_k = valid_k == (1u << kChunks) - 1u && kv0 >= t.kv_lo && kv0 + kN <= t.kv_hi;
+        // Side data for the softmax in slot i % 4 (its reader, the softmax
+        // of tile i - 4, is done: S(i - 2) was issued after P(i - 4) V(i - 4)).
+        if (ctid == 0) smask[sd] = valid_k;
+        if constexpr (Geo::kPth) {
+          // Per-key scales, one thread per key (0 for a key without a copied
+          // row); each converter warp publishes the largest value scale it saw.
+          float vmax = 0.0f;
+          for (int n = ctid; n < kN; n += Geo::kConv) {
+            const int jj = kv0 + n;
+            const bool live = jj >= t.kv_lo && jj < t.kv_hi && ((valid_k >> (n >> 4)) & 1u);
+            const uint32_t off = (uint32_t)((st * kN + n) * 16);
+            const float ks = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
+            const float vs = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
+            sk[sd * kN + n] = ks;
+            sv[sd * kN + n] = vs;
+            vmax = fmaxf(vmax, vs);  // stays >= 0 (a NaN or negative scale is ignored)
+          }
+          const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
+          if ((ctid & 31) == 0) vmaxw[sd * 8 + (ctid >> 5)] = wmax;
         }
-        const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
-        if ((ctid & 31) == 0) vmaxw[st * 8 + (ctid >> 5)] = wmax;
+        mbar_arrive(bar(Geo::kBarSide + sd));
+        convert(i, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
+                base + Geo::kOffCodeK + (uint32_t)(st * kN * D), valid_k, whole_k);
+        tc::fence_async_smem();
+        mbar_arrive(bar(Geo::kBarKFull + st));
+        // done with the K codes and tails of stage st
+        mbar_arrive(bar(Geo::kBarCodesKFree + st));
       }
-      convert(j, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
-              base + Geo::kOffCodeK + (uint32_t)(st * kN * D), whole);
-      tc::fence_async_smem();
-      mbar_arrive(bar(Geo::kBarKFull + st));
-      convert(j, base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes),
-              base + Geo::kOffCodeV + (uint32_t)(st * kN * D), whole);
-      tc::fence_async_smem();
-      mbar_arrive(bar(Geo::kBarVFull + st));
-      // This thread is done with code stage st: the MMA thread refills it
-      // with tile j + 2 once every converter is.
-      mbar_arrive(bar(Geo::kBarCodesFree + st));
+      if (i >= 1) {
+        const int jv = i - 1, st = jv & 1;
+        if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesV + st), (uint32_t)((jv >> 1) & 1),
+                                                   abort_flag)))
+          break;
+        if (jv >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarVEmpty + st),
+                                                               (uint32_t)(((jv >> 1) - 1) & 1), abort_flag)))
+          break;
+        convert(jv, base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes),
+                base + Geo::kOffCodeV + (uint32_t)(st * kN * D), valid_v, whole_v);
+        tc::fence_async_smem();
+        mbar_arrive(bar(Geo::kBarVFull + st));
+        mbar_arrive(bar(Geo::kBarCodesVFree + st));
+      }
+      valid_v = valid_k;
+      whole_v = whole_k;
     }
     __syncwarp();
   } else {
@@ -610,10 +709,10 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
     for (int j = 0; j < T; ++j) {
       const int st = j & 1;
       const int kv0 = kv_first + j * kN;
-      // S(j) is in tensor memory; K(j) (and V(j)) side data is in smem.
+      const int sd = j & (Geo::kSide - 1);
+      // S(j) is in tensor memory; tile j's side data is in slot sd.
       ok = wait_or_abort(bar(Geo::kBarSFull + st), (uint32_t)((j >> 1) & 1), abort_flag) &&
-           wait_or_abort(bar(Geo::kBarKFull + st), (uint32_t)((j >> 1) & 1), abort_flag) &&
-           (!Geo::kPth || wait_or_abort(bar(Geo::kBarVFull + st), (uint32_t)((j >> 1) & 1), abort_flag));
+           wait_or_abort(bar(Geo::kBarSide + sd), (uint32_t)((j >> 2) & 1), abort_flag);
       ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory accesses are collective
       if (!ok) break;
       tc::fence_after_sync();
@@ -621,7 +720,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // Visible keys n of this row: lo_n <= n < hi_n, in a 16-key chunk
       // that was copied.  Masks are needed unless every row of the warp
       // sees the whole tile and every chunk is in.
-      const uint32_t cmask = smask[st];
+      const uint32_t cmask = smask[sd];
       const int lo_n = row_lo - kv0, hi_n = row_hi - kv0;
       const bool full = __all_sync(0xffffffffu, lo_n <= 0 && hi_n >= kN) && cmask == kAllChunks;
       float alpha = 1.0f;  // factor for O (score reference and value reference)
@@ -630,7 +729,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       if constexpr (Geo::kPth) {
         uint32_t mb = 0;
 #pragma unroll
-        for (int w = 0; w < kVMaxSlots; ++w) mb = max(mb, vmaxw[st * 8 + w]);
+        for (int w = 0; w < kVMaxSlots; ++w) mb = max(mb, vmaxw[sd * 8 + w]);
         const float smax = __uint_as_float(mb);
         if (smax > 0.0f) {
           int e;
@@ -653,7 +752,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       };
       // 64 scores from column c0: r in place, the row's maximum of r.
       auto raw64 = [&](auto full_c, uint32_t* v, int c0) -> float {
-        const float* skp = sk + st * kN + c0;
+        const float* skp = sk + sd * kN + c0;
         const int lo = lo_n - c0, hi = hi_n - c0;
         const uint32_t cm = cmask >> (c0 >> 4);
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
@@ -680,7 +779,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
       // weights clear of the f16 subnormal range; l carries the same factor.
       float lsum_tile = 0.0f;
       auto weights64 = [&](auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
-        const float* svp = sv + st * kN + c0;
+        const float* svp = sv + sd * kN + c0;
         float ls0 = 0.0f, ls1 = 0.0f;
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
