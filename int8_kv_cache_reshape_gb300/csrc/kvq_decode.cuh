@@ -78,35 +78,20 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
 // and lse_s = m_s + log2(l_s) (log2 units); the merged row is
 //   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
 // Each lane owns D/32 consecutive dims.  Partials are read through L2
-// (other warps wrote them).
+// (other warps wrote them).  Merges run at the end of the kernel (a cut
+// tile's last piece to finish is the one at the end of a warp's segment),
+// so their latency is the kernel's tail: lane s holds split s's lse (the
+// next row's is loaded while this row is merged) and the partial rows are
+// loaded 8 splits at a time.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeItem& m, int lane) {
   constexpr int kPer = D / 32;
+  constexpr int kBatch = 8;
   const int G = p.group;
   const int q0 = p.query_start_loc[m.req];
-  for (int n = 0; n < m.nrows; ++n) {
-    float M = -INFINITY;
-    for (int s = lane; s < m.nsplits; s += 32)
-      M = fmaxf(M, __ldcg(p.part_lse + m.part + s * m.nrows + n));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
-    float wsum = 0.0f;
-    for (int s = 0; s < m.nsplits; ++s) {
-      const int row = m.part + s * m.nrows + n;
-      const float lse = __ldcg(p.part_lse + row);
-      const float w = (lse == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(lse - M);
-      wsum += w;
-      const float* src = p.part_o + (int64_t)row * D + lane * kPer;
-#pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
-      }
-    }
+  const int ns = m.nsplits, nr = m.nrows;
+  const float* lse = p.part_lse + m.part;
+  auto store_row = [&](int n, const float (&acc)[kPer], float wsum) {
     const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
     const int R = m.row0 + n;
     const int tok = q0 + R / G;
@@ -115,6 +100,69 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
 #pragma unroll
     for (int e = 0; e < kPer; e += 2)
       *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+  };
+  if (ns <= 32) {
+    float l_next = lane < ns && nr > 0 ? __ldcg(lse + lane * nr) : -INFINITY;
+    for (int n = 0; n < nr; ++n) {
+      const float l_cur = l_next;
+      if (n + 1 < nr) l_next = lane < ns ? __ldcg(lse + lane * nr + n + 1) : -INFINITY;
+      float M = l_cur;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+      const float w_lane = (l_cur == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l_cur - M);
+      float wsum = w_lane;
+#pragma unroll
+      for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
+      float acc[kPer];
+#pragma unroll
+      for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
+      for (int s0 = 0; s0 < ns; s0 += kBatch) {
+        float2 v[kBatch][kPer / 2];
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const int s = min(s0 + u, ns - 1);
+          const float* src = p.part_o + (int64_t)(m.part + s * nr + n) * D + lane * kPer;
+#pragma unroll
+          for (int e = 0; e < kPer; e += 2) v[u][e / 2] = __ldcg(reinterpret_cast<const float2*>(src + e));
+        }
+#pragma unroll
+        for (int u = 0; u < kBatch; ++u) {
+          const float w = __shfl_sync(0xffffffffu, w_lane, (s0 + u) & 31);
+          if (s0 + u < ns) {
+#pragma unroll
+            for (int e = 0; e < kPer; e += 2) {
+              acc[e] += w * v[u][e / 2].x;
+              acc[e + 1] += w * v[u][e / 2].y;
+            }
+          }
+        }
+      }
+      store_row(n, acc, wsum);
+    }
+    return;
+  }
+  for (int n = 0; n < nr; ++n) {
+    float M = -INFINITY;
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + s * nr + n));
+#pragma unroll
+    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    float acc[kPer];
+#pragma unroll
+    for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
+    float wsum = 0.0f;
+    for (int s = 0; s < ns; ++s) {
+      const float l = __ldcg(lse + s * nr + n);
+      const float w = (l == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l - M);
+      wsum += w;
+      const float* src = p.part_o + (int64_t)(m.part + s * nr + n) * D + lane * kPer;
+#pragma unroll
+      for (int e = 0; e < kPer; e += 2) {
+        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
+        acc[e] += w * v.x;
+        acc[e + 1] += w * v.y;
+      }
+    }
+    store_row(n, acc, wsum);
   }
 }
 
