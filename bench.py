@@ -39,12 +39,12 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/; valid only while the kernel's sources
 # hash as they did when captured.
 PROFILED_TRAFFIC = {
-    2: {"bytes": 362.000896e6 + 5.402624e6, "profile": "profiles/splitkv_decode_decode_batch.md",
+    2: {"bytes": 361.43872e6 + 5.21216e6, "profile": "profiles/splitkv_decode_decode_batch.md",
          "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "a7763bcf8af7b2995e0506000ed312235a4528e0"},
-    3: {"bytes": 37.85984e6 + 0.655616e6, "profile": "profiles/prefill_attention_large_prefill.md",
+         "sha1": "d096121612351476e6113d589e8ba42863466e65"},
+    3: {"bytes": 37.863936e6 + 0.707328e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "b30d5205b969c9f064d5c2e2966d28410256f597"},
+         "sha1": "4ddbb9d55ca7e6e475fea8fdd9af029622e144b4"},
 }
 
 
