@@ -44,7 +44,7 @@ PROFILED_TRAFFIC = {
          "sha1": "d096121612351476e6113d589e8ba42863466e65"},
     3: {"bytes": 37.863936e6 + 0.707328e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "4ddbb9d55ca7e6e475fea8fdd9af029622e144b4"},
+         "sha1": "c672f0e22e493d8c4f61fd900051ff4dbf8e1ddf"},
 }
 
 

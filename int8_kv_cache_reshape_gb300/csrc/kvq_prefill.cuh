@@ -17,23 +17,32 @@
 //     S(j)'s buffer), and Q (D/2 columns of f16 pairs).  Both MMAs take A
 //     from tensor memory: S = Q K^T and O += P V read only K and V from
 //     shared memory.
-//   * Converter warps (1-3, 8-11): a thread takes (key, 32 dims) pieces; one
-//     block-table lookup serves the key's K and V rows (the caches share a
-//     layout); it loads 32 codes of each (one 32-byte sector), converts them
-//     exactly to f16 (every e4m3 / e5m2 / int8 value is an f16 value) and
-//     stores both as key-major rows in the 128-byte swizzle into a 2-stage
-//     ring.  K is read by the tensor core K-major, V MN-major, so neither
-//     needs a transpose.  The next tile's codes are loaded while the current
-//     tile is consumed.  Per-token-head scales and key-valid flags go beside.
-//   * Warp 0, one thread: issues S(j+1) as soon as K(j+1) is in and P(j-1)
-//     has been consumed, and O += P(j) V(j) as soon as P(j) and V(j) are in,
-//     whichever comes first; commits free the ring and signal the softmax.
-//   * Softmax warps (4-7): thread t owns row t (tensor-memory lane t).  A
-//     maximum pass over its row of S, then a weights pass that writes P in
-//     f16 straight into tensor memory.  The reference maximum is lazy (moved
-//     only when a score exceeds it by 2^8; weights are lifted by 2^6, so
-//     P <= 2^14); only when it moves does the thread wait for P(j-1) V(j-1)
-//     and rescale its row of O.  At the end it reads O and writes bf16.
+//   * Copy warp (11): bulk tensor copies (TMA) of each tile's K codes (with
+//     both per-token-head scale tails) and V codes into a two-stage code
+//     ring, in two groups with a barrier each; the K group of tile j + 2 goes
+//     out once K(j) is converted, the V group once V(j) is.
+//   * Converter warps (1-3, 8-10): a thread takes (key, 16 codes) units,
+//     converts the codes exactly to f16 (every e4m3 / e5m2 / int8 value is
+//     an f16 value) and stores them as key-major rows in the 128-byte
+//     swizzle into a two-stage K ring and V ring.  K is read by the tensor
+//     core K-major, V MN-major, so neither needs a transpose.  Step i
+//     converts K(i) (its buffer is free once S(i-2) is complete) and then
+//     V(i-1) (free once P(i-3) V(i-3) is): K runs a tile ahead of V.
+//     Per-key scales, the tile's chunk mask and its largest value scale go
+//     to one of four side-data slots for the softmax.
+//   * MMA warp (0): one elected lane issues S(j) as soon as K(j) is in and
+//     PV(j-2) was issued (P(j-2) shares the buffer; one thread's MMAs run in
+//     order), and O += P(j) V(j) as soon as P(j) and V(j) are in; one
+//     warp-wide non-blocking barrier test per pass decides for the warp.
+//   * Softmax warps (4-7): thread t owns row t (tensor-memory lane t).  One
+//     pass over its row of S, 64 scores per tensor-memory round trip: the
+//     round's maximum, then the weights, written as f16 straight into
+//     tensor memory.  The reference maximum is an integer (log2 units) and
+//     lazy: it moves only when a score exceeds it by 2^8 (weights are lifted
+//     by 2^6, so P <= 2^14), to the next integer at or above the maximum,
+//     and the weights, O and l already accumulated are rescaled by the exact
+//     power of two (O only after P(j-1) V(j-1) is complete).  At the end it
+//     reads O and writes bf16.
 //   * Q enters as f16 exactly: each row is scaled by a power of two that puts
 //     its largest |q| in [2^14, 2^15) (a bf16 significand fits in f16's);
 //     the scale, sm_scale, log2(e) and k_scale (per tensor) or the key's
@@ -44,7 +53,8 @@
 //     of two when ev grows and multiplied by 2^ev at the end.
 //   * Every mbarrier wait is bounded: on a timeout the kernel sets the
 //     schedule's error word, the other roles stop at their next wait, the
-//     MMA thread drains its tensor-core work and the tensor memory is freed.
+//     MMA warp drains its tensor-core work, the copy warp waits for its
+//     copies in flight, and the tensor memory is freed.
 #pragma once
 
 #include <cuda_fp16.h>
