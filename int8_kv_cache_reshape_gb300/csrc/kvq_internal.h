@@ -79,8 +79,12 @@ KVQ_HD constexpr size_t decode_smem_bytes(int dtype, int head_dim) {
 // exceed kTileMaxRows go to this kernel.
 constexpr int kPrefillRows = 128;
 constexpr int kPrefillStages = 2;        // K / V^T tiles in flight
-constexpr int kPrefillThreads = 384;     // 1 MMA, 4 softmax, 6 converter warps, 1 copy warp
-constexpr int kPrefillConvThreads = 192;
+// Threads of a prefill CTA: 1 MMA warp, 4 softmax warps, 1 copy warp and
+// the converter warps.  16 warps of at most 128 registers (the SM's 65,536)
+// at head_dim 64 and 128; at head_dim 256 the softmax and converters need
+// more registers than that without spilling, so 12 warps.
+KVQ_HD constexpr int prefill_threads(int head_dim) { return head_dim >= 256 ? 384 : 512; }
+KVQ_HD constexpr int prefill_conv_threads(int head_dim) { return prefill_threads(head_dim) - 6 * 32; }
 // Keys per KV tile: 128, or 64 at head_dim 256 (shared memory).
 KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 128; }
 // Tensor-memory columns: O (head_dim fp32), two S buffers (keys fp32 each,

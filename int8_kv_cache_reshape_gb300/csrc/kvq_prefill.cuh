@@ -10,22 +10,22 @@
 // item 3 (_prepare_kv_tile); vllm PR 50194 page, Key source snippet (the
 // large fp8 prefill with block_size 2176).
 //
-// GB300 design: one CTA of 12 warps per 128-row tile, warp-specialised and
-// pipelined through mbarriers.
+// GB300 design: one CTA of 16 warps (12 at head_dim 256) per 128-row tile,
+// warp-specialised and pipelined through mbarriers.
 //   * Tensor memory (512 columns): O (D fp32 columns), two S buffers (keys
 //     fp32 columns each; P(j) is written as f16 pairs over the first half of
 //     S(j)'s buffer), and Q (D/2 columns of f16 pairs).  Both MMAs take A
 //     from tensor memory: S = Q K^T and O += P V read only K and V from
 //     shared memory.
-//   * Copy warp (11): bulk tensor copies (TMA) of each tile's K codes (with
-//     both per-token-head scale tails) and V codes into a two-stage code
-//     ring, in two groups with a barrier each; the K group of tile j + 2 goes
-//     out once K(j) is converted, the V group once V(j) is.
-//   * Converter warps (1-3, 8-10): a thread takes (key, 16 codes) units,
-//     converts the codes exactly to f16 (every e4m3 / e5m2 / int8 value is
-//     an f16 value) and stores them as key-major rows in the 128-byte
-//     swizzle into a two-stage K ring and V ring.  K is read by the tensor
-//     core K-major, V MN-major, so neither needs a transpose.  Step i
+//   * Copy warp (the last): bulk tensor copies (TMA) of each tile's K codes
+//     (with both per-token-head scale tails) and V codes into a two-stage
+//     code ring, in two groups with a barrier each; the K group of tile
+//     j + 2 goes out once K(j) is converted, the V group once V(j) is.
+//   * Converter warps (1-3, and 8 up to the copy warp): a thread takes (key,
+//     16 codes) units, converts the codes exactly to f16 (every e4m3 / e5m2
+//     / int8 value is an f16 value) and stores them as key-major rows in the
+//     128-byte swizzle into a two-stage K ring and V ring.  K is read by the
+//     tensor core K-major, V MN-major, so neither needs a transpose.  Step i
 //     converts K(i) (its buffer is free once S(i-2) is complete) and then
 //     V(i-1) (free once P(i-3) V(i-3) is): K runs a tile ahead of V.
 //     Per-key scales, the tile's chunk mask and its largest value scale go
@@ -72,8 +72,8 @@ template <int DT, int D>
 struct PrefillGeom {
   static constexpr int kM = kPrefillRows;      // packed rows per tile
   static constexpr int kN = prefill_keys(D);   // keys per KV tile
-  static constexpr int kThreads = kPrefillThreads;
-  static constexpr int kConv = kPrefillConvThreads;
+  static constexpr int kThreads = prefill_threads(D);
+  static constexpr int kConv = prefill_conv_threads(D);
   static constexpr int kStages = kPrefillStages;
   static constexpr bool kPth = is_per_token_head(DT);
   static constexpr int kRow = row_bytes(DT, D);
@@ -107,7 +107,7 @@ struct PrefillGeom {
                     kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
                 "1024-byte operand tiles, 128-byte copy destinations");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
-  static_assert(kConv / 32 <= 8 && kSide == 4, "side data space");
+  static_assert((kN + 31) / 32 <= 8 && kSide == 4, "side data space");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
   // barrier slots (8 bytes each).  K and V travel separately: the K codes
   // of tile j + 2 are copied once K(j) is converted, K(j + 2) is converted
@@ -192,7 +192,7 @@ __device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
 }
 
 template <int DT, int D>
-__global__ void __launch_bounds__(kPrefillThreads, 1)
+__global__ void __launch_bounds__(prefill_threads(D), 1)
     prefill_attention_kernel(const AttnParams p, const __grid_constant__ PrefillMaps maps) {
   using Geo = PrefillGeom<DT, D>;
   constexpr int kM = Geo::kM, kN = Geo::kN;
@@ -241,7 +241,7 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
 
   // ---- converter state (warps 1-3, 8-11); converter 0 also issues the bulk
   // tensor copies of each tile's codes.
-  constexpr int kCopyWarp = 11;  // issues the bulk tensor copies
+  constexpr int kCopyWarp = Geo::kThreads / 32 - 1;  // issues the bulk tensor copies
   const bool is_conv = (warp >= 1 && warp < 4) || (warp >= 8 && warp < kCopyWarp);
   const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
   const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
@@ -663,7 +663,8 @@ __global__ void __launch_bounds__(kPrefillThreads, 1)
             vmax = fmaxf(vmax, vs);  // stays >= 0 (a NaN or negative scale is ignored)
           }
           const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
-          if ((ctid & 31) == 0) vmaxw[sd * 8 + (ctid >> 5)] = wmax;
+          // (only the first (kN + 31) / 32 converter warps hold keys)
+          if ((ctid & 31) == 0 && (ctid >> 5) < (kN + 31) / 32) vmaxw[sd * 8 + (ctid >> 5)] = wmax;
         }
         mbar_arrive(bar(Geo::kBarSide + sd));
         convert(i, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
@@ -956,7 +957,7 @@ int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
-  kern<<<(unsigned)num_tiles, kPrefillThreads, smem, stream>>>(p, maps);
+  kern<<<(unsigned)num_tiles, prefill_threads(D), smem, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 
