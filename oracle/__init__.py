@@ -35,7 +35,7 @@ _SRC = os.path.join(_HERE, "kvq_oracle.c")
 _BUILD_DIR = os.path.join(_HERE, "_build", platform.machine())
 _LIB_PATH = os.path.join(_BUILD_DIR, "libkvq_oracle.so")
 
-AUTO, FP8_E4M3, FP8_E5M2, INT8_PER_TOKEN_HEAD, FP8_PER_TOKEN_HEAD = range(5)
+AUTO, FP8_E4M3, FP8_E5M2, INT8_PER_TOKEN_HEAD, FP8_PER_TOKEN_HEAD, FP8_E5M2_PER_TOKEN_HEAD = range(6)
 E4M3, E5M2 = 0, 1
 
 _lock = threading.Lock()

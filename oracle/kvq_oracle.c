@@ -31,8 +31,10 @@
  *     "clamping" of [P3] Review read as saturation, not truncation).
  *   - The quotient x / scale is a correctly rounded binary32 division.
  *   - int8 encoding: round half to even, clamp to [-128, 127].
- *   - Per-token-head: s = amax / qmax in binary32, qmax = 127 (int8) or
- *     448 (fp8 = e4m3); s == 0 gives all-zero codes.  Row layout:
+ *   - Per-token-head: s = amax / qmax in binary32, qmax = 127 (int8), 448
+ *     (fp8 = e4m3) or 57344 (fp8 e5m2, the "other scale granularities" of
+ *     [P3] Risks applied to the e5m2 format); s == 0 gives all-zero codes.
+ *     Row layout:
  *     [D codes][s as little-endian binary32][12 zero bytes].
  *   - Paged layout: cache[block][slot_in_block][kv_head][row bytes].
  *   - Query row i of a request with Q queries and L keys sits at position
@@ -53,9 +55,11 @@
 #endif
 
 /* dtype numbering: 0..2 follow the kv_cache_dtype indices printed in [P2]'s
- * source snippet; 3 and 4 are the per-token-head modes of [P3]. */
+ * source snippet; 3 and 4 are the per-token-head modes of [P3]; 5 is the
+ * per-token-head mode with e5m2 codes. */
 enum { KVO_AUTO = 0, KVO_FP8_E4M3 = 1, KVO_FP8_E5M2 = 2,
-       KVO_INT8_PER_TOKEN_HEAD = 3, KVO_FP8_PER_TOKEN_HEAD = 4 };
+       KVO_INT8_PER_TOKEN_HEAD = 3, KVO_FP8_PER_TOKEN_HEAD = 4,
+       KVO_FP8_E5M2_PER_TOKEN_HEAD = 5 };
 /* fp8 format selector for the scalar codec. */
 enum { KVO_E4M3 = 0, KVO_E5M2 = 1 };
 
@@ -154,7 +158,8 @@ int64_t kvo_row_bytes(int dtype, int head_dim) {
     case KVO_FP8_E4M3:
     case KVO_FP8_E5M2: return head_dim;
     case KVO_INT8_PER_TOKEN_HEAD:
-    case KVO_FP8_PER_TOKEN_HEAD: return (int64_t)head_dim + 16;
+    case KVO_FP8_PER_TOKEN_HEAD:
+    case KVO_FP8_E5M2_PER_TOKEN_HEAD: return (int64_t)head_dim + 16;
     default: return -1;
   }
 }
@@ -199,7 +204,8 @@ static void write_row(int dtype, const uint16_t* x, int D, float tensor_scale,
   /* per-token-head: dynamic scale from the row's absolute maximum. */
   {
     float amax = 0.0f, s;
-    float qmax = dtype == KVO_INT8_PER_TOKEN_HEAD ? 127.0f : 448.0f;
+    float qmax = dtype == KVO_INT8_PER_TOKEN_HEAD ? 127.0f
+                 : dtype == KVO_FP8_E5M2_PER_TOKEN_HEAD ? 57344.0f : 448.0f;
     for (int d = 0; d < D; ++d) {
       float a = fabsf(bf16_to_float(x[d]));
       if (a > amax) amax = a;
@@ -216,7 +222,7 @@ static void write_row(int dtype, const uint16_t* x, int D, float tensor_scale,
         int8_t c = kvo_int8_encode(y);
         memcpy(&row[d], &c, 1);
       } else {
-        row[d] = kvo_fp8_encode(KVO_E4M3, y);
+        row[d] = kvo_fp8_encode(dtype == KVO_FP8_E5M2_PER_TOKEN_HEAD ? KVO_E5M2 : KVO_E4M3, y);
       }
     }
     store_f32_le(row + D, s);
@@ -277,6 +283,8 @@ static double dequant(int dtype, const uint8_t* row, int d, int D,
     }
     case KVO_FP8_PER_TOKEN_HEAD:
       return kvo_fp8_decode(KVO_E4M3, row[d]) * (double)load_f32_le(row + D);
+    case KVO_FP8_E5M2_PER_TOKEN_HEAD:
+      return kvo_fp8_decode(KVO_E5M2, row[d]) * (double)load_f32_le(row + D);
     default:
       return NAN;
   }

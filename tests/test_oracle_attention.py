@@ -19,7 +19,8 @@ from int8_kv_cache_reshape_gb300 import workloads as W
 
 DT = {"auto": oracle.AUTO, "fp8_e4m3": oracle.FP8_E4M3,
       "fp8_e5m2": oracle.FP8_E5M2, "int8_per_token_head": oracle.INT8_PER_TOKEN_HEAD,
-      "fp8_per_token_head": oracle.FP8_PER_TOKEN_HEAD}
+      "fp8_per_token_head": oracle.FP8_PER_TOKEN_HEAD,
+      "fp8_e5m2_per_token_head": oracle.FP8_E5M2_PER_TOKEN_HEAD}
 
 
 def _cache(wl):
@@ -56,7 +57,7 @@ def _dequant_library(wl, cache, scale):
     codes = rows[..., :D].contiguous()
     if dt in ("fp8_e4m3", "fp8_per_token_head"):
         val = codes.view(torch.float8_e4m3fn).to(torch.float64)
-    elif dt == "fp8_e5m2":
+    elif dt in ("fp8_e5m2", "fp8_e5m2_per_token_head"):
         val = codes.view(torch.float8_e5m2).to(torch.float64)
     else:
         val = codes.view(torch.int8).to(torch.float64)
@@ -101,6 +102,7 @@ CASES = [
     ("fp8_e5m2", dict(query_lens=[3, 1, 6], seq_lens=[50, 70, 6], hq=8, hkv=2, D=64)),
     ("int8_per_token_head", dict(query_lens=[5, 1], seq_lens=[40, 33], hq=4, hkv=4, D=128)),
     ("fp8_per_token_head", dict(query_lens=[2, 4], seq_lens=[19, 64], hq=6, hkv=2, D=64)),
+    ("fp8_e5m2_per_token_head", dict(query_lens=[3, 1], seq_lens=[30, 45], hq=4, hkv=2, D=64)),
     ("auto", dict(query_lens=[4], seq_lens=[21], hq=2, hkv=1, D=64)),
 ]
 

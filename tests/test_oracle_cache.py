@@ -66,7 +66,8 @@ def test_per_tensor_matches_torch(fmt, dtype):
 
 
 @pytest.mark.parametrize("dtype", [oracle.INT8_PER_TOKEN_HEAD,
-                                   oracle.FP8_PER_TOKEN_HEAD])
+                                   oracle.FP8_PER_TOKEN_HEAD,
+                                   oracle.FP8_E5M2_PER_TOKEN_HEAD])
 def test_per_token_head_matches_torch(dtype):
     wl = W.custom("t", [2, 5], [33, 17], 4, 2, 128, 16, "int8_per_token_head",
                   12, token_scale_range=(0.1, 10.0))
@@ -77,13 +78,16 @@ def test_per_token_head_matches_torch(dtype):
     for x, cache in ((wl.key, kc), (wl.value, vc)):
         xf = x.float()
         amax = xf.abs().amax(dim=-1)                      # exact in fp32
-        qmax = 127.0 if dtype == oracle.INT8_PER_TOKEN_HEAD else 448.0
+        qmax = {oracle.INT8_PER_TOKEN_HEAD: 127.0, oracle.FP8_PER_TOKEN_HEAD: 448.0,
+                oracle.FP8_E5M2_PER_TOKEN_HEAD: 57344.0}[dtype]
         s = amax / torch.tensor(qmax, dtype=torch.float32)  # fp32 division
         y = xf / s.unsqueeze(-1)
         if dtype == oracle.INT8_PER_TOKEN_HEAD:
             codes = torch.round(y).clamp(-128, 127).to(torch.int8).view(torch.uint8)
-        else:
+        elif dtype == oracle.FP8_PER_TOKEN_HEAD:
             codes = y.clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        else:
+            codes = y.clamp(-57344, 57344).to(torch.float8_e5m2).view(torch.uint8)
         rows = _rows_at_slots(cache, slots, wl.block_size)
         assert np.array_equal(rows[..., :D], codes.numpy())
         assert np.array_equal(rows[..., D:D + 4].copy().view(np.float32)[..., 0],
@@ -92,13 +96,15 @@ def test_per_token_head_matches_torch(dtype):
         # the row's absmax element lands on +-qmax
         arg = xf.abs().argmax(dim=-1, keepdim=True)
         top = torch.gather(torch.from_numpy(rows[..., :D].copy()), -1, arg)
-        want = 127 if dtype == oracle.INT8_PER_TOKEN_HEAD else 0x7E
+        want = {oracle.INT8_PER_TOKEN_HEAD: 127, oracle.FP8_PER_TOKEN_HEAD: 0x7E,
+                oracle.FP8_E5M2_PER_TOKEN_HEAD: 0x7B}[dtype]
         assert np.all((top.numpy() & 0x7F) == want if dtype != oracle.INT8_PER_TOKEN_HEAD
                       else np.abs(top.numpy().view(np.int8)) == want)
 
 
 @pytest.mark.parametrize("dtype", [oracle.INT8_PER_TOKEN_HEAD,
-                                   oracle.FP8_PER_TOKEN_HEAD])
+                                   oracle.FP8_PER_TOKEN_HEAD,
+                                   oracle.FP8_E5M2_PER_TOKEN_HEAD])
 def test_per_token_head_zero_row(dtype):
     D, H = 64, 1
     key = np.zeros((1, H, D), np.uint16)

@@ -175,3 +175,4 @@ def test_row_bytes():
     assert oracle.row_bytes(oracle.FP8_E5M2, 64) == 64
     assert oracle.row_bytes(oracle.INT8_PER_TOKEN_HEAD, 128) == 144
     assert oracle.row_bytes(oracle.FP8_PER_TOKEN_HEAD, 256) == 272
+    assert oracle.row_bytes(oracle.FP8_E5M2_PER_TOKEN_HEAD, 128) == 144
