@@ -169,7 +169,8 @@ def kv_bytes_read(wl) -> int:
     some query of its request, once (the window bounds it)."""
     row = {"fp8_e4m3": wl.head_dim, "fp8_e5m2": wl.head_dim,
            "int8_per_token_head": wl.head_dim + 4,
-           "fp8_per_token_head": wl.head_dim + 4}[wl.kv_cache_dtype]
+           "fp8_per_token_head": wl.head_dim + 4,
+           "fp8_e5m2_per_token_head": wl.head_dim + 4}[wl.kv_cache_dtype]
     total = 0
     for Q, L in zip(wl.query_lens, wl.seq_lens):
         if Q == 0:

@@ -65,6 +65,10 @@ extern "C" {
  *   KVQ_FP8_E5M2             OCP E5M2 codes, per-tensor scale, row = D bytes
  *   KVQ_INT8_PER_TOKEN_HEAD  int8 codes + inline fp32 scale, row = D+16 bytes
  *   KVQ_FP8_PER_TOKEN_HEAD   E4M3FN codes + inline fp32 scale, row = D+16 bytes
+ *   KVQ_FP8_E5M2_PER_TOKEN_HEAD  E5M2 codes + inline fp32 scale, row = D+16
+ *                            bytes: [P3]'s per-token-head scaling with the
+ *                            other fp8 format (its Risks name other scale
+ *                            granularities as the next modes)
  *
  * Per-token-head row layout: [D codes][scale: little-endian fp32][12 zero
  * bytes]; the 16-byte pad keeps every row 16-byte aligned.
@@ -74,7 +78,8 @@ typedef enum {
   KVQ_FP8_E4M3 = 1,
   KVQ_FP8_E5M2 = 2,
   KVQ_INT8_PER_TOKEN_HEAD = 3,
-  KVQ_FP8_PER_TOKEN_HEAD = 4
+  KVQ_FP8_PER_TOKEN_HEAD = 4,
+  KVQ_FP8_E5M2_PER_TOKEN_HEAD = 5
 } kvq_dtype_t;
 
 /* Opaque schedule (work list + sizes), owned by the library. */
@@ -82,7 +87,8 @@ typedef struct kvq_sched kvq_sched_t;
 
 /* Parse a kv_cache_dtype string.  Accepts "auto" (the default of [P2]
  * Breakdown item 2), "fp8" (alias of fp8_e4m3), "fp8_e4m3", "fp8_e5m2",
- * "int8_per_token_head", "fp8_per_token_head".  s == NULL or "" reads as
+ * "int8_per_token_head", "fp8_per_token_head", "fp8_e5m2_per_token_head".
+ * s == NULL or "" reads as
  * "auto".  Unknown strings: KVQ_E_INVALID_ARG. */
 KVQ_API int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out);
 
@@ -112,7 +118,8 @@ KVQ_API int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
  *                     round-to-nearest-even and saturation to +-448 (e4m3) /
  *                     +-57344 (e5m2).  Must be finite and > 0 for those
  *                     dtypes; ignored otherwise.
- * Per-token-head: s = amax/qmax in fp32 (qmax 127 for int8, 448 for fp8),
+ * Per-token-head: s = amax/qmax in fp32 (qmax 127 for int8, 448 for fp8
+ * e4m3, 57344 for fp8 e5m2),
  * code = Q(x / s) (int8: round half to even, clamp [-128,127]); s == 0 gives
  * zero codes.  Inputs must be finite.  num_tokens == 0 is a no-op. */
 KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,

@@ -69,11 +69,9 @@ __device__ __forceinline__ void write_part(const uint4 x, float tensor_scale, ui
 #pragma unroll
     for (int off = TPR / 2; off > 0; off >>= 1)
       m = fmaxf(m, __shfl_xor_sync(0xffffffffu, m, off));
-    const float qmax = DT == KVQ_INT8_PER_TOKEN_HEAD ? 127.0f : 448.0f;
-    const float s = __fdiv_rn(m, qmax);
+    const float s = __fdiv_rn(m, per_token_head_qmax(DT));
     uint32_t lo = 0, hi = 0;
-    if (s != 0.0f) quantise8<DT == KVQ_INT8_PER_TOKEN_HEAD ? KVQ_INT8_PER_TOKEN_HEAD
-                                                           : KVQ_FP8_E4M3>(x, s, lo, hi);
+    if (s != 0.0f) quantise8<code_format(DT)>(x, s, lo, hi);
     if (active) {
       *reinterpret_cast<uint2*>(row + part * 8) = make_uint2(lo, hi);
       if (part == 0)
@@ -179,6 +177,7 @@ int launch_reshape_and_cache(const void* key, const void* value, int64_t num_tok
     KVQ_CACHE_CASE(KVQ_FP8_E5M2)
     KVQ_CACHE_CASE(KVQ_INT8_PER_TOKEN_HEAD)
     KVQ_CACHE_CASE(KVQ_FP8_PER_TOKEN_HEAD)
+    KVQ_CACHE_CASE(KVQ_FP8_E5M2_PER_TOKEN_HEAD)
     default:
       return KVQ_E_UNSUPPORTED;
   }

@@ -689,6 +689,7 @@ int launch_decode_d(const AttnParams& p, int dtype, int ntiles, cudaStream_t str
     KVQ_DECODE_CASE(KVQ_FP8_E5M2)
     KVQ_DECODE_CASE(KVQ_INT8_PER_TOKEN_HEAD)
     KVQ_DECODE_CASE(KVQ_FP8_PER_TOKEN_HEAD)
+    KVQ_DECODE_CASE(KVQ_FP8_E5M2_PER_TOKEN_HEAD)
     default:
       return KVQ_E_UNSUPPORTED;
   }

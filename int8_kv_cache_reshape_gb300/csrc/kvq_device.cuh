@@ -7,6 +7,7 @@
 #include <cuda_runtime.h>
 
 #include "../../include/kvq.h"
+#include "kvq_internal.h"
 
 namespace kvq {
 namespace dev {
@@ -73,8 +74,9 @@ __device__ __forceinline__ uint32_t int8x2_to_f16x2(uint32_t pair) {
 
 template <int DT>
 __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t pair) {
-  if constexpr (DT == KVQ_FP8_E5M2) return e5m2x2_to_f16x2(pair);
-  else if constexpr (DT == KVQ_INT8_PER_TOKEN_HEAD) return int8x2_to_f16x2(pair);
+  constexpr int F = code_format(DT);
+  if constexpr (F == KVQ_FP8_E5M2) return e5m2x2_to_f16x2(pair);
+  else if constexpr (F == KVQ_INT8_PER_TOKEN_HEAD) return int8x2_to_f16x2(pair);
   else return e4m3x2_to_f16x2(pair);
 }
 
@@ -82,11 +84,12 @@ __device__ __forceinline__ uint32_t codes_to_f16x2(uint32_t pair) {
 // 2-3.  The word is split into its 16-bit halves inside the asm block.
 template <int DT>
 __device__ __forceinline__ void word_to_f16x2x2(uint32_t w, uint32_t& lo, uint32_t& hi) {
-  if constexpr (DT == KVQ_FP8_E5M2) {
+  constexpr int F = code_format(DT);
+  if constexpr (F == KVQ_FP8_E5M2) {
     // E5M2 code = upper byte of the f16: place each byte above a zero byte.
     lo = prmt(w, 0u, 0x1404u);
     hi = prmt(w, 0u, 0x3424u);
-  } else if constexpr (DT == KVQ_INT8_PER_TOKEN_HEAD) {
+  } else if constexpr (F == KVQ_INT8_PER_TOKEN_HEAD) {
     // bias to unsigned, put each byte under the f16 exponent of 1024 (0x64),
     // subtract 1024 + 128.
     const uint32_t u = w ^ 0x80808080u;

@@ -187,6 +187,10 @@ int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out) {
   if (!std::strcmp(s, "fp8_e5m2")) { *out = KVQ_FP8_E5M2; return KVQ_OK; }
   if (!std::strcmp(s, "int8_per_token_head")) { *out = KVQ_INT8_PER_TOKEN_HEAD; return KVQ_OK; }
   if (!std::strcmp(s, "fp8_per_token_head")) { *out = KVQ_FP8_PER_TOKEN_HEAD; return KVQ_OK; }
+  if (!std::strcmp(s, "fp8_e5m2_per_token_head")) {
+    *out = KVQ_FP8_E5M2_PER_TOKEN_HEAD;
+    return KVQ_OK;
+  }
   return KVQ_E_INVALID_ARG;
 }
 

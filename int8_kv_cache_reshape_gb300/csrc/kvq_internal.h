@@ -25,9 +25,22 @@ namespace kvq {
 
 // ---- cache rows --------------------------------------------------------
 KVQ_HD constexpr bool is_per_token_head(int dtype) {
-  return dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD;
+  return dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD ||
+         dtype == KVQ_FP8_E5M2_PER_TOKEN_HEAD;
 }
-KVQ_HD constexpr bool is_valid_dtype(int dtype) { return dtype >= 0 && dtype <= 4; }
+KVQ_HD constexpr bool is_valid_dtype(int dtype) { return dtype >= 0 && dtype <= 5; }
+// The code format of a quantised dtype: KVQ_FP8_E4M3, KVQ_FP8_E5M2 or
+// KVQ_INT8_PER_TOKEN_HEAD (int8 codes).
+KVQ_HD constexpr int code_format(int dtype) {
+  return dtype == KVQ_FP8_E5M2 || dtype == KVQ_FP8_E5M2_PER_TOKEN_HEAD ? KVQ_FP8_E5M2
+         : dtype == KVQ_INT8_PER_TOKEN_HEAD                          ? KVQ_INT8_PER_TOKEN_HEAD
+                                                                      : KVQ_FP8_E4M3;
+}
+// Largest code magnitude a per-token-head scale maps the row's absmax to.
+KVQ_HD constexpr float per_token_head_qmax(int dtype) {
+  return dtype == KVQ_INT8_PER_TOKEN_HEAD ? 127.0f
+         : dtype == KVQ_FP8_E5M2_PER_TOKEN_HEAD ? 57344.0f : 448.0f;
+}
 // Bytes of one cached K or V element (the KV element size).
 KVQ_HD constexpr int kv_elem_bytes(int dtype) { return dtype == KVQ_AUTO ? 2 : 1; }
 // Bytes of one (token, kv_head) row: codes plus, per-token-head, a 16-byte
@@ -38,8 +51,7 @@ KVQ_HD constexpr int row_bytes(int dtype, int head_dim) {
 KVQ_HD constexpr bool head_dim_supported(int d) { return d == 64 || d == 128 || d == 256; }
 // Dtypes with built attention kernels (bf16 "auto" cache: not yet).
 KVQ_HD constexpr bool attention_dtype_supported(int dtype) {
-  return dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2 ||
-         dtype == KVQ_INT8_PER_TOKEN_HEAD || dtype == KVQ_FP8_PER_TOKEN_HEAD;
+  return dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2 || is_per_token_head(dtype);
 }
 
 // ---- split-KV decode kernel (stream decomposition) -------------------------

@@ -76,7 +76,6 @@ struct PrefillGeom {
   static constexpr int kConv = prefill_conv_threads(D);
   static constexpr int kStages = kPrefillStages;
   static constexpr bool kPth = is_per_token_head(DT);
-  static constexpr int kRow = row_bytes(DT, D);
   static constexpr int kTileBytes = kN * D * 2;                     // one K or V tile (f16)
   static constexpr int kOffK = 0;                                   // stages x K tile
   static constexpr int kOffV = kOffK + kStages * kTileBytes;        // stages x V tile
@@ -971,6 +970,8 @@ int launch_prefill_d(const AttnParams& p, const PrefillMaps& maps, int dtype, in
       return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
     case KVQ_FP8_PER_TOKEN_HEAD:
       return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
+    case KVQ_FP8_E5M2_PER_TOKEN_HEAD:
+      return launch_prefill_instance<KVQ_FP8_E5M2_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
     default:
       return KVQ_E_UNSUPPORTED;
   }

@@ -21,7 +21,7 @@ E_INVALID_ARG, E_UNSUPPORTED, E_SCHED_MISMATCH = -1, -2, -3
 E_WORKSPACE_TOO_SMALL, E_CUDA, E_NO_MEMORY, E_TIMEOUT = -4, -5, -6, -7
 
 DTYPES = {"auto": 0, "fp8_e4m3": 1, "fp8_e5m2": 2, "int8_per_token_head": 3,
-          "fp8_per_token_head": 4}
+          "fp8_per_token_head": 4, "fp8_e5m2_per_token_head": 5}
 
 
 class KvqError(RuntimeError):

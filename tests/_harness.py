@@ -29,7 +29,8 @@ from int8_kv_cache_reshape_gb300 import workloads as W
 ORACLE_DT = {"auto": oracle.AUTO, "fp8_e4m3": oracle.FP8_E4M3,
              "fp8_e5m2": oracle.FP8_E5M2,
              "int8_per_token_head": oracle.INT8_PER_TOKEN_HEAD,
-             "fp8_per_token_head": oracle.FP8_PER_TOKEN_HEAD}
+             "fp8_per_token_head": oracle.FP8_PER_TOKEN_HEAD,
+             "fp8_e5m2_per_token_head": oracle.FP8_E5M2_PER_TOKEN_HEAD}
 FILL = 0xCD
 
 

@@ -34,7 +34,8 @@ def test_every_declared_function_is_exported():
 
 @pytest.mark.parametrize("s,want", [("auto", 0), (None, 0), ("", 0), ("fp8", 1),
                                     ("fp8_e4m3", 1), ("fp8_e5m2", 2),
-                                    ("int8_per_token_head", 3), ("fp8_per_token_head", 4)])
+                                    ("int8_per_token_head", 3), ("fp8_per_token_head", 4),
+                                    ("fp8_e5m2_per_token_head", 5)])
 def test_parse_dtype(s, want):
     assert kvq.parse_kv_cache_dtype(s) == want
 
@@ -51,6 +52,7 @@ def test_row_bytes():
     assert kvq.cache_row_bytes("fp8_e5m2", 256) == 256
     assert kvq.cache_row_bytes("int8_per_token_head", 128) == 144
     assert kvq.cache_row_bytes("fp8_per_token_head", 64) == 80
+    assert kvq.cache_row_bytes("fp8_e5m2_per_token_head", 128) == 144
     with pytest.raises(kvq.KvqError):
         kvq.cache_row_bytes("fp8_e4m3", 100)
 

@@ -36,12 +36,14 @@ def test_config1_tiny(cuda_device):
 
 
 @pytest.mark.parametrize("index,dtype", [(2, None), (3, None), (4, "int8_per_token_head"),
-                                         (4, "fp8_per_token_head"), (5, None)])
+                                         (4, "fp8_per_token_head"),
+                                         (4, "fp8_e5m2_per_token_head"), (5, None)])
 def test_scaled_configs(cuda_device, index, dtype):
     _check(W.scaled(index, kv_cache_dtype=dtype))
 
 
-DTYPES = ["fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head"]
+DTYPES = ["fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head",
+          "fp8_e5m2_per_token_head"]
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -132,7 +134,8 @@ def test_unwritten_pages_outside_window_are_ignored(cuda_device):
 
 
 @pytest.mark.parametrize("index,dtype", [(2, None), (3, None), (4, "int8_per_token_head"),
-                                         (4, "fp8_per_token_head"), (5, None)])
+                                         (4, "fp8_per_token_head"),
+                                         (4, "fp8_e5m2_per_token_head"), (5, None)])
 def test_full_size_sampled(cuda_device, index, dtype):
     """Full-size workloads in the benchmark's launch configuration: the
     whole batch runs on the GPU; sampled query tokens are compared with the

@@ -13,7 +13,8 @@ from _harness import FILL, GpuRun, oracle_cache
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ["auto", "fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head"]
+DTYPES = ["auto", "fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head",
+          "fp8_e5m2_per_token_head"]
 
 
 @pytest.mark.parametrize("dtype", DTYPES)
@@ -60,7 +61,8 @@ def test_every_finite_bf16_value(cuda_device, dtype, scale):
     assert np.array_equal(g.vc.cpu().numpy(), vc)
 
 
-@pytest.mark.parametrize("dtype", ["int8_per_token_head", "fp8_per_token_head"])
+@pytest.mark.parametrize("dtype", ["int8_per_token_head", "fp8_per_token_head",
+                                   "fp8_e5m2_per_token_head"])
 def test_per_token_head_special_rows(cuda_device, dtype):
     """Zero rows, rows of signed zeros, subnormal-only rows, huge rows and
     exact ties after the division."""
@@ -103,7 +105,8 @@ def test_strided_key_value(cuda_device):
 
 @pytest.mark.parametrize("index,dtype", [(1, None), (2, None), (3, None),
                                          (4, "int8_per_token_head"),
-                                         (4, "fp8_per_token_head"), (5, None)])
+                                         (4, "fp8_per_token_head"),
+                                         (4, "fp8_e5m2_per_token_head"), (5, None)])
 def test_full_size_cache_write_sampled(cuda_device, index, dtype):
     """The bulk cache write of each full-size workload; sampled tokens are
     compared with the oracle (written into a compact cache, block size 1)."""

@@ -21,7 +21,8 @@ from _harness import (GpuRun, _oracle_args, assert_attention_close, oracle_cache
 
 pytestmark = pytest.mark.gpu
 
-DTYPES = ["fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head"]
+DTYPES = ["fp8_e4m3", "fp8_e5m2", "int8_per_token_head", "fp8_per_token_head",
+          "fp8_e5m2_per_token_head"]
 
 
 def _check(wl):
@@ -94,7 +95,8 @@ def test_prefill_rows_without_blocks(cuda_device):
     assert float(abs(g.out_f32(range(64))).max()) == 0.0
 
 
-@pytest.mark.parametrize("dtype", ["int8_per_token_head", "fp8_per_token_head"])
+@pytest.mark.parametrize("dtype", ["int8_per_token_head", "fp8_per_token_head",
+                                   "fp8_e5m2_per_token_head"])
 def test_prefill_large_blocks_window_per_token_head(cuda_device, dtype):
     """block_size 2176 (vllm PR 50194 page, Key source snippet) with a
     sliding window and per-token-head scales at D = 256: the 16-key copies
