@@ -8,7 +8,7 @@ the CUDA path can both be fed from it.
 Every tensor is built on the CPU with ``torch.Generator('cpu')`` seeded by
 ``1000 + index`` so that the oracle and the GPU see identical bytes.
 
-Workloads (the shapes of the pages' cases, see the design doc for the recipe):
+Workloads (the shapes of the pages' cases):
   1 tiny      2 requests (Q, L) = (1, 37), (8, 8); Hq 4, Hkv 2, D 64, B 16,
               8 physical blocks, fp8_e4m3, k_scale 0.05, v_scale 0.04.
   2 decode    64 requests, Q = 1, L ~ U[1024, 4096]; Hq 32, Hkv 8, D 128,

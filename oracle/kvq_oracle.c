@@ -24,7 +24,7 @@
  *        absolute maximum, stored inline in a padded head row; the test's
  *        reference quantiser reproduces the kernel's clamping.
  *
- * Readings where the pages are silent (each is listed in the design doc):
+ * Readings where the pages are silent:
  *   - fp8 e4m3 is OCP E4M3FN (bias 7, no infinities, max 448); fp8 e5m2 is
  *     OCP E5M2 (bias 15, IEEE-like, max 57344).  Encoding rounds to nearest,
  *     ties to even, and saturates to the largest finite magnitude (the
