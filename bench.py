@@ -39,9 +39,9 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/; valid only while the kernel's sources
 # hash as they did when captured.
 PROFILED_TRAFFIC = {
-    2: {"bytes": 361.36448e6 + 5.870848e6, "profile": "profiles/splitkv_decode_decode_batch.md",
+    2: {"bytes": 361.074432e6 + 5.945344e6, "profile": "profiles/splitkv_decode_decode_batch.md",
          "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "c686f96a51f72bb3d468b924696cbc4d44715c88"},
+         "sha1": "142c9b241fa7d2a1b9daa1aaae457bce637bb4d0"},
     3: {"bytes": 37.864448e6 + 0.718592e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
          "sha1": "2783b1a4ea09df86ee80303a5ef6512053afc84f"},

@@ -77,70 +77,67 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
 // enable_kv_split), by one warp.  Piece s left o_s = (sum_j p_j v_j) / l_s
 // and lse_s = m_s + log2(l_s) (log2 units); the merged row is
 //   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
-// Each lane owns D/32 consecutive dims.  Partials are read through L2
-// (other warps wrote them).  Merges run at the end of the kernel (a cut
-// tile's last piece to finish is the one at the end of a warp's segment),
-// so their latency is the kernel's tail: lane s holds split s's lse (the
-// next row's is loaded while this row is merged) and the partial rows are
-// loaded 8 splits at a time.
+// Partials are read through L2 (other warps wrote them).  Merges run at the
+// end of the kernel (a cut tile's last piece to finish is the one at the end
+// of a warp's segment), so their latency is the kernel's tail: with at most
+// 16 splits the rows are merged side by side -- lpr lanes per row, each with
+// a run of D / lpr dims -- and every split's partial of a 4-dim step is
+// loaded at once.
 template <int D>
 __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeItem& m, int lane) {
-  constexpr int kPer = D / 32;
-  constexpr int kBatch = 8;
+  constexpr int kMaxSplits = 16;
   const int G = p.group;
   const int q0 = p.query_start_loc[m.req];
   const int ns = m.nsplits, nr = m.nrows;
   const float* lse = p.part_lse + m.part;
-  auto store_row = [&](int n, const float (&acc)[kPer], float wsum) {
-    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+  auto out_row = [&](int n) {
     const int R = m.row0 + n;
-    const int tok = q0 + R / G;
-    const int head = m.kv_head * G + R % G;
-    uint16_t* dst = p.out + ((int64_t)tok * p.heads_q + head) * D + lane * kPer;
-#pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-      *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
+    return p.out + ((int64_t)(q0 + R / G) * p.heads_q + m.kv_head * G + R % G) * D;
   };
-  if (ns <= 32) {
-    float l_next = lane < ns && nr > 0 ? __ldcg(lse + lane * nr) : -INFINITY;
-    for (int n = 0; n < nr; ++n) {
-      const float l_cur = l_next;
-      if (n + 1 < nr) l_next = lane < ns ? __ldcg(lse + lane * nr + n + 1) : -INFINITY;
-      float M = l_cur;
+  if (ns <= kMaxSplits) {
+    const int np2 = nr <= 1 ? 1 : nr <= 2 ? 2 : nr <= 4 ? 4 : nr <= 8 ? 8 : 16;
+    const int lpr = min(32 / np2, D / 4);  // lanes per row
+    const int n = lane / lpr, sub = lane % lpr;
+    const bool active = n < nr;
+    const int per = D / lpr;               // dims per lane, a multiple of 4
+    float w[kMaxSplits];
+    float M = -INFINITY;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-      const float w_lane = (l_cur == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l_cur - M);
-      float wsum = w_lane;
+    for (int s = 0; s < kMaxSplits; ++s) {
+      w[s] = active && s < ns ? __ldcg(lse + s * nr + n) : -INFINITY;
+      M = fmaxf(M, w[s]);
+    }
+    float wsum = 0.0f;
 #pragma unroll
-      for (int off = 16; off > 0; off >>= 1) wsum += __shfl_xor_sync(0xffffffffu, wsum, off);
-      float acc[kPer];
+    for (int s = 0; s < kMaxSplits; ++s) {
+      w[s] = (w[s] == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(w[s] - M);
+      wsum += w[s];
+    }
+    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    if (!active) return;
+    const float* src = p.part_o + (int64_t)(m.part + n) * D + sub * per;  // split s: + s * nr * D
+    uint16_t* dst = out_row(n) + sub * per;
+    for (int d0 = 0; d0 < per; d0 += 4) {
+      float4 v[kMaxSplits];
 #pragma unroll
-      for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
-      for (int s0 = 0; s0 < ns; s0 += kBatch) {
-        float2 v[kBatch][kPer / 2];
+      for (int s = 0; s < kMaxSplits; ++s)
+        v[s] = s < ns ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)s * nr * D + d0))
+                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const int s = min(s0 + u, ns - 1);
-          const float* src = p.part_o + (int64_t)(m.part + s * nr + n) * D + lane * kPer;
-#pragma unroll
-          for (int e = 0; e < kPer; e += 2) v[u][e / 2] = __ldcg(reinterpret_cast<const float2*>(src + e));
-        }
-#pragma unroll
-        for (int u = 0; u < kBatch; ++u) {
-          const float w = __shfl_sync(0xffffffffu, w_lane, (s0 + u) & 31);
-          if (s0 + u < ns) {
-#pragma unroll
-            for (int e = 0; e < kPer; e += 2) {
-              acc[e] += w * v[u][e / 2].x;
-              acc[e + 1] += w * v[u][e / 2].y;
-            }
-          }
-        }
+      for (int s = 0; s < kMaxSplits; ++s) {
+        a0 += w[s] * v[s].x;
+        a1 += w[s] * v[s].y;
+        a2 += w[s] * v[s].z;
+        a3 += w[s] * v[s].w;
       }
-      store_row(n, acc, wsum);
+      *reinterpret_cast<uint2*>(dst + d0) =
+          make_uint2(dev::pack_bf16x2(a0 * inv, a1 * inv), dev::pack_bf16x2(a2 * inv, a3 * inv));
     }
     return;
   }
+  // More splits: one row at a time, each lane D/32 consecutive dims.
+  constexpr int kPer = D / 32;
   for (int n = 0; n < nr; ++n) {
     float M = -INFINITY;
     for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + s * nr + n));
@@ -162,7 +159,11 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
         acc[e + 1] += w * v.y;
       }
     }
-    store_row(n, acc, wsum);
+    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
+    uint16_t* dst = out_row(n) + lane * kPer;
+#pragma unroll
+    for (int e = 0; e < kPer; e += 2)
+      *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
   }
 }
 
