@@ -269,6 +269,58 @@ typedef struct {
 
 KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
 
+/* ---- the plan, for tests and tools (host copies; no device access) --------
+ * [P2] Breakdown item 1: the schedule is the single source of the tile and
+ * scratch sizes the kernels run with; these calls expose it for checking.
+ *
+ * A decode piece is a run of consecutive 16-token chunks of one row tile
+ * (<= 16 packed rows of one kv head), streamed by one warp.  The pieces of a
+ * launch class lie end to end in its flat chunk sequence, which is cut into
+ * equal segments, one per warp (segment w starts at floor(w * chunks /
+ * warps)); a tile cut by a segment boundary has several pieces, whose
+ * partial rows a merge item combines. */
+typedef struct {
+  int32_t launch;          /* decode launch class: 0 (tiles of <= 8 rows) or 1 */
+  int32_t req, kv_head, row0, nrows;
+  int32_t part;            /* first partial row of the piece in the workspace; -1: writes out */
+  int32_t merge;           /* merge item of a cut tile; -1: not cut */
+  int32_t key_lo, key_hi;  /* keys some row of the tile can see: [key_lo, key_hi) */
+  int32_t flat0;           /* the piece's first position in its class's chunk sequence */
+  int32_t chunk0;          /* that chunk's 16-token index within the request */
+  int32_t nchunks;         /* chunks in the piece */
+} kvq_plan_piece_t;
+
+typedef struct {
+  int32_t req, kv_head, row0, nrows;
+  int32_t part;            /* partial row of (split 0, row 0); split s row n at part + s*nrows + n */
+  int32_t nsplits;
+} kvq_plan_merge_t;
+
+typedef struct {
+  int32_t req, kv_head, row0, nrows;  /* up to 128 packed rows of one kv head */
+  int32_t key_lo, key_hi;             /* keys some row of the tile can see */
+} kvq_plan_prefill_tile_t;
+
+typedef struct {
+  int64_t num_pieces, num_merges, num_prefill_tiles;
+  int64_t num_chunks[2];   /* per decode launch class */
+  int32_t num_warps[2];    /* per decode launch class */
+} kvq_plan_sizes_t;
+
+KVQ_API int kvq_sched_get_plan_sizes(const kvq_sched_t* sched, kvq_plan_sizes_t* out);
+
+/* Copy the plan: pieces (class 0 then class 1, each in flat order), the
+ * first piece of every warp's segment (class 0's warps then class 1's, as
+ * indices into `pieces`; -1 for an empty segment), merge items and prefill
+ * tiles (in launch order).  Any array may be NULL; otherwise its capacity
+ * must hold the count from kvq_sched_get_plan_sizes (warps: num_warps[0] +
+ * num_warps[1]), else KVQ_E_INVALID_ARG and nothing is written. */
+KVQ_API int kvq_sched_export_plan(const kvq_sched_t* sched, kvq_plan_piece_t* pieces,
+                                  int64_t pieces_cap, int32_t* warp_first_piece,
+                                  int64_t warps_cap, kvq_plan_merge_t* merges,
+                                  int64_t merges_cap, kvq_plan_prefill_tile_t* tiles,
+                                  int64_t tiles_cap);
+
 /* Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
  * kernel run with this schedule gave up waiting for the tensor core (a
  * bounded wait of about a second; the kernel then released its tensor

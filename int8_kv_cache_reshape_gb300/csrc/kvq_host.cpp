@@ -491,6 +491,76 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   return KVQ_OK;
 }
 
+int kvq_sched_get_plan_sizes(const kvq_sched_t* s, kvq_plan_sizes_t* out) {
+  if (!s || !out) return KVQ_E_INVALID_ARG;
+  std::memset(out, 0, sizeof(*out));
+  out->num_pieces = (int64_t)s->pieces.size();
+  out->num_merges = (int64_t)s->merges.size();
+  out->num_prefill_tiles = (int64_t)s->prefill.size();
+  for (int c = 0; c < 2; ++c) {
+    out->num_chunks[c] = s->launch[c].num_chunks;
+    out->num_warps[c] = s->launch[c].num_warps;
+  }
+  return KVQ_OK;
+}
+
+int kvq_sched_export_plan(const kvq_sched_t* s, kvq_plan_piece_t* pieces, int64_t pieces_cap,
+                          int32_t* warp_first_piece, int64_t warps_cap, kvq_plan_merge_t* merges,
+                          int64_t merges_cap, kvq_plan_prefill_tile_t* tiles, int64_t tiles_cap) {
+  if (!s) return KVQ_E_INVALID_ARG;
+  const int64_t nw = (int64_t)s->launch[0].num_warps + s->launch[1].num_warps;
+  if ((pieces && pieces_cap < (int64_t)s->pieces.size()) || (warp_first_piece && warps_cap < nw) ||
+      (merges && merges_cap < (int64_t)s->merges.size()) ||
+      (tiles && tiles_cap < (int64_t)s->prefill.size()))
+    return KVQ_E_INVALID_ARG;
+  for (int c = 0; c < 2; ++c) {
+    const DecodeLaunch& dl = s->launch[c];
+    if (pieces) {
+      for (int64_t i = 0; i < dl.num_pieces; ++i) {
+        const DecodePiece& pc = s->pieces[(size_t)(dl.piece_off + i)];
+        const int64_t end = i + 1 < dl.num_pieces ? s->pieces[(size_t)(dl.piece_off + i + 1)].flat0
+                                                  : dl.num_chunks;
+        kvq_plan_piece_t& o = pieces[dl.piece_off + i];
+        o.launch = c;
+        o.req = pc.req;
+        o.kv_head = pc.kv_head;
+        o.row0 = pc.row0;
+        o.nrows = pc.nrows;
+        o.part = pc.part;
+        o.merge = pc.merge;
+        o.key_lo = pc.any_lo;
+        o.key_hi = pc.any_hi;
+        o.flat0 = pc.flat0;
+        o.chunk0 = pc.chunk0;
+        o.nchunks = (int32_t)(end - pc.flat0);
+      }
+    }
+    if (warp_first_piece) {
+      const int64_t base = c == 0 ? 0 : s->launch[0].num_warps;
+      for (int w = 0; w < dl.num_warps; ++w) {
+        // segment w of this class: [floor(w T / W), floor((w + 1) T / W))
+        const int64_t lo = (int64_t)w * dl.num_chunks / dl.num_warps;
+        const int64_t hi = (int64_t)(w + 1) * dl.num_chunks / dl.num_warps;
+        warp_first_piece[base + w] =
+            hi > lo ? (int32_t)(dl.piece_off + s->warp_piece[(size_t)(dl.warp_off + w)]) : -1;
+      }
+    }
+  }
+  if (merges) {
+    for (size_t i = 0; i < s->merges.size(); ++i) {
+      const MergeItem& m = s->merges[i];
+      merges[i] = kvq_plan_merge_t{m.req, m.kv_head, m.row0, m.nrows, m.part, m.nsplits};
+    }
+  }
+  if (tiles) {
+    for (size_t i = 0; i < s->prefill.size(); ++i) {
+      const PrefillTile& t = s->prefill[i];
+      tiles[i] = kvq_plan_prefill_tile_t{t.req, t.kv_head, t.row0, t.nrows, t.kv_lo, t.kv_hi};
+    }
+  }
+  return KVQ_OK;
+}
+
 int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   if (!s || !out) return KVQ_E_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));

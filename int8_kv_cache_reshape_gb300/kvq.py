@@ -12,6 +12,8 @@ import ctypes
 import os
 import re
 
+import numpy as np
+
 _HERE = os.path.dirname(os.path.abspath(__file__))
 LIB_PATH = os.path.join(_HERE, "libkvq.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
@@ -96,6 +98,27 @@ lib.kvq_sched_get_info.restype = _c.c_int
 lib.kvq_sched_get_info.argtypes = [_p, _c.POINTER(SchedInfo)]
 
 
+class PlanSizes(ctypes.Structure):
+    _fields_ = [("num_pieces", ctypes.c_int64), ("num_merges", ctypes.c_int64),
+                ("num_prefill_tiles", ctypes.c_int64), ("num_chunks", ctypes.c_int64 * 2),
+                ("num_warps", ctypes.c_int32 * 2)]
+
+
+# numpy layouts of kvq_plan_piece_t, kvq_plan_merge_t, kvq_plan_prefill_tile_t
+PLAN_PIECE = np.dtype([(n, np.int32) for n in (
+    "launch", "req", "kv_head", "row0", "nrows", "part", "merge", "key_lo", "key_hi", "flat0",
+    "chunk0", "nchunks")])
+PLAN_MERGE = np.dtype([(n, np.int32) for n in ("req", "kv_head", "row0", "nrows", "part",
+                                                "nsplits")])
+PLAN_PREFILL = np.dtype([(n, np.int32) for n in ("req", "kv_head", "row0", "nrows", "key_lo",
+                                                  "key_hi")])
+lib.kvq_sched_get_plan_sizes.restype = _c.c_int
+lib.kvq_sched_get_plan_sizes.argtypes = [_p, _c.POINTER(PlanSizes)]
+lib.kvq_sched_export_plan.restype = _c.c_int
+lib.kvq_sched_export_plan.argtypes = [_p, _p, _c.c_int64, _p, _c.c_int64, _p, _c.c_int64, _p,
+                                      _c.c_int64]
+
+
 def declared_functions() -> list:
     """Names of the functions include/kvq.h declares."""
     text = open(HEADER).read()
@@ -161,6 +184,22 @@ class Sched:
         inf = SchedInfo()
         _check(lib.kvq_sched_get_info(self.handle, _c.byref(inf)), "kvq_sched_get_info")
         return inf.as_dict()
+
+    def plan(self) -> dict:
+        """The schedule's plan as numpy arrays (kvq_sched_export_plan)."""
+        sz = PlanSizes()
+        _check(lib.kvq_sched_get_plan_sizes(self.handle, _c.byref(sz)), "kvq_sched_get_plan_sizes")
+        pieces = np.zeros(sz.num_pieces, PLAN_PIECE)
+        warps = np.zeros(sz.num_warps[0] + sz.num_warps[1], np.int32)
+        merges = np.zeros(sz.num_merges, PLAN_MERGE)
+        tiles = np.zeros(sz.num_prefill_tiles, PLAN_PREFILL)
+        _check(lib.kvq_sched_export_plan(
+            self.handle, pieces.ctypes.data, pieces.size, warps.ctypes.data, warps.size,
+            merges.ctypes.data, merges.size, tiles.ctypes.data, tiles.size),
+            "kvq_sched_export_plan")
+        return {"pieces": pieces, "warp_first_piece": warps, "merges": merges,
+                "prefill_tiles": tiles, "num_chunks": list(sz.num_chunks),
+                "num_warps": list(sz.num_warps)}
 
     def check_device(self) -> None:
         """Raise KvqError(E_TIMEOUT) if a kernel run with this schedule gave
