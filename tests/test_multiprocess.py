@@ -66,3 +66,23 @@ def test_reference_arm_under_torchrun_prints_one_line():
     res = json.loads(lines[0])
     assert res["impl"] == "reference" and res["n_gpus"] == 2 and res["value"] > 0
     assert res["cpu_baseline"]["kind"] == "oracle"
+
+
+def test_reference_arm_line_keeps_the_contract():
+    """One rank: the reference arm's JSON line carries the keys the driver
+    reads, with the oracle as its CPU baseline and zero host transfers."""
+    cmd = [sys.executable, "bench.py", "--impl", "reference", "--workload", "1", "--steps", "2",
+           "--warmup", "3"]
+    out = subprocess.run(cmd, cwd=ROOT, capture_output=True, text=True, timeout=300)
+    assert out.returncode == 0, out.stderr[-2000:]
+    lines = [l for l in out.stdout.splitlines() if l.startswith("{")]
+    assert len(lines) == 1
+    res = json.loads(lines[0])
+    for k in ("metric", "value", "unit", "n_gpus", "steps", "warmup", "ms_per_step",
+              "higher_is_better", "scaling", "vs_baseline", "dtype", "data", "config",
+              "cpu_baseline", "e2e", "impl"):
+        assert k in res, k
+    assert res["n_gpus"] == 1 and res["steps"] == 2 and res["warmup"] == 3
+    assert res["e2e"]["value"] == res["value"]
+    assert res["e2e"]["h2d_bytes_per_step"] == 0 and res["e2e"]["d2h_bytes_per_step"] == 0
+    assert res["cpu_baseline"]["value"] == res["value"] and res["cpu_baseline"]["cores"] >= 1
