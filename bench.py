@@ -44,7 +44,7 @@ PROFILED_TRAFFIC = {
          "sha1": "142c9b241fa7d2a1b9daa1aaae457bce637bb4d0"},
     3: {"bytes": 37.864448e6 + 0.718592e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "2783b1a4ea09df86ee80303a5ef6512053afc84f"},
+         "sha1": "160303ad39db27ace633acce9e3834c725e000d9"},
 }
 
 

@@ -238,8 +238,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     tc::tmem_relinquish();
   }
 
-  // ---- converter state (warps 1-3, 8-11); converter 0 also issues the bulk
-  // tensor copies of each tile's codes.
+  // ---- roles: warp 0 issues the MMAs, warps 4-7 run the softmax, the last
+  // warp issues the bulk tensor copies, the others convert codes to f16.
   constexpr int kCopyWarp = Geo::kThreads / 32 - 1;  // issues the bulk tensor copies
   const bool is_conv = (warp >= 1 && warp < 4) || (warp >= 8 && warp < kCopyWarp);
   const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
@@ -347,15 +347,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       }
     }
   };
-  // The MMA warp issues the copies: tiles 0 and 1 now; then the K group of
-  // tile j + 2 once every converter has released the K codes of stage j & 1
-  // (and the V group of tile j is out: the chunk list is per stage), the V
-  // group once the V codes are released.  The table entries of the next
-  // tile to copy are read ahead.
+  // The copy warp issues the copies: tiles 0 and 1 before Q is staged; then
+  // the K group of tile j + 2 once every converter has released the K codes
+  // of stage j & 1 (the V group of tile j is out by then: the chunk list is
+  // per stage), the V group once the V codes are released.  The table
+  // entries of the next tile to copy are read ahead.
   int nk = 0, nv = 0;  // tiles whose K / V copies are issued
   int nx_blk[kChunks];
   uint32_t nx_off[kChunks];
-  // Run by the whole of warp 0 (uniform state); the leader issues.
+  // Run by the whole copy warp (uniform state); the leader issues.
   auto issue_next_k = [&](bool leader) {  // K copies of tile nk (entries fetched), fetch tile nk + 1
     int slot0[kChunks];
     uint32_t valid;
