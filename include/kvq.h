@@ -93,7 +93,11 @@ typedef struct kvq_sched kvq_sched_t;
 KVQ_API int kvq_parse_kv_cache_dtype(const char* s, kvq_dtype_t* out);
 
 /* Bytes of one (token, kv_head) cache row: 2*D (AUTO), D (per-tensor fp8)
- * or D+16 (per-token-head).  head_dim must be a positive multiple of 16. */
+ * or D+16 (per-token-head).  [P3] Risks: the per-token-head scale is stored
+ * inline by padding the head size (here by 16 bytes: the fp32 scale and 12
+ * zero bytes, so every row stays 16-byte aligned); [P1] Risks: an fp8 row
+ * is half the bytes of a bf16 one.  head_dim must be a positive multiple
+ * of 16; KVQ_E_INVALID_ARG otherwise, or for an unknown dtype. */
 KVQ_API int kvq_cache_row_bytes(kvq_dtype_t dtype, int head_dim, size_t* out);
 
 /* reshape_and_cache -- quantise new K/V tokens into the paged caches.
@@ -238,14 +242,19 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
     int block_table_stride, int block_size, int64_t num_blocks, float sm_scale, int causal,
     int window, float soft_cap, float k_scale, float v_scale, void* out, void* stream);
 
-/* Free a schedule (NULL is a no-op).  Its device work list goes back to a
+/* Free a schedule (NULL is a no-op).  No counterpart on the pages (their
+ * schedule is a torch tensor that the garbage collector frees); it is the
+ * C ABI's ownership rule for the object get_scheduler_metadata returns.  Its device work list goes back to a
  * small library pool that later schedules on the same device reuse (no
  * cudaFree / cudaMalloc per step), so destroy a schedule only once the
  * attention calls that use it have completed on the device, as for any
  * memory the caller frees. */
 KVQ_API void kvq_sched_destroy(kvq_sched_t* sched);
 
-/* Summary of a schedule, for tests and benchmarks. */
+/* Summary of a schedule, for tests and benchmarks.  [P2] Breakdown item 1:
+ * the sizes the scheduler derived from the KV element size (kv_elem_bytes,
+ * row_bytes, workspace and shared-memory bytes) are the ones the kernels
+ * run with.  Returns KVQ_E_INVALID_ARG for a NULL argument. */
 typedef struct {
   int num_req, heads_q, heads_kv, head_dim;
   int dtype;                   /* kvq_dtype_t the schedule was built for      */
@@ -321,14 +330,17 @@ KVQ_API int kvq_sched_export_plan(const kvq_sched_t* sched, kvq_plan_piece_t* pi
                                   int64_t merges_cap, kvq_plan_prefill_tile_t* tiles,
                                   int64_t tiles_cap);
 
-/* Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
+/* No counterpart on the pages (their kernels have no bounded waits).
+ * Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
  * kernel run with this schedule gave up waiting for the tensor core (a
  * bounded wait of about a second; the kernel then released its tensor
  * memory and returned without writing its tile), else KVQ_OK.  Blocks until
  * the device is idle. */
 KVQ_API int kvq_sched_check_device(const kvq_sched_t* sched);
 
-/* Short English description of a status code (static storage). */
+/* Short English description of a status code (static storage; never NULL:
+ * unknown codes give "unknown status").  No counterpart on the pages: the
+ * C ABI returns status codes where their C++ entry points raise. */
 KVQ_API const char* kvq_status_string(int status);
 
 #ifdef __cplusplus

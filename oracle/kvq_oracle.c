@@ -109,33 +109,36 @@ double kvo_fp8_decode(int fmt, uint8_t code) {
   return sign ? -v : v;
 }
 
-/* fp8 encode of a binary32, by brute force: scan every non-negative finite
- * code and keep the nearest; on a tie keep the even code (round half to
- * even).  Magnitudes at or beyond the largest finite value saturate to it
+/* fp8 encode of a binary32: the nearest finite code, ties to the even code
+ * (round half to even).  The non-negative finite codes 0 .. max_code have
+ * strictly increasing values in both formats, so the nearest one is one of
+ * the two codes that bracket |y|: a bisection over the code range finds the
+ * largest code whose value is <= |y|, and the nearer of it and the next code
+ * wins.  Magnitudes at or beyond the largest finite value saturate to it
  * (satfinite), infinities included.  The sign bit is copied, so a negative
  * value that rounds to zero gives the negative-zero code 0x80.
  *
- * The distance |dec(c) - a| is exact in binary64 for the two codes that
- * bracket a (both are short multiples of a power of two within two binades
- * of a), so the tie test is exact; far codes may round but never win.
+ * Both distances are exact in binary64: |y| is a binary32 and the two
+ * bracketing code values are short multiples of a power of two within a
+ * binade of it, so the tie test is exact.
  * [P1] Key files: float_to_fp8e4m3_scalar; [P3] Review (clamping). */
 uint8_t kvo_fp8_encode(int fmt, float y) {
   uint8_t max_code = fmt == KVO_E4M3 ? 0x7E : 0x7B;
   uint8_t sign = signbit(y) ? 0x80 : 0x00;
-  uint8_t best = 0;
-  double a, best_dist;
+  int lo = 0, hi = max_code; /* invariant: dec(lo) <= a < dec(hi) */
+  double a, d_lo, d_hi;
   if (isnan(y)) return 0x7F;
   a = fabs((double)y);
   if (a >= kvo_fp8_decode(fmt, max_code)) return (uint8_t)(sign | max_code);
-  best_dist = a; /* distance to code 0 (value 0) */
-  for (int c = 1; c <= max_code; ++c) {
-    double d = fabs(kvo_fp8_decode(fmt, (uint8_t)c) - a);
-    if (d < best_dist || (d == best_dist && (c & 1) == 0)) {
-      best = (uint8_t)c;
-      best_dist = d;
-    }
+  while (hi - lo > 1) {
+    int mid = (lo + hi) / 2;
+    if (kvo_fp8_decode(fmt, (uint8_t)mid) <= a) lo = mid;
+    else hi = mid;
   }
-  return (uint8_t)(sign | best);
+  d_lo = a - kvo_fp8_decode(fmt, (uint8_t)lo);
+  d_hi = kvo_fp8_decode(fmt, (uint8_t)hi) - a;
+  if (d_lo < d_hi || (d_lo == d_hi && (lo & 1) == 0)) return (uint8_t)(sign | lo);
+  return (uint8_t)(sign | hi);
 }
 
 /* int8 encode: round half to even (rint under the default rounding mode),

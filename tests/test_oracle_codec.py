@@ -176,3 +176,36 @@ def test_row_bytes():
     assert oracle.row_bytes(oracle.INT8_PER_TOKEN_HEAD, 128) == 144
     assert oracle.row_bytes(oracle.FP8_PER_TOKEN_HEAD, 256) == 272
     assert oracle.row_bytes(oracle.FP8_E5M2_PER_TOKEN_HEAD, 128) == 144
+
+
+def _nearest_code_brute(values: np.ndarray, y: np.ndarray) -> np.ndarray:
+    """Nearest of the non-negative finite code values (index = code) to
+    |y|, ties to the even code, saturating; sign bit copied.  A plain scan
+    over every code in binary64, independent of the oracle's bisection."""
+    a = np.abs(y.astype(np.float64))[:, None]
+    d = np.abs(values[None, :] - a)
+    best = d.min(axis=1, keepdims=True)
+    codes = np.arange(values.size)
+    cand = np.where(d == best, codes[None, :], 10 ** 6)
+    # among equidistant codes (at most two) keep the even one
+    even = np.where((cand % 2 == 0) & (cand < 10 ** 6), cand, 10 ** 6).min(axis=1)
+    pick = np.where(even < 10 ** 6, even, cand.min(axis=1))
+    pick = np.where(a[:, 0] >= values[-1], values.size - 1, pick)
+    return (pick | np.where(np.signbit(y), 0x80, 0)).astype(np.uint8)
+
+
+@pytest.mark.parametrize("fmt", list(FMTS))
+def test_fp8_encode_matches_brute_force_scan(fmt):
+    """Every finite bf16 value divided by a handful of scales (the quotients
+    the cache writer encodes) against a plain scan of all codes."""
+    ofmt, _, _, _ = FMTS[fmt]
+    max_code = 0x7E if ofmt == oracle.E4M3 else 0x7B
+    values = np.array([oracle.fp8_decode(ofmt, c) for c in range(max_code + 1)])
+    bits = np.arange(1 << 16, dtype=np.uint32)
+    x = (bits << 16).view(np.float32)
+    x = x[np.isfinite(x)]
+    for s in (1.0, 0.0371, 1.0 / 448.0, 3.3e-5):
+        y = (x / np.float32(s)).astype(np.float32)
+        y = y[np.isfinite(y)]
+        got = oracle.fp8_encode_array(ofmt, y)
+        assert np.array_equal(got, _nearest_code_brute(values, y)), s
