@@ -240,6 +240,23 @@ def scaled(index: int, seed_offset: int = 0,
     raise ValueError(f"no scaled workload {index}")
 
 
+def alibi_slopes(heads_q: int):
+    """float32 [heads_q] ALiBi slopes, the usual geometric sequence
+    2^(-8 (h + 1) / n) over the next power of two n >= heads_q, interleaved
+    as in the ALiBi paper for head counts that are not powers of two."""
+    n = 1 << max(0, math.ceil(math.log2(max(1, heads_q))))
+    base = [2.0 ** (-8.0 * (h + 1) / n) for h in range(n)]
+    if n == heads_q:
+        return torch.tensor(base, dtype=torch.float32).numpy()
+    extra = [2.0 ** (-4.0 * (2 * h + 1) / n) for h in range(heads_q - n // 2)]
+    return torch.tensor(base[: n // 2] + extra, dtype=torch.float32).numpy()
+
+
+def sink_logits(heads_q: int, seed: int):
+    """float32 [heads_q] seeded sink logits ~ N(0, 2^2)."""
+    return (torch.randn((heads_q,), generator=_gen(seed), dtype=torch.float32) * 2.0).numpy()
+
+
 def bf16_bits(t: torch.Tensor):
     """uint16 numpy view of a bf16 tensor's bit patterns (CPU copy)."""
     return t.detach().cpu().contiguous().view(torch.int16).numpy().view("uint16")

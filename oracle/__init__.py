@@ -80,14 +80,14 @@ def _load():
         lib.kvo_attention.argtypes = [
             c.c_int, c.c_int, c.c_int, c.c_int, p, p, p, c.c_int, c.c_int, p,
             p, p, c.c_int, c.c_double, c.c_int, c.c_int, c.c_double,
-            c.c_float, c.c_float, p, c.c_int64, p]
+            c.c_float, c.c_float, p, p, p, c.c_int64, p]
         lib.kvo_attention_fp32_bound.restype = c.c_int
         lib.kvo_attention_fp32_bound.argtypes = lib.kvo_attention.argtypes
         lib.kvo_attention_probs.restype = c.c_int64
         lib.kvo_attention_probs.argtypes = [
             c.c_int, c.c_int, c.c_int, c.c_int, p, p, c.c_int, c.c_int, p, p,
             p, c.c_int, c.c_double, c.c_int, c.c_int, c.c_double, c.c_float,
-            c.c_int64, c.c_int, p]
+            p, p, c.c_int64, c.c_int, p, p]
         lib.kvo_num_threads.restype = c.c_int
         lib.kvo_num_threads.argtypes = []
         _lib = lib
@@ -156,30 +156,42 @@ def attention(q_bits: np.ndarray, key_cache: np.ndarray,
               value_cache: np.ndarray, query_start_loc, seq_lens, block_table,
               heads_kv: int, block_size: int, dtype: int, sm_scale: float,
               causal: bool, window: int, soft_cap: float, k_scale: float,
-              v_scale: float, tokens=None) -> np.ndarray:
+              v_scale: float, tokens=None, alibi_slopes=None, sinks=None) -> np.ndarray:
     """float32 [n, Hq, D] attention output for the listed query tokens
-    (all tokens when ``tokens`` is None)."""
+    (all tokens when ``tokens`` is None).  alibi_slopes / sinks: float32
+    [Hq] per q head, or None."""
     return _attention_call("kvo_attention", q_bits, key_cache, value_cache, query_start_loc,
                            seq_lens, block_table, heads_kv, block_size, dtype, sm_scale, causal,
-                           window, soft_cap, k_scale, v_scale, tokens)
+                           window, soft_cap, k_scale, v_scale, tokens, alibi_slopes, sinks)
 
 
 def attention_fp32_bound(q_bits: np.ndarray, key_cache: np.ndarray,
                          value_cache: np.ndarray, query_start_loc, seq_lens, block_table,
                          heads_kv: int, block_size: int, dtype: int, sm_scale: float,
                          causal: bool, window: int, soft_cap: float, k_scale: float,
-                         v_scale: float, tokens=None) -> np.ndarray:
+                         v_scale: float, tokens=None, alibi_slopes=None,
+                         sinks=None) -> np.ndarray:
     """float32 [n, Hq, D]: first-order bound on how far a binary32
     evaluation (binary32 scores and sums, 11-bit softmax weights) of the
     attention may land from the exact result (kvo_attention_fp32_bound)."""
     return _attention_call("kvo_attention_fp32_bound", q_bits, key_cache, value_cache,
                            query_start_loc, seq_lens, block_table, heads_kv, block_size, dtype,
-                           sm_scale, causal, window, soft_cap, k_scale, v_scale, tokens)
+                           sm_scale, causal, window, soft_cap, k_scale, v_scale, tokens,
+                           alibi_slopes, sinks)
+
+
+def _per_head(x, Hq):
+    if x is None:
+        return None
+    a = _c(x, np.float32).ravel()
+    if a.size != Hq:
+        raise ValueError("per-head array must have heads_q entries")
+    return a
 
 
 def _attention_call(fn, q_bits, key_cache, value_cache, query_start_loc, seq_lens, block_table,
                     heads_kv, block_size, dtype, sm_scale, causal, window, soft_cap, k_scale,
-                    v_scale, tokens):
+                    v_scale, tokens, alibi_slopes=None, sinks=None):
     q_bits = _c(q_bits, np.uint16)
     qsl = _c(query_start_loc, np.int32)
     sl = _c(seq_lens, np.int32)
@@ -190,11 +202,12 @@ def _attention_call(fn, q_bits, key_cache, value_cache, query_start_loc, seq_len
     tok = None if tokens is None else _c(tokens, np.int64)
     n = int(qsl[-1]) if tok is None else tok.size
     out = np.zeros((n, Hq, D), dtype=np.float32)
+    al, sk = _per_head(alibi_slopes, Hq), _per_head(sinks, Hq)
     rc = getattr(_load(), fn)(
         len(sl), Hq, heads_kv, D, _ptr(q_bits), _ptr(key_cache),
         _ptr(value_cache), block_size, dtype, _ptr(qsl), _ptr(sl), _ptr(bt),
         bt.shape[1], float(sm_scale), int(bool(causal)), int(window),
-        float(soft_cap), float(k_scale), float(v_scale), _ptr(tok),
+        float(soft_cap), float(k_scale), float(v_scale), _ptr(al), _ptr(sk), _ptr(tok),
         0 if tok is None else tok.size, _ptr(out))
     if rc != 0:
         raise ValueError(f"oracle {fn} rejected its arguments")
@@ -205,8 +218,9 @@ def attention_probs(q_bits: np.ndarray, key_cache: np.ndarray,
                     query_start_loc, seq_lens, block_table, heads_kv: int,
                     block_size: int, dtype: int, sm_scale: float, causal: bool,
                     window: int, soft_cap: float, k_scale: float, token: int,
-                    head_q: int) -> np.ndarray:
-    """Softmax weights (float64 [L]) of one query token and q head."""
+                    head_q: int, alibi_slopes=None, sinks=None, with_sink=False):
+    """Softmax weights (float64 [L]) of one query token and q head; with
+    ``with_sink`` also the sink's weight (a float)."""
     q_bits = _c(q_bits, np.uint16)
     qsl = _c(query_start_loc, np.int32)
     sl = _c(seq_lens, np.int32)
@@ -215,11 +229,13 @@ def attention_probs(q_bits: np.ndarray, key_cache: np.ndarray,
         bt = bt.reshape(len(sl), -1)
     _, Hq, D = q_bits.shape
     probs = np.zeros(max(1, int(sl.max())), dtype=np.float64)
+    sink_w = np.zeros(1, dtype=np.float64)
+    al, sk = _per_head(alibi_slopes, Hq), _per_head(sinks, Hq)
     L = _load().kvo_attention_probs(
         len(sl), Hq, heads_kv, D, _ptr(q_bits), _ptr(key_cache), block_size,
         dtype, _ptr(qsl), _ptr(sl), _ptr(bt), bt.shape[1], float(sm_scale),
         int(bool(causal)), int(window), float(soft_cap), float(k_scale),
-        int(token), int(head_q), _ptr(probs))
+        _ptr(al), _ptr(sk), int(token), int(head_q), _ptr(probs), _ptr(sink_w))
     if L < 0:
         raise ValueError("oracle attention_probs rejected its arguments")
-    return probs[:L].copy()
+    return (probs[:L].copy(), float(sink_w[0])) if with_sink else probs[:L].copy()

@@ -267,29 +267,41 @@ int kvo_reshape_and_cache(const uint16_t* key, const uint16_t* value,
   return 0;
 }
 
-/* Dequantised value of element d of one cache row (binary64). */
-static double dequant(int dtype, const uint8_t* row, int d, int D,
-                      float tensor_scale) {
+/* Dequantised values of one cache row (binary64): out[d] = dec(code_d) *
+ * scale, with the per-tensor scale (fp8_e4m3 / fp8_e5m2) or the row's
+ * inline scale (per-token-head); a bf16 row ("auto") is read as is.  `dec`
+ * is the fp8 decode of the row's format, tabulated once per call from
+ * kvo_fp8_decode (the same values). */
+static void dequant_row(int dtype, const double* dec, const uint8_t* row, int D,
+                        float tensor_scale, double* out) {
   switch (dtype) {
-    case KVO_AUTO: {
-      uint16_t b = (uint16_t)(row[2 * d] | (row[2 * d + 1] << 8));
-      return kvo_bf16_to_double(b);
-    }
+    case KVO_AUTO:
+      for (int d = 0; d < D; ++d) {
+        uint16_t b = (uint16_t)(row[2 * d] | (row[2 * d + 1] << 8));
+        out[d] = kvo_bf16_to_double(b);
+      }
+      return;
     case KVO_FP8_E4M3:
-      return kvo_fp8_decode(KVO_E4M3, row[d]) * (double)tensor_scale;
     case KVO_FP8_E5M2:
-      return kvo_fp8_decode(KVO_E5M2, row[d]) * (double)tensor_scale;
+      for (int d = 0; d < D; ++d) out[d] = dec[row[d]] * (double)tensor_scale;
+      return;
     case KVO_INT8_PER_TOKEN_HEAD: {
-      int8_t c;
-      memcpy(&c, &row[d], 1);
-      return (double)c * (double)load_f32_le(row + D);
+      double s = (double)load_f32_le(row + D);
+      for (int d = 0; d < D; ++d) {
+        int8_t c;
+        memcpy(&c, &row[d], 1);
+        out[d] = (double)c * s;
+      }
+      return;
     }
     case KVO_FP8_PER_TOKEN_HEAD:
-      return kvo_fp8_decode(KVO_E4M3, row[d]) * (double)load_f32_le(row + D);
-    case KVO_FP8_E5M2_PER_TOKEN_HEAD:
-      return kvo_fp8_decode(KVO_E5M2, row[d]) * (double)load_f32_le(row + D);
+    case KVO_FP8_E5M2_PER_TOKEN_HEAD: {
+      double s = (double)load_f32_le(row + D);
+      for (int d = 0; d < D; ++d) out[d] = dec[row[d]] * s;
+      return;
+    }
     default:
-      return NAN;
+      for (int d = 0; d < D; ++d) out[d] = NAN;
   }
 }
 
@@ -303,22 +315,25 @@ typedef struct {
   const uint8_t *key_cache, *value_cache;
   int block_size;
   int dtype;
+  int64_t row_bytes;
   const int32_t *query_start_loc, *seq_lens, *block_table;
   int block_table_stride;
   double sm_scale;
   int causal, window;
   double soft_cap;
   float k_scale, v_scale;
+  const float* alibi_slopes; /* [heads_q] or NULL */
+  const float* sinks;        /* [heads_q] or NULL */
+  double dec[256];           /* fp8 decode of the cache's code format */
 } attn_args;
 
 /* Address of the cache row of logical key j of request r, kv head h. */
 static const uint8_t* cache_row(const attn_args* a, const uint8_t* cache,
                                 int r, int64_t j, int h) {
-  int64_t row = kvo_row_bytes(a->dtype, a->head_dim);
   int64_t phys = a->block_table[(int64_t)r * a->block_table_stride +
                                 j / a->block_size];
   int64_t slot = phys * a->block_size + j % a->block_size;
-  return cache + (slot * a->heads_kv + h) * row;
+  return cache + (slot * a->heads_kv + h) * a->row_bytes;
 }
 
 static int request_of(const attn_args* a, int64_t tok) {
@@ -328,15 +343,25 @@ static int request_of(const attn_args* a, int64_t tok) {
   return -1;
 }
 
+/* Per-thread work buffers: D doubles each. */
+typedef struct {
+  double *q, *k, *v, *o, *e, *wv, *va;
+} row_bufs;
+
 /* Scores of query token `tok`, q head `hq` against every key of its request;
- * probs[j] is the softmax weight (0 for masked keys).  Returns L, or -1. */
-static int64_t row_probs(const attn_args* a, int64_t tok, int hq,
-                         double* probs, int64_t cap) {
+ * probs[j] is the softmax weight (0 for masked keys).  *sink_w receives the
+ * weight of the attention sink (0 without one).  Returns L, or -1.
+ *   z_j = sm_scale * (q . k_j);  z_j <- cap * tanh(z_j / cap) with a soft
+ *   cap;  z_j <- z_j + slope * (j - p) with ALiBi;  P = softmax over the
+ *   visible keys and, with a sink, the sink's logit s (no value). */
+static int64_t row_probs(const attn_args* a, int64_t tok, int hq, double* probs,
+                         double* sink_w, int64_t cap, const row_bufs* b) {
   int r = request_of(a, tok);
   int64_t L, Q, p;
   int G, hk, D = a->head_dim;
   const uint16_t* qrow;
-  double m = -INFINITY, sum = 0.0;
+  double m = -INFINITY, sum = 0.0, sink = -INFINITY;
+  *sink_w = 0.0;
   if (r < 0) return -1;
   L = a->seq_lens[r];
   Q = a->query_start_loc[r + 1] - a->query_start_loc[r];
@@ -345,21 +370,25 @@ static int64_t row_probs(const attn_args* a, int64_t tok, int hq,
   G = a->heads_q / a->heads_kv;
   hk = hq / G;
   qrow = a->q + (tok * a->heads_q + hq) * (int64_t)D;
+  for (int d = 0; d < D; ++d) b->q[d] = kvo_bf16_to_double(qrow[d]);
   for (int64_t j = 0; j < L; ++j) {
     int visible = (!a->causal || j <= p) && (a->window <= 0 || p - j < a->window);
-    const uint8_t* krow;
     double z = 0.0;
     if (!visible) {
       probs[j] = -INFINITY;
       continue;
     }
-    krow = cache_row(a, a->key_cache, r, j, hk);
-    for (int d = 0; d < D; ++d)
-      z += kvo_bf16_to_double(qrow[d]) * dequant(a->dtype, krow, d, D, a->k_scale);
+    dequant_row(a->dtype, a->dec, cache_row(a, a->key_cache, r, j, hk), D, a->k_scale, b->k);
+    for (int d = 0; d < D; ++d) z += b->q[d] * b->k[d];
     z *= a->sm_scale;
     if (a->soft_cap > 0.0) z = a->soft_cap * tanh(z / a->soft_cap);
+    if (a->alibi_slopes) z += (double)a->alibi_slopes[hq] * (double)(j - p);
     probs[j] = z;
     if (z > m) m = z;
+  }
+  if (a->sinks) {
+    sink = (double)a->sinks[hq];
+    if (sink > m) m = sink;
   }
   for (int64_t j = 0; j < L; ++j) {
     if (probs[j] == -INFINITY) {
@@ -369,28 +398,38 @@ static int64_t row_probs(const attn_args* a, int64_t tok, int hq,
     probs[j] = exp(probs[j] - m);
     sum += probs[j];
   }
-  for (int64_t j = 0; j < L; ++j) probs[j] /= sum;
+  if (a->sinks) {
+    *sink_w = exp(sink - m);
+    sum += *sink_w;
+  }
+  if (sum > 0.0) {
+    for (int64_t j = 0; j < L; ++j) probs[j] /= sum;
+    *sink_w /= sum;
+  }
   return L;
 }
 
-/* o = sum_j P_j * v_j for one (token, q head); returns 0 or -1. */
+/* o = sum_j P_j * v_j for one (token, q head), accumulated key by key in
+ * order for every d; returns 0 or -1. */
 static int row_output(const attn_args* a, int64_t tok, int hq, float* out,
-                      double* probs, int64_t cap) {
-  int64_t L = row_probs(a, tok, hq, probs, cap);
+                      double* probs, int64_t cap, const row_bufs* b) {
+  double sink_w;
+  int64_t L = row_probs(a, tok, hq, probs, &sink_w, cap, b);
   int r = request_of(a, tok);
   int D = a->head_dim, G = a->heads_q / a->heads_kv, hk = hq / G;
   if (L < 0) return -1;
-  for (int d = 0; d < D; ++d) {
-    double o = 0.0;
-    for (int64_t j = 0; j < L; ++j) {
-      if (probs[j] == 0.0) continue;
-      o += probs[j] *
-           dequant(a->dtype, cache_row(a, a->value_cache, r, j, hk), d, D,
-                   a->v_scale);
-    }
-    out[d] = (float)o;
+  for (int d = 0; d < D; ++d) b->o[d] = 0.0;
+  for (int64_t j = 0; j < L; ++j) {
+    if (probs[j] == 0.0) continue;
+    dequant_row(a->dtype, a->dec, cache_row(a, a->value_cache, r, j, hk), D, a->v_scale, b->v);
+    for (int d = 0; d < D; ++d) b->o[d] += probs[j] * b->v[d];
   }
+  for (int d = 0; d < D; ++d) out[d] = (float)b->o[d];
   return 0;
+}
+
+static int code_format_of(int dtype) {
+  return dtype == KVO_FP8_E5M2 || dtype == KVO_FP8_E5M2_PER_TOKEN_HEAD ? KVO_E5M2 : KVO_E4M3;
 }
 
 static attn_args make_args(int num_req, int heads_q, int heads_kv,
@@ -401,7 +440,8 @@ static attn_args make_args(int num_req, int heads_q, int heads_kv,
                            const int32_t* seq_lens, const int32_t* block_table,
                            int block_table_stride, double sm_scale, int causal,
                            int window, double soft_cap, float k_scale,
-                           float v_scale) {
+                           float v_scale, const float* alibi_slopes,
+                           const float* sinks) {
   attn_args a;
   a.num_req = num_req;
   a.heads_q = heads_q;
@@ -412,6 +452,7 @@ static attn_args make_args(int num_req, int heads_q, int heads_kv,
   a.value_cache = value_cache;
   a.block_size = block_size;
   a.dtype = dtype;
+  a.row_bytes = kvo_row_bytes(dtype, head_dim);
   a.query_start_loc = query_start_loc;
   a.seq_lens = seq_lens;
   a.block_table = block_table;
@@ -422,6 +463,9 @@ static attn_args make_args(int num_req, int heads_q, int heads_kv,
   a.soft_cap = soft_cap;
   a.k_scale = k_scale;
   a.v_scale = v_scale;
+  a.alibi_slopes = alibi_slopes;
+  a.sinks = sinks;
+  for (int c = 0; c < 256; ++c) a.dec[c] = kvo_fp8_decode(code_format_of(dtype), (uint8_t)c);
   return a;
 }
 
@@ -432,51 +476,73 @@ static int64_t max_seq_len(const attn_args* a) {
   return m;
 }
 
+static double* alloc_bufs(row_bufs* b, int D) {
+  double* mem = (double*)malloc(sizeof(double) * 7 * (size_t)D);
+  if (mem) {
+    b->q = mem;
+    b->k = mem + D;
+    b->v = mem + 2 * D;
+    b->o = mem + 3 * D;
+    b->e = mem + 4 * D;
+    b->wv = mem + 5 * D;
+    b->va = mem + 6 * D;
+  }
+  return mem;
+}
+
 /* Attention output (binary32) for the listed query tokens, all q heads:
  * out[i][hq][d] for tokens[i].  tokens == NULL means every token
  * 0 .. query_start_loc[num_req]-1 (then n_tokens is ignored).
+ * alibi_slopes / sinks: per q head, or NULL for none.
  * [P1] Breakdown items 2-3 (attention over the fp8 cache, scale folding);
- * [P2] Key source snippet (causal, window_size, soft_cap, paged blocks). */
+ * [P2] Key source snippet (causal, window_size, soft_cap, paged blocks,
+ * use_alibi, use_sink). */
 int kvo_attention(int num_req, int heads_q, int heads_kv, int head_dim,
                   const uint16_t* q, const uint8_t* key_cache,
                   const uint8_t* value_cache, int block_size, int dtype,
                   const int32_t* query_start_loc, const int32_t* seq_lens,
                   const int32_t* block_table, int block_table_stride,
                   double sm_scale, int causal, int window, double soft_cap,
-                  float k_scale, float v_scale, const int64_t* tokens,
-                  int64_t n_tokens, float* out) {
-  attn_args a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache,
-                          value_cache, block_size, dtype, query_start_loc,
-                          seq_lens, block_table, block_table_stride, sm_scale,
-                          causal, window, soft_cap, k_scale, v_scale);
-  int64_t cap = max_seq_len(&a);
-  int64_t n = tokens ? n_tokens : query_start_loc[num_req];
-  int64_t work = n * heads_q;
+                  float k_scale, float v_scale, const float* alibi_slopes,
+                  const float* sinks, const int64_t* tokens, int64_t n_tokens,
+                  float* out) {
+  attn_args a;
+  int64_t cap, n, work;
   int failed = 0;
   if (heads_kv <= 0 || heads_q % heads_kv != 0 || kvo_row_bytes(dtype, head_dim) < 0)
     return -1;
+  a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache, value_cache, block_size,
+                dtype, query_start_loc, seq_lens, block_table, block_table_stride, sm_scale,
+                causal, window, soft_cap, k_scale, v_scale, alibi_slopes, sinks);
+  cap = max_seq_len(&a);
+  n = tokens ? n_tokens : query_start_loc[num_req];
+  work = n * heads_q;
 #pragma omp parallel
   {
     double* probs = (double*)malloc(sizeof(double) * (size_t)cap);
+    row_bufs b;
+    double* mem = alloc_bufs(&b, head_dim);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t w = 0; w < work; ++w) {
       int64_t i = w / heads_q;
       int hq = (int)(w % heads_q);
       int64_t tok = tokens ? tokens[i] : i;
-      if (!probs ||
-          row_output(&a, tok, hq, out + (i * heads_q + hq) * (int64_t)head_dim,
-                     probs, cap) != 0) {
+      if (!probs || !mem ||
+          row_output(&a, tok, hq, out + (i * heads_q + hq) * (int64_t)head_dim, probs, cap,
+                     &b) != 0) {
 #pragma omp atomic write
         failed = 1;
       }
     }
     free(probs);
+    free(mem);
   }
   return failed ? -1 : 0;
 }
 
 /* Softmax weights of one (token, q head) over its request's L keys
- * (masked keys get 0).  probs must hold max seq_len doubles.  Returns L. */
+ * (masked keys get 0), and in *sink_w the sink's weight.  probs must hold
+ * max seq_len doubles.  Returns L. */
 int64_t kvo_attention_probs(int num_req, int heads_q, int heads_kv,
                             int head_dim, const uint16_t* q,
                             const uint8_t* key_cache, int block_size, int dtype,
@@ -484,12 +550,22 @@ int64_t kvo_attention_probs(int num_req, int heads_q, int heads_kv,
                             const int32_t* seq_lens, const int32_t* block_table,
                             int block_table_stride, double sm_scale, int causal,
                             int window, double soft_cap, float k_scale,
-                            int64_t token, int head_q, double* probs) {
-  attn_args a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache,
-                          NULL, block_size, dtype, query_start_loc, seq_lens,
-                          block_table, block_table_stride, sm_scale, causal,
-                          window, soft_cap, k_scale, 1.0f);
-  return row_probs(&a, token, head_q, probs, max_seq_len(&a));
+                            const float* alibi_slopes, const float* sinks,
+                            int64_t token, int head_q, double* probs, double* sink_w) {
+  attn_args a;
+  row_bufs b;
+  double* mem;
+  int64_t L;
+  if (heads_kv <= 0 || heads_q % heads_kv != 0 || kvo_row_bytes(dtype, head_dim) < 0)
+    return -1;
+  a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache, NULL, block_size, dtype,
+                query_start_loc, seq_lens, block_table, block_table_stride, sm_scale, causal,
+                window, soft_cap, k_scale, 1.0f, alibi_slopes, sinks);
+  mem = alloc_bufs(&b, head_dim);
+  if (!mem) return -1;
+  L = row_probs(&a, token, head_q, probs, sink_w, max_seq_len(&a), &b);
+  free(mem);
+  return L;
 }
 
 /* ------------------------------------------------------------------ */
@@ -505,17 +581,19 @@ int64_t kvo_attention_probs(int num_req, int heads_q, int heads_kv,
  * weights accumulated in binary32.
  *
  *   s_j -> s_j + e_j,  |e_j| <= gamma_{D+4} * A_j  (+ 2^-20 * cap with a soft
- *   cap: tanh evaluated to a few ulp; the cap's derivative is <= 1), where
- *   A_j = sm_scale * sum_d |q_d| |k_jd| and gamma_n = n 2^-23 / (1 - n 2^-23);
- *   a score perturbation moves the output by sum_j w_j (v_j - o) e_j to
- *   first order (softmax derivative), and the weight / sum rounding by at
- *   most (2^-11 + gamma_{2n+8}) sum_j w_j |v_j| over the n visible keys,
- *   plus 2^-25 sum_j |v_j| / sum_j p_j for weights that fall below the
- *   binary16 normal range (absolute error 2^-25 with the largest unnormalised
+ *   cap: tanh evaluated to a few ulp; the cap's derivative is <= 1; + 2^-21
+ *   * |slope (j - p)| with ALiBi: the bias formed and added in binary32),
+ *   where A_j = sm_scale * sum_d |q_d| |k_jd| and gamma_n = n 2^-23 /
+ *   (1 - n 2^-23); a score perturbation moves the output by
+ *   sum_j w_j (v_j - o) e_j to first order (softmax derivative), and the
+ *   weight / sum rounding by at most (2^-11 + gamma_{2n+8}) sum_j w_j |v_j|
+ *   over the n visible keys (n + 1 with a sink), plus
+ *   2^-25 sum_j |v_j| / sum_j p_j for weights that fall below the binary16
+ *   normal range (absolute error 2^-25 with the largest unnormalised
  *   weight p at 1).
  *
- * The bound is the sum of those two terms; it is zero only where nothing
- * is visible.  Used by the tests to widen the stated tolerance by what
+ * The bound is the sum of those terms; it is zero only where nothing is
+ * visible.  Used by the tests to widen the stated tolerance by what
  * binary32 arithmetic itself cannot avoid on inputs with outliers. */
 static double gamma_n(double n) {
   const double u = 1.0 / 8388608.0; /* 2^-23 */
@@ -523,48 +601,57 @@ static double gamma_n(double n) {
 }
 
 static int row_bound(const attn_args* a, int64_t tok, int hq, float* out,
-                     double* probs, double* err, int64_t cap) {
-  int64_t L = row_probs(a, tok, hq, probs, cap);
+                     double* probs, double* err, int64_t cap, const row_bufs* b) {
+  double sink_w;
+  int64_t L = row_probs(a, tok, hq, probs, &sink_w, cap, b);
   int r = request_of(a, tok);
   int D = a->head_dim, G = a->heads_q / a->heads_kv, hk = hq / G;
-  const uint16_t* qrow = a->q + (tok * a->heads_q + hq) * (int64_t)D;
-  int64_t n = 0;
+  int64_t n = 0, p;
   if (L < 0) return -1;
+  p = L - (a->query_start_loc[r + 1] - a->query_start_loc[r]) + (tok - a->query_start_loc[r]);
   for (int64_t j = 0; j < L; ++j) {
-    const uint8_t* krow;
     double A = 0.0;
     err[j] = 0.0;
     if (probs[j] == 0.0) continue;
     ++n;
-    krow = cache_row(a, a->key_cache, r, j, hk);
-    for (int d = 0; d < D; ++d)
-      A += fabs(kvo_bf16_to_double(qrow[d]) * dequant(a->dtype, krow, d, D, a->k_scale));
+    dequant_row(a->dtype, a->dec, cache_row(a, a->key_cache, r, j, hk), D, a->k_scale, b->k);
+    for (int d = 0; d < D; ++d) A += fabs(b->q[d] * b->k[d]);
     err[j] = gamma_n(D + 4) * A * fabs(a->sm_scale);
     if (a->soft_cap > 0.0) err[j] += a->soft_cap / 1048576.0; /* 2^-20 cap */
+    if (a->alibi_slopes)
+      err[j] += fabs((double)a->alibi_slopes[hq] * (double)(j - p)) / 2097152.0; /* 2^-21 */
   }
+  if (a->sinks) ++n;
   /* sum_j p_j with the largest p at 1: the softmax normaliser of the
    * unnormalised weights a kernel rounds */
-  double lsum = 0.0, pmax = 0.0;
+  double lsum = 0.0, pmax = sink_w;
   for (int64_t j = 0; j < L; ++j)
     if (probs[j] > pmax) pmax = probs[j];
   for (int64_t j = 0; j < L; ++j) lsum += probs[j] / (pmax > 0.0 ? pmax : 1.0);
+  lsum += sink_w / (pmax > 0.0 ? pmax : 1.0);
   for (int d = 0; d < D; ++d) {
-    double o = 0.0, e_score = 0.0, wv = 0.0, v_abs = 0.0;
-    for (int64_t j = 0; j < L; ++j) {
-      if (probs[j] == 0.0) continue;
-      o += probs[j] * dequant(a->dtype, cache_row(a, a->value_cache, r, j, hk), d, D, a->v_scale);
-    }
-    for (int64_t j = 0; j < L; ++j) {
-      double v;
-      if (probs[j] == 0.0) continue;
-      v = dequant(a->dtype, cache_row(a, a->value_cache, r, j, hk), d, D, a->v_scale);
-      e_score += probs[j] * fabs(v - o) * err[j];
-      wv += probs[j] * fabs(v);
-      v_abs += fabs(v);
-    }
-    out[d] = (float)(e_score + (1.0 / 2048.0 + gamma_n(2.0 * (double)n + 8.0)) * wv +
-                     v_abs / 33554432.0 / (lsum > 0.0 ? lsum : 1.0));
+    b->o[d] = 0.0;
+    b->e[d] = 0.0;
+    b->wv[d] = 0.0;
+    b->va[d] = 0.0;
   }
+  for (int64_t j = 0; j < L; ++j) {
+    if (probs[j] == 0.0) continue;
+    dequant_row(a->dtype, a->dec, cache_row(a, a->value_cache, r, j, hk), D, a->v_scale, b->v);
+    for (int d = 0; d < D; ++d) b->o[d] += probs[j] * b->v[d];
+  }
+  for (int64_t j = 0; j < L; ++j) {
+    if (probs[j] == 0.0) continue;
+    dequant_row(a->dtype, a->dec, cache_row(a, a->value_cache, r, j, hk), D, a->v_scale, b->v);
+    for (int d = 0; d < D; ++d) {
+      b->e[d] += probs[j] * fabs(b->v[d] - b->o[d]) * err[j];
+      b->wv[d] += probs[j] * fabs(b->v[d]);
+      b->va[d] += fabs(b->v[d]);
+    }
+  }
+  for (int d = 0; d < D; ++d)
+    out[d] = (float)(b->e[d] + (1.0 / 2048.0 + gamma_n(2.0 * (double)n + 8.0)) * b->wv[d] +
+                     b->va[d] / 33554432.0 / (lsum > 0.0 ? lsum : 1.0));
   return 0;
 }
 
@@ -576,36 +663,41 @@ int kvo_attention_fp32_bound(int num_req, int heads_q, int heads_kv, int head_di
                              const int32_t* query_start_loc, const int32_t* seq_lens,
                              const int32_t* block_table, int block_table_stride,
                              double sm_scale, int causal, int window, double soft_cap,
-                             float k_scale, float v_scale, const int64_t* tokens,
-                             int64_t n_tokens, float* out) {
-  attn_args a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache,
-                          value_cache, block_size, dtype, query_start_loc,
-                          seq_lens, block_table, block_table_stride, sm_scale,
-                          causal, window, soft_cap, k_scale, v_scale);
-  int64_t cap = max_seq_len(&a);
-  int64_t n = tokens ? n_tokens : query_start_loc[num_req];
-  int64_t work = n * heads_q;
+                             float k_scale, float v_scale, const float* alibi_slopes,
+                             const float* sinks, const int64_t* tokens, int64_t n_tokens,
+                             float* out) {
+  attn_args a;
+  int64_t cap, n, work;
   int failed = 0;
   if (heads_kv <= 0 || heads_q % heads_kv != 0 || kvo_row_bytes(dtype, head_dim) < 0)
     return -1;
+  a = make_args(num_req, heads_q, heads_kv, head_dim, q, key_cache, value_cache, block_size,
+                dtype, query_start_loc, seq_lens, block_table, block_table_stride, sm_scale,
+                causal, window, soft_cap, k_scale, v_scale, alibi_slopes, sinks);
+  cap = max_seq_len(&a);
+  n = tokens ? n_tokens : query_start_loc[num_req];
+  work = n * heads_q;
 #pragma omp parallel
   {
     double* probs = (double*)malloc(sizeof(double) * (size_t)cap);
     double* err = (double*)malloc(sizeof(double) * (size_t)cap);
+    row_bufs b;
+    double* mem = alloc_bufs(&b, head_dim);
 #pragma omp for schedule(dynamic, 1)
     for (int64_t w = 0; w < work; ++w) {
       int64_t i = w / heads_q;
       int hq = (int)(w % heads_q);
       int64_t tok = tokens ? tokens[i] : i;
-      if (!probs || !err ||
-          row_bound(&a, tok, hq, out + (i * heads_q + hq) * (int64_t)head_dim, probs, err,
-                    cap) != 0) {
+      if (!probs || !err || !mem ||
+          row_bound(&a, tok, hq, out + (i * heads_q + hq) * (int64_t)head_dim, probs, err, cap,
+                    &b) != 0) {
 #pragma omp atomic write
         failed = 1;
       }
     }
     free(probs);
     free(err);
+    free(mem);
   }
   return failed ? -1 : 0;
 }
