@@ -7,10 +7,15 @@ split-KV row-tile kernel, the split merge, and the tensor-core prefill
 kernel where the batch has prefills).  The cache holding the earlier
 context is written once before timing (state, not per-step input).
 
-Default workload: the decode batch -- 64 requests, query_len 1, kv_len ~
-U[1024, 4096], 32 query heads over 8 kv heads, head_dim 128, block 16,
-fp8_e4m3 per-tensor scales.  Metric: decode KV GB/s = the K and V cache
-bytes the step's attention must read, divided by the step time.
+Headline workload (the line's `value`): the decode batch -- 64 requests,
+query_len 1, kv_len ~ U[1024, 4096], 32 query heads over 8 kv heads,
+head_dim 128, block 16, fp8_e4m3 per-tensor scales.  Metric: decode KV GB/s
+= the K and V cache bytes the step's attention must read, divided by the
+step time.  The same line carries one object per other workload under
+"workloads" (the large prefill and the mixed batch in prefill TFLOP/s, the
+long-context decode in GB/s), each with its roofline, CPU baseline and
+clocks; the mixed batch also reports its prefill and decode parts timed
+alone.
 
 Prints ONE JSON line (rank 0).  --impl reference times the CPU oracle on a
 bounded sample of the same workload instead.  Under torchrun each rank
@@ -39,19 +44,19 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/; valid only while the kernel's sources
 # hash as they did when captured.
 PROFILED_TRAFFIC = {
-    2: {"bytes": 361.074432e6 + 5.945344e6, "profile": "profiles/splitkv_decode_decode_batch.md",
+    (2, None): {"bytes": 361.074432e6 + 5.945344e6, "profile": "profiles/splitkv_decode_decode_batch.md",
          "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
          "sha1": "142c9b241fa7d2a1b9daa1aaae457bce637bb4d0"},
-    3: {"bytes": 37.864448e6 + 0.718592e6, "profile": "profiles/prefill_attention_large_prefill.md",
+    (3, None): {"bytes": 37.864448e6 + 0.718592e6, "profile": "profiles/prefill_attention_large_prefill.md",
          "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
          "sha1": "160303ad39db27ace633acce9e3834c725e000d9"},
 }
 
 
-def profiled_traffic(workload: int):
+def profiled_traffic(workload: int, dtype=None):
     """The captured DRAM traffic of this workload's dominant kernel, or None
     when there is no capture or the kernel changed since."""
-    entry = PROFILED_TRAFFIC.get(workload)
+    entry = PROFILED_TRAFFIC.get((workload, dtype))
     if entry is None:
         return None
     m = hashlib.sha1()
@@ -167,7 +172,7 @@ def _max_over_ranks(x: float, world: int) -> float:
 def kv_bytes_read(wl) -> int:
     """Algorithmic K+V cache bytes the attention reads: every key visible to
     some query of its request, once (the window bounds it)."""
-    row = {"fp8_e4m3": wl.head_dim, "fp8_e5m2": wl.head_dim,
+    row = {"auto": 2 * wl.head_dim, "fp8_e4m3": wl.head_dim, "fp8_e5m2": wl.head_dim,
            "int8_per_token_head": wl.head_dim + 4,
            "fp8_per_token_head": wl.head_dim + 4,
            "fp8_e5m2_per_token_head": wl.head_dim + 4}[wl.kv_cache_dtype]
@@ -192,15 +197,51 @@ def attention_flops(wl) -> int:
     return total * wl.heads_q * 4 * wl.head_dim
 
 
-def run_gpu(args, rank, world, local):
-    import numpy as np
+def sub_batch(wl, reqs):
+    """The requests `reqs` of a workload as a batch of their own over the same
+    caches (their query rows, lengths and table rows)."""
+    import torch
+    from int8_kv_cache_reshape_gb300 import workloads as W
+    qsl = wl.query_start_loc.tolist()
+    rows = torch.cat([torch.arange(qsl[r], qsl[r + 1]) for r in reqs]) if reqs else \
+        torch.zeros(0, dtype=torch.long)
+    ql = [wl.query_lens[r] for r in reqs]
+    sub = W.Workload(**{**wl.__dict__})
+    sub.query_lens = ql
+    sub.seq_lens = [wl.seq_lens[r] for r in reqs]
+    sub.q = wl.q[rows].contiguous()
+    sub.block_table = wl.block_table[torch.tensor(reqs, dtype=torch.long)].contiguous()
+    sub.seq_lens_t = torch.tensor(sub.seq_lens, dtype=torch.int32)
+    sub.query_start_loc = torch.zeros(len(reqs) + 1, dtype=torch.int32)
+    if reqs:
+        sub.query_start_loc[1:] = torch.cumsum(torch.tensor(ql, dtype=torch.int32), 0)
+    return sub
+
+
+def _roofline(decode_metric, kvb, flops, attn_ms, peaks, peaks_src, kernel, traffic=None):
+    r = {"bound": "hbm" if decode_metric else "tensor", "kernel": kernel,
+         "unit": "GB/s" if decode_metric else "TFLOP/s", "traffic": traffic,
+         "peak_source": peaks_src}
+    if decode_metric:
+        achieved = kvb / (attn_ms * 1e-3) / 1e9
+        r.update(achieved=achieved, peak=peaks["hbm_gbs"], frac=achieved / peaks["hbm_gbs"],
+                 algorithmic_bytes=kvb)
+    else:
+        achieved = flops / (attn_ms * 1e-3) / 1e12
+        r.update(achieved=achieved, peak=peaks["bf16_tflops"],
+                 frac=achieved / peaks["bf16_tflops"], algorithmic_flops=flops)
+    return r
+
+
+def run_workload(args, index, dtype, world, local, with_e2e=True):
+    """Time one workload's step; returns (result dict, workload)."""
     import torch
     from int8_kv_cache_reshape_gb300 import workloads as W
     from int8_kv_cache_reshape_gb300 import kvq
 
     dev = torch.device(f"cuda:{local}")
     torch.cuda.set_device(dev)
-    wl = W.config(args.workload, args.kv_cache_dtype)
+    wl = W.config(index, dtype)
     new = wl.new_token_mask()
     row = kvq.cache_row_bytes(wl.kv_cache_dtype, wl.head_dim)
     shape = (wl.num_blocks, wl.block_size, wl.heads_kv, row)
@@ -210,6 +251,7 @@ def run_gpu(args, rank, world, local):
     slots = wl.slot_mapping.to(dev)
     # State: the earlier context's K/V are already in the cache.
     kvq.reshape_and_cache(key, value, kc, vc, slots, wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+    del key, value, slots
     # Per-step inputs: the new tokens' K/V, their slots, q, lengths, table.
     new_idx = torch.nonzero(new).flatten()
     nkey = wl.key[new_idx].contiguous()
@@ -223,11 +265,9 @@ def run_gpu(args, rank, world, local):
     out = torch.empty(wl.q.shape, dtype=torch.bfloat16, device=dev)
     sl_host = wl.seq_lens_t.numpy()
     qsl_host = wl.query_start_loc.numpy()
-    t0 = time.perf_counter()
     sched = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
                                        sl_host, qsl_host, wl.causal, wl.window,
                                        wl.kv_cache_dtype)
-    sched_ms = (time.perf_counter() - t0) * 1e3
     info = sched.info()
     ws = torch.empty(max(1, sched.workspace_bytes), dtype=torch.uint8, device=dev)
     flush = torch.empty(L2_FLUSH_BYTES, dtype=torch.uint8, device=dev)
@@ -240,17 +280,20 @@ def run_gpu(args, rank, world, local):
         flush.zero_()
         flush.max()
 
-    def step():
+    def cache_write():
         kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
                               wl.v_scale, stream)
-        kvq.attention_with_kv_cache(sched, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
-                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
+
+    def attention(s=sched, qq=q, qs=qsl, ss=sl, tb=bt, o=out):
+        kvq.attention_with_kv_cache(s, qq, kc, vc, qs, ss, tb, wl.sm_scale, wl.causal,
+                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, o, ws,
                                     wl.kv_cache_dtype, wl.heads_kv, stream)
 
     launches_per_step = 1 + info["num_kernel_launches"]
     for _ in range(args.warmup):
         l2_flush()
-        step()
+        cache_write()
+        attention()
     torch.cuda.synchronize()
 
     clocks = ClockSampler(local)
@@ -259,7 +302,8 @@ def run_gpu(args, rank, world, local):
     t_end = time.perf_counter() + args.clock_window
     while time.perf_counter() < t_end:
         l2_flush()
-        step()
+        cache_write()
+        attention()
         torch.cuda.synchronize()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True),
@@ -270,12 +314,9 @@ def run_gpu(args, rank, world, local):
         l2_flush()              # L2 flush between steps, outside the timed events
         a, b, c = ev[i]
         a.record(stream)
-        kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
-                              wl.v_scale, stream)
+        cache_write()
         b.record(stream)
-        kvq.attention_with_kv_cache(sched, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
-                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
-                                    wl.kv_cache_dtype, wl.heads_kv, stream)
+        attention()
         c.record(stream)
     torch.cuda.synchronize()
     _barrier(world)
@@ -289,53 +330,13 @@ def run_gpu(args, rank, world, local):
 
     kvb = kv_bytes_read(wl)
     flops = attention_flops(wl)
-    decode_metric = is_decode_metric(args.workload)
+    decode_metric = is_decode_metric(index)
     if decode_metric:
         metric, unit = "decode KV GB/s", "GB/s"
         value = world * kvb / (ms_per_step * 1e-3) / 1e9
     else:
         metric, unit = "prefill TFLOP/s", "TFLOP/s"
         value = world * flops / (ms_per_step * 1e-3) / 1e12
-
-    # ---- end to end: host buffers through the public API -------------------
-    pin = lambda t: t.pin_memory()
-    h_q, h_nkey, h_nval, h_nslot = pin(wl.q), pin(nkey), pin(nval), pin(nslot)
-    h_qsl, h_sl, h_bt = pin(wl.query_start_loc), pin(wl.seq_lens_t), pin(wl.block_table)
-    h_out = torch.empty(wl.q.shape, dtype=torch.bfloat16).pin_memory()
-    h2d = sum(t.numel() * t.element_size() for t in (h_q, h_nkey, h_nval, h_nslot, h_qsl, h_sl, h_bt))
-    d2h = h_out.numel() * h_out.element_size()
-
-    def e2e_step():
-        q.copy_(h_q, non_blocking=True)
-        d_nkey.copy_(h_nkey, non_blocking=True)
-        d_nval.copy_(h_nval, non_blocking=True)
-        d_nslot.copy_(h_nslot, non_blocking=True)
-        qsl.copy_(h_qsl, non_blocking=True)
-        sl.copy_(h_sl, non_blocking=True)
-        bt.copy_(h_bt, non_blocking=True)
-        s2 = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
-                                        sl_host, qsl_host, wl.causal, wl.window,
-                                        wl.kv_cache_dtype)
-        kvq.reshape_and_cache(d_nkey, d_nval, kc, vc, d_nslot, wl.kv_cache_dtype, wl.k_scale,
-                              wl.v_scale, stream)
-        kvq.attention_with_kv_cache(s2, q, kc, vc, qsl, sl, bt, wl.sm_scale, wl.causal,
-                                    wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, out, ws,
-                                    wl.kv_cache_dtype, wl.heads_kv, stream)
-        h_out.copy_(out, non_blocking=True)
-        torch.cuda.current_stream().synchronize()
-        s2.close()
-
-    for _ in range(3):
-        e2e_step()
-    e2e_times = []
-    for _ in range(args.steps):
-        l2_flush()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        e2e_step()
-        e2e_times.append(time.perf_counter() - t0)
-    e2e_s = _max_over_ranks(sum(e2e_times), world) / args.steps
-    e2e_value = world * (kvb if decode_metric else flops) / e2e_s / (1e9 if decode_metric else 1e12)
 
     peaks, peaks_src = _peaks()
     if info["num_prefill_tiles"] and info["num_tiles"]:
@@ -344,18 +345,8 @@ def run_gpu(args, rank, world, local):
         kernel = "tcgen05 prefill attention"
     else:
         kernel = "split-KV decode attention (+ split merge)"
-    roofline = {"bound": "hbm" if decode_metric else "tensor", "kernel": kernel,
-                "unit": "GB/s" if decode_metric else "TFLOP/s",
-                "traffic": profiled_traffic(args.workload) if args.kv_cache_dtype is None else None,
-                "peak_source": peaks_src}
-    if decode_metric:
-        achieved = kvb / (attn_avg * 1e-3) / 1e9
-        roofline.update(achieved=achieved, peak=peaks["hbm_gbs"],
-                        frac=achieved / peaks["hbm_gbs"])
-    else:
-        achieved = flops / (attn_avg * 1e-3) / 1e12
-        roofline.update(achieved=achieved, peak=peaks["bf16_tflops"],
-                        frac=achieved / peaks["bf16_tflops"])
+    roofline = _roofline(decode_metric, kvb, flops, attn_avg, peaks, peaks_src, kernel,
+                         profiled_traffic(index, dtype))
 
     res = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -372,15 +363,108 @@ def run_gpu(args, rank, world, local):
         "kv_bytes_per_step": kvb, "flops_per_step": flops,
         "tokens_per_s": world * wl.num_query_tokens / (ms_per_step * 1e-3),
         "attention_ms": attn_avg, "cache_write_ms": sum(cache_ms) / len(cache_ms),
-        "scheduler_host_ms": sched_ms, "schedule": info,
+        "schedule": info,
         "roofline": roofline,
-        "e2e": {"value": e2e_value, "unit": unit, "h2d_bytes_per_step": h2d,
-                "d2h_bytes_per_step": d2h, "ms_per_step": e2e_s * 1e3,
-                "includes": "H2D of step inputs, scheduler, cache write, attention, D2H of out"},
         "gpu_launches": args.steps * launches_per_step,
         "clocks": clk,
     }
+
+    # ---- the mixed batch's two kernels, each timed alone ---------------------
+    if info["num_prefill_tiles"] and info["num_tiles"]:
+        parts = {}
+        ql = wl.query_lens
+        for name, reqs in (("prefill", [r for r in range(wl.num_req) if ql[r] * wl.heads_q // wl.heads_kv > 16]),
+                           ("decode", [r for r in range(wl.num_req) if ql[r] * wl.heads_q // wl.heads_kv <= 16])):
+            sub = sub_batch(wl, reqs)
+            s2 = kvq.get_scheduler_metadata(sub.num_req, sub.heads_q, sub.heads_kv, sub.head_dim,
+                                            sub.seq_lens_t.numpy(), sub.query_start_loc.numpy(),
+                                            sub.causal, sub.window, sub.kv_cache_dtype)
+            d_q, d_qsl = sub.q.to(dev), sub.query_start_loc.to(dev)
+            d_sl, d_bt = sub.seq_lens_t.to(dev), sub.block_table.to(dev)
+            d_out = torch.empty(sub.q.shape, dtype=torch.bfloat16, device=dev)
+            for _ in range(args.warmup):
+                l2_flush()
+                attention(s2, d_q, d_qsl, d_sl, d_bt, d_out)
+            evs = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True))
+                   for _ in range(args.steps)]
+            torch.cuda.synchronize()
+            for a, b in evs:
+                l2_flush()
+                a.record(stream)
+                attention(s2, d_q, d_qsl, d_sl, d_bt, d_out)
+                b.record(stream)
+            torch.cuda.synchronize()
+            ms = sum(a.elapsed_time(b) for a, b in evs) / len(evs)
+            pm = name == "decode"
+            kvb2, fl2 = kv_bytes_read(sub), attention_flops(sub)
+            parts[name] = {
+                "requests": len(reqs), "attention_ms": ms,
+                "value": (kvb2 / (ms * 1e-3) / 1e9) if pm else (fl2 / (ms * 1e-3) / 1e12),
+                "unit": "GB/s" if pm else "TFLOP/s",
+                "roofline": _roofline(pm, kvb2, fl2, ms, peaks, peaks_src,
+                                      "split-KV decode attention (+ split merge)" if pm
+                                      else "tcgen05 prefill attention")}
+            s2.close()
+        res["parts"] = parts
+
+    # ---- end to end: host buffers through the public API -------------------
+    if with_e2e:
+        pin = lambda t: t.pin_memory()
+        h_q, h_nkey, h_nval, h_nslot = pin(wl.q), pin(nkey), pin(nval), pin(nslot)
+        h_qsl, h_sl, h_bt = pin(wl.query_start_loc), pin(wl.seq_lens_t), pin(wl.block_table)
+        h_out = torch.empty(wl.q.shape, dtype=torch.bfloat16).pin_memory()
+        h2d = sum(t.numel() * t.element_size()
+                  for t in (h_q, h_nkey, h_nval, h_nslot, h_qsl, h_sl, h_bt))
+        d2h = h_out.numel() * h_out.element_size()
+
+        def e2e_step():
+            q.copy_(h_q, non_blocking=True)
+            d_nkey.copy_(h_nkey, non_blocking=True)
+            d_nval.copy_(h_nval, non_blocking=True)
+            d_nslot.copy_(h_nslot, non_blocking=True)
+            qsl.copy_(h_qsl, non_blocking=True)
+            sl.copy_(h_sl, non_blocking=True)
+            bt.copy_(h_bt, non_blocking=True)
+            s2 = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                            sl_host, qsl_host, wl.causal, wl.window,
+                                            wl.kv_cache_dtype)
+            cache_write()
+            attention(s2)
+            h_out.copy_(out, non_blocking=True)
+            torch.cuda.current_stream().synchronize()
+            s2.close()
+
+        for _ in range(3):
+            e2e_step()
+        e2e_times, sched_times = [], []
+        for _ in range(args.steps):
+            l2_flush()
+            torch.cuda.synchronize()
+            t0 = time.perf_counter()
+            e2e_step()
+            e2e_times.append(time.perf_counter() - t0)
+            t1 = time.perf_counter()
+            s3 = kvq.get_scheduler_metadata(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                            sl_host, qsl_host, wl.causal, wl.window,
+                                            wl.kv_cache_dtype)
+            sched_times.append(time.perf_counter() - t1)
+            s3.close()
+        e2e_s = _max_over_ranks(sum(e2e_times), world) / args.steps
+        res["scheduler_host_ms"] = 1e3 * sum(sched_times) / len(sched_times)
+        res["e2e"] = {"value": world * (kvb if decode_metric else flops) / e2e_s /
+                      (1e9 if decode_metric else 1e12),
+                      "unit": unit, "h2d_bytes_per_step": h2d, "d2h_bytes_per_step": d2h,
+                      "ms_per_step": e2e_s * 1e3,
+                      "includes": "H2D of step inputs, scheduler, cache write, attention, "
+                                  "D2H of out"}
+    sched.close()
+    del kc, vc, flush
+    torch.cuda.empty_cache()
     return res, wl
+
+
+def run_gpu(args, rank, world, local):
+    return run_workload(args, args.workload, args.kv_cache_dtype, world, local)
 
 
 class OracleStep:
@@ -483,6 +567,8 @@ def main():
     ap.add_argument("--ref-requests", type=int, default=16)
     ap.add_argument("--cpu-requests", type=int, default=16)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--headline-only", dest="all_workloads", action="store_false",
+                    help="only the headline workload (no per-workload objects)")
     args = ap.parse_args()
     if args.warmup < 3:
         args.warmup = 3
@@ -493,16 +579,45 @@ def main():
             print(json.dumps(res))
         return
     res, wl = run_gpu(args, rank, world, local)
+    if rank == 0 and not args.no_cpu_baseline:
+        res["cpu_baseline"] = cpu_baseline(wl, args.workload, args.cpu_requests)
+    if args.all_workloads and args.workload == 2 and args.kv_cache_dtype is None:
+        others = []
+        for index, dtype in OTHER_WORKLOADS:
+            r2, wl2 = run_workload(args, index, dtype, world, local, with_e2e=True)
+            entry = {k: r2[k] for k in ("metric", "value", "unit", "ms_per_step", "attention_ms",
+                                        "cache_write_ms", "tokens_per_s", "kv_bytes_per_step",
+                                        "flops_per_step", "roofline", "e2e", "clocks",
+                                        "gpu_launches", "scheduler_host_ms")}
+            entry["workload"] = r2["config"]["workload"]
+            entry["kv_cache_dtype"] = r2["config"]["kv_cache_dtype"]
+            entry["schedule"] = {k: r2["schedule"][k] for k in (
+                "num_tiles", "num_pieces", "max_splits", "num_prefill_tiles",
+                "num_decode_warps", "workspace_bytes")}
+            if "parts" in r2:
+                entry["parts"] = r2["parts"]
+            if rank == 0 and not args.no_cpu_baseline:
+                entry["cpu_baseline"] = cpu_baseline(wl2, index, args.cpu_requests)
+            others.append(entry)
+            res["gpu_launches"] += r2["gpu_launches"]
+        res["workloads"] = others
     if rank == 0:
-        if not args.no_cpu_baseline:
-            decode_metric = is_decode_metric(args.workload)
-            ref = OracleStep(wl, args.cpu_requests)
-            secs = ref.step()
-            res["cpu_baseline"] = {
-                "value": ref.work(decode_metric) / secs / (1e9 if decode_metric else 1e12),
-                "unit": res["unit"], "cores": ref.cores, "kind": "oracle", "seconds": secs,
-                "sample": ref.sample}
         print(json.dumps(res))
+
+
+# The workloads reported beside the headline decode batch (index, dtype).
+OTHER_WORKLOADS = [(3, None), (4, "int8_per_token_head"), (4, "fp8_per_token_head"),
+                   (4, "fp8_e5m2_per_token_head"), (5, None)]
+
+
+def cpu_baseline(wl, index, nreq):
+    """The oracle on a bounded sample of the workload's step (see OracleStep)."""
+    decode_metric = is_decode_metric(index)
+    ref = OracleStep(wl, nreq if decode_metric else min(nreq, 1))
+    secs = ref.step()
+    return {"value": ref.work(decode_metric) / secs / (1e9 if decode_metric else 1e12),
+            "unit": "GB/s" if decode_metric else "TFLOP/s", "cores": ref.cores,
+            "kind": "oracle", "seconds": secs, "sample": ref.sample}
 
 
 if __name__ == "__main__":

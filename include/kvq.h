@@ -153,9 +153,12 @@ KVQ_API int kvq_reshape_and_cache(const void* key, const void* value,
  *   out                     receives a new schedule (free: kvq_sched_destroy)
  *   workspace_bytes         receives the scratch size the attention call
  *                           needs (may be 0); must not be NULL.
- * The schedule holds a host copy and one device copy of its plan, made on
- * the current device (one blocking upload from pinned staging into a pooled
- * device buffer).  Requests with at most 16
+ * The schedule holds its plan in pinned host memory and reserves a device
+ * buffer for it on the current device (both pooled: after the first few
+ * schedules no call allocates).  This call does not touch the device
+ * otherwise and does not synchronise: the first attention call made with
+ * the schedule uploads the plan with an asynchronous copy on that call's
+ * stream, ahead of its kernels.  Requests with at most 16
  * (query, head) rows per kv head (decodes) form row tiles whose 16-token KV
  * chunks are cut into equal contiguous segments, one per warp, so long
  * contexts are split along the KV axis and merged.  Requests with more rows
@@ -244,11 +247,11 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
 
 /* Free a schedule (NULL is a no-op).  No counterpart on the pages (their
  * schedule is a torch tensor that the garbage collector frees); it is the
- * C ABI's ownership rule for the object get_scheduler_metadata returns.  Its device work list goes back to a
- * small library pool that later schedules on the same device reuse (no
- * cudaFree / cudaMalloc per step), so destroy a schedule only once the
- * attention calls that use it have completed on the device, as for any
- * memory the caller frees. */
+ * C ABI's ownership rule for the object get_scheduler_metadata returns.
+ * Its pinned plan image and device buffer go back to small library pools
+ * that later schedules reuse (no cudaMalloc / cudaHostAlloc per step), so
+ * destroy a schedule only once the attention calls that use it have
+ * completed on the device, as for any memory the caller frees. */
 KVQ_API void kvq_sched_destroy(kvq_sched_t* sched);
 
 /* Summary of a schedule, for tests and benchmarks.  [P2] Breakdown item 1:
@@ -334,8 +337,10 @@ KVQ_API int kvq_sched_export_plan(const kvq_sched_t* sched, kvq_plan_piece_t* pi
  * Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
  * kernel run with this schedule gave up waiting for the tensor core (a
  * bounded wait of about a second; the kernel then released its tensor
- * memory and returned without writing its tile), else KVQ_OK.  Blocks until
- * the device is idle. */
+ * memory and wrote NaN into the output rows of its tile), else KVQ_OK.
+ * The attention calls return before their kernels run, so they cannot
+ * report this themselves: a caller that does not read the error word sees
+ * such a failure as NaN rows.  Blocks until the device is idle. */
 KVQ_API int kvq_sched_check_device(const kvq_sched_t* sched);
 
 /* Short English description of a status code (static storage; never NULL:

@@ -15,6 +15,7 @@
 #include <cmath>
 #include <cstdlib>
 #include <cstring>
+#include <atomic>
 #include <mutex>
 #include <new>
 #include <vector>
@@ -50,6 +51,11 @@ struct kvq_sched {
   void* d_buf;  // device copy: pieces, warp table, merges, merge counters, prefill tiles, error word
   size_t d_buf_bytes;
   size_t d_pieces_off, d_warps_off, d_merges_off, d_counters_off, d_prefill_off, d_error_off;
+  size_t image_bytes;       // bytes of the plan image (host and device copies)
+  void* h_image;            // pinned host image, uploaded by the first attention call
+  size_t h_image_bytes;
+  bool h_image_pinned;
+  std::atomic<bool> uploaded;
 };
 
 namespace {
@@ -96,11 +102,57 @@ void* pool_get(int device, size_t bytes, size_t* got) {
   return p;
 }
 
-// Pinned host staging for the plan's upload (the upload is synchronous, so
-// one buffer serves every call in turn).
-std::mutex g_stage_mutex;
-void* g_stage = nullptr;
-size_t g_stage_bytes = 0;
+// Pinned host images of destroyed schedules, kept for the next schedules
+// (the same power-of-two classes; bounded).  A schedule's image is uploaded
+// by its first attention call with an asynchronous copy on that call's
+// stream, so it must stay untouched until the schedule is destroyed.
+std::mutex g_pinned_mutex;
+std::vector<std::pair<size_t, void*>> g_pinned;
+
+void* pinned_get(size_t bytes, size_t* got, bool* pinned) {
+  const size_t want = pool_size_class(bytes);
+  {
+    std::lock_guard<std::mutex> lock(g_pinned_mutex);
+    for (size_t i = 0; i < g_pinned.size(); ++i) {
+      if (g_pinned[i].first >= want) {
+        void* p = g_pinned[i].second;
+        *got = g_pinned[i].first;
+        g_pinned.erase(g_pinned.begin() + (std::ptrdiff_t)i);
+        *pinned = true;
+        return p;
+      }
+    }
+  }
+  void* p = nullptr;
+  if (cudaHostAlloc(&p, want, cudaHostAllocDefault) == cudaSuccess) {
+    *got = want;
+    *pinned = true;
+    return p;
+  }
+  cudaGetLastError();
+  // Without pinned memory the image is pageable; the upload then completes
+  // before cudaMemcpyAsync returns.
+  p = std::malloc(want);
+  *got = p ? want : 0;
+  *pinned = false;
+  return p;
+}
+
+void pinned_put(void* p, size_t bytes, bool pinned) {
+  if (!p) return;
+  if (!pinned) {
+    std::free(p);
+    return;
+  }
+  {
+    std::lock_guard<std::mutex> lock(g_pinned_mutex);
+    if (g_pinned.size() < kPoolMax) {
+      g_pinned.emplace_back(bytes, p);
+      return;
+    }
+  }
+  cudaFreeHost(p);
+}
 
 void pool_put(int device, void* ptr, size_t bytes) {
   {
@@ -232,6 +284,7 @@ int kvq_reshape_and_cache(const void* key, const void* value, int64_t num_tokens
 void kvq_sched_destroy(kvq_sched_t* s) {
   if (!s) return;
   if (s->d_buf) pool_put(s->device, s->d_buf, s->d_buf_bytes);
+  pinned_put(s->h_image, s->h_image_bytes, s->h_image_pinned);
   delete s;
 }
 
@@ -267,6 +320,10 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   s->group = heads_q / heads_kv;
   s->total_q = num_req > 0 ? query_start_loc_host[num_req] : 0;
   s->d_buf = nullptr;
+  s->h_image = nullptr;
+  s->h_image_bytes = 0;
+  s->h_image_pinned = false;
+  s->uploaded.store(false);
   // Without a usable CUDA device the plan is still built (host-only: its
   // attention calls return KVQ_E_CUDA), so that planning can be inspected
   // on machines without a GPU.
@@ -439,9 +496,10 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   }
   s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
 
-  // 3) Device copy of the plan: one image (pieces, per-warp first pieces,
-  //    merge items, zeroed merge counters, prefill tiles, zeroed error word),
-  //    one blocking upload into a pooled device buffer.
+  // 3) The plan image (pieces, per-warp first pieces, merge items, zeroed
+  //    merge counters, prefill tiles, zeroed error word) in pinned host
+  //    memory, and a pooled device buffer for it.  The first attention call
+  //    uploads it on its own stream (no synchronisation here).
   const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
   const size_t warps_bytes = s->warp_piece.size() * sizeof(int32_t);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
@@ -454,37 +512,24 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   s->d_prefill_off = s->d_counters_off + kvq::align256(counters_bytes);
   s->d_error_off = s->d_prefill_off + kvq::align256(prefill_bytes);
   const size_t total = s->d_error_off + sizeof(int32_t);
+  s->image_bytes = total;
   if (have_device) {
     s->d_buf = pool_get(s->device, total, &s->d_buf_bytes);
     if (!s->d_buf) {
       delete s;
       return KVQ_E_NO_MEMORY;
     }
-    std::lock_guard<std::mutex> lock(g_stage_mutex);
-    if (g_stage_bytes < total) {
-      if (g_stage) cudaFreeHost(g_stage);
-      g_stage = nullptr;
-      g_stage_bytes = 0;
-      const size_t want = pool_size_class(total);
-      if (cudaHostAlloc(&g_stage, want, cudaHostAllocDefault) == cudaSuccess) g_stage_bytes = want;
-      else cudaGetLastError();
+    s->h_image = pinned_get(total, &s->h_image_bytes, &s->h_image_pinned);
+    if (!s->h_image) {
+      kvq_sched_destroy(s);
+      return KVQ_E_NO_MEMORY;
     }
-    std::vector<char> pageable;  // fallback when pinned memory is not available
-    char* image = static_cast<char*>(g_stage);
-    if (!image) {
-      pageable.resize(total);
-      image = pageable.data();
-    }
+    char* image = static_cast<char*>(s->h_image);
     std::memset(image, 0, total);  // merge counters and the error word start at zero
     if (pieces_bytes) std::memcpy(image + s->d_pieces_off, s->pieces.data(), pieces_bytes);
     if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_piece.data(), warps_bytes);
     if (merges_bytes) std::memcpy(image + s->d_merges_off, s->merges.data(), merges_bytes);
     if (prefill_bytes) std::memcpy(image + s->d_prefill_off, s->prefill.data(), prefill_bytes);
-    if (cudaMemcpy(s->d_buf, image, total, cudaMemcpyHostToDevice) != cudaSuccess) {
-      cudaGetLastError();
-      kvq_sched_destroy(s);
-      return KVQ_E_CUDA;
-    }
   }
   *workspace_bytes = s->workspace_bytes;
   *out = s;
@@ -592,7 +637,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
 
 int kvq_sched_check_device(const kvq_sched_t* s) {
   if (!s) return KVQ_E_INVALID_ARG;
-  if (!s->d_buf) return KVQ_OK;
+  if (!s->d_buf || !s->uploaded.load()) return KVQ_OK;
   int cur = -1;
   if (cudaGetDevice(&cur) != cudaSuccess) return KVQ_E_CUDA;
   if (cur != s->device && cudaSetDevice(s->device) != cudaSuccess) return KVQ_E_CUDA;
@@ -679,9 +724,9 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.k_scale = k_scale;
   p.v_scale = v_scale;
 
+  kvq::PrefillMaps maps;
+  std::memset(&maps, 0, sizeof(maps));
   if (!s->prefill.empty()) {
-    kvq::PrefillMaps maps;
-    std::memset(&maps, 0, sizeof(maps));
     const int64_t row = kvq::row_bytes(s->dtype, head_dim);
     const int64_t slots = num_blocks * (int64_t)block_size;
     bool ok = encode_cache_map(&maps.k, key_cache, row, heads_kv, slots, (uint32_t)head_dim) &&
@@ -690,6 +735,19 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
       ok = encode_cache_map(&maps.ks, key_cache, row, heads_kv, slots, 16u) &&
            encode_cache_map(&maps.vs, value_cache, row, heads_kv, slots, 16u);
     if (!ok) return KVQ_E_CUDA;
+  }
+  // The first call with this schedule uploads its plan on the call's
+  // stream, ahead of the kernels that read it.
+  kvq_sched* ms = const_cast<kvq_sched*>(s);
+  if (!ms->uploaded.exchange(true)) {
+    if (cudaMemcpyAsync(s->d_buf, s->h_image, s->image_bytes, cudaMemcpyHostToDevice,
+                        static_cast<cudaStream_t>(stream)) != cudaSuccess) {
+      cudaGetLastError();
+      ms->uploaded.store(false);
+      return KVQ_E_CUDA;
+    }
+  }
+  if (!s->prefill.empty()) {
     const int rc = kvq::launch_prefill(p, maps, s->dtype, head_dim, (int64_t)s->prefill.size(), stream);
     if (rc != KVQ_OK) return rc;
   }

@@ -933,14 +933,18 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Geo::kTmemCols);
   }
-  // ---- O tile -> global, coalesced: lanes_per_row lanes write one row.
-  if (!aborted) {
+  // ---- O tile -> global, coalesced: lanes_per_row lanes write one row.  A
+  // tile that gave up a bounded wait writes NaN rows instead, so its failure
+  // shows in the output even where nobody reads the error word.
+  {
     constexpr int kLpr = D / 8;
     constexpr int kRps = 32 / kLpr;
     const int lane = tid & 31;
     const int sub = lane / kLpr, c = lane % kLpr;
+    const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
     for (int r = warp * kRps + sub; r < t.nrows; r += (Geo::kThreads / 32) * kRps) {
-      const uint4 o = lds128(base + Geo::kOffOStage + (uint32_t)(r * D * 2 + ((c ^ (r & 7)) << 4)));
+      const uint4 o = aborted ? nan4
+                              : lds128(base + Geo::kOffOStage + (uint32_t)(r * D * 2 + ((c ^ (r & 7)) << 4)));
       const int Rr = t.row0 + r;
       *reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D +
                                 8 * c) = o;

@@ -3,20 +3,25 @@
 
 Tolerances (written here, used by every attention parity test):
   * cache bytes and scales: bit-exact;
-  * attention output (bf16) against the oracle -- the stated bounds are
-    max-abs 1e-2 and mean-abs 1e-3, widened by two things no binary32
-    kernel can avoid:
-      - rounding the output to bf16 moves it by up to half a bf16 ulp
-        (0.0156 at |ref| >= 4, a mean of about 1e-3 for outputs near 1);
+  * attention output (bf16) against the oracle's binary64 result: the stated
+    bounds are max-abs 1e-2 and mean-abs 1e-3.  Every comparison reports
+    the plain max-abs and mean-abs errors against them.  Two effects that no
+    kernel with a bf16 output and binary32 arithmetic avoids can make the
+    stated bounds unreachable:
+      - the output is a bf16 number: rounding it moves it by up to half a
+        bf16 ulp (0.0156 where |o| >= 4) -- even the oracle's own result,
+        rounded to bf16, misses 1e-2 there ("floor" in the report);
       - scores accumulated in binary32 and softmax weights rounded to an
-        11-bit significand move the output by up to B, the first-order
-        forward error bound the oracle computes for every element
-        (oracle.attention_fp32_bound).  B matters only for the large
-        scores that x20 outliers times x10 token scales produce, where a
-        binary32 score error of a few 1e-4 moves a weight by as much.
-    Per element  |gpu - ref| <= max(1e-2, ulp(ref)) + B,  and
-    mean |gpu - ref| <= 1e-3 + mean(ulp(ref) / 2) + mean(B).  The plain
-    max-abs and mean-abs errors are returned (and reported) as well.
+        11-bit significand (the 16-bit P operand of the P.V product, which
+        the pages' own tile GEMMs also use) move the binary32 result by up
+        to B, the first-order forward error bound the oracle computes for
+        every element (oracle.attention_fp32_bound).
+    A binary32 result within B of the exact value, rounded to bf16, lands
+    within half_ulp(|ref| + B) + B of it.  So per element
+        |gpu - ref| <= max(1e-2, half_ulp(|ref| + B) + B),
+    and  mean |gpu - ref| <= max(1e-3, mean(half_ulp) + mean(B)).
+    Where that allowance exceeds the stated 1e-2 the report counts the
+    elements, and how much of their allowance is B.
 """
 from __future__ import annotations
 
@@ -160,25 +165,65 @@ def bf16_ulp(x: np.ndarray) -> np.ndarray:
     return 2.0 ** (np.floor(np.log2(ax)) - 7)
 
 
+def bf16_round(x: np.ndarray) -> np.ndarray:
+    """x (float32) rounded to bf16, to nearest even, back in float64."""
+    return torch.from_numpy(np.ascontiguousarray(x, np.float32)).to(torch.bfloat16).double().numpy()
+
+
+STATED_MAX, STATED_MEAN = 1e-2, 1e-3
+REPORTS = []   # one entry per comparison (written out by conftest when asked)
+
+
 def attention_errors(got: np.ndarray, ref: np.ndarray, bound=None) -> dict:
     err = np.abs(got.astype(np.float64) - ref.astype(np.float64))
     b = np.zeros_like(err) if bound is None else np.asarray(bound, np.float64)
-    allowed = np.maximum(1e-2, bf16_ulp(ref)) + b
-    return {"max_abs": float(err.max()) if err.size else 0.0,
-            "mean_abs": float(err.mean()) if err.size else 0.0,
-            "worst_ratio": float((err / allowed).max()) if err.size else 0.0,
-            "mean_bound": 1e-3 + (float(bf16_ulp(ref).mean()) / 2 + float(b.mean())
-                                  if err.size else 0.0),
-            "n": int(err.size)}
+    if not err.size:
+        return {"n": 0, "max_abs": 0.0, "mean_abs": 0.0, "worst_ratio": 0.0,
+                "mean_allowed": STATED_MEAN, "stated_max_ok": True, "stated_mean_ok": True,
+                "floor_max": 0.0, "floor_mean": 0.0, "n_beyond_stated": 0,
+                "b_share_beyond": 0.0, "mean_b": 0.0}
+    half = bf16_ulp(np.abs(ref.astype(np.float64)) + b) / 2
+    allowed = np.maximum(STATED_MAX, half + b)
+    floor = np.abs(bf16_round(ref) - ref.astype(np.float64))
+    beyond = err > STATED_MAX
+    share = (b[beyond] / (half[beyond] + b[beyond])) if beyond.any() else np.zeros(0)
+    mean_allowed = max(STATED_MEAN, float(half.mean()) + float(b.mean()))
+    max_abs, mean_abs = float(err.max()), float(err.mean())
+    return {"n": int(err.size), "max_abs": max_abs, "mean_abs": mean_abs,
+            "stated_max_ok": max_abs <= STATED_MAX, "stated_mean_ok": mean_abs <= STATED_MEAN,
+            "floor_max": float(floor.max()), "floor_mean": float(floor.mean()),
+            "n_beyond_stated": int(beyond.sum()),
+            # elements beyond 1e-2 whose allowance is mostly B (not bf16 rounding)
+            "n_beyond_mostly_b": int((share > 0.5).sum()),
+            "b_share_beyond": float(share.mean()) if share.size else 0.0,
+            "mean_b": float(b.mean()), "max_b": float(b.max()),
+            "worst_ratio": float((err / allowed).max()), "mean_allowed": mean_allowed}
 
 
 def assert_attention_close(got: np.ndarray, ref: np.ndarray, what: str = "",
-                           bound=None) -> dict:
+                           bound=None, stated=False) -> dict:
+    """Compare; with ``stated`` the plain stated bounds (max-abs 1e-2,
+    mean-abs 1e-3) must hold as well."""
     assert np.all(np.isfinite(got)), f"{what}: non-finite output"
     e = attention_errors(got, ref, bound)
+    REPORTS.append(dict(e, what=what))
     assert e["worst_ratio"] <= 1.0, f"{what}: {e}"
-    assert e["mean_abs"] <= e["mean_bound"], f"{what}: {e}"
+    assert e["mean_abs"] <= e["mean_allowed"], f"{what}: {e}"
+    if stated:
+        assert e["stated_max_ok"] and e["stated_mean_ok"], f"{what} (stated bounds): {e}"
     return e
+
+
+def describe(e: dict) -> str:
+    """One line: the plain errors against the stated bounds, and why any
+    element beyond 1e-2 is allowed."""
+    s = (f"max|err| {e['max_abs']:.2e}, mean {e['mean_abs']:.2e} "
+         f"(stated 1e-2 / 1e-3: {'met' if e['stated_max_ok'] and e['stated_mean_ok'] else 'missed'})")
+    if not (e["stated_max_ok"] and e["stated_mean_ok"]):
+        s += (f"; bf16(oracle) itself misses by max {e['floor_max']:.2e}, mean "
+              f"{e['floor_mean']:.2e}; {e['n_beyond_stated']} elements beyond 1e-2, all within "
+              f"half a bf16 ulp + the binary32 bound B (B's share {e['b_share_beyond']:.0%})")
+    return s
 
 
 def visible_window_mask(wl, tokens_of_requests):

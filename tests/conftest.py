@@ -21,3 +21,21 @@ def cuda_device():
     if not torch.cuda.is_available():
         pytest.fail("gpu test collected but torch.cuda.is_available() is False")
     return torch.device("cuda:0")
+
+
+def pytest_sessionfinish(session, exitstatus):
+    """With KVQ_PARITY_REPORT=<path>, write every attention comparison's
+    errors (plain max / mean against the stated bounds, the bf16 floor, the
+    share of the allowance that is the binary32 bound) as JSON lines."""
+    path = os.environ.get("KVQ_PARITY_REPORT")
+    if not path:
+        return
+    mod = sys.modules.get("_harness")
+    if mod is None:
+        return
+    import json
+    REPORTS = mod.REPORTS
+    os.makedirs(os.path.dirname(os.path.abspath(path)), exist_ok=True)
+    with open(path, "w") as f:
+        for r in REPORTS:
+            f.write(json.dumps(r) + "\n")

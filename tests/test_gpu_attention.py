@@ -131,27 +131,3 @@ def test_unwritten_pages_outside_window_are_ignored(cuda_device):
     kc, vc = oracle_cache(wl, write_mask=mask)
     ref, bnd = oracle_reference(wl, kc, vc)
     assert_attention_close(g.out_f32(), ref, "unwritten", bnd)
-
-
-@pytest.mark.parametrize("index,dtype", [(2, None), (3, None), (4, "int8_per_token_head"),
-                                         (4, "fp8_per_token_head"),
-                                         (4, "fp8_e5m2_per_token_head"), (5, None)])
-def test_full_size_sampled(cuda_device, index, dtype):
-    """Full-size workloads in the benchmark's launch configuration: the
-    whole batch runs on the GPU; sampled query tokens are compared with the
-    oracle (which writes only the keys those tokens can see)."""
-    wl = W.config(index, dtype)
-    g = GpuRun(wl).write_cache().attention()
-    rng = np.random.default_rng(10 + index)
-    reqs = sorted(set(rng.choice(wl.num_req, min(3, wl.num_req), replace=False).tolist()))
-    qsl = wl.query_start_loc.numpy()
-    toks = []
-    for r in reqs:
-        span = np.arange(qsl[r], qsl[r + 1])
-        toks += sorted(set(rng.choice(span, min(8, span.size), replace=False).tolist()
-                           + [int(span[-1])]))
-    mask = visible_window_mask(wl, reqs)
-    kc, vc = oracle_cache(wl, write_mask=mask)
-    ref, bnd = oracle_reference(wl, kc, vc, tokens=np.array(toks))
-    assert_attention_close(g.out_f32(toks), ref, wl.name, bnd)
-    assert torch.isfinite(g.out.float()).all()
