@@ -173,8 +173,9 @@ KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  * caches, dequantisation fused into the tiles, online softmax.
  * [P1] Breakdown items 2-3 (tile GEMMs with fused fp8 dequantisation,
  * cpu_attention_with_kv_cache) and Risks (scale folding); [P2] Key source
- * snippet (causal, window_size, soft_cap, paged blocks); [P3] Breakdown
- * item 3 (_prepare_kv_tile: per-token-head dequantisation in the tile).
+ * snippet (causal, window_size, soft_cap, paged blocks, use_alibi,
+ * use_sink); [P3] Breakdown item 3 (_prepare_kv_tile: per-token-head
+ * dequantisation in the tile).
  *
  *   sched                   from kvq_get_scheduler_metadata.
  *   heads_q, heads_kv,      what the caller believes the caches and q hold;
@@ -182,6 +183,8 @@ KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  *                           the schedule was built for, else
  *                           KVQ_E_SCHED_MISMATCH.  (The bug of [P2]: tiles
  *                           sized for one KV element size, run on another.)
+ *                           Every dtype is supported, KVQ_AUTO (bf16 rows)
+ *                           included.
  *   q                       device bf16 [sum Q, heads_q, head_dim], contiguous,
  *                           16-byte aligned.
  *   key_cache, value_cache  as written by kvq_reshape_and_cache.
@@ -196,15 +199,24 @@ KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  *   sm_scale                score scale (typically 1/sqrt(head_dim)).
  *   soft_cap                > 0: z <- soft_cap * tanh(z / soft_cap) after
  *                           sm_scale; <= 0: off.
+ *   alibi_slopes            device fp32 [heads_q] or NULL: z <- z + slope_h *
+ *                           (j - p) for key j and query position p, after
+ *                           the soft cap (use_alibi of [P2]).
+ *   sinks                   device fp32 [heads_q] or NULL: one extra logit
+ *                           s_h per q head in the softmax normaliser, with
+ *                           no value: o = sum_j e^z_j v_j / (e^s_h +
+ *                           sum_j e^z_j) (use_sink of [P2]).
  *   k_scale, v_scale        per-tensor scales (per-tensor fp8 only), folded
  *                           into the scores and the output.
  *   out                     device bf16 [sum Q, heads_q, head_dim].
  *   workspace               device scratch of >= the scheduler's
  *                           workspace_bytes (256-byte aligned; may be NULL
  *                           when that is 0).  Calls sharing one workspace
- *                           must be ordered on one stream.
+ *                           or one schedule must be ordered on one stream.
  * Query row i of a request sits at position L - Q + i; key j is visible iff
- * (!causal || j <= p) and (window <= 0 || p - j < window). */
+ * (!causal || j <= p) and (window <= 0 || p - j < window).  A kernel that
+ * gives up one of its bounded waits writes NaN rows and sets the schedule's
+ * error word (kvq_sched_check_device). */
 KVQ_API int kvq_attention_with_kv_cache(const kvq_sched_t* sched, int heads_q,
                                 int heads_kv, int head_dim, kvq_dtype_t dtype,
                                 const void* q,
@@ -214,9 +226,11 @@ KVQ_API int kvq_attention_with_kv_cache(const kvq_sched_t* sched, int heads_q,
                                 const int32_t* block_table,
                                 int block_table_stride, int block_size,
                                 int64_t num_blocks, float sm_scale, int causal,
-                                int window, float soft_cap, float k_scale,
-                                float v_scale, void* out, void* workspace,
-                                size_t workspace_bytes, void* stream);
+                                int window, float soft_cap,
+                                const float* alibi_slopes, const float* sinks,
+                                float k_scale, float v_scale, void* out,
+                                void* workspace, size_t workspace_bytes,
+                                void* stream);
 
 /* attention_with_kv_cache_static_scratch -- the same attention for callers
  * that cannot allocate device memory (no cudaMalloc in their context: a
@@ -243,7 +257,8 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
     const void* q, const void* key_cache, const void* value_cache,
     const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,
     int block_table_stride, int block_size, int64_t num_blocks, float sm_scale, int causal,
-    int window, float soft_cap, float k_scale, float v_scale, void* out, void* stream);
+    int window, float soft_cap, const float* alibi_slopes, const float* sinks, float k_scale,
+    float v_scale, void* out, void* stream);
 
 /* Free a schedule (NULL is a no-op).  No counterpart on the pages (their
  * schedule is a torch tensor that the garbage collector frees); it is the

@@ -52,10 +52,12 @@ namespace kvq {
 
 template <int DT, int D>
 struct DecodeGeom {
+  static constexpr bool kAuto = DT == KVQ_AUTO;  // bf16 rows, bf16 MMAs
+  static constexpr int kEB = kv_elem_bytes(DT);
   static constexpr int kKsteps = D / 16;     // MMA k-steps over head_dim (QK)
   static constexpr int kMtiles = D / 16;     // MMA m-tiles over head_dim (PV)
-  static constexpr int kK16 = D / 64;        // 16-byte K pieces per lane per row
-  static constexpr int kVBytes = D / 8;      // V bytes per lane per row
+  static constexpr int kK16 = D * kEB / 64;  // 16-byte K pieces per lane per row
+  static constexpr int kVBytes = D * kEB / 8;  // V bytes per lane per row
   static constexpr int kVPieces = kVBytes >= 16 ? kVBytes / 16 : 1;
   static constexpr int kVSlots = D / 32;     // 16-byte V slots per lane
   static constexpr bool kPth = is_per_token_head(DT);
@@ -66,11 +68,16 @@ struct DecodeGeom {
 
 // Head dim of element k (0: MMA row g, 1: row g + 8) of P.V m-tile mi for a
 // lane of group g: each lane owns 16-byte runs of every V row (8 bytes for
-// head_dim 64), the runs of the 8 groups side by side.
-template <int D>
+// head_dim 64), the runs of the 8 groups side by side.  A 16-byte run is 16
+// codes (two per m-tile) or, for bf16 rows, 8 values (two per m-tile).
+template <int DT, int D>
 __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
-  constexpr int run = D / 8 >= 16 ? 16 : D / 8;
-  return (mi / 8) * 128 + g * run + 2 * (mi % 8) + k;
+  if constexpr (DT == KVQ_AUTO) {
+    return (mi / 4) * 64 + g * 8 + 2 * (mi % 4) + k;
+  } else {
+    constexpr int run = D / 8 >= 16 ? 16 : D / 8;
+    return (mi / 8) * 128 + g * run + 2 * (mi % 8) + k;
+  }
 }
 
 // Merge of a tile's pieces (vllm PR 50194 page, Key source snippet:
@@ -107,7 +114,14 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
       w[s] = active && s < ns ? __ldcg(lse + s * nr + n) : -INFINITY;
       M = fmaxf(M, w[s]);
     }
-    float wsum = 0.0f;
+    // An attention sink is one more term of the normaliser (no value).  The
+    // pieces' log-sum-exps carry the weights' 2^6 lift, so the sink's logit
+    // (log2 units) does too.
+    const float sink = p.sinks && active
+                           ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], 1.4426950408889634f, 6.0f)
+                           : -INFINITY;
+    M = fmaxf(M, sink);
+    float wsum = sink == -INFINITY ? 0.0f : exp2f(sink - M);
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
       w[s] = (w[s] == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(w[s] - M);
@@ -143,10 +157,14 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
     for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + s * nr + n));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float sink =  // (log2 units, with the pieces' 2^6 lift)
+        p.sinks ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], 1.4426950408889634f, 6.0f)
+                : -INFINITY;
+    M = fmaxf(M, sink);
     float acc[kPer];
 #pragma unroll
     for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
-    float wsum = 0.0f;
+    float wsum = sink == -INFINITY ? 0.0f : exp2f(sink - M);
     for (int s = 0; s < ns; ++s) {
       const float l = __ldcg(lse + s * nr + n);
       const float w = (l == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l - M);
@@ -167,7 +185,7 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
   }
 }
 
-template <int DT, int D, int NT>
+template <int DT, int D, int NT, bool AL>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_ctas(DT, D, NT))
 splitkv_decode_kernel(const AttnParams p) {
   using Geo = DecodeGeom<DT, D>;
@@ -328,6 +346,9 @@ splitkv_decode_kernel(const AttnParams p) {
   float o[NT][Geo::kMtiles][4];
   float m_run[NT][2], l_run[NT][2];
   int ev = -1000;
+  // ALiBi: per column, the slope in log2 units and the query position.
+  float al_slope[NT][2];
+  int al_pos[NT][2];
 
   // Start a piece: Q fragments (B operand of S^T = K Q^T) and masks.  Q
   // enters the MMA exactly: bf16 values scaled by a power of two only (8
@@ -342,6 +363,28 @@ splitkv_decode_kernel(const AttnParams p) {
     const int p_max = L - Q + (pc.row0 + pc.nrows - 1) / G;
     all_lo = W > 0 ? p_max - W + 1 : 0;
     all_hi = p.causal ? p_min + 1 : L;
+    float q_unmul = 1.0f;
+    if constexpr (Geo::kAuto) {
+      // bf16 rows: Q enters the bf16 MMA as it is.  Lane c holds dims
+      // 32i + 8c + [0, 8) of its rows (k-steps 2i and 2i + 1).
+#pragma unroll
+      for (int t = 0; t < NT; ++t) {
+        const int nr = 8 * t + g;
+        const bool valid = nr < pc.nrows;
+        const int R = pc.row0 + (valid ? nr : 0);
+        const int tok = q0 + R / G;
+        const int head = pc.kv_head * G + R % G;
+        const uint16_t* src = p.q + ((int64_t)tok * p.heads_q + head) * D + 8 * c;
+#pragma unroll
+        for (int i = 0; i < D / 32; ++i) {
+          const uint4 w = valid ? *reinterpret_cast<const uint4*>(src + 32 * i) : make_uint4(0, 0, 0, 0);
+          qf[t][2 * i][0] = w.x;
+          qf[t][2 * i][1] = w.y;
+          qf[t][2 * i + 1][0] = w.z;
+          qf[t][2 * i + 1][1] = w.w;
+        }
+      }
+    } else {
     float qv[NT][D / 4];
     float qmax = 0.0f;
 #pragma unroll
@@ -379,7 +422,7 @@ splitkv_decode_kernel(const AttnParams p) {
       shift = max(-126, min(126, 15 - e));
     }
     const float q_mul = __int_as_float((127 + shift) << 23);
-    const float q_unmul = __int_as_float((127 - shift) << 23);
+    q_unmul = __int_as_float((127 - shift) << 23);
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -387,6 +430,7 @@ splitkv_decode_kernel(const AttnParams p) {
         qf[t][j][0] = dev::pack_f16x2(qv[t][4 * j] * q_mul, qv[t][4 * j + 1] * q_mul);
         qf[t][j][1] = dev::pack_f16x2(qv[t][4 * j + 2] * q_mul, qv[t][4 * j + 3] * q_mul);
       }
+    }
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -395,8 +439,12 @@ splitkv_decode_kernel(const AttnParams p) {
         const int pn = L - Q + (pc.row0 + nr) / G;
         col_hi[t][k] = p.causal ? pn + 1 : L;
         col_lo[t][k] = W > 0 ? pn - W + 1 : 0;
+        if constexpr (AL) {
+          al_slope[t][k] = p.alibi_slopes[pc.kv_head * G + (pc.row0 + nr) % G] * log2e;
+          al_pos[t][k] = pn;
+        }
       }
-    score_mul = q_unmul * base_scale * (Geo::kPth ? 1.0f : p.k_scale);
+    score_mul = q_unmul * base_scale * (Geo::kPth || Geo::kAuto ? 1.0f : p.k_scale);
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
 #pragma unroll
@@ -418,7 +466,20 @@ splitkv_decode_kernel(const AttnParams p) {
         for (int off = 4; off < 32; off <<= 1)
           l_run[t][k] += __shfl_xor_sync(0xffffffffu, l_run[t][k], off);
     const float unit = Geo::kPth && ev > -1000 ? ldexpf(1.0f, ev) : 1.0f;
-    const float vmul = Geo::kPth ? 1.0f : p.v_scale;
+    const float vmul = Geo::kPth || Geo::kAuto ? 1.0f : p.v_scale;
+    // An attention sink joins the normaliser of a whole (uncut) tile here;
+    // a cut tile's merge adds it once.  The weights carry 2^-(m_run - 6).
+    if (p.sinks && pc.part < 0) {
+#pragma unroll
+      for (int t = 0; t < NT; ++t)
+#pragma unroll
+        for (int k = 0; k < 2; ++k) {
+          const int nr = min(8 * t + 2 * c + k, pc.nrows - 1);
+          const float sk = p.sinks[pc.kv_head * G + (pc.row0 + nr) % G] * log2e;
+          if (m_run[t][k] != -INFINITY && sk != -INFINITY)
+            l_run[t][k] += exp2f(fminf(sk - m_run[t][k] + 6.0f, 126.0f));
+        }
+    }
 #pragma unroll
     for (int t = 0; t < NT; ++t)
 #pragma unroll
@@ -441,13 +502,13 @@ splitkv_decode_kernel(const AttnParams p) {
             uint2 w2;
             w2.x = dev::pack_bf16x2(o[t][r0 + 2][k] * sc, o[t][r0 + 2][k + 2] * sc);
             w2.y = dev::pack_bf16x2(o[t][r0 + 3][k] * sc, o[t][r0 + 3][k + 2] * sc);
-            *reinterpret_cast<uint4*>(dst + pv_dim<D>(r0, g, 0)) = make_uint4(w.x, w.y, w2.x, w2.y);
+            *reinterpret_cast<uint4*>(dst + pv_dim<DT, D>(r0, g, 0)) = make_uint4(w.x, w.y, w2.x, w2.y);
           }
         } else {
           float* dst = p.part_o + (int64_t)(pc.part + nr) * D;
 #pragma unroll
           for (int r0 = 0; r0 < Geo::kMtiles; r0 += 2)
-            *reinterpret_cast<float4*>(dst + pv_dim<D>(r0, g, 0)) =
+            *reinterpret_cast<float4*>(dst + pv_dim<DT, D>(r0, g, 0)) =
                 make_float4(o[t][r0][k] * sc, o[t][r0][k + 2] * sc, o[t][r0 + 1][k] * sc,
                             o[t][r0 + 1][k + 2] * sc);
           if (g == 0) p.part_lse[pc.part + nr] = l > 0.0f ? m_run[t][k] + log2f(l) : -INFINITY;
@@ -526,16 +587,30 @@ splitkv_decode_kernel(const AttnParams p) {
       const uint4 kg8 = kreg[1][i];
       const uint32_t wg[4] = {kg.x, kg.y, kg.z, kg.w};
       const uint32_t wg8[4] = {kg8.x, kg8.y, kg8.z, kg8.w};
+      if constexpr (Geo::kAuto) {
+        // 8 bf16 per piece: k-steps 2i (words 0, 1) and 2i + 1 (words 2, 3).
 #pragma unroll
-      for (int w = 0; w < 4; ++w) {
-        const int j = 4 * i + w;
-        uint32_t a[4];
-        dev::word_to_f16x2x2<DT>(wg[w], a[0], a[2]);
-        dev::word_to_f16x2x2<DT>(wg8[w], a[1], a[3]);
+        for (int w2 = 0; w2 < 2; ++w2) {
+          const int j = 2 * i + w2;
+          const uint32_t a[4] = {wg[2 * w2], wg8[2 * w2], wg[2 * w2 + 1], wg8[2 * w2 + 1]};
 #pragma unroll
-        for (int t = 0; t < NT; ++t) {
-          if (w & 1) dev::mma_f16_16816(s2[t], a, qf[t][j][0], qf[t][j][1]);
-          else dev::mma_f16_16816(s[t], a, qf[t][j][0], qf[t][j][1]);
+          for (int t = 0; t < NT; ++t) {
+            if (w2 & 1) dev::mma_bf16_16816(s2[t], a, qf[t][j][0], qf[t][j][1]);
+            else dev::mma_bf16_16816(s[t], a, qf[t][j][0], qf[t][j][1]);
+          }
+        }
+      } else {
+#pragma unroll
+        for (int w = 0; w < 4; ++w) {
+          const int j = 4 * i + w;
+          uint32_t a[4];
+          dev::word_to_f16x2x2<DT>(wg[w], a[0], a[2]);
+          dev::word_to_f16x2x2<DT>(wg8[w], a[1], a[3]);
+#pragma unroll
+          for (int t = 0; t < NT; ++t) {
+            if (w & 1) dev::mma_f16_16816(s2[t], a, qf[t][j][0], qf[t][j][1]);
+            else dev::mma_f16_16816(s[t], a, qf[t][j][0], qf[t][j][1]);
+          }
         }
       }
     }
@@ -549,6 +624,7 @@ splitkv_decode_kernel(const AttnParams p) {
     // shuffles.  l carries the same 2^6 factor, which cancels in O / l.
     const bool full = chunk_ok && tok0 >= all_lo && tok0 + kChunkTokens <= all_hi;
     uint32_t pb0[NT], pb1[NT];
+    uint32_t pl0[NT], pl1[NT];  // bf16 rows: the low halves of P (P = hi + lo)
     float z[NT][4];
     bool grow = false;
 #pragma unroll
@@ -558,6 +634,8 @@ splitkv_decode_kernel(const AttnParams p) {
         const float sk = (e < 2) ? sk0 : sk1;
         float v = (s[t][e] + s2[t][e]) * score_mul * sk;
         if (cap > 0.0f) v = cap_l2 * dev::tanh_exp(v * inv_cap);
+        if constexpr (AL)  // bias from the exact integer distance, after the cap
+          v = fmaf(al_slope[t][e & 1], (float)(tok0 + g + 8 * (e >> 1) - al_pos[t][e & 1]), v);
         if (!full) {
           const int tok = tok0 + g + 8 * (e >> 1);
           const int col = e & 1;
@@ -598,8 +676,17 @@ splitkv_decode_kernel(const AttnParams p) {
       l_run[t][0] += p0 + p2;
       l_run[t][1] += p1 + p3;
       // P^T (tokens x rows) -> B operand of O^T = V^T P^T via transposes.
-      pb0[t] = dev::movmatrix_trans(dev::pack_f16x2(p0 * sv0, p1 * sv0));
-      pb1[t] = dev::movmatrix_trans(dev::pack_f16x2(p2 * sv1, p3 * sv1));
+      if constexpr (Geo::kAuto) {
+        // bf16 MMA: P as the sum of two bf16 numbers (16 significant bits).
+        const uint32_t h01 = dev::pack_bf16x2(p0, p1), h23 = dev::pack_bf16x2(p2, p3);
+        pb0[t] = dev::movmatrix_trans(h01);
+        pb1[t] = dev::movmatrix_trans(h23);
+        pl0[t] = dev::movmatrix_trans(dev::pack_bf16x2(p0 - dev::bf16_lo(h01), p1 - dev::bf16_hi(h01)));
+        pl1[t] = dev::movmatrix_trans(dev::pack_bf16x2(p2 - dev::bf16_lo(h23), p3 - dev::bf16_hi(h23)));
+      } else {
+        pb0[t] = dev::movmatrix_trans(dev::pack_f16x2(p0 * sv0, p1 * sv0));
+        pb1[t] = dev::movmatrix_trans(dev::pack_f16x2(p2 * sv1, p3 * sv1));
+      }
     }
     if (rescale || rescale_v) {
 #pragma unroll
@@ -631,21 +718,37 @@ splitkv_decode_kernel(const AttnParams p) {
         r2[0] = a2.x; r2[1] = a2.y; r2[2] = a2.z; r2[3] = a2.w;
         r3[0] = a3.x; r3[1] = a3.y; r3[2] = a3.z; r3[3] = a3.w;
       }
-      // Word w of rows 2c / 2c+1 -> bytes (b0, b1) and (b2, b3) paired across
-      // the two tokens: m-tiles 2(vs*kWords + w) and 2(vs*kWords + w) + 1.
+      if constexpr (Geo::kAuto) {
+        // Word w of rows 2c / 2c+1 holds dims (2w, 2w + 1) of the run: the
+        // two tokens' values of one dim pair up per half (m-tile 4 vs + w).
 #pragma unroll
-      for (int w = 0; w < kWords; ++w) {
+        for (int w = 0; w < 4; ++w) {
+          const uint32_t a[4] = {dev::prmt(r0[w], r1[w], 0x5410u), dev::prmt(r0[w], r1[w], 0x7632u),
+                                 dev::prmt(r2[w], r3[w], 0x5410u), dev::prmt(r2[w], r3[w], 0x7632u)};
+          const int i = vs * 4 + w;  // m-tile
 #pragma unroll
-        for (int half = 0; half < 2; ++half) {
-          const uint32_t sel = half ? 0x7362u : 0x5140u;
-          const uint32_t x01 = dev::prmt(r0[w], r1[w], sel);
-          const uint32_t x23 = dev::prmt(r2[w], r3[w], sel);
-          uint32_t a[4];
-          dev::word_to_f16x2x2<DT>(x01, a[0], a[1]);
-          dev::word_to_f16x2x2<DT>(x23, a[2], a[3]);
-          const int i = (vs * kWords + w) * 2 + half;  // m-tile
+          for (int t = 0; t < NT; ++t) {
+            dev::mma_bf16_16816(o[t][i], a, pb0[t], pb1[t]);
+            dev::mma_bf16_16816(o[t][i], a, pl0[t], pl1[t]);
+          }
+        }
+      } else {
+        // Word w of rows 2c / 2c+1 -> bytes (b0, b1) and (b2, b3) paired
+        // across the two tokens: m-tiles 2(vs*kWords + w) and 2(vs*kWords + w) + 1.
 #pragma unroll
-          for (int t = 0; t < NT; ++t) dev::mma_f16_16816(o[t][i], a, pb0[t], pb1[t]);
+        for (int w = 0; w < kWords; ++w) {
+#pragma unroll
+          for (int half = 0; half < 2; ++half) {
+            const uint32_t sel = half ? 0x7362u : 0x5140u;
+            const uint32_t x01 = dev::prmt(r0[w], r1[w], sel);
+            const uint32_t x23 = dev::prmt(r2[w], r3[w], sel);
+            uint32_t a[4];
+            dev::word_to_f16x2x2<DT>(x01, a[0], a[1]);
+            dev::word_to_f16x2x2<DT>(x23, a[2], a[3]);
+            const int i = (vs * kWords + w) * 2 + half;  // m-tile
+#pragma unroll
+            for (int t = 0; t < NT; ++t) dev::mma_f16_16816(o[t][i], a, pb0[t], pb1[t]);
+          }
         }
       }
     }
@@ -668,10 +771,10 @@ splitkv_decode_kernel(const AttnParams p) {
 }
 
 // Launch one instance (used by the per-head_dim translation units).
-template <int DT, int D, int NT>
+template <int DT, int D, int NT, bool AL>
 int launch_decode_instance(const AttnParams& p, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes(DT, D);
-  auto kern = splitkv_decode_kernel<DT, D, NT>;
+  auto kern = splitkv_decode_kernel<DT, D, NT, AL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
@@ -679,13 +782,16 @@ int launch_decode_instance(const AttnParams& p, cudaStream_t stream) {
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 
-template <int D>
+// The instances of one head_dim and one ALiBi setting (one translation unit
+// each keeps the build parallel).
+template <int D, bool AL>
 int launch_decode_d(const AttnParams& p, int dtype, int ntiles, cudaStream_t stream) {
-#define KVQ_DECODE_CASE(DT)                                                                   \
-  case DT:                                                                                    \
-    return ntiles == 1 ? launch_decode_instance<DT, D, 1>(p, stream)                          \
-                       : launch_decode_instance<DT, D, 2>(p, stream);
+#define KVQ_DECODE_CASE(DT)                                                  \
+  case DT:                                                                   \
+    return ntiles == 1 ? launch_decode_instance<DT, D, 1, AL>(p, stream)     \
+                       : launch_decode_instance<DT, D, 2, AL>(p, stream);
   switch (dtype) {
+    KVQ_DECODE_CASE(KVQ_AUTO)
     KVQ_DECODE_CASE(KVQ_FP8_E4M3)
     KVQ_DECODE_CASE(KVQ_FP8_E5M2)
     KVQ_DECODE_CASE(KVQ_INT8_PER_TOKEN_HEAD)

@@ -1,9 +1,9 @@
 // kvq_decode_d128.cu -- split-KV decode kernels for head_dim 128 (one
-// translation unit per head_dim keeps the build parallel).
+// translation unit per head_dim and ALiBi setting keeps the build parallel).
 #include "kvq_decode.cuh"
 
 namespace kvq {
 int launch_decode_d128(const AttnParams& p, int dtype, int ntiles, void* stream) {
-  return launch_decode_d<128>(p, dtype, ntiles, static_cast<cudaStream_t>(stream));
+  return launch_decode_d<128, false>(p, dtype, ntiles, static_cast<cudaStream_t>(stream));
 }
 }  // namespace kvq

@@ -1,23 +1,30 @@
-// kvq_decode_dispatch.cu -- head_dim dispatch of the split-KV decode and the
-// tensor-core prefill kernels (one translation unit per head_dim holds the
-// instances).
+// kvq_decode_dispatch.cu -- head_dim (and ALiBi) dispatch of the split-KV
+// decode and the tensor-core prefill kernels (one translation unit per
+// head_dim and ALiBi setting holds the instances).
 #include "kvq_internal.h"
 
 namespace kvq {
 
-int launch_decode_d64(const AttnParams&, int, int, void*);
-int launch_decode_d128(const AttnParams&, int, int, void*);
-int launch_decode_d256(const AttnParams&, int, int, void*);
-int launch_prefill_d64(const AttnParams&, const PrefillMaps&, int, int64_t, void*);
-int launch_prefill_d128(const AttnParams&, const PrefillMaps&, int, int64_t, void*);
-int launch_prefill_d256(const AttnParams&, const PrefillMaps&, int, int64_t, void*);
+#define KVQ_DECLARE(D)                                                                       \
+  int launch_decode_d##D(const AttnParams&, int, int, void*);                               \
+  int launch_decode_d##D##_alibi(const AttnParams&, int, int, void*);                       \
+  int launch_prefill_d##D(const AttnParams&, const PrefillMaps&, int, int64_t, void*);      \
+  int launch_prefill_d##D##_alibi(const AttnParams&, const PrefillMaps&, int, int64_t, void*);
+KVQ_DECLARE(64)
+KVQ_DECLARE(128)
+KVQ_DECLARE(256)
+#undef KVQ_DECLARE
 
 int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream) {
   if (p.num_chunks <= 0) return KVQ_OK;
+  const bool al = uses_alibi(p);
   switch (head_dim) {
-    case 64: return launch_decode_d64(p, dtype, ntiles, stream);
-    case 128: return launch_decode_d128(p, dtype, ntiles, stream);
-    case 256: return launch_decode_d256(p, dtype, ntiles, stream);
+    case 64: return al ? launch_decode_d64_alibi(p, dtype, ntiles, stream)
+                       : launch_decode_d64(p, dtype, ntiles, stream);
+    case 128: return al ? launch_decode_d128_alibi(p, dtype, ntiles, stream)
+                        : launch_decode_d128(p, dtype, ntiles, stream);
+    case 256: return al ? launch_decode_d256_alibi(p, dtype, ntiles, stream)
+                        : launch_decode_d256(p, dtype, ntiles, stream);
     default: return KVQ_E_UNSUPPORTED;
   }
 }
@@ -25,10 +32,14 @@ int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
                    int64_t num_tiles, void* stream) {
   if (num_tiles <= 0) return KVQ_OK;
+  const bool al = uses_alibi(p);
   switch (head_dim) {
-    case 64: return launch_prefill_d64(p, maps, dtype, num_tiles, stream);
-    case 128: return launch_prefill_d128(p, maps, dtype, num_tiles, stream);
-    case 256: return launch_prefill_d256(p, maps, dtype, num_tiles, stream);
+    case 64: return al ? launch_prefill_d64_alibi(p, maps, dtype, num_tiles, stream)
+                       : launch_prefill_d64(p, maps, dtype, num_tiles, stream);
+    case 128: return al ? launch_prefill_d128_alibi(p, maps, dtype, num_tiles, stream)
+                        : launch_prefill_d128(p, maps, dtype, num_tiles, stream);
+    case 256: return al ? launch_prefill_d256_alibi(p, maps, dtype, num_tiles, stream)
+                        : launch_prefill_d256(p, maps, dtype, num_tiles, stream);
     default: return KVQ_E_UNSUPPORTED;
   }
 }

@@ -195,6 +195,23 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t row, int head
              CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// Map of a bf16 ("auto") cache for the prefill's bulk tensor copies:
+// {head_dim values, kv heads, slots} with boxes {64, 1, 16} written in the
+// 128-byte swizzle, i.e. straight into the tensor core's operand layout.
+bool encode_auto_map(CUtensorMap* map, const void* cache, int head_dim, int heads_kv,
+                     int64_t slots) {
+  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
+  if (!enc) return false;
+  const cuuint64_t row = 2 * (cuuint64_t)head_dim;
+  const cuuint64_t dims[3] = {(cuuint64_t)head_dim, (cuuint64_t)heads_kv, (cuuint64_t)slots};
+  const cuuint64_t strides[2] = {row, row * (cuuint64_t)heads_kv};
+  const cuuint32_t box[3] = {64u, 1u, 16u};
+  const cuuint32_t estr[3] = {1u, 1u, 1u};
+  return enc(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides, box,
+             estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+             CU_TENSOR_MAP_L2_PROMOTION_L2_128B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 int sm_count() {
   int dev = 0, sms = 0;
   if (cudaGetDevice(&dev) != cudaSuccess) return 0;
@@ -659,8 +676,9 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
                                 const int32_t* seq_lens, const int32_t* block_table,
                                 int block_table_stride, int block_size, int64_t num_blocks,
                                 float sm_scale, int causal, int window, float soft_cap,
-                                float k_scale, float v_scale, void* out, void* workspace,
-                                size_t workspace_bytes, void* stream) {
+                                const float* alibi_slopes, const float* sinks, float k_scale,
+                                float v_scale, void* out, void* workspace, size_t workspace_bytes,
+                                void* stream) {
   if (!s) return KVQ_E_INVALID_ARG;
   if (heads_q != s->heads_q || heads_kv != s->heads_kv || head_dim != s->head_dim ||
       (int)dtype != s->dtype || (causal ? 1 : 0) != s->causal ||
@@ -674,7 +692,8 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   if (!q || !key_cache || !value_cache || !query_start_loc || !seq_lens || !block_table || !out)
     return KVQ_E_INVALID_ARG;
   if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
-      !aligned(out, 16) || !aligned(block_table, 4))
+      !aligned(out, 16) || !aligned(block_table, 4) || !aligned(alibi_slopes, 4) ||
+      !aligned(sinks, 4))
     return KVQ_E_INVALID_ARG;
   if (block_size <= 0 || block_size % kvq::kChunkTokens) return KVQ_E_UNSUPPORTED;
   if (num_blocks <= 0 || block_table_stride <= 0) return KVQ_E_INVALID_ARG;
@@ -723,14 +742,19 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.soft_cap = soft_cap > 0.0f ? soft_cap : 0.0f;
   p.k_scale = k_scale;
   p.v_scale = v_scale;
+  p.alibi_slopes = alibi_slopes;
+  p.sinks = sinks;
 
   kvq::PrefillMaps maps;
   std::memset(&maps, 0, sizeof(maps));
   if (!s->prefill.empty()) {
     const int64_t row = kvq::row_bytes(s->dtype, head_dim);
     const int64_t slots = num_blocks * (int64_t)block_size;
-    bool ok = encode_cache_map(&maps.k, key_cache, row, heads_kv, slots, (uint32_t)head_dim) &&
-              encode_cache_map(&maps.v, value_cache, row, heads_kv, slots, (uint32_t)head_dim);
+    bool ok = s->dtype == KVQ_AUTO
+                  ? encode_auto_map(&maps.k, key_cache, head_dim, heads_kv, slots) &&
+                        encode_auto_map(&maps.v, value_cache, head_dim, heads_kv, slots)
+                  : encode_cache_map(&maps.k, key_cache, row, heads_kv, slots, (uint32_t)head_dim) &&
+                        encode_cache_map(&maps.v, value_cache, row, heads_kv, slots, (uint32_t)head_dim);
     if (ok && kvq::is_per_token_head(s->dtype))
       ok = encode_cache_map(&maps.ks, key_cache, row, heads_kv, slots, 16u) &&
            encode_cache_map(&maps.vs, value_cache, row, heads_kv, slots, 16u);

@@ -49,10 +49,9 @@ KVQ_HD constexpr int row_bytes(int dtype, int head_dim) {
   return head_dim * kv_elem_bytes(dtype) + (is_per_token_head(dtype) ? 16 : 0);
 }
 KVQ_HD constexpr bool head_dim_supported(int d) { return d == 64 || d == 128 || d == 256; }
-// Dtypes with built attention kernels (bf16 "auto" cache: not yet).
-KVQ_HD constexpr bool attention_dtype_supported(int dtype) {
-  return dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2 || is_per_token_head(dtype);
-}
+// Dtypes with built attention kernels: all of them (the bf16 "auto" cache
+// reads its rows as they are).
+KVQ_HD constexpr bool attention_dtype_supported(int dtype) { return is_valid_dtype(dtype); }
 
 // ---- split-KV decode kernel (stream decomposition) -------------------------
 // A row tile is up to 16 packed (query token, head) rows of one kv head with
@@ -73,9 +72,12 @@ KVQ_HD constexpr int decode_chunk_bytes(int dtype, int head_dim) {
   return 2 * kChunkTokens * head_dim * kv_elem_bytes(dtype) +
          (is_per_token_head(dtype) ? 32 * 16 : 0);
 }
-// Resident CTAs per SM the kernel is compiled for (register budget).
+// Resident CTAs per SM the kernel is compiled for (register budget): a
+// bf16 ("auto") chunk is twice the bytes of a code chunk, so its register
+// lead is too.
 KVQ_HD constexpr int decode_min_ctas(int dtype, int head_dim, int ntiles) {
-  return head_dim >= 256 ? 2 : (ntiles == 1 ? 4 : 3);
+  return dtype == KVQ_AUTO ? (head_dim >= 256 ? 1 : head_dim >= 128 ? 3 : 4)
+                           : (head_dim >= 256 ? 2 : (ntiles == 1 ? 4 : 3));
 }
 // Shared memory: only each warp's ring of chunk records.
 KVQ_HD constexpr size_t decode_warp_smem(int dtype, int head_dim) {
@@ -200,6 +202,8 @@ struct AttnParams {
   int heads_q, heads_kv, group;  // group = Hq / Hkv
   int causal, window;
   float sm_scale, soft_cap, k_scale, v_scale;
+  const float* alibi_slopes;   // [Hq] or null: score += slope * (key - query position)
+  const float* sinks;          // [Hq] or null: one extra logit in the softmax normaliser
 };
 
 }  // namespace kvq
@@ -216,4 +220,6 @@ int launch_reshape_and_cache(const void* key, const void* value,
 int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream);
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
                    int64_t num_tiles, void* stream);
+// Whether a launch needs the ALiBi instances of the kernels.
+inline bool uses_alibi(const AttnParams& p) { return p.alibi_slopes != nullptr; }
 }  // namespace kvq

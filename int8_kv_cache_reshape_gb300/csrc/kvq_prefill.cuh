@@ -70,6 +70,9 @@ namespace kvq {
 
 template <int DT, int D>
 struct PrefillGeom {
+  // bf16 ("auto") rows need no conversion: the bulk copies write K and V
+  // straight into the operand tiles, and the MMAs take bf16 operands.
+  static constexpr bool kAuto = DT == KVQ_AUTO;
   static constexpr int kM = kPrefillRows;      // packed rows per tile
   static constexpr int kN = prefill_keys(D);   // keys per KV tile
   static constexpr int kThreads = prefill_threads(D);
@@ -94,7 +97,10 @@ struct PrefillGeom {
   static constexpr int kOffQScale = kOffVMax + 32 * kSide;          // kM f32: 2^-sh of each Q row
   static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
   static constexpr int kBytes = kOffBar + 256;
-  static constexpr int kOffQStage = kOffK;  // Q (kM x D f16, swizzled) staged over the K ring
+  // Q (kM x D, swizzled) is staged over the K ring -- or, for bf16 rows,
+  // whose first K tiles land in the K ring while Q is staged, over the
+  // (unused) code rings.
+  static constexpr int kOffQStage = kAuto ? kOffCodeK : kOffK;
   static constexpr int kOffOStage = kOffK;  // O (kM x D bf16) staged over the K ring at the end
   static constexpr int kColO = 0;                 // O: D fp32 columns
   static constexpr int kColS = D;                 // S buffers: kN fp32 columns each
@@ -102,6 +108,7 @@ struct PrefillGeom {
   static constexpr int kTmemCols = prefill_tmem_cols(D);
   static_assert(kColQ + D / 2 <= kTmemCols, "tensor memory: O + 2 S buffers + Q");
   static_assert(kM * D * 2 <= kStages * kTileBytes, "Q / O staging fits the K ring");
+  static_assert(!kAuto || kM * D * 2 <= 2 * kStages * kN * D, "Q staging fits the code rings");
   static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0 && kOffCodeK % 1024 == 0 &&
                     kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
                 "1024-byte operand tiles, 128-byte copy destinations");
@@ -190,7 +197,7 @@ __device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
   return h;
 }
 
-template <int DT, int D>
+template <int DT, int D, bool AL>
 __global__ void __launch_bounds__(prefill_threads(D), 1)
     prefill_attention_kernel(const AttnParams p, const __grid_constant__ PrefillMaps maps) {
   using Geo = PrefillGeom<DT, D>;
@@ -226,7 +233,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
       tc::mbar_init(bar(Geo::kBarPFull + s), 128);
     }
-    for (int s = 0; s < Geo::kSide; ++s) tc::mbar_init(bar(Geo::kBarSide + s), Geo::kConv);
+    for (int s = 0; s < Geo::kSide; ++s)
+      tc::mbar_init(bar(Geo::kBarSide + s), Geo::kAuto ? 1 : Geo::kConv);
     tc::mbar_init(bar(Geo::kBarODone), 1);
     tc::mbar_init(bar(Geo::kBarOFinal), 1);
     tc::mbar_init(bar(Geo::kBarDrain), 1);
@@ -247,6 +255,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
   float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
   uint32_t* smask = reinterpret_cast<uint32_t*>(sm + Geo::kOffSMask);
+  volatile uint32_t* smask_w = smask;  // written by the copy warp for bf16 rows
   uint32_t* vmaxw = reinterpret_cast<uint32_t*>(sm + Geo::kOffVMax);
   volatile uint32_t* chunk_valid = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffChunkValid);
   // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
@@ -295,6 +304,37 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   // indices, selected by the uniform stage) for the V group.
   int kept_slot[2][kChunks];
   uint32_t kept_valid[2] = {0u, 0u};
+  // bf16 rows ("auto"): a chunk's rows go straight into the operand tile,
+  // one {64 values, 1, 16 slots} box per 64-dim column block, which the
+  // copy writes in the 128-byte swizzle the MMAs read.  Chunks that are not
+  // copied are zeroed by the copy warp (the tile must hold no stale NaN).
+  auto zero_chunk = [&](uint32_t tile, int c) {
+    const int lane = tid & 31;
+#pragma unroll 1
+    for (int cb = 0; cb < D / 64; ++cb)
+      for (int u = lane; u < 16 * 8; u += 32)
+        sts128(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128 + u * 16), make_uint4(0, 0, 0, 0));
+  };
+  auto issue_auto = [&](uint32_t tile, const CUtensorMap* map, const int (&slot0)[kChunks],
+                        uint32_t valid, uint32_t cb_bar, bool leader) {
+    if ((valid & ((1u << kChunks) - 1u)) != ((1u << kChunks) - 1u)) {
+#pragma unroll 1
+      for (int c = 0; c < kChunks; ++c)
+        if (!((valid >> c) & 1u)) zero_chunk(tile, c);
+      tc::fence_async_smem();
+    }
+    __syncwarp();
+    if (leader) {
+      mbar_arrive_expect_tx(cb_bar, (uint32_t)__popc(valid) * 16u * D * 2u);
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c)
+        if ((valid >> c) & 1u)
+#pragma unroll
+          for (int cb = 0; cb < D / 64; ++cb)
+            tma_load_3d(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128), map, 64 * cb, t.kv_head,
+                        slot0[c], cb_bar);
+    }
+  };
   auto issue_k = [&](int j, const int (&slot0)[kChunks], uint32_t valid, bool leader) {
     const int st = j & 1;
     constexpr uint32_t kChunkBytes = 16u * D + (Geo::kPth ? 2u * 16u * 16u : 0u);
@@ -307,7 +347,13 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         kept_valid[s2] = valid;
       }
     }
-    if (leader) {
+    if constexpr (Geo::kAuto) {
+      issue_auto(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), &maps.k, slot0, valid, cb, leader);
+      // The tile's chunk mask for the softmax (side slot j % 4).
+      if (leader) smask_w[j & (Geo::kSide - 1)] = valid;
+      __syncwarp();
+      if (leader) mbar_arrive(bar(Geo::kBarSide + (j & (Geo::kSide - 1))));
+    } else if (leader) {
       chunk_valid[st] = valid;
       mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * kChunkBytes);
 #pragma unroll
@@ -336,7 +382,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         valid = kept_valid[s2];
       }
     }
-    if (leader) {
+    if constexpr (Geo::kAuto) {
+      issue_auto(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), &maps.v, slot0, valid, cb, leader);
+    } else if (leader) {
       mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * 16u * D);
 #pragma unroll
       for (int c = 0; c < kChunks; ++c) {
@@ -422,14 +470,16 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 #pragma unroll
       for (int o = kLpr / 2; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
       // largest |q| < 2^(emax - 126)
-      const int sh = emax > 0 ? min(140 - emax, 126) : 0;
+      const int sh = emax > 0 && !Geo::kAuto ? min(140 - emax, 126) : 0;
       const float up = ldexpf(1.0f, sh);
       if (m < kM) {
-        uint4 o;
-        o.x = dev::pack_f16x2(dev::bf16_lo(w[0]) * up, dev::bf16_hi(w[0]) * up);
-        o.y = dev::pack_f16x2(dev::bf16_lo(w[1]) * up, dev::bf16_hi(w[1]) * up);
-        o.z = dev::pack_f16x2(dev::bf16_lo(w[2]) * up, dev::bf16_hi(w[2]) * up);
-        o.w = dev::pack_f16x2(dev::bf16_lo(w[3]) * up, dev::bf16_hi(w[3]) * up);
+        uint4 o = qv[i];  // bf16 rows: Q enters the bf16 MMA as it is
+        if constexpr (!Geo::kAuto) {
+          o.x = dev::pack_f16x2(dev::bf16_lo(w[0]) * up, dev::bf16_hi(w[0]) * up);
+          o.y = dev::pack_f16x2(dev::bf16_lo(w[1]) * up, dev::bf16_hi(w[1]) * up);
+          o.z = dev::pack_f16x2(dev::bf16_lo(w[2]) * up, dev::bf16_hi(w[2]) * up);
+          o.w = dev::pack_f16x2(dev::bf16_lo(w[3]) * up, dev::bf16_hi(w[3]) * up);
+        }
         sts128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 8 * q_c), o);
         if (q_c == 0) qscale[m] = ldexpf(1.0f, -sh);
       }
@@ -469,8 +519,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     if (T > 0) {
       const int lane = tid & 31;
       const bool leader = elect_one();
-      constexpr uint32_t idesc_s = tc::idesc_f16(kM, kN);
-      constexpr uint32_t idesc_o = tc::idesc_f16(kM, D) | tc::kBMajorMN;
+      constexpr uint32_t idesc_s = Geo::kAuto ? tc::idesc_bf16(kM, kN) : tc::idesc_f16(kM, kN);
+      constexpr uint32_t idesc_o =
+          (Geo::kAuto ? tc::idesc_bf16(kM, D) : tc::idesc_f16(kM, D)) | tc::kBMajorMN;
       auto issue_s = [&](int j) {
         const int st = j & 1;
         // (descriptor start addresses are in 16-byte units in the low bits)
@@ -492,9 +543,21 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             tc::desc_sw128_mn(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), kN * 128, 1024);
         if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk)
-            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
-                       d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+          for (int kk = 0; kk < kN / 16; ++kk) {
+            if constexpr (Geo::kAuto) {
+              // P = hi + lo, both bf16: round c0 of the softmax wrote the hi
+              // halves of keys c0 .. c0 + 63 to columns c0 .. c0 + 31 and the
+              // lo halves to c0 + 32 .. c0 + 63.
+              const uint32_t pc = (uint32_t)(st * kN + 64 * (kk / 4) + 8 * (kk % 4));
+              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc, d0 + (uint64_t)(kk * (2048 >> 4)),
+                         idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc + 32u,
+                         d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, 1u);
+            } else {
+              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
+                         d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
+            }
+          }
           tc::mma_commit(bar(Geo::kBarODone));
           tc::mma_commit(bar(Geo::kBarVEmpty + st));
           if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
@@ -509,11 +572,14 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       int ns = 0, npv = 0;
       bool ok = true;
       long long t_idle = clock64();
+      // (bf16 rows: the copies themselves fill K and V)
+      constexpr int kBarK = Geo::kAuto ? Geo::kBarCodesK : Geo::kBarKFull;
+      constexpr int kBarV = Geo::kAuto ? Geo::kBarCodesV : Geo::kBarVFull;
       while (npv < T) {
-        uint32_t tb = bar(Geo::kBarKFull + (ns & 1)), tp = (uint32_t)((ns >> 1) & 1);
+        uint32_t tb = bar(kBarK + (ns & 1)), tp = (uint32_t)((ns >> 1) & 1);
         bool cond = ns < T && ns <= npv + 1;
         if (lane == 1 || lane == 2) {
-          tb = bar((lane == 1 ? Geo::kBarPFull : Geo::kBarVFull) + (npv & 1));
+          tb = bar((lane == 1 ? Geo::kBarPFull : kBarV) + (npv & 1));
           tp = (uint32_t)((npv >> 1) & 1);
           cond = npv < ns;
         }
@@ -559,15 +625,19 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       const bool leader = elect_one();
       bool ok = true;
       for (int i = 1; i < T; ++i) {
+        // (bf16 rows: K(j) waits for S(j - 2) to complete, V(i) for
+        // P(i - 2) V(i - 2); code rows wait for the converters.)
+        constexpr int kBarKFree = Geo::kAuto ? Geo::kBarSFull : Geo::kBarCodesKFree;
+        constexpr int kBarVFree = Geo::kAuto ? Geo::kBarVEmpty : Geo::kBarCodesVFree;
         if (i + 1 < T) {
           const int j = i + 1;
-          ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesKFree + (j & 1)),
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarKFree + (j & 1)),
                                                       (uint32_t)(((j >> 1) - 1) & 1), abort_flag));
           if (!ok) break;
           issue_next_k(leader);
         }
         if (i >= 2) {
-          ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesVFree + (i & 1)),
+          ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarVFree + (i & 1)),
                                                       (uint32_t)(((i >> 1) - 1) & 1), abort_flag));
           if (!ok) break;
           issue_v(i, leader);
@@ -585,6 +655,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     }
     __syncwarp();
   } else if (is_conv) {
+    if constexpr (!Geo::kAuto) {
     // ======================= converters ========================================
     // A unit is (key n, 16 codes pc): consecutive threads take consecutive
     // 16-byte pieces of a code row (conflict-free reads).  The two 16-byte f16
@@ -690,6 +761,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       valid_v = valid_k;
       whole_v = whole_k;
     }
+    }
     __syncwarp();
   } else {
     // ======================= softmax ===========================================
@@ -707,8 +779,11 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     const float cap = p.soft_cap;
     // scores in log2 units (natural units under a soft cap, which converts)
     const float q_unscale = reinterpret_cast<const float*>(sm + Geo::kOffQScale)[m];  // 2^-sh
-    const float score_mul =
-        p.sm_scale * q_unscale * (cap > 0.0f ? 1.0f : log2e) * (Geo::kPth ? 1.0f : p.k_scale);
+    const float score_mul = p.sm_scale * q_unscale * (cap > 0.0f ? 1.0f : log2e) *
+                            (Geo::kPth || Geo::kAuto ? 1.0f : p.k_scale);
+    // ALiBi: this row's slope in log2 units (the bias uses the exact integer
+    // distance key - position, added after the soft cap).
+    const float al_slope = AL ? p.alibi_slopes[t.kv_head * G + R % G] * log2e : 0.0f;
     const float cap_l2 = cap * log2e;
     const float inv_cap = cap > 0.0f ? 1.0f / cap : 0.0f;
     // m_ref: the reference maximum, an integer (log2 units) once set, so
@@ -760,11 +835,14 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         else
           return r * score_mul;
       };
-      // 64 scores from column c0: r in place, the row's maximum of r.
+      // 64 scores from column c0: r in place, the row's maximum of r.  With
+      // ALiBi the bias differs per key, so the final scores (log2 units) are
+      // stored and maximised instead.
       auto raw64 = [&](auto full_c, uint32_t* v, int c0) -> float {
         const float* skp = sk + sd * kN + c0;
         const int lo = lo_n - c0, hi = hi_n - c0;
         const uint32_t cm = cmask >> (c0 >> 4);
+        const int dist0 = kv0 + c0 - pos;  // key - position of column c0
         float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
 #pragma unroll
         for (int e = 0; e < 64; e += 2) {
@@ -773,6 +851,17 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             const float2 k2 = *reinterpret_cast<const float2*>(skp + e);
             r0 *= k2.x;
             r1 *= k2.y;
+          }
+          if constexpr (AL) {
+            if (cap > 0.0f) {
+              r0 = cap_l2 * dev::tanh_exp(r0 * score_mul * inv_cap);
+              r1 = cap_l2 * dev::tanh_exp(r1 * score_mul * inv_cap);
+            } else {
+              r0 *= score_mul;
+              r1 *= score_mul;
+            }
+            r0 = fmaf(al_slope, (float)(dist0 + e), r0);
+            r1 = fmaf(al_slope, (float)(dist0 + e + 1), r1);
           }
           if constexpr (!decltype(full_c)::value) {
             const bool in = (cm >> (e >> 4)) & 1u;
@@ -795,7 +884,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         for (int e = 0; e < 64; e += 2) {
           const float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
           float p0, p1;
-          if constexpr (decltype(cap_c)::value) {
+          if constexpr (AL) {  // v holds the final scores
+            p0 = dev::fast_exp2(r0 - ref);
+            p1 = dev::fast_exp2(r1 - ref);
+          } else if constexpr (decltype(cap_c)::value) {
             p0 = dev::fast_exp2(score(cap_c, r0) - ref);
             p1 = dev::fast_exp2(score(cap_c, r1) - ref);
           } else {
@@ -809,7 +901,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             p0 *= v2.x * v_mul;
             p1 *= v2.y * v_mul;
           }
-          pw[e / 2] = dev::pack_f16x2(p0, p1);
+          if constexpr (Geo::kAuto) {
+            // bf16 MMA: P = hi + lo, both bf16 (16 significant bits); hi in
+            // pw[0 .. 31], lo in pw[32 .. 63].
+            const uint32_t h = dev::pack_bf16x2(p0, p1);
+            pw[e / 2] = h;
+            pw[32 + e / 2] = dev::pack_bf16x2(p0 - dev::bf16_lo(h), p1 - dev::bf16_hi(h));
+          } else {
+            pw[e / 2] = dev::pack_f16x2(p0, p1);
+          }
         }
         lsum_tile += ls0 + ls1;
       };
@@ -826,8 +926,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         tc::tmem_ld32(tmem_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
         tc::tmem_wait_ld();
         const float mr = full ? raw64(std::true_type{}, v, c0) : raw64(std::false_type{}, v, c0);
-        // the score is monotonic in r (score_mul > 0, tanh increasing)
-        const float mx = cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
+        // the score is monotonic in r (score_mul > 0, tanh increasing); with
+        // ALiBi mr is the largest final score already
+        const float mx = AL ? mr : cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
         float a = 1.0f;
         if (mx > m_ref + 8.0f) {
           const float nref = ceilf(mx);
@@ -838,26 +939,35 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           lsum_tile *= a;
         }
         const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
-        uint32_t pw[32];
+        constexpr int kPw = Geo::kAuto ? 64 : 32;  // P words of the round (bf16: hi and lo)
+        uint32_t pw[kPw];
         if (cap > 0.0f)
           weights64(std::true_type{}, v, c0, ref, pw);
         else
           weights64(std::false_type{}, v, c0, ref, pw);
-        tc::tmem_st16(tmem_s + c0 / 2, *reinterpret_cast<uint32_t(*)[16]>(pw));
-        tc::tmem_st16(tmem_s + c0 / 2 + 16, *reinterpret_cast<uint32_t(*)[16]>(pw + 16));
+        // f16 P of the round goes to columns c0 / 2 .. c0 / 2 + 31; bf16 hi
+        // and lo halves to c0 .. c0 + 63 (the columns this round read).
+        const int pcol = Geo::kAuto ? c0 : c0 / 2;
+#pragma unroll
+        for (int h = 0; h < kPw; h += 16)
+          tc::tmem_st16(tmem_s + pcol + h, *reinterpret_cast<uint32_t(*)[16]>(pw + h));
         if (c0 > 0 && __any_sync(0xffffffffu, a != 1.0f)) {
-          // Weights of the earlier rounds (columns [0, c0 / 2)) against the
-          // new reference: a power-of-two scaling, exact unless subnormal.
+          // Weights of the earlier rounds against the new reference: a
+          // power-of-two scaling, exact unless subnormal.
           tc::tmem_wait_st();
 #pragma unroll 1
-          for (int c = 0; c < c0 / 2; c += 32) {
+          for (int c = 0; c < pcol; c += 32) {
             uint32_t w[32];
             tc::tmem_ld32(tmem_s + c, w);
             tc::tmem_wait_ld();
 #pragma unroll
             for (int e = 0; e < 32; ++e) {
-              const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-              w[e] = dev::pack_f16x2(f.x * a, f.y * a);
+              if constexpr (Geo::kAuto) {
+                w[e] = dev::pack_bf16x2(dev::bf16_lo(w[e]) * a, dev::bf16_hi(w[e]) * a);
+              } else {
+                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                w[e] = dev::pack_f16x2(f.x * a, f.y * a);
+              }
             }
             tc::tmem_st32(tmem_s + c, w);
           }
@@ -897,8 +1007,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       const uint32_t orow = base + Geo::kOffOStage + (uint32_t)(m * D * 2);
       if (T > 0) {
         tc::fence_after_sync();
+        // An attention sink joins the normaliser (the weights carry
+        // 2^-(m_ref - 6)).
+        if (p.sinks && row_valid && m_ref != -INFINITY) {
+          const float sk = p.sinks[t.kv_head * G + R % G] * log2e;
+          if (sk != -INFINITY) l_sum += exp2f(fminf(sk - m_ref + 6.0f, 126.0f));
+        }
         const float sc = (l_sum > 0.0f ? 1.0f / l_sum : 0.0f) *
-                         (Geo::kPth ? (ev > -1000 ? ldexpf(1.0f, ev) : 0.0f) : p.v_scale);
+                         (Geo::kPth ? (ev > -1000 ? ldexpf(1.0f, ev) : 0.0f)
+                                    : Geo::kAuto ? 1.0f : p.v_scale);
 #pragma unroll 1
         for (int c0 = 0; c0 < D; c0 += 32) {
           uint32_t v[32];
@@ -952,11 +1069,11 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   }
 }
 
-template <int DT, int D>
+template <int DT, int D, bool AL>
 int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_t num_tiles,
                             cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes(D);
-  auto kern = prefill_attention_kernel<DT, D>;
+  auto kern = prefill_attention_kernel<DT, D, AL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
@@ -964,18 +1081,21 @@ int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 
-template <int D>
+// The instances of one head_dim and one ALiBi setting (one translation unit
+// each keeps the build parallel).
+template <int D, bool AL>
 int launch_prefill_d(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
                      cudaStream_t stream) {
   switch (dtype) {
-    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D>(p, maps, num_tiles, stream);
-    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D>(p, maps, num_tiles, stream);
+    case KVQ_AUTO: return launch_prefill_instance<KVQ_AUTO, D, AL>(p, maps, num_tiles, stream);
+    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D, AL>(p, maps, num_tiles, stream);
+    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D, AL>(p, maps, num_tiles, stream);
     case KVQ_INT8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
     case KVQ_FP8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
     case KVQ_FP8_E5M2_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_FP8_E5M2_PER_TOKEN_HEAD, D>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_FP8_E5M2_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
     default:
       return KVQ_E_UNSUPPORTED;
   }

@@ -1,0 +1,11 @@
+// kvq_prefill_d128_alibi.cu -- tensor-core prefill kernels for head_dim 128, with the ALiBi bias (one
+// translation unit per head_dim and ALiBi setting keeps the build parallel).
+#include "kvq_prefill.cuh"
+
+namespace kvq {
+int launch_prefill_d128_alibi(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+                              void* stream) {
+  return launch_prefill_d<128, true>(p, maps, dtype, num_tiles,
+                                       static_cast<cudaStream_t>(stream));
+}
+}  // namespace kvq

@@ -50,7 +50,8 @@ extern "C" int kvq_attention_with_kv_cache_static_scratch(
     const void* q, const void* key_cache, const void* value_cache,
     const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,
     int block_table_stride, int block_size, int64_t num_blocks, float sm_scale, int causal,
-    int window, float soft_cap, float k_scale, float v_scale, void* out, void* stream) {
+    int window, float soft_cap, const float* alibi_slopes, const float* sinks, float k_scale,
+    float v_scale, void* out, void* stream) {
   if (!sched) return KVQ_E_INVALID_ARG;
   kvq_sched_info_t info;
   int rc = kvq_sched_get_info(sched, &info);
@@ -62,6 +63,7 @@ extern "C" int kvq_attention_with_kv_cache_static_scratch(
   return kvq_attention_with_kv_cache(sched, heads_q, heads_kv, head_dim, dtype, q, key_cache,
                                      value_cache, query_start_loc, seq_lens, block_table,
                                      block_table_stride, block_size, num_blocks, sm_scale,
-                                     causal, window, soft_cap, k_scale, v_scale, out, scratch,
+                                     causal, window, soft_cap, alibi_slopes, sinks, k_scale,
+                                     v_scale, out, scratch,
                                      (size_t)KVQ_STATIC_SCRATCH_BYTES, stream);
 }

@@ -83,12 +83,12 @@ lib.kvq_attention_with_kv_cache.restype = _c.c_int
 lib.kvq_attention_with_kv_cache.argtypes = [
     _p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _p, _p, _p, _p,
     _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
-    _c.c_float, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
+    _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
 lib.kvq_attention_with_kv_cache_static_scratch.restype = _c.c_int
 lib.kvq_attention_with_kv_cache_static_scratch.argtypes = [
     _p, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _p, _p, _p, _p,
     _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
-    _c.c_float, _c.c_float, _c.c_float, _p, _p]
+    _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p]
 STATIC_SCRATCH_BYTES = 16 << 20
 lib.kvq_sched_destroy.restype = None
 lib.kvq_sched_destroy.argtypes = [_p]
@@ -236,10 +236,11 @@ def attention_with_kv_cache(sched: Sched, q, key_cache, value_cache, query_start
                             seq_lens, block_table, sm_scale: float, causal: bool,
                             window: int, soft_cap: float, k_scale: float, v_scale: float,
                             out, workspace, kv_cache_dtype, heads_kv: int, stream=None,
-                            num_blocks=None) -> None:
+                            num_blocks=None, alibi_slopes=None, sinks=None) -> None:
     """q / out: bf16 [sum Q, Hq, D]; caches uint8 [NB, B, Hkv, row];
     block_table int32 [R, max_blocks]; query_start_loc / seq_lens device
-    int32; workspace: a uint8 device tensor of >= sched.workspace_bytes."""
+    int32; workspace: a uint8 device tensor of >= sched.workspace_bytes;
+    alibi_slopes / sinks: device float32 [Hq] or None."""
     dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
     _, Hq, D = q.shape
     nb = key_cache.shape[0] if num_blocks is None else num_blocks
@@ -248,8 +249,8 @@ def attention_with_kv_cache(sched: Sched, q, key_cache, value_cache, query_start
         sched.handle, Hq, heads_kv, D, dt, _ptr(q), _ptr(key_cache), _ptr(value_cache),
         _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), block_table.stride(0),
         key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
-        float(soft_cap), float(k_scale), float(v_scale), _ptr(out), _ptr(workspace),
-        ws_bytes, _stream(stream)), "kvq_attention_with_kv_cache")
+        float(soft_cap), _ptr(alibi_slopes), _ptr(sinks), float(k_scale), float(v_scale),
+        _ptr(out), _ptr(workspace), ws_bytes, _stream(stream)), "kvq_attention_with_kv_cache")
 
 
 def attention_with_kv_cache_static_scratch(sched: Sched, q, key_cache, value_cache,
@@ -257,7 +258,8 @@ def attention_with_kv_cache_static_scratch(sched: Sched, q, key_cache, value_cac
                                            sm_scale: float, causal: bool, window: int,
                                            soft_cap: float, k_scale: float, v_scale: float,
                                            out, kv_cache_dtype, heads_kv: int, stream=None,
-                                           num_blocks=None) -> None:
+                                           num_blocks=None, alibi_slopes=None,
+                                           sinks=None) -> None:
     """attention_with_kv_cache without a workspace argument: the library's
     fixed device scratch (STATIC_SCRATCH_BYTES) holds the split partials.
     For callers that cannot allocate device memory; calls must not overlap
@@ -269,5 +271,5 @@ def attention_with_kv_cache_static_scratch(sched: Sched, q, key_cache, value_cac
         sched.handle, Hq, heads_kv, D, dt, _ptr(q), _ptr(key_cache), _ptr(value_cache),
         _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table), block_table.stride(0),
         key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
-        float(soft_cap), float(k_scale), float(v_scale), _ptr(out), _stream(stream)),
-        "kvq_attention_with_kv_cache_static_scratch")
+        float(soft_cap), _ptr(alibi_slopes), _ptr(sinks), float(k_scale), float(v_scale),
+        _ptr(out), _stream(stream)), "kvq_attention_with_kv_cache_static_scratch")

@@ -77,10 +77,14 @@ class Guarded:
 class GpuRun:
     """Device tensors and results of one workload run through the library."""
 
-    def __init__(self, wl, device="cuda:0", write_mask=None):
+    def __init__(self, wl, device="cuda:0", write_mask=None, alibi_slopes=None, sinks=None):
         self.wl = wl
         dev = torch.device(device)
         self.dev = dev
+        # optional ALiBi slopes / sink logits (float32 [Hq] numpy arrays)
+        self.alibi_np, self.sinks_np = alibi_slopes, sinks
+        self.alibi = None if alibi_slopes is None else torch.from_numpy(alibi_slopes).to(dev)
+        self.sinks = None if sinks is None else torch.from_numpy(sinks).to(dev)
         self.key = wl.key.to(dev)
         self.value = wl.value.to(dev)
         slots = wl.slot_mapping.clone()
@@ -114,7 +118,8 @@ class GpuRun:
         ws = Guarded((max(sched.workspace_bytes, 1),), torch.uint8, 0, self.q.device)
         k.attention_with_kv_cache(sched, self.q, self.kc, self.vc, self.qsl, self.sl, self.bt,
                                   wl.sm_scale, wl.causal, wl.window, wl.soft_cap, wl.k_scale,
-                                  wl.v_scale, self.out, ws.t, wl.kv_cache_dtype, wl.heads_kv)
+                                  wl.v_scale, self.out, ws.t, wl.kv_cache_dtype, wl.heads_kv,
+                                  alibi_slopes=self.alibi, sinks=self.sinks)
         torch.cuda.synchronize()
         sched.check_device()   # no kernel gave up a bounded wait
         ws.check("workspace")
@@ -149,15 +154,16 @@ def _oracle_args(wl, kc, vc):
             wl.window, wl.soft_cap, wl.k_scale, wl.v_scale)
 
 
-def oracle_attention(wl, kc, vc, tokens=None):
-    return oracle.attention(*_oracle_args(wl, kc, vc), tokens=tokens)
+def oracle_attention(wl, kc, vc, tokens=None, alibi_slopes=None, sinks=None):
+    return oracle.attention(*_oracle_args(wl, kc, vc), tokens=tokens, alibi_slopes=alibi_slopes,
+                            sinks=sinks)
 
 
-def oracle_reference(wl, kc, vc, tokens=None):
+def oracle_reference(wl, kc, vc, tokens=None, alibi_slopes=None, sinks=None):
     """(oracle output, binary32 evaluation bound) for the listed tokens."""
     args = _oracle_args(wl, kc, vc)
-    return (oracle.attention(*args, tokens=tokens),
-            oracle.attention_fp32_bound(*args, tokens=tokens))
+    kw = dict(tokens=tokens, alibi_slopes=alibi_slopes, sinks=sinks)
+    return (oracle.attention(*args, **kw), oracle.attention_fp32_bound(*args, **kw))
 
 
 def bf16_ulp(x: np.ndarray) -> np.ndarray:

@@ -168,7 +168,7 @@ def test_prefill_tiles_and_decode_boundary():
 
 @pytest.mark.parametrize("kw,want", [
     (dict(hq=30, hkv=8), kvq.E_UNSUPPORTED), (dict(D=96), kvq.E_UNSUPPORTED),
-    (dict(dtype="auto"), kvq.E_UNSUPPORTED), (dict(causal=False, window=8), kvq.E_INVALID_ARG),
+    (dict(causal=False, window=8), kvq.E_INVALID_ARG),
 ])
 def test_scheduler_rejects(kw, want):
     with pytest.raises(kvq.KvqError) as e:
@@ -194,7 +194,7 @@ def test_attention_refuses_mismatched_schedule():
     f = kvq.lib.kvq_attention_with_kv_cache
     args = lambda hq, hkv, D, dt, causal=1, window=0: (
         s.handle, hq, hkv, D, dt, *([ctypes.c_void_p(256)] * 6), 4, 16, 8, 0.1, causal,
-        window, 0.0, 1.0, 1.0, ctypes.c_void_p(256), None, 0, None)
+        window, 0.0, None, None, 1.0, 1.0, ctypes.c_void_p(256), None, 0, None)
     assert f(*args(32, 8, 128, 3)) == kvq.E_SCHED_MISMATCH     # other dtype
     assert f(*args(32, 8, 64, 1)) == kvq.E_SCHED_MISMATCH      # other head_dim
     assert f(*args(16, 8, 128, 1)) == kvq.E_SCHED_MISMATCH     # other heads
