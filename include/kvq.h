@@ -260,6 +260,75 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
     int window, float soft_cap, const float* alibi_slopes, const float* sinks, float k_scale,
     float v_scale, void* out, void* stream);
 
+/* decode_step -- one serving step of a decode batch in ONE kernel launch:
+ * the step's new K/V rows are quantised into the caches (exactly as
+ * kvq_reshape_and_cache), the work plan is built on the device from the
+ * device's query_start_loc / seq_lens (no host scheduler, no host copy of
+ * the lengths), and causal split-KV attention runs over the caches (exactly
+ * as kvq_attention_with_kv_cache).  [P2] Key source snippet
+ * (get_scheduler_metadata feeding the attention, enable_kv_split) and
+ * Breakdown item 1 (the schedule sized from the KV element size); [P1]
+ * Breakdown items 1-3 (reshape_and_cache, then the attention).  Because
+ * nothing of the plan lives on the host, a step captured in a CUDA graph
+ * replays correctly with other lengths, new tokens and block tables, within
+ * the capacities its workspace was sized for.
+ *
+ *   num_req, heads_q, heads_kv, head_dim, dtype   as for the other calls.
+ *   key, value, num_new_tokens, key_stride_tok, value_stride_tok,
+ *   slot_mapping            the step's new rows, as for kvq_reshape_and_cache
+ *                           (num_new_tokens may be 0).
+ *   key_cache, value_cache, num_blocks, block_size   the paged caches.
+ *   q, query_start_loc,     as for kvq_attention_with_kv_cache (device);
+ *   seq_lens, block_table,  every request must have 1 <= Q <= max_query_len
+ *   block_table_stride      queries (Q = 0: skipped) and Q <= L; its table
+ *                           row holds ceil(L / block_size) entries (entries
+ *                           beyond block_table_stride, or outside the pool,
+ *                           read as masked keys).
+ *   max_query_len           host bound on Q; max_query_len * heads_q /
+ *                           heads_kv must be <= 16 (decode rows), else
+ *                           KVQ_E_UNSUPPORTED.  A request whose device Q
+ *                           breaks the bound is skipped and flags the error
+ *                           word (kvq_decode_step_check: KVQ_E_INVALID_ARG).
+ *   sm_scale, window, soft_cap, alibi_slopes, sinks, k_scale, v_scale
+ *                           as for kvq_attention_with_kv_cache (causal).
+ *   out                     device bf16 [sum Q, heads_q, head_dim].
+ *   workspace               device scratch of >= the size
+ *                           kvq_decode_step_workspace_size gives for the
+ *                           same num_req, shape, dtype, max_query_len and
+ *                           ALiBi setting, 256-byte aligned, ZERO-FILLED
+ *                           before its first use (e.g. cudaMemsetAsync);
+ *                           every call leaves it ready for the next.  Calls
+ *                           sharing a workspace must be ordered on one stream.
+ * The kernel is a cooperative launch (all its CTAs resident at once, one
+ * grid-wide barrier between the cache write and the attention); the barrier
+ * wait is bounded (about a second) and a timeout flags the error word
+ * (kvq_decode_step_check: KVQ_E_TIMEOUT).  Allocates nothing. */
+KVQ_API int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim,
+                            kvq_dtype_t dtype, const void* key, const void* value,
+                            int64_t num_new_tokens, int64_t key_stride_tok,
+                            int64_t value_stride_tok, const int64_t* slot_mapping,
+                            void* key_cache, void* value_cache, int64_t num_blocks,
+                            int block_size, const void* q, const int32_t* query_start_loc,
+                            const int32_t* seq_lens, const int32_t* block_table,
+                            int block_table_stride, int max_query_len, float sm_scale,
+                            int window, float soft_cap, const float* alibi_slopes,
+                            const float* sinks, float k_scale, float v_scale, void* out,
+                            void* workspace, size_t workspace_bytes, void* stream);
+
+/* Workspace bytes of kvq_decode_step for these arguments on the current
+ * device ([P2] Breakdown item 1: scratch sized from the KV element size and
+ * the tile geometry).  use_alibi: whether alibi_slopes will be non-NULL.
+ * Errors as kvq_decode_step's shape checks. */
+KVQ_API int kvq_decode_step_workspace_size(int num_req, int heads_q, int heads_kv, int head_dim,
+                                           kvq_dtype_t dtype, int max_query_len, int use_alibi,
+                                           size_t* workspace_bytes);
+
+/* No counterpart on the pages.  Read, and clear, a decode_step workspace's
+ * error word: KVQ_E_TIMEOUT (the grid barrier gave up), KVQ_E_INVALID_ARG
+ * (a request's device lengths broke the bounds) or KVQ_OK.  Blocks until
+ * the device is idle. */
+KVQ_API int kvq_decode_step_check(const void* workspace);
+
 /* Free a schedule (NULL is a no-op).  No counterpart on the pages (their
  * schedule is a torch tensor that the garbage collector frees); it is the
  * C ABI's ownership rule for the object get_scheduler_metadata returns.

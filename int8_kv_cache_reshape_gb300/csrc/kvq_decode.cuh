@@ -45,6 +45,7 @@
 
 #include <cuda_runtime.h>
 
+#include "kvq_cache_row.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
 
@@ -90,13 +91,15 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
 // 16 splits the rows are merged side by side -- lpr lanes per row, each with
 // a run of D / lpr dims -- and every split's partial of a 4-dim step is
 // loaded at once.
-template <int D>
-__device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeItem& m, int lane) {
+// `base(s)` is the partial row of split s's row 0 (its row n at base(s) + n).
+template <int D, class Base>
+__device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeItem& m, int lane,
+                                             Base base) {
   constexpr int kMaxSplits = 16;
   const int G = p.group;
   const int q0 = p.query_start_loc[m.req];
   const int ns = m.nsplits, nr = m.nrows;
-  const float* lse = p.part_lse + m.part;
+  const float* lse = p.part_lse;
   auto out_row = [&](int n) {
     const int R = m.row0 + n;
     return p.out + ((int64_t)(q0 + R / G) * p.heads_q + m.kv_head * G + R % G) * D;
@@ -111,7 +114,7 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
     float M = -INFINITY;
 #pragma unroll
     for (int s = 0; s < kMaxSplits; ++s) {
-      w[s] = active && s < ns ? __ldcg(lse + s * nr + n) : -INFINITY;
+      w[s] = active && s < ns ? __ldcg(lse + base(s) + n) : -INFINITY;
       M = fmaxf(M, w[s]);
     }
     // An attention sink is one more term of the normaliser (no value).  The
@@ -129,13 +132,16 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
     }
     const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
     if (!active) return;
-    const float* src = p.part_o + (int64_t)(m.part + n) * D + sub * per;  // split s: + s * nr * D
+    int64_t row_off[kMaxSplits];  // split s's partial row n, in floats
+#pragma unroll
+    for (int s = 0; s < kMaxSplits; ++s)
+      row_off[s] = s < ns ? (int64_t)(base(s) + n) * D + sub * per : 0;
     uint16_t* dst = out_row(n) + sub * per;
     for (int d0 = 0; d0 < per; d0 += 4) {
       float4 v[kMaxSplits];
 #pragma unroll
       for (int s = 0; s < kMaxSplits; ++s)
-        v[s] = s < ns ? __ldcg(reinterpret_cast<const float4*>(src + (int64_t)s * nr * D + d0))
+        v[s] = s < ns ? __ldcg(reinterpret_cast<const float4*>(p.part_o + row_off[s] + d0))
                       : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
       float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
 #pragma unroll
@@ -154,7 +160,7 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
   constexpr int kPer = D / 32;
   for (int n = 0; n < nr; ++n) {
     float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + s * nr + n));
+    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + base(s) + n));
 #pragma unroll
     for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float sink =  // (log2 units, with the pieces' 2^6 lift)
@@ -166,10 +172,10 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
     for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
     float wsum = sink == -INFINITY ? 0.0f : exp2f(sink - M);
     for (int s = 0; s < ns; ++s) {
-      const float l = __ldcg(lse + s * nr + n);
+      const float l = __ldcg(lse + base(s) + n);
       const float w = (l == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l - M);
       wsum += w;
-      const float* src = p.part_o + (int64_t)(m.part + s * nr + n) * D + lane * kPer;
+      const float* src = p.part_o + (int64_t)(base(s) + n) * D + lane * kPer;
 #pragma unroll
       for (int e = 0; e < kPer; e += 2) {
         const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
@@ -185,9 +191,93 @@ __device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeIte
   }
 }
 
-template <int DT, int D, int NT, bool AL>
+// ---- fused decode step: the plan built on the device ----------------------
+// One row tile per (request, kv head): its first 16-token chunk, the keys
+// some of its rows see and its rows; the tiles' chunk counts are
+// prefix-summed by the kernel's first CTA (kDecodeThreads threads), which
+// also zeroes the merge counters.  A request with more rows than the launch
+// was built for (or more queries than keys) is left out and flags the error
+// word.
+__device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams& sp) {
+  __shared__ int32_t warp_sums[kDecodeWarps];
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  const int nt = sp.num_tiles;
+  const int per = (nt + kDecodeThreads - 1) / kDecodeThreads;
+  const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
+  auto chunks_of = [&](int t, bool store) {
+    const int r = t / p.heads_kv;
+    const int Q = p.query_start_loc[r + 1] - p.query_start_loc[r];
+    const int L = p.seq_lens[r];
+    const int rows = Q * p.group;
+    if (Q <= 0 || L < Q || rows > sp.max_rows) {
+      if (store) {
+        if (Q != 0) atomicExch(p.error_flag, 2);  // (1 is the barrier's timeout)
+        sp.tiles[t] = make_int4(0, 0, 0, 0);
+      }
+      return 0;
+    }
+    const int lo = p.window > 0 ? max(0, L - Q - p.window + 1) : 0;
+    if (store) sp.tiles[t] = make_int4(lo / kChunkTokens, lo, L, rows);
+    return (L + kChunkTokens - 1) / kChunkTokens - lo / kChunkTokens;
+  };
+  int local = 0;
+  for (int t = t0; t < t1; ++t) local += chunks_of(t, true);
+  // exclusive scan of the threads' sums
+  int incl = local;
+#pragma unroll
+  for (int off = 1; off < 32; off <<= 1) {
+    const int v = __shfl_up_sync(0xffffffffu, incl, off);
+    if (lane >= off) incl += v;
+  }
+  if (lane == 31) warp_sums[warp] = incl;
+  __syncthreads();
+  int run = incl - local;
+  for (int w = 0; w < warp; ++w) run += warp_sums[w];
+  for (int t = t0; t < t1; ++t) {
+    sp.prefix[t] = run;
+    run += chunks_of(t, false);
+  }
+  if (tid == kDecodeThreads - 1) sp.prefix[nt] = run;
+  for (int t = tid; t < nt; t += kDecodeThreads) p.merge_counters[t] = 0;
+}
+
+// Grid-wide barrier of a cooperative launch (every CTA resident): arrival
+// count and generation in global memory; the last CTA to arrive resets the
+// count and advances the generation.  Bounded: a CTA that waits about a
+// second flags the error word and the call gives up.
+__device__ __forceinline__ bool grid_barrier(uint32_t* bar, int32_t* error_flag) {
+  __syncthreads();
+  int ok = 1;
+  if (threadIdx.x == 0) {
+    volatile uint32_t* gen = bar + 1;
+    const uint32_t g0 = *gen;
+    __threadfence();
+    const uint32_t prev = atomicAdd(bar, 1u);
+    if (prev == gridDim.x - 1) {
+      atomicExch(bar, 0u);
+      __threadfence();
+      atomicAdd(bar + 1, 1u);
+    } else {
+      const long long t0 = clock64();
+      while (*gen == g0) {
+        if (clock64() - t0 > 2000000000LL) {  // about a second
+          ok = 0;
+          atomicExch(error_flag, 1);
+          break;
+        }
+      }
+    }
+    __threadfence();
+  }
+  return __syncthreads_and(ok) != 0;
+}
+
+// DEV: the fused decode step -- the new tokens are written to the caches,
+// the plan is built from the device's lengths, and a grid barrier separates
+// both from the attention (which then reads the caches with coherent loads).
+template <int DT, int D, int NT, bool AL, bool DEV>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_ctas(DT, D, NT))
-splitkv_decode_kernel(const AttnParams p) {
+splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   using Geo = DecodeGeom<DT, D>;
   extern __shared__ __align__(128) uint8_t smem[];
   const int lane = threadIdx.x & 31;
@@ -195,12 +285,32 @@ splitkv_decode_kernel(const AttnParams p) {
   const int g = lane >> 2;
   const int c = lane & 3;
 
+  // ---- the fused step's prologue -------------------------------------------
+  int64_t total_chunks = p.num_chunks;
+  int64_t total_warps = p.num_warps;
+  if constexpr (DEV) {
+    row::write_rows<DT, D>(sp.key, sp.value, sp.num_tokens, sp.key_stride, sp.value_stride,
+                           p.heads_kv, sp.key_cache, sp.value_cache, sp.num_slots,
+                           sp.slot_mapping, p.k_scale, p.v_scale, kDecodeThreads, threadIdx.x,
+                           blockIdx.x, gridDim.x);
+    if (blockIdx.x == 0) plan_step(p, sp);
+    if (!grid_barrier(sp.barrier, p.error_flag)) return;
+    total_chunks = __ldcg(sp.prefix + sp.num_tiles);
+    total_warps = (int64_t)gridDim.x * kDecodeWarps;
+  }
+  auto load16 = [&](const void* a) {
+    if constexpr (DEV) return dev::ldg_stream_coherent(a);
+    else return dev::ldg_stream(a);
+  };
+
   // ---- this warp's segment of the flat chunk sequence -------------------
   const int gw = blockIdx.x * kDecodeWarps + warp;
-  const int64_t seg0 = (int64_t)gw * p.num_chunks / p.num_warps;
-  const int n = (int)((int64_t)(gw + 1) * p.num_chunks / p.num_warps - seg0);
+  const int64_t seg0 = (int64_t)gw * total_chunks / total_warps;
+  const int n = (int)((int64_t)(gw + 1) * total_chunks / total_warps - seg0);
   // The piece of each position: the warp's first piece comes from the
   // schedule; a lane's cursor only moves forward as its positions grow.
+  // (Fused step: the pieces are the tiles themselves -- the part of a tile
+  // inside this warp's segment -- found in the device-built prefix.)
   uint4* records = reinterpret_cast<uint4*>(smem + warp * Geo::kWarpSmem);
 
   const uint8_t* kbase = p.key_cache;
@@ -226,28 +336,55 @@ splitkv_decode_kernel(const AttnParams p) {
   // that the dependent loads (chunk ref -> piece -> block table) overlap
   // with the streaming.
   int f_piece = -1, f_chunk = 0;
-  int cur_piece = n > 0 ? p.warp_piece[gw] : 0;
+  int cur_piece = 0;
+  if constexpr (DEV) {
+    if (n > 0) {  // the tile holding position seg0: the first with prefix[t + 1] > seg0
+      int lo = 0, hi = sp.num_tiles - 1;
+      while (lo < hi) {
+        const int mid = (lo + hi) >> 1;
+        if (__ldcg(sp.prefix + mid + 1) > seg0) hi = mid;
+        else lo = mid + 1;
+      }
+      cur_piece = lo;
+    }
+  } else {
+    cur_piece = n > 0 ? p.warp_piece[gw] : 0;
+  }
   int4 f_pc = make_int4(0, 0, 0, 0);  // req, kv_head, any_lo, any_hi
   int f_blk = -1;
   auto fill_load_ref = [&](int pos) {
     f_piece = -1;
     if (lane < 16 && pos + lane < n) {
       const int64_t flat = seg0 + pos + lane;
-      while (cur_piece + 1 < p.num_pieces && (int64_t)__ldg(&p.pieces[cur_piece + 1].flat0) <= flat)
-        ++cur_piece;
-      f_piece = cur_piece;
-      f_chunk = __ldg(&p.pieces[cur_piece].chunk0) + (int)(flat - __ldg(&p.pieces[cur_piece].flat0));
+      if constexpr (DEV) {
+        while (cur_piece + 1 < sp.num_tiles && (int64_t)__ldcg(sp.prefix + cur_piece + 1) <= flat)
+          ++cur_piece;
+        f_piece = cur_piece;
+        f_chunk = __ldcg(&sp.tiles[cur_piece].x) + (int)(flat - __ldcg(sp.prefix + cur_piece));
+      } else {
+        while (cur_piece + 1 < p.num_pieces &&
+               (int64_t)__ldg(&p.pieces[cur_piece + 1].flat0) <= flat)
+          ++cur_piece;
+        f_piece = cur_piece;
+        f_chunk = __ldg(&p.pieces[cur_piece].chunk0) + (int)(flat - __ldg(&p.pieces[cur_piece].flat0));
+      }
     }
   };
   auto fill_load_piece = [&]() {
     if (f_piece >= 0) {
-      const DecodePiece* pc = p.pieces + f_piece;
-      f_pc = make_int4(pc->req, pc->kv_head, pc->any_lo, pc->any_hi);
+      if constexpr (DEV) {
+        const int4 ti = __ldcg(sp.tiles + f_piece);
+        f_pc = make_int4(f_piece / p.heads_kv, f_piece % p.heads_kv, ti.y, ti.z);
+      } else {
+        const DecodePiece* pc = p.pieces + f_piece;
+        f_pc = make_int4(pc->req, pc->kv_head, pc->any_lo, pc->any_hi);
+      }
     }
   };
   auto fill_load_block = [&]() {
     f_blk = -1;
-    if (f_piece >= 0)
+    // (the fused step's table width is not known on the host: check it here)
+    if (f_piece >= 0 && (!DEV || f_chunk / cpb < p.block_table_stride))
       f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_chunk / cpb];
   };
   auto fill_store = [&](int pos) {
@@ -299,12 +436,11 @@ splitkv_decode_kernel(const AttnParams p) {
       const bool lv = (nx_live >> (g + 8 * rr)) & 1u;
 #pragma unroll
       for (int i = 0; i < Geo::kK16; ++i)
-        kreg[rr][i] = lv ? dev::ldg_stream(kchunk + (rr ? koff1 : koff0) + 64 * i)
-                         : make_uint4(0, 0, 0, 0);
+        kreg[rr][i] = lv ? load16(kchunk + (rr ? koff1 : koff0) + 64 * i) : make_uint4(0, 0, 0, 0);
     }
     if constexpr (Geo::kPth) {
       const bool lv = (nx_live >> (g + 8 * (c & 1))) & 1u;
-      treg = lv ? dev::ldg_stream((c < 2 ? kbase : vbase) + nx_base + toff) : make_uint4(0, 0, 0, 0);
+      treg = lv ? load16((c < 2 ? kbase : vbase) + nx_base + toff) : make_uint4(0, 0, 0, 0);
     }
   };
   auto load_v = [&]() {  // V codes of the chunk whose K was loaded last
@@ -319,7 +455,7 @@ splitkv_decode_kernel(const AttnParams p) {
       } else {
 #pragma unroll
         for (int i = 0; i < Geo::kVPieces; ++i)
-          vreg[vr][i] = lv ? dev::ldg_stream(vchunk + voff[vr] + 128 * i) : make_uint4(0, 0, 0, 0);
+          vreg[vr][i] = lv ? load16(vchunk + voff[vr] + 128 * i) : make_uint4(0, 0, 0, 0);
       }
     }
   };
@@ -355,7 +491,26 @@ splitkv_decode_kernel(const AttnParams p) {
   // significant bits fit f16's 11); sm_scale and log2(e) are applied to the
   // fp32 scores.  Lane c holds dims 64i + 16c + [0, 16) of its rows.
   auto start_piece = [&](int piece) {
-    pc = p.pieces[piece];
+    if constexpr (DEV) {
+      // The tile's part inside this warp's segment; a cut tile's partial
+      // rows go to one of the warp's two 16-row slots: 2 gw for the tile the
+      // segment starts in, 2 gw + 1 for the one it ends in.
+      const int4 ti = __ldcg(sp.tiles + piece);
+      const int64_t f0 = __ldcg(sp.prefix + piece), f1 = __ldcg(sp.prefix + piece + 1);
+      const bool cut = f0 < seg0 || f1 > seg0 + n;
+      pc.req = piece / p.heads_kv;
+      pc.kv_head = piece % p.heads_kv;
+      pc.row0 = 0;
+      pc.nrows = ti.w;
+      pc.part = cut ? (2 * gw + (f0 <= seg0 ? 0 : 1)) * kTileMaxRows : -1;
+      pc.merge = piece;
+      pc.any_lo = ti.y;
+      pc.any_hi = ti.z;
+      pc.flat0 = (int32_t)f0;
+      pc.chunk0 = ti.x;
+    } else {
+      pc = p.pieces[piece];
+    }
     q0 = p.query_start_loc[pc.req];
     const int Q = p.query_start_loc[pc.req + 1] - q0;
     const int L = p.seq_lens[pc.req];
@@ -519,16 +674,43 @@ splitkv_decode_kernel(const AttnParams p) {
       // piece waits for another.
       __threadfence();
       __syncwarp();
+      MergeItem m;
+      int64_t f0 = 0, w0 = 0;
+      // warp whose segment holds flat chunk f: floor(((f + 1) W - 1) / T)
+      auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / total_chunks; };
+      if constexpr (DEV) {
+        // The tile's splits are the warps whose segments hold its chunks:
+        // w0 .. w1 when every segment has chunks (T >= W), else one warp per
+        // chunk (every non-empty segment is a single chunk).
+        f0 = __ldcg(sp.prefix + pc.merge);
+        const int64_t f1 = __ldcg(sp.prefix + pc.merge + 1);
+        w0 = warp_of(f0);
+        const int64_t ns = total_chunks >= total_warps ? warp_of(f1 - 1) - w0 + 1 : f1 - f0;
+        m = MergeItem{pc.req, pc.kv_head, 0, pc.nrows, 0, (int32_t)ns, 0, 0};
+      } else {
+        m = p.merges[pc.merge];
+      }
       int last = 0;
       if (lane == 0) {
         const int prev = atomicAdd(p.merge_counters + pc.merge, 1);
-        last = prev == p.merges[pc.merge].nsplits - 1;
+        last = prev == m.nsplits - 1;
       }
       last = __shfl_sync(0xffffffffu, last, 0);
       if (last) {
         __threadfence();
-        const MergeItem m = p.merges[pc.merge];
-        merge_pieces<D>(p, m, lane);
+        if constexpr (DEV) {
+          // split s is warp w0 + s: its slot 2 (w0 + s), except that the
+          // first split's tile is warp w0's last one unless w0's segment
+          // starts exactly at the tile
+          const bool first_is_last = (w0 * total_chunks) / total_warps < f0;
+          const bool dense = total_chunks >= total_warps;
+          merge_pieces<D>(p, m, lane, [&](int s) {
+            const int64_t w = dense ? w0 + s : warp_of(f0 + s);
+            return (int)((2 * w + (s == 0 && first_is_last ? 1 : 0)) * kTileMaxRows);
+          });
+        } else {
+          merge_pieces<D>(p, m, lane, [&](int s) { return m.part + s * m.nrows; });
+        }
         if (lane == 0) atomicExch(p.merge_counters + pc.merge, 0);  // ready for the next call
       }
     }
@@ -774,16 +956,72 @@ splitkv_decode_kernel(const AttnParams p) {
 template <int DT, int D, int NT, bool AL>
 int launch_decode_instance(const AttnParams& p, cudaStream_t stream) {
   const size_t smem = decode_smem_bytes(DT, D);
-  auto kern = splitkv_decode_kernel<DT, D, NT, AL>;
+  auto kern = splitkv_decode_kernel<DT, D, NT, AL, false>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
-  kern<<<(unsigned)(p.num_warps / kDecodeWarps), kDecodeThreads, smem, stream>>>(p);
+  StepParams none{};
+  kern<<<(unsigned)(p.num_warps / kDecodeWarps), kDecodeThreads, smem, stream>>>(p, none);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
+}
+
+// The fused step: every CTA resident at once (a cooperative launch), as many
+// as fit on the device.  `warps` == 0 asks for that number instead.
+template <int DT, int D, int NT, bool AL>
+int launch_step_instance(const AttnParams& p, const StepParams& sp, int64_t* warps,
+                         cudaStream_t stream) {
+  const size_t smem = decode_smem_bytes(DT, D);
+  auto kern = splitkv_decode_kernel<DT, D, NT, AL, true>;
+  int dev = 0, sms = 0, per_sm = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess ||
+      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+          cudaSuccess ||
+      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) !=
+          cudaSuccess || per_sm <= 0) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  const int64_t grid = (int64_t)sms * per_sm;
+  if (*warps == 0) {
+    *warps = grid * kDecodeWarps;
+    return KVQ_OK;
+  }
+  if (*warps != grid * kDecodeWarps) return KVQ_E_INVALID_ARG;
+  AttnParams pp = p;
+  StepParams ss = sp;
+  void* args[] = {&pp, &ss};
+  if (cudaLaunchCooperativeKernel(reinterpret_cast<const void*>(kern), dim3((unsigned)grid),
+                                  dim3(kDecodeThreads), args, smem, stream) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return KVQ_OK;
 }
 
 // The instances of one head_dim and one ALiBi setting (one translation unit
 // each keeps the build parallel).
+// (tiles of up to 8 rows: one MMA n-tile; up to 16: two)
+template <int D, bool AL>
+int launch_step_d(const AttnParams& p, const StepParams& sp, int dtype, int64_t* warps,
+                  cudaStream_t stream) {
+#define KVQ_STEP_CASE(DT)                                                          \
+  case DT:                                                                         \
+    return sp.max_rows <= 8 ? launch_step_instance<DT, D, 1, AL>(p, sp, warps, stream) \
+                            : launch_step_instance<DT, D, 2, AL>(p, sp, warps, stream);
+  switch (dtype) {
+    KVQ_STEP_CASE(KVQ_AUTO)
+    KVQ_STEP_CASE(KVQ_FP8_E4M3)
+    KVQ_STEP_CASE(KVQ_FP8_E5M2)
+    KVQ_STEP_CASE(KVQ_INT8_PER_TOKEN_HEAD)
+    KVQ_STEP_CASE(KVQ_FP8_PER_TOKEN_HEAD)
+    KVQ_STEP_CASE(KVQ_FP8_E5M2_PER_TOKEN_HEAD)
+    default:
+      return KVQ_E_UNSUPPORTED;
+  }
+#undef KVQ_STEP_CASE
+}
+
 template <int D, bool AL>
 int launch_decode_d(const AttnParams& p, int dtype, int ntiles, cudaStream_t stream) {
 #define KVQ_DECODE_CASE(DT)                                                  \

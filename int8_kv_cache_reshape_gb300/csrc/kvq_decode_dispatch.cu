@@ -8,6 +8,8 @@ namespace kvq {
 #define KVQ_DECLARE(D)                                                                       \
   int launch_decode_d##D(const AttnParams&, int, int, void*);                               \
   int launch_decode_d##D##_alibi(const AttnParams&, int, int, void*);                       \
+  int launch_step_d##D(const AttnParams&, const StepParams&, int, int64_t*, void*);         \
+  int launch_step_d##D##_alibi(const AttnParams&, const StepParams&, int, int64_t*, void*); \
   int launch_prefill_d##D(const AttnParams&, const PrefillMaps&, int, int64_t, void*);      \
   int launch_prefill_d##D##_alibi(const AttnParams&, const PrefillMaps&, int, int64_t, void*);
 KVQ_DECLARE(64)
@@ -27,6 +29,34 @@ int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void
                         : launch_decode_d256(p, dtype, ntiles, stream);
     default: return KVQ_E_UNSUPPORTED;
   }
+}
+
+namespace {
+int step_dispatch(const AttnParams& p, const StepParams& sp, int dtype, int head_dim, bool al,
+                  int64_t* warps, void* stream) {
+  switch (head_dim) {
+    case 64: return al ? launch_step_d64_alibi(p, sp, dtype, warps, stream)
+                       : launch_step_d64(p, sp, dtype, warps, stream);
+    case 128: return al ? launch_step_d128_alibi(p, sp, dtype, warps, stream)
+                        : launch_step_d128(p, sp, dtype, warps, stream);
+    case 256: return al ? launch_step_d256_alibi(p, sp, dtype, warps, stream)
+                        : launch_step_d256(p, sp, dtype, warps, stream);
+    default: return KVQ_E_UNSUPPORTED;
+  }
+}
+}  // namespace
+
+int step_warps(int dtype, int head_dim, bool alibi, int max_rows, int64_t* warps) {
+  AttnParams p{};
+  StepParams sp{};
+  sp.max_rows = max_rows;
+  *warps = 0;
+  return step_dispatch(p, sp, dtype, head_dim, alibi, warps, nullptr);
+}
+
+int launch_decode_step(const AttnParams& p, const StepParams& sp, int dtype, int head_dim,
+                       int64_t warps, void* stream) {
+  return step_dispatch(p, sp, dtype, head_dim, uses_alibi(p), &warps, stream);
 }
 
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,

@@ -789,4 +789,136 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   return KVQ_OK;
 }
 
+// ---- the fused decode step ------------------------------------------------
+
+namespace {
+int step_rows(int max_query_len, int group) { return max_query_len * group <= 8 ? 8 : 16; }
+}  // namespace
+
+int kvq_decode_step_workspace_size(int num_req, int heads_q, int heads_kv, int head_dim,
+                                   kvq_dtype_t dtype, int max_query_len, int use_alibi,
+                                   size_t* workspace_bytes) {
+  if (!workspace_bytes) return KVQ_E_INVALID_ARG;
+  *workspace_bytes = 0;
+  if (num_req < 0 || heads_q <= 0 || heads_kv <= 0 || max_query_len <= 0) return KVQ_E_INVALID_ARG;
+  if (!kvq::is_valid_dtype(dtype)) return KVQ_E_INVALID_ARG;
+  if (heads_q % heads_kv || !kvq::head_dim_supported(head_dim)) return KVQ_E_UNSUPPORTED;
+  const int G = heads_q / heads_kv;
+  if ((int64_t)max_query_len * G > kvq::kTileMaxRows) return KVQ_E_UNSUPPORTED;
+  if ((int64_t)num_req * heads_kv > kvq::kMaxStepTiles) return KVQ_E_UNSUPPORTED;
+  int64_t warps = 0;
+  const int rc = kvq::step_warps(dtype, head_dim, use_alibi != 0, step_rows(max_query_len, G), &warps);
+  if (rc != KVQ_OK) return rc;
+  *workspace_bytes = kvq::step_workspace(num_req * heads_kv, head_dim, warps).total;
+  return KVQ_OK;
+}
+
+int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype,
+                    const void* key, const void* value, int64_t num_new_tokens,
+                    int64_t key_stride_tok, int64_t value_stride_tok, const int64_t* slot_mapping,
+                    void* key_cache, void* value_cache, int64_t num_blocks, int block_size,
+                    const void* q, const int32_t* query_start_loc, const int32_t* seq_lens,
+                    const int32_t* block_table, int block_table_stride, int max_query_len,
+                    float sm_scale, int window, float soft_cap, const float* alibi_slopes,
+                    const float* sinks, float k_scale, float v_scale, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  size_t need = 0;
+  int rc = kvq_decode_step_workspace_size(num_req, heads_q, heads_kv, head_dim, dtype,
+                                          max_query_len, alibi_slopes != nullptr, &need);
+  if (rc != KVQ_OK) return rc;
+  if (num_new_tokens < 0 || num_blocks <= 0 || block_table_stride <= 0) return KVQ_E_INVALID_ARG;
+  if (block_size <= 0 || block_size % kvq::kChunkTokens) return KVQ_E_UNSUPPORTED;
+  if (num_blocks * (int64_t)block_size >= ((int64_t)1 << 31)) return KVQ_E_UNSUPPORTED;
+  if (!key_cache || !value_cache || !q || !out || !query_start_loc || !seq_lens || !block_table ||
+      !workspace)
+    return KVQ_E_INVALID_ARG;
+  if (num_new_tokens > 0) {
+    const int64_t min_stride = (int64_t)heads_kv * head_dim;
+    if (!key || !value || !slot_mapping || key_stride_tok < min_stride ||
+        value_stride_tok < min_stride || key_stride_tok % 8 || value_stride_tok % 8 ||
+        !aligned(key, 16) || !aligned(value, 16) || !aligned(slot_mapping, 8))
+      return KVQ_E_INVALID_ARG;
+  }
+  if (!aligned(q, 16) || !aligned(key_cache, 16) || !aligned(value_cache, 16) ||
+      !aligned(out, 16) || !aligned(block_table, 4) || !aligned(alibi_slopes, 4) ||
+      !aligned(sinks, 4) || !aligned(workspace, 256))
+    return KVQ_E_INVALID_ARG;
+  if (window < 0 || !std::isfinite(sm_scale) || !std::isfinite(soft_cap)) return KVQ_E_INVALID_ARG;
+  if (dtype == KVQ_FP8_E4M3 || dtype == KVQ_FP8_E5M2) {
+    if (!(std::isfinite(k_scale) && k_scale > 0.0f && std::isfinite(v_scale) && v_scale > 0.0f))
+      return KVQ_E_INVALID_ARG;
+  }
+  if (workspace_bytes < need) return KVQ_E_WORKSPACE_TOO_SMALL;
+  const int G = heads_q / heads_kv;
+  const int max_rows = step_rows(max_query_len, G);
+  int64_t warps = 0;
+  rc = kvq::step_warps(dtype, head_dim, alibi_slopes != nullptr, max_rows, &warps);
+  if (rc != KVQ_OK) return rc;
+  const int num_tiles = num_req * heads_kv;
+  const kvq::StepWorkspace lay = kvq::step_workspace(num_tiles, head_dim, warps);
+  char* ws = static_cast<char*>(workspace);
+
+  kvq::AttnParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = static_cast<const uint16_t*>(q);
+  p.key_cache = static_cast<const uint8_t*>(key_cache);
+  p.value_cache = static_cast<const uint8_t*>(value_cache);
+  p.query_start_loc = query_start_loc;
+  p.seq_lens = seq_lens;
+  p.block_table = block_table;
+  p.out = static_cast<uint16_t*>(out);
+  p.part_o = reinterpret_cast<float*>(ws + lay.o);
+  p.part_lse = reinterpret_cast<float*>(ws + lay.lse);
+  p.merge_counters = reinterpret_cast<int32_t*>(ws + lay.counters);
+  p.error_flag = reinterpret_cast<int32_t*>(ws);
+  p.num_blocks = num_blocks;
+  p.block_table_stride = block_table_stride;
+  p.block_size = block_size;
+  p.heads_q = heads_q;
+  p.heads_kv = heads_kv;
+  p.group = G;
+  p.causal = 1;
+  p.window = window;
+  p.sm_scale = sm_scale;
+  p.soft_cap = soft_cap > 0.0f ? soft_cap : 0.0f;
+  p.k_scale = k_scale;
+  p.v_scale = v_scale;
+  p.alibi_slopes = alibi_slopes;
+  p.sinks = sinks;
+
+  kvq::StepParams sp;
+  std::memset(&sp, 0, sizeof(sp));
+  sp.key = static_cast<const uint16_t*>(key);
+  sp.value = static_cast<const uint16_t*>(value);
+  sp.num_tokens = num_new_tokens;
+  sp.key_stride = key_stride_tok;
+  sp.value_stride = value_stride_tok;
+  sp.slot_mapping = slot_mapping;
+  sp.key_cache = static_cast<uint8_t*>(key_cache);
+  sp.value_cache = static_cast<uint8_t*>(value_cache);
+  sp.num_slots = num_blocks * (int64_t)block_size;
+  sp.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
+  sp.tiles = reinterpret_cast<int4*>(ws + lay.tiles);
+  sp.barrier = reinterpret_cast<uint32_t*>(ws + 128);
+  sp.num_req = num_req;
+  sp.num_tiles = num_tiles;
+  sp.max_rows = max_rows;
+  return kvq::launch_decode_step(p, sp, dtype, head_dim, warps, stream);
+}
+
+int kvq_decode_step_check(const void* workspace) {
+  if (!workspace) return KVQ_E_INVALID_ARG;
+  int32_t flag = 0;
+  if (cudaMemcpy(&flag, workspace, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  if (flag == 0) return KVQ_OK;
+  if (cudaMemset(const_cast<void*>(workspace), 0, sizeof(flag)) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return flag == 1 ? KVQ_E_TIMEOUT : KVQ_E_INVALID_ARG;
+}
+
 }  // extern "C"

@@ -206,6 +206,45 @@ struct AttnParams {
   const float* sinks;          // [Hq] or null: one extra logit in the softmax normaliser
 };
 
+// ---- fused decode step (cache write + device-built plan + decode) --------
+// Extra kernel arguments of the fused step: the new tokens' rows for the
+// cache write and the plan the kernel builds in its workspace.  Each
+// (request, kv head) is one row tile of the request's Q * G <= 16 rows.
+struct StepParams {
+  const uint16_t* key;          // bf16 [num_tokens, Hkv, D] (token stride given)
+  const uint16_t* value;
+  int64_t num_tokens, key_stride, value_stride;
+  const int64_t* slot_mapping;  // [num_tokens]
+  uint8_t* key_cache;           // the caches the attention reads, writable
+  uint8_t* value_cache;
+  int64_t num_slots;            // num_blocks * block_size
+  int32_t* prefix;              // [num_tiles + 1]: flat index of each tile's first chunk
+  int4* tiles;                  // [num_tiles]: {first chunk, key_lo, key_hi, rows}
+  uint32_t* barrier;            // [2]: arrivals, generation (grid barrier)
+  int num_req, num_tiles;       // num_tiles = num_req * Hkv
+  int max_rows;                 // 8 or 16: rows per tile the launch is built for
+};
+
+// Workspace of the fused step for `warps` decode warps: an error word and
+// the grid barrier's two words (256 bytes), the prefix, the tile table, the
+// merge counters, then partial log-sum-exps and outputs: each warp owns two
+// 16-row slots (the tile its segment starts in and the one it ends in).
+struct StepWorkspace {
+  size_t prefix, tiles, counters, lse, o, total;
+};
+KVQ_HD constexpr StepWorkspace step_workspace(int num_tiles, int head_dim, int64_t warps) {
+  StepWorkspace w{};
+  w.prefix = 256;
+  w.tiles = w.prefix + align256((size_t)(num_tiles + 1) * 4);
+  w.counters = w.tiles + align256((size_t)num_tiles * 16);
+  w.lse = w.counters + align256((size_t)num_tiles * 4);
+  w.o = w.lse + align256((size_t)warps * 2 * kTileMaxRows * 4);
+  w.total = w.o + (size_t)warps * 2 * kTileMaxRows * head_dim * 4;
+  return w;
+}
+// Largest num_req * heads_kv of one fused step.
+constexpr int kMaxStepTiles = 1 << 16;
+
 }  // namespace kvq
 
 // Launchers (defined in the .cu files; return KVQ_OK or KVQ_E_CUDA).
@@ -218,6 +257,13 @@ int launch_reshape_and_cache(const void* key, const void* value,
                              const int64_t* slot_mapping, int dtype,
                              float k_scale, float v_scale, void* stream);
 int launch_decode(const AttnParams& p, int dtype, int head_dim, int ntiles, void* stream);
+// The fused step's kernel (cooperative launch of `warps` / 4 CTAs); `warps`
+// from step_warps().
+int launch_decode_step(const AttnParams& p, const StepParams& sp, int dtype, int head_dim,
+                       int64_t warps, void* stream);
+// Decode warps of the fused step's grid on the current device (every CTA
+// resident at once) in *warps; KVQ_OK or a KVQ_E_* status.
+int step_warps(int dtype, int head_dim, bool alibi, int max_rows, int64_t* warps);
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
                    int64_t num_tiles, void* stream);
 // Whether a launch needs the ALiBi instances of the kernels.

@@ -90,6 +90,16 @@ lib.kvq_attention_with_kv_cache_static_scratch.argtypes = [
     _c.c_int, _c.c_int, _c.c_int64, _c.c_float, _c.c_int, _c.c_int,
     _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p]
 STATIC_SCRATCH_BYTES = 16 << 20
+lib.kvq_decode_step.restype = _c.c_int
+lib.kvq_decode_step.argtypes = [
+    _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _c.c_int64, _c.c_int64,
+    _c.c_int64, _p, _p, _p, _c.c_int64, _c.c_int, _p, _p, _p, _p, _c.c_int, _c.c_int,
+    _c.c_float, _c.c_int, _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
+lib.kvq_decode_step_workspace_size.restype = _c.c_int
+lib.kvq_decode_step_workspace_size.argtypes = [
+    _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(_c.c_size_t)]
+lib.kvq_decode_step_check.restype = _c.c_int
+lib.kvq_decode_step_check.argtypes = [_p]
 lib.kvq_sched_destroy.restype = None
 lib.kvq_sched_destroy.argtypes = [_p]
 lib.kvq_sched_check_device.restype = _c.c_int
@@ -273,3 +283,42 @@ def attention_with_kv_cache_static_scratch(sched: Sched, q, key_cache, value_cac
         key_cache.shape[1], nb, float(sm_scale), int(bool(causal)), int(window),
         float(soft_cap), _ptr(alibi_slopes), _ptr(sinks), float(k_scale), float(v_scale),
         _ptr(out), _stream(stream)), "kvq_attention_with_kv_cache_static_scratch")
+
+
+def decode_step_workspace_size(num_req: int, heads_q: int, heads_kv: int, head_dim: int,
+                               kv_cache_dtype, max_query_len: int = 1,
+                               use_alibi: bool = False) -> int:
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    out = _c.c_size_t()
+    _check(lib.kvq_decode_step_workspace_size(num_req, heads_q, heads_kv, head_dim, dt,
+                                              max_query_len, int(bool(use_alibi)),
+                                              _c.byref(out)), "kvq_decode_step_workspace_size")
+    return out.value
+
+
+def decode_step(key, value, slot_mapping, key_cache, value_cache, q, query_start_loc, seq_lens,
+                block_table, max_query_len: int, sm_scale: float, window: int, soft_cap: float,
+                k_scale: float, v_scale: float, out, workspace, kv_cache_dtype, heads_kv: int,
+                alibi_slopes=None, sinks=None, stream=None, num_blocks=None) -> None:
+    """kvq_decode_step: the new rows key/value bf16 [T, Hkv, D] with their
+    slot_mapping int64 [T]; q / out bf16 [sum Q, Hq, D]; query_start_loc,
+    seq_lens int32 device; workspace: a zero-filled uint8 device tensor of
+    >= decode_step_workspace_size(...) bytes."""
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    _, Hq, D = q.shape
+    T = key.shape[0]
+    nb = key_cache.shape[0] if num_blocks is None else num_blocks
+    _check(lib.kvq_decode_step(
+        seq_lens.shape[0], Hq, heads_kv, D, dt, _ptr(key), _ptr(value), T, key.stride(0),
+        value.stride(0), _ptr(slot_mapping), _ptr(key_cache), _ptr(value_cache), nb,
+        key_cache.shape[1], _ptr(q), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table),
+        block_table.stride(0), int(max_query_len), float(sm_scale), int(window), float(soft_cap),
+        _ptr(alibi_slopes), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out),
+        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
+        "kvq_decode_step")
+
+
+def decode_step_check(workspace) -> None:
+    """Raise KvqError if a decode_step run with this workspace flagged an
+    error (synchronises the device)."""
+    _check(lib.kvq_decode_step_check(_ptr(workspace)), "kvq_decode_step_check")

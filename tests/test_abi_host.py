@@ -200,3 +200,18 @@ def test_attention_refuses_mismatched_schedule():
     assert f(*args(16, 8, 128, 1)) == kvq.E_SCHED_MISMATCH     # other heads
     assert f(*args(32, 8, 128, 1, causal=0)) == kvq.E_SCHED_MISMATCH
     assert f(*args(32, 8, 128, 1, window=5)) == kvq.E_SCHED_MISMATCH
+
+
+def test_decode_step_shape_checks_come_first():
+    """kvq_decode_step_workspace_size refuses bad shapes on the host before
+    it asks the device anything (no GPU needed for these)."""
+    f = kvq.lib.kvq_decode_step_workspace_size
+    out = ctypes.c_size_t()
+    assert f(4, 32, 8, 128, 1, 5, 0, ctypes.byref(out)) == kvq.E_UNSUPPORTED   # 20 rows
+    assert f(4, 30, 8, 128, 1, 1, 0, ctypes.byref(out)) == kvq.E_UNSUPPORTED   # GQA ratio
+    assert f(4, 32, 8, 96, 1, 1, 0, ctypes.byref(out)) == kvq.E_UNSUPPORTED    # head_dim
+    assert f(-1, 32, 8, 128, 1, 1, 0, ctypes.byref(out)) == kvq.E_INVALID_ARG
+    assert f(4, 32, 8, 128, 1, 0, 0, ctypes.byref(out)) == kvq.E_INVALID_ARG   # max_query_len
+    assert f(4, 32, 8, 128, 9, 1, 0, ctypes.byref(out)) == kvq.E_INVALID_ARG   # dtype
+    assert f(4, 32, 8, 128, 1, 1, 0, None) == kvq.E_INVALID_ARG
+    assert kvq.lib.kvq_decode_step_check(None) == kvq.E_INVALID_ARG

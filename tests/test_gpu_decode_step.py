@@ -1,0 +1,181 @@
+"""GPU parity of the fused decode step (kvq_decode_step): the step's new K/V
+rows written into the caches, the plan built on the device from the
+device's lengths, and split-KV attention -- one cooperative launch.
+
+vllm PR 50194 page, Key source snippet (get_scheduler_metadata feeding the
+attention) and Breakdown item 1; vllm PR 39445 page, Breakdown items 1-3.
+The caches it leaves must equal the oracle's writer bit for bit; the
+output must match the oracle within the parity bound of tests/_harness.py.
+A step captured once in a CUDA graph is replayed with other lengths, new
+tokens and tables (the plan lives on the device), and must match the oracle
+for those.
+"""
+import numpy as np
+import pytest
+import torch
+
+from int8_kv_cache_reshape_gb300 import workloads as W
+
+from _harness import (Guarded, GpuRun, assert_attention_close, kvq, oracle_cache,
+                      oracle_reference)
+
+pytestmark = pytest.mark.gpu
+
+
+class Step:
+    """A decode batch split into its cached context and the step's new rows
+    (the last Q tokens of every request), on the device."""
+
+    def __init__(self, wl, alibi=None, sinks=None, max_query_len=None):
+        self.wl = wl
+        self.g = GpuRun(wl, alibi_slopes=alibi, sinks=sinks)
+        new = wl.new_token_mask()
+        old_slots = wl.slot_mapping.clone()
+        old_slots[new] = -1
+        k = kvq()
+        # the context written beforehand; the step writes the new rows
+        k.reshape_and_cache(self.g.key, self.g.value, self.g.kc, self.g.vc, old_slots.to(self.g.dev),
+                            wl.kv_cache_dtype, wl.k_scale, wl.v_scale)
+        idx = torch.nonzero(new).flatten()
+        dev = self.g.dev
+        self.nkey = wl.key[idx].contiguous().to(dev)
+        self.nval = wl.value[idx].contiguous().to(dev)
+        self.nslot = wl.slot_mapping[idx].contiguous().to(dev)
+        self.mql = max(wl.query_lens) if max_query_len is None else max_query_len
+        nbytes = k.decode_step_workspace_size(wl.num_req, wl.heads_q, wl.heads_kv, wl.head_dim,
+                                              wl.kv_cache_dtype, self.mql, alibi is not None)
+        self.ws = Guarded((nbytes,), torch.uint8, 0, dev)
+
+    def run(self):
+        wl, g = self.wl, self.g
+        kvq().decode_step(self.nkey, self.nval, self.nslot, g.kc, g.vc, g.q, g.qsl, g.sl, g.bt,
+                          self.mql, wl.sm_scale, wl.window, wl.soft_cap, wl.k_scale, wl.v_scale,
+                          g.out, self.ws.t, wl.kv_cache_dtype, wl.heads_kv,
+                          alibi_slopes=g.alibi, sinks=g.sinks)
+        return self
+
+    def check(self, what):
+        torch.cuda.synchronize()
+        kvq().decode_step_check(self.ws.t)
+        self.ws.check("decode-step workspace")
+        self.g._kc.check("key cache")
+        self.g._vc.check("value cache")
+        self.g._out.check("output")
+        wl = self.wl
+        kc, vc = oracle_cache(wl)
+        assert np.array_equal(self.g.kc.cpu().numpy(), kc), f"{what}: key cache"
+        assert np.array_equal(self.g.vc.cpu().numpy(), vc), f"{what}: value cache"
+        ref, bnd = oracle_reference(wl, kc, vc, alibi_slopes=self.g.alibi_np,
+                                    sinks=self.g.sinks_np)
+        return assert_attention_close(self.g.out_f32(), ref, what, bnd)
+
+
+CASES = [("fp8_e4m3", 128, 32, 8, [1] * 12, 0, 0.0),
+         ("fp8_e5m2", 128, 64, 8, [1] * 5, 300, 50.0),
+         ("int8_per_token_head", 128, 32, 8, [1, 2, 4, 1, 3], 0, 0.0),
+         ("fp8_per_token_head", 64, 8, 2, [2, 1, 4, 1], 100, 0.0),
+         ("auto", 128, 16, 4, [1, 3, 1], 0, 20.0),
+         ("fp8_e5m2_per_token_head", 256, 16, 2, [1, 2, 1], 0, 0.0)]
+
+
+@pytest.mark.parametrize("dtype,D,hq,hkv,ql,window,cap", CASES)
+def test_fused_step_matches_oracle(cuda_device, dtype, D, hq, hkv, ql, window, cap):
+    rng = np.random.default_rng(len(ql) + D)
+    sl = [int(x) for x in rng.integers(max(ql), 3000, len(ql))]
+    sl[0] = ql[0]                          # a request that is all new tokens
+    wl = W.custom(f"step-{dtype}-{D}", ql, sl, hq, hkv, D, 16, dtype, 600 + D + hq,
+                  window=window, soft_cap=cap,
+                  token_scale_range=(0.1, 10.0) if "per_token" in dtype else None)
+    Step(wl).run().check(wl.name)
+
+
+def test_fused_step_alibi_sinks(cuda_device):
+    hq = 32
+    wl = W.custom("step-ext", [1, 2, 1, 4], [2500, 700, 33, 1200], hq, 8, 128, 16, "fp8_e4m3", 610,
+                  window=600)
+    Step(wl, W.alibi_slopes(hq), W.sink_logits(hq, 611)).run().check("step alibi + sinks")
+
+
+def test_fused_step_tiny_batch_and_big_batch(cuda_device):
+    """Fewer chunks than warps (every segment at most one chunk) and many
+    more (the decode batch's shape)."""
+    wl = W.custom("step-tiny", [1, 1], [20, 47], 8, 2, 64, 16, "fp8_e4m3", 612)
+    Step(wl).run().check("step tiny")
+    wl = W.config(2)
+    Step(wl).run().check("step decode batch")
+
+
+def test_fused_step_graph_replay_with_new_lengths(cuda_device):
+    """Capture one step, then change the device lengths, tables, slots, new
+    rows and q in place (same capacities) and replay: the output follows."""
+    hq, hkv, D = 32, 8, 128
+    a = W.custom("replay-a", [1] * 6, [900, 40, 3200, 300, 1, 1500], hq, hkv, D, 16,
+                 "int8_per_token_head", 620, token_scale_range=(0.1, 10.0), extra_blocks=200)
+    st = Step(a)
+    st.run()
+    st.check("replay: direct")
+    # a second batch of the same shape with other lengths, in the same pool
+    b = W.custom("replay-b", [1] * 6, [1700, 2, 600, 3100, 45, 900], hq, hkv, D, 16,
+                 "int8_per_token_head", 621, token_scale_range=(0.1, 10.0),
+                 num_blocks=a.num_blocks)
+    assert b.block_table.shape[1] <= a.block_table.shape[1]
+    graph = torch.cuda.CUDAGraph()
+    side = torch.cuda.Stream()
+    side.wait_stream(torch.cuda.current_stream())
+    with torch.cuda.stream(side):
+        st.run()
+    torch.cuda.current_stream().wait_stream(side)
+    torch.cuda.synchronize()
+    with torch.cuda.graph(graph):
+        st.run()
+    # swap in batch b: caches rewritten from scratch with b's context
+    g = st.g
+    sb = Step.__new__(Step)
+    sb.wl = b
+    sb.g = GpuRun(b)
+    new = b.new_token_mask()
+    old_slots = b.slot_mapping.clone()
+    old_slots[new] = -1
+    g.kc.fill_(0xCD)
+    g.vc.fill_(0xCD)
+    kvq().reshape_and_cache(sb.g.key, sb.g.value, g.kc, g.vc, old_slots.to(g.dev),
+                            b.kv_cache_dtype, b.k_scale, b.v_scale)
+    idx = torch.nonzero(new).flatten()
+    st.nkey.copy_(b.key[idx])
+    st.nval.copy_(b.value[idx])
+    st.nslot.copy_(b.slot_mapping[idx])
+    g.q.copy_(b.q)
+    g.qsl.copy_(b.query_start_loc)
+    g.sl.copy_(b.seq_lens_t)
+    g.bt.fill_(-1)
+    g.bt[:, :b.block_table.shape[1]].copy_(b.block_table)
+    g.out.fill_(float("nan"))
+    graph.replay()
+    torch.cuda.synchronize()
+    kvq().decode_step_check(st.ws.t)
+    kc, vc = oracle_cache(b)
+    assert np.array_equal(g.kc.cpu().numpy(), kc) and np.array_equal(g.vc.cpu().numpy(), vc)
+    ref, bnd = oracle_reference(b, kc, vc)
+    assert_attention_close(g.out.float().cpu().numpy(), ref, "replay with new lengths", bnd)
+
+
+def test_fused_step_refuses_wide_tiles(cuda_device):
+    with pytest.raises(kvq().KvqError) as e:
+        kvq().decode_step_workspace_size(4, 32, 8, 128, "fp8_e4m3", 5)   # 5 * 4 rows > 16
+    assert e.value.status == kvq().E_UNSUPPORTED
+
+
+def test_fused_step_flags_device_lengths_beyond_the_bound(cuda_device):
+    """A device query length above max_query_len: the request is skipped and
+    the error word says so; the other requests still match the oracle."""
+    wl = W.custom("step-bad", [1, 3, 1], [500, 90, 40], 16, 4, 128, 16, "fp8_e4m3", 630)
+    st = Step(wl, max_query_len=2)
+    st.run()
+    torch.cuda.synchronize()
+    with pytest.raises(kvq().KvqError) as e:
+        kvq().decode_step_check(st.ws.t)
+    assert e.value.status == kvq().E_INVALID_ARG
+    kc, vc = oracle_cache(wl)
+    toks = [0, 4]                                      # requests 0 and 2
+    ref, bnd = oracle_reference(wl, kc, vc, tokens=toks)
+    assert_attention_close(st.g.out_f32(toks), ref, "step: good requests", bnd)
