@@ -237,8 +237,25 @@ __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams&
     sp.prefix[t] = run;
     run += chunks_of(t, false);
   }
-  if (tid == kDecodeThreads - 1) sp.prefix[nt] = run;
+  __shared__ int32_t total;
+  if (tid == kDecodeThreads - 1) {
+    sp.prefix[nt] = run;
+    total = run;
+  }
   for (int t = tid; t < nt; t += kDecodeThreads) p.merge_counters[t] = 0;
+  __syncthreads();
+  // Each warp's first tile: warp w's segment starts at floor(w T / W), which
+  // lies in tile t for w in [ceil(f0 W / T), ceil(f1 W / T)).
+  const int64_t T = total, W = (int64_t)gridDim.x * kDecodeWarps;
+  if (T > 0) {
+    int64_t f0 = t0 < t1 ? sp.prefix[t0] : 0;  // (this thread's own stores)
+    for (int t = t0; t < t1; ++t) {
+      const int64_t f1 = t + 1 < t1 ? sp.prefix[t + 1] : (t + 1 == nt ? T : f0 + chunks_of(t, false));
+      for (int64_t w = (f0 * W + T - 1) / T; w < (f1 * W + T - 1) / T && w < W; ++w)
+        sp.warp_tile[w] = t;
+      f0 = f1;
+    }
+  }
 }
 
 // Grid-wide barrier of a cooperative launch (every CTA resident): arrival
@@ -338,15 +355,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   int f_piece = -1, f_chunk = 0;
   int cur_piece = 0;
   if constexpr (DEV) {
-    if (n > 0) {  // the tile holding position seg0: the first with prefix[t + 1] > seg0
-      int lo = 0, hi = sp.num_tiles - 1;
-      while (lo < hi) {
-        const int mid = (lo + hi) >> 1;
-        if (__ldcg(sp.prefix + mid + 1) > seg0) hi = mid;
-        else lo = mid + 1;
-      }
-      cur_piece = lo;
-    }
+    if (n > 0) cur_piece = __ldcg(sp.warp_tile + gw);  // the tile holding position seg0
   } else {
     cur_piece = n > 0 ? p.warp_piece[gw] : 0;
   }

@@ -899,6 +899,7 @@ int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dt
   sp.num_slots = num_blocks * (int64_t)block_size;
   sp.prefix = reinterpret_cast<int32_t*>(ws + lay.prefix);
   sp.tiles = reinterpret_cast<int4*>(ws + lay.tiles);
+  sp.warp_tile = reinterpret_cast<int32_t*>(ws + lay.warp_tile);
   sp.barrier = reinterpret_cast<uint32_t*>(ws + 128);
   sp.num_req = num_req;
   sp.num_tiles = num_tiles;

@@ -220,23 +220,26 @@ struct StepParams {
   int64_t num_slots;            // num_blocks * block_size
   int32_t* prefix;              // [num_tiles + 1]: flat index of each tile's first chunk
   int4* tiles;                  // [num_tiles]: {first chunk, key_lo, key_hi, rows}
+  int32_t* warp_tile;           // [warps]: the tile holding each warp's first chunk
   uint32_t* barrier;            // [2]: arrivals, generation (grid barrier)
   int num_req, num_tiles;       // num_tiles = num_req * Hkv
   int max_rows;                 // 8 or 16: rows per tile the launch is built for
 };
 
 // Workspace of the fused step for `warps` decode warps: an error word and
-// the grid barrier's two words (256 bytes), the prefix, the tile table, the
-// merge counters, then partial log-sum-exps and outputs: each warp owns two
-// 16-row slots (the tile its segment starts in and the one it ends in).
+// the grid barrier's two words (256 bytes), the prefix, the tile table, each
+// warp's first tile, the merge counters, then partial log-sum-exps and
+// outputs: each warp owns two 16-row slots (the tile its segment starts in
+// and the one it ends in).
 struct StepWorkspace {
-  size_t prefix, tiles, counters, lse, o, total;
+  size_t prefix, tiles, warp_tile, counters, lse, o, total;
 };
 KVQ_HD constexpr StepWorkspace step_workspace(int num_tiles, int head_dim, int64_t warps) {
   StepWorkspace w{};
   w.prefix = 256;
   w.tiles = w.prefix + align256((size_t)(num_tiles + 1) * 4);
-  w.counters = w.tiles + align256((size_t)num_tiles * 16);
+  w.warp_tile = w.tiles + align256((size_t)num_tiles * 16);
+  w.counters = w.warp_tile + align256((size_t)warps * 4);
   w.lse = w.counters + align256((size_t)num_tiles * 4);
   w.o = w.lse + align256((size_t)warps * 2 * kTileMaxRows * 4);
   w.total = w.o + (size_t)warps * 2 * kTileMaxRows * head_dim * 4;

@@ -296,6 +296,40 @@ def decode_step_workspace_size(num_req: int, heads_q: int, heads_kv: int, head_d
     return out.value
 
 
+class Prepared:
+    """One C-ABI call with its arguments marshalled once (pointers, sizes,
+    the stream), for a serving loop that calls it every step on the same
+    buffers: calling the object only crosses into the library.  The tensors
+    behind the pointers must stay alive (and in place) while it is used."""
+
+    def __init__(self, fn, args, what: str):
+        self.fn = fn
+        self.args = tuple(args)
+        self.what = what
+
+    def __call__(self) -> None:
+        _check(self.fn(*self.args), self.what)
+
+
+def _decode_step_args(key, value, slot_mapping, key_cache, value_cache, q, query_start_loc,
+                      seq_lens, block_table, max_query_len, sm_scale, window, soft_cap, k_scale,
+                      v_scale, out, workspace, kv_cache_dtype, heads_kv, alibi_slopes, sinks,
+                      stream, num_blocks):
+    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
+    _, Hq, D = q.shape
+    T = key.shape[0]
+    nb = key_cache.shape[0] if num_blocks is None else num_blocks
+    return (_c.c_int(seq_lens.shape[0]), _c.c_int(Hq), _c.c_int(heads_kv), _c.c_int(D),
+            _c.c_int(dt), _ptr(key), _ptr(value), _c.c_int64(T), _c.c_int64(key.stride(0)),
+            _c.c_int64(value.stride(0)), _ptr(slot_mapping), _ptr(key_cache), _ptr(value_cache),
+            _c.c_int64(nb), _c.c_int(key_cache.shape[1]), _ptr(q), _ptr(query_start_loc),
+            _ptr(seq_lens), _ptr(block_table), _c.c_int(block_table.stride(0)),
+            _c.c_int(int(max_query_len)), _c.c_float(sm_scale), _c.c_int(int(window)),
+            _c.c_float(soft_cap), _ptr(alibi_slopes), _ptr(sinks), _c.c_float(k_scale),
+            _c.c_float(v_scale), _ptr(out), _ptr(workspace),
+            _c.c_size_t(workspace.numel() * workspace.element_size()), _stream(stream))
+
+
 def decode_step(key, value, slot_mapping, key_cache, value_cache, q, query_start_loc, seq_lens,
                 block_table, max_query_len: int, sm_scale: float, window: int, soft_cap: float,
                 k_scale: float, v_scale: float, out, workspace, kv_cache_dtype, heads_kv: int,
@@ -304,18 +338,22 @@ def decode_step(key, value, slot_mapping, key_cache, value_cache, q, query_start
     slot_mapping int64 [T]; q / out bf16 [sum Q, Hq, D]; query_start_loc,
     seq_lens int32 device; workspace: a zero-filled uint8 device tensor of
     >= decode_step_workspace_size(...) bytes."""
-    dt = parse_kv_cache_dtype(kv_cache_dtype) if isinstance(kv_cache_dtype, str) else kv_cache_dtype
-    _, Hq, D = q.shape
-    T = key.shape[0]
-    nb = key_cache.shape[0] if num_blocks is None else num_blocks
-    _check(lib.kvq_decode_step(
-        seq_lens.shape[0], Hq, heads_kv, D, dt, _ptr(key), _ptr(value), T, key.stride(0),
-        value.stride(0), _ptr(slot_mapping), _ptr(key_cache), _ptr(value_cache), nb,
-        key_cache.shape[1], _ptr(q), _ptr(query_start_loc), _ptr(seq_lens), _ptr(block_table),
-        block_table.stride(0), int(max_query_len), float(sm_scale), int(window), float(soft_cap),
-        _ptr(alibi_slopes), _ptr(sinks), float(k_scale), float(v_scale), _ptr(out),
-        _ptr(workspace), workspace.numel() * workspace.element_size(), _stream(stream)),
-        "kvq_decode_step")
+    _check(lib.kvq_decode_step(*_decode_step_args(
+        key, value, slot_mapping, key_cache, value_cache, q, query_start_loc, seq_lens,
+        block_table, max_query_len, sm_scale, window, soft_cap, k_scale, v_scale, out, workspace,
+        kv_cache_dtype, heads_kv, alibi_slopes, sinks, stream, num_blocks)), "kvq_decode_step")
+
+
+def prepare_decode_step(key, value, slot_mapping, key_cache, value_cache, q, query_start_loc,
+                        seq_lens, block_table, max_query_len: int, sm_scale: float, window: int,
+                        soft_cap: float, k_scale: float, v_scale: float, out, workspace,
+                        kv_cache_dtype, heads_kv: int, alibi_slopes=None, sinks=None,
+                        stream=None, num_blocks=None) -> Prepared:
+    """decode_step with its arguments marshalled once (see Prepared)."""
+    return Prepared(lib.kvq_decode_step, _decode_step_args(
+        key, value, slot_mapping, key_cache, value_cache, q, query_start_loc, seq_lens,
+        block_table, max_query_len, sm_scale, window, soft_cap, k_scale, v_scale, out, workspace,
+        kv_cache_dtype, heads_kv, alibi_slopes, sinks, stream, num_blocks), "kvq_decode_step")
 
 
 def decode_step_check(workspace) -> None:
