@@ -377,7 +377,8 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
           pt.nrows = (int32_t)nrows;
           pt.kv_hi = (int32_t)(s->causal ? p_max + 1 : L);
           pt.kv_lo = (int32_t)(s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0);
-          pt.pad0 = pt.pad1 = 0;
+          pt.q0 = query_start_loc_host[r];
+          pt.pos0 = (int32_t)(L - Q);
           s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)((pt.kv_hi - 1) / kvq::kChunkTokens));
           s->prefill.push_back(pt);
         }
@@ -729,6 +730,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.merges = reinterpret_cast<const MergeItem*>(b + s->d_merges_off);
   p.merge_counters = reinterpret_cast<int32_t*>(b + s->d_counters_off);
   p.prefill_tiles = reinterpret_cast<const PrefillTile*>(b + s->d_prefill_off);
+  p.num_prefill_tiles = (int32_t)s->prefill.size();
   p.error_flag = reinterpret_cast<int32_t*>(b + s->d_error_off);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;

@@ -134,7 +134,8 @@ struct alignas(64) PrefillMaps {
 struct PrefillTile {
   int32_t req, kv_head, row0, nrows;
   int32_t kv_lo, kv_hi;  // keys some row of the tile can see
-  int32_t pad0, pad1;
+  int32_t q0;            // the request's first query token (query_start_loc[req])
+  int32_t pos0;          // position of its query 0: L - Q
 };
 static_assert(sizeof(PrefillTile) == 32, "PrefillTile layout");
 
@@ -195,6 +196,7 @@ struct AttnParams {
   const MergeItem* merges;
   int32_t* merge_counters;     // one per merge item, zero between calls
   const PrefillTile* prefill_tiles;
+  int32_t num_prefill_tiles;
   int32_t* error_flag;         // set by a kernel whose bounded wait timed out
   int64_t num_blocks;
   int block_table_stride;

@@ -209,11 +209,11 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
 
+  // The tile record carries the request's first query token and the
+  // position of its query 0, so the Q loads depend on one load only.
   const PrefillTile t = p.prefill_tiles[blockIdx.x];
   const int G = p.group;
-  const int q0 = p.query_start_loc[t.req];
-  const int Q = p.query_start_loc[t.req + 1] - q0;
-  const int L = p.seq_lens[t.req];
+  const int q0 = t.q0;
   const int kv_first = (t.kv_lo / kN) * kN;
   const int T = t.kv_hi > kv_first ? (t.kv_hi - kv_first + kN - 1) / kN : 0;  // KV tiles
 
@@ -436,6 +436,15 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   }
   int blk1[kChunks];
   uint32_t off1[kChunks];
+  if (warp == kCopyWarp && (tid & 31) == 0) {
+    // the tensor maps' descriptors, ahead of the first copies
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.k)) : "memory");
+    asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.v)) : "memory");
+    if constexpr (Geo::kPth) {
+      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.ks)) : "memory");
+      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.vs)) : "memory");
+    }
+  }
   if (warp == kCopyWarp && T > 0) {
     fetch_chunks(0, nx_blk, nx_off);
     if (T > 1) fetch_chunks(1, blk1, off1);
@@ -617,6 +626,28 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     __syncwarp();
   } else if (warp == kCopyWarp) {
     // ======================= copy producer =====================================
+    // One CTA fits on an SM, so the tile that will start when this one ends
+    // is about a grid's worth of SMs later in launch order: pull its record
+    // and its Q rows into L2 now (its prologue then reads them from L2).
+    {
+      uint32_t nsm;
+      asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
+      const int nb = (int)(blockIdx.x + nsm);
+      if (nb < p.num_prefill_tiles) {
+        const PrefillTile tn = p.prefill_tiles[nb];
+        const int lane = tid & 31;
+        // rows R of the tile: token q0 + R / G, heads kv_head * G .. + G - 1
+        // contiguous (G * D * 2 bytes per token)
+        const int tok0 = tn.row0 / G, tok1 = (tn.row0 + tn.nrows - 1) / G;
+        const int64_t run = (int64_t)G * D * 2;
+        for (int tk = tok0; tk <= tok1; ++tk) {
+          const char* base_q = reinterpret_cast<const char*>(
+              p.q + ((int64_t)(tn.q0 + tk) * p.heads_q + (int64_t)tn.kv_head * G) * D);
+          for (int64_t off = (int64_t)lane * 128; off < run; off += 32 * 128)
+            asm volatile("prefetch.global.L2 [%0];" :: "l"(base_q + off));
+        }
+      }
+    }
     // Tiles 0 and 1 went out before Q was staged.  Step i copies the K codes
     // of tile i + 1 (once K(i - 1) is converted) and then the V codes of
     // tile i (once V(i - 2) is), the order in which the converters release
@@ -771,9 +802,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     const uint32_t* vmaxw = reinterpret_cast<const uint32_t*>(sm + Geo::kOffVMax);
     constexpr uint32_t kAllChunks = (kChunks >= 32) ? 0xFFFFFFFFu : ((1u << kChunks) - 1u);
     constexpr int kVMaxSlots = (kN + 31) / 32;  // converter warps that hold keys
-    const int pos = L - Q + R / G;
+    const int pos = t.pos0 + R / G;
     const int W = p.window;
-    const int row_hi = row_valid ? (p.causal ? pos + 1 : L) : 0;  // padding rows see nothing
+    // (without causality every row sees the request's L keys: the tile's kv_hi)
+    const int row_hi = row_valid ? (p.causal ? pos + 1 : t.kv_hi) : 0;  // padding rows see nothing
     const int row_lo = W > 0 ? pos - W + 1 : 0;
     const float log2e = 1.4426950408889634f;
     const float cap = p.soft_cap;
