@@ -321,9 +321,20 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   };
 
   // ---- this warp's segment of the flat chunk sequence -------------------
+  // (host plan: from the schedule's warp table; fused step: equal cuts)
   const int gw = blockIdx.x * kDecodeWarps + warp;
-  const int64_t seg0 = (int64_t)gw * total_chunks / total_warps;
-  const int n = (int)((int64_t)(gw + 1) * total_chunks / total_warps - seg0);
+  int64_t seg0;
+  int n;
+  int first_piece = 0;
+  if constexpr (DEV) {
+    seg0 = (int64_t)gw * total_chunks / total_warps;
+    n = (int)((int64_t)(gw + 1) * total_chunks / total_warps - seg0);
+  } else {
+    const WarpSeg ws = p.warp_seg[gw];
+    seg0 = ws.seg0;
+    n = ws.n;
+    first_piece = ws.piece;
+  }
   // The piece of each position: the warp's first piece comes from the
   // schedule; a lane's cursor only moves forward as its positions grow.
   // (Fused step: the pieces are the tiles themselves -- the part of a tile
@@ -357,7 +368,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   if constexpr (DEV) {
     if (n > 0) cur_piece = __ldcg(sp.warp_tile + gw);  // the tile holding position seg0
   } else {
-    cur_piece = n > 0 ? p.warp_piece[gw] : 0;
+    cur_piece = n > 0 ? first_piece : 0;
   }
   int4 f_pc = make_int4(0, 0, 0, 0);  // req, kv_head, any_lo, any_hi
   int f_blk = -1;

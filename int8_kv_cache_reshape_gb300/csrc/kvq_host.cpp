@@ -25,15 +25,17 @@
 using kvq::DecodePiece;
 using kvq::MergeItem;
 using kvq::PrefillTile;
+using kvq::WarpSeg;
 
 // One launch of the split-KV decode kernel: the tiles with one 8-row n-tile
 // (class 0) or two (class 1).
 struct DecodeLaunch {
   int64_t piece_off = 0;   // the launch's first piece
   int64_t num_pieces = 0;
-  int64_t warp_off = 0;    // its first entry of the per-warp first-piece table
+  int64_t warp_off = 0;    // its first entry of the warp table
   int64_t num_chunks = 0;  // length of its flat chunk sequence
   int num_warps = 0;       // warps the sequence is cut among
+  bool lockstep = false;   // every kv head of a request cut at the same chunks
 };
 
 struct kvq_sched {
@@ -41,7 +43,7 @@ struct kvq_sched {
   int device;
   int64_t total_q;
   std::vector<DecodePiece> pieces;
-  std::vector<int32_t> warp_piece;  // per launch, per warp: the piece of its first chunk
+  std::vector<WarpSeg> warp_seg;  // per launch, per warp: its segment and first piece
   std::vector<MergeItem> merges;
   std::vector<PrefillTile> prefill;
   DecodeLaunch launch[2];
@@ -411,14 +413,25 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
                      return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
                    });
 
-  // 2) Stream decomposition: per class, lay the tiles' chunks end to end and
-  //    cut the sequence into equal contiguous segments, one per warp.  A
+  // 2) Work decomposition: per class, lay the tiles' chunks end to end (in
+  //    (request, kv head) order) and give each warp a contiguous segment.  A
   //    tile cut by a segment boundary becomes several pieces whose partial
-  //    rows are merged.  KVQ_DECODE_WARPS (tests, benchmarks) forces the
-  //    warp count.
+  //    rows are merged.  Two ways to cut, chosen by the cache row size:
+  //    - stream-K: equal segments of the whole sequence (perfect balance);
+  //    - head lockstep, when a row is not a whole number of 128-byte lines
+  //      (per-token-head rows of D + 16 bytes, 64-byte rows): the kv heads of
+  //      a request share the lines where their rows meet, so every head of a
+  //      request is cut at the same chunks (s_r equal pieces, one warp each)
+  //      and the warps reading neighbouring heads' rows of the same tokens
+  //      run side by side -- the second read of a shared line hits L2.  s_r
+  //      is apportioned to keep the longest piece short.
+  //    KVQ_DECODE_WARPS (tests, benchmarks) forces the warp count;
+  //    KVQ_DECODE_LOCKSTEP = 0 / 1 forces the cut.
   const int sms = have_device ? std::max(1, sm_count()) : kDefaultSmCount;
   int64_t forced = 0;
   if (const char* env = std::getenv("KVQ_DECODE_WARPS")) forced = std::atoll(env);
+  bool lockstep = kvq::row_bytes(dtype, head_dim) % 128 != 0 && heads_kv > 1;
+  if (const char* env = std::getenv("KVQ_DECODE_LOCKSTEP")) lockstep = std::atoi(env) != 0;
   s->partial_rows = 0;
   s->max_splits = 0;
   struct Cut {
@@ -429,10 +442,41 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   cuts.reserve(64);
   s->pieces.reserve(tiles[0].size() + tiles[1].size() + 2 * 4096);
   s->merges.reserve(tiles[0].size() + tiles[1].size());
+  auto add_piece = [&](const Tile& t, int64_t flat, int64_t chunk, int32_t part, int32_t merge) {
+    DecodePiece pc;
+    pc.req = t.req;
+    pc.kv_head = t.kv_head;
+    pc.row0 = t.row0;
+    pc.nrows = t.nrows;
+    pc.part = part;
+    pc.merge = merge;
+    pc.any_lo = (int32_t)t.any_lo;
+    pc.any_hi = (int32_t)t.any_hi;
+    pc.flat0 = (int32_t)flat;
+    pc.chunk0 = (int32_t)chunk;
+    pc.pad0 = pc.pad1 = 0;
+    s->pieces.push_back(pc);
+  };
+  // A merge item for a tile cut into np pieces; its partial rows follow the
+  // ones handed out so far.
+  auto add_merge = [&](const Tile& t, int64_t np) {
+    MergeItem m;
+    m.req = t.req;
+    m.kv_head = t.kv_head;
+    m.row0 = t.row0;
+    m.nrows = t.nrows;
+    m.part = (int32_t)s->partial_rows;
+    m.nsplits = (int32_t)np;
+    m.pad0 = m.pad1 = 0;
+    s->merges.push_back(m);
+    s->partial_rows += np * t.nrows;
+    s->max_splits = std::max(s->max_splits, np);
+    return (int32_t)(s->merges.size() - 1);
+  };
   for (int cls = 0; cls < 2; ++cls) {
     DecodeLaunch& dl = s->launch[cls];
     dl.piece_off = (int64_t)s->pieces.size();
-    dl.warp_off = (int64_t)s->warp_piece.size();
+    dl.warp_off = (int64_t)s->warp_seg.size();
     int64_t T = 0;
     for (const Tile& t : tiles[cls]) T += t.c_hi - t.c_lo;
     dl.num_chunks = T;
@@ -440,9 +484,77 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     const int64_t max_ctas = (int64_t)sms * kvq::decode_min_ctas(dtype, head_dim, cls + 1);
     int64_t ctas = std::min<int64_t>(max_ctas, std::max<int64_t>(1, ceil_div(T, kvq::kDecodeWarps * kvq::kMinChunksPerWarp)));
     if (forced > 0) ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(forced, kvq::kDecodeWarps), ceil_div(T, kvq::kDecodeWarps)));
-    const int64_t W = ctas * kvq::kDecodeWarps;
+    int64_t W = ctas * kvq::kDecodeWarps;
+
+    // Head lockstep needs every tile of a request to span the same chunks
+    // (true for decode tiles: one per (request, kv head)) and a warp per tile.
+    bool ls = lockstep && (int64_t)tiles[cls].size() <= W;
+    for (size_t k = 0; ls && k + 1 < tiles[cls].size(); ++k) {
+      const Tile& a = tiles[cls][k];
+      const Tile& b = tiles[cls][k + 1];
+      if (a.req == b.req && (a.c_lo != b.c_lo || a.c_hi != b.c_hi || a.row0 != b.row0)) ls = false;
+    }
+    dl.lockstep = ls;
+    if (ls) {
+      // groups: the runs of tiles of one request (its kv heads)
+      struct Grp {
+        size_t first;
+        int64_t heads, nc, splits;
+      };
+      std::vector<Grp> grps;
+      for (size_t k = 0; k < tiles[cls].size(); ++k) {
+        const Tile& t = tiles[cls][k];
+        if (grps.empty() || tiles[cls][grps.back().first].req != t.req)
+          grps.push_back(Grp{k, 0, t.c_hi - t.c_lo, 1});
+        grps.back().heads += 1;
+      }
+      // one split per tile to start; then, while warps remain, one more
+      // split for the request whose pieces are longest
+      int64_t used = (int64_t)tiles[cls].size();
+      auto longest = [](const Grp& g) { return ceil_div(g.nc, g.splits); };
+      std::vector<size_t> heap(grps.size());
+      for (size_t g = 0; g < grps.size(); ++g) heap[g] = g;
+      auto less = [&](size_t a, size_t b) { return longest(grps[a]) < longest(grps[b]); };
+      std::make_heap(heap.begin(), heap.end(), less);
+      while (!heap.empty()) {
+        std::pop_heap(heap.begin(), heap.end(), less);
+        Grp& g = grps[heap.back()];
+        if (g.splits >= g.nc || used + g.heads > W) {
+          heap.pop_back();
+          continue;
+        }
+        g.splits += 1;
+        used += g.heads;
+        std::push_heap(heap.begin(), heap.end(), less);
+      }
+      W = ceil_div(used, kvq::kDecodeWarps) * kvq::kDecodeWarps;
+      dl.num_warps = (int)W;
+      int64_t F = 0;
+      for (const Grp& g : grps) {
+        for (int64_t h = 0; h < g.heads; ++h) {
+          const Tile& t = tiles[cls][g.first + (size_t)h];
+          const int32_t merge = g.splits > 1 ? add_merge(t, g.splits) : -1;
+          const int64_t part0 = g.splits > 1 ? s->partial_rows - g.splits * t.nrows : -1;
+          for (int64_t k = 0; k < g.splits; ++k) {
+            const int64_t lo = k * g.nc / g.splits, hi = (k + 1) * g.nc / g.splits;
+            s->warp_seg.push_back(WarpSeg{(int32_t)((int64_t)s->pieces.size() - dl.piece_off),
+                                          (int32_t)(F + lo), (int32_t)(hi - lo), 0});
+            add_piece(t, F + lo, t.c_lo + lo, g.splits > 1 ? (int32_t)(part0 + k * t.nrows) : -1,
+                      merge);
+          }
+          s->max_splits = std::max(s->max_splits, g.splits);
+          F += g.nc;
+        }
+      }
+      while ((int64_t)s->warp_seg.size() < dl.warp_off + W)
+        s->warp_seg.push_back(WarpSeg{0, (int32_t)T, 0, 0});
+      dl.num_pieces = (int64_t)s->pieces.size() - dl.piece_off;
+      continue;
+    }
+
+    // Stream-K: segment w is [floor(w T / W), floor((w + 1) T / W)).
     dl.num_warps = (int)W;
-    s->warp_piece.resize((size_t)(dl.warp_off + W), 0);
+    s->warp_seg.resize((size_t)(dl.warp_off + W), WarpSeg{0, 0, 0, 0});
     // Segment starts floor(w T / W), incrementally (no divides in the loop).
     seg.resize((size_t)W + 1);
     {
@@ -458,6 +570,11 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         }
       }
     }
+    for (int64_t w = 0; w < W; ++w) {
+      WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + w)];
+      ws.seg0 = (int32_t)seg[(size_t)w];
+      ws.n = (int32_t)(seg[(size_t)w + 1] - seg[(size_t)w]);
+    }
     // Tiles and warps in one pass: w is the warp whose segment holds F.
     int64_t F = 0;  // flat position of the current tile's first chunk
     int64_t w = 0;
@@ -471,43 +588,18 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         if (hi > lo) cuts.push_back(Cut{ww, lo, hi});
       }
       const int64_t np = (int64_t)cuts.size();
-      s->max_splits = std::max(s->max_splits, np);
-      int32_t merge = -1;
-      int64_t part0 = -1;
-      if (np > 1) {
-        MergeItem m;
-        m.req = t.req;
-        m.kv_head = t.kv_head;
-        m.row0 = t.row0;
-        m.nrows = t.nrows;
-        m.part = (int32_t)s->partial_rows;
-        m.nsplits = (int32_t)np;
-        m.pad0 = m.pad1 = 0;
-        merge = (int32_t)s->merges.size();
-        s->merges.push_back(m);
-        part0 = s->partial_rows;
-        s->partial_rows += np * t.nrows;
-      }
+      const int32_t merge = np > 1 ? add_merge(t, np) : -1;
+      const int64_t part0 = np > 1 ? s->partial_rows - np * t.nrows : -1;
       for (int64_t k = 0; k < np; ++k) {
         const Cut& cu = cuts[(size_t)k];
-        DecodePiece pc;
-        pc.req = t.req;
-        pc.kv_head = t.kv_head;
-        pc.row0 = t.row0;
-        pc.nrows = t.nrows;
-        pc.part = np > 1 ? (int32_t)(part0 + k * t.nrows) : -1;
-        pc.merge = merge;
-        pc.any_lo = (int32_t)t.any_lo;
-        pc.any_hi = (int32_t)t.any_hi;
-        pc.flat0 = (int32_t)cu.lo;
-        pc.chunk0 = (int32_t)(t.c_lo + (cu.lo - F));
-        pc.pad0 = pc.pad1 = 0;
         // A warp whose segment starts inside this tile starts with this piece.
         if (seg[(size_t)cu.warp] >= F)
-          s->warp_piece[(size_t)(dl.warp_off + cu.warp)] =
+          s->warp_seg[(size_t)(dl.warp_off + cu.warp)].piece =
               (int32_t)((int64_t)s->pieces.size() - dl.piece_off);
-        s->pieces.push_back(pc);
+        add_piece(t, cu.lo, t.c_lo + (cu.lo - F), np > 1 ? (int32_t)(part0 + k * t.nrows) : -1,
+                  merge);
       }
+      s->max_splits = std::max(s->max_splits, np);
       F += nt;
     }
     dl.num_pieces = (int64_t)s->pieces.size() - dl.piece_off;
@@ -519,7 +611,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   //    memory, and a pooled device buffer for it.  The first attention call
   //    uploads it on its own stream (no synchronisation here).
   const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
-  const size_t warps_bytes = s->warp_piece.size() * sizeof(int32_t);
+  const size_t warps_bytes = s->warp_seg.size() * sizeof(WarpSeg);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
   const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
   const size_t prefill_bytes = s->prefill.size() * sizeof(PrefillTile);
@@ -545,7 +637,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     char* image = static_cast<char*>(s->h_image);
     std::memset(image, 0, total);  // merge counters and the error word start at zero
     if (pieces_bytes) std::memcpy(image + s->d_pieces_off, s->pieces.data(), pieces_bytes);
-    if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_piece.data(), warps_bytes);
+    if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_seg.data(), warps_bytes);
     if (merges_bytes) std::memcpy(image + s->d_merges_off, s->merges.data(), merges_bytes);
     if (prefill_bytes) std::memcpy(image + s->d_prefill_off, s->prefill.data(), prefill_bytes);
   }
@@ -563,6 +655,7 @@ int kvq_sched_get_plan_sizes(const kvq_sched_t* s, kvq_plan_sizes_t* out) {
   for (int c = 0; c < 2; ++c) {
     out->num_chunks[c] = s->launch[c].num_chunks;
     out->num_warps[c] = s->launch[c].num_warps;
+    out->lockstep[c] = s->launch[c].lockstep ? 1 : 0;
   }
   return KVQ_OK;
 }
@@ -601,11 +694,8 @@ int kvq_sched_export_plan(const kvq_sched_t* s, kvq_plan_piece_t* pieces, int64_
     if (warp_first_piece) {
       const int64_t base = c == 0 ? 0 : s->launch[0].num_warps;
       for (int w = 0; w < dl.num_warps; ++w) {
-        // segment w of this class: [floor(w T / W), floor((w + 1) T / W))
-        const int64_t lo = (int64_t)w * dl.num_chunks / dl.num_warps;
-        const int64_t hi = (int64_t)(w + 1) * dl.num_chunks / dl.num_warps;
-        warp_first_piece[base + w] =
-            hi > lo ? (int32_t)(dl.piece_off + s->warp_piece[(size_t)(dl.warp_off + w)]) : -1;
+        const WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + w)];
+        warp_first_piece[base + w] = ws.n > 0 ? (int32_t)(dl.piece_off + ws.piece) : -1;
       }
     }
   }
@@ -782,7 +872,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     if (dl.num_chunks == 0) continue;
     p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off) + dl.piece_off;
     p.num_pieces = (int32_t)dl.num_pieces;
-    p.warp_piece = reinterpret_cast<const int32_t*>(b + s->d_warps_off) + dl.warp_off;
+    p.warp_seg = reinterpret_cast<const WarpSeg*>(b + s->d_warps_off) + dl.warp_off;
     p.num_chunks = dl.num_chunks;
     p.num_warps = dl.num_warps;
     const int rc = kvq::launch_decode(p, s->dtype, head_dim, cls + 1, stream);

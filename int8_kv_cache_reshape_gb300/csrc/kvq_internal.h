@@ -155,6 +155,13 @@ struct DecodePiece {
 };
 static_assert(sizeof(DecodePiece) == 48, "DecodePiece layout");
 
+// One decode warp's work: the segment [seg0, seg0 + n) of its launch's flat
+// chunk sequence and the piece holding chunk seg0.
+struct WarpSeg {
+  int32_t piece, seg0, n, pad;
+};
+static_assert(sizeof(WarpSeg) == 16, "WarpSeg layout");
+
 // One merge item: the partial rows of a tile that was split along KV.
 struct MergeItem {
   int32_t req, kv_head, row0, nrows;
@@ -190,7 +197,7 @@ struct AttnParams {
   float* part_lse;             // [P]
   const DecodePiece* pieces;   // this launch's pieces, in flat order
   int32_t num_pieces;
-  const int32_t* warp_piece;   // per warp: the piece holding its first chunk
+  const struct WarpSeg* warp_seg;  // per warp: its segment and the piece of its first chunk
   int64_t num_chunks;          // length of the launch's flat chunk sequence
   int num_warps;               // warps it is cut among (grid * kDecodeWarps)
   const MergeItem* merges;

@@ -111,7 +111,7 @@ lib.kvq_sched_get_info.argtypes = [_p, _c.POINTER(SchedInfo)]
 class PlanSizes(ctypes.Structure):
     _fields_ = [("num_pieces", ctypes.c_int64), ("num_merges", ctypes.c_int64),
                 ("num_prefill_tiles", ctypes.c_int64), ("num_chunks", ctypes.c_int64 * 2),
-                ("num_warps", ctypes.c_int32 * 2)]
+                ("num_warps", ctypes.c_int32 * 2), ("lockstep", ctypes.c_int32 * 2)]
 
 
 # numpy layouts of kvq_plan_piece_t, kvq_plan_merge_t, kvq_plan_prefill_tile_t
@@ -209,7 +209,7 @@ class Sched:
             "kvq_sched_export_plan")
         return {"pieces": pieces, "warp_first_piece": warps, "merges": merges,
                 "prefill_tiles": tiles, "num_chunks": list(sz.num_chunks),
-                "num_warps": list(sz.num_warps)}
+                "num_warps": list(sz.num_warps), "lockstep": list(sz.lockstep)}
 
     def check_device(self) -> None:
         """Raise KvqError(E_TIMEOUT) if a kernel run with this schedule gave
