@@ -372,15 +372,15 @@ KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
  * A decode piece is a run of consecutive 16-token chunks of one row tile
  * (<= 16 packed rows of one kv head), streamed by one warp.  The pieces of a
  * launch class lie end to end in its flat chunk sequence, which is cut into
- * contiguous segments, one per warp; a tile cut by a segment boundary has
- * several pieces, whose partial rows a merge item combines.  Two cuts:
- * stream-K, equal segments (segment w starts at floor(w * chunks / warps)),
- * used when a cache row is a whole number of 128-byte lines; and head
- * lockstep (lockstep[c] == 1), used otherwise: every kv head of a request is
- * cut into the same number of equal pieces at the same chunks, and warp w's
- * segment is exactly piece w of the class (warps past the last piece have
- * empty segments), so the warps reading neighbouring heads' rows -- which
- * share 128-byte lines -- run side by side. */
+ * contiguous segments, one per warp (stream-K: segment w starts at
+ * floor(w * chunks / warps)); a tile cut by a segment boundary has several
+ * pieces, whose partial rows a merge item combines.  The tiles are in
+ * (request, kv head) order when a cache row is a whole number of 128-byte
+ * lines; otherwise in head lockstep (lockstep[c] == 1): kv-head-major order,
+ * a warp count that is a multiple of the kv heads (Hkv), every head's run cut
+ * at the same chunks, and segment h * (warps / Hkv) + v on warp v * Hkv + h,
+ * so the warps reading neighbouring heads' rows of the same tokens -- which
+ * share 128-byte lines -- are neighbours and run side by side. */
 typedef struct {
   int32_t launch;          /* decode launch class: 0 (tiles of <= 8 rows) or 1 */
   int32_t req, kv_head, row0, nrows;

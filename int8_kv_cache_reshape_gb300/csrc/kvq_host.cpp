@@ -18,6 +18,7 @@
 #include <atomic>
 #include <mutex>
 #include <new>
+#include <numeric>
 #include <vector>
 
 #include "kvq_internal.h"
@@ -413,25 +414,28 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
                      return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
                    });
 
-  // 2) Work decomposition: per class, lay the tiles' chunks end to end (in
-  //    (request, kv head) order) and give each warp a contiguous segment.  A
-  //    tile cut by a segment boundary becomes several pieces whose partial
-  //    rows are merged.  Two ways to cut, chosen by the cache row size:
-  //    - stream-K: equal segments of the whole sequence (perfect balance);
-  //    - head lockstep, when a row is not a whole number of 128-byte lines
-  //      (per-token-head rows of D + 16 bytes, 64-byte rows): the kv heads of
-  //      a request share the lines where their rows meet, so every head of a
-  //      request is cut at the same chunks (s_r equal pieces, one warp each)
-  //      and the warps reading neighbouring heads' rows of the same tokens
-  //      run side by side -- the second read of a shared line hits L2.  s_r
-  //      is apportioned to keep the longest piece short.
+  // 2) Work decomposition (stream-K): per class, lay the tiles' chunks end
+  //    to end and cut the sequence into equal contiguous segments, one per
+  //    warp.  A tile cut by a segment boundary becomes several pieces whose
+  //    partial rows are merged.  Tile order:
+  //    - request-major ((request, kv head) order) when a cache row is a whole
+  //      number of 128-byte lines;
+  //    - head lockstep otherwise (per-token-head rows of D + 16 bytes, 64-byte
+  //      rows), where the rows of one token's neighbouring kv heads share a
+  //      128-byte line: head-major order (every request's tile of kv head 0,
+  //      then of kv head 1, ...) with a warp count that is a multiple of the
+  //      kv heads, so every head's run of the sequence is cut at the same
+  //      chunks, and the v-th segments of all heads go to neighbouring warps.
+  //      Those warps stream the same tokens' rows side by side, and the
+  //      second read of a shared line hits L2.
   //    KVQ_DECODE_WARPS (tests, benchmarks) forces the warp count;
-  //    KVQ_DECODE_LOCKSTEP = 0 / 1 forces the cut.
+  //    KVQ_DECODE_LOCKSTEP = 0 / 1 forces the order.
   const int sms = have_device ? std::max(1, sm_count()) : kDefaultSmCount;
   int64_t forced = 0;
   if (const char* env = std::getenv("KVQ_DECODE_WARPS")) forced = std::atoll(env);
-  bool lockstep = kvq::row_bytes(dtype, head_dim) % 128 != 0 && heads_kv > 1;
+  bool lockstep = kvq::row_bytes(dtype, head_dim) % 128 != 0;
   if (const char* env = std::getenv("KVQ_DECODE_LOCKSTEP")) lockstep = std::atoi(env) != 0;
+  lockstep = lockstep && heads_kv > 1;
   s->partial_rows = 0;
   s->max_splits = 0;
   struct Cut {
@@ -481,75 +485,25 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     for (const Tile& t : tiles[cls]) T += t.c_hi - t.c_lo;
     dl.num_chunks = T;
     if (T == 0) continue;
+    // Head-major order when every request has one tile per kv head in this
+    // class (row tiles of up to 16 rows: always, for decodes).
+    bool ls = lockstep && tiles[cls].size() % (size_t)heads_kv == 0;
+    for (size_t k = 0; ls && k < tiles[cls].size(); ++k)
+      if (tiles[cls][k].kv_head != (int)(k % (size_t)heads_kv) ||
+          tiles[cls][k].req != tiles[cls][k - k % (size_t)heads_kv].req)
+        ls = false;
+    if (ls)
+      std::stable_sort(tiles[cls].begin(), tiles[cls].end(),
+                       [](const Tile& a, const Tile& b) { return a.kv_head < b.kv_head; });
+    dl.lockstep = ls;
     const int64_t max_ctas = (int64_t)sms * kvq::decode_min_ctas(dtype, head_dim, cls + 1);
     int64_t ctas = std::min<int64_t>(max_ctas, std::max<int64_t>(1, ceil_div(T, kvq::kDecodeWarps * kvq::kMinChunksPerWarp)));
     if (forced > 0) ctas = std::max<int64_t>(1, std::min<int64_t>(ceil_div(forced, kvq::kDecodeWarps), ceil_div(T, kvq::kDecodeWarps)));
     int64_t W = ctas * kvq::kDecodeWarps;
-
-    // Head lockstep needs every tile of a request to span the same chunks
-    // (true for decode tiles: one per (request, kv head)) and a warp per tile.
-    bool ls = lockstep && (int64_t)tiles[cls].size() <= W;
-    for (size_t k = 0; ls && k + 1 < tiles[cls].size(); ++k) {
-      const Tile& a = tiles[cls][k];
-      const Tile& b = tiles[cls][k + 1];
-      if (a.req == b.req && (a.c_lo != b.c_lo || a.c_hi != b.c_hi || a.row0 != b.row0)) ls = false;
-    }
-    dl.lockstep = ls;
-    if (ls) {
-      // groups: the runs of tiles of one request (its kv heads)
-      struct Grp {
-        size_t first;
-        int64_t heads, nc, splits;
-      };
-      std::vector<Grp> grps;
-      for (size_t k = 0; k < tiles[cls].size(); ++k) {
-        const Tile& t = tiles[cls][k];
-        if (grps.empty() || tiles[cls][grps.back().first].req != t.req)
-          grps.push_back(Grp{k, 0, t.c_hi - t.c_lo, 1});
-        grps.back().heads += 1;
-      }
-      // one split per tile to start; then, while warps remain, one more
-      // split for the request whose pieces are longest
-      int64_t used = (int64_t)tiles[cls].size();
-      auto longest = [](const Grp& g) { return ceil_div(g.nc, g.splits); };
-      std::vector<size_t> heap(grps.size());
-      for (size_t g = 0; g < grps.size(); ++g) heap[g] = g;
-      auto less = [&](size_t a, size_t b) { return longest(grps[a]) < longest(grps[b]); };
-      std::make_heap(heap.begin(), heap.end(), less);
-      while (!heap.empty()) {
-        std::pop_heap(heap.begin(), heap.end(), less);
-        Grp& g = grps[heap.back()];
-        if (g.splits >= g.nc || used + g.heads > W) {
-          heap.pop_back();
-          continue;
-        }
-        g.splits += 1;
-        used += g.heads;
-        std::push_heap(heap.begin(), heap.end(), less);
-      }
-      W = ceil_div(used, kvq::kDecodeWarps) * kvq::kDecodeWarps;
-      dl.num_warps = (int)W;
-      int64_t F = 0;
-      for (const Grp& g : grps) {
-        for (int64_t h = 0; h < g.heads; ++h) {
-          const Tile& t = tiles[cls][g.first + (size_t)h];
-          const int32_t merge = g.splits > 1 ? add_merge(t, g.splits) : -1;
-          const int64_t part0 = g.splits > 1 ? s->partial_rows - g.splits * t.nrows : -1;
-          for (int64_t k = 0; k < g.splits; ++k) {
-            const int64_t lo = k * g.nc / g.splits, hi = (k + 1) * g.nc / g.splits;
-            s->warp_seg.push_back(WarpSeg{(int32_t)((int64_t)s->pieces.size() - dl.piece_off),
-                                          (int32_t)(F + lo), (int32_t)(hi - lo), 0});
-            add_piece(t, F + lo, t.c_lo + lo, g.splits > 1 ? (int32_t)(part0 + k * t.nrows) : -1,
-                      merge);
-          }
-          s->max_splits = std::max(s->max_splits, g.splits);
-          F += g.nc;
-        }
-      }
-      while ((int64_t)s->warp_seg.size() < dl.warp_off + W)
-        s->warp_seg.push_back(WarpSeg{0, (int32_t)T, 0, 0});
-      dl.num_pieces = (int64_t)s->pieces.size() - dl.piece_off;
-      continue;
+    if (ls && W >= heads_kv) {
+      // a multiple of the kv head count (and of the CTA's warps)
+      const int64_t unit = (int64_t)heads_kv * kvq::kDecodeWarps / std::gcd<int64_t>(heads_kv, kvq::kDecodeWarps);
+      if (W >= unit) W = W / unit * unit;
     }
 
     // Stream-K: segment w is [floor(w T / W), floor((w + 1) T / W)).
@@ -570,8 +524,13 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         }
       }
     }
+    // Segment w goes to warp phys(w).  Head lockstep with W = Hkv * Wh: the
+    // v-th segments of all kv heads go to neighbouring warps.
+    const bool interleave = ls && W % heads_kv == 0;
+    const int64_t Wh = W / heads_kv;
+    auto phys = [&](int64_t w) { return interleave ? (w % Wh) * heads_kv + w / Wh : w; };
     for (int64_t w = 0; w < W; ++w) {
-      WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + w)];
+      WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + phys(w))];
       ws.seg0 = (int32_t)seg[(size_t)w];
       ws.n = (int32_t)(seg[(size_t)w + 1] - seg[(size_t)w]);
     }
@@ -594,7 +553,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
         const Cut& cu = cuts[(size_t)k];
         // A warp whose segment starts inside this tile starts with this piece.
         if (seg[(size_t)cu.warp] >= F)
-          s->warp_seg[(size_t)(dl.warp_off + cu.warp)].piece =
+          s->warp_seg[(size_t)(dl.warp_off + phys(cu.warp))].piece =
               (int32_t)((int64_t)s->pieces.size() - dl.piece_off);
         add_piece(t, cu.lo, t.c_lo + (cu.lo - F), np > 1 ? (int32_t)(part0 + k * t.nrows) : -1,
                   merge);

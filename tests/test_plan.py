@@ -122,32 +122,33 @@ def check_plan(seq_lens, query_lens, hq=32, hkv=8, D=128, causal=True, window=0,
     if intervals:
         assert info["workspace_bytes"] >= intervals[-1][1] * (D + 1) * 4
 
-    # each warp: stream-K -- its segment [w T / W, (w + 1) T / W) starts in
-    # its first piece; head lockstep -- warp w streams exactly piece w
+    # each warp: its stream-K segment [w T / W, (w + 1) T / W) starts in its
+    # first piece.  Head lockstep (head-major tile order, W a multiple of the
+    # kv heads): segment w = h * W / Hkv + v runs on warp v * Hkv + h.
     base = 0
     for c in (0, 1):
         W, T = plan["num_warps"][c], plan["num_chunks"][c]
-        idx = np.nonzero(P["launch"] == c)[0]
-        if plan["lockstep"][c]:
-            assert len(idx) <= W and W % 4 == 0
-            for w in range(W):
-                fp = int(plan["warp_first_piece"][base + w])
-                assert fp == (int(idx[w]) if w < len(idx) else -1)
-        else:
-            for w in range(W):
-                lo, hi = w * T // W, (w + 1) * T // W
-                fp = int(plan["warp_first_piece"][base + w])
-                if hi == lo:
-                    assert fp == -1
-                    continue
-                assert P["launch"][fp] == c
-                assert P["flat0"][fp] <= lo < P["flat0"][fp] + P["nchunks"][fp]
+        inter = plan["lockstep"][c] and W % hkv == 0
+        for w in range(W):
+            lo, hi = w * T // W, (w + 1) * T // W
+            phys = (w % (W // hkv)) * hkv + w // (W // hkv) if inter else w
+            fp = int(plan["warp_first_piece"][base + phys])
+            if hi == lo:
+                assert fp == -1
+                continue
+            assert P["launch"][fp] == c
+            assert P["flat0"][fp] <= lo < P["flat0"][fp] + P["nchunks"][fp]
         base += W
 
-    # head lockstep: every kv head of a request cut at the same chunks, into
-    # pieces whose lengths differ by at most one
+    # head lockstep: tiles in head-major order, and, when W is a multiple of
+    # the kv head count, every kv head of a request cut at the same chunks
     for c in (0, 1):
         if not plan["lockstep"][c]:
+            continue
+        idx = np.nonzero(P["launch"] == c)[0]
+        heads = P["kv_head"][idx]
+        assert np.all(np.diff(heads) >= 0)
+        if plan["num_warps"][c] % hkv:
             continue
         cuts = {}
         for key, ids in tiles.items():
@@ -155,8 +156,6 @@ def check_plan(seq_lens, query_lens, hq=32, hkv=8, D=128, causal=True, window=0,
                 continue
             cut = tuple((int(P["chunk0"][i]), int(P["nchunks"][i]))
                         for i in sorted(ids, key=lambda i: P["flat0"][i]))
-            lens = [n for _, n in cut]
-            assert max(lens) - min(lens) <= 1
             cuts.setdefault(key[0], set()).add(cut)
         assert all(len(v) == 1 for v in cuts.values())
     return plan
@@ -220,29 +219,34 @@ def test_export_refuses_small_arrays():
     s.close()
 
 
-def test_lockstep_cut_follows_the_row_size(monkeypatch):
-    """Rows that are whole 128-byte lines (fp8 at head_dim 128) are cut
-    stream-K; per-token-head rows (D + 16 bytes) and 64-byte rows in head
-    lockstep; KVQ_DECODE_LOCKSTEP forces either."""
+def test_lockstep_follows_the_row_size(monkeypatch):
+    """Rows that are whole 128-byte lines (fp8 at head_dim 128) keep the
+    request-major order; per-token-head rows (D + 16 bytes) and 64-byte rows
+    are laid out head-major with a warp count that is a multiple of the kv
+    heads; KVQ_DECODE_LOCKSTEP forces either; one kv head has nothing to lock."""
     monkeypatch.delenv("KVQ_DECODE_WARPS", raising=False)
     L, Q = _batch(11, 40, 1, 4000, mixed=False)
     assert check_plan(L, Q, 32, 8, D=128, dtype="fp8_e4m3")["lockstep"][0] == 0
-    assert check_plan(L, Q, 32, 8, D=128, dtype="int8_per_token_head")["lockstep"][0] == 1
-    assert check_plan(L, Q, 32, 8, D=64, dtype="fp8_e5m2")["lockstep"][0] == 1
+    for D, dtype in ((128, "int8_per_token_head"), (64, "fp8_e5m2")):
+        plan = check_plan(L, Q, 32, 8, D=D, dtype=dtype)
+        assert plan["lockstep"][0] == 1 and plan["num_warps"][0] % 8 == 0
+    assert check_plan(L, Q, 8, 1, D=64)["lockstep"][0] == 0
     monkeypatch.setenv("KVQ_DECODE_LOCKSTEP", "1")
     assert check_plan(L, Q, 32, 8, D=128, dtype="fp8_e4m3")["lockstep"][0] == 1
     monkeypatch.setenv("KVQ_DECODE_LOCKSTEP", "0")
-    assert check_plan(L, Q, 32, 8, D=128, dtype="int8_per_token_head")["lockstep"][0] == 0
+    plan = check_plan(L, Q, 32, 8, D=128, dtype="int8_per_token_head")
+    assert plan["lockstep"][0] == 0
+    assert list(plan["pieces"]["req"]) == sorted(plan["pieces"]["req"])
 
 
 @pytest.mark.parametrize("seed", range(4))
-def test_lockstep_pieces_are_balanced(monkeypatch, seed):
-    """The apportioned splits keep the longest piece within one chunk plus a
-    quarter of the stream-K segment length, on decode batches of mixed lengths."""
+@pytest.mark.parametrize("hkv", [2, 3, 8])
+def test_lockstep_keeps_stream_k_balance(monkeypatch, seed, hkv):
+    """Head-major order keeps the equal stream-K segments: no warp streams
+    more than one chunk above the mean, on decode batches of mixed lengths."""
     monkeypatch.delenv("KVQ_DECODE_WARPS", raising=False)
     L, Q = _batch(200 + seed, 64, 1, 8192, mixed=False)
-    plan = check_plan(L, Q, 32, 8, D=128, dtype="fp8_per_token_head")
+    plan = check_plan(L, Q, 4 * hkv, hkv, D=128, dtype="fp8_per_token_head")
     assert plan["lockstep"][0] == 1
     T, W = plan["num_chunks"][0], plan["num_warps"][0]
-    longest = int(plan["pieces"]["nchunks"].max())
-    assert longest <= math.ceil(T / W) * 1.25 + 1
+    assert int(plan["pieces"]["nchunks"].max()) <= math.ceil(T / W)
