@@ -60,16 +60,16 @@ int launch_decode_step(const AttnParams& p, const StepParams& sp, int dtype, int
 }
 
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
-                   int64_t num_tiles, void* stream) {
-  if (num_tiles <= 0) return KVQ_OK;
+                   int64_t ctas, void* stream) {
+  if (ctas <= 0) return KVQ_OK;
   const bool al = uses_alibi(p);
   switch (head_dim) {
-    case 64: return al ? launch_prefill_d64_alibi(p, maps, dtype, num_tiles, stream)
-                       : launch_prefill_d64(p, maps, dtype, num_tiles, stream);
-    case 128: return al ? launch_prefill_d128_alibi(p, maps, dtype, num_tiles, stream)
-                        : launch_prefill_d128(p, maps, dtype, num_tiles, stream);
-    case 256: return al ? launch_prefill_d256_alibi(p, maps, dtype, num_tiles, stream)
-                        : launch_prefill_d256(p, maps, dtype, num_tiles, stream);
+    case 64: return al ? launch_prefill_d64_alibi(p, maps, dtype, ctas, stream)
+                       : launch_prefill_d64(p, maps, dtype, ctas, stream);
+    case 128: return al ? launch_prefill_d128_alibi(p, maps, dtype, ctas, stream)
+                        : launch_prefill_d128(p, maps, dtype, ctas, stream);
+    case 256: return al ? launch_prefill_d256_alibi(p, maps, dtype, ctas, stream)
+                        : launch_prefill_d256(p, maps, dtype, ctas, stream);
     default: return KVQ_E_UNSUPPORTED;
   }
 }

@@ -183,21 +183,6 @@ PFN_cuTensorMapEncodeTiled_v12000 tensor_map_encoder() {
   return fn;
 }
 
-// Maps of one cache for the prefill's bulk tensor copies: {row bytes, kv
-// heads, slots} with boxes {box0, 1, 16}.
-bool encode_cache_map(CUtensorMap* map, const void* cache, int64_t row, int heads_kv, int64_t slots,
-                      uint32_t box0) {
-  PFN_cuTensorMapEncodeTiled_v12000 enc = tensor_map_encoder();
-  if (!enc) return false;
-  const cuuint64_t dims[3] = {(cuuint64_t)row, (cuuint64_t)heads_kv, (cuuint64_t)slots};
-  const cuuint64_t strides[2] = {(cuuint64_t)row, (cuuint64_t)row * (cuuint64_t)heads_kv};
-  const cuuint32_t box[3] = {box0, 1u, 16u};
-  const cuuint32_t estr[3] = {1u, 1u, 1u};
-  return enc(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides, box, estr,
-             CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE, CU_TENSOR_MAP_L2_PROMOTION_L2_128B,
-             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
-}
-
 // Map of a bf16 ("auto") cache for the prefill's bulk tensor copies:
 // {head_dim values, kv heads, slots} with boxes {64, 1, 16} written in the
 // 128-byte swizzle, i.e. straight into the tensor core's operand layout.
@@ -796,20 +781,15 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.alibi_slopes = alibi_slopes;
   p.sinks = sinks;
 
+  // bf16 rows: tensor maps for the prefill's bulk copies straight into the
+  // operand tiles (quantised rows are loaded by the converter warps).
   kvq::PrefillMaps maps;
   std::memset(&maps, 0, sizeof(maps));
-  if (!s->prefill.empty()) {
-    const int64_t row = kvq::row_bytes(s->dtype, head_dim);
+  if (!s->prefill.empty() && s->dtype == KVQ_AUTO) {
     const int64_t slots = num_blocks * (int64_t)block_size;
-    bool ok = s->dtype == KVQ_AUTO
-                  ? encode_auto_map(&maps.k, key_cache, head_dim, heads_kv, slots) &&
-                        encode_auto_map(&maps.v, value_cache, head_dim, heads_kv, slots)
-                  : encode_cache_map(&maps.k, key_cache, row, heads_kv, slots, (uint32_t)head_dim) &&
-                        encode_cache_map(&maps.v, value_cache, row, heads_kv, slots, (uint32_t)head_dim);
-    if (ok && kvq::is_per_token_head(s->dtype))
-      ok = encode_cache_map(&maps.ks, key_cache, row, heads_kv, slots, 16u) &&
-           encode_cache_map(&maps.vs, value_cache, row, heads_kv, slots, 16u);
-    if (!ok) return KVQ_E_CUDA;
+    if (!encode_auto_map(&maps.k, key_cache, head_dim, heads_kv, slots) ||
+        !encode_auto_map(&maps.v, value_cache, head_dim, heads_kv, slots))
+      return KVQ_E_CUDA;
   }
   // The first call with this schedule uploads its plan on the call's
   // stream, ahead of the kernels that read it.
@@ -823,7 +803,13 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     }
   }
   if (!s->prefill.empty()) {
-    const int rc = kvq::launch_prefill(p, maps, s->dtype, head_dim, (int64_t)s->prefill.size(), stream);
+    // One persistent CTA per SM (KVQ_PREFILL_CTAS, for tests, forces fewer),
+    // never more than tiles.
+    int64_t ctas = std::max(1, sm_count());
+    if (const char* env = std::getenv("KVQ_PREFILL_CTAS"))
+      if (std::atoll(env) > 0) ctas = std::atoll(env);
+    ctas = std::min<int64_t>(ctas, (int64_t)s->prefill.size());
+    const int rc = kvq::launch_prefill(p, maps, s->dtype, head_dim, ctas, stream);
     if (rc != KVQ_OK) return rc;
   }
   for (int cls = 0; cls < 2; ++cls) {

@@ -106,29 +106,29 @@ KVQ_HD constexpr int prefill_keys(int head_dim) { return head_dim >= 256 ? 64 : 
 // pairs); always 512.
 KVQ_HD constexpr int prefill_tmem_cols(int /*head_dim*/) { return 512; }
 // Side-data slots of the prefill (per-key scales, chunk mask, largest value
-// scale): tile j uses slot j % 4, so the converters may run two tiles
+// scale): KV tile g uses slot g % 4, so the converters may run two tiles
 // ahead of the softmax.
 constexpr int kPrefillSideSlots = 4;
-// Shared memory: 2 x K and 2 x V (keys x D f16 each); 2 x the K and V codes
-// (keys x D bytes each, as the bulk tensor copies deliver them) and their
-// 16-byte scale tails (per-token-head); 4 x the tile's key / value scales;
-// 4 x the tile's chunk mask and per-warp largest value scales (144 bytes);
-// the 128 rows' Q scales; barriers and flags (256 bytes); +1 KB for
-// 1024-byte alignment.
-// Q and O are staged through the K ring.
+// Slot tables of the prefill's KV tiles (first slot of each 16-key chunk and
+// the chunk mask), published by the copy warp up to 4 tiles ahead.
+constexpr int kPrefillSlotRing = 4;
+// Shared memory: 2 x K and 2 x V (keys x D f16 each); 4 x the tile's key /
+// value scales; 4 x the tile's chunk mask and per-warp largest value scales
+// (144 bytes); 4 x 64-byte slot tables; barriers and flags (512 bytes); +1 KB
+// for 1024-byte alignment.  (The codes go from global memory to the
+// converters' registers, Q from global memory to tensor memory and O back
+// through registers.)
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
   return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
-         2 * (size_t)kPrefillStages * prefill_keys(head_dim) * (head_dim + 16) +
-         (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillRows * 4 + 256 +
+         (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillSlotRing * 64 + 512 +
          1024;
 }
 
-// Tensor maps of the paged caches for the prefill's bulk tensor copies: a
-// cache is a rank-3 byte tensor {row bytes, kv heads, slots}; the code maps
-// copy boxes of {head_dim, 1, 16 slots}, the scale-tail maps {16, 1, 16}
-// starting at byte head_dim (per-token-head only).
-struct alignas(64) PrefillMaps {
-  CUtensorMap k, v, ks, vs;
+// Tensor maps of bf16 ("auto") caches for the prefill's bulk tensor copies:
+// a cache is a rank-3 bf16 tensor {head_dim, kv heads, slots} copied in
+// boxes of {64, 1, 16 slots} in the 128-byte swizzle.
+struct PrefillMaps {
+  CUtensorMap k, v;
 };
 
 struct PrefillTile {
@@ -276,8 +276,10 @@ int launch_decode_step(const AttnParams& p, const StepParams& sp, int dtype, int
 // Decode warps of the fused step's grid on the current device (every CTA
 // resident at once) in *warps; KVQ_OK or a KVQ_E_* status.
 int step_warps(int dtype, int head_dim, bool alibi, int max_rows, int64_t* warps);
+// The persistent prefill over p.num_prefill_tiles tiles on `ctas` CTAs
+// (at most one per SM is resident).
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,
-                   int64_t num_tiles, void* stream);
+                   int64_t ctas, void* stream);
 // Whether a launch needs the ALiBi instances of the kernels.
 inline bool uses_alibi(const AttnParams& p) { return p.alibi_slopes != nullptr; }
 }  // namespace kvq

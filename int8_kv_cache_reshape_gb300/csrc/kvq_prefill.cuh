@@ -82,54 +82,51 @@ struct PrefillGeom {
   static constexpr int kTileBytes = kN * D * 2;                     // one K or V tile (f16)
   static constexpr int kOffK = 0;                                   // stages x K tile
   static constexpr int kOffV = kOffK + kStages * kTileBytes;        // stages x V tile
-  static constexpr int kOffCodeK = kOffV + kStages * kTileBytes;   // stages x kN x D code bytes
-  static constexpr int kOffCodeV = kOffCodeK + kStages * kN * D;    // stages x kN x D code bytes
-  static constexpr int kOffTailK = kOffCodeV + kStages * kN * D;    // stages x kN x 16 (scale tails)
-  static constexpr int kOffTailV = kOffTailK + kStages * kN * 16;   // stages x kN x 16
-  // Side data of tile j, for the softmax, in slot j % kSide: per-key scales,
-  // the 16-key chunk mask and, per converter warp, the largest value scale
-  // of its keys (bits of a float >= 0).
+  // Side data of KV tile g, for the softmax, in slot g % kSide: per-key
+  // scales, the 16-key chunk mask and, per converter warp, the largest
+  // value scale of its keys (bits of a float >= 0).
   static constexpr int kSide = kPrefillSideSlots;
-  static constexpr int kOffSk = kOffTailV + kStages * kN * 16;      // kSide x kN f32
+  static constexpr int kOffSk = kOffV + kStages * kTileBytes;       // kSide x kN f32
   static constexpr int kOffSv = kOffSk + kSide * kN * 4;            // kSide x kN f32
   static constexpr int kOffSMask = kOffSv + kSide * kN * 4;         // kSide x u32
   static constexpr int kOffVMax = kOffSMask + 4 * kSide;            // kSide x 8 u32
-  static constexpr int kOffQScale = kOffVMax + 32 * kSide;          // kM f32: 2^-sh of each Q row
-  static constexpr int kOffBar = kOffQScale + kM * 4;               // mbarriers, tmem slot, flags
-  static constexpr int kBytes = kOffBar + 256;
-  // Q (kM x D, swizzled) is staged over the K ring -- or, for bf16 rows,
-  // whose first K tiles land in the K ring while Q is staged, over the
-  // (unused) code rings.
-  static constexpr int kOffQStage = kAuto ? kOffCodeK : kOffK;
-  static constexpr int kOffOStage = kOffK;  // O (kM x D bf16) staged over the K ring at the end
+  // Slot tables of KV tiles g, in entry g % kSlotRing: the first slot of
+  // each 16-key chunk (entries 0 .. kN / 16 - 1) and the chunk mask (15).
+  static constexpr int kSlotRing = kPrefillSlotRing;
+  static constexpr int kOffSlots = kOffVMax + 32 * kSide;           // kSlotRing x 16 i32
+  static constexpr int kOffBar = kOffSlots + kSlotRing * 64;        // mbarriers, tmem slot, flags
+  static constexpr int kBytes = kOffBar + 512;
   static constexpr int kColO = 0;                 // O: D fp32 columns
   static constexpr int kColS = D;                 // S buffers: kN fp32 columns each
   static constexpr int kColQ = D + 2 * kN;        // Q: D/2 columns of f16 pairs
   static constexpr int kTmemCols = prefill_tmem_cols(D);
   static_assert(kColQ + D / 2 <= kTmemCols, "tensor memory: O + 2 S buffers + Q");
-  static_assert(kM * D * 2 <= kStages * kTileBytes, "Q / O staging fits the K ring");
-  static_assert(!kAuto || kM * D * 2 <= 2 * kStages * kN * D, "Q staging fits the code rings");
-  static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0 && kOffCodeK % 1024 == 0 &&
-                    kOffCodeV % 128 == 0 && kOffTailK % 128 == 0 && kOffTailV % 128 == 0,
-                "1024-byte operand tiles, 128-byte copy destinations");
+  static_assert(kTileBytes % 1024 == 0 && kOffV % 1024 == 0, "1024-byte operand tiles");
   static_assert(kOffBar % 8 == 0, "mbarrier alignment");
   static_assert((kN + 31) / 32 <= 8 && kSide == 4, "side data space");
+  static_assert(kN / 16 <= 15 && (kSlotRing & (kSlotRing - 1)) == 0, "slot table layout");
+  static_assert(kConv >= kN && kConv % 32 == 0, "a converter thread per key, whole warps");
   static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
-  // barrier slots (8 bytes each).  K and V travel separately: the K codes
-  // of tile j + 2 are copied once K(j) is converted, K(j + 2) is converted
-  // once S(j) is complete, V(j + 2) once P(j) V(j) is.  One P barrier per
-  // S buffer: P(j+1) may be ready before PV(j) is issued.  A parity wait is
-  // unambiguous only while the waiter is at most one phase behind, so the
-  // epilogue (which may be several PVs ahead of the last phase it saw)
-  // waits on a one-shot barrier for the last PV, and the side data (which
-  // the converters may write two tiles ahead) has four slots.
-  static constexpr int kBarCodesK = 0, kBarCodesV = 2, kBarCodesKFree = 4, kBarCodesVFree = 6,
-                       kBarKFull = 8, kBarVFull = 10, kBarVEmpty = 12, kBarSFull = 14, kBarPFull = 16,
-                       kBarSide = 18, kBarODone = 22, kBarOFinal = 23, kBarDrain = 24, kNumBars = 25;
+  // barrier slots (8 bytes each).  Quantised rows: the copy warp publishes
+  // KV tile g's slot table (Slots, ring entry g % 4) once the converters
+  // released entry g - 4 (SlotsFree); K(g) is converted once S(g - 2) is
+  // complete, V(g) once P(g - 2) V(g - 2) is (KFull / VFull).  bf16 rows:
+  // bulk copies fill the K and V tiles (CodesK / CodesV).  One P barrier
+  // per S buffer: P(g+1) may be ready before PV(g) is issued.  A parity
+  // wait is unambiguous only while the waiter is at most one phase behind,
+  // so the epilogue (which may be several PVs ahead of the last phase it
+  // saw) waits on a barrier of its own for a tile's last PV (one phase per
+  // tile), and the side data (which the converters may write two tiles
+  // ahead) has four slots.  Across tiles: Q full (the softmax warps wrote
+  // the tile's Q; the tile's first S waits) and O free (the epilogue read
+  // O; the next tile's first PV waits), one phase per tile each.
+  static constexpr int kBarCodesK = 0, kBarCodesV = 2, kBarKFull = 4, kBarVFull = 6, kBarVEmpty = 8,
+                       kBarSFull = 10, kBarPFull = 12, kBarSide = 14, kBarODone = 18, kBarOFinal = 19,
+                       kBarDrain = 20, kBarQFull = 21, kBarOFree = 22, kBarSlots = 23,
+                       kBarSlotsFree = kBarSlots + kSlotRing, kNumBars = kBarSlotsFree + kSlotRing;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
-  static constexpr int kOffChunkValid = kOffAbort + 4;          // stages x u32: 16-key chunks copied
-  static_assert(kOffChunkValid + 4 * kStages <= kBytes, "flag space");
+  static_assert(kOffAbort + 4 <= kBytes, "flag space");
   static_assert(kN / 16 <= 32, "chunk mask");
 };
 
@@ -174,6 +171,14 @@ __device__ __forceinline__ void mbar_arrive(uint32_t bar) {
   asm volatile("mbarrier.arrive.release.cta.shared::cta.b64 _, [%0];" :: "r"(bar) : "memory");
 }
 
+// One arrival for the (converged) warp, after every lane's prior writes:
+// the barriers count warps.  Per-thread arrivals would put hundreds of
+// shared-memory atomics per KV tile in front of the MMA warp's polls.
+__device__ __forceinline__ void warp_arrive(uint32_t bar) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
+}
+
 // Bounded wait that also gives up when another role has aborted.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
   if (tc::mbar_try_wait(bar, parity)) return true;
@@ -197,6 +202,65 @@ __device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
   return h;
 }
 
+// This CTA's k-th tile: the longest-first tile list dealt out over the grid
+// in serpentine order (CTA b takes tile b of the first round, tile 2G-1-b of
+// the second, ...), so every CTA gets a similar amount of work.
+__device__ __forceinline__ int dealt_tile(int k) {
+  const int G = (int)gridDim.x, b = (int)blockIdx.x;
+  return k * G + ((k & 1) ? G - 1 - b : b);
+}
+
+// A tile and its run of KV tiles: kN-key tiles from kv_first (kv_lo rounded
+// down to a tile) up to kv_hi.
+template <int kN>
+struct TileRun {
+  PrefillTile t;
+  int kv_first, T;
+  __device__ __forceinline__ void set(const PrefillTile& x) {
+    t = x;
+    kv_first = (t.kv_lo / kN) * kN;
+    T = t.kv_hi > kv_first ? (t.kv_hi - kv_first + kN - 1) / kN : 0;
+  }
+};
+
+// Walks this CTA's KV tiles in order: KV tile j of its tile ordinal k
+// (tiles without keys skipped), n = the tiles with keys before this one.
+// The next tile's record is loaded a tile ahead, so that a move to it does
+// not wait for memory.
+template <int kN>
+struct KvCursor {
+  TileRun<kN> cur;
+  PrefillTile nxt;
+  int k, j, n;
+  bool valid, nxt_valid;
+  __device__ __forceinline__ void start(const AttnParams& p) {
+    k = -1;
+    n = -1;
+    nxt_valid = dealt_tile(0) < p.num_prefill_tiles;
+    if (nxt_valid) nxt = p.prefill_tiles[dealt_tile(0)];
+    next_tile(p);
+  }
+  __device__ __forceinline__ void next_tile(const AttnParams& p) {
+    valid = false;
+    while (nxt_valid) {
+      cur.set(nxt);
+      ++k;
+      const int idx = dealt_tile(k + 1);
+      nxt_valid = idx < p.num_prefill_tiles;
+      if (nxt_valid) nxt = p.prefill_tiles[idx];
+      if (cur.T > 0) {
+        valid = true;
+        ++n;
+        j = 0;
+        return;
+      }
+    }
+  }
+  __device__ __forceinline__ void advance(const AttnParams& p) {
+    if (++j >= cur.T) next_tile(p);
+  }
+};
+
 template <int DT, int D, bool AL>
 __global__ void __launch_bounds__(prefill_threads(D), 1)
     prefill_attention_kernel(const AttnParams p, const __grid_constant__ PrefillMaps maps) {
@@ -208,36 +272,34 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   uint8_t* sm = smem_raw + (base - raw);
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
-
-  // The tile record carries the request's first query token and the
-  // position of its query 0, so the Q loads depend on one load only.
-  const PrefillTile t = p.prefill_tiles[blockIdx.x];
   const int G = p.group;
-  const int q0 = t.q0;
-  const int kv_first = (t.kv_lo / kN) * kN;
-  const int T = t.kv_hi > kv_first ? (t.kv_hi - kv_first + kN - 1) / kN : 0;  // KV tiles
 
   const uint32_t bars = base + Geo::kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
   volatile uint32_t* abort_flag = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffAbort);
+  constexpr int kCopyWarp = Geo::kThreads / 32 - 1;  // issues the bulk tensor copies
 
   if (tid == 0) {
+    for (int s = 0; s < Geo::kSlotRing; ++s) {
+      tc::mbar_init(bar(Geo::kBarSlots + s), 1);
+      tc::mbar_init(bar(Geo::kBarSlotsFree + s), Geo::kConv / 32);
+    }
     for (int s = 0; s < Geo::kStages; ++s) {
       tc::mbar_init(bar(Geo::kBarCodesK + s), 1);
       tc::mbar_init(bar(Geo::kBarCodesV + s), 1);
-      tc::mbar_init(bar(Geo::kBarCodesKFree + s), Geo::kConv);
-      tc::mbar_init(bar(Geo::kBarCodesVFree + s), Geo::kConv);
-      tc::mbar_init(bar(Geo::kBarKFull + s), Geo::kConv);
-      tc::mbar_init(bar(Geo::kBarVFull + s), Geo::kConv);
+      tc::mbar_init(bar(Geo::kBarKFull + s), Geo::kConv / 32);
+      tc::mbar_init(bar(Geo::kBarVFull + s), Geo::kConv / 32);
       tc::mbar_init(bar(Geo::kBarVEmpty + s), 1);
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
-      tc::mbar_init(bar(Geo::kBarPFull + s), 128);
+      tc::mbar_init(bar(Geo::kBarPFull + s), 4);
     }
     for (int s = 0; s < Geo::kSide; ++s)
-      tc::mbar_init(bar(Geo::kBarSide + s), Geo::kAuto ? 1 : Geo::kConv);
+      tc::mbar_init(bar(Geo::kBarSide + s), Geo::kAuto ? 1 : Geo::kConv / 32);
     tc::mbar_init(bar(Geo::kBarODone), 1);
     tc::mbar_init(bar(Geo::kBarOFinal), 1);
     tc::mbar_init(bar(Geo::kBarDrain), 1);
+    tc::mbar_init(bar(Geo::kBarQFull), 4);
+    tc::mbar_init(bar(Geo::kBarOFree), 4);
     *abort_flag = 0u;
     tc::mbar_fence_init();
   }
@@ -245,438 +307,315 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     tc::tmem_alloc(base + Geo::kOffTmemSlot, Geo::kTmemCols);
     tc::tmem_relinquish();
   }
-
-  // ---- roles: warp 0 issues the MMAs, warps 4-7 run the softmax, the last
-  // warp issues the bulk tensor copies, the others convert codes to f16.
-  constexpr int kCopyWarp = Geo::kThreads / 32 - 1;  // issues the bulk tensor copies
-  const bool is_conv = (warp >= 1 && warp < 4) || (warp >= 8 && warp < kCopyWarp);
-  const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
-  const int32_t* btab = p.block_table + (int64_t)t.req * p.block_table_stride;
-  float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
-  float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
-  uint32_t* smask = reinterpret_cast<uint32_t*>(sm + Geo::kOffSMask);
-  volatile uint32_t* smask_w = smask;  // written by the copy warp for bf16 rows
-  uint32_t* vmaxw = reinterpret_cast<uint32_t*>(sm + Geo::kOffVMax);
-  volatile uint32_t* chunk_valid = reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffChunkValid);
-  // Logical key j -> (table entry, offset) without a divide: q0 = hi32(j *
-  // floor((2^32 - 1) / B)) is q or q - 1 for every 32-bit j.
-  const uint32_t bsz = (uint32_t)p.block_size;
-  const uint32_t bdiv = 0xFFFFFFFFu / bsz;
-  // Tile j's 16-key chunks: their table entries are loaded one tile ahead
-  // (fetch_chunks, whose loads nobody waits for until the copies are issued),
-  // then resolved to first slots and a mask of the chunks with a key in the
-  // tile's range and a block (resolve_chunks).
-  constexpr int kChunks = kN / 16;
-  auto fetch_chunks = [&](int j, int (&blk)[kChunks], uint32_t (&off)[kChunks]) {
-    const int kv0 = kv_first + j * kN;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      const int j0 = kv0 + 16 * c;
-      blk[c] = -1;
-      off[c] = 0;
-      if (j0 + 16 > t.kv_lo && j0 < t.kv_hi) {
-        uint32_t q = __umulhi((uint32_t)j0, bdiv);
-        uint32_t r = (uint32_t)j0 - q * bsz;
-        if (r >= bsz) {
-          ++q;
-          r -= bsz;
-        }
-        blk[c] = btab[q];
-        off[c] = r;
-      }
-    }
-  };
-  auto resolve_chunks = [&](const int (&blk)[kChunks], const uint32_t (&off)[kChunks],
-                            int (&slot0)[kChunks], uint32_t& valid) {
-    valid = 0;
-#pragma unroll
-    for (int c = 0; c < kChunks; ++c) {
-      slot0[c] = 0;
-      if (blk[c] >= 0 && (int64_t)blk[c] < p.num_blocks) {
-        valid |= 1u << c;
-        slot0[c] = blk[c] * (int)bsz + (int)off[c];  // < num_blocks * block_size < 2^31
-      }
-    }
-  };
-  // Copies of those chunks into code stage j & 1, in two groups with a
-  // barrier each: the K codes (and, per token-head, both scale tails), and
-  // the V codes.  The chunk list of each stage stays in registers (static
-  // indices, selected by the uniform stage) for the V group.
-  int kept_slot[2][kChunks];
-  uint32_t kept_valid[2] = {0u, 0u};
-  // bf16 rows ("auto"): a chunk's rows go straight into the operand tile,
-  // one {64 values, 1, 16 slots} box per 64-dim column block, which the
-  // copy writes in the 128-byte swizzle the MMAs read.  Chunks that are not
-  // copied are zeroed by the copy warp (the tile must hold no stale NaN).
-  auto zero_chunk = [&](uint32_t tile, int c) {
-    const int lane = tid & 31;
-#pragma unroll 1
-    for (int cb = 0; cb < D / 64; ++cb)
-      for (int u = lane; u < 16 * 8; u += 32)
-        sts128(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128 + u * 16), make_uint4(0, 0, 0, 0));
-  };
-  auto issue_auto = [&](uint32_t tile, const CUtensorMap* map, const int (&slot0)[kChunks],
-                        uint32_t valid, uint32_t cb_bar, bool leader) {
-    if ((valid & ((1u << kChunks) - 1u)) != ((1u << kChunks) - 1u)) {
-#pragma unroll 1
-      for (int c = 0; c < kChunks; ++c)
-        if (!((valid >> c) & 1u)) zero_chunk(tile, c);
-      tc::fence_async_smem();
-    }
-    __syncwarp();
-    if (leader) {
-      mbar_arrive_expect_tx(cb_bar, (uint32_t)__popc(valid) * 16u * D * 2u);
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c)
-        if ((valid >> c) & 1u)
-#pragma unroll
-          for (int cb = 0; cb < D / 64; ++cb)
-            tma_load_3d(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128), map, 64 * cb, t.kv_head,
-                        slot0[c], cb_bar);
-    }
-  };
-  auto issue_k = [&](int j, const int (&slot0)[kChunks], uint32_t valid, bool leader) {
-    const int st = j & 1;
-    constexpr uint32_t kChunkBytes = 16u * D + (Geo::kPth ? 2u * 16u * 16u : 0u);
-    const uint32_t cb = bar(Geo::kBarCodesK + st);
-#pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      if (s2 == st) {
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) kept_slot[s2][c] = slot0[c];
-        kept_valid[s2] = valid;
-      }
-    }
-    if constexpr (Geo::kAuto) {
-      issue_auto(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), &maps.k, slot0, valid, cb, leader);
-      // The tile's chunk mask for the softmax (side slot j % 4).
-      if (leader) smask_w[j & (Geo::kSide - 1)] = valid;
-      __syncwarp();
-      if (leader) mbar_arrive(bar(Geo::kBarSide + (j & (Geo::kSide - 1))));
-    } else if (leader) {
-      chunk_valid[st] = valid;
-      mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * kChunkBytes);
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        if ((valid >> c) & 1u) {
-          const uint32_t off = (uint32_t)(st * kN + 16 * c);
-          tma_load_3d(base + Geo::kOffCodeK + off * D, &maps.k, 0, t.kv_head, slot0[c], cb);
-          if constexpr (Geo::kPth) {
-            tma_load_3d(base + Geo::kOffTailK + off * 16, &maps.ks, D, t.kv_head, slot0[c], cb);
-            tma_load_3d(base + Geo::kOffTailV + off * 16, &maps.vs, D, t.kv_head, slot0[c], cb);
-          }
-        }
-      }
-    }
-  };
-  auto issue_v = [&](int j, bool leader) {
-    const int st = j & 1;
-    const uint32_t cb = bar(Geo::kBarCodesV + st);
-    int slot0[kChunks];
-    uint32_t valid = 0;
-#pragma unroll
-    for (int s2 = 0; s2 < 2; ++s2) {
-      if (s2 == st) {
-#pragma unroll
-        for (int c = 0; c < kChunks; ++c) slot0[c] = kept_slot[s2][c];
-        valid = kept_valid[s2];
-      }
-    }
-    if constexpr (Geo::kAuto) {
-      issue_auto(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), &maps.v, slot0, valid, cb, leader);
-    } else if (leader) {
-      mbar_arrive_expect_tx(cb, (uint32_t)__popc(valid) * 16u * D);
-#pragma unroll
-      for (int c = 0; c < kChunks; ++c) {
-        if ((valid >> c) & 1u) {
-          const uint32_t off = (uint32_t)(st * kN + 16 * c);
-          tma_load_3d(base + Geo::kOffCodeV + off * D, &maps.v, 0, t.kv_head, slot0[c], cb);
-        }
-      }
-    }
-  };
-  // The copy warp issues the copies: tiles 0 and 1 before Q is staged; then
-  // the K group of tile j + 2 once every converter has released the K codes
-  // of stage j & 1 (the V group of tile j is out by then: the chunk list is
-  // per stage), the V group once the V codes are released.  The table
-  // entries of the next tile to copy are read ahead.
-  int nk = 0, nv = 0;  // tiles whose K / V copies are issued
-  int nx_blk[kChunks];
-  uint32_t nx_off[kChunks];
-  // Run by the whole copy warp (uniform state); the leader issues.
-  auto issue_next_k = [&](bool leader) {  // K copies of tile nk (entries fetched), fetch tile nk + 1
-    int slot0[kChunks];
-    uint32_t valid;
-    resolve_chunks(nx_blk, nx_off, slot0, valid);
-    issue_k(nk, slot0, valid, leader);
-    ++nk;
-    if (nk < T) fetch_chunks(nk, nx_blk, nx_off);
-  };
-  // ---- Q tile -> staging (swizzled rows), all warps: lanes_per_row lanes
-  // hold one row (16 bytes each, coalesced); the row's largest exponent
-  // comes from a shuffle reduction over those lanes, and the row is scaled
-  // by the power of two that puts its largest |q| in [2^14, 2^15).  The
-  // loads are issued first: their latency overlaps the table reads and the
-  // first copies.
-  constexpr int kLpr = D / 8;            // lanes per row
-  constexpr int kRps = 32 / kLpr;        // rows per warp step
-  constexpr int kQWarps = Geo::kThreads / 32;
-  constexpr int kQSteps = (kM / kRps + kQWarps - 1) / kQWarps;
-  const int q_sub = (tid & 31) / kLpr, q_c = (tid & 31) % kLpr;
-  uint4 qv[kQSteps];
-#pragma unroll
-  for (int i = 0; i < kQSteps; ++i) {
-    const int m = (warp + i * kQWarps) * kRps + q_sub;
-    qv[i] = make_uint4(0, 0, 0, 0);
-    if (m < t.nrows) {
-      const int R = t.row0 + m;
-      qv[i] = *reinterpret_cast<const uint4*>(
-          p.q + ((int64_t)(q0 + R / G) * p.heads_q + t.kv_head * G + R % G) * D + 8 * q_c);
-    }
-  }
-  int blk1[kChunks];
-  uint32_t off1[kChunks];
-  if (warp == kCopyWarp && (tid & 31) == 0) {
+  if (Geo::kAuto && warp == kCopyWarp && (tid & 31) == 0) {
     // the tensor maps' descriptors, ahead of the first copies
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.k)) : "memory");
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.v)) : "memory");
-    if constexpr (Geo::kPth) {
-      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.ks)) : "memory");
-      asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.vs)) : "memory");
-    }
-  }
-  if (warp == kCopyWarp && T > 0) {
-    fetch_chunks(0, nx_blk, nx_off);
-    if (T > 1) fetch_chunks(1, blk1, off1);
-  }
-  __syncthreads();  // barriers initialised
-  if (warp == kCopyWarp && T > 0) {
-    const bool leader = elect_one();
-    int slot0[kChunks];
-    uint32_t valid;
-    resolve_chunks(nx_blk, nx_off, slot0, valid);
-    issue_k(0, slot0, valid, leader);
-    issue_v(0, leader);
-    nk = nv = 1;
-    if (T > 1) {
-      resolve_chunks(blk1, off1, slot0, valid);
-      issue_k(1, slot0, valid, leader);
-      issue_v(1, leader);
-      nk = nv = 2;
-      if (nk < T) fetch_chunks(nk, nx_blk, nx_off);
-    }
-    __syncwarp();
-  }
-  {
-    float* qscale = reinterpret_cast<float*>(sm + Geo::kOffQScale);
-#pragma unroll
-    for (int i = 0; i < kQSteps; ++i) {
-      const int m = (warp + i * kQWarps) * kRps + q_sub;
-      const uint32_t w[4] = {qv[i].x, qv[i].y, qv[i].z, qv[i].w};
-      int emax = 0;
-#pragma unroll
-      for (int k = 0; k < 4; ++k) emax = max(emax, (int)max((w[k] >> 7) & 0xFFu, (w[k] >> 23) & 0xFFu));
-#pragma unroll
-      for (int o = kLpr / 2; o > 0; o >>= 1) emax = max(emax, __shfl_xor_sync(0xffffffffu, emax, o));
-      // largest |q| < 2^(emax - 126)
-      const int sh = emax > 0 && !Geo::kAuto ? min(140 - emax, 126) : 0;
-      const float up = ldexpf(1.0f, sh);
-      if (m < kM) {
-        uint4 o = qv[i];  // bf16 rows: Q enters the bf16 MMA as it is
-        if constexpr (!Geo::kAuto) {
-          o.x = dev::pack_f16x2(dev::bf16_lo(w[0]) * up, dev::bf16_hi(w[0]) * up);
-          o.y = dev::pack_f16x2(dev::bf16_lo(w[1]) * up, dev::bf16_hi(w[1]) * up);
-          o.z = dev::pack_f16x2(dev::bf16_lo(w[2]) * up, dev::bf16_hi(w[2]) * up);
-          o.w = dev::pack_f16x2(dev::bf16_lo(w[3]) * up, dev::bf16_hi(w[3]) * up);
-        }
-        sts128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 8 * q_c), o);
-        if (q_c == 0) qscale[m] = ldexpf(1.0f, -sh);
-      }
-    }
-  }
-  __syncthreads();
-  tc::fence_after_sync();
-  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffTmemSlot);
-  const bool is_softmax = warp >= 4 && warp < 8;
-  const int m = tid - 128;  // row (softmax warps)
-  const bool row_valid = is_softmax && m < t.nrows;
-  const int R = t.row0 + (row_valid ? m : 0);
-  const uint32_t lane_base = (uint32_t)(((warp - 4) & 3) * 32) << 16;
-  if (is_softmax) {
-    // The softmax warps move Q rows (their own lanes) into tensor memory.
-#pragma unroll
-    for (int c0 = 0; c0 < D / 2; c0 += 16) {
-      uint32_t w[16];
-#pragma unroll
-      for (int q = 0; q < 4; ++q) {
-        const uint4 x = lds128(base + Geo::kOffQStage + tc::sw128_offset(kM, m, 2 * c0 + 8 * q));
-        w[4 * q] = x.x; w[4 * q + 1] = x.y; w[4 * q + 2] = x.z; w[4 * q + 3] = x.w;
-      }
-      tc::tmem_st16(tmem + Geo::kColQ + lane_base + c0, w);
-    }
-    tc::tmem_wait_st();
   }
   tc::fence_before_sync();
-  __syncthreads();  // Q is in tensor memory; the staging area is free
+  __syncthreads();  // barriers initialised, tensor memory allocated
   tc::fence_after_sync();
+  const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffTmemSlot);
+
+  // ---- roles: warp 0 issues the MMAs, warps 4-7 run the softmax, the last
+  // warp issues the bulk tensor copies, the others convert codes to f16.
+  // Every role walks the same sequence of KV tiles g = 0, 1, ... (over all
+  // of this CTA's tiles), so the rings' stages and phases follow g.
+  const bool is_conv = (warp >= 1 && warp < 4) || (warp >= 8 && warp < kCopyWarp);
+  const int ctid = warp < 4 ? tid - 32 : tid - 256 + 96;
+  float* sk = reinterpret_cast<float*>(sm + Geo::kOffSk);
+  float* sv = reinterpret_cast<float*>(sm + Geo::kOffSv);
+  uint32_t* smask = reinterpret_cast<uint32_t*>(sm + Geo::kOffSMask);
+  uint32_t* vmaxw = reinterpret_cast<uint32_t*>(sm + Geo::kOffVMax);
+  constexpr int kChunks = kN / 16;
 
   if (warp == 0) {
     // ======================= MMA issuer ========================================
     // The whole warp runs the loop with warp-uniform state (descriptors and
     // counters stay in the uniform datapath); one elected lane issues every
     // MMA (the tensor core runs one thread's MMAs in order).
-    if (T > 0) {
-      const int lane = tid & 31;
-      const bool leader = elect_one();
-      constexpr uint32_t idesc_s = Geo::kAuto ? tc::idesc_bf16(kM, kN) : tc::idesc_f16(kM, kN);
-      constexpr uint32_t idesc_o =
-          (Geo::kAuto ? tc::idesc_bf16(kM, D) : tc::idesc_f16(kM, D)) | tc::kBMajorMN;
-      auto issue_s = [&](int j) {
-        const int st = j & 1;
-        // (descriptor start addresses are in 16-byte units in the low bits)
-        const uint64_t d0 = tc::desc_sw128(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes));
-        if (leader) {
+    const bool leader = elect_one();
+    KvCursor<kN> cs;
+    cs.start(p);
+    constexpr uint32_t idesc_s = Geo::kAuto ? tc::idesc_bf16(kM, kN) : tc::idesc_f16(kM, kN);
+    constexpr uint32_t idesc_o = (Geo::kAuto ? tc::idesc_bf16(kM, D) : tc::idesc_f16(kM, D)) | tc::kBMajorMN;
+    auto issue_s = [&](int g) {
+      const int st = g & 1;
+      // (descriptor start addresses are in 16-byte units in the low bits)
+      const uint64_t d0 = tc::desc_sw128(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes));
+      if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
-            tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
-                       d0 + (uint64_t)(boff >> 4), idesc_s, kk > 0 ? 1u : 0u);
-          }
-          tc::mma_commit(bar(Geo::kBarSFull + st));
+        for (int kk = 0; kk < D / 16; ++kk) {
+          const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
+          tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
+                     d0 + (uint64_t)(boff >> 4), idesc_s, kk > 0 ? 1u : 0u);
         }
-        __syncwarp();
-      };
-      auto issue_pv = [&](int j) {
-        const int st = j & 1;
-        const uint64_t d0 =
-            tc::desc_sw128_mn(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), kN * 128, 1024);
-        if (leader) {
+        tc::mma_commit(bar(Geo::kBarSFull + st));
+      }
+      __syncwarp();
+    };
+    auto issue_pv = [&](int g, bool first, bool last) {
+      const int st = g & 1;
+      const uint64_t d0 =
+          tc::desc_sw128_mn(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), kN * 128, 1024);
+      if (leader) {
 #pragma unroll
-          for (int kk = 0; kk < kN / 16; ++kk) {
-            if constexpr (Geo::kAuto) {
-              // P = hi + lo, both bf16: round c0 of the softmax wrote the hi
-              // halves of keys c0 .. c0 + 63 to columns c0 .. c0 + 31 and the
-              // lo halves to c0 + 32 .. c0 + 63.
-              const uint32_t pc = (uint32_t)(st * kN + 64 * (kk / 4) + 8 * (kk % 4));
-              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc, d0 + (uint64_t)(kk * (2048 >> 4)),
-                         idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc + 32u,
-                         d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, 1u);
-            } else {
-              tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
-                         d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (j > 0 || kk > 0) ? 1u : 0u);
-            }
-          }
-          tc::mma_commit(bar(Geo::kBarODone));
-          tc::mma_commit(bar(Geo::kBarVEmpty + st));
-          if (j == T - 1) tc::mma_commit(bar(Geo::kBarOFinal));
-        }
-        __syncwarp();
-      };
-      // S(j) needs K(j) and PV(j-2) issued (P(j-2) shares its buffer; the
-      // tensor core runs one thread's MMAs in order).  PV(j) needs P(j) and
-      // V(j).  One warp-wide non-blocking test per pass (lane 0: K(ns) in,
-      // lane 1: P(npv), lane 2: V(npv)) and one ballot decide for the warp;
-      // everything ready is issued, PV first.
-      int ns = 0, npv = 0;
-      bool ok = true;
-      long long t_idle = clock64();
-      // (bf16 rows: the copies themselves fill K and V)
-      constexpr int kBarK = Geo::kAuto ? Geo::kBarCodesK : Geo::kBarKFull;
-      constexpr int kBarV = Geo::kAuto ? Geo::kBarCodesV : Geo::kBarVFull;
-      while (npv < T) {
-        uint32_t tb = bar(kBarK + (ns & 1)), tp = (uint32_t)((ns >> 1) & 1);
-        bool cond = ns < T && ns <= npv + 1;
-        if (lane == 1 || lane == 2) {
-          tb = bar((lane == 1 ? Geo::kBarPFull : kBarV) + (npv & 1));
-          tp = (uint32_t)((npv >> 1) & 1);
-          cond = npv < ns;
-        }
-        const bool r = tc::mbar_test_wait(tb, tp) && cond;
-        const uint32_t rb = __ballot_sync(0xffffffffu, r);
-        __syncwarp();  // orders the testing lanes' acquires before the leader's issues
-        if ((rb & 6u) == 6u) {
-          tc::fence_after_sync();
-          issue_pv(npv);
-          ++npv;
-        }
-        if (rb & 1u) {
-          tc::fence_after_sync();
-          issue_s(ns);
-          ++ns;
-        }
-        if ((rb & 1u) || (rb & 6u) == 6u) {
-          t_idle = clock64();
-        } else if (clock64() - t_idle > 20000) {  // idle a while: look for an abort
-          const bool give_up = __shfl_sync(0xffffffffu, (*abort_flag != 0u) ? 1 : 0, 0) != 0;
-          const bool timeout = __shfl_sync(0xffffffffu, (clock64() - t_idle > 2000000000LL) ? 1 : 0, 0) != 0;
-          if (give_up || timeout) {
-            if (timeout && leader) *abort_flag = 1u;
-            ok = false;
-            break;
+        for (int kk = 0; kk < kN / 16; ++kk) {
+          if constexpr (Geo::kAuto) {
+            // P = hi + lo, both bf16: round c0 of the softmax wrote the hi
+            // halves of keys c0 .. c0 + 63 to columns c0 .. c0 + 31 and the
+            // lo halves to c0 + 32 .. c0 + 63.
+            const uint32_t pc = (uint32_t)(st * kN + 64 * (kk / 4) + 8 * (kk % 4));
+            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc, d0 + (uint64_t)(kk * (2048 >> 4)),
+                       idesc_o, (!first || kk > 0) ? 1u : 0u);
+            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc + 32u,
+                       d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, 1u);
+          } else {
+            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
+                       d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (!first || kk > 0) ? 1u : 0u);
           }
         }
+        tc::mma_commit(bar(Geo::kBarODone));
+        tc::mma_commit(bar(Geo::kBarVEmpty + st));
+        if (last) tc::mma_commit(bar(Geo::kBarOFinal));
       }
-      if (!ok && leader) {
-        // Drain whatever was issued before the tensor memory is freed.
-        tc::mma_commit(bar(Geo::kBarDrain));
-        (void)tc::mbar_wait(bar(Geo::kBarDrain), 0u, 200000000LL);
-      }
+      __syncwarp();
+    };
+    // S(g) needs K(g), PV(g-2) issued (P(g-2) shares its buffer; the tensor
+    // core runs one thread's MMAs in order) and, for a tile's first KV
+    // tile, the tile's Q in tensor memory.  PV(g) needs P(g), V(g) and, for
+    // a tile's first KV tile after the CTA's first tile, O read out by the
+    // previous tile's epilogue.  So the issue order is fixed -- S(0), then
+    // per g: S(g+1), PV(g) -- and the warp waits for each barrier in turn
+    // (a blocking wait wakes as soon as the phase completes; polling several
+    // barriers costs a shared-memory round trip per pass).  At a tile
+    // boundary S(g+1) needs the next tile's Q, which the softmax writes after
+    // P(g): PV(g) goes first there.  Flags of S(g) for its PV, 4 bits in
+    // slot g % 4: first KV tile of its tile, last, the tile's ordinal (with
+    // keys) odd, ordinal 0.
+    int ns = 0;
+    uint32_t flags = 0;
+    bool ok = true;
+    // (bf16 rows: the copies themselves fill K and V)
+    constexpr int kBarK = Geo::kAuto ? Geo::kBarCodesK : Geo::kBarKFull;
+    constexpr int kBarV = Geo::kAuto ? Geo::kBarCodesV : Geo::kBarVFull;
+    auto wait = [&](int b, uint32_t parity) {
+      return __all_sync(0xffffffffu, wait_or_abort(bar(b), parity, abort_flag));
+    };
+    auto next_s = [&]() -> bool {  // S(ns) at the cursor
+      if (cs.j == 0 && !wait(Geo::kBarQFull, (uint32_t)(cs.n & 1))) return false;
+      if (!wait(kBarK + (ns & 1), (uint32_t)((ns >> 1) & 1))) return false;
+      tc::fence_after_sync();
+      issue_s(ns);
+      const uint32_t nf = (cs.j == 0 ? 1u : 0u) | (cs.j == cs.cur.T - 1 ? 2u : 0u) |
+                          ((uint32_t)(cs.n & 1) << 2) | (cs.n == 0 ? 8u : 0u);
+      flags = (flags & ~(0xFu << (4 * (ns & 3)))) | (nf << (4 * (ns & 3)));
+      ++ns;
+      cs.advance(p);
+      return true;
+    };
+    if (cs.valid) ok = next_s();
+    for (int g = 0; ok && g < ns; ++g) {
+      const bool s_after = cs.valid && cs.j == 0;  // S(g+1) starts a tile: after PV(g)
+      if (cs.valid && !s_after && !(ok = next_s())) break;
+      const uint32_t f = (flags >> (4 * (g & 3))) & 0xFu;
+      // O of the previous tile read out: its OFree completion (ordinal - 1)
+      if ((f & 1u) && !(f & 8u) && !(ok = wait(Geo::kBarOFree, ((f >> 2) & 1u) ^ 1u))) break;
+      if (!(ok = wait(Geo::kBarPFull + (g & 1), (uint32_t)((g >> 1) & 1)) &&
+                 wait(kBarV + (g & 1), (uint32_t)((g >> 1) & 1))))
+        break;
+      tc::fence_after_sync();
+      issue_pv(g, (f & 1u) != 0, (f & 2u) != 0);
+      if (s_after && !(ok = next_s())) break;
+    }
+    if (!ok && leader) {
+      // Drain whatever was issued before the tensor memory is freed.
+      tc::mma_commit(bar(Geo::kBarDrain));
+      (void)tc::mbar_wait(bar(Geo::kBarDrain), 0u, 200000000LL);
     }
     __syncwarp();
   } else if (warp == kCopyWarp) {
     // ======================= copy producer =====================================
-    // One CTA fits on an SM, so the tile that will start when this one ends
-    // is about a grid's worth of SMs later in launch order: pull its record
-    // and its Q rows into L2 now (its prologue then reads them from L2).
-    {
-      uint32_t nsm;
-      asm("mov.u32 %0, %%nsmid;" : "=r"(nsm));
-      const int nb = (int)(blockIdx.x + nsm);
-      if (nb < p.num_prefill_tiles) {
-        const PrefillTile tn = p.prefill_tiles[nb];
-        const int lane = tid & 31;
-        // rows R of the tile: token q0 + R / G, heads kv_head * G .. + G - 1
-        // contiguous (G * D * 2 bytes per token)
-        const int tok0 = tn.row0 / G, tok1 = (tn.row0 + tn.nrows - 1) / G;
-        const int64_t run = (int64_t)G * D * 2;
-        for (int tk = tok0; tk <= tok1; ++tk) {
-          const char* base_q = reinterpret_cast<const char*>(
-              p.q + ((int64_t)(tn.q0 + tk) * p.heads_q + (int64_t)tn.kv_head * G) * D);
-          for (int64_t off = (int64_t)lane * 128; off < run; off += 32 * 128)
-            asm volatile("prefetch.global.L2 [%0];" :: "l"(base_q + off));
+    // Logical key j of a tile's request -> (table entry, offset) without a
+    // divide: q0 = hi32(j * floor((2^32 - 1) / B)) is q or q - 1 for every
+    // 32-bit j.  KV tile g's 16-key chunks: their table entries are loaded
+    // one KV tile ahead (fetch_chunks, whose loads nobody waits for until
+    // they are used), then resolved to first slots and a mask of the chunks
+    // with a key in the tile's range and a block (resolve_chunks).  (A
+    // chunk's 16 slots are consecutive: the block size is a multiple of 16.)
+    const uint32_t bsz = (uint32_t)p.block_size;
+    const uint32_t bdiv = 0xFFFFFFFFu / bsz;
+    auto fetch_chunks = [&](const TileRun<kN>& r, int j, int (&blk)[kChunks], uint32_t (&off)[kChunks]) {
+      const int32_t* btab = p.block_table + (int64_t)r.t.req * p.block_table_stride;
+      const int kv0 = r.kv_first + j * kN;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        const int j0 = kv0 + 16 * c;
+        blk[c] = -1;
+        off[c] = 0;
+        if (j0 + 16 > r.t.kv_lo && j0 < r.t.kv_hi) {
+          uint32_t q = __umulhi((uint32_t)j0, bdiv);
+          uint32_t rr = (uint32_t)j0 - q * bsz;
+          if (rr >= bsz) {
+            ++q;
+            rr -= bsz;
+          }
+          blk[c] = btab[q];
+          off[c] = rr;
         }
       }
-    }
-    // Tiles 0 and 1 went out before Q was staged.  Step i copies the K codes
-    // of tile i + 1 (once K(i - 1) is converted) and then the V codes of
-    // tile i (once V(i - 2) is), the order in which the converters release
-    // them.
-    if (T > 2) {
-      const bool leader = elect_one();
-      bool ok = true;
-      for (int i = 1; i < T; ++i) {
-        // (bf16 rows: K(j) waits for S(j - 2) to complete, V(i) for
-        // P(i - 2) V(i - 2); code rows wait for the converters.)
-        constexpr int kBarKFree = Geo::kAuto ? Geo::kBarSFull : Geo::kBarCodesKFree;
-        constexpr int kBarVFree = Geo::kAuto ? Geo::kBarVEmpty : Geo::kBarCodesVFree;
-        if (i + 1 < T) {
-          const int j = i + 1;
-          ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarKFree + (j & 1)),
-                                                      (uint32_t)(((j >> 1) - 1) & 1), abort_flag));
-          if (!ok) break;
-          issue_next_k(leader);
+    };
+    auto resolve_chunks = [&](const int (&blk)[kChunks], const uint32_t (&off)[kChunks],
+                              int (&slot0)[kChunks], uint32_t& valid) {
+      valid = 0;
+#pragma unroll
+      for (int c = 0; c < kChunks; ++c) {
+        slot0[c] = 0;
+        if (blk[c] >= 0 && (int64_t)blk[c] < p.num_blocks) {
+          valid |= 1u << c;
+          slot0[c] = blk[c] * (int)bsz + (int)off[c];  // < num_blocks * block_size < 2^31
         }
-        if (i >= 2) {
-          ok = __all_sync(0xffffffffu, wait_or_abort(bar(kBarVFree + (i & 1)),
-                                                      (uint32_t)(((i >> 1) - 1) & 1), abort_flag));
-          if (!ok) break;
-          issue_v(i, leader);
+      }
+    };
+    const bool leader = elect_one();
+    KvCursor<kN> ck;
+    ck.start(p);
+    int nx_blk[kChunks];
+    uint32_t nx_off[kChunks];
+    if (ck.valid) fetch_chunks(ck.cur, 0, nx_blk, nx_off);
+    if constexpr (!Geo::kAuto) {
+      // Quantised rows: the converters load the codes themselves.  KV tile
+      // g's slot table (first slot of each chunk, then the chunk mask in
+      // entry 15) goes to ring entry g % 4 once the converters are done
+      // with KV tile g - 4's.
+      int32_t* table = reinterpret_cast<int32_t*>(sm + Geo::kOffSlots);
+      for (int g = 0; ck.valid; ++g) {
+        const int e = g & (Geo::kSlotRing - 1);
+        if (g >= Geo::kSlotRing &&
+            !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlotsFree + e),
+                                                    (uint32_t)(((g / Geo::kSlotRing) - 1) & 1), abort_flag)))
+          break;
+        int slot0[kChunks];
+        uint32_t valid;
+        resolve_chunks(nx_blk, nx_off, slot0, valid);
+        if (leader) {
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c) table[e * 16 + c] = slot0[c];
+          table[e * 16 + 15] = (int32_t)valid;
+          mbar_arrive(bar(Geo::kBarSlots + e));
+        }
+        __syncwarp();
+        ck.advance(p);
+        if (ck.valid) fetch_chunks(ck.cur, ck.j, nx_blk, nx_off);
+      }
+    } else {
+      // bf16 rows ("auto"): a chunk's rows go straight into the operand
+      // tile, one {64 values, 1, 16 slots} box per 64-dim column block, which
+      // the copy writes in the 128-byte swizzle the MMAs read.  Chunks that
+      // are not copied are zeroed by the copy warp (the tile must hold no
+      // stale NaN).  The chunk list and kv head of each stage stay in
+      // registers (static indices, selected by the uniform stage) for the V
+      // copies.
+      volatile uint32_t* smask_w = smask;
+      int kept_slot[2][kChunks];
+      uint32_t kept_valid[2] = {0u, 0u};
+      int kept_head[2] = {0, 0};
+      auto zero_chunk = [&](uint32_t tile, int c) {
+        const int lane = tid & 31;
+#pragma unroll 1
+        for (int cb = 0; cb < D / 64; ++cb)
+          for (int u = lane; u < 16 * 8; u += 32)
+            sts128(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128 + u * 16), make_uint4(0, 0, 0, 0));
+      };
+      auto issue_auto = [&](uint32_t tile, const CUtensorMap* map, int head, const int (&slot0)[kChunks],
+                            uint32_t valid, uint32_t cb_bar) {
+        if ((valid & ((1u << kChunks) - 1u)) != ((1u << kChunks) - 1u)) {
+#pragma unroll 1
+          for (int c = 0; c < kChunks; ++c)
+            if (!((valid >> c) & 1u)) zero_chunk(tile, c);
+          tc::fence_async_smem();
+        }
+        __syncwarp();
+        if (leader) {
+          mbar_arrive_expect_tx(cb_bar, (uint32_t)__popc(valid) * 16u * D * 2u);
+#pragma unroll
+          for (int c = 0; c < kChunks; ++c)
+            if ((valid >> c) & 1u)
+#pragma unroll
+              for (int cb = 0; cb < D / 64; ++cb)
+                tma_load_3d(tile + (uint32_t)(cb * kN * 128 + (16 * c) * 128), map, 64 * cb, head, slot0[c],
+                            cb_bar);
+        }
+      };
+      auto issue_k = [&](int g, int head, const int (&slot0)[kChunks], uint32_t valid) {
+        const int st = g & 1;
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          if (s2 == st) {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) kept_slot[s2][c] = slot0[c];
+            kept_valid[s2] = valid;
+            kept_head[s2] = head;
+          }
+        }
+        issue_auto(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), &maps.k, head, slot0, valid,
+                   bar(Geo::kBarCodesK + st));
+        // The tile's chunk mask for the softmax (side slot g % 4).
+        if (leader) smask_w[g & (Geo::kSide - 1)] = valid;
+        __syncwarp();
+        if (leader) mbar_arrive(bar(Geo::kBarSide + (g & (Geo::kSide - 1))));
+      };
+      auto issue_v = [&](int g) {
+        const int st = g & 1;
+        int slot0[kChunks];
+        uint32_t valid = 0;
+        int head = 0;
+#pragma unroll
+        for (int s2 = 0; s2 < 2; ++s2) {
+          if (s2 == st) {
+#pragma unroll
+            for (int c = 0; c < kChunks; ++c) slot0[c] = kept_slot[s2][c];
+            valid = kept_valid[s2];
+            head = kept_head[s2];
+          }
+        }
+        issue_auto(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), &maps.v, head, slot0, valid,
+                   bar(Geo::kBarCodesV + st));
+      };
+      // Step g copies K(g) (once S(g - 2) is complete: its buffer) and then
+      // V(g - 1) (once P(g - 3) V(g - 3) is).
+      int nk = 0, nv = 0;  // KV tiles whose K / V copies are issued
+      bool ok = true;
+      for (int g = 0;; ++g) {
+        const bool have_k = ck.valid;
+        if (have_k) {
+          if (g >= 2) {
+            ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSFull + (g & 1)),
+                                                        (uint32_t)(((g >> 1) - 1) & 1), abort_flag));
+            if (!ok) break;
+          }
+          int slot0[kChunks];
+          uint32_t valid;
+          resolve_chunks(nx_blk, nx_off, slot0, valid);
+          issue_k(g, ck.cur.t.kv_head, slot0, valid);
+          ++nk;
+          ck.advance(p);
+          if (ck.valid) fetch_chunks(ck.cur, ck.j, nx_blk, nx_off);
+        }
+        if (g >= 1) {
+          const int gv = g - 1;
+          if (gv >= 2) {
+            ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarVEmpty + (gv & 1)),
+                                                        (uint32_t)(((gv >> 1) - 1) & 1), abort_flag));
+            if (!ok) break;
+          }
+          issue_v(gv);
           ++nv;
         }
+        if (!have_k) break;
       }
       if (!ok && leader) {
-        // Let the last copies (at most two tiles of each group in flight)
+        // Let the last copies (at most two KV tiles of each group in flight)
         // land before the shared memory is released.
         for (int j = nk >= 2 ? nk - 2 : 0; j < nk; ++j)
           (void)tc::mbar_wait(bar(Geo::kBarCodesK + (j & 1)), (uint32_t)((j >> 1) & 1), 200000000LL);
@@ -689,15 +628,19 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     if constexpr (!Geo::kAuto) {
     // ======================= converters ========================================
     // A unit is (key n, 16 codes pc): consecutive threads take consecutive
-    // 16-byte pieces of a code row (conflict-free reads).  The two 16-byte f16
-    // chunks go out in the order that keeps the 8 lanes of a quarter-warp on
-    // 8 bank groups (lanes in odd 64-dim blocks store their odd chunk first).
-    // A unit's offsets do not change from tile to tile.
+    // 16-byte pieces of a key's row (coalesced loads).  The codes come from
+    // global memory into registers one KV tile ahead of their conversion (K
+    // of tile g + 1 and V of tile g while tile g is converted), so their
+    // latency hides behind a step; dead keys (outside the key range or in a
+    // chunk without a block) load as zero.  The two 16-byte f16 chunks go
+    // out in the order that keeps the 8 lanes of a quarter-warp on 8 bank
+    // groups (lanes in odd 64-dim blocks store their odd chunk first).  A
+    // unit's offsets do not change from tile to tile.
     constexpr int kPieces = D / 16;
     constexpr int kUnits = kN * kPieces;
     constexpr int kSlots = (kUnits + Geo::kConv - 1) / Geo::kConv;
+    constexpr int64_t kRow = row_bytes(DT, D);
     uint32_t code_off[kSlots], st_first[kSlots], st_second[kSlots];
-    int unit_key[kSlots];
     uint32_t odd_mask = 0;
 #pragma unroll
     for (int i = 0; i < kSlots; ++i) {
@@ -708,351 +651,504 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       code_off[i] = (uint32_t)(n * D + 16 * pc);
       st_first[i] = odd ? a_hi : a_lo;
       st_second[i] = odd ? a_lo : a_hi;
-      unit_key[i] = n;
       odd_mask |= (odd ? 1u : 0u) << i;
     }
-    auto convert = [&](int j, uint32_t tile, uint32_t codes, uint32_t valid, bool whole) {
-      const int kv0 = kv_first + j * kN;
+    const int32_t* table = reinterpret_cast<const int32_t*>(sm + Geo::kOffSlots);
+    // Codes of KV tile g (slot table entry e, kv head `head`, live keys
+    // [win & 0xFFFF, win >> 16) of the tile) into registers; returns the
+    // tile's chunk mask.
+    auto load_codes = [&](const uint8_t* cache, int e, int head, uint32_t win, uint4 (&dst)[kSlots]) {
+      const uint32_t valid = (uint32_t)table[e * 16 + 15];
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
-        if (ctid + i * Geo::kConv < kUnits) {
-          uint4 c = make_uint4(0, 0, 0, 0);
-          const int n = unit_key[i];
-          if (whole || (((valid >> (n >> 4)) & 1u) && kv0 + n >= t.kv_lo && kv0 + n < t.kv_hi))
-            c = lds128(codes + code_off[i]);
-          const bool odd = (odd_mask >> i) & 1u;
-          sts128(tile + st_first[i], codes8_to_f16<DT>(odd ? c.z : c.x, odd ? c.w : c.y));
-          sts128(tile + st_second[i], codes8_to_f16<DT>(odd ? c.x : c.z, odd ? c.y : c.w));
+        dst[i] = make_uint4(0, 0, 0, 0);
+        const int n = (int)(code_off[i] / D);
+        if (ctid + i * Geo::kConv < kUnits && ((valid >> (n >> 4)) & 1u) && n >= (int)(win & 0xFFFFu) &&
+            n < (int)(win >> 16)) {
+          const int64_t slot = table[e * 16 + (n >> 4)] + (n & 15);
+          dst[i] = dev::ldg_stream(cache + (slot * p.heads_kv + head) * kRow + (code_off[i] & (D - 1)));
+        }
+      }
+      return valid;
+    };
+    // Per token-head: key ctid's two scales (the fp32 after the codes; 0 for
+    // a dead key), loaded with the tile's K codes.
+    auto load_scales = [&](int e, int head, uint32_t win, uint32_t valid, float& ks, float& vs) {
+      ks = vs = 0.0f;
+      if constexpr (Geo::kPth) {
+        const int n = ctid;
+        if (n < kN && ((valid >> (n >> 4)) & 1u) && n >= (int)(win & 0xFFFFu) && n < (int)(win >> 16)) {
+          const int64_t off = ((int64_t)(table[e * 16 + (n >> 4)] + (n & 15)) * p.heads_kv + head) * kRow + D;
+          ks = __ldg(reinterpret_cast<const float*>(p.key_cache + off));
+          vs = __ldg(reinterpret_cast<const float*>(p.value_cache + off));
         }
       }
     };
-    // Step i converts K(i), then V(i - 1): K(i) needs S(i - 2) complete
-    // (its buffer), V(i - 1) needs P(i - 3) V(i - 3) complete, which the
-    // tensor core finishes later.  The chunk mask of a tile is read with its
-    // K codes and kept for its V codes (the issuer rewrites it for tile
-    // i + 2 once K(i) is converted).
-    uint32_t valid_k = 0, valid_v = 0;
-    bool whole_k = false, whole_v = false;
-    for (int i = 0; i <= T; ++i) {
-      if (i < T) {
-        const int st = i & 1, sd = i & (Geo::kSide - 1);
-        const int kv0 = kv_first + i * kN;
-        if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesK + st), (uint32_t)((i >> 1) & 1),
-                                                   abort_flag)))
+    auto convert = [&](uint32_t tile, const uint4 (&c)[kSlots]) {
+#pragma unroll
+      for (int i = 0; i < kSlots; ++i) {
+        if (ctid + i * Geo::kConv < kUnits) {
+          const bool odd = (odd_mask >> i) & 1u;
+          sts128(tile + st_first[i], codes8_to_f16<DT>(odd ? c[i].z : c[i].x, odd ? c[i].w : c[i].y));
+          sts128(tile + st_second[i], codes8_to_f16<DT>(odd ? c[i].x : c[i].z, odd ? c[i].y : c[i].w));
+        }
+      }
+    };
+    // A KV tile's live keys relative to its first key, packed lo | hi << 16.
+    auto window_of = [&](const KvCursor<kN>& c) {
+      const int kv0 = c.cur.kv_first + c.j * kN;
+      const int klo = min(max(c.cur.t.kv_lo - kv0, 0), kN), khi = min(max(c.cur.t.kv_hi - kv0, 0), kN);
+      return (uint32_t)klo | ((uint32_t)khi << 16);
+    };
+    // Step g: convert K(g) (its buffer is free once S(g - 2) is complete)
+    // and publish its side data; load K(g + 1); convert V(g - 1) (its buffer
+    // is free once P(g - 3) V(g - 3) is complete); load V(g), after which
+    // slot table g is released.
+    KvCursor<kN> ck;
+    ck.start(p);
+    uint4 ka[kSlots], vb[kSlots];
+    float ks_a = 0.0f, vs_a = 0.0f;
+    uint32_t valid_a = 0, win_a = 0;
+    bool ok = true;
+    if (ck.valid) {
+      ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlots), 0u, abort_flag));
+      if (ok) {
+        win_a = window_of(ck);
+        valid_a = load_codes(p.key_cache, 0, ck.cur.t.kv_head, win_a, ka);
+        load_scales(0, ck.cur.t.kv_head, win_a, valid_a, ks_a, vs_a);
+      }
+    }
+    for (int g = 0; ok; ++g) {
+      const bool have_k = ck.valid;
+      const int head_g = ck.cur.t.kv_head;
+      const uint32_t win_g = win_a;
+      if (have_k) {
+        const int st = g & 1, sd = g & (Geo::kSide - 1);
+        if (g >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSFull + st),
+                                                                    (uint32_t)(((g >> 1) - 1) & 1), abort_flag))))
           break;
-        if (i >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSFull + st),
-                                                              (uint32_t)(((i >> 1) - 1) & 1), abort_flag)))
-          break;
-        valid_k = chunk_valid[st];
-        // every key of the tile in range and copied: no per-unit checks
-        whole_k = valid_k == (1u << kChunks) - 1u && kv0 >= t.kv_lo && kv0 + kN <= t.kv_hi;
-        // Side data for the softmax in slot i % 4 (its reader, the softmax
-        // of tile i - 4, is done: S(i - 2) was issued after P(i - 4) V(i - 4)).
-        if (ctid == 0) smask[sd] = valid_k;
+        // Side data for the softmax in slot g % 4 (its reader, the softmax
+        // of KV tile g - 4, is done: S(g - 2) was issued after P(g - 4) V(g - 4)).
+        if (ctid == 0) smask[sd] = valid_a;
         if constexpr (Geo::kPth) {
-          // Per-key scales, one thread per key (0 for a key without a copied
-          // row); each converter warp publishes the largest value scale it saw.
-          float vmax = 0.0f;
-          for (int n = ctid; n < kN; n += Geo::kConv) {
-            const int jj = kv0 + n;
-            const bool live = jj >= t.kv_lo && jj < t.kv_hi && ((valid_k >> (n >> 4)) & 1u);
-            const uint32_t off = (uint32_t)((st * kN + n) * 16);
-            const float ks = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailK + off) : 0.0f;
-            const float vs = live ? *reinterpret_cast<const float*>(sm + Geo::kOffTailV + off) : 0.0f;
-            sk[sd * kN + n] = ks;
-            sv[sd * kN + n] = vs;
-            vmax = fmaxf(vmax, vs);  // stays >= 0 (a NaN or negative scale is ignored)
+          // per-key scales (0 for a dead key); each converter warp publishes
+          // the largest value scale of its keys
+          if (ctid < kN) {
+            sk[sd * kN + ctid] = ks_a;
+            sv[sd * kN + ctid] = vs_a;
           }
+          const float vmax = ctid < kN ? fmaxf(vs_a, 0.0f) : 0.0f;  // (a NaN or negative scale is ignored)
           const uint32_t wmax = __reduce_max_sync(0xffffffffu, __float_as_uint(vmax));
           // (only the first (kN + 31) / 32 converter warps hold keys)
           if ((ctid & 31) == 0 && (ctid >> 5) < (kN + 31) / 32) vmaxw[sd * 8 + (ctid >> 5)] = wmax;
         }
-        mbar_arrive(bar(Geo::kBarSide + sd));
-        convert(i, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes),
-                base + Geo::kOffCodeK + (uint32_t)(st * kN * D), valid_k, whole_k);
+        warp_arrive(bar(Geo::kBarSide + sd));
+        convert(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), ka);
         tc::fence_async_smem();
-        mbar_arrive(bar(Geo::kBarKFull + st));
-        // done with the K codes and tails of stage st
-        mbar_arrive(bar(Geo::kBarCodesKFree + st));
+        warp_arrive(bar(Geo::kBarKFull + st));
+        ck.advance(p);
+        if (ck.valid) {
+          const int e1 = (g + 1) & (Geo::kSlotRing - 1);
+          if (!(ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlots + e1),
+                                                            (uint32_t)(((g + 1) / Geo::kSlotRing) & 1), abort_flag))))
+            break;
+          win_a = window_of(ck);
+          valid_a = load_codes(p.key_cache, e1, ck.cur.t.kv_head, win_a, ka);
+          load_scales(e1, ck.cur.t.kv_head, win_a, valid_a, ks_a, vs_a);
+        }
       }
-      if (i >= 1) {
-        const int jv = i - 1, st = jv & 1;
-        if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarCodesV + st), (uint32_t)((jv >> 1) & 1),
-                                                   abort_flag)))
+      if (g >= 1) {
+        const int gv = g - 1, st = gv & 1;
+        if (gv >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarVEmpty + st),
+                                                                     (uint32_t)(((gv >> 1) - 1) & 1), abort_flag))))
           break;
-        if (jv >= 2 && !__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarVEmpty + st),
-                                                               (uint32_t)(((jv >> 1) - 1) & 1), abort_flag)))
-          break;
-        convert(jv, base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes),
-                base + Geo::kOffCodeV + (uint32_t)(st * kN * D), valid_v, whole_v);
+        convert(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), vb);
         tc::fence_async_smem();
-        mbar_arrive(bar(Geo::kBarVFull + st));
-        mbar_arrive(bar(Geo::kBarCodesVFree + st));
+        warp_arrive(bar(Geo::kBarVFull + st));
       }
-      valid_v = valid_k;
-      whole_v = whole_k;
+      if (!have_k) break;
+      const int e = g & (Geo::kSlotRing - 1);
+      (void)load_codes(p.value_cache, e, head_g, win_g, vb);
+      warp_arrive(bar(Geo::kBarSlotsFree + e));
     }
     }
     __syncwarp();
   } else {
     // ======================= softmax ===========================================
-    const float* sk = reinterpret_cast<const float*>(sm + Geo::kOffSk);
-    const float* sv = reinterpret_cast<const float*>(sm + Geo::kOffSv);
-    const uint32_t* smask = reinterpret_cast<const uint32_t*>(sm + Geo::kOffSMask);
-    const uint32_t* vmaxw = reinterpret_cast<const uint32_t*>(sm + Geo::kOffVMax);
     constexpr uint32_t kAllChunks = (kChunks >= 32) ? 0xFFFFFFFFu : ((1u << kChunks) - 1u);
     constexpr int kVMaxSlots = (kN + 31) / 32;  // converter warps that hold keys
-    const int pos = t.pos0 + R / G;
-    const int W = p.window;
-    // (without causality every row sees the request's L keys: the tile's kv_hi)
-    const int row_hi = row_valid ? (p.causal ? pos + 1 : t.kv_hi) : 0;  // padding rows see nothing
-    const int row_lo = W > 0 ? pos - W + 1 : 0;
+    const int m = tid - 128;  // row (tensor-memory lane m)
+    const uint32_t lane_base = (uint32_t)(((warp - 4) & 3) * 32) << 16;
     const float log2e = 1.4426950408889634f;
     const float cap = p.soft_cap;
-    // scores in log2 units (natural units under a soft cap, which converts)
-    const float q_unscale = reinterpret_cast<const float*>(sm + Geo::kOffQScale)[m];  // 2^-sh
-    const float score_mul = p.sm_scale * q_unscale * (cap > 0.0f ? 1.0f : log2e) *
-                            (Geo::kPth || Geo::kAuto ? 1.0f : p.k_scale);
-    // ALiBi: this row's slope in log2 units (the bias uses the exact integer
-    // distance key - position, added after the soft cap).
-    const float al_slope = AL ? p.alibi_slopes[t.kv_head * G + R % G] * log2e : 0.0f;
     const float cap_l2 = cap * log2e;
     const float inv_cap = cap > 0.0f ? 1.0f / cap : 0.0f;
-    // m_ref: the reference maximum, an integer (log2 units) once set, so
-    // that moving it scales weights, O and l by exact powers of two.
-    float m_ref = -INFINITY, l_sum = 0.0f;
-    int ev = -1000;  // exponent of the value-scale reference (per-token-head)
-    bool ok = true;
-    for (int j = 0; j < T; ++j) {
-      const int st = j & 1;
-      const int kv0 = kv_first + j * kN;
-      const int sd = j & (Geo::kSide - 1);
-      // S(j) is in tensor memory; tile j's side data is in slot sd.
-      ok = wait_or_abort(bar(Geo::kBarSFull + st), (uint32_t)((j >> 1) & 1), abort_flag) &&
-           wait_or_abort(bar(Geo::kBarSide + sd), (uint32_t)((j >> 2) & 1), abort_flag);
-      ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory accesses are collective
-      if (!ok) break;
-      tc::fence_after_sync();
-      const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN) + lane_base;
-      // Visible keys n of this row: lo_n <= n < hi_n, in a 16-key chunk
-      // that was copied.  Masks are needed unless every row of the warp
-      // sees the whole tile and every chunk is in.
-      const uint32_t cmask = smask[sd];
-      const int lo_n = row_lo - kv0, hi_n = row_hi - kv0;
-      const bool full = __all_sync(0xffffffffu, lo_n <= 0 && hi_n >= kN) && cmask == kAllChunks;
-      float alpha = 1.0f;  // factor for O (score reference and value reference)
-      // Value-scale reference (per-token-head): the largest exponent so far.
-      float v_mul = 1.0f;  // 2^-ev
-      if constexpr (Geo::kPth) {
-        uint32_t mb = 0;
-#pragma unroll
-        for (int w = 0; w < kVMaxSlots; ++w) mb = max(mb, vmaxw[sd * 8 + w]);
-        const float smax = __uint_as_float(mb);
-        if (smax > 0.0f) {
-          int e;
-          (void)frexpf(smax, &e);  // smax < 2^e
-          if (e > ev) {
-            if (ev > -1000) alpha = ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
-            ev = e;
-          }
-        }
-        v_mul = ldexpf(1.0f, -ev);
+    const int W = p.window;
+    // Output row m of a tile, bf16: D values from `dst` (null: not a row).
+    auto out_row = [&](const PrefillTile& t) -> uint16_t* {
+      if (m >= t.nrows) return nullptr;
+      const int Rr = t.row0 + m;
+      return p.out + ((int64_t)(t.q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D;
+    };
+    // Tiles without keys (an empty key range) get zero rows as they are passed.
+    auto zero_rows = [&](const PrefillTile& t) {
+      uint16_t* dst = out_row(t);
+      if (dst)
+        for (int c = 0; c < D / 8; ++c) reinterpret_cast<uint4*>(dst)[c] = make_uint4(0, 0, 0, 0);
+    };
+    // Next tile with keys after ordinal k (k moves to it); false: none.
+    auto next_run = [&](int& k, TileRun<kN>& r) -> bool {
+      while (true) {
+        const int idx = dealt_tile(++k);
+        if (idx >= p.num_prefill_tiles) return false;
+        r.set(p.prefill_tiles[idx]);
+        if (r.T > 0) return true;
+        zero_rows(r.t);
       }
-      // The score in log2 units from r (the raw score, times the key's scale
-      // per token-head; -inf when masked).  Under a cap, masked r stays
-      // masked (a capped -inf would be finite).
-      auto score = [&](auto cap_c, float r) -> float {
-        if constexpr (decltype(cap_c)::value)
-          return r == -INFINITY ? -INFINITY : cap_l2 * dev::tanh_exp(r * score_mul * inv_cap);
-        else
-          return r * score_mul;
-      };
-      // 64 scores from column c0: r in place, the row's maximum of r.  With
-      // ALiBi the bias differs per key, so the final scores (log2 units) are
-      // stored and maximised instead.
-      auto raw64 = [&](auto full_c, uint32_t* v, int c0) -> float {
-        const float* skp = sk + sd * kN + c0;
-        const int lo = lo_n - c0, hi = hi_n - c0;
-        const uint32_t cm = cmask >> (c0 >> 4);
-        const int dist0 = kv0 + c0 - pos;  // key - position of column c0
-        float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+    };
+    // Q row m of a tile -> tensor memory (columns kColQ.., f16 pairs), and
+    // the arrival that lets the tile's first S go.  Q enters as f16 exactly:
+    // the row is scaled by the power of two that puts its largest |q| in
+    // [2^14, 2^15) (a bf16 significand fits in f16's).  Elements more than
+    // 2^28 below the row's largest land in f16's subnormal range (bits lost)
+    // or flush to zero: a Q row with that dynamic range loses them.  The
+    // raw bf16 row goes to tensor memory first (batches of 8 16-byte loads,
+    // two batches in flight) while its largest exponent is found; then it is
+    // converted in place.  bf16 rows ("auto") enter the bf16 MMA as they
+    // are.  Returns the row's 2^-shift.
+    auto load_q = [&](const TileRun<kN>& r) -> float {
+      constexpr int kQv = D / 8;               // 16-byte pieces of a row
+      constexpr int kB = kQv < 8 ? kQv : 8;    // pieces per batch
+      const PrefillTile& t = r.t;
+      const bool valid = m < t.nrows;
+      const int Rq = t.row0 + (valid ? m : 0);
+      const uint4* src = reinterpret_cast<const uint4*>(
+          p.q + ((int64_t)(t.q0 + Rq / G) * p.heads_q + t.kv_head * G + Rq % G) * D);
+      int emax = 0;
+      uint4 qa[kB];
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
-          if constexpr (Geo::kPth) {
-            const float2 k2 = *reinterpret_cast<const float2*>(skp + e);
-            r0 *= k2.x;
-            r1 *= k2.y;
-          }
-          if constexpr (AL) {
-            if (cap > 0.0f) {
-              r0 = cap_l2 * dev::tanh_exp(r0 * score_mul * inv_cap);
-              r1 = cap_l2 * dev::tanh_exp(r1 * score_mul * inv_cap);
-            } else {
-              r0 *= score_mul;
-              r1 *= score_mul;
-            }
-            r0 = fmaf(al_slope, (float)(dist0 + e), r0);
-            r1 = fmaf(al_slope, (float)(dist0 + e + 1), r1);
-          }
-          if constexpr (!decltype(full_c)::value) {
-            const bool in = (cm >> (e >> 4)) & 1u;
-            r0 = in && e >= lo && e < hi ? r0 : -INFINITY;
-            r1 = in && e + 1 >= lo && e + 1 < hi ? r1 : -INFINITY;
-          }
-          v[e] = __float_as_uint(r0);
-          v[e + 1] = __float_as_uint(r1);
-          mx4[(e >> 1) & 3] = fmaxf(mx4[(e >> 1) & 3], fmaxf(r0, r1));
-        }
-        return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
-      };
-      // P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs: the 2^6 lifts small
-      // weights clear of the f16 subnormal range; l carries the same factor.
-      float lsum_tile = 0.0f;
-      auto weights64 = [&](auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
-        const float* svp = sv + sd * kN + c0;
-        float ls0 = 0.0f, ls1 = 0.0f;
+      for (int c = 0; c < kB; ++c) qa[c] = valid ? src[c] : make_uint4(0, 0, 0, 0);
 #pragma unroll
-        for (int e = 0; e < 64; e += 2) {
-          const float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
-          float p0, p1;
-          if constexpr (AL) {  // v holds the final scores
-            p0 = dev::fast_exp2(r0 - ref);
-            p1 = dev::fast_exp2(r1 - ref);
-          } else if constexpr (decltype(cap_c)::value) {
-            p0 = dev::fast_exp2(score(cap_c, r0) - ref);
-            p1 = dev::fast_exp2(score(cap_c, r1) - ref);
-          } else {
-            p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
-            p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
-          }
-          ls0 += p0;
-          ls1 += p1;
-          if constexpr (Geo::kPth) {
-            const float2 v2 = *reinterpret_cast<const float2*>(svp + e);
-            p0 *= v2.x * v_mul;
-            p1 *= v2.y * v_mul;
-          }
-          if constexpr (Geo::kAuto) {
-            // bf16 MMA: P = hi + lo, both bf16 (16 significant bits); hi in
-            // pw[0 .. 31], lo in pw[32 .. 63].
-            const uint32_t h = dev::pack_bf16x2(p0, p1);
-            pw[e / 2] = h;
-            pw[32 + e / 2] = dev::pack_bf16x2(p0 - dev::bf16_lo(h), p1 - dev::bf16_hi(h));
-          } else {
-            pw[e / 2] = dev::pack_f16x2(p0, p1);
+      for (int b = 0; b < kQv / kB; ++b) {
+        uint4 qb[kB];
+#pragma unroll
+        for (int c = 0; c < kB; ++c)
+          qb[c] = valid && b + 1 < kQv / kB ? src[(b + 1) * kB + c] : make_uint4(0, 0, 0, 0);
+        uint32_t w[4 * kB];
+#pragma unroll
+        for (int c = 0; c < kB; ++c) {
+          const uint32_t x[4] = {qa[c].x, qa[c].y, qa[c].z, qa[c].w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            w[4 * c + e] = x[e];
+            emax = max(emax, (int)max((x[e] >> 7) & 0xFFu, (x[e] >> 23) & 0xFFu));
           }
         }
-        lsum_tile += ls0 + ls1;
-      };
-      // One pass over the row, 64 scores per tensor-memory round trip: the
-      // round's maximum, then its weights against the reference, written
-      // as f16 pairs over columns of S(j) already read.  A round maximum
-      // more than 2^8 above the reference moves it (lazily) to the next
-      // integer at or above; weights already written in this tile are then
-      // scaled by the same power of two.
-#pragma unroll 1
-      for (int c0 = 0; c0 < kN; c0 += 64) {
-        uint32_t v[64];
-        tc::tmem_ld32(tmem_s + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
-        tc::tmem_ld32(tmem_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
-        tc::tmem_wait_ld();
-        const float mr = full ? raw64(std::true_type{}, v, c0) : raw64(std::false_type{}, v, c0);
-        // the score is monotonic in r (score_mul > 0, tanh increasing); with
-        // ALiBi mr is the largest final score already
-        const float mx = AL ? mr : cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
-        float a = 1.0f;
-        if (mx > m_ref + 8.0f) {
-          const float nref = ceilf(mx);
-          if (m_ref != -INFINITY) a = ldexpf(1.0f, (int)fmaxf(m_ref - nref, -200.0f));
-          m_ref = nref;
-          alpha *= a;
-          l_sum *= a;
-          lsum_tile *= a;
-        }
-        const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
-        constexpr int kPw = Geo::kAuto ? 64 : 32;  // P words of the round (bf16: hi and lo)
-        uint32_t pw[kPw];
-        if (cap > 0.0f)
-          weights64(std::true_type{}, v, c0, ref, pw);
-        else
-          weights64(std::false_type{}, v, c0, ref, pw);
-        // f16 P of the round goes to columns c0 / 2 .. c0 / 2 + 31; bf16 hi
-        // and lo halves to c0 .. c0 + 63 (the columns this round read).
-        const int pcol = Geo::kAuto ? c0 : c0 / 2;
 #pragma unroll
-        for (int h = 0; h < kPw; h += 16)
-          tc::tmem_st16(tmem_s + pcol + h, *reinterpret_cast<uint32_t(*)[16]>(pw + h));
-        if (c0 > 0 && __any_sync(0xffffffffu, a != 1.0f)) {
-          // Weights of the earlier rounds against the new reference: a
-          // power-of-two scaling, exact unless subnormal.
-          tc::tmem_wait_st();
-#pragma unroll 1
-          for (int c = 0; c < pcol; c += 32) {
-            uint32_t w[32];
-            tc::tmem_ld32(tmem_s + c, w);
-            tc::tmem_wait_ld();
+        for (int h = 0; h < 4 * kB; h += 16)
+          tc::tmem_st16(tmem + Geo::kColQ + lane_base + (uint32_t)(b * 4 * kB + h),
+                        *reinterpret_cast<uint32_t(*)[16]>(w + h));
 #pragma unroll
-            for (int e = 0; e < 32; ++e) {
-              if constexpr (Geo::kAuto) {
-                w[e] = dev::pack_bf16x2(dev::bf16_lo(w[e]) * a, dev::bf16_hi(w[e]) * a);
-              } else {
-                const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
-                w[e] = dev::pack_f16x2(f.x * a, f.y * a);
-              }
-            }
-            tc::tmem_st32(tmem_s + c, w);
-          }
-        }
-      }
-      l_sum += lsum_tile;
-      // A moved reference rescales O: PV(j-1) must be complete first.  (S(j)
-      // being complete implies PV(j-2) is, and PV(j) waits for this tile's
-      // P, so the barrier is at completion j-1 or j: the wait is exact.)
-      if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
-        ok = __all_sync(0xffffffffu,
-                        wait_or_abort(bar(Geo::kBarODone), (uint32_t)((j - 1) & 1), abort_flag));
-        if (!ok) break;
-        tc::fence_after_sync();
-#pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
-          tc::tmem_wait_ld();
-#pragma unroll
-          for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-          tc::tmem_st32(tmem + Geo::kColO + lane_base + c0, v);
-        }
+        for (int c = 0; c < kB; ++c) qa[c] = qb[c];
       }
       tc::tmem_wait_st();
-      tc::fence_before_sync();
-      mbar_arrive(bar(Geo::kBarPFull + st));
-    }
-    // ---- epilogue: O / l -> bf16 -------------------------------------------
-    if (ok && T > 0)
-      ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarOFinal), 0u, abort_flag));
-    // ok is warp-uniform here: the whole warp reads O (tcgen05.ld is a
-    // warp-collective instruction).  Each thread writes its row in bf16 to
-    // the (now idle) K ring, row-major with the 16-byte chunks of row m
-    // rotated by m mod 8; all warps then copy the tile out coalesced.
-    if (ok) {
-      const uint32_t orow = base + Geo::kOffOStage + (uint32_t)(m * D * 2);
-      if (T > 0) {
-        tc::fence_after_sync();
-        // An attention sink joins the normaliser (the weights carry
-        // 2^-(m_ref - 6)).
-        if (p.sinks && row_valid && m_ref != -INFINITY) {
-          const float sk = p.sinks[t.kv_head * G + R % G] * log2e;
-          if (sk != -INFINITY) l_sum += exp2f(fminf(sk - m_ref + 6.0f, 126.0f));
-        }
-        const float sc = (l_sum > 0.0f ? 1.0f / l_sum : 0.0f) *
-                         (Geo::kPth ? (ev > -1000 ? ldexpf(1.0f, ev) : 0.0f)
-                                    : Geo::kAuto ? 1.0f : p.v_scale);
+      // largest |q| < 2^(emax - 126)
+      const int sh = emax > 0 && !Geo::kAuto ? min(140 - emax, 126) : 0;
+      if constexpr (!Geo::kAuto) {
+        const float up = ldexpf(1.0f, sh);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D; c0 += 32) {
-          uint32_t v[32];
-          tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
+        for (int c0 = 0; c0 < D / 2; c0 += 32) {
+          uint32_t w[32];
+          tc::tmem_ld32(tmem + Geo::kColQ + lane_base + (uint32_t)c0, w);
           tc::tmem_wait_ld();
+#pragma unroll
+          for (int e = 0; e < 32; ++e) w[e] = dev::pack_f16x2(dev::bf16_lo(w[e]) * up, dev::bf16_hi(w[e]) * up);
+          tc::tmem_st32(tmem + Geo::kColQ + lane_base + (uint32_t)c0, w);
+        }
+        tc::tmem_wait_st();
+      }
+      tc::fence_before_sync();
+      warp_arrive(bar(Geo::kBarQFull));
+      return ldexpf(1.0f, -sh);
+    };
+
+    TileRun<kN> cur;
+    int k = -1;
+    bool have = next_run(k, cur);
+    float q_unscale = have ? load_q(cur) : 1.0f;
+    bool ok = true;
+    int g = 0;
+    for (int n = 0; have; ++n) {
+      // The next tile with keys (its record is read again after this tile's
+      // loop, from L1: only its ordinal stays in registers).
+      int k2 = k;
+      {
+        TileRun<kN> nxt;
+        if (!next_run(k2, nxt)) k2 = -1;
+        const bool have_next = k2 >= 0;
+        if (have_next && m < nxt.t.nrows) {
+          // the next tile's Q row into L2 now (its load then comes from L2)
+          const int Rn = nxt.t.row0 + m;
+          const char* qn = reinterpret_cast<const char*>(
+              p.q + ((int64_t)(nxt.t.q0 + Rn / G) * p.heads_q + nxt.t.kv_head * G + Rn % G) * D);
+#pragma unroll
+          for (int off = 0; off < D * 2; off += 128) asm volatile("prefetch.global.L2 [%0];" :: "l"(qn + off));
+        }
+      }
+      const PrefillTile& t = cur.t;
+      const int kv_first = cur.kv_first, T = cur.T;
+      const bool row_valid = m < t.nrows;
+      const int R = t.row0 + (row_valid ? m : 0);
+      const int pos = t.pos0 + R / G;
+
+      // (without causality every row sees the request's L keys: the tile's kv_hi)
+      const int row_hi = row_valid ? (p.causal ? pos + 1 : t.kv_hi) : 0;  // padding rows see nothing
+      const int row_lo = W > 0 ? pos - W + 1 : 0;
+      // scores in log2 units (natural units under a soft cap, which converts)
+      const float score_mul = p.sm_scale * q_unscale * (cap > 0.0f ? 1.0f : log2e) *
+                              (Geo::kPth || Geo::kAuto ? 1.0f : p.k_scale);
+      // ALiBi: this row's slope in log2 units (the bias uses the exact integer
+      // distance key - position, added after the soft cap).
+      const float al_slope = AL ? p.alibi_slopes[t.kv_head * G + R % G] * log2e : 0.0f;
+      // m_ref: the reference maximum, an integer (log2 units) once set, so
+      // that moving it scales weights, O and l by exact powers of two.
+      float m_ref = -INFINITY, l_sum = 0.0f;
+      int ev = -1000;  // exponent of the value-scale reference (per-token-head)
+      for (int j = 0; j < T; ++j, ++g) {
+        const int st = g & 1;
+        const int kv0 = kv_first + j * kN;
+        const int sd = g & (Geo::kSide - 1);
+        // S(g) is in tensor memory; KV tile g's side data is in slot sd.
+        ok = wait_or_abort(bar(Geo::kBarSFull + st), (uint32_t)((g >> 1) & 1), abort_flag) &&
+             wait_or_abort(bar(Geo::kBarSide + sd), (uint32_t)((g >> 2) & 1), abort_flag);
+        ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory accesses are collective
+        if (!ok) break;
+        tc::fence_after_sync();
+        const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN) + lane_base;
+        // Visible keys n of this row: lo_n <= n < hi_n, in a 16-key chunk
+        // that was copied.  Masks are needed unless every row of the warp
+        // sees the whole tile and every chunk is in.
+        const uint32_t cmask = smask[sd];
+        const int lo_n = row_lo - kv0, hi_n = row_hi - kv0;
+        const bool full = __all_sync(0xffffffffu, lo_n <= 0 && hi_n >= kN) && cmask == kAllChunks;
+        float alpha = 1.0f;  // factor for O (score reference and value reference)
+        // Value-scale reference (per-token-head): the largest exponent so far.
+        float v_mul = 1.0f;  // 2^-ev
+        if constexpr (Geo::kPth) {
+          uint32_t mb = 0;
+#pragma unroll
+          for (int w = 0; w < kVMaxSlots; ++w) mb = max(mb, vmaxw[sd * 8 + w]);
+          const float smax = __uint_as_float(mb);
+          if (smax > 0.0f) {
+            int e;
+            (void)frexpf(smax, &e);  // smax < 2^e
+            if (e > ev) {
+              if (ev > -1000) alpha = ldexpf(1.0f, ev - e);  // O was accumulated against 2^ev
+              ev = e;
+            }
+          }
+          v_mul = ldexpf(1.0f, -ev);
+        }
+        auto score = [&](auto cap_c, float r) -> float {
+          if constexpr (decltype(cap_c)::value)
+            return r == -INFINITY ? -INFINITY : cap_l2 * dev::tanh_exp(r * score_mul * inv_cap);
+          else
+            return r * score_mul;
+        };
+        // 64 scores from column c0: r in place, the row's maximum of r.  With
+        // ALiBi the bias differs per key, so the final scores (log2 units) are
+        // stored and maximised instead.
+        auto raw64 = [&](auto full_c, uint32_t* v, int c0) -> float {
+          const float* skp = sk + sd * kN + c0;
+          const int lo = lo_n - c0, hi = hi_n - c0;
+          const uint32_t cm = cmask >> (c0 >> 4);
+          const int dist0 = kv0 + c0 - pos;  // key - position of column c0
+          float mx4[4] = {-INFINITY, -INFINITY, -INFINITY, -INFINITY};
+  #pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
+            if constexpr (Geo::kPth) {
+              const float2 k2 = *reinterpret_cast<const float2*>(skp + e);
+              r0 *= k2.x;
+              r1 *= k2.y;
+            }
+            if constexpr (AL) {
+              if (cap > 0.0f) {
+                r0 = cap_l2 * dev::tanh_exp(r0 * score_mul * inv_cap);
+                r1 = cap_l2 * dev::tanh_exp(r1 * score_mul * inv_cap);
+              } else {
+                r0 *= score_mul;
+                r1 *= score_mul;
+              }
+              r0 = fmaf(al_slope, (float)(dist0 + e), r0);
+              r1 = fmaf(al_slope, (float)(dist0 + e + 1), r1);
+            }
+            if constexpr (!decltype(full_c)::value) {
+              const bool in = (cm >> (e >> 4)) & 1u;
+              r0 = in && e >= lo && e < hi ? r0 : -INFINITY;
+              r1 = in && e + 1 >= lo && e + 1 < hi ? r1 : -INFINITY;
+            }
+            v[e] = __float_as_uint(r0);
+            v[e + 1] = __float_as_uint(r1);
+            mx4[(e >> 1) & 3] = fmaxf(mx4[(e >> 1) & 3], fmaxf(r0, r1));
+          }
+          return fmaxf(fmaxf(mx4[0], mx4[1]), fmaxf(mx4[2], mx4[3]));
+        };
+        // P = 2^(z - m_ref + 6) <= 2^14 in f16 pairs: the 2^6 lifts small
+        // weights clear of the f16 subnormal range; l carries the same factor.
+        float lsum_tile = 0.0f;
+        auto weights64 = [&](auto cap_c, const uint32_t* v, int c0, float ref, uint32_t* pw) {
+          const float* svp = sv + sd * kN + c0;
+          float ls0 = 0.0f, ls1 = 0.0f;
+  #pragma unroll
+          for (int e = 0; e < 64; e += 2) {
+            const float r0 = __uint_as_float(v[e]), r1 = __uint_as_float(v[e + 1]);
+            float p0, p1;
+            if constexpr (AL) {  // v holds the final scores
+              p0 = dev::fast_exp2(r0 - ref);
+              p1 = dev::fast_exp2(r1 - ref);
+            } else if constexpr (decltype(cap_c)::value) {
+              p0 = dev::fast_exp2(score(cap_c, r0) - ref);
+              p1 = dev::fast_exp2(score(cap_c, r1) - ref);
+            } else {
+              p0 = dev::fast_exp2(fmaf(r0, score_mul, -ref));
+              p1 = dev::fast_exp2(fmaf(r1, score_mul, -ref));
+            }
+            ls0 += p0;
+            ls1 += p1;
+            if constexpr (Geo::kPth) {
+              const float2 v2 = *reinterpret_cast<const float2*>(svp + e);
+              p0 *= v2.x * v_mul;
+              p1 *= v2.y * v_mul;
+            }
+            if constexpr (Geo::kAuto) {
+              // bf16 MMA: P = hi + lo, both bf16 (16 significant bits); hi in
+              // pw[0 .. 31], lo in pw[32 .. 63].
+              const uint32_t h = dev::pack_bf16x2(p0, p1);
+              pw[e / 2] = h;
+              pw[32 + e / 2] = dev::pack_bf16x2(p0 - dev::bf16_lo(h), p1 - dev::bf16_hi(h));
+            } else {
+              pw[e / 2] = dev::pack_f16x2(p0, p1);
+            }
+          }
+          lsum_tile += ls0 + ls1;
+        };
+        // One pass over the row, 64 scores per tensor-memory round trip: the
+        // round's maximum, then its weights against the reference, written
+        // as f16 pairs over columns of S(j) already read.  A round maximum
+        // more than 2^8 above the reference moves it (lazily) to the next
+        // integer at or above; weights already written in this tile are then
+        // scaled by the same power of two.
+  #pragma unroll 1
+        for (int c0 = 0; c0 < kN; c0 += 64) {
+          uint32_t v[64];
+          tc::tmem_ld32(tmem_s + c0, *reinterpret_cast<uint32_t(*)[32]>(v));
+          tc::tmem_ld32(tmem_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(v + 32));
+          tc::tmem_wait_ld();
+          const float mr = full ? raw64(std::true_type{}, v, c0) : raw64(std::false_type{}, v, c0);
+          // the score is monotonic in r (score_mul > 0, tanh increasing); with
+          // ALiBi mr is the largest final score already
+          const float mx = AL ? mr : cap > 0.0f ? score(std::true_type{}, mr) : score(std::false_type{}, mr);
+          float a = 1.0f;
+          if (mx > m_ref + 8.0f) {
+            const float nref = ceilf(mx);
+            if (m_ref != -INFINITY) a = ldexpf(1.0f, (int)fmaxf(m_ref - nref, -200.0f));
+            m_ref = nref;
+            alpha *= a;
+            l_sum *= a;
+            lsum_tile *= a;
+          }
+          const float ref = m_ref == -INFINITY ? 0.0f : m_ref - 6.0f;
+          constexpr int kPw = Geo::kAuto ? 64 : 32;  // P words of the round (bf16: hi and lo)
+          uint32_t pw[kPw];
+          if (cap > 0.0f)
+            weights64(std::true_type{}, v, c0, ref, pw);
+          else
+            weights64(std::false_type{}, v, c0, ref, pw);
+          // f16 P of the round goes to columns c0 / 2 .. c0 / 2 + 31; bf16 hi
+          // and lo halves to c0 .. c0 + 63 (the columns this round read).
+          const int pcol = Geo::kAuto ? c0 : c0 / 2;
+  #pragma unroll
+          for (int h = 0; h < kPw; h += 16)
+            tc::tmem_st16(tmem_s + pcol + h, *reinterpret_cast<uint32_t(*)[16]>(pw + h));
+          if (c0 > 0 && __any_sync(0xffffffffu, a != 1.0f)) {
+            // Weights of the earlier rounds against the new reference: a
+            // power-of-two scaling, exact unless subnormal.
+            tc::tmem_wait_st();
+  #pragma unroll 1
+            for (int c = 0; c < pcol; c += 32) {
+              uint32_t w[32];
+              tc::tmem_ld32(tmem_s + c, w);
+              tc::tmem_wait_ld();
+  #pragma unroll
+              for (int e = 0; e < 32; ++e) {
+                if constexpr (Geo::kAuto) {
+                  w[e] = dev::pack_bf16x2(dev::bf16_lo(w[e]) * a, dev::bf16_hi(w[e]) * a);
+                } else {
+                  const float2 f = __half22float2(*reinterpret_cast<const __half2*>(&w[e]));
+                  w[e] = dev::pack_f16x2(f.x * a, f.y * a);
+                }
+              }
+              tc::tmem_st32(tmem_s + c, w);
+            }
+          }
+        }
+        l_sum += lsum_tile;
+        // A moved reference rescales O: PV(g-1) must be complete first.  (S(g)
+        // being complete implies PV(g-2) is, and PV(g) waits for this KV
+        // tile's P, so the barrier is at completion g-1 or g: the wait is
+        // exact.  The tile's first KV tile starts O afresh.)
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.0f)) {
+          ok = __all_sync(0xffffffffu,
+                          wait_or_abort(bar(Geo::kBarODone), (uint32_t)((g - 1) & 1), abort_flag));
+          if (!ok) break;
+          tc::fence_after_sync();
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 32) {
+            uint32_t v[32];
+            tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
+            tc::tmem_wait_ld();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
+            tc::tmem_st32(tmem + Geo::kColO + lane_base + c0, v);
+          }
+        }
+        tc::tmem_wait_st();
+        tc::fence_before_sync();
+        warp_arrive(bar(Geo::kBarPFull + st));
+      }
+      if (!ok) break;
+      // Every S of this tile is complete (the last one was waited for), so
+      // the next tile's Q may replace this one's; its first S can then run
+      // while this tile's last P V and epilogue do.
+      TileRun<kN> nxt;
+      float q_next = 1.0f;
+      if (k2 >= 0) {
+        nxt.set(p.prefill_tiles[dealt_tile(k2)]);
+        q_next = load_q(nxt);
+      }
+      // ---- epilogue: O / l -> bf16, straight from the row's thread to
+      // global memory; then O is free for the next tile's first P V.
+      ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarOFinal), (uint32_t)(n & 1), abort_flag));
+      if (!ok) break;
+      tc::fence_after_sync();
+      // An attention sink joins the normaliser (the weights carry
+      // 2^-(m_ref - 6)).
+      // (this tile's record again, from L1: not kept in registers over the loop)
+      const PrefillTile te = p.prefill_tiles[dealt_tile(k)];
+      if (p.sinks && m < te.nrows && m_ref != -INFINITY) {
+        const float skl = p.sinks[te.kv_head * G + (te.row0 + m) % G] * log2e;
+        if (skl != -INFINITY) l_sum += exp2f(fminf(skl - m_ref + 6.0f, 126.0f));
+      }
+      uint16_t* const dst = out_row(te);
+      const float sc = (l_sum > 0.0f ? 1.0f / l_sum : 0.0f) *
+                       (Geo::kPth ? (ev > -1000 ? ldexpf(1.0f, ev) : 0.0f) : Geo::kAuto ? 1.0f : p.v_scale);
+#pragma unroll 1
+      for (int c0 = 0; c0 < D; c0 += 32) {
+        uint32_t v[32];
+        tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
+        tc::tmem_wait_ld();
+        if (dst) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             uint4 o;
@@ -1060,15 +1156,16 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             o.y = dev::pack_bf16x2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
             o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
             o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
-            const int c = (c0 + e) / 8;
-            sts128(orow + (uint32_t)(((c ^ (m & 7)) << 4)), o);
+            *reinterpret_cast<uint4*>(dst + c0 + e) = o;
           }
         }
-      } else {
-        // No key tile at all (an empty key range): the output row is zero.
-#pragma unroll 1
-        for (int c = 0; c < D / 8; ++c) sts128(orow + (uint32_t)(c << 4), make_uint4(0, 0, 0, 0));
       }
+      tc::fence_before_sync();
+      warp_arrive(bar(Geo::kBarOFree));
+      cur = nxt;
+      k = k2;
+      have = k2 >= 0;
+      q_unscale = q_next;
     }
     // Order this warp's tensor-memory accesses before the teardown barrier.
     tc::fence_before_sync();
@@ -1077,57 +1174,58 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
 
   __syncthreads();
   const bool aborted = *abort_flag != 0u;
-  if (tid == 0 && aborted) atomicExch(p.error_flag, 1);
   if (warp == 0) {
     tc::fence_after_sync();
     tc::tmem_dealloc(tmem, Geo::kTmemCols);
   }
-  // ---- O tile -> global, coalesced: lanes_per_row lanes write one row.  A
-  // tile that gave up a bounded wait writes NaN rows instead, so its failure
-  // shows in the output even where nobody reads the error word.
-  {
+  // A CTA that gave up a bounded wait writes NaN over every row of its
+  // tiles, so its failure shows in the output even where nobody reads the
+  // error word.
+  if (aborted) {
+    if (tid == 0) atomicExch(p.error_flag, 1);
     constexpr int kLpr = D / 8;
     constexpr int kRps = 32 / kLpr;
     const int lane = tid & 31;
     const int sub = lane / kLpr, c = lane % kLpr;
     const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-    for (int r = warp * kRps + sub; r < t.nrows; r += (Geo::kThreads / 32) * kRps) {
-      const uint4 o = aborted ? nan4
-                              : lds128(base + Geo::kOffOStage + (uint32_t)(r * D * 2 + ((c ^ (r & 7)) << 4)));
-      const int Rr = t.row0 + r;
-      *reinterpret_cast<uint4*>(p.out + ((int64_t)(q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D +
-                                8 * c) = o;
+    for (int k = 0; dealt_tile(k) < p.num_prefill_tiles; ++k) {
+      const PrefillTile t = p.prefill_tiles[dealt_tile(k)];
+      for (int r = warp * kRps + sub; r < t.nrows; r += (Geo::kThreads / 32) * kRps) {
+        const int Rr = t.row0 + r;
+        *reinterpret_cast<uint4*>(p.out + ((int64_t)(t.q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D +
+                                  8 * c) = nan4;
+      }
     }
   }
 }
 
 template <int DT, int D, bool AL>
-int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_t num_tiles,
+int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_t ctas,
                             cudaStream_t stream) {
   const size_t smem = prefill_smem_bytes(D);
   auto kern = prefill_attention_kernel<DT, D, AL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
-  kern<<<(unsigned)num_tiles, prefill_threads(D), smem, stream>>>(p, maps);
+  kern<<<(unsigned)ctas, prefill_threads(D), smem, stream>>>(p, maps);
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 
 // The instances of one head_dim and one ALiBi setting (one translation unit
 // each keeps the build parallel).
 template <int D, bool AL>
-int launch_prefill_d(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+int launch_prefill_d(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t ctas,
                      cudaStream_t stream) {
   switch (dtype) {
-    case KVQ_AUTO: return launch_prefill_instance<KVQ_AUTO, D, AL>(p, maps, num_tiles, stream);
-    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D, AL>(p, maps, num_tiles, stream);
-    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D, AL>(p, maps, num_tiles, stream);
+    case KVQ_AUTO: return launch_prefill_instance<KVQ_AUTO, D, AL>(p, maps, ctas, stream);
+    case KVQ_FP8_E4M3: return launch_prefill_instance<KVQ_FP8_E4M3, D, AL>(p, maps, ctas, stream);
+    case KVQ_FP8_E5M2: return launch_prefill_instance<KVQ_FP8_E5M2, D, AL>(p, maps, ctas, stream);
     case KVQ_INT8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_INT8_PER_TOKEN_HEAD, D, AL>(p, maps, ctas, stream);
     case KVQ_FP8_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_FP8_PER_TOKEN_HEAD, D, AL>(p, maps, ctas, stream);
     case KVQ_FP8_E5M2_PER_TOKEN_HEAD:
-      return launch_prefill_instance<KVQ_FP8_E5M2_PER_TOKEN_HEAD, D, AL>(p, maps, num_tiles, stream);
+      return launch_prefill_instance<KVQ_FP8_E5M2_PER_TOKEN_HEAD, D, AL>(p, maps, ctas, stream);
     default:
       return KVQ_E_UNSUPPORTED;
   }

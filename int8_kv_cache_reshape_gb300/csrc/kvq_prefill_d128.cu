@@ -3,9 +3,9 @@
 #include "kvq_prefill.cuh"
 
 namespace kvq {
-int launch_prefill_d128(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+int launch_prefill_d128(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t ctas,
                         void* stream) {
-  return launch_prefill_d<128, false>(p, maps, dtype, num_tiles,
+  return launch_prefill_d<128, false>(p, maps, dtype, ctas,
                                        static_cast<cudaStream_t>(stream));
 }
 }  // namespace kvq

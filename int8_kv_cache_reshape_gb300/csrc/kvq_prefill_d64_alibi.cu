@@ -3,9 +3,9 @@
 #include "kvq_prefill.cuh"
 
 namespace kvq {
-int launch_prefill_d64_alibi(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t num_tiles,
+int launch_prefill_d64_alibi(const AttnParams& p, const PrefillMaps& maps, int dtype, int64_t ctas,
                              void* stream) {
-  return launch_prefill_d<64, true>(p, maps, dtype, num_tiles,
+  return launch_prefill_d<64, true>(p, maps, dtype, ctas,
                                        static_cast<cudaStream_t>(stream));
 }
 }  // namespace kvq

@@ -159,3 +159,28 @@ def test_reruns_are_bit_identical(cuda_device, monkeypatch):
     b = g.attention().out.clone()
     assert g.sched_info["num_merge_items"] > 0
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+@pytest.mark.parametrize("dtype,D,ctas", [("fp8_e4m3", 256, 1), ("int8_per_token_head", 128, 3),
+                                          ("fp8_e5m2_per_token_head", 64, 2), ("auto", 128, 5),
+                                          ("fp8_per_token_head", 128, 7)])
+def test_persistent_ctas_walk_many_tiles(cuda_device, monkeypatch, dtype, D, ctas):
+    """The prefill runs one persistent CTA per SM over the dealt tile list;
+    with KVQ_PREFILL_CTAS forcing a few CTAs, each walks many tiles of
+    different requests, kv heads and key ranges back to back (the rings,
+    Q and O carried over tile boundaries).  The output is bit-identical to
+    the one-tile-per-CTA run and matches the oracle."""
+    wl = W.custom(f"pf-persist-{dtype}-{D}", [150, 40, 1, 300, 17], [400, 40, 900, 1300, 17], 16, 4, D,
+                  16, dtype, 420 + D, window=0, token_scale_range=_pth(dtype), outlier_p=0.01)
+    monkeypatch.delenv("KVQ_PREFILL_CTAS", raising=False)
+    g = GpuRun(wl).write_cache().attention()
+    a = g.out.clone()
+    tiles = g.sched_info["num_prefill_tiles"]
+    assert tiles > 4 * ctas
+    monkeypatch.setenv("KVQ_PREFILL_CTAS", str(ctas))
+    g.out.fill_(float("nan"))
+    b = g.attention().out.clone()
+    assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+    kc, vc = oracle_cache(wl)
+    ref, bnd = oracle_reference(wl, kc, vc)
+    assert_attention_close(g.out_f32(), ref, wl.name, bnd)
