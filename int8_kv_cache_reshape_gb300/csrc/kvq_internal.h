@@ -114,14 +114,14 @@ constexpr int kPrefillSideSlots = 4;
 constexpr int kPrefillSlotRing = 4;
 // Shared memory: 2 x K and 2 x V (keys x D f16 each); 4 x the tile's key /
 // value scales; 4 x the tile's chunk mask and per-warp largest value scales
-// (144 bytes); 4 x 64-byte slot tables; barriers and flags (512 bytes); +1 KB
-// for 1024-byte alignment.  (The codes go from global memory to the
-// converters' registers, Q from global memory to tensor memory and O back
-// through registers.)
+// (144 bytes); 4 x 64-byte slot tables; the finished tile's O rows (128 x
+// (D * 2 + 16) bytes); barriers and flags (512 bytes); +1 KB for 1024-byte
+// alignment.  (The codes go from global memory to the converters'
+// registers, Q from global memory to tensor memory.)
 KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
   return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
-         (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillSlotRing * 64 + 512 +
-         1024;
+         (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillSlotRing * 64 +
+         (size_t)kPrefillRows * (head_dim * 2 + 16) + 512 + 1024;
 }
 
 // Tensor maps of bf16 ("auto") caches for the prefill's bulk tensor copies:

@@ -44,9 +44,11 @@
 //     power of two (O only after P(j-1) V(j-1) is complete).  At the end it
 //     reads O and writes bf16.
 //   * Q enters as f16 exactly: each row is scaled by a power of two that puts
-//     its largest |q| in [2^14, 2^15) (a bf16 significand fits in f16's);
+//     its largest |q| in [2^13, 2^14) (a bf16 significand fits in f16's);
 //     the scale, sm_scale, log2(e) and k_scale (per tensor) or the key's
 //     scale (per token-head) multiply the fp32 scores; v_scale the output.
+//     Elements more than about 2^27 below the row's largest fall into f16's
+//     subnormals and lose low bits (further down, flush to zero).
 //   * Per-token-head value scales are folded into P relative to a running
 //     power-of-two reference 2^ev (the largest scale exponent seen so far),
 //     so P * sv * 2^-ev < 2^14 stays in f16 range; O is rescaled by a power
@@ -94,7 +96,12 @@ struct PrefillGeom {
   // each 16-key chunk (entries 0 .. kN / 16 - 1) and the chunk mask (15).
   static constexpr int kSlotRing = kPrefillSlotRing;
   static constexpr int kOffSlots = kOffVMax + 32 * kSide;           // kSlotRing x 16 i32
-  static constexpr int kOffBar = kOffSlots + kSlotRing * 64;        // mbarriers, tmem slot, flags
+  // O of a finished tile, bf16 rows for the bulk stores: kM rows of D * 2
+  // bytes, 16 bytes of padding after each (a warp's 16-byte stores of one
+  // column chunk then cover all 32 banks).
+  static constexpr int kOutPitch = D * 2 + 16;
+  static constexpr int kOffOut = kOffSlots + kSlotRing * 64;         // kM x kOutPitch
+  static constexpr int kOffBar = kOffOut + kM * kOutPitch;          // mbarriers, tmem slot, flags
   static constexpr int kBytes = kOffBar + 512;
   static constexpr int kColO = 0;                 // O: D fp32 columns
   static constexpr int kColS = D;                 // S buffers: kN fp32 columns each
@@ -809,13 +816,13 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     // Q row m of a tile -> tensor memory (columns kColQ.., f16 pairs), and
     // the arrival that lets the tile's first S go.  Q enters as f16 exactly:
     // the row is scaled by the power of two that puts its largest |q| in
-    // [2^14, 2^15) (a bf16 significand fits in f16's).  Elements more than
-    // 2^28 below the row's largest land in f16's subnormal range (bits lost)
-    // or flush to zero: a Q row with that dynamic range loses them.  The
-    // raw bf16 row goes to tensor memory first (batches of 8 16-byte loads,
-    // two batches in flight) while its largest exponent is found; then it is
-    // converted in place.  bf16 rows ("auto") enter the bf16 MMA as they
-    // are.  Returns the row's 2^-shift.
+    // [2^13, 2^14) (a bf16 significand fits in f16's).  Elements more than
+    // about 2^27 below the row's largest land in f16's subnormal range (bits
+    // lost) or flush to zero: a Q row with that dynamic range loses them.
+    // The raw bf16 row goes to tensor memory first (batches of 8 16-byte
+    // loads, two batches in flight) while its largest exponent is found;
+    // then it is converted in place.  bf16 rows ("auto") enter the bf16 MMA
+    // as they are.  Returns the row's 2^-shift.
     auto load_q = [&](const TileRun<kN>& r) -> float {
       constexpr int kQv = D / 8;               // 16-byte pieces of a row
       constexpr int kB = kQv < 8 ? kQv : 8;    // pieces per batch
@@ -852,8 +859,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         for (int c = 0; c < kB; ++c) qa[c] = qb[c];
       }
       tc::tmem_wait_st();
-      // largest |q| < 2^(emax - 126)
-      const int sh = emax > 0 && !Geo::kAuto ? min(140 - emax, 126) : 0;
+      // largest |q| < 2^(emax - 126): scaled into [2^13, 2^14)
+      const int sh = emax == 0 || Geo::kAuto ? 0 : min(140 - emax, 126);
       if constexpr (!Geo::kAuto) {
         const float up = ldexpf(1.0f, sh);
 #pragma unroll 1
@@ -1127,8 +1134,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         nxt.set(p.prefill_tiles[dealt_tile(k2)]);
         q_next = load_q(nxt);
       }
-      // ---- epilogue: O / l -> bf16, straight from the row's thread to
-      // global memory; then O is free for the next tile's first P V.
+      // ---- epilogue: O / l -> bf16 rows in shared memory; then O is free
+      // for the next tile's first P V, and each row goes to global memory by
+      // one bulk copy of its thread (coalesced, asynchronous).
       ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarOFinal), (uint32_t)(n & 1), abort_flag));
       if (!ok) break;
       tc::fence_after_sync();
@@ -1143,30 +1151,39 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       uint16_t* const dst = out_row(te);
       const float sc = (l_sum > 0.0f ? 1.0f / l_sum : 0.0f) *
                        (Geo::kPth ? (ev > -1000 ? ldexpf(1.0f, ev) : 0.0f) : Geo::kAuto ? 1.0f : p.v_scale);
+      // (the previous tile's bulk copy of this row has read its staging row)
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      const uint32_t orow = base + Geo::kOffOut + (uint32_t)(m * Geo::kOutPitch);
 #pragma unroll 1
       for (int c0 = 0; c0 < D; c0 += 32) {
         uint32_t v[32];
         tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
         tc::tmem_wait_ld();
-        if (dst) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 o;
-            o.x = dev::pack_bf16x2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
-            o.y = dev::pack_bf16x2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
-            o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
-            o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
-            *reinterpret_cast<uint4*>(dst + c0 + e) = o;
-          }
+        for (int e = 0; e < 32; e += 8) {
+          uint4 o;
+          o.x = dev::pack_bf16x2(__uint_as_float(v[e]) * sc, __uint_as_float(v[e + 1]) * sc);
+          o.y = dev::pack_bf16x2(__uint_as_float(v[e + 2]) * sc, __uint_as_float(v[e + 3]) * sc);
+          o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
+          o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
+          sts128(orow + (uint32_t)((c0 + e) * 2), o);
         }
       }
       tc::fence_before_sync();
       warp_arrive(bar(Geo::kBarOFree));
+      if (dst) {
+        tc::fence_async_smem();
+        asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
+                     "cp.async.bulk.commit_group;"
+                     :: "l"(reinterpret_cast<uint64_t>(dst)), "r"(orow), "n"(D * 2) : "memory");
+      }
       cur = nxt;
       k = k2;
       have = k2 >= 0;
       q_unscale = q_next;
     }
+    // The rows' bulk copies are complete before the shared memory goes.
+    asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
     // Order this warp's tensor-memory accesses before the teardown barrier.
     tc::fence_before_sync();
     __syncwarp();
