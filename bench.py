@@ -44,19 +44,32 @@ FALLBACK_PEAKS = {"hbm_gbs": 6800.0, "bf16_tflops": 1900.0, "bf16_tflops_sustain
 # captures summarised in profiles/; valid only while the kernel's sources
 # hash as they did when captured.
 PROFILED_TRAFFIC = {
-    (2, None): {"bytes": 361.074432e6 + 5.945344e6, "profile": "profiles/splitkv_decode_decode_batch.md",
-         "sources": ["kvq_decode.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "142c9b241fa7d2a1b9daa1aaae457bce637bb4d0"},
-    (3, None): {"bytes": 37.864448e6 + 0.718592e6, "profile": "profiles/prefill_attention_large_prefill.md",
-         "sources": ["kvq_prefill.cuh", "kvq_tcgen05.cuh", "kvq_device.cuh", "kvq_internal.h"],
-         "sha1": "160303ad39db27ace633acce9e3834c725e000d9"},
+    # (workload, kv cache dtype, part of a mixed batch): DRAM bytes read +
+    # written by that kernel in one launch, from the ncu capture in `profile`
+    # (taken while the listed sources hashed to `sha1`).
+    (2, "fp8_e4m3", None): {"bytes": 360.846080e6 + 5.375744e6,
+                            "profile": "profiles/splitkv_decode_decode_batch.md",
+                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "7a80fb6dd82c5d486da67c782ea179b47779b64c"},
+    (5, "fp8_e5m2", None): {"bytes": 269.253376e6 + 5.068288e6,
+                            "profile": "profiles/splitkv_decode_long_context.md",
+                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "7a80fb6dd82c5d486da67c782ea179b47779b64c"},
+    (4, "int8_per_token_head", "decode"): {"bytes": 484.701184e6 + 5.961472e6,
+                                           "profile": "profiles/mixed_batch_int8_per_token_head.md",
+                                           "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "7a80fb6dd82c5d486da67c782ea179b47779b64c"},
+    (4, "int8_per_token_head", "prefill"): {"bytes": 389.563392e6 + 93.926656e6,
+                                            "profile": "profiles/mixed_batch_int8_per_token_head.md",
+                                            "sources": ['kvq_prefill.cuh', 'kvq_tcgen05.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "3a908fb001f25ac7de4ae27ea633e766cb8bee6f"},
+    (3, "fp8_e4m3", None): {"bytes": 37.883904e6 + 0.606464e6,
+                            "profile": "profiles/prefill_attention_large_prefill.md",
+                            "sources": ['kvq_prefill.cuh', 'kvq_tcgen05.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "3a908fb001f25ac7de4ae27ea633e766cb8bee6f"},
 }
 
 
-def profiled_traffic(workload: int, dtype=None):
-    """The captured DRAM traffic of this workload's dominant kernel, or None
-    when there is no capture or the kernel changed since."""
-    entry = PROFILED_TRAFFIC.get((workload, dtype))
+def profiled_traffic(workload: int, dtype: str, part=None):
+    """The captured DRAM traffic of this workload's dominant kernel (or of
+    one part of a mixed batch), or None when there is no capture or the
+    kernel changed since."""
+    entry = PROFILED_TRAFFIC.get((workload, dtype, part))
     if entry is None:
         return None
     m = hashlib.sha1()
@@ -345,8 +358,9 @@ def run_workload(args, index, dtype, world, local, with_e2e=True):
         kernel = "tcgen05 prefill attention"
     else:
         kernel = "split-KV decode attention (+ split merge)"
+    mixed = bool(info["num_prefill_tiles"] and info["num_tiles"])
     roofline = _roofline(decode_metric, kvb, flops, attn_avg, peaks, peaks_src, kernel,
-                         profiled_traffic(index, dtype))
+                         None if mixed else profiled_traffic(index, wl.kv_cache_dtype))
 
     res = {
         "metric": metric, "value": value, "unit": unit, "n_gpus": world, "steps": args.steps,
@@ -403,7 +417,8 @@ def run_workload(args, index, dtype, world, local, with_e2e=True):
                 "unit": "GB/s" if pm else "TFLOP/s",
                 "roofline": _roofline(pm, kvb2, fl2, ms, peaks, peaks_src,
                                       "split-KV decode attention (+ split merge)" if pm
-                                      else "tcgen05 prefill attention")}
+                                      else "tcgen05 prefill attention",
+                                      profiled_traffic(index, wl.kv_cache_dtype, name))}
             s2.close()
         res["parts"] = parts
 
