@@ -214,7 +214,10 @@ KVQ_API int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv,
  *                           when that is 0).  Calls sharing one workspace
  *                           or one schedule must be ordered on one stream.
  * Query row i of a request sits at position L - Q + i; key j is visible iff
- * (!causal || j <= p) and (window <= 0 || p - j < window).  A kernel that
+ * (!causal || j <= p) and (window <= 0 || p - j < window).  The call
+ * launches the prefill kernel (if the schedule has prefill tiles), the decode
+ * kernel of each row-tile class, and the merge of the cut decode tiles (the
+ * schedule's num_kernel_launches), in that order on `stream`.  A kernel that
  * gives up one of its bounded waits writes NaN rows and sets the schedule's
  * error word (kvq_sched_check_device). */
 KVQ_API int kvq_attention_with_kv_cache(const kvq_sched_t* sched, int heads_q,

@@ -81,9 +81,9 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
   }
 }
 
-// Merge of a tile's pieces (vllm PR 50194 page, Key source snippet:
-// enable_kv_split), by one warp.  Piece s left o_s = (sum_j p_j v_j) / l_s
-// and lse_s = m_s + log2(l_s) (log2 units); the merged row is
+// Merge of a tile's pieces in the fused decode step (vllm PR 50194 page, Key
+// source snippet: enable_kv_split), by one warp.  Piece s left o_s = (sum_j
+// p_j v_j) / l_s and lse_s = m_s + log2(l_s) (log2 units); the merged row is
 //   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
 // Partials are read through L2 (other warps wrote them).  Merges run at the
 // end of the kernel (a cut tile's last piece to finish is the one at the end
@@ -302,6 +302,10 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   const int g = lane >> 2;
   const int c = lane & 3;
 
+  // The merge of the cut tiles (its own kernel, after this one) may be
+  // scheduled now: it waits for this grid to complete before it reads a
+  // partial row.
+  if constexpr (!DEV) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- the fused step's prologue -------------------------------------------
   int64_t total_chunks = p.num_chunks;
   int64_t total_warps = p.num_warps;
@@ -689,36 +693,31 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
           if (g == 0) p.part_lse[pc.part + nr] = l > 0.0f ? m_run[t][k] + log2f(l) : -INFINITY;
         }
       }
-    if (pc.part >= 0) {
-      // Publish the partials, count arrivals; the last piece merges.  No
-      // piece waits for another.
-      __threadfence();
-      __syncwarp();
-      MergeItem m;
-      int64_t f0 = 0, w0 = 0;
-      // warp whose segment holds flat chunk f: floor(((f + 1) W - 1) / T)
-      auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / total_chunks; };
-      if constexpr (DEV) {
+    if constexpr (DEV) {
+      if (pc.part >= 0) {
+        // Fused step: publish the partials, count arrivals; the last piece
+        // merges.  No piece waits for another.  (Host-planned calls merge in
+        // a kernel of their own after the decode kernels: kvq_merge.cuh.)
+        __threadfence();
+        __syncwarp();
+        // warp whose segment holds flat chunk f: floor(((f + 1) W - 1) / T)
+        auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / total_chunks; };
         // The tile's splits are the warps whose segments hold its chunks:
         // w0 .. w1 when every segment has chunks (T >= W), else one warp per
         // chunk (every non-empty segment is a single chunk).
-        f0 = __ldcg(sp.prefix + pc.merge);
+        const int64_t f0 = __ldcg(sp.prefix + pc.merge);
         const int64_t f1 = __ldcg(sp.prefix + pc.merge + 1);
-        w0 = warp_of(f0);
+        const int64_t w0 = warp_of(f0);
         const int64_t ns = total_chunks >= total_warps ? warp_of(f1 - 1) - w0 + 1 : f1 - f0;
-        m = MergeItem{pc.req, pc.kv_head, 0, pc.nrows, 0, (int32_t)ns, 0, 0};
-      } else {
-        m = p.merges[pc.merge];
-      }
-      int last = 0;
-      if (lane == 0) {
-        const int prev = atomicAdd(p.merge_counters + pc.merge, 1);
-        last = prev == m.nsplits - 1;
-      }
-      last = __shfl_sync(0xffffffffu, last, 0);
-      if (last) {
-        __threadfence();
-        if constexpr (DEV) {
+        const MergeItem m{pc.req, pc.kv_head, 0, pc.nrows, 0, (int32_t)ns, 0, 0};
+        int last = 0;
+        if (lane == 0) {
+          const int prev = atomicAdd(p.merge_counters + pc.merge, 1);
+          last = prev == m.nsplits - 1;
+        }
+        last = __shfl_sync(0xffffffffu, last, 0);
+        if (last) {
+          __threadfence();
           // split s is warp w0 + s: its slot 2 (w0 + s), except that the
           // first split's tile is warp w0's last one unless w0's segment
           // starts exactly at the tile
@@ -728,10 +727,8 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
             const int64_t w = dense ? w0 + s : warp_of(f0 + s);
             return (int)((2 * w + (s == 0 && first_is_last ? 1 : 0)) * kTileMaxRows);
           });
-        } else {
-          merge_pieces<D>(p, m, lane, [&](int s) { return m.part + s * m.nrows; });
+          if (lane == 0) atomicExch(p.merge_counters + pc.merge, 0);  // ready for the next call
         }
-        if (lane == 0) atomicExch(p.merge_counters + pc.merge, 0);  // ready for the next call
       }
     }
   };

@@ -2,8 +2,38 @@
 // decode and the tensor-core prefill kernels (one translation unit per
 // head_dim and ALiBi setting holds the instances).
 #include "kvq_internal.h"
+#include "kvq_merge.cuh"
 
 namespace kvq {
+
+// The merge runs right after the decode kernel on the stream, launched as its
+// programmatic dependent (the decode kernel lets it be scheduled at once; it
+// waits for the decode grid before reading): no launch gap between the two.
+int launch_merge(const AttnParams& p, int head_dim, int64_t num_merges, void* stream) {
+  if (num_merges <= 0) return KVQ_OK;
+  void (*kern)(AttnParams);
+  switch (head_dim) {
+    case 64: kern = merge_splits_kernel<64>; break;
+    case 128: kern = merge_splits_kernel<128>; break;
+    case 256: kern = merge_splits_kernel<256>; break;
+    default: return KVQ_E_UNSUPPORTED;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)num_merges);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return KVQ_OK;
+}
 
 #define KVQ_DECLARE(D)                                                                       \
   int launch_decode_d##D(const AttnParams&, int, int, void*);                               \

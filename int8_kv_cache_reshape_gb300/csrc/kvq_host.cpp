@@ -51,9 +51,9 @@ struct kvq_sched {
   int64_t num_tiles, max_splits, partial_rows;
   int32_t max_chunk;  // highest 16-token chunk index any tile reads
   size_t workspace_bytes;
-  void* d_buf;  // device copy: pieces, warp table, merges, merge counters, prefill tiles, error word
+  void* d_buf;  // device copy: pieces, warp table, merge items, prefill tiles, error word
   size_t d_buf_bytes;
-  size_t d_pieces_off, d_warps_off, d_merges_off, d_counters_off, d_prefill_off, d_error_off;
+  size_t d_pieces_off, d_warps_off, d_merges_off, d_prefill_off, d_error_off;
   size_t image_bytes;       // bytes of the plan image (host and device copies)
   void* h_image;            // pinned host image, uploaded by the first attention call
   size_t h_image_bytes;
@@ -550,20 +550,18 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   }
   s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
 
-  // 3) The plan image (pieces, per-warp first pieces, merge items, zeroed
-  //    merge counters, prefill tiles, zeroed error word) in pinned host
+  // 3) The plan image (pieces, per-warp first pieces, merge items, prefill
+  //    tiles, zeroed error word) in pinned host
   //    memory, and a pooled device buffer for it.  The first attention call
   //    uploads it on its own stream (no synchronisation here).
   const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
   const size_t warps_bytes = s->warp_seg.size() * sizeof(WarpSeg);
   const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
-  const size_t counters_bytes = s->merges.size() * sizeof(int32_t);
   const size_t prefill_bytes = s->prefill.size() * sizeof(PrefillTile);
   s->d_pieces_off = 0;
   s->d_warps_off = kvq::align256(pieces_bytes);
   s->d_merges_off = s->d_warps_off + kvq::align256(warps_bytes);
-  s->d_counters_off = s->d_merges_off + kvq::align256(merges_bytes);
-  s->d_prefill_off = s->d_counters_off + kvq::align256(counters_bytes);
+  s->d_prefill_off = s->d_merges_off + kvq::align256(merges_bytes);
   s->d_error_off = s->d_prefill_off + kvq::align256(prefill_bytes);
   const size_t total = s->d_error_off + sizeof(int32_t);
   s->image_bytes = total;
@@ -579,7 +577,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
       return KVQ_E_NO_MEMORY;
     }
     char* image = static_cast<char*>(s->h_image);
-    std::memset(image, 0, total);  // merge counters and the error word start at zero
+    std::memset(image, 0, total);  // the error word starts at zero
     if (pieces_bytes) std::memcpy(image + s->d_pieces_off, s->pieces.data(), pieces_bytes);
     if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_seg.data(), warps_bytes);
     if (merges_bytes) std::memcpy(image + s->d_merges_off, s->merges.data(), merges_bytes);
@@ -683,7 +681,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->num_prefill_tiles = (int64_t)s->prefill.size();
   out->prefill_smem_bytes = kvq::prefill_smem_bytes(s->head_dim);
   out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0) +
-                             (!s->prefill.empty());
+                             (!s->merges.empty()) + (!s->prefill.empty());
   return KVQ_OK;
 }
 
@@ -762,7 +760,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   char* b = static_cast<char*>(s->d_buf);
   p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off);
   p.merges = reinterpret_cast<const MergeItem*>(b + s->d_merges_off);
-  p.merge_counters = reinterpret_cast<int32_t*>(b + s->d_counters_off);
+  p.merge_counters = nullptr;  // (the fused step's in-kernel merges only)
   p.prefill_tiles = reinterpret_cast<const PrefillTile*>(b + s->d_prefill_off);
   p.num_prefill_tiles = (int32_t)s->prefill.size();
   p.error_flag = reinterpret_cast<int32_t*>(b + s->d_error_off);
@@ -823,7 +821,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     const int rc = kvq::launch_decode(p, s->dtype, head_dim, cls + 1, stream);
     if (rc != KVQ_OK) return rc;
   }
-  return KVQ_OK;
+  return kvq::launch_merge(p, head_dim, (int64_t)s->merges.size(), stream);
 }
 
 // ---- the fused decode step ------------------------------------------------

@@ -276,6 +276,9 @@ int launch_decode_step(const AttnParams& p, const StepParams& sp, int dtype, int
 // Decode warps of the fused step's grid on the current device (every CTA
 // resident at once) in *warps; KVQ_OK or a KVQ_E_* status.
 int step_warps(int dtype, int head_dim, bool alibi, int max_rows, int64_t* warps);
+// The merge of the decode's cut tiles (p.merges, one CTA each), after the
+// decode kernels of a host-planned call.
+int launch_merge(const AttnParams& p, int head_dim, int64_t num_merges, void* stream);
 // The persistent prefill over p.num_prefill_tiles tiles on `ctas` CTAs
 // (at most one per SM is resident).
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,

@@ -1,0 +1,95 @@
+// kvq_merge.cuh -- merge of the split-KV decode's cut tiles, one CTA per
+// tile, after the decode kernels of an attention call.
+//
+// vllm PR 50194 page, Key source snippet (enable_kv_split: the KV range of a
+// tile is split and the partial results combined).  Piece s of a tile left,
+// for each of its rows, o_s = (sum_j p_j v_j) / l_s and lse_s = m_s +
+// log2(l_s) (log2 units, the weights' 2^6 lift included); the merged row is
+//   o = sum_s 2^(lse_s - M) o_s / (sum_s 2^(lse_s - M) + sink),  M = max_s lse_s.
+// An attention sink (log2 units, with the same 2^6 lift) is one more term of
+// the normaliser.
+//
+// The pieces of a cut tile all end at the ends of warp segments, i.e. at the
+// end of the decode kernel; merged there by the last piece's warp, a tile's
+// partial rows were read by one warp with a few loads in flight, while the
+// other warps' streaming still loaded the memory system (up to 10-17 us of
+// tail).  Here a CTA of 128 threads merges a tile: the rows' maxima and
+// normalisers first (8 threads per row), then (row, 4-dim) items, consecutive
+// threads on consecutive dims of a partial row.
+#pragma once
+
+#include <cuda_runtime.h>
+
+#include "kvq_device.cuh"
+#include "kvq_internal.h"
+
+namespace kvq {
+
+constexpr int kMergeThreads = 128;
+
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
+  // Launched as a programmatic dependent of the decode kernel: this CTA may
+  // be resident before the decode grid ends; the partials are read only once
+  // that grid has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const MergeItem m = p.merges[blockIdx.x];
+  const int G = p.group;
+  const int nr = m.nrows, ns = m.nsplits;
+  const int tid = threadIdx.x;
+  const float log2e = 1.4426950408889634f;
+  __shared__ float row_max[kTileMaxRows], row_inv[kTileMaxRows];
+  // (row n of split s is partial row m.part + s * nr + n)
+  {
+    const int n = tid >> 3, sub = tid & 7;
+    const bool live = n < nr;
+    float M = -INFINITY;
+    if (live)
+      for (int s = sub; s < ns; s += 8) M = fmaxf(M, __ldcg(p.part_lse + m.part + s * nr + n));
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    const float sink = p.sinks && live ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], log2e, 6.0f)
+                                       : -INFINITY;
+    M = fmaxf(M, sink);
+    float sum = 0.0f;
+    if (live && M != -INFINITY)
+      for (int s = sub; s < ns; s += 8) {
+        const float l = __ldcg(p.part_lse + m.part + s * nr + n);
+        if (l != -INFINITY) sum += exp2f(l - M);
+      }
+#pragma unroll
+    for (int off = 4; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    if (live && sub == 0) {
+      if (sink != -INFINITY) sum += exp2f(sink - M);
+      row_max[n] = M;
+      row_inv[n] = sum > 0.0f ? 1.0f / sum : 0.0f;
+    }
+  }
+  __syncthreads();
+  const int q0 = p.query_start_loc[m.req];
+  constexpr int kQuads = D / 4;
+  for (int it = tid; it < nr * kQuads; it += kMergeThreads) {
+    const int n = it / kQuads, d = (it % kQuads) * 4;
+    const float M = row_max[n], inv = row_inv[n];
+    float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    if (M != -INFINITY) {
+#pragma unroll 4
+      for (int s = 0; s < ns; ++s) {
+        const int64_t r = (int64_t)m.part + (int64_t)s * nr + n;
+        const float l = __ldcg(p.part_lse + r);
+        const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d));
+        const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
+        a0 += w * v.x;
+        a1 += w * v.y;
+        a2 += w * v.z;
+        a3 += w * v.w;
+      }
+    }
+    const int R = m.row0 + n;
+    uint16_t* dst = p.out + ((int64_t)(q0 + R / G) * p.heads_q + m.kv_head * G + R % G) * D + d;
+    *reinterpret_cast<uint2*>(dst) =
+        make_uint2(dev::pack_bf16x2(a0 * inv, a1 * inv), dev::pack_bf16x2(a2 * inv, a3 * inv));
+  }
+}
+
+}  // namespace kvq
