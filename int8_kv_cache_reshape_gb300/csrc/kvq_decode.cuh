@@ -366,7 +366,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   // first token, piece, visible-row mask | kv_head << 16}, built by lanes
   // 0-15 for 16 positions at a time in three steps a few chunks apart so
   // that the dependent loads (chunk ref -> piece -> block table) overlap
-  // with the streaming.
+  // with the streaming; the first 32 positions before streaming starts.
   int f_piece = -1, f_chunk = 0;
   int cur_piece = 0;
   if constexpr (DEV) {
@@ -376,9 +376,9 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   }
   int4 f_pc = make_int4(0, 0, 0, 0);  // req, kv_head, any_lo, any_hi
   int f_blk = -1;
-  auto fill_load_ref = [&](int pos) {
+  auto fill_load_ref = [&](int pos, int lanes) {
     f_piece = -1;
-    if (lane < 16 && pos + lane < n) {
+    if (lane < lanes && pos + lane < n) {
       const int64_t flat = seg0 + pos + lane;
       if constexpr (DEV) {
         while (cur_piece + 1 < sp.num_tiles && (int64_t)__ldcg(sp.prefix + cur_piece + 1) <= flat)
@@ -411,8 +411,8 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
     if (f_piece >= 0 && (!DEV || f_chunk / cpb < p.block_table_stride))
       f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_chunk / cpb];
   };
-  auto fill_store = [&](int pos) {
-    if (lane < 16 && pos + lane < n) {
+  auto fill_store = [&](int pos, int lanes) {
+    if (lane < lanes && pos + lane < n) {
       const int chunk = f_chunk;
       const int tok0 = chunk * kChunkTokens;
       const bool ok = f_blk >= 0 && (int64_t)f_blk < p.num_blocks;
@@ -425,13 +425,21 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
                      live | ((uint32_t)f_pc.y << 16));
     }
   };
-  // Positions [0, 32) are prepared before streaming starts.
+  // Positions [0, 32) are prepared before streaming starts: one per lane
+  // (the fused step walks its device prefix per lane: 16 at a time there).
+  if constexpr (DEV) {
 #pragma unroll
-  for (int b = 0; b < 2; ++b) {
-    fill_load_ref(16 * b);
+    for (int b = 0; b < 2; ++b) {
+      fill_load_ref(16 * b, 16);
+      fill_load_piece();
+      fill_load_block();
+      fill_store(16 * b, 16);
+    }
+  } else {
+    fill_load_ref(0, 32);
     fill_load_piece();
     fill_load_block();
-    fill_store(16 * b);
+    fill_store(0, 32);
   }
   __syncwarp();
 
@@ -957,11 +965,11 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
     // Records for positions q + 17 .. q + 32, in three steps (see above).
     {
       const int phase = q % 16;
-      if (phase == 0) fill_load_ref(q + 32);
+      if (phase == 0) fill_load_ref(q + 32, 16);
       else if (phase == 5) fill_load_piece();
       else if (phase == 10) fill_load_block();
       else if (phase == 15) {
-        fill_store(q + 17);
+        fill_store(q + 17, 16);
         __syncwarp();
       }
     }
