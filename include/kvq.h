@@ -431,7 +431,11 @@ KVQ_API int kvq_sched_export_plan(const kvq_sched_t* sched, kvq_plan_piece_t* pi
  * Read, and clear, the schedule's device error word: KVQ_E_TIMEOUT if a
  * kernel run with this schedule gave up waiting for the tensor core (a
  * bounded wait of about a second; the kernel then released its tensor
- * memory and wrote NaN into the output rows of its tile), else KVQ_OK.
+ * memory and wrote NaN into the output rows of its tile); in the
+ * bounds-checked build (libkvq_checked.so, compiled with KVQ_CHECKED=1)
+ * KVQ_E_INVALID_ARG if a kernel found an index it derived from a device
+ * array (query_start_loc row offsets, block-table positions) outside its
+ * array and skipped the access; else KVQ_OK.
  * The attention calls return before their kernels run, so they cannot
  * report this themselves: a caller that does not read the error word sees
  * such a failure as NaN rows.  Blocks until the device is idle. */

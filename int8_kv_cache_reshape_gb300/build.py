@@ -17,6 +17,9 @@ HERE = os.path.dirname(os.path.abspath(__file__))
 CSRC = os.path.join(HERE, "csrc")
 BUILD = os.path.join(HERE, "_build", platform.machine())
 LIB = os.path.join(HERE, "libkvq.so")
+# The bounds-checked build (-DKVQ_CHECKED=1): same sources, its own objects.
+BUILD_CHECKED = os.path.join(HERE, "_build", platform.machine() + "-checked")
+LIB_CHECKED = os.path.join(HERE, "libkvq_checked.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -37,8 +40,8 @@ def _headers_mtime() -> float:
     return max(os.path.getmtime(h) for h in hs)
 
 
-def _compile(src: str, force: bool, extra) -> str:
-    obj = os.path.join(BUILD, os.path.basename(src) + ".o")
+def _compile(src: str, force: bool, extra, build_dir: str = BUILD) -> str:
+    obj = os.path.join(build_dir, os.path.basename(src) + ".o")
     if (not force and os.path.exists(obj)
             and os.path.getmtime(obj) >= max(os.path.getmtime(src), _headers_mtime())):
         return obj
@@ -53,25 +56,28 @@ def _compile(src: str, force: bool, extra) -> str:
     return obj
 
 
-def build(force: bool = False, extra_flags=(), jobs: int = 0) -> str:
-    """Compile and link libkvq.so; returns its path."""
-    os.makedirs(BUILD, exist_ok=True)
+def build(force: bool = False, extra_flags=(), jobs: int = 0, checked: bool = False) -> str:
+    """Compile and link libkvq.so (checked: libkvq_checked.so, the
+    bounds-checked build); returns its path."""
+    build_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
+    extra = list(extra_flags) + (["-DKVQ_CHECKED=1"] if checked else [])
+    os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)
     with cf.ThreadPoolExecutor(jobs) as ex:
-        objs = list(ex.map(lambda s: _compile(s, force, extra_flags), srcs))
-    stamp = os.path.join(BUILD, "libkvq.stamp")
-    if (force or not os.path.exists(LIB) or not os.path.exists(stamp)
-            or os.path.getmtime(LIB) < max(os.path.getmtime(o) for o in objs)):
-        tmp = LIB + f".tmp{os.getpid()}"
+        objs = list(ex.map(lambda s: _compile(s, force, extra, build_dir), srcs))
+    stamp = os.path.join(build_dir, "libkvq.stamp")
+    if (force or not os.path.exists(lib) or not os.path.exists(stamp)
+            or os.path.getmtime(lib) < max(os.path.getmtime(o) for o in objs)):
+        tmp = lib + f".tmp{os.getpid()}"
         cmd = [_nvcc()] + ARCH + ["-shared", "-cudart", "static", "-o", tmp] + objs
         res = subprocess.run(cmd, capture_output=True, text=True)
         if res.returncode != 0:
             raise RuntimeError(f"link failed:\n{res.stdout}{res.stderr}")
-        os.replace(tmp, LIB)
-        with open(stamp, "w") as f:     # marks libkvq.so as built on this machine
+        os.replace(tmp, lib)
+        with open(stamp, "w") as f:     # marks the library as built on this machine
             f.write(platform.machine() + "\n")
-    return LIB
+    return lib
 
 
 if __name__ == "__main__":

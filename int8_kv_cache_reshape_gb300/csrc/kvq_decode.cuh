@@ -407,9 +407,15 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   };
   auto fill_load_block = [&]() {
     f_blk = -1;
-    // (the fused step's table width is not known on the host: check it here)
-    if (f_piece >= 0 && (!DEV || f_chunk / cpb < p.block_table_stride))
-      f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_chunk / cpb];
+    // (the fused step's table width is not known on the host: check it here;
+    // the bounds-checked build checks the host plan's positions too)
+    if (f_piece >= 0) {
+      const bool in_table = f_chunk / cpb < p.block_table_stride;
+      if constexpr (KVQ_CHECKED && !DEV)
+        if (!in_table) atomicExch(p.error_flag, 2);
+      if (!(DEV || KVQ_CHECKED) || in_table)
+        f_blk = p.block_table[(int64_t)f_pc.x * p.block_table_stride + f_chunk / cpb];
+    }
   };
   auto fill_store = [&](int pos, int lanes) {
     if (lane < lanes && pos + lane < n) {
@@ -507,6 +513,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   const int W = p.window;
   int cur = -1;                 // current piece
   DecodePiece pc;               // its descriptor
+  bool piece_bad = false;       // (bounds-checked build) its rows lie outside q / out
   int q0 = 0, all_lo = 0, all_hi = 0;
   int col_lo[NT][2], col_hi[NT][2];
   float score_mul = 0.0f;
@@ -544,6 +551,12 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
       pc = p.pieces[piece];
     }
     q0 = p.query_start_loc[pc.req];
+    if constexpr (KVQ_CHECKED && !DEV) {
+      // the piece's rows must lie in q and out (the device offsets are the
+      // caller's copy of the planned ones)
+      piece_bad = q0 < 0 || q0 + (pc.row0 + pc.nrows - 1) / G >= p.total_q_tokens;
+      if (piece_bad && lane == 0) atomicExch(p.error_flag, 2);
+    }
     const int Q = p.query_start_loc[pc.req + 1] - q0;
     const int L = p.seq_lens[pc.req];
     const int p_min = L - Q + pc.row0 / G;
@@ -557,7 +570,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
 #pragma unroll
       for (int t = 0; t < NT; ++t) {
         const int nr = 8 * t + g;
-        const bool valid = nr < pc.nrows;
+        const bool valid = nr < pc.nrows && !piece_bad;
         const int R = pc.row0 + (valid ? nr : 0);
         const int tok = q0 + R / G;
         const int head = pc.kv_head * G + R % G;
@@ -577,7 +590,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
 #pragma unroll
     for (int t = 0; t < NT; ++t) {
       const int nr = 8 * t + g;
-      const bool valid = nr < pc.nrows;
+      const bool valid = nr < pc.nrows && !piece_bad;
       const int R = pc.row0 + (valid ? nr : 0);
       const int tok = q0 + R / G;
       const int head = pc.kv_head * G + R % G;
@@ -677,6 +690,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
         const float sc = (l > 0.0f ? 1.0f / l : 0.0f) * unit * vmul;
         const int R = pc.row0 + nr;
         if (pc.part < 0) {
+          if (piece_bad) continue;
           const int tok = q0 + R / G;
           const int head = pc.kv_head * G + R % G;
           uint16_t* dst = p.out + ((int64_t)tok * p.heads_q + head) * D;

@@ -696,7 +696,7 @@ int kvq_sched_check_device(const kvq_sched_t* s) {
   int rc = KVQ_OK;
   if (cudaMemcpy(&flag, err, sizeof(flag), cudaMemcpyDeviceToHost) != cudaSuccess) rc = KVQ_E_CUDA;
   else if (flag != 0) {
-    rc = KVQ_E_TIMEOUT;
+    rc = flag == 1 ? KVQ_E_TIMEOUT : KVQ_E_INVALID_ARG;
     cudaMemset(err, 0, sizeof(flag));
   }
   if (cur != s->device) cudaSetDevice(cur);
@@ -763,6 +763,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   p.merge_counters = nullptr;  // (the fused step's in-kernel merges only)
   p.prefill_tiles = reinterpret_cast<const PrefillTile*>(b + s->d_prefill_off);
   p.num_prefill_tiles = (int32_t)s->prefill.size();
+  p.total_q_tokens = (int32_t)s->total_q;
   p.error_flag = reinterpret_cast<int32_t*>(b + s->d_error_off);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;

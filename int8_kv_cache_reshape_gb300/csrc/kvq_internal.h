@@ -21,6 +21,15 @@
 #define KVQ_HD
 #endif
 
+// Bounds-checked build (-DKVQ_CHECKED=1, libkvq_checked.so): the kernels
+// also check the indices they derive from device arrays the host did not
+// plan from (query_start_loc's row offsets, block-table positions); an index
+// outside its array sets the error word to 2 and the access is skipped.
+// Never a trap: the word is read by kvq_sched_check_device.
+#ifndef KVQ_CHECKED
+#define KVQ_CHECKED 0
+#endif
+
 namespace kvq {
 
 // ---- cache rows --------------------------------------------------------
@@ -204,7 +213,8 @@ struct AttnParams {
   int32_t* merge_counters;     // one per merge item, zero between calls
   const PrefillTile* prefill_tiles;
   int32_t num_prefill_tiles;
-  int32_t* error_flag;         // set by a kernel whose bounded wait timed out
+  int32_t total_q_tokens;      // rows of q and out (the host plan's sum Q)
+  int32_t* error_flag;         // 1: a bounded wait timed out; 2: an index outside its array
   int64_t num_blocks;
   int block_table_stride;
   int block_size;

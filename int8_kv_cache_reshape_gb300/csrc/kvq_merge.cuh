@@ -67,6 +67,13 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   }
   __syncthreads();
   const int q0 = p.query_start_loc[m.req];
+  if constexpr (KVQ_CHECKED) {
+    // the tile's rows must lie in out
+    if (q0 < 0 || q0 + (m.row0 + nr - 1) / G >= p.total_q_tokens) {
+      if (tid == 0) atomicExch(p.error_flag, 2);
+      return;
+    }
+  }
   constexpr int kQuads = D / 4;
   for (int it = tid; it < nr * kQuads; it += kMergeThreads) {
     const int n = it / kQuads, d = (it % kQuads) * 4;

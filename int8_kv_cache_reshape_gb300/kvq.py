@@ -15,7 +15,9 @@ import re
 import numpy as np
 
 _HERE = os.path.dirname(os.path.abspath(__file__))
-LIB_PATH = os.path.join(_HERE, "libkvq.so")
+# KVQ_LIBRARY selects another build of the library (the bounds-checked
+# libkvq_checked.so); default libkvq.so next to this file.
+LIB_PATH = os.environ.get("KVQ_LIBRARY") or os.path.join(_HERE, "libkvq.so")
 HEADER = os.path.join(os.path.dirname(_HERE), "include", "kvq.h")
 
 OK = 0
@@ -33,7 +35,7 @@ class KvqError(RuntimeError):
 
 
 if not os.path.exists(LIB_PATH):
-    raise ImportError(f"libkvq.so is not built ({LIB_PATH}); run "
+    raise ImportError(f"{os.path.basename(LIB_PATH)} is not built ({LIB_PATH}); run "
                       "int8_kv_cache_reshape_gb300.build.build() first")
 
 lib = ctypes.CDLL(LIB_PATH)
