@@ -361,9 +361,13 @@ typedef struct {
   size_t workspace_bytes;
   size_t decode_smem_bytes;    /* dynamic shared memory per decode CTA        */
   size_t decode_chunk_bytes;   /* K+V bytes a warp streams per 16-token chunk */
-  int64_t num_prefill_tiles;   /* 128-row tiles of the tensor-core prefill    */
+  int64_t num_prefill_tiles;   /* 128-row tiles of the tensor-core prefill
+                                  (CTA pairs: list entries, empty partners
+                                  included; see kvq_plan_prefill_tile_t) */
   size_t prefill_smem_bytes;   /* dynamic shared memory per prefill CTA       */
   int64_t num_kernel_launches; /* kernels one attention call launches         */
+  int64_t prefill_cta_group;   /* CTAs per prefill tile MMA: 1, or 2 for CTA
+                                  pairs (a build option)                      */
 } kvq_sched_info_t;
 
 KVQ_API int kvq_sched_get_info(const kvq_sched_t* sched, kvq_sched_info_t* out);
@@ -401,6 +405,10 @@ typedef struct {
   int32_t nsplits;
 } kvq_plan_merge_t;
 
+/* A prefill tile.  Quantised caches at head_dim 128 and 256 run the prefill
+ * on CTA pairs: entries 2i and 2i + 1 of the list are then two consecutive
+ * row tiles of one (request, kv head), whose MMAs (M = 256) share each KV
+ * tile, or a last tile and an empty partner (nrows 0, the same key range). */
 typedef struct {
   int32_t req, kv_head, row0, nrows;  /* up to 128 packed rows of one kv head */
   int32_t key_lo, key_hi;             /* keys some row of the tile can see */

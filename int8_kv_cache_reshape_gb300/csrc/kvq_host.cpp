@@ -18,6 +18,7 @@
 #include <atomic>
 #include <mutex>
 #include <new>
+#include <utility>
 #include <numeric>
 #include <vector>
 
@@ -394,10 +395,42 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   }
   s->num_tiles = (int64_t)(tiles[0].size() + tiles[1].size());
   // Longest prefill tiles first, so the tail of the grid is short tiles.
-  std::stable_sort(s->prefill.begin(), s->prefill.end(),
-                   [](const PrefillTile& a, const PrefillTile& b) {
-                     return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
-                   });
+  // CTA pairs take pair tiles: consecutive row tiles of one (request, kv
+  // head) at list entries 2i and 2i + 1 (a last odd tile with an empty
+  // partner: nrows 0, its key range), longest key-range union first.
+  if (kvq::prefill_cta_group(s->dtype, s->head_dim) == 2 && !s->prefill.empty()) {
+    std::vector<std::pair<PrefillTile, PrefillTile>> pairs;
+    for (size_t i = 0; i < s->prefill.size();) {
+      const PrefillTile& a = s->prefill[i];
+      if (i + 1 < s->prefill.size() && s->prefill[i + 1].req == a.req &&
+          s->prefill[i + 1].kv_head == a.kv_head) {
+        pairs.emplace_back(a, s->prefill[i + 1]);
+        i += 2;
+      } else {
+        PrefillTile e = a;
+        e.row0 = a.row0 + a.nrows;
+        e.nrows = 0;
+        pairs.emplace_back(a, e);
+        i += 1;
+      }
+    }
+    auto span = [](const std::pair<PrefillTile, PrefillTile>& q) {
+      return std::max(q.first.kv_hi, q.second.kv_hi) - std::min(q.first.kv_lo, q.second.kv_lo);
+    };
+    std::stable_sort(pairs.begin(), pairs.end(),
+                     [&](const std::pair<PrefillTile, PrefillTile>& a,
+                         const std::pair<PrefillTile, PrefillTile>& b) { return span(a) > span(b); });
+    s->prefill.clear();
+    for (const auto& q : pairs) {
+      s->prefill.push_back(q.first);
+      s->prefill.push_back(q.second);
+    }
+  } else {
+    std::stable_sort(s->prefill.begin(), s->prefill.end(),
+                     [](const PrefillTile& a, const PrefillTile& b) {
+                       return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
+                     });
+  }
 
   // 2) Work decomposition (stream-K): per class, lay the tiles' chunks end
   //    to end and cut the sequence into equal contiguous segments, one per
@@ -679,9 +712,11 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->decode_smem_bytes = kvq::decode_smem_bytes(s->dtype, s->head_dim);
   out->decode_chunk_bytes = (size_t)kvq::decode_chunk_bytes(s->dtype, s->head_dim);
   out->num_prefill_tiles = (int64_t)s->prefill.size();
-  out->prefill_smem_bytes = kvq::prefill_smem_bytes(s->head_dim);
+  out->prefill_smem_bytes =
+      kvq::prefill_smem_bytes(s->head_dim, kvq::prefill_cta_group(s->dtype, s->head_dim));
   out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0) +
                              (!s->merges.empty()) + (!s->prefill.empty());
+  out->prefill_cta_group = kvq::prefill_cta_group(s->dtype, s->head_dim);
   return KVQ_OK;
 }
 
@@ -803,7 +838,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   }
   if (!s->prefill.empty()) {
     // One persistent CTA per SM (KVQ_PREFILL_CTAS, for tests, forces fewer),
-    // never more than tiles.
+    // never more than tiles (CTA pairs: list entries, two per pair tile).
     int64_t ctas = std::max(1, sm_count());
     if (const char* env = std::getenv("KVQ_PREFILL_CTAS"))
       if (std::atoll(env) > 0) ctas = std::atoll(env);

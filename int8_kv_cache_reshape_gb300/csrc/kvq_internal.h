@@ -121,14 +121,27 @@ constexpr int kPrefillSideSlots = 4;
 // Slot tables of the prefill's KV tiles (first slot of each 16-key chunk and
 // the chunk mask), published by the copy warp up to 4 tiles ahead.
 constexpr int kPrefillSlotRing = 4;
-// Shared memory: 2 x K and 2 x V (keys x D f16 each); 4 x the tile's key /
-// value scales; 4 x the tile's chunk mask and per-warp largest value scales
-// (144 bytes); 4 x 64-byte slot tables; the finished tile's O rows (128 x
-// (D * 2 + 16) bytes); barriers and flags (512 bytes); +1 KB for 1024-byte
-// alignment.  (The codes go from global memory to the converters'
-// registers, Q from global memory to tensor memory.)
-KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim) {
-  return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 +
+// CTA pairs for the prefill (-DKVQ_PREFILL_PAIR=1; measured slower than
+// single CTAs on the prefill workloads, so off by default).
+#ifndef KVQ_PREFILL_PAIR
+#define KVQ_PREFILL_PAIR 0
+#endif
+// CTAs per tile MMA: quantised caches at head_dim 128 and 256 run on CTA
+// pairs (cta_group::2, M = 256: two 128-row tiles of one kv head share each
+// converted KV tile, each CTA converting half of it); bf16 caches and
+// head_dim 64 (a V half of 32 dims is narrower than the 128-byte swizzle)
+// on single CTAs.
+KVQ_HD constexpr int prefill_cta_group(int dtype, int head_dim) {
+  return KVQ_PREFILL_PAIR && dtype != KVQ_AUTO && head_dim >= 128 ? 2 : 1;
+}
+// Shared memory: 2 x K and 2 x V (keys x D f16 each, halves for a pair); 4 x
+// the tile's key / value scales; 4 x the tile's chunk mask and per-warp
+// largest value scales (144 bytes); 4 x 64-byte slot tables; the finished
+// tile's O rows (128 x (D * 2 + 16) bytes); barriers and flags (512 bytes);
+// +1 KB for 1024-byte alignment.  (The codes go from global memory to the
+// converters' registers, Q from global memory to tensor memory.)
+KVQ_HD constexpr size_t prefill_smem_bytes(int head_dim, int cta_group = 1) {
+  return 2 * (size_t)kPrefillStages * prefill_keys(head_dim) * head_dim * 2 / cta_group +
          (size_t)kPrefillSideSlots * prefill_keys(head_dim) * 8 + 144 + kPrefillSlotRing * 64 +
          (size_t)kPrefillRows * (head_dim * 2 + 16) + 512 + 1024;
 }

@@ -43,6 +43,10 @@
 //     and the weights, O and l already accumulated are rescaled by the exact
 //     power of two (O only after P(j-1) V(j-1) is complete).  At the end it
 //     reads O and writes bf16.
+//   * Q rows of the next tile are bulk-copied into shared memory (the output
+//     staging area, free between epilogues) when a tile starts, and moved
+//     into tensor memory once the tile's last S is complete, so that the
+//     next tile's first S runs beside the last softmax.
 //   * Q enters as f16 exactly: each row is scaled by a power of two that puts
 //     its largest |q| in [2^13, 2^14) (a bf16 significand fits in f16's);
 //     the scale, sm_scale, log2(e) and k_scale (per tensor) or the key's
@@ -62,6 +66,7 @@
 #include <cuda_fp16.h>
 #include <cuda_runtime.h>
 
+#include <algorithm>
 #include <type_traits>
 
 #include "kvq_device.cuh"
@@ -81,7 +86,13 @@ struct PrefillGeom {
   static constexpr int kConv = prefill_conv_threads(D);
   static constexpr int kStages = kPrefillStages;
   static constexpr bool kPth = is_per_token_head(DT);
-  static constexpr int kTileBytes = kN * D * 2;                     // one K or V tile (f16)
+  // CTA pair (kCG = 2): this CTA holds keys [r * kN / 2, (r + 1) * kN / 2) of
+  // each K tile (all D dims) and dims [r * D / 2, (r + 1) * D / 2) of each V
+  // tile (all kN keys), r its rank in the cluster.
+  static constexpr int kCG = prefill_cta_group(DT, D);
+  static constexpr int kKeysK = kN / kCG;                           // keys of a K tile held here
+  static constexpr int kDimsV = D / kCG;                            // dims of a V tile held here
+  static constexpr int kTileBytes = kN * D * 2 / kCG;               // this CTA's K or V tile (f16)
   static constexpr int kOffK = 0;                                   // stages x K tile
   static constexpr int kOffV = kOffK + kStages * kTileBytes;        // stages x V tile
   // Side data of KV tile g, for the softmax, in slot g % kSide: per-key
@@ -113,7 +124,8 @@ struct PrefillGeom {
   static_assert((kN + 31) / 32 <= 8 && kSide == 4, "side data space");
   static_assert(kN / 16 <= 15 && (kSlotRing & (kSlotRing - 1)) == 0, "slot table layout");
   static_assert(kConv >= kN && kConv % 32 == 0, "a converter thread per key, whole warps");
-  static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D), "smem must follow the geometry");
+  static_assert((size_t)kBytes + 1024 == prefill_smem_bytes(D, kCG), "smem must follow the geometry");
+  static_assert(kCG == 1 || (!kAuto && kDimsV % 64 == 0 && kKeysK % 8 == 0), "pair halves in the swizzle");
   // barrier slots (8 bytes each).  Quantised rows: the copy warp publishes
   // KV tile g's slot table (Slots, ring entry g % 4) once the converters
   // released entry g - 4 (SlotsFree); K(g) is converted once S(g - 2) is
@@ -126,10 +138,14 @@ struct PrefillGeom {
   // tile), and the side data (which the converters may write two tiles
   // ahead) has four slots.  Across tiles: Q full (the softmax warps wrote
   // the tile's Q; the tile's first S waits) and O free (the epilogue read
-  // O; the next tile's first PV waits), one phase per tile each.
+  // O; the next tile's first PV waits) and Q staged (the softmax threads'
+  // bulk copies of a tile's Q rows landed), one phase per tile each.  A CTA
+  // pair: the barriers the MMA warp waits on (KFull, VFull, PFull, QFull,
+  // OFree) are the even CTA's, counting the warps of both CTAs; each commit
+  // arrives on both CTAs' barriers.
   static constexpr int kBarCodesK = 0, kBarCodesV = 2, kBarKFull = 4, kBarVFull = 6, kBarVEmpty = 8,
                        kBarSFull = 10, kBarPFull = 12, kBarSide = 14, kBarODone = 18, kBarOFinal = 19,
-                       kBarDrain = 20, kBarQFull = 21, kBarOFree = 22, kBarSlots = 23,
+                       kBarDrain = 20, kBarQFull = 21, kBarOFree = 22, kBarQStage = 23, kBarSlots = 24,
                        kBarSlotsFree = kBarSlots + kSlotRing, kNumBars = kBarSlotsFree + kSlotRing;
   static constexpr int kOffTmemSlot = kOffBar + 8 * kNumBars;   // u32
   static constexpr int kOffAbort = kOffTmemSlot + 4;            // u32
@@ -186,12 +202,35 @@ __device__ __forceinline__ void warp_arrive(uint32_t bar) {
   if ((threadIdx.x & 31) == 0) mbar_arrive(bar);
 }
 
-// Bounded wait that also gives up when another role has aborted.
+// One arrival of the (converged) warp on a barrier of the CTA that issues
+// the MMAs: this CTA's, or for the odd CTA of a pair the even CTA's (a
+// release at cluster scope).
+template <int CG>
+__device__ __forceinline__ void warp_arrive_mma(uint32_t bar, uint32_t rank) {
+  __syncwarp();
+  if ((threadIdx.x & 31) == 0) {
+    if (CG == 2 && rank != 0)
+      tc::mbar_arrive_remote(bar, 0u);
+    else
+      mbar_arrive(bar);
+  }
+}
+
+// Bounded wait that also gives up when another role has aborted (CG = 2:
+// acquire at cluster scope, for the MMA warp of a pair, whose barriers see
+// arrivals from both CTAs).
+template <int CG = 1>
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity, volatile uint32_t* abort) {
-  if (tc::mbar_try_wait(bar, parity)) return true;
+  auto test = [&]() {
+    if constexpr (CG == 2)
+      return tc::mbar_try_wait_cluster(bar, parity);
+    else
+      return tc::mbar_try_wait(bar, parity);
+  };
+  if (test()) return true;
   const long long t0 = clock64();
   while (true) {
-    if (tc::mbar_try_wait(bar, parity)) return true;
+    if (test()) return true;
     if (*abort) return false;
     if (clock64() - t0 > 2000000000LL) {  // about a second
       *abort = 1u;
@@ -211,50 +250,68 @@ __device__ __forceinline__ uint4 codes8_to_f16(uint32_t w0, uint32_t w1) {
 
 // This CTA's k-th tile: the longest-first tile list dealt out over the grid
 // in serpentine order (CTA b takes tile b of the first round, tile 2G-1-b of
-// the second, ...), so every CTA gets a similar amount of work.
+// the second, ...), so every CTA gets a similar amount of work.  CTA pairs
+// (CG = 2) deal pair tiles (list entries 2i, 2i + 1: two consecutive row
+// tiles of one kv head) to the clusters; the CTA of rank r takes entry 2i + r.
+template <int CG>
 __device__ __forceinline__ int dealt_tile(int k) {
-  const int G = (int)gridDim.x, b = (int)blockIdx.x;
-  return k * G + ((k & 1) ? G - 1 - b : b);
+  const int G = (int)gridDim.x / CG, b = (int)blockIdx.x / CG;
+  const int i = k * G + ((k & 1) ? G - 1 - b : b);
+  return CG == 1 ? i : 2 * i + (int)(blockIdx.x & 1u);
 }
 
-// A tile and its run of KV tiles: kN-key tiles from kv_first (kv_lo rounded
-// down to a tile) up to kv_hi.
+// A tile and its run of KV tiles: kN-key tiles from kv_first (the key range's
+// start rounded down to a tile) up to its end.  For a CTA pair the key range
+// is the union of both halves' (both CTAs walk the same KV tiles; each row
+// masks the keys it does not see).
 template <int kN>
 struct TileRun {
   PrefillTile t;
-  int kv_first, T;
-  __device__ __forceinline__ void set(const PrefillTile& x) {
+  int lo, hi, kv_first, T;
+  __device__ __forceinline__ void set(const PrefillTile& x, const PrefillTile& y) {
     t = x;
-    kv_first = (t.kv_lo / kN) * kN;
-    T = t.kv_hi > kv_first ? (t.kv_hi - kv_first + kN - 1) / kN : 0;
+    lo = min(x.kv_lo, y.kv_lo);
+    hi = max(x.kv_hi, y.kv_hi);
+    kv_first = (lo / kN) * kN;
+    T = hi > kv_first ? (hi - kv_first + kN - 1) / kN : 0;
   }
 };
+
+// The record of list entry idx and, for a pair, its partner's.
+template <int CG>
+__device__ __forceinline__ void load_tiles(const AttnParams& p, int idx, PrefillTile& x, PrefillTile& y) {
+  x = p.prefill_tiles[idx];
+  if constexpr (CG == 2)
+    y = p.prefill_tiles[idx ^ 1];
+  else
+    y = x;
+}
 
 // Walks this CTA's KV tiles in order: KV tile j of its tile ordinal k
 // (tiles without keys skipped), n = the tiles with keys before this one.
 // The next tile's record is loaded a tile ahead, so that a move to it does
 // not wait for memory.
-template <int kN>
+template <int kN, int CG>
 struct KvCursor {
   TileRun<kN> cur;
-  PrefillTile nxt;
+  PrefillTile nxt, nxt_y;
   int k, j, n;
   bool valid, nxt_valid;
   __device__ __forceinline__ void start(const AttnParams& p) {
     k = -1;
     n = -1;
-    nxt_valid = dealt_tile(0) < p.num_prefill_tiles;
-    if (nxt_valid) nxt = p.prefill_tiles[dealt_tile(0)];
+    nxt_valid = dealt_tile<CG>(0) < p.num_prefill_tiles;
+    if (nxt_valid) load_tiles<CG>(p, dealt_tile<CG>(0), nxt, nxt_y);
     next_tile(p);
   }
   __device__ __forceinline__ void next_tile(const AttnParams& p) {
     valid = false;
     while (nxt_valid) {
-      cur.set(nxt);
+      cur.set(nxt, nxt_y);
       ++k;
-      const int idx = dealt_tile(k + 1);
+      const int idx = dealt_tile<CG>(k + 1);
       nxt_valid = idx < p.num_prefill_tiles;
-      if (nxt_valid) nxt = p.prefill_tiles[idx];
+      if (nxt_valid) load_tiles<CG>(p, idx, nxt, nxt_y);
       if (cur.T > 0) {
         valid = true;
         ++n;
@@ -272,7 +329,7 @@ template <int DT, int D, bool AL>
 __global__ void __launch_bounds__(prefill_threads(D), 1)
     prefill_attention_kernel(const AttnParams p, const __grid_constant__ PrefillMaps maps) {
   using Geo = PrefillGeom<DT, D>;
-  constexpr int kM = Geo::kM, kN = Geo::kN;
+  constexpr int kM = Geo::kM, kN = Geo::kN, CG = Geo::kCG;
   extern __shared__ uint8_t smem_raw[];
   const uint32_t raw = dev::smem_u32(smem_raw);
   const uint32_t base = (raw + 1023u) & ~1023u;
@@ -280,6 +337,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   const int tid = threadIdx.x;
   const int warp = tid >> 5;
   const int G = p.group;
+  // rank in the CTA pair (0: issues the MMAs of both)
+  const uint32_t rank = CG == 2 ? tc::cluster_ctarank() : 0u;
 
   const uint32_t bars = base + Geo::kOffBar;
   auto bar = [&](int i) { return bars + 8u * (uint32_t)i; };
@@ -294,25 +353,27 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     for (int s = 0; s < Geo::kStages; ++s) {
       tc::mbar_init(bar(Geo::kBarCodesK + s), 1);
       tc::mbar_init(bar(Geo::kBarCodesV + s), 1);
-      tc::mbar_init(bar(Geo::kBarKFull + s), Geo::kConv / 32);
-      tc::mbar_init(bar(Geo::kBarVFull + s), Geo::kConv / 32);
+      tc::mbar_init(bar(Geo::kBarKFull + s), CG * Geo::kConv / 32);
+      tc::mbar_init(bar(Geo::kBarVFull + s), CG * Geo::kConv / 32);
       tc::mbar_init(bar(Geo::kBarVEmpty + s), 1);
       tc::mbar_init(bar(Geo::kBarSFull + s), 1);
-      tc::mbar_init(bar(Geo::kBarPFull + s), 4);
+      tc::mbar_init(bar(Geo::kBarPFull + s), 4 * CG);
     }
     for (int s = 0; s < Geo::kSide; ++s)
       tc::mbar_init(bar(Geo::kBarSide + s), Geo::kAuto ? 1 : Geo::kConv / 32);
     tc::mbar_init(bar(Geo::kBarODone), 1);
     tc::mbar_init(bar(Geo::kBarOFinal), 1);
     tc::mbar_init(bar(Geo::kBarDrain), 1);
-    tc::mbar_init(bar(Geo::kBarQFull), 4);
-    tc::mbar_init(bar(Geo::kBarOFree), 4);
+    tc::mbar_init(bar(Geo::kBarQFull), 4 * CG);
+    tc::mbar_init(bar(Geo::kBarQStage), 128);
+    tc::mbar_init(bar(Geo::kBarOFree), 4 * CG);
     *abort_flag = 0u;
     tc::mbar_fence_init();
   }
   if (warp == 0) {
-    tc::tmem_alloc(base + Geo::kOffTmemSlot, Geo::kTmemCols);
-    tc::tmem_relinquish();
+    // (a pair: warp 0 of both CTAs, the same columns in both)
+    tc::tmem_alloc<CG>(base + Geo::kOffTmemSlot, Geo::kTmemCols);
+    tc::tmem_relinquish<CG>();
   }
   if (Geo::kAuto && warp == kCopyWarp && (tid & 31) == 0) {
     // the tensor maps' descriptors, ahead of the first copies
@@ -320,7 +381,12 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     asm volatile("prefetch.tensormap [%0];" :: "l"(reinterpret_cast<uint64_t>(&maps.v)) : "memory");
   }
   tc::fence_before_sync();
-  __syncthreads();  // barriers initialised, tensor memory allocated
+  // barriers initialised, tensor memory allocated (a pair: in both CTAs,
+  // before either arrives on the other's barriers)
+  if constexpr (CG == 2)
+    tc::cluster_sync();
+  else
+    __syncthreads();
   tc::fence_after_sync();
   const uint32_t tmem = *reinterpret_cast<volatile uint32_t*>(sm + Geo::kOffTmemSlot);
 
@@ -337,15 +403,20 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   constexpr int kChunks = kN / 16;
 
   if (warp == 0) {
+    if (rank == 0) {
     // ======================= MMA issuer ========================================
     // The whole warp runs the loop with warp-uniform state (descriptors and
     // counters stay in the uniform datapath); one elected lane issues every
-    // MMA (the tensor core runs one thread's MMAs in order).
+    // MMA (the tensor core runs one thread's MMAs in order).  A CTA pair's
+    // MMAs (M = 256) are issued by the even CTA: rows 128-255 are the odd
+    // CTA's tile, and the B operands' halves are read from both CTAs' shared
+    // memory at the same offsets.
     const bool leader = elect_one();
-    KvCursor<kN> cs;
+    KvCursor<kN, CG> cs;
     cs.start(p);
-    constexpr uint32_t idesc_s = Geo::kAuto ? tc::idesc_bf16(kM, kN) : tc::idesc_f16(kM, kN);
-    constexpr uint32_t idesc_o = (Geo::kAuto ? tc::idesc_bf16(kM, D) : tc::idesc_f16(kM, D)) | tc::kBMajorMN;
+    constexpr uint32_t idesc_s = Geo::kAuto ? tc::idesc_bf16(kM, kN) : tc::idesc_f16(kM * CG, kN);
+    constexpr uint32_t idesc_o =
+        (Geo::kAuto ? tc::idesc_bf16(kM, D) : tc::idesc_f16(kM * CG, D)) | tc::kBMajorMN;
     auto issue_s = [&](int g) {
       const int st = g & 1;
       // (descriptor start addresses are in 16-byte units in the low bits)
@@ -353,11 +424,11 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       if (leader) {
 #pragma unroll
         for (int kk = 0; kk < D / 16; ++kk) {
-          const uint32_t boff = (kk >> 2) * (kN * 128) + (kk & 3) * 32;
-          tc::mma_ts(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
-                     d0 + (uint64_t)(boff >> 4), idesc_s, kk > 0 ? 1u : 0u);
+          const uint32_t boff = (kk >> 2) * (Geo::kKeysK * 128) + (kk & 3) * 32;
+          tc::mma_ts<CG>(tmem + Geo::kColS + (uint32_t)(st * kN), tmem + Geo::kColQ + (uint32_t)(kk * 8),
+                         d0 + (uint64_t)(boff >> 4), idesc_s, kk > 0 ? 1u : 0u);
         }
-        tc::mma_commit(bar(Geo::kBarSFull + st));
+        tc::mma_commit<CG>(bar(Geo::kBarSFull + st));
       }
       __syncwarp();
     };
@@ -378,13 +449,13 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
             tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + pc + 32u,
                        d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, 1u);
           } else {
-            tc::mma_ts(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
-                       d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (!first || kk > 0) ? 1u : 0u);
+            tc::mma_ts<CG>(tmem + Geo::kColO, tmem + Geo::kColS + (uint32_t)(st * kN + kk * 8),
+                           d0 + (uint64_t)(kk * (2048 >> 4)), idesc_o, (!first || kk > 0) ? 1u : 0u);
           }
         }
-        tc::mma_commit(bar(Geo::kBarODone));
-        tc::mma_commit(bar(Geo::kBarVEmpty + st));
-        if (last) tc::mma_commit(bar(Geo::kBarOFinal));
+        tc::mma_commit<CG>(bar(Geo::kBarODone));
+        tc::mma_commit<CG>(bar(Geo::kBarVEmpty + st));
+        if (last) tc::mma_commit<CG>(bar(Geo::kBarOFinal));
       }
       __syncwarp();
     };
@@ -396,8 +467,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     // per g: S(g+1), PV(g) -- and the warp waits for each barrier in turn
     // (a blocking wait wakes as soon as the phase completes; polling several
     // barriers costs a shared-memory round trip per pass).  At a tile
-    // boundary S(g+1) needs the next tile's Q, which the softmax writes after
-    // P(g): PV(g) goes first there.  Flags of S(g) for its PV, 4 bits in
+    // boundary S(g+1) needs the next tile's Q, which the softmax writes as
+    // soon as S(g) is complete, before P(g).  Flags of S(g) for its PV, 4 bits in
     // slot g % 4: first KV tile of its tile, last, the tile's ordinal (with
     // keys) odd, ordinal 0.
     int ns = 0;
@@ -407,7 +478,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     constexpr int kBarK = Geo::kAuto ? Geo::kBarCodesK : Geo::kBarKFull;
     constexpr int kBarV = Geo::kAuto ? Geo::kBarCodesV : Geo::kBarVFull;
     auto wait = [&](int b, uint32_t parity) {
-      return __all_sync(0xffffffffu, wait_or_abort(bar(b), parity, abort_flag));
+      return __all_sync(0xffffffffu, wait_or_abort<CG>(bar(b), parity, abort_flag));
     };
     auto next_s = [&]() -> bool {  // S(ns) at the cursor
       if (cs.j == 0 && !wait(Geo::kBarQFull, (uint32_t)(cs.n & 1))) return false;
@@ -423,8 +494,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     };
     if (cs.valid) ok = next_s();
     for (int g = 0; ok && g < ns; ++g) {
-      const bool s_after = cs.valid && cs.j == 0;  // S(g+1) starts a tile: after PV(g)
-      if (cs.valid && !s_after && !(ok = next_s())) break;
+      if (cs.valid && !(ok = next_s())) break;
       const uint32_t f = (flags >> (4 * (g & 3))) & 0xFu;
       // O of the previous tile read out: its OFree completion (ordinal - 1)
       if ((f & 1u) && !(f & 8u) && !(ok = wait(Geo::kBarOFree, ((f >> 2) & 1u) ^ 1u))) break;
@@ -433,12 +503,12 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         break;
       tc::fence_after_sync();
       issue_pv(g, (f & 1u) != 0, (f & 2u) != 0);
-      if (s_after && !(ok = next_s())) break;
     }
     if (!ok && leader) {
       // Drain whatever was issued before the tensor memory is freed.
-      tc::mma_commit(bar(Geo::kBarDrain));
+      tc::mma_commit<CG>(bar(Geo::kBarDrain), 1);
       (void)tc::mbar_wait(bar(Geo::kBarDrain), 0u, 200000000LL);
+    }
     }
     __syncwarp();
   } else if (warp == kCopyWarp) {
@@ -460,7 +530,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         const int j0 = kv0 + 16 * c;
         blk[c] = -1;
         off[c] = 0;
-        if (j0 + 16 > r.t.kv_lo && j0 < r.t.kv_hi) {
+        if (j0 + 16 > r.lo && j0 < r.hi) {
           uint32_t q = __umulhi((uint32_t)j0, bdiv);
           uint32_t rr = (uint32_t)j0 - q * bsz;
           if (rr >= bsz) {
@@ -485,7 +555,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       }
     };
     const bool leader = elect_one();
-    KvCursor<kN> ck;
+    KvCursor<kN, CG> ck;
     ck.start(p);
     int nx_blk[kChunks];
     uint32_t nx_off[kChunks];
@@ -642,38 +712,52 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     // chunk without a block) load as zero.  The two 16-byte f16 chunks go
     // out in the order that keeps the 8 lanes of a quarter-warp on 8 bank
     // groups (lanes in odd 64-dim blocks store their odd chunk first).  A
-    // unit's offsets do not change from tile to tile.
-    constexpr int kPieces = D / 16;
-    constexpr int kUnits = kN * kPieces;
+    // unit's offsets do not change from tile to tile.  A CTA of a pair
+    // converts its half of each tile: of K, keys [r * kN / 2, (r + 1) * kN / 2)
+    // (rows of its K tile); of V, dims [r * D / 2, (r + 1) * D / 2) of every
+    // key (columns of its V tile).
+    constexpr int kUnits = kN * D / 16 / CG;
     constexpr int kSlots = (kUnits + Geo::kConv - 1) / Geo::kConv;
     constexpr int64_t kRow = row_bytes(DT, D);
-    uint32_t code_off[kSlots], st_first[kSlots], st_second[kSlots];
-    uint32_t odd_mask = 0;
+    struct Units {
+      uint32_t code_off[kSlots];  // key in the tile * D + dim in the row
+      uint32_t st_first[kSlots], st_second[kSlots], odd_mask;
+    };
+    // units of a tile held as `rows` rows of `pieces` 16-code pieces, its
+    // row n being key key0 + n, dims from dim0
+    auto make_units = [&](int rows, int pieces, int key0, int dim0) {
+      Units t;
+      t.odd_mask = 0;
 #pragma unroll
-    for (int i = 0; i < kSlots; ++i) {
-      const int u = min(ctid + i * Geo::kConv, kUnits - 1);
-      const int n = u / kPieces, pc = u % kPieces;
-      const bool odd = (pc >> 2) & 1;
-      const uint32_t a_lo = tc::sw128_offset(kN, n, 16 * pc), a_hi = tc::sw128_offset(kN, n, 16 * pc + 8);
-      code_off[i] = (uint32_t)(n * D + 16 * pc);
-      st_first[i] = odd ? a_hi : a_lo;
-      st_second[i] = odd ? a_lo : a_hi;
-      odd_mask |= (odd ? 1u : 0u) << i;
-    }
+      for (int i = 0; i < kSlots; ++i) {
+        const int u = min(ctid + i * Geo::kConv, kUnits - 1);
+        const int n = u / pieces, pc = u % pieces;
+        const bool odd = (pc >> 2) & 1;
+        const uint32_t a_lo = tc::sw128_offset(rows, n, 16 * pc), a_hi = tc::sw128_offset(rows, n, 16 * pc + 8);
+        t.code_off[i] = (uint32_t)((key0 + n) * D + dim0 + 16 * pc);
+        t.st_first[i] = odd ? a_hi : a_lo;
+        t.st_second[i] = odd ? a_lo : a_hi;
+        t.odd_mask |= (odd ? 1u : 0u) << i;
+      }
+      return t;
+    };
+    const Units uk = make_units(Geo::kKeysK, D / 16, (int)rank * Geo::kKeysK, 0);
+    const Units uv = CG == 1 ? uk : make_units(kN, Geo::kDimsV / 16, 0, (int)rank * Geo::kDimsV);
     const int32_t* table = reinterpret_cast<const int32_t*>(sm + Geo::kOffSlots);
     // Codes of KV tile g (slot table entry e, kv head `head`, live keys
     // [win & 0xFFFF, win >> 16) of the tile) into registers; returns the
     // tile's chunk mask.
-    auto load_codes = [&](const uint8_t* cache, int e, int head, uint32_t win, uint4 (&dst)[kSlots]) {
+    auto load_codes = [&](const Units& un, const uint8_t* cache, int e, int head, uint32_t win,
+                          uint4 (&dst)[kSlots]) {
       const uint32_t valid = (uint32_t)table[e * 16 + 15];
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
         dst[i] = make_uint4(0, 0, 0, 0);
-        const int n = (int)(code_off[i] / D);
+        const int n = (int)(un.code_off[i] / D);
         if (ctid + i * Geo::kConv < kUnits && ((valid >> (n >> 4)) & 1u) && n >= (int)(win & 0xFFFFu) &&
             n < (int)(win >> 16)) {
           const int64_t slot = table[e * 16 + (n >> 4)] + (n & 15);
-          dst[i] = dev::ldg_stream(cache + (slot * p.heads_kv + head) * kRow + (code_off[i] & (D - 1)));
+          dst[i] = dev::ldg_stream(cache + (slot * p.heads_kv + head) * kRow + (un.code_off[i] & (D - 1)));
         }
       }
       return valid;
@@ -691,27 +775,30 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         }
       }
     };
-    auto convert = [&](uint32_t tile, const uint4 (&c)[kSlots]) {
+    auto convert = [&](const Units& un, uint32_t tile, const uint4 (&c)[kSlots]) {
 #pragma unroll
       for (int i = 0; i < kSlots; ++i) {
         if (ctid + i * Geo::kConv < kUnits) {
-          const bool odd = (odd_mask >> i) & 1u;
-          sts128(tile + st_first[i], codes8_to_f16<DT>(odd ? c[i].z : c[i].x, odd ? c[i].w : c[i].y));
-          sts128(tile + st_second[i], codes8_to_f16<DT>(odd ? c[i].x : c[i].z, odd ? c[i].y : c[i].w));
+          const bool odd = (un.odd_mask >> i) & 1u;
+          sts128(tile + un.st_first[i], codes8_to_f16<DT>(odd ? c[i].z : c[i].x, odd ? c[i].w : c[i].y));
+          sts128(tile + un.st_second[i], codes8_to_f16<DT>(odd ? c[i].x : c[i].z, odd ? c[i].y : c[i].w));
         }
       }
     };
+    // The converted tile is visible to the tensor core (for a pair, the MMAs
+    // the even CTA issues read it after that CTA's barrier wait).
+    auto fence_operands = [&]() { tc::fence_async_smem(); };
     // A KV tile's live keys relative to its first key, packed lo | hi << 16.
-    auto window_of = [&](const KvCursor<kN>& c) {
+    auto window_of = [&](const KvCursor<kN, CG>& c) {
       const int kv0 = c.cur.kv_first + c.j * kN;
-      const int klo = min(max(c.cur.t.kv_lo - kv0, 0), kN), khi = min(max(c.cur.t.kv_hi - kv0, 0), kN);
+      const int klo = min(max(c.cur.lo - kv0, 0), kN), khi = min(max(c.cur.hi - kv0, 0), kN);
       return (uint32_t)klo | ((uint32_t)khi << 16);
     };
     // Step g: convert K(g) (its buffer is free once S(g - 2) is complete)
     // and publish its side data; load K(g + 1); convert V(g - 1) (its buffer
     // is free once P(g - 3) V(g - 3) is complete); load V(g), after which
     // slot table g is released.
-    KvCursor<kN> ck;
+    KvCursor<kN, CG> ck;
     ck.start(p);
     uint4 ka[kSlots], vb[kSlots];
     float ks_a = 0.0f, vs_a = 0.0f;
@@ -721,7 +808,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlots), 0u, abort_flag));
       if (ok) {
         win_a = window_of(ck);
-        valid_a = load_codes(p.key_cache, 0, ck.cur.t.kv_head, win_a, ka);
+        valid_a = load_codes(uk, p.key_cache, 0, ck.cur.t.kv_head, win_a, ka);
         load_scales(0, ck.cur.t.kv_head, win_a, valid_a, ks_a, vs_a);
       }
     }
@@ -750,32 +837,41 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           if ((ctid & 31) == 0 && (ctid >> 5) < (kN + 31) / 32) vmaxw[sd * 8 + (ctid >> 5)] = wmax;
         }
         warp_arrive(bar(Geo::kBarSide + sd));
-        convert(base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), ka);
-        tc::fence_async_smem();
-        warp_arrive(bar(Geo::kBarKFull + st));
+        convert(uk, base + Geo::kOffK + (uint32_t)(st * Geo::kTileBytes), ka);
+        fence_operands();
+        warp_arrive_mma<CG>(bar(Geo::kBarKFull + st), rank);
         ck.advance(p);
-        if (ck.valid) {
+      }
+      // K(g + 1) into registers.  The odd CTA of a pair issues it after
+      // V(g - 1)'s arrival: an arrival on the other CTA's barrier releases at
+      // cluster scope, which waits for this thread's loads in flight.
+      auto load_next_k = [&]() -> bool {
+        if (have_k && ck.valid) {
           const int e1 = (g + 1) & (Geo::kSlotRing - 1);
-          if (!(ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlots + e1),
-                                                            (uint32_t)(((g + 1) / Geo::kSlotRing) & 1), abort_flag))))
-            break;
+          if (!__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarSlots + e1),
+                                                     (uint32_t)(((g + 1) / Geo::kSlotRing) & 1), abort_flag)))
+            return false;
           win_a = window_of(ck);
-          valid_a = load_codes(p.key_cache, e1, ck.cur.t.kv_head, win_a, ka);
+          valid_a = load_codes(uk, p.key_cache, e1, ck.cur.t.kv_head, win_a, ka);
           load_scales(e1, ck.cur.t.kv_head, win_a, valid_a, ks_a, vs_a);
         }
-      }
+        return true;
+      };
+      const bool defer_k = CG == 2 && rank != 0;
+      if (!defer_k && !(ok = load_next_k())) break;
       if (g >= 1) {
         const int gv = g - 1, st = gv & 1;
         if (gv >= 2 && !(ok = __all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarVEmpty + st),
                                                                      (uint32_t)(((gv >> 1) - 1) & 1), abort_flag))))
           break;
-        convert(base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), vb);
-        tc::fence_async_smem();
-        warp_arrive(bar(Geo::kBarVFull + st));
+        convert(uv, base + Geo::kOffV + (uint32_t)(st * Geo::kTileBytes), vb);
+        fence_operands();
+        warp_arrive_mma<CG>(bar(Geo::kBarVFull + st), rank);
       }
+      if (defer_k && !(ok = load_next_k())) break;
       if (!have_k) break;
       const int e = g & (Geo::kSlotRing - 1);
-      (void)load_codes(p.value_cache, e, head_g, win_g, vb);
+      (void)load_codes(uv, p.value_cache, e, head_g, win_g, vb);
       warp_arrive(bar(Geo::kBarSlotsFree + e));
     }
     }
@@ -806,102 +902,103 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     // Next tile with keys after ordinal k (k moves to it); false: none.
     auto next_run = [&](int& k, TileRun<kN>& r) -> bool {
       while (true) {
-        const int idx = dealt_tile(++k);
+        const int idx = dealt_tile<CG>(++k);
         if (idx >= p.num_prefill_tiles) return false;
-        r.set(p.prefill_tiles[idx]);
+        PrefillTile x, y;
+        load_tiles<CG>(p, idx, x, y);
+        r.set(x, y);
         if (r.T > 0) return true;
         zero_rows(r.t);
       }
     };
-    // Q row m of a tile -> tensor memory (columns kColQ.., f16 pairs), and
-    // the arrival that lets the tile's first S go.  Q enters as f16 exactly:
-    // the row is scaled by the power of two that puts its largest |q| in
-    // [2^13, 2^14) (a bf16 significand fits in f16's).  Elements more than
-    // about 2^27 below the row's largest land in f16's subnormal range (bits
-    // lost) or flush to zero: a Q row with that dynamic range loses them.
-    // The raw bf16 row goes to tensor memory first (batches of 8 16-byte
-    // loads, two batches in flight) while its largest exponent is found;
-    // then it is converted in place.  bf16 rows ("auto") enter the bf16 MMA
-    // as they are.  Returns the row's 2^-shift.
-    auto load_q = [&](const TileRun<kN>& r) -> float {
-      constexpr int kQv = D / 8;               // 16-byte pieces of a row
-      constexpr int kB = kQv < 8 ? kQv : 8;    // pieces per batch
-      const PrefillTile& t = r.t;
+    // Q rows of a tile are staged in shared memory a tile ahead: each thread
+    // copies its row of the next tile (one bulk copy, completing on the
+    // QStage barrier) into its row of the output staging area, which is free
+    // from the previous tile's bulk store until this tile's epilogue.  Rows
+    // past the tile's end copy nothing.
+    const uint32_t srow = base + Geo::kOffOut + (uint32_t)(m * Geo::kOutPitch);
+    auto stage_q = [&](const PrefillTile& t) {
       const bool valid = m < t.nrows;
-      const int Rq = t.row0 + (valid ? m : 0);
-      const uint4* src = reinterpret_cast<const uint4*>(
-          p.q + ((int64_t)(t.q0 + Rq / G) * p.heads_q + t.kv_head * G + Rq % G) * D);
-      int emax = 0;
-      uint4 qa[kB];
-#pragma unroll
-      for (int c = 0; c < kB; ++c) qa[c] = valid ? src[c] : make_uint4(0, 0, 0, 0);
-#pragma unroll
-      for (int b = 0; b < kQv / kB; ++b) {
-        uint4 qb[kB];
-#pragma unroll
-        for (int c = 0; c < kB; ++c)
-          qb[c] = valid && b + 1 < kQv / kB ? src[(b + 1) * kB + c] : make_uint4(0, 0, 0, 0);
-        uint32_t w[4 * kB];
-#pragma unroll
-        for (int c = 0; c < kB; ++c) {
-          const uint32_t x[4] = {qa[c].x, qa[c].y, qa[c].z, qa[c].w};
-#pragma unroll
-          for (int e = 0; e < 4; ++e) {
-            w[4 * c + e] = x[e];
-            emax = max(emax, (int)max((x[e] >> 7) & 0xFFu, (x[e] >> 23) & 0xFFu));
-          }
-        }
-#pragma unroll
-        for (int h = 0; h < 4 * kB; h += 16)
-          tc::tmem_st16(tmem + Geo::kColQ + lane_base + (uint32_t)(b * 4 * kB + h),
-                        *reinterpret_cast<uint32_t(*)[16]>(w + h));
-#pragma unroll
-        for (int c = 0; c < kB; ++c) qa[c] = qb[c];
+      // (this thread's previous bulk store has read its staging row)
+      asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
+      mbar_arrive_expect_tx(bar(Geo::kBarQStage), valid ? (uint32_t)(D * 2) : 0u);
+      if (valid) {
+        const int Rq = t.row0 + m;
+        const uint16_t* src = p.q + ((int64_t)(t.q0 + Rq / G) * p.heads_q + t.kv_head * G + Rq % G) * D;
+        asm volatile(
+            "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];"
+            :: "r"(srow), "l"(reinterpret_cast<uint64_t>(src)), "n"(D * 2), "r"(bar(Geo::kBarQStage))
+            : "memory");
       }
-      tc::tmem_wait_st();
+    };
+    // Staged Q row m of the tile with ordinal (with keys) n_tile -> tensor
+    // memory (columns kColQ.., f16 pairs), and the arrival that lets the
+    // tile's first S go.  Q enters as f16 exactly: the row is scaled by the
+    // power of two that puts its largest |q| in [2^13, 2^14) (a bf16
+    // significand fits in f16's).  Elements more than about 2^27 below the
+    // row's largest land in f16's subnormal range (bits lost) or flush to
+    // zero: a Q row with that dynamic range loses them.  bf16 rows ("auto")
+    // enter the bf16 MMA as they are.  Returns the row's 2^-shift.
+    auto load_q = [&](int nrows, int n_tile) -> float {
+      const bool valid = m < nrows;
+      (void)__all_sync(0xffffffffu, wait_or_abort(bar(Geo::kBarQStage), (uint32_t)(n_tile & 1), abort_flag));
+      int emax = 0;
+      if (valid && !Geo::kAuto) {
+#pragma unroll 8
+        for (int c = 0; c < D / 8; ++c) {
+          const uint4 x4 = lds128(srow + (uint32_t)(16 * c));
+          const uint32_t x[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e) emax = max(emax, (int)max((x[e] >> 7) & 0xFFu, (x[e] >> 23) & 0xFFu));
+        }
+      }
       // largest |q| < 2^(emax - 126): scaled into [2^13, 2^14)
       const int sh = emax == 0 || Geo::kAuto ? 0 : min(140 - emax, 126);
-      if constexpr (!Geo::kAuto) {
-        const float up = ldexpf(1.0f, sh);
+      const float up = ldexpf(1.0f, sh);
 #pragma unroll 1
-        for (int c0 = 0; c0 < D / 2; c0 += 32) {
-          uint32_t w[32];
-          tc::tmem_ld32(tmem + Geo::kColQ + lane_base + (uint32_t)c0, w);
-          tc::tmem_wait_ld();
+      for (int h = 0; h < D / 2; h += 16) {
+        uint32_t w[16];
 #pragma unroll
-          for (int e = 0; e < 32; ++e) w[e] = dev::pack_f16x2(dev::bf16_lo(w[e]) * up, dev::bf16_hi(w[e]) * up);
-          tc::tmem_st32(tmem + Geo::kColQ + lane_base + (uint32_t)c0, w);
+        for (int c = 0; c < 4; ++c) {
+          const uint4 x4 = valid ? lds128(srow + (uint32_t)(4 * h + 16 * c)) : make_uint4(0, 0, 0, 0);
+          const uint32_t x[4] = {x4.x, x4.y, x4.z, x4.w};
+#pragma unroll
+          for (int e = 0; e < 4; ++e)
+            w[4 * c + e] = Geo::kAuto ? x[e] : dev::pack_f16x2(dev::bf16_lo(x[e]) * up, dev::bf16_hi(x[e]) * up);
         }
-        tc::tmem_wait_st();
+        tc::tmem_st16(tmem + Geo::kColQ + lane_base + (uint32_t)h, w);
       }
+      tc::tmem_wait_st();
       tc::fence_before_sync();
-      warp_arrive(bar(Geo::kBarQFull));
+      warp_arrive_mma<CG>(bar(Geo::kBarQFull), rank);
       return ldexpf(1.0f, -sh);
     };
 
     TileRun<kN> cur;
     int k = -1;
     bool have = next_run(k, cur);
-    float q_unscale = have ? load_q(cur) : 1.0f;
+    if (have) stage_q(cur.t);
+    float q_unscale = have ? load_q(cur.t.nrows, 0) : 1.0f;
     bool ok = true;
     int g = 0;
+    int staged = 0;  // tiles whose Q was staged
+    if (have) staged = 1;
     for (int n = 0; have; ++n) {
-      // The next tile with keys (its record is read again after this tile's
-      // loop, from L1: only its ordinal stays in registers).
+      // The next tile with keys (its record is read again when its Q is
+      // staged and after this tile's loop, from L1: only its ordinal stays
+      // in registers).
       int k2 = k;
       {
         TileRun<kN> nxt;
         if (!next_run(k2, nxt)) k2 = -1;
-        const bool have_next = k2 >= 0;
-        if (have_next && m < nxt.t.nrows) {
-          // the next tile's Q row into L2 now (its load then comes from L2)
-          const int Rn = nxt.t.row0 + m;
-          const char* qn = reinterpret_cast<const char*>(
-              p.q + ((int64_t)(nxt.t.q0 + Rn / G) * p.heads_q + nxt.t.kv_head * G + Rn % G) * D);
-#pragma unroll
-          for (int off = 0; off < D * 2; off += 128) asm volatile("prefetch.global.L2 [%0];" :: "l"(qn + off));
-        }
       }
+      // the next tile's Q rows into the staging area (free from this
+      // thread's previous bulk store until this tile's epilogue)
+      if (k2 >= 0) {
+        stage_q(p.prefill_tiles[dealt_tile<CG>(k2)]);
+        ++staged;
+      }
+      float q_next = 1.0f;
       const PrefillTile& t = cur.t;
       const int kv_first = cur.kv_first, T = cur.T;
       const bool row_valid = m < t.nrows;
@@ -931,6 +1028,9 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         ok = __all_sync(0xffffffffu, ok);  // warp-uniform: the warp's tensor-memory accesses are collective
         if (!ok) break;
         tc::fence_after_sync();
+        // S(g), this tile's last, is complete: Q's tensor memory takes the
+        // next tile's Q now, so that its first S runs beside this softmax.
+        if (j == T - 1 && k2 >= 0) q_next = load_q(p.prefill_tiles[dealt_tile<CG>(k2)].nrows, n + 1);
         const uint32_t tmem_s = tmem + Geo::kColS + (uint32_t)(st * kN) + lane_base;
         // Visible keys n of this row: lo_n <= n < hi_n, in a 16-key chunk
         // that was copied.  Masks are needed unless every row of the warp
@@ -1122,17 +1222,16 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         }
         tc::tmem_wait_st();
         tc::fence_before_sync();
-        warp_arrive(bar(Geo::kBarPFull + st));
+        warp_arrive_mma<CG>(bar(Geo::kBarPFull + st), rank);
       }
       if (!ok) break;
-      // Every S of this tile is complete (the last one was waited for), so
-      // the next tile's Q may replace this one's; its first S can then run
-      // while this tile's last P V and epilogue do.
+      // (the next tile's Q is in tensor memory: loaded at this tile's last
+      // KV tile)
       TileRun<kN> nxt;
-      float q_next = 1.0f;
       if (k2 >= 0) {
-        nxt.set(p.prefill_tiles[dealt_tile(k2)]);
-        q_next = load_q(nxt);
+        PrefillTile x, y;
+        load_tiles<CG>(p, dealt_tile<CG>(k2), x, y);
+        nxt.set(x, y);
       }
       // ---- epilogue: O / l -> bf16 rows in shared memory; then O is free
       // for the next tile's first P V, and each row goes to global memory by
@@ -1143,7 +1242,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       // An attention sink joins the normaliser (the weights carry
       // 2^-(m_ref - 6)).
       // (this tile's record again, from L1: not kept in registers over the loop)
-      const PrefillTile te = p.prefill_tiles[dealt_tile(k)];
+      const PrefillTile te = p.prefill_tiles[dealt_tile<CG>(k)];
       if (p.sinks && m < te.nrows && m_ref != -INFINITY) {
         const float skl = p.sinks[te.kv_head * G + (te.row0 + m) % G] * log2e;
         if (skl != -INFINITY) l_sum += exp2f(fminf(skl - m_ref + 6.0f, 126.0f));
@@ -1170,7 +1269,7 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
         }
       }
       tc::fence_before_sync();
-      warp_arrive(bar(Geo::kBarOFree));
+      warp_arrive_mma<CG>(bar(Geo::kBarOFree), rank);
       if (dst) {
         tc::fence_async_smem();
         asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;\n\t"
@@ -1182,18 +1281,25 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       have = k2 >= 0;
       q_unscale = q_next;
     }
-    // The rows' bulk copies are complete before the shared memory goes.
+    // The rows' bulk copies are complete before the shared memory goes (and
+    // a staged Q that was not used, after an abort, has landed).
     asm volatile("cp.async.bulk.wait_group 0;" ::: "memory");
+    if (staged > 0) (void)tc::mbar_wait(bar(Geo::kBarQStage), (uint32_t)((staged - 1) & 1), 200000000LL);
     // Order this warp's tensor-memory accesses before the teardown barrier.
     tc::fence_before_sync();
     __syncwarp();
   }
 
-  __syncthreads();
+  // (a pair: neither CTA leaves while the other's MMAs may read its shared
+  // or tensor memory, or its warps may arrive on its barriers)
+  if constexpr (CG == 2)
+    tc::cluster_sync();
+  else
+    __syncthreads();
   const bool aborted = *abort_flag != 0u;
   if (warp == 0) {
     tc::fence_after_sync();
-    tc::tmem_dealloc(tmem, Geo::kTmemCols);
+    tc::tmem_dealloc<CG>(tmem, Geo::kTmemCols);
   }
   // A CTA that gave up a bounded wait writes NaN over every row of its
   // tiles, so its failure shows in the output even where nobody reads the
@@ -1205,8 +1311,8 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
     const int lane = tid & 31;
     const int sub = lane / kLpr, c = lane % kLpr;
     const uint4 nan4 = make_uint4(0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u, 0x7FC07FC0u);
-    for (int k = 0; dealt_tile(k) < p.num_prefill_tiles; ++k) {
-      const PrefillTile t = p.prefill_tiles[dealt_tile(k)];
+    for (int k = 0; dealt_tile<CG>(k) < p.num_prefill_tiles; ++k) {
+      const PrefillTile t = p.prefill_tiles[dealt_tile<CG>(k)];
       for (int r = warp * kRps + sub; r < t.nrows; r += (Geo::kThreads / 32) * kRps) {
         const int Rr = t.row0 + r;
         *reinterpret_cast<uint4*>(p.out + ((int64_t)(t.q0 + Rr / G) * p.heads_q + t.kv_head * G + Rr % G) * D +
@@ -1216,15 +1322,51 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
   }
 }
 
+// `ctas`: CTAs wanted (one per SM, or fewer).  CTA pairs launch as clusters
+// of two: max(1, ctas / 2) of them, at most as many as fit on the device at
+// once (the kernel is persistent: a second wave would run its pairs' whole
+// tile lists after the first).
 template <int DT, int D, bool AL>
 int launch_prefill_instance(const AttnParams& p, const PrefillMaps& maps, int64_t ctas,
                             cudaStream_t stream) {
-  const size_t smem = prefill_smem_bytes(D);
+  constexpr int CG = prefill_cta_group(DT, D);
+  const size_t smem = prefill_smem_bytes(D, CG);
   auto kern = prefill_attention_kernel<DT, D, AL>;
   if (cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
       cudaSuccess)
     return KVQ_E_CUDA;
-  kern<<<(unsigned)ctas, prefill_threads(D), smem, stream>>>(p, maps);
+  if constexpr (CG == 1) {
+    kern<<<(unsigned)ctas, prefill_threads(D), smem, stream>>>(p, maps);
+  } else {
+    cudaLaunchConfig_t cfg = {};
+    cfg.blockDim = dim3(prefill_threads(D));
+    cfg.dynamicSmemBytes = smem;
+    cfg.stream = stream;
+    cudaLaunchAttribute attr[1];
+    attr[0].id = cudaLaunchAttributeClusterDimension;
+    attr[0].val.clusterDim.x = 2;
+    attr[0].val.clusterDim.y = 1;
+    attr[0].val.clusterDim.z = 1;
+    cfg.attrs = attr;
+    cfg.numAttrs = 1;
+    static const int max_pairs = [&]() {
+      cudaLaunchConfig_t q = cfg;
+      q.gridDim = dim3(2);
+      int n = 0;
+      if (cudaOccupancyMaxActiveClusters(&n, kern, &q) != cudaSuccess) {
+        cudaGetLastError();
+        n = 0;
+      }
+      return n;
+    }();
+    int64_t pairs = std::max<int64_t>(1, ctas / 2);
+    if (max_pairs > 0) pairs = std::min<int64_t>(pairs, max_pairs);
+    cfg.gridDim = dim3((unsigned)(2 * pairs));
+    if (cudaLaunchKernelEx(&cfg, kern, p, maps) != cudaSuccess) {
+      cudaGetLastError();
+      return KVQ_E_CUDA;
+    }
+  }
   return cudaGetLastError() == cudaSuccess ? KVQ_OK : KVQ_E_CUDA;
 }
 

@@ -59,7 +59,8 @@ class SchedInfo(ctypes.Structure):
                 ("decode_chunk_bytes", ctypes.c_size_t),
                 ("num_prefill_tiles", ctypes.c_int64),
                 ("prefill_smem_bytes", ctypes.c_size_t),
-                ("num_kernel_launches", ctypes.c_int64)]
+                ("num_kernel_launches", ctypes.c_int64),
+                ("prefill_cta_group", ctypes.c_int64)]
 
     def as_dict(self):
         return {k: getattr(self, k) for k, _ in self._fields_}

@@ -61,10 +61,26 @@ def check_plan(seq_lens, query_lens, hq=32, hkv=8, D=128, causal=True, window=0,
     decode, prefill = derive(seq_lens, query_lens, hq, hkv, causal, window)
     P = plan["pieces"]
 
-    # prefill tiles: the derived set, longest key range first
-    got = [tuple(int(x) for x in t) for t in plan["prefill_tiles"]]
+    # prefill tiles: the derived set, longest key range first.  A build with
+    # CTA pairs (quantised caches at head_dim >= 128): list entries 2i, 2i + 1
+    # are consecutive row tiles of one (request, kv head) (or a last tile and
+    # an empty partner, nrows 0), longest key-range union first.
+    allt = [tuple(int(x) for x in t) for t in plan["prefill_tiles"]]
+    got = [t for t in allt if t[3] > 0]
     assert sorted(got) == sorted(prefill)
-    spans = [t[5] - t[4] for t in got]
+    if info["prefill_cta_group"] == 2:
+        assert len(allt) % 2 == 0
+        spans = []
+        for a, b in zip(allt[0::2], allt[1::2]):
+            assert (a[0], a[1]) == (b[0], b[1]) and b[2] == a[2] + a[3] and a[3] > 0
+            assert a[3] == 128 or b[3] == 0
+            if b[3] == 0:
+                # the empty partner: the last tile of its (request, kv head)
+                assert a[2] + a[3] == query_lens[a[0]] * (hq // hkv) and b[4:] == a[4:]
+            spans.append(max(a[5], b[5]) - min(a[4], b[4]))
+    else:
+        assert len(allt) == len(got)
+        spans = [t[5] - t[4] for t in got]
     assert all(a >= b for a, b in zip(spans, spans[1:]))
 
     # decode tiles: the derived set, each in its launch class
