@@ -20,6 +20,9 @@ LIB = os.path.join(HERE, "libkvq.so")
 # The bounds-checked build (-DKVQ_CHECKED=1): same sources, its own objects.
 BUILD_CHECKED = os.path.join(HERE, "_build", platform.machine() + "-checked")
 LIB_CHECKED = os.path.join(HERE, "libkvq_checked.so")
+# The prefill on CTA pairs (-DKVQ_PREFILL_PAIR=1), a build option.
+BUILD_PAIR = os.path.join(HERE, "_build", platform.machine() + "-pair")
+LIB_PAIR = os.path.join(HERE, "libkvq_pair.so")
 INCLUDE = os.path.join(os.path.dirname(HERE), "include")
 
 ARCH = ["-gencode", "arch=compute_103a,code=sm_103a"]
@@ -56,11 +59,16 @@ def _compile(src: str, force: bool, extra, build_dir: str = BUILD) -> str:
     return obj
 
 
-def build(force: bool = False, extra_flags=(), jobs: int = 0, checked: bool = False) -> str:
+def build(force: bool = False, extra_flags=(), jobs: int = 0, checked: bool = False,
+          pair: bool = False) -> str:
     """Compile and link libkvq.so (checked: libkvq_checked.so, the
-    bounds-checked build); returns its path."""
-    build_dir, lib = (BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD, LIB)
-    extra = list(extra_flags) + (["-DKVQ_CHECKED=1"] if checked else [])
+    bounds-checked build; pair: libkvq_pair.so, the prefill on CTA pairs);
+    returns its path."""
+    assert not (checked and pair)
+    build_dir, lib = ((BUILD_CHECKED, LIB_CHECKED) if checked else (BUILD_PAIR, LIB_PAIR) if pair
+                      else (BUILD, LIB))
+    extra = (list(extra_flags) + (["-DKVQ_CHECKED=1"] if checked else [])
+             + (["-DKVQ_PREFILL_PAIR=1"] if pair else []))
     os.makedirs(build_dir, exist_ok=True)
     srcs = sorted(glob.glob(os.path.join(CSRC, "*.cu")) + glob.glob(os.path.join(CSRC, "*.cpp")))
     jobs = jobs or min(len(srcs), os.cpu_count() or 4)

@@ -10,30 +10,29 @@
 // item 3 (_prepare_kv_tile); vllm PR 50194 page, Key source snippet (the
 // large fp8 prefill with block_size 2176).
 //
-// GB300 design: one CTA of 16 warps (12 at head_dim 256) per 128-row tile,
-// warp-specialised and pipelined through mbarriers.
+// GB300 design: persistent CTAs (one per SM) walking a dealt list of tiles,
+// 16 warps (12 at head_dim 256), warp-specialised and pipelined through
+// mbarriers.
 //   * Tensor memory (512 columns): O (D fp32 columns), two S buffers (keys
 //     fp32 columns each; P(j) is written as f16 pairs over the first half of
 //     S(j)'s buffer), and Q (D/2 columns of f16 pairs).  Both MMAs take A
 //     from tensor memory: S = Q K^T and O += P V read only K and V from
 //     shared memory.
-//   * Copy warp (the last): bulk tensor copies (TMA) of each tile's K codes
-//     (with both per-token-head scale tails) and V codes into a two-stage
-//     code ring, in two groups with a barrier each; the K group of tile
-//     j + 2 goes out once K(j) is converted, the V group once V(j) is.
+//   * Copy warp (the last): resolves each KV tile's 16-key chunks through
+//     the block table into first slots (a slot table per KV tile, up to four
+//     ahead).  bf16 ("auto") rows: bulk tensor copies (TMA) of the chunks
+//     straight into the K and V operand tiles.
 //   * Converter warps (1-3, and 8 up to the copy warp): a thread takes (key,
-//     16 codes) units, converts the codes exactly to f16 (every e4m3 / e5m2
-//     / int8 value is an f16 value) and stores them as key-major rows in the
-//     128-byte swizzle into a two-stage K ring and V ring.  K is read by the
-//     tensor core K-major, V MN-major, so neither needs a transpose.  Step i
-//     converts K(i) (its buffer is free once S(i-2) is complete) and then
-//     V(i-1) (free once P(i-3) V(i-3) is): K runs a tile ahead of V.
-//     Per-key scales, the tile's chunk mask and its largest value scale go
-//     to one of four side-data slots for the softmax.
-//   * MMA warp (0): one elected lane issues S(j) as soon as K(j) is in and
-//     PV(j-2) was issued (P(j-2) shares the buffer; one thread's MMAs run in
-//     order), and O += P(j) V(j) as soon as P(j) and V(j) are in; one
-//     warp-wide non-blocking barrier test per pass decides for the warp.
+//     16 codes) units, loads the codes from global memory one KV tile ahead,
+//     converts them exactly to f16 (every e4m3 / e5m2 / int8 value is an f16
+//     value) and stores them as key-major rows in the 128-byte swizzle into a
+//     two-stage K ring and V ring.  K is read by the tensor core K-major, V
+//     MN-major, so neither needs a transpose.  Step i converts K(i) (its
+//     buffer is free once S(i-2) is complete) and then V(i-1) (free once
+//     P(i-3) V(i-3) is).  Per-key scales, the tile's chunk mask and its
+//     largest value scale go to one of four side-data slots for the softmax.
+//   * MMA warp (0): one elected lane issues, in a fixed order, S(j+1) and
+//     then O += P(j) V(j), each once its operands are in (blocking waits).
 //   * Softmax warps (4-7): thread t owns row t (tensor-memory lane t).  One
 //     pass over its row of S, 64 scores per tensor-memory round trip: the
 //     round's maximum, then the weights, written as f16 straight into
@@ -41,8 +40,9 @@
 //     lazy: it moves only when a score exceeds it by 2^8 (weights are lifted
 //     by 2^6, so P <= 2^14), to the next integer at or above the maximum,
 //     and the weights, O and l already accumulated are rescaled by the exact
-//     power of two (O only after P(j-1) V(j-1) is complete).  At the end it
-//     reads O and writes bf16.
+//     power of two (O only after P(j-1) V(j-1) is complete; 32 columns a
+//     round, the next round's tensor-memory load in flight).  At the end it
+//     reads O and stages bf16 rows for one bulk store per row.
 //   * Q rows of the next tile are bulk-copied into shared memory (the output
 //     staging area, free between epilogues) when a tile starts, and moved
 //     into tensor memory once the tile's last S is complete, so that the
@@ -1210,14 +1210,26 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
                           wait_or_abort(bar(Geo::kBarODone), (uint32_t)((g - 1) & 1), abort_flag));
           if (!ok) break;
           tc::fence_after_sync();
-#pragma unroll 1
-          for (int c0 = 0; c0 < D; c0 += 32) {
-            uint32_t v[32];
-            tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
-            tc::tmem_wait_ld();
+          // 32 columns per round, the next round's load in flight while
+          // this one is scaled and stored
+          const uint32_t orow_t = tmem + Geo::kColO + lane_base;
+          auto scale32 = [&](uint32_t (&v)[32]) {
 #pragma unroll
             for (int e = 0; e < 32; ++e) v[e] = __float_as_uint(__uint_as_float(v[e]) * alpha);
-            tc::tmem_st32(tmem + Geo::kColO + lane_base + c0, v);
+          };
+          uint32_t va[32], vb[32];
+          tc::tmem_ld32(orow_t, va);
+          tc::tmem_wait_ld_for(va);
+#pragma unroll 1
+          for (int c0 = 0; c0 < D; c0 += 64) {
+            tc::tmem_ld32(orow_t + (uint32_t)(c0 + 32), vb);
+            scale32(va);
+            tc::tmem_st32(orow_t + (uint32_t)c0, va);
+            tc::tmem_wait_ld_for(vb);
+            if (c0 + 64 < D) tc::tmem_ld32(orow_t + (uint32_t)(c0 + 64), va);
+            scale32(vb);
+            tc::tmem_st32(orow_t + (uint32_t)(c0 + 32), vb);
+            if (c0 + 64 < D) tc::tmem_wait_ld_for(va);
           }
         }
         tc::tmem_wait_st();
@@ -1253,11 +1265,10 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
       // (the previous tile's bulk copy of this row has read its staging row)
       asm volatile("cp.async.bulk.wait_group.read 0;" ::: "memory");
       const uint32_t orow = base + Geo::kOffOut + (uint32_t)(m * Geo::kOutPitch);
-#pragma unroll 1
-      for (int c0 = 0; c0 < D; c0 += 32) {
-        uint32_t v[32];
-        tc::tmem_ld32(tmem + Geo::kColO + lane_base + c0, v);
-        tc::tmem_wait_ld();
+      // 32 columns per round, the next round's load in flight while this one
+      // is packed and staged
+      const uint32_t orow_t = tmem + Geo::kColO + lane_base;
+      auto stage32 = [&](const uint32_t (&v)[32], int c0) {
 #pragma unroll
         for (int e = 0; e < 32; e += 8) {
           uint4 o;
@@ -1266,6 +1277,20 @@ __global__ void __launch_bounds__(prefill_threads(D), 1)
           o.z = dev::pack_bf16x2(__uint_as_float(v[e + 4]) * sc, __uint_as_float(v[e + 5]) * sc);
           o.w = dev::pack_bf16x2(__uint_as_float(v[e + 6]) * sc, __uint_as_float(v[e + 7]) * sc);
           sts128(orow + (uint32_t)((c0 + e) * 2), o);
+        }
+      };
+      {
+        uint32_t va[32], vb[32];
+        tc::tmem_ld32(orow_t, va);
+        tc::tmem_wait_ld_for(va);
+#pragma unroll 1
+        for (int c0 = 0; c0 < D; c0 += 64) {
+          tc::tmem_ld32(orow_t + (uint32_t)(c0 + 32), vb);
+          stage32(va, c0);
+          tc::tmem_wait_ld_for(vb);
+          if (c0 + 64 < D) tc::tmem_ld32(orow_t + (uint32_t)(c0 + 64), va);
+          stage32(vb, c0 + 32);
+          if (c0 + 64 < D) tc::tmem_wait_ld_for(va);
         }
       }
       tc::fence_before_sync();
