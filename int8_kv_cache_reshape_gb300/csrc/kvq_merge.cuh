@@ -13,9 +13,11 @@
 // end of the decode kernel; merged there by the last piece's warp, a tile's
 // partial rows were read by one warp with a few loads in flight, while the
 // other warps' streaming still loaded the memory system (up to 10-17 us of
-// tail).  Here a CTA of 128 threads merges a tile: the rows' maxima and
-// normalisers first (8 threads per row), then (row, 4-dim) items, consecutive
-// threads on consecutive dims of a partial row.
+// tail).  Here a CTA of 256 threads merges a tile: 16 threads per row find
+// its largest lse and the splits' weights 2^(lse_s - M) (kept in shared
+// memory for up to kMergeWSplits splits) and normaliser; then each thread
+// takes (row, 4-dim) items, consecutive threads on consecutive dims of a
+// partial row, with eight splits' loads in flight.
 #pragma once
 
 #include <cuda_runtime.h>
@@ -25,7 +27,8 @@
 
 namespace kvq {
 
-constexpr int kMergeThreads = 128;
+constexpr int kMergeThreads = 256;
+constexpr int kMergeWSplits = 64;  // splits whose weights stay in shared memory
 
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
@@ -38,27 +41,31 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   const int nr = m.nrows, ns = m.nsplits;
   const int tid = threadIdx.x;
   const float log2e = 1.4426950408889634f;
+  const bool w_smem = ns <= kMergeWSplits;
   __shared__ float row_max[kTileMaxRows], row_inv[kTileMaxRows];
+  __shared__ float wts[kTileMaxRows * kMergeWSplits];
   // (row n of split s is partial row m.part + s * nr + n)
   {
-    const int n = tid >> 3, sub = tid & 7;
+    const int n = tid >> 4, sub = tid & 15;
     const bool live = n < nr;
     float M = -INFINITY;
     if (live)
-      for (int s = sub; s < ns; s += 8) M = fmaxf(M, __ldcg(p.part_lse + m.part + s * nr + n));
+      for (int s = sub; s < ns; s += 16) M = fmaxf(M, __ldcg(p.part_lse + m.part + s * nr + n));
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
+    for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float sink = p.sinks && live ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], log2e, 6.0f)
                                        : -INFINITY;
     M = fmaxf(M, sink);
     float sum = 0.0f;
     if (live && M != -INFINITY)
-      for (int s = sub; s < ns; s += 8) {
+      for (int s = sub; s < ns; s += 16) {
         const float l = __ldcg(p.part_lse + m.part + s * nr + n);
-        if (l != -INFINITY) sum += exp2f(l - M);
+        const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
+        if (w_smem) wts[n * kMergeWSplits + s] = w;
+        sum += w;
       }
 #pragma unroll
-    for (int off = 4; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
+    for (int off = 8; off > 0; off >>= 1) sum += __shfl_xor_sync(0xffffffffu, sum, off);
     if (live && sub == 0) {
       if (sink != -INFINITY) sum += exp2f(sink - M);
       row_max[n] = M;
@@ -80,12 +87,17 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     const float M = row_max[n], inv = row_inv[n];
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
     if (M != -INFINITY) {
-#pragma unroll 4
+#pragma unroll 8
       for (int s = 0; s < ns; ++s) {
         const int64_t r = (int64_t)m.part + (int64_t)s * nr + n;
-        const float l = __ldcg(p.part_lse + r);
+        float w;
+        if (w_smem) {
+          w = wts[n * kMergeWSplits + s];
+        } else {
+          const float l = __ldcg(p.part_lse + r);
+          w = l == -INFINITY ? 0.0f : exp2f(l - M);
+        }
         const float4 v = __ldcg(reinterpret_cast<const float4*>(p.part_o + r * D + d));
-        const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
         a0 += w * v.x;
         a1 += w * v.y;
         a2 += w * v.z;
