@@ -318,6 +318,33 @@ KVQ_API int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim
                             const float* sinks, float k_scale, float v_scale, void* out,
                             void* workspace, size_t workspace_bytes, void* stream);
 
+/* No counterpart on the pages (their steps start from device tensors).  One
+ * decode step from host memory to host memory, for a serving loop whose
+ * step inputs and result live on the host: copies in_bytes from host_in to
+ * dev_in (one cudaMemcpyAsync on `stream`), runs kvq_decode_step with the
+ * arguments after out_bytes -- its device pointers (key, value,
+ * slot_mapping, q, query_start_loc, seq_lens, block_table, ...) may point
+ * into dev_in --, copies the first out_bytes of `out` to host_out, and
+ * waits for the stream.  host_in and host_out should be pinned (page-locked)
+ * for the copies to be asynchronous; out_bytes must not exceed the output's
+ * size.  in_bytes / out_bytes may be 0 (no copy).  Errors: those of
+ * kvq_decode_step (nothing is copied back then), KVQ_E_INVALID_ARG for a
+ * NULL buffer with a nonzero size, KVQ_E_CUDA for a failed copy or wait.
+ * Allocates nothing. */
+KVQ_API int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes,
+                                    void* host_out, size_t out_bytes, int num_req, int heads_q,
+                                    int heads_kv, int head_dim, kvq_dtype_t dtype, const void* key,
+                                    const void* value, int64_t num_new_tokens,
+                                    int64_t key_stride_tok, int64_t value_stride_tok,
+                                    const int64_t* slot_mapping, void* key_cache,
+                                    void* value_cache, int64_t num_blocks, int block_size,
+                                    const void* q, const int32_t* query_start_loc,
+                                    const int32_t* seq_lens, const int32_t* block_table,
+                                    int block_table_stride, int max_query_len, float sm_scale,
+                                    int window, float soft_cap, const float* alibi_slopes,
+                                    const float* sinks, float k_scale, float v_scale, void* out,
+                                    void* workspace, size_t workspace_bytes, void* stream);
+
 /* Workspace bytes of kvq_decode_step for these arguments on the current
  * device ([P2] Breakdown item 1: scratch sized from the KV element size and
  * the tile geometry).  use_alibi: whether alibi_slopes will be non-NULL.

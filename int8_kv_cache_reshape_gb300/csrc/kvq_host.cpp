@@ -978,6 +978,44 @@ int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dt
   return kvq::launch_decode_step(p, sp, dtype, head_dim, warps, stream);
 }
 
+int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, void* host_out,
+                            size_t out_bytes, int num_req, int heads_q, int heads_kv, int head_dim,
+                            kvq_dtype_t dtype, const void* key, const void* value,
+                            int64_t num_new_tokens, int64_t key_stride_tok, int64_t value_stride_tok,
+                            const int64_t* slot_mapping, void* key_cache, void* value_cache,
+                            int64_t num_blocks, int block_size, const void* q,
+                            const int32_t* query_start_loc, const int32_t* seq_lens,
+                            const int32_t* block_table, int block_table_stride, int max_query_len,
+                            float sm_scale, int window, float soft_cap, const float* alibi_slopes,
+                            const float* sinks, float k_scale, float v_scale, void* out,
+                            void* workspace, size_t workspace_bytes, void* stream) {
+  if ((in_bytes > 0 && (!host_in || !dev_in)) || (out_bytes > 0 && (!host_out || !out)))
+    return KVQ_E_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (in_bytes > 0 &&
+      cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  const int rc = kvq_decode_step(num_req, heads_q, heads_kv, head_dim, dtype, key, value,
+                                 num_new_tokens, key_stride_tok, value_stride_tok, slot_mapping,
+                                 key_cache, value_cache, num_blocks, block_size, q, query_start_loc,
+                                 seq_lens, block_table, block_table_stride, max_query_len, sm_scale,
+                                 window, soft_cap, alibi_slopes, sinks, k_scale, v_scale, out,
+                                 workspace, workspace_bytes, stream);
+  if (rc != KVQ_OK) return rc;
+  if (out_bytes > 0 &&
+      cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  if (cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return KVQ_OK;
+}
+
 int kvq_decode_step_check(const void* workspace) {
   if (!workspace) return KVQ_E_INVALID_ARG;
   int32_t flag = 0;

@@ -98,6 +98,8 @@ lib.kvq_decode_step.argtypes = [
     _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _p, _p, _c.c_int64, _c.c_int64,
     _c.c_int64, _p, _p, _p, _c.c_int64, _c.c_int, _p, _p, _p, _p, _c.c_int, _c.c_int,
     _c.c_float, _c.c_int, _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
+lib.kvq_decode_step_host_io.restype = _c.c_int
+lib.kvq_decode_step_host_io.argtypes = [_p, _p, _c.c_size_t, _p, _c.c_size_t] + lib.kvq_decode_step.argtypes
 lib.kvq_decode_step_workspace_size.restype = _c.c_int
 lib.kvq_decode_step_workspace_size.argtypes = [
     _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(_c.c_size_t)]
@@ -357,6 +359,34 @@ def prepare_decode_step(key, value, slot_mapping, key_cache, value_cache, q, que
         key, value, slot_mapping, key_cache, value_cache, q, query_start_loc, seq_lens,
         block_table, max_query_len, sm_scale, window, soft_cap, k_scale, v_scale, out, workspace,
         kv_cache_dtype, heads_kv, alibi_slopes, sinks, stream, num_blocks), "kvq_decode_step")
+
+
+def _host_io_args(host_in, dev_in, host_out, out_bytes):
+    in_bytes = host_in.numel() * host_in.element_size()
+    if dev_in.numel() * dev_in.element_size() < in_bytes:
+        raise ValueError("dev_in is smaller than host_in")
+    if out_bytes > host_out.numel() * host_out.element_size():
+        raise ValueError("out_bytes exceeds host_out")
+    return (_ptr(host_in), _ptr(dev_in), _c.c_size_t(in_bytes), _ptr(host_out),
+            _c.c_size_t(int(out_bytes)))
+
+
+def prepare_decode_step_host_io(host_in, dev_in, host_out, out_bytes: int, key, value,
+                                slot_mapping, key_cache, value_cache, q, query_start_loc,
+                                seq_lens, block_table, max_query_len: int, sm_scale: float,
+                                window: int, soft_cap: float, k_scale: float, v_scale: float,
+                                out, workspace, kv_cache_dtype, heads_kv: int, alibi_slopes=None,
+                                sinks=None, stream=None, num_blocks=None) -> Prepared:
+    """kvq_decode_step_host_io, marshalled once (see Prepared): each call
+    copies host_in (a pinned uint8 tensor) to dev_in, runs the decode step
+    (whose device tensors may be views of dev_in), copies out_bytes of out
+    to host_out (pinned) and waits for the stream."""
+    return Prepared(lib.kvq_decode_step_host_io, _host_io_args(host_in, dev_in, host_out, out_bytes)
+                    + _decode_step_args(key, value, slot_mapping, key_cache, value_cache, q,
+                                        query_start_loc, seq_lens, block_table, max_query_len,
+                                        sm_scale, window, soft_cap, k_scale, v_scale, out,
+                                        workspace, kv_cache_dtype, heads_kv, alibi_slopes, sinks,
+                                        stream, num_blocks), "kvq_decode_step_host_io")
 
 
 def decode_step_check(workspace) -> None:

@@ -179,3 +179,47 @@ def test_fused_step_flags_device_lengths_beyond_the_bound(cuda_device):
     toks = [0, 4]                                      # requests 0 and 2
     ref, bnd = oracle_reference(wl, kc, vc, tokens=toks)
     assert_attention_close(st.g.out_f32(toks), ref, "step: good requests", bnd)
+
+
+def test_fused_step_from_host_buffers(cuda_device):
+    """kvq_decode_step_host_io: the step's inputs packed in one pinned host
+    buffer, copied to the device, the fused step run on views of the device
+    copy, the output copied back to pinned host memory -- one C-ABI call.
+    The caches and the host output equal the device-input step's, bit for
+    bit, and match the oracle."""
+    wl = W.custom("step-host-io", [1, 2, 1, 4, 1], [700, 333, 1, 2048, 96], 32, 8, 128, 16,
+                  "fp8_e4m3", 907)
+    ref_step = Step(wl).run()
+    ref_step.check("device inputs")
+    want_out = ref_step.g.out.view(torch.int16).cpu()
+    want_kc, want_vc = ref_step.g.kc.cpu(), ref_step.g.vc.cpu()
+
+    st = Step(wl)
+    g = st.g
+    parts = [g.q, st.nkey, st.nval, st.nslot, g.qsl, g.sl, g.bt]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    h_in = torch.zeros(o, dtype=torch.uint8).pin_memory()
+    for t, off, n in zip(parts, offs, sizes):
+        h_in[off:off + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+    d_in = torch.full((o,), 0xA5, dtype=torch.uint8, device=g.dev)   # garbage until the copy
+    views = [d_in[off:off + n].view(t.dtype).view(t.shape) for t, off, n in zip(parts, offs, sizes)]
+    q, nkey, nval, nslot, qsl, sl, bt = views
+    h_out = torch.zeros(g.out.shape, dtype=torch.bfloat16).pin_memory()
+    out_bytes = g.out.numel() * g.out.element_size()
+    call = kvq().prepare_decode_step_host_io(
+        h_in, d_in, h_out, out_bytes, nkey, nval, nslot, g.kc, g.vc, q, qsl, sl, bt, st.mql,
+        wl.sm_scale, wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, g.out, st.ws.t,
+        wl.kv_cache_dtype, wl.heads_kv)
+    call()                                     # returns with the output on the host
+    assert torch.equal(h_out.view(torch.int16), want_out)
+    assert torch.equal(g.kc.cpu(), want_kc) and torch.equal(g.vc.cpu(), want_vc)
+    st.check("host inputs")
+    # a second call from the same buffers gives the same output (the
+    # workspace is left ready; the cache rows are rewritten with equal bytes)
+    h_out.zero_()
+    call()
+    assert torch.equal(h_out.view(torch.int16), want_out)
