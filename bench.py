@@ -422,7 +422,7 @@ def run_workload(args, index, dtype, world, local, with_e2e=True):
             s2.close()
         res["parts"] = parts
 
-    # ---- the fused decode step (decode batches): one launch, plan on device --
+    # ---- the fused decode step (decode batches): plan on the device --------
     fused_ok = all(Q * wl.heads_q // wl.heads_kv <= 16 for Q in wl.query_lens) and wl.causal
     mql = max(wl.query_lens) if wl.query_lens else 1
     if fused_ok:
@@ -450,11 +450,12 @@ def run_workload(args, index, dtype, world, local, with_e2e=True):
         kvq.decode_step_check(step_ws)
         fms = _max_over_ranks(sum(a.elapsed_time(b) for a, b in evs), world) / args.steps
         res["fused_step"] = {
-            "call": "kvq_decode_step (cache write + device-built plan + attention, one launch)",
+            "call": "kvq_decode_step (cache write + device-built plan + attention in one "
+                    "launch, then the merge of its cut tiles)",
             "ms_per_step": fms, "value": world * kvb / (fms * 1e-3) / 1e9, "unit": "GB/s",
             "roofline": _roofline(True, kvb, flops, fms, peaks, peaks_src,
                                   "fused decode step (cache write + split-KV decode)"),
-            "gpu_launches_per_step": 1}
+            "gpu_launches_per_step": 2}
         res["gpu_launches"] += args.steps
 
     # ---- end to end: host buffers through the public API -------------------
@@ -529,8 +530,9 @@ def run_workload(args, index, dtype, world, local, with_e2e=True):
         if fused_ok:
             res["e2e"] = e2e_obj(time_e2e(e2e_fused),
                                  "one C-ABI call, kvq_decode_step_host_io: one H2D of the packed "
-                                 "step inputs, the fused step (one launch: cache write, plan on "
-                                 "the device, attention), D2H of out, stream synchronize")
+                                 "step inputs, the fused step (cache write, plan on the device, "
+                                 "attention; merge of the cut tiles), D2H of out, stream "
+                                 "synchronize")
             res["e2e_two_calls"] = two
         else:
             res["e2e"] = two

@@ -303,7 +303,9 @@ KVQ_API int kvq_attention_with_kv_cache_static_scratch(
  *                           every call leaves it ready for the next.  Calls
  *                           sharing a workspace must be ordered on one stream.
  * The kernel is a cooperative launch (all its CTAs resident at once, one
- * grid-wide barrier between the cache write and the attention); the barrier
+ * grid-wide barrier between the cache write and the attention), followed
+ * on the stream by the merge of the tiles it cut among warps (a kernel of
+ * its own, launched as a programmatic dependent); the barrier
  * wait is bounded (about a second) and a timeout flags the error word
  * (kvq_decode_step_check: KVQ_E_TIMEOUT).  Allocates nothing. */
 KVQ_API int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim,

@@ -81,121 +81,11 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
   }
 }
 
-// Merge of a tile's pieces in the fused decode step (vllm PR 50194 page, Key
-// source snippet: enable_kv_split), by one warp.  Piece s left o_s = (sum_j
-// p_j v_j) / l_s and lse_s = m_s + log2(l_s) (log2 units); the merged row is
-//   o = sum_s 2^(lse_s - M) o_s / sum_s 2^(lse_s - M),  M = max_s lse_s.
-// Partials are read through L2 (other warps wrote them).  Merges run at the
-// end of the kernel (a cut tile's last piece to finish is the one at the end
-// of a warp's segment), so their latency is the kernel's tail: with at most
-// 16 splits the rows are merged side by side -- lpr lanes per row, each with
-// a run of D / lpr dims -- and every split's partial of a 4-dim step is
-// loaded at once.
-// `base(s)` is the partial row of split s's row 0 (its row n at base(s) + n).
-template <int D, class Base>
-__device__ __forceinline__ void merge_pieces(const AttnParams& p, const MergeItem& m, int lane,
-                                             Base base) {
-  constexpr int kMaxSplits = 16;
-  const int G = p.group;
-  const int q0 = p.query_start_loc[m.req];
-  const int ns = m.nsplits, nr = m.nrows;
-  const float* lse = p.part_lse;
-  auto out_row = [&](int n) {
-    const int R = m.row0 + n;
-    return p.out + ((int64_t)(q0 + R / G) * p.heads_q + m.kv_head * G + R % G) * D;
-  };
-  if (ns <= kMaxSplits) {
-    const int np2 = nr <= 1 ? 1 : nr <= 2 ? 2 : nr <= 4 ? 4 : nr <= 8 ? 8 : 16;
-    const int lpr = min(32 / np2, D / 4);  // lanes per row
-    const int n = lane / lpr, sub = lane % lpr;
-    const bool active = n < nr;
-    const int per = D / lpr;               // dims per lane, a multiple of 4
-    float w[kMaxSplits];
-    float M = -INFINITY;
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      w[s] = active && s < ns ? __ldcg(lse + base(s) + n) : -INFINITY;
-      M = fmaxf(M, w[s]);
-    }
-    // An attention sink is one more term of the normaliser (no value).  The
-    // pieces' log-sum-exps carry the weights' 2^6 lift, so the sink's logit
-    // (log2 units) does too.
-    const float sink = p.sinks && active
-                           ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], 1.4426950408889634f, 6.0f)
-                           : -INFINITY;
-    M = fmaxf(M, sink);
-    float wsum = sink == -INFINITY ? 0.0f : exp2f(sink - M);
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s) {
-      w[s] = (w[s] == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(w[s] - M);
-      wsum += w[s];
-    }
-    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-    if (!active) return;
-    int64_t row_off[kMaxSplits];  // split s's partial row n, in floats
-#pragma unroll
-    for (int s = 0; s < kMaxSplits; ++s)
-      row_off[s] = s < ns ? (int64_t)(base(s) + n) * D + sub * per : 0;
-    uint16_t* dst = out_row(n) + sub * per;
-    for (int d0 = 0; d0 < per; d0 += 4) {
-      float4 v[kMaxSplits];
-#pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s)
-        v[s] = s < ns ? __ldcg(reinterpret_cast<const float4*>(p.part_o + row_off[s] + d0))
-                      : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
-      float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
-#pragma unroll
-      for (int s = 0; s < kMaxSplits; ++s) {
-        a0 += w[s] * v[s].x;
-        a1 += w[s] * v[s].y;
-        a2 += w[s] * v[s].z;
-        a3 += w[s] * v[s].w;
-      }
-      *reinterpret_cast<uint2*>(dst + d0) =
-          make_uint2(dev::pack_bf16x2(a0 * inv, a1 * inv), dev::pack_bf16x2(a2 * inv, a3 * inv));
-    }
-    return;
-  }
-  // More splits: one row at a time, each lane D/32 consecutive dims.
-  constexpr int kPer = D / 32;
-  for (int n = 0; n < nr; ++n) {
-    float M = -INFINITY;
-    for (int s = lane; s < ns; s += 32) M = fmaxf(M, __ldcg(lse + base(s) + n));
-#pragma unroll
-    for (int off = 16; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
-    const float sink =  // (log2 units, with the pieces' 2^6 lift)
-        p.sinks ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], 1.4426950408889634f, 6.0f)
-                : -INFINITY;
-    M = fmaxf(M, sink);
-    float acc[kPer];
-#pragma unroll
-    for (int e = 0; e < kPer; ++e) acc[e] = 0.0f;
-    float wsum = sink == -INFINITY ? 0.0f : exp2f(sink - M);
-    for (int s = 0; s < ns; ++s) {
-      const float l = __ldcg(lse + base(s) + n);
-      const float w = (l == -INFINITY || M == -INFINITY) ? 0.0f : exp2f(l - M);
-      wsum += w;
-      const float* src = p.part_o + (int64_t)(base(s) + n) * D + lane * kPer;
-#pragma unroll
-      for (int e = 0; e < kPer; e += 2) {
-        const float2 v = __ldcg(reinterpret_cast<const float2*>(src + e));
-        acc[e] += w * v.x;
-        acc[e + 1] += w * v.y;
-      }
-    }
-    const float inv = wsum > 0.0f ? 1.0f / wsum : 0.0f;
-    uint16_t* dst = out_row(n) + lane * kPer;
-#pragma unroll
-    for (int e = 0; e < kPer; e += 2)
-      *reinterpret_cast<uint32_t*>(dst + e) = dev::pack_bf16x2(acc[e] * inv, acc[e + 1] * inv);
-  }
-}
-
 // ---- fused decode step: the plan built on the device ----------------------
 // One row tile per (request, kv head): its first 16-token chunk, the keys
 // some of its rows see and its rows; the tiles' chunk counts are
-// prefix-summed by the kernel's first CTA (kDecodeThreads threads), which
-// also zeroes the merge counters.  A request with more rows than the launch
+// prefix-summed by the kernel's first CTA (kDecodeThreads threads).  A
+// request with more rows than the launch
 // was built for (or more queries than keys) is left out and flags the error
 // word.
 __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams& sp) {
@@ -242,7 +132,6 @@ __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams&
     sp.prefix[nt] = run;
     total = run;
   }
-  for (int t = tid; t < nt; t += kDecodeThreads) p.merge_counters[t] = 0;
   __syncthreads();
   // Each warp's first tile: warp w's segment starts at floor(w T / W), which
   // lies in tile t for w in [ceil(f0 W / T), ceil(f1 W / T)).
@@ -305,7 +194,7 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   // The merge of the cut tiles (its own kernel, after this one) may be
   // scheduled now: it waits for this grid to complete before it reads a
   // partial row.
-  if constexpr (!DEV) asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
+  asm volatile("griddepcontrol.launch_dependents;" ::: "memory");
   // ---- the fused step's prologue -------------------------------------------
   int64_t total_chunks = p.num_chunks;
   int64_t total_warps = p.num_warps;
@@ -715,44 +604,6 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
           if (g == 0) p.part_lse[pc.part + nr] = l > 0.0f ? m_run[t][k] + log2f(l) : -INFINITY;
         }
       }
-    if constexpr (DEV) {
-      if (pc.part >= 0) {
-        // Fused step: publish the partials, count arrivals; the last piece
-        // merges.  No piece waits for another.  (Host-planned calls merge in
-        // a kernel of their own after the decode kernels: kvq_merge.cuh.)
-        __threadfence();
-        __syncwarp();
-        // warp whose segment holds flat chunk f: floor(((f + 1) W - 1) / T)
-        auto warp_of = [&](int64_t f) { return ((f + 1) * total_warps - 1) / total_chunks; };
-        // The tile's splits are the warps whose segments hold its chunks:
-        // w0 .. w1 when every segment has chunks (T >= W), else one warp per
-        // chunk (every non-empty segment is a single chunk).
-        const int64_t f0 = __ldcg(sp.prefix + pc.merge);
-        const int64_t f1 = __ldcg(sp.prefix + pc.merge + 1);
-        const int64_t w0 = warp_of(f0);
-        const int64_t ns = total_chunks >= total_warps ? warp_of(f1 - 1) - w0 + 1 : f1 - f0;
-        const MergeItem m{pc.req, pc.kv_head, 0, pc.nrows, 0, (int32_t)ns, 0, 0};
-        int last = 0;
-        if (lane == 0) {
-          const int prev = atomicAdd(p.merge_counters + pc.merge, 1);
-          last = prev == m.nsplits - 1;
-        }
-        last = __shfl_sync(0xffffffffu, last, 0);
-        if (last) {
-          __threadfence();
-          // split s is warp w0 + s: its slot 2 (w0 + s), except that the
-          // first split's tile is warp w0's last one unless w0's segment
-          // starts exactly at the tile
-          const bool first_is_last = (w0 * total_chunks) / total_warps < f0;
-          const bool dense = total_chunks >= total_warps;
-          merge_pieces<D>(p, m, lane, [&](int s) {
-            const int64_t w = dense ? w0 + s : warp_of(f0 + s);
-            return (int)((2 * w + (s == 0 && first_is_last ? 1 : 0)) * kTileMaxRows);
-          });
-          if (lane == 0) atomicExch(p.merge_counters + pc.merge, 0);  // ready for the next call
-        }
-      }
-    }
   };
 
   // ---- stream the segment -------------------------------------------------

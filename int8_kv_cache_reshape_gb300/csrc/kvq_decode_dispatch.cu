@@ -35,6 +35,33 @@ int launch_merge(const AttnParams& p, int head_dim, int64_t num_merges, void* st
   return KVQ_OK;
 }
 
+int launch_merge_step(const AttnParams& p, const StepParams& sp, int head_dim, int64_t warps,
+                      void* stream) {
+  if (sp.num_tiles <= 0) return KVQ_OK;
+  void (*kern)(AttnParams, StepParams, int64_t);
+  switch (head_dim) {
+    case 64: kern = merge_step_kernel<64>; break;
+    case 128: kern = merge_step_kernel<128>; break;
+    case 256: kern = merge_step_kernel<256>; break;
+    default: return KVQ_E_UNSUPPORTED;
+  }
+  cudaLaunchConfig_t cfg = {};
+  cfg.gridDim = dim3((unsigned)sp.num_tiles);
+  cfg.blockDim = dim3(kMergeThreads);
+  cfg.dynamicSmemBytes = 0;
+  cfg.stream = static_cast<cudaStream_t>(stream);
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeProgrammaticStreamSerialization;
+  attr[0].val.programmaticStreamSerializationAllowed = 1;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  if (cudaLaunchKernelEx(&cfg, kern, p, sp, warps) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return KVQ_OK;
+}
+
 #define KVQ_DECLARE(D)                                                                       \
   int launch_decode_d##D(const AttnParams&, int, int, void*);                               \
   int launch_decode_d##D##_alibi(const AttnParams&, int, int, void*);                       \

@@ -795,7 +795,6 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
   char* b = static_cast<char*>(s->d_buf);
   p.pieces = reinterpret_cast<const DecodePiece*>(b + s->d_pieces_off);
   p.merges = reinterpret_cast<const MergeItem*>(b + s->d_merges_off);
-  p.merge_counters = nullptr;  // (the fused step's in-kernel merges only)
   p.prefill_tiles = reinterpret_cast<const PrefillTile*>(b + s->d_prefill_off);
   p.num_prefill_tiles = (int32_t)s->prefill.size();
   p.total_q_tokens = (int32_t)s->total_q;
@@ -940,7 +939,6 @@ int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dt
   p.out = static_cast<uint16_t*>(out);
   p.part_o = reinterpret_cast<float*>(ws + lay.o);
   p.part_lse = reinterpret_cast<float*>(ws + lay.lse);
-  p.merge_counters = reinterpret_cast<int32_t*>(ws + lay.counters);
   p.error_flag = reinterpret_cast<int32_t*>(ws);
   p.num_blocks = num_blocks;
   p.block_table_stride = block_table_stride;
@@ -975,7 +973,11 @@ int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dt
   sp.num_req = num_req;
   sp.num_tiles = num_tiles;
   sp.max_rows = max_rows;
-  return kvq::launch_decode_step(p, sp, dtype, head_dim, warps, stream);
+  // the fused kernel, then the merge of its cut tiles as a programmatic
+  // dependent launch
+  rc = kvq::launch_decode_step(p, sp, dtype, head_dim, warps, stream);
+  if (rc != KVQ_OK) return rc;
+  return kvq::launch_merge_step(p, sp, head_dim, warps, stream);
 }
 
 int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, void* host_out,

@@ -223,7 +223,6 @@ struct AttnParams {
   int64_t num_chunks;          // length of the launch's flat chunk sequence
   int num_warps;               // warps it is cut among (grid * kDecodeWarps)
   const MergeItem* merges;
-  int32_t* merge_counters;     // one per merge item, zero between calls
   const PrefillTile* prefill_tiles;
   int32_t num_prefill_tiles;
   int32_t total_q_tokens;      // rows of q and out (the host plan's sum Q)
@@ -260,19 +259,17 @@ struct StepParams {
 
 // Workspace of the fused step for `warps` decode warps: an error word and
 // the grid barrier's two words (256 bytes), the prefix, the tile table, each
-// warp's first tile, the merge counters, then partial log-sum-exps and
-// outputs: each warp owns two 16-row slots (the tile its segment starts in
-// and the one it ends in).
+// warp's first tile, then partial log-sum-exps and outputs: each warp owns
+// two 16-row slots (the tile its segment starts in and the one it ends in).
 struct StepWorkspace {
-  size_t prefix, tiles, warp_tile, counters, lse, o, total;
+  size_t prefix, tiles, warp_tile, lse, o, total;
 };
 KVQ_HD constexpr StepWorkspace step_workspace(int num_tiles, int head_dim, int64_t warps) {
   StepWorkspace w{};
   w.prefix = 256;
   w.tiles = w.prefix + align256((size_t)(num_tiles + 1) * 4);
   w.warp_tile = w.tiles + align256((size_t)num_tiles * 16);
-  w.counters = w.warp_tile + align256((size_t)warps * 4);
-  w.lse = w.counters + align256((size_t)num_tiles * 4);
+  w.lse = w.warp_tile + align256((size_t)warps * 4);
   w.o = w.lse + align256((size_t)warps * 2 * kTileMaxRows * 4);
   w.total = w.o + (size_t)warps * 2 * kTileMaxRows * head_dim * 4;
   return w;
@@ -302,6 +299,11 @@ int step_warps(int dtype, int head_dim, bool alibi, int max_rows, int64_t* warps
 // The merge of the decode's cut tiles (p.merges, one CTA each), after the
 // decode kernels of a host-planned call.
 int launch_merge(const AttnParams& p, int head_dim, int64_t num_merges, void* stream);
+// The fused step's merge of its cut tiles: one CTA per tile of the device
+// plan (tiles left whole return at once), a programmatic dependent of the
+// fused kernel, whose `warps` warps cut the chunk sequence.
+int launch_merge_step(const AttnParams& p, const StepParams& sp, int head_dim, int64_t warps,
+                      void* stream);
 // The persistent prefill over p.num_prefill_tiles tiles on `ctas` CTAs
 // (at most one per SM is resident).
 int launch_prefill(const AttnParams& p, const PrefillMaps& maps, int dtype, int head_dim,

@@ -30,27 +30,24 @@ namespace kvq {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWSplits = 64;  // splits whose weights stay in shared memory
 
-template <int D>
-__global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
-  // Launched as a programmatic dependent of the decode kernel: this CTA may
-  // be resident before the decode grid ends; the partials are read only once
-  // that grid has completed and its writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
-  const MergeItem m = p.merges[blockIdx.x];
+// Merge of one cut tile m (nr = m.nrows rows, ns splits) by a CTA of
+// kMergeThreads threads; base(s): the partial row of split s's row 0 (its
+// row n at base(s) + n).
+template <int D, class Base>
+__device__ __forceinline__ void merge_tile(const AttnParams& p, const MergeItem& m, int ns, Base base) {
   const int G = p.group;
-  const int nr = m.nrows, ns = m.nsplits;
+  const int nr = m.nrows;
   const int tid = threadIdx.x;
   const float log2e = 1.4426950408889634f;
   const bool w_smem = ns <= kMergeWSplits;
   __shared__ float row_max[kTileMaxRows], row_inv[kTileMaxRows];
   __shared__ float wts[kTileMaxRows * kMergeWSplits];
-  // (row n of split s is partial row m.part + s * nr + n)
   {
     const int n = tid >> 4, sub = tid & 15;
     const bool live = n < nr;
     float M = -INFINITY;
     if (live)
-      for (int s = sub; s < ns; s += 16) M = fmaxf(M, __ldcg(p.part_lse + m.part + s * nr + n));
+      for (int s = sub; s < ns; s += 16) M = fmaxf(M, __ldcg(p.part_lse + base(s) + n));
 #pragma unroll
     for (int off = 8; off > 0; off >>= 1) M = fmaxf(M, __shfl_xor_sync(0xffffffffu, M, off));
     const float sink = p.sinks && live ? fmaf(p.sinks[m.kv_head * G + (m.row0 + n) % G], log2e, 6.0f)
@@ -59,7 +56,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     float sum = 0.0f;
     if (live && M != -INFINITY)
       for (int s = sub; s < ns; s += 16) {
-        const float l = __ldcg(p.part_lse + m.part + s * nr + n);
+        const float l = __ldcg(p.part_lse + base(s) + n);
         const float w = l == -INFINITY ? 0.0f : exp2f(l - M);
         if (w_smem) wts[n * kMergeWSplits + s] = w;
         sum += w;
@@ -75,8 +72,8 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
   __syncthreads();
   const int q0 = p.query_start_loc[m.req];
   if constexpr (KVQ_CHECKED) {
-    // the tile's rows must lie in out
-    if (q0 < 0 || q0 + (m.row0 + nr - 1) / G >= p.total_q_tokens) {
+    // the tile's rows must lie in out (host plans: total_q_tokens is set)
+    if (p.total_q_tokens > 0 && (q0 < 0 || q0 + (m.row0 + nr - 1) / G >= p.total_q_tokens)) {
       if (tid == 0) atomicExch(p.error_flag, 2);
       return;
     }
@@ -89,7 +86,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     if (M != -INFINITY) {
 #pragma unroll 8
       for (int s = 0; s < ns; ++s) {
-        const int64_t r = (int64_t)m.part + (int64_t)s * nr + n;
+        const int64_t r = (int64_t)base(s) + n;
         float w;
         if (w_smem) {
           w = wts[n * kMergeWSplits + s];
@@ -109,6 +106,47 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
     *reinterpret_cast<uint2*>(dst) =
         make_uint2(dev::pack_bf16x2(a0 * inv, a1 * inv), dev::pack_bf16x2(a2 * inv, a3 * inv));
   }
+}
+
+// Host-planned calls: merge item blockIdx.x of the schedule (split s's rows
+// at m.part + s * nrows).
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
+  // Launched as a programmatic dependent of the decode kernel: this CTA may
+  // be resident before the decode grid ends; the partials are read only once
+  // that grid has completed and its writes are visible.
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const MergeItem m = p.merges[blockIdx.x];
+  merge_tile<D>(p, m, m.nsplits, [&](int s) { return m.part + s * m.nrows; });
+}
+
+// The fused decode step: tile blockIdx.x (request t / Hkv, kv head t % Hkv)
+// of the device-built plan, if its chunks span more than one warp segment.
+// The fused kernel cut its flat chunk sequence into `warps` equal segments;
+// split s is warp w0 + s (one warp per chunk when there are fewer chunks
+// than warps), whose partial rows sit in its second 16-row slot for the
+// tile its segment ends in, and in its first for the one it starts in.
+template <int D>
+__global__ void __launch_bounds__(kMergeThreads) merge_step_kernel(const AttnParams p, const StepParams sp,
+                                                                 int64_t warps) {
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  const int t = blockIdx.x;
+  const int64_t T = __ldcg(sp.prefix + sp.num_tiles);
+  const int64_t f0 = __ldcg(sp.prefix + t), f1 = __ldcg(sp.prefix + t + 1);
+  if (T <= 0 || f1 <= f0) return;
+  // warp whose segment holds flat chunk f: floor(((f + 1) W - 1) / T)
+  auto warp_of = [&](int64_t f) { return ((f + 1) * warps - 1) / T; };
+  const bool dense = T >= warps;
+  const int64_t w0 = warp_of(f0);
+  const int64_t ns = dense ? warp_of(f1 - 1) - w0 + 1 : f1 - f0;
+  if (ns <= 1) return;  // one piece: written by its warp
+  const bool first_is_last = (w0 * T) / warps < f0;
+  const int4 ti = __ldcg(sp.tiles + t);
+  const MergeItem m{t / p.heads_kv, t % p.heads_kv, 0, ti.w, 0, (int32_t)ns, 0, 0};
+  merge_tile<D>(p, m, (int)ns, [&](int s) {
+    const int64_t w = dense ? w0 + s : warp_of(f0 + s);
+    return (int)((2 * w + (s == 0 && first_is_last ? 1 : 0)) * kTileMaxRows);
+  });
 }
 
 }  // namespace kvq

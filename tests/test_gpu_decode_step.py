@@ -1,6 +1,7 @@
 """GPU parity of the fused decode step (kvq_decode_step): the step's new K/V
 rows written into the caches, the plan built on the device from the
-device's lengths, and split-KV attention -- one cooperative launch.
+device's lengths, and split-KV attention -- one cooperative launch --, then
+the merge of the cut tiles (a kernel of its own, a programmatic dependent).
 
 vllm PR 50194 page, Key source snippet (get_scheduler_metadata feeding the
 attention) and Breakdown item 1; vllm PR 39445 page, Breakdown items 1-3.

@@ -5,8 +5,8 @@ batch with cut decode tiles and prefill tiles, captured once and replayed:
 the replays give the same bits as the direct calls, and match the oracle
 within the parity tolerance of tests/_harness.py.  Neither call
 synchronises with the host, allocates, or keeps state between calls that a
-replay would repeat wrongly (the split-KV arrival counters are reset by the
-merging warp; the prefill's tensor maps are kernel arguments).
+replay would repeat wrongly (cut decode tiles are merged by a kernel of
+their own; the prefill's tensor maps are kernel arguments).
 """
 import pytest
 import torch
