@@ -30,18 +30,36 @@ namespace kvq {
 constexpr int kMergeThreads = 256;
 constexpr int kMergeWSplits = 64;  // splits whose weights stay in shared memory
 
-// Merge of one cut tile m (nr = m.nrows rows, ns splits) by a CTA of
-// kMergeThreads threads; base(s): the partial row of split s's row 0 (its
-// row n at base(s) + n).
-template <int D, class Base>
-__device__ __forceinline__ void merge_tile(const AttnParams& p, const MergeItem& m, int ns, Base base) {
+// Merge of one cut tile m (nr = m.nrows rows, ns splits; its request's
+// first query token q0) by a CTA of kMergeThreads threads; base(s): the
+// partial row of split s's row 0 (its row n at base(s) + n).  With PRE, a
+// thread's first item's partials of the first kMergePre splits are loaded
+// together with the rows' lse values, so the merge is one round trip to L2
+// after the decode grid completes (host plans, where base(s) is one
+// multiply-add; the fused step's split rows take 64-bit divisions to find,
+// and there the early loads measured slower).
+constexpr int kMergePre = 8;
+template <int D, bool PRE, class Base>
+__device__ __forceinline__ void merge_tile(const AttnParams& p, const MergeItem& m, int q0, int ns,
+                                           Base base) {
   const int G = p.group;
   const int nr = m.nrows;
   const int tid = threadIdx.x;
   const float log2e = 1.4426950408889634f;
   const bool w_smem = ns <= kMergeWSplits;
+  constexpr int kQuads = D / 4;
   __shared__ float row_max[kTileMaxRows], row_inv[kTileMaxRows];
   __shared__ float wts[kTileMaxRows * kMergeWSplits];
+  float4 pre[kMergePre];
+  if constexpr (PRE) {
+    const bool have = tid < nr * kQuads;
+    const int n = tid / kQuads, d = (tid % kQuads) * 4;
+#pragma unroll
+    for (int s = 0; s < kMergePre; ++s)
+      pre[s] = have && s < ns
+                   ? __ldcg(reinterpret_cast<const float4*>(p.part_o + ((int64_t)base(s) + n) * D + d))
+                   : make_float4(0.0f, 0.0f, 0.0f, 0.0f);
+  }
   {
     const int n = tid >> 4, sub = tid & 15;
     const bool live = n < nr;
@@ -70,7 +88,6 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const MergeItem&
     }
   }
   __syncthreads();
-  const int q0 = p.query_start_loc[m.req];
   if constexpr (KVQ_CHECKED) {
     // the tile's rows must lie in out (host plans: total_q_tokens is set)
     if (p.total_q_tokens > 0 && (q0 < 0 || q0 + (m.row0 + nr - 1) / G >= p.total_q_tokens)) {
@@ -78,14 +95,34 @@ __device__ __forceinline__ void merge_tile(const AttnParams& p, const MergeItem&
       return;
     }
   }
-  constexpr int kQuads = D / 4;
   for (int it = tid; it < nr * kQuads; it += kMergeThreads) {
     const int n = it / kQuads, d = (it % kQuads) * 4;
     const float M = row_max[n], inv = row_inv[n];
     float a0 = 0.0f, a1 = 0.0f, a2 = 0.0f, a3 = 0.0f;
+    int s0 = 0;
+    if (PRE && it == tid && M != -INFINITY) {
+      // the first item: its first splits' partials are in registers
+#pragma unroll
+      for (int s = 0; s < kMergePre; ++s) {
+        if (s < ns) {
+          float w;
+          if (w_smem) {
+            w = wts[n * kMergeWSplits + s];
+          } else {
+            const float l = __ldcg(p.part_lse + base(s) + n);
+            w = l == -INFINITY ? 0.0f : exp2f(l - M);
+          }
+          a0 += w * pre[s].x;
+          a1 += w * pre[s].y;
+          a2 += w * pre[s].z;
+          a3 += w * pre[s].w;
+        }
+      }
+      s0 = kMergePre;
+    }
     if (M != -INFINITY) {
 #pragma unroll 8
-      for (int s = 0; s < ns; ++s) {
+      for (int s = s0; s < ns; ++s) {
         const int64_t r = (int64_t)base(s) + n;
         float w;
         if (w_smem) {
@@ -114,10 +151,13 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnParams p) {
   // Launched as a programmatic dependent of the decode kernel: this CTA may
   // be resident before the decode grid ends; the partials are read only once
-  // that grid has completed and its writes are visible.
-  asm volatile("griddepcontrol.wait;" ::: "memory");
+  // that grid has completed and its writes are visible.  (The merge item and
+  // the request's first token come from the host plan and the caller's
+  // inputs, written before the decode kernel started.)
   const MergeItem m = p.merges[blockIdx.x];
-  merge_tile<D>(p, m, m.nsplits, [&](int s) { return m.part + s * m.nrows; });
+  const int q0 = p.query_start_loc[m.req];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
+  merge_tile<D, true>(p, m, q0, m.nsplits, [&](int s) { return m.part + s * m.nrows; });
 }
 
 // The fused decode step: tile blockIdx.x (request t / Hkv, kv head t % Hkv)
@@ -129,8 +169,10 @@ __global__ void __launch_bounds__(kMergeThreads) merge_splits_kernel(const AttnP
 template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_step_kernel(const AttnParams p, const StepParams sp,
                                                                  int64_t warps) {
-  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int t = blockIdx.x;
+  // (the caller's input; the plan is the fused kernel's, read after the wait)
+  const int q0 = p.query_start_loc[t / p.heads_kv];
+  asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t T = __ldcg(sp.prefix + sp.num_tiles);
   const int64_t f0 = __ldcg(sp.prefix + t), f1 = __ldcg(sp.prefix + t + 1);
   if (T <= 0 || f1 <= f0) return;
@@ -143,7 +185,7 @@ __global__ void __launch_bounds__(kMergeThreads) merge_step_kernel(const AttnPar
   const bool first_is_last = (w0 * T) / warps < f0;
   const int4 ti = __ldcg(sp.tiles + t);
   const MergeItem m{t / p.heads_kv, t % p.heads_kv, 0, ti.w, 0, (int32_t)ns, 0, 0};
-  merge_tile<D>(p, m, (int)ns, [&](int s) {
+  merge_tile<D, false>(p, m, q0, (int)ns, [&](int s) {
     const int64_t w = dense ? w0 + s : warp_of(f0 + s);
     return (int)((2 * w + (s == 0 && first_is_last ? 1 : 0)) * kTileMaxRows);
   });
