@@ -329,10 +329,13 @@ KVQ_API int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim
  * into dev_in --, copies the first out_bytes of `out` to host_out, and
  * waits for the stream.  host_in and host_out should be pinned (page-locked)
  * for the copies to be asynchronous; out_bytes must not exceed the output's
- * size.  in_bytes / out_bytes may be 0 (no copy).  Errors: those of
+ * size.  in_bytes / out_bytes may be 0 (no copy).  With out NULL the step
+ * writes its output straight into host_out (pinned host memory the device
+ * addresses; out_bytes is then ignored): the rows cross to the host as the
+ * kernels store them, with no copy after the step.  Errors: those of
  * kvq_decode_step (nothing is copied back then), KVQ_E_INVALID_ARG for a
- * NULL buffer with a nonzero size, KVQ_E_CUDA for a failed copy or wait.
- * Allocates nothing. */
+ * NULL buffer with a nonzero size or an out NULL whose host_out the device
+ * cannot address, KVQ_E_CUDA for a failed copy or wait.  Allocates nothing. */
 KVQ_API int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes,
                                     void* host_out, size_t out_bytes, int num_req, int heads_q,
                                     int heads_kv, int head_dim, kvq_dtype_t dtype, const void* key,

@@ -991,8 +991,18 @@ int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, 
                             float sm_scale, int window, float soft_cap, const float* alibi_slopes,
                             const float* sinks, float k_scale, float v_scale, void* out,
                             void* workspace, size_t workspace_bytes, void* stream) {
-  if ((in_bytes > 0 && (!host_in || !dev_in)) || (out_bytes > 0 && (!host_out || !out)))
+  if ((in_bytes > 0 && (!host_in || !dev_in)) || (out_bytes > 0 && out && !host_out))
     return KVQ_E_INVALID_ARG;
+  // out NULL: the kernels store the output rows into host_out through its
+  // device mapping
+  void* out_dev = out;
+  if (!out) {
+    if (!host_out || cudaHostGetDevicePointer(&out_dev, host_out, 0) != cudaSuccess || !out_dev) {
+      cudaGetLastError();
+      return KVQ_E_INVALID_ARG;
+    }
+    out_bytes = 0;
+  }
   cudaStream_t s = static_cast<cudaStream_t>(stream);
   if (in_bytes > 0 &&
       cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
@@ -1003,7 +1013,7 @@ int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, 
                                  num_new_tokens, key_stride_tok, value_stride_tok, slot_mapping,
                                  key_cache, value_cache, num_blocks, block_size, q, query_start_loc,
                                  seq_lens, block_table, block_table_stride, max_query_len, sm_scale,
-                                 window, soft_cap, alibi_slopes, sinks, k_scale, v_scale, out,
+                                 window, soft_cap, alibi_slopes, sinks, k_scale, v_scale, out_dev,
                                  workspace, workspace_bytes, stream);
   if (rc != KVQ_OK) return rc;
   if (out_bytes > 0 &&

@@ -380,7 +380,8 @@ def prepare_decode_step_host_io(host_in, dev_in, host_out, out_bytes: int, key, 
     """kvq_decode_step_host_io, marshalled once (see Prepared): each call
     copies host_in (a pinned uint8 tensor) to dev_in, runs the decode step
     (whose device tensors may be views of dev_in), copies out_bytes of out
-    to host_out (pinned) and waits for the stream."""
+    to host_out (pinned) and waits for the stream.  out None: the step
+    writes its output straight into host_out (out_bytes ignored)."""
     return Prepared(lib.kvq_decode_step_host_io, _host_io_args(host_in, dev_in, host_out, out_bytes)
                     + _decode_step_args(key, value, slot_mapping, key_cache, value_cache, q,
                                         query_start_loc, seq_lens, block_table, max_query_len,

@@ -224,3 +224,27 @@ def test_fused_step_from_host_buffers(cuda_device):
     h_out.zero_()
     call()
     assert torch.equal(h_out.view(torch.int16), want_out)
+
+
+def test_fused_step_output_straight_to_host(cuda_device):
+    """kvq_decode_step_host_io with out NULL: the kernels store the output
+    rows into the pinned host buffer through its device mapping (no copy
+    after the step); the rows equal the device-output step's."""
+    wl = W.custom("step-host-out", [1, 3, 1, 2], [1500, 900, 33, 4000], 32, 8, 128, 16,
+                  "int8_per_token_head", 911, token_scale_range=(0.1, 10.0))
+    ref_step = Step(wl).run()
+    ref_step.check("device output")
+    want_out = ref_step.g.out.view(torch.int16).cpu()
+    st = Step(wl)
+    g = st.g
+    h_in = torch.zeros(256, dtype=torch.uint8).pin_memory()
+    d_in = torch.zeros(256, dtype=torch.uint8, device=g.dev)
+    h_out = torch.full(g.out.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    call = kvq().prepare_decode_step_host_io(
+        h_in, d_in, h_out, 0, st.nkey, st.nval, st.nslot, g.kc, g.vc, g.q, g.qsl, g.sl, g.bt, st.mql,
+        wl.sm_scale, wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, None, st.ws.t,
+        wl.kv_cache_dtype, wl.heads_kv)
+    call()
+    assert torch.equal(h_out.view(torch.int16), want_out)
+    assert torch.equal(g.kc.cpu(), ref_step.g.kc.cpu()) and torch.equal(g.vc.cpu(), ref_step.g.vc.cpu())
+    kvq().decode_step_check(st.ws.t)
