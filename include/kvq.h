@@ -322,14 +322,21 @@ KVQ_API int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim
 
 /* No counterpart on the pages (their steps start from device tensors).  One
  * decode step from host memory to host memory, for a serving loop whose
- * step inputs and result live on the host: copies in_bytes from host_in to
- * dev_in (one cudaMemcpyAsync on `stream`), runs kvq_decode_step with the
- * arguments after out_bytes -- its device pointers (key, value,
- * slot_mapping, q, query_start_loc, seq_lens, block_table, ...) may point
- * into dev_in --, copies the first out_bytes of `out` to host_out, and
- * waits for the stream.  host_in and host_out should be pinned (page-locked)
- * for the copies to be asynchronous; out_bytes must not exceed the output's
- * size.  in_bytes / out_bytes may be 0 (no copy).  With out NULL the step
+ * step inputs and result live on the host: brings in_bytes from host_in to
+ * dev_in, runs kvq_decode_step with the arguments after out_bytes -- its
+ * device pointers (key, value, slot_mapping, q, query_start_loc, seq_lens,
+ * block_table, ...) may point into dev_in --, copies the first out_bytes of
+ * `out` to host_out, and waits for the stream.  When the device addresses
+ * host_in (cudaHostGetDevicePointer succeeds: pinned memory, or any host
+ * memory on systems whose GPU reads pageable memory) and both it and dev_in
+ * are 16-byte aligned, the fused kernel does the copy: the
+ * cache write and the plan read their inputs from host_in directly and the
+ * kernel's other CTAs copy host_in to dev_in before its grid barrier (no
+ * separate copy to wait for); otherwise one cudaMemcpyAsync on `stream`
+ * comes first.  Either way dev_in holds host_in's bytes after the call.
+ * host_in and host_out should be pinned (page-locked) for the copies to be
+ * asynchronous; out_bytes must not exceed the output's size.  in_bytes /
+ * out_bytes may be 0 (no copy).  With out NULL the step
  * writes its output straight into host_out (pinned host memory the device
  * addresses; out_bytes is then ignored): the rows cross to the host as the
  * kernels store them, with no copy after the step.  Errors: those of
@@ -349,6 +356,46 @@ KVQ_API int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in
                                     int window, float soft_cap, const float* alibi_slopes,
                                     const float* sinks, float k_scale, float v_scale, void* out,
                                     void* workspace, size_t workspace_bytes, void* stream);
+
+/* No counterpart on the pages.  kvq_decode_step_host_io's work (without the
+ * final wait) captured once in a CUDA graph, for a serving loop that runs
+ * the same step on the same buffers every step: each
+ * kvq_decode_step_graph_launch replays it on `stream` and waits, so a step
+ * costs one graph launch instead of the call's several launches.  The
+ * caller rewrites host_in between launches (new rows, lengths, tables and
+ * slots within the capacities given here: num_req, max_query_len, the
+ * table's width); the plan lives on the device, so the replay follows.
+ * Arguments as kvq_decode_step_host_io's, minus the stream.  Unless
+ * in_bytes is 0, the fused kernel must be able to stage host_in (memory the
+ * device addresses, 16-byte aligned, as is dev_in): otherwise
+ * KVQ_E_UNSUPPORTED.  host_out must be pinned.
+ * Every buffer must stay allocated, in place, until the graph is destroyed.
+ * Errors: those of kvq_decode_step_host_io (nothing is created then),
+ * KVQ_E_CUDA for a failed capture.  Allocates the graph, its executable
+ * form and a private capture stream; *graph NULL on error. */
+typedef struct kvq_step_graph kvq_step_graph_t;
+KVQ_API int kvq_decode_step_graph_create(const void* host_in, void* dev_in, size_t in_bytes,
+                                         void* host_out, size_t out_bytes, int num_req,
+                                         int heads_q, int heads_kv, int head_dim,
+                                         kvq_dtype_t dtype, const void* key, const void* value,
+                                         int64_t num_new_tokens, int64_t key_stride_tok,
+                                         int64_t value_stride_tok, const int64_t* slot_mapping,
+                                         void* key_cache, void* value_cache, int64_t num_blocks,
+                                         int block_size, const void* q,
+                                         const int32_t* query_start_loc, const int32_t* seq_lens,
+                                         const int32_t* block_table, int block_table_stride,
+                                         int max_query_len, float sm_scale, int window,
+                                         float soft_cap, const float* alibi_slopes,
+                                         const float* sinks, float k_scale, float v_scale,
+                                         void* out, void* workspace, size_t workspace_bytes,
+                                         kvq_step_graph_t** graph);
+/* Replay a captured step on `stream` and wait for it.  KVQ_E_INVALID_ARG for
+ * a NULL graph, KVQ_E_CUDA for a failed launch or wait; the step's own
+ * errors (device lengths beyond the capacities, a barrier timeout) go to the
+ * workspace's error word, as kvq_decode_step's (kvq_decode_step_check). */
+KVQ_API int kvq_decode_step_graph_launch(kvq_step_graph_t* graph, void* stream);
+/* Free a captured step (NULL is a no-op); no launch of it may be pending. */
+KVQ_API void kvq_decode_step_graph_destroy(kvq_step_graph_t* graph);
 
 /* Workspace bytes of kvq_decode_step for these arguments on the current
  * device ([P2] Breakdown item 1: scratch sized from the KV element size and

@@ -45,6 +45,8 @@
 
 #include <cuda_runtime.h>
 
+#include <atomic>
+
 #include "kvq_cache_row.cuh"
 #include "kvq_device.cuh"
 #include "kvq_internal.h"
@@ -85,9 +87,11 @@ __device__ __forceinline__ int pv_dim(int mi, int g, int k) {
 // One row tile per (request, kv head): its first 16-token chunk, the keys
 // some of its rows see and its rows; the tiles' chunk counts are
 // prefix-summed by the kernel's first CTA (kDecodeThreads threads).  A
-// request with more rows than the launch
-// was built for (or more queries than keys) is left out and flags the error
-// word.
+// request with more rows than the launch was built for (or more queries
+// than keys) is left out and flags the error word.  (The lengths are read
+// where the step's inputs are before the barrier: host memory when the
+// kernel stages them.  Issuing a batch of tiles' loads together measured
+// slower, also from host memory.)
 __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams& sp) {
   __shared__ int32_t warp_sums[kDecodeWarps];
   const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
@@ -96,8 +100,8 @@ __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams&
   const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
   auto chunks_of = [&](int t, bool store) {
     const int r = t / p.heads_kv;
-    const int Q = p.query_start_loc[r + 1] - p.query_start_loc[r];
-    const int L = p.seq_lens[r];
+    const int Q = sp.in_query_start_loc[r + 1] - sp.in_query_start_loc[r];
+    const int L = sp.in_seq_lens[r];
     const int rows = Q * p.group;
     if (Q <= 0 || L < Q || rows > sp.max_rows) {
       if (store) {
@@ -145,6 +149,46 @@ __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams&
       f0 = f1;
     }
   }
+}
+
+// Staged inputs: every CTA but the planner (CTA 0, unless it is alone)
+// copies 16 bytes a thread from the mapped host buffer to the device one.
+// The loads are issued before the cache write and stored after it, so the
+// two host round trips overlap.
+constexpr int kStageRegs = 2;
+struct StageLane {
+  bool on;
+  int64_t i0, step, n16;
+  uint4 v[kStageRegs];
+};
+__device__ __forceinline__ void stage_issue(const StepParams& sp, StageLane& st) {
+  st.on = sp.stage_bytes > 0 && !(gridDim.x > 1 && blockIdx.x == 0);
+  if (!st.on) return;
+  const int64_t ctas = gridDim.x > 1 ? gridDim.x - 1 : 1;
+  const int64_t cta = gridDim.x > 1 ? blockIdx.x - 1 : 0;
+  st.i0 = cta * kDecodeThreads + threadIdx.x;
+  st.step = ctas * kDecodeThreads;
+  st.n16 = sp.stage_bytes >> 4;
+  const uint4* src = reinterpret_cast<const uint4*>(sp.stage_src);
+#pragma unroll
+  for (int k = 0; k < kStageRegs; ++k) {
+    const int64_t i = st.i0 + k * st.step;
+    if (i < st.n16) st.v[k] = src[i];
+  }
+}
+__device__ __forceinline__ void stage_finish(const StepParams& sp, const StageLane& st) {
+  if (!st.on) return;
+  const uint4* src = reinterpret_cast<const uint4*>(sp.stage_src);
+  uint4* dst = reinterpret_cast<uint4*>(sp.stage_dst);
+#pragma unroll
+  for (int k = 0; k < kStageRegs; ++k) {
+    const int64_t i = st.i0 + k * st.step;
+    if (i < st.n16) dst[i] = st.v[k];
+  }
+  for (int64_t i = st.i0 + kStageRegs * st.step; i < st.n16; i += st.step) dst[i] = src[i];
+  // the tail of a size that is not a multiple of 16
+  for (int64_t b = (st.n16 << 4) + st.i0; b < sp.stage_bytes; b += st.step)
+    sp.stage_dst[b] = sp.stage_src[b];
 }
 
 // Grid-wide barrier of a cooperative launch (every CTA resident): arrival
@@ -199,10 +243,13 @@ splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
   int64_t total_chunks = p.num_chunks;
   int64_t total_warps = p.num_warps;
   if constexpr (DEV) {
+    StageLane st;
+    stage_issue(sp, st);
     row::write_rows<DT, D>(sp.key, sp.value, sp.num_tokens, sp.key_stride, sp.value_stride,
                            p.heads_kv, sp.key_cache, sp.value_cache, sp.num_slots,
                            sp.slot_mapping, p.k_scale, p.v_scale, kDecodeThreads, threadIdx.x,
                            blockIdx.x, gridDim.x);
+    stage_finish(sp, st);
     if (blockIdx.x == 0) plan_step(p, sp);
     if (!grid_barrier(sp.barrier, p.error_flag)) return;
     total_chunks = __ldcg(sp.prefix + sp.num_tiles);
@@ -862,17 +909,28 @@ int launch_step_instance(const AttnParams& p, const StepParams& sp, int64_t* war
                          cudaStream_t stream) {
   const size_t smem = decode_smem_bytes(DT, D);
   auto kern = splitkv_decode_kernel<DT, D, NT, AL, true>;
-  int dev = 0, sms = 0, per_sm = 0;
-  if (cudaGetDevice(&dev) != cudaSuccess ||
-      cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
-      cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
-          cudaSuccess ||
-      cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) !=
-          cudaSuccess || per_sm <= 0) {
+  // The grid of each device, found once (the attribute and occupancy queries
+  // cost microseconds of host time, and a step calls this twice).
+  static std::atomic<int64_t> grid_of[kMaxCachedDevices];
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess) {
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
-  const int64_t grid = (int64_t)sms * per_sm;
+  int64_t grid = dev < kMaxCachedDevices ? grid_of[dev].load(std::memory_order_acquire) : 0;
+  if (grid <= 0) {
+    int sms = 0, per_sm = 0;
+    if (cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess ||
+        cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smem) !=
+            cudaSuccess ||
+        cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kDecodeThreads, smem) !=
+            cudaSuccess || per_sm <= 0) {
+      cudaGetLastError();
+      return KVQ_E_CUDA;
+    }
+    grid = (int64_t)sms * per_sm;
+    if (dev < kMaxCachedDevices) grid_of[dev].store(grid, std::memory_order_release);
+  }
   if (*warps == 0) {
     *warps = grid * kDecodeWarps;
     return KVQ_OK;

@@ -883,15 +883,28 @@ int kvq_decode_step_workspace_size(int num_req, int heads_q, int heads_kv, int h
   return KVQ_OK;
 }
 
-int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype,
-                    const void* key, const void* value, int64_t num_new_tokens,
-                    int64_t key_stride_tok, int64_t value_stride_tok, const int64_t* slot_mapping,
-                    void* key_cache, void* value_cache, int64_t num_blocks, int block_size,
-                    const void* q, const int32_t* query_start_loc, const int32_t* seq_lens,
-                    const int32_t* block_table, int block_table_stride, int max_query_len,
-                    float sm_scale, int window, float soft_cap, const float* alibi_slopes,
-                    const float* sinks, float k_scale, float v_scale, void* out, void* workspace,
-                    size_t workspace_bytes, void* stream) {
+namespace {
+// Inputs the fused kernel stages itself: `bytes` at `dev` are a copy of the
+// mapped host buffer `host`.  Before its grid barrier the kernel reads the
+// inputs that lie in that range from `host` and copies the range to `dev`;
+// after the barrier it reads `dev`.
+struct StageRange {
+  const char* host;
+  char* dev;
+  size_t bytes;
+};
+
+int decode_step_impl(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype,
+                     const void* key, const void* value, int64_t num_new_tokens,
+                     int64_t key_stride_tok, int64_t value_stride_tok,
+                     const int64_t* slot_mapping, void* key_cache, void* value_cache,
+                     int64_t num_blocks, int block_size, const void* q,
+                     const int32_t* query_start_loc, const int32_t* seq_lens,
+                     const int32_t* block_table, int block_table_stride, int max_query_len,
+                     float sm_scale, int window, float soft_cap, const float* alibi_slopes,
+                     const float* sinks, float k_scale, float v_scale, void* out,
+                     void* workspace, size_t workspace_bytes, void* stream,
+                     const StageRange* stage) {
   size_t need = 0;
   int rc = kvq_decode_step_workspace_size(num_req, heads_q, heads_kv, head_dim, dtype,
                                           max_query_len, alibi_slopes != nullptr, &need);
@@ -973,60 +986,202 @@ int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dt
   sp.num_req = num_req;
   sp.num_tiles = num_tiles;
   sp.max_rows = max_rows;
+  sp.in_query_start_loc = query_start_loc;
+  sp.in_seq_lens = seq_lens;
+  if (stage && stage->bytes > 0) {
+    // what the cache write and the plan read comes from the host buffer
+    auto host_side = [&](const void* ptr) -> const void* {
+      const char* a = static_cast<const char*>(ptr);
+      if (a && a >= stage->dev && a < stage->dev + stage->bytes) return stage->host + (a - stage->dev);
+      return ptr;
+    };
+    sp.key = static_cast<const uint16_t*>(host_side(key));
+    sp.value = static_cast<const uint16_t*>(host_side(value));
+    sp.slot_mapping = static_cast<const int64_t*>(host_side(slot_mapping));
+    sp.in_query_start_loc = static_cast<const int32_t*>(host_side(query_start_loc));
+    sp.in_seq_lens = static_cast<const int32_t*>(host_side(seq_lens));
+    sp.stage_src = reinterpret_cast<const uint8_t*>(stage->host);
+    sp.stage_dst = reinterpret_cast<uint8_t*>(stage->dev);
+    sp.stage_bytes = (int64_t)stage->bytes;
+  }
   // the fused kernel, then the merge of its cut tiles as a programmatic
   // dependent launch
   rc = kvq::launch_decode_step(p, sp, dtype, head_dim, warps, stream);
   if (rc != KVQ_OK) return rc;
   return kvq::launch_merge_step(p, sp, head_dim, warps, stream);
 }
+}  // namespace
 
-int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, void* host_out,
-                            size_t out_bytes, int num_req, int heads_q, int heads_kv, int head_dim,
-                            kvq_dtype_t dtype, const void* key, const void* value,
-                            int64_t num_new_tokens, int64_t key_stride_tok, int64_t value_stride_tok,
-                            const int64_t* slot_mapping, void* key_cache, void* value_cache,
-                            int64_t num_blocks, int block_size, const void* q,
-                            const int32_t* query_start_loc, const int32_t* seq_lens,
-                            const int32_t* block_table, int block_table_stride, int max_query_len,
-                            float sm_scale, int window, float soft_cap, const float* alibi_slopes,
-                            const float* sinks, float k_scale, float v_scale, void* out,
-                            void* workspace, size_t workspace_bytes, void* stream) {
+int kvq_decode_step(int num_req, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype,
+                    const void* key, const void* value, int64_t num_new_tokens,
+                    int64_t key_stride_tok, int64_t value_stride_tok, const int64_t* slot_mapping,
+                    void* key_cache, void* value_cache, int64_t num_blocks, int block_size,
+                    const void* q, const int32_t* query_start_loc, const int32_t* seq_lens,
+                    const int32_t* block_table, int block_table_stride, int max_query_len,
+                    float sm_scale, int window, float soft_cap, const float* alibi_slopes,
+                    const float* sinks, float k_scale, float v_scale, void* out, void* workspace,
+                    size_t workspace_bytes, void* stream) {
+  return decode_step_impl(num_req, heads_q, heads_kv, head_dim, dtype, key, value, num_new_tokens,
+                          key_stride_tok, value_stride_tok, slot_mapping, key_cache, value_cache,
+                          num_blocks, block_size, q, query_start_loc, seq_lens, block_table,
+                          block_table_stride, max_query_len, sm_scale, window, soft_cap,
+                          alibi_slopes, sinks, k_scale, v_scale, out, workspace, workspace_bytes,
+                          stream, nullptr);
+}
+
+#define KVQ_STEP_PARAMS                                                                      \
+  int num_req, int heads_q, int heads_kv, int head_dim, kvq_dtype_t dtype, const void* key,  \
+      const void* value, int64_t num_new_tokens, int64_t key_stride_tok,                      \
+      int64_t value_stride_tok, const int64_t* slot_mapping, void* key_cache,                 \
+      void* value_cache, int64_t num_blocks, int block_size, const void* q,                   \
+      const int32_t* query_start_loc, const int32_t* seq_lens, const int32_t* block_table,    \
+      int block_table_stride, int max_query_len, float sm_scale, int window, float soft_cap,  \
+      const float* alibi_slopes, const float* sinks, float k_scale, float v_scale, void* out, \
+      void* workspace, size_t workspace_bytes
+#define KVQ_STEP_ARGS                                                                          \
+  num_req, heads_q, heads_kv, head_dim, dtype, key, value, num_new_tokens, key_stride_tok,    \
+      value_stride_tok, slot_mapping, key_cache, value_cache, num_blocks, block_size, q,      \
+      query_start_loc, seq_lens, block_table, block_table_stride, max_query_len, sm_scale,    \
+      window, soft_cap, alibi_slopes, sinks, k_scale, v_scale, out, workspace, workspace_bytes
+
+namespace {
+// Where a host-buffer step's bytes go: host_in mapped into the device's
+// address space (pinned memory) is staged by the fused kernel itself
+// (stage), otherwise copied first (copy_in); out NULL stores the output rows
+// into host_out through its mapping (out_dev), otherwise out_bytes are
+// copied back.  for_graph: a step to be captured, where a copy from memory
+// the device cannot address is refused (KVQ_E_UNSUPPORTED).
+struct HostIo {
+  StageRange stage;
+  bool copy_in;
+  void* out_dev;
+  size_t out_bytes;
+};
+int host_io_resolve(const void* host_in, void* dev_in, size_t in_bytes, void* host_out,
+                    size_t out_bytes, void* out, bool for_graph, HostIo* io) {
   if ((in_bytes > 0 && (!host_in || !dev_in)) || (out_bytes > 0 && out && !host_out))
     return KVQ_E_INVALID_ARG;
-  // out NULL: the kernels store the output rows into host_out through its
-  // device mapping
-  void* out_dev = out;
+  io->stage = StageRange{nullptr, static_cast<char*>(dev_in), 0};
+  io->copy_in = false;
+  io->out_dev = out;
+  io->out_bytes = out_bytes;
   if (!out) {
-    if (!host_out || cudaHostGetDevicePointer(&out_dev, host_out, 0) != cudaSuccess || !out_dev) {
+    if (!host_out || cudaHostGetDevicePointer(&io->out_dev, host_out, 0) != cudaSuccess ||
+        !io->out_dev) {
       cudaGetLastError();
       return KVQ_E_INVALID_ARG;
     }
-    out_bytes = 0;
+    io->out_bytes = 0;
   }
-  cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (in_bytes > 0 &&
+  if (in_bytes > 0) {
+    void* in_map = nullptr;
+    if (cudaHostGetDevicePointer(&in_map, const_cast<void*>(host_in), 0) == cudaSuccess && in_map &&
+        aligned(in_map, 16) && aligned(dev_in, 16)) {
+      io->stage.host = static_cast<const char*>(in_map);
+      io->stage.bytes = in_bytes;
+    } else {
+      cudaGetLastError();
+      if (for_graph) return KVQ_E_UNSUPPORTED;
+      io->copy_in = true;
+    }
+  }
+  return KVQ_OK;
+}
+
+// The host-buffer step's work on stream s, without the final wait.
+int host_io_enqueue(const HostIo& io, const void* host_in, void* dev_in, size_t in_bytes,
+                    void* host_out, KVQ_STEP_PARAMS, cudaStream_t s) {
+  if (io.copy_in &&
       cudaMemcpyAsync(dev_in, host_in, in_bytes, cudaMemcpyHostToDevice, s) != cudaSuccess) {
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
-  const int rc = kvq_decode_step(num_req, heads_q, heads_kv, head_dim, dtype, key, value,
-                                 num_new_tokens, key_stride_tok, value_stride_tok, slot_mapping,
-                                 key_cache, value_cache, num_blocks, block_size, q, query_start_loc,
-                                 seq_lens, block_table, block_table_stride, max_query_len, sm_scale,
-                                 window, soft_cap, alibi_slopes, sinks, k_scale, v_scale, out_dev,
-                                 workspace, workspace_bytes, stream);
-  if (rc != KVQ_OK) return rc;
-  if (out_bytes > 0 &&
-      cudaMemcpyAsync(host_out, out, out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+  void* const out_arg = out;
+  {
+    void* out = io.out_dev;
+    const int rc = decode_step_impl(KVQ_STEP_ARGS, s, &io.stage);
+    if (rc != KVQ_OK) return rc;
+  }
+  if (io.out_bytes > 0 &&
+      cudaMemcpyAsync(host_out, out_arg, io.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
+  return KVQ_OK;
+}
+}  // namespace
+
+int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in_bytes, void* host_out,
+                            size_t out_bytes, KVQ_STEP_PARAMS, void* stream) {
+  HostIo io;
+  int rc = host_io_resolve(host_in, dev_in, in_bytes, host_out, out_bytes, out, false, &io);
+  if (rc != KVQ_OK) return rc;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  rc = host_io_enqueue(io, host_in, dev_in, in_bytes, host_out, KVQ_STEP_ARGS, s);
+  if (rc != KVQ_OK) return rc;
   if (cudaStreamSynchronize(s) != cudaSuccess) {
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
   return KVQ_OK;
 }
+
+struct kvq_step_graph {
+  cudaStream_t capture = nullptr;  // the private stream the step was captured on
+  cudaGraph_t graph = nullptr;
+  cudaGraphExec_t exec = nullptr;
+};
+
+void kvq_decode_step_graph_destroy(kvq_step_graph_t* g) {
+  if (!g) return;
+  if (g->exec) cudaGraphExecDestroy(g->exec);
+  if (g->graph) cudaGraphDestroy(g->graph);
+  if (g->capture) cudaStreamDestroy(g->capture);
+  cudaGetLastError();
+  delete g;
+}
+
+int kvq_decode_step_graph_create(const void* host_in, void* dev_in, size_t in_bytes,
+                                 void* host_out, size_t out_bytes, KVQ_STEP_PARAMS,
+                                 kvq_step_graph_t** graph) {
+  if (!graph) return KVQ_E_INVALID_ARG;
+  *graph = nullptr;
+  HostIo io;
+  int rc = host_io_resolve(host_in, dev_in, in_bytes, host_out, out_bytes, out, true, &io);
+  if (rc != KVQ_OK) return rc;
+  kvq_step_graph_t* g = new (std::nothrow) kvq_step_graph_t();
+  if (!g) return KVQ_E_CUDA;
+  if (cudaStreamCreateWithFlags(&g->capture, cudaStreamNonBlocking) != cudaSuccess ||
+      cudaStreamBeginCapture(g->capture, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
+    cudaGetLastError();
+    kvq_decode_step_graph_destroy(g);
+    return KVQ_E_CUDA;
+  }
+  rc = host_io_enqueue(io, host_in, dev_in, in_bytes, host_out, KVQ_STEP_ARGS, g->capture);
+  // the capture always ends (a failed step leaves an unusable graph)
+  const cudaError_t end = cudaStreamEndCapture(g->capture, &g->graph);
+  if (rc != KVQ_OK || end != cudaSuccess || !g->graph ||
+      cudaGraphInstantiate(&g->exec, g->graph, 0) != cudaSuccess) {
+    cudaGetLastError();
+    kvq_decode_step_graph_destroy(g);
+    return rc != KVQ_OK ? rc : KVQ_E_CUDA;
+  }
+  *graph = g;
+  return KVQ_OK;
+}
+
+int kvq_decode_step_graph_launch(kvq_step_graph_t* g, void* stream) {
+  if (!g || !g->exec) return KVQ_E_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (cudaGraphLaunch(g->exec, s) != cudaSuccess || cudaStreamSynchronize(s) != cudaSuccess) {
+    cudaGetLastError();
+    return KVQ_E_CUDA;
+  }
+  return KVQ_OK;
+}
+
+#undef KVQ_STEP_PARAMS
+#undef KVQ_STEP_ARGS
 
 int kvq_decode_step_check(const void* workspace) {
   if (!workspace) return KVQ_E_INVALID_ARG;

@@ -255,6 +255,17 @@ struct StepParams {
   uint32_t* barrier;            // [2]: arrivals, generation (grid barrier)
   int num_req, num_tiles;       // num_tiles = num_req * Hkv
   int max_rows;                 // 8 or 16: rows per tile the launch is built for
+  // The lengths as read before the grid barrier (the plan; the merge reads
+  // query_start_loc before it waits): AttnParams' own pointers, or their
+  // host mappings when the kernel stages the inputs itself.
+  const int32_t* in_query_start_loc;
+  const int32_t* in_seq_lens;
+  // Staged inputs: stage_bytes copied from a mapped host buffer to the device
+  // buffer the attention reads after the barrier (by every CTA but the
+  // planner); 0 when the inputs are already on the device.
+  const uint8_t* stage_src;
+  uint8_t* stage_dst;
+  int64_t stage_bytes;
 };
 
 // Workspace of the fused step for `warps` decode warps: an error word and
@@ -276,6 +287,9 @@ KVQ_HD constexpr StepWorkspace step_workspace(int num_tiles, int head_dim, int64
 }
 // Largest num_req * heads_kv of one fused step.
 constexpr int kMaxStepTiles = 1 << 16;
+// Devices whose launch configuration the host code keeps (others query it
+// on every call).
+constexpr int kMaxCachedDevices = 64;
 
 }  // namespace kvq
 

@@ -170,8 +170,10 @@ template <int D>
 __global__ void __launch_bounds__(kMergeThreads) merge_step_kernel(const AttnParams p, const StepParams sp,
                                                                  int64_t warps) {
   const int t = blockIdx.x;
-  // (the caller's input; the plan is the fused kernel's, read after the wait)
-  const int q0 = p.query_start_loc[t / p.heads_kv];
+  // (the caller's input, as the fused kernel read it before its barrier --
+  // host memory when that kernel stages the inputs; the plan is the fused
+  // kernel's, read after the wait)
+  const int q0 = sp.in_query_start_loc[t / p.heads_kv];
   asm volatile("griddepcontrol.wait;" ::: "memory");
   const int64_t T = __ldcg(sp.prefix + sp.num_tiles);
   const int64_t f0 = __ldcg(sp.prefix + t), f1 = __ldcg(sp.prefix + t + 1);

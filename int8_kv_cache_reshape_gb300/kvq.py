@@ -100,6 +100,14 @@ lib.kvq_decode_step.argtypes = [
     _c.c_float, _c.c_int, _c.c_float, _p, _p, _c.c_float, _c.c_float, _p, _p, _c.c_size_t, _p]
 lib.kvq_decode_step_host_io.restype = _c.c_int
 lib.kvq_decode_step_host_io.argtypes = [_p, _p, _c.c_size_t, _p, _c.c_size_t] + lib.kvq_decode_step.argtypes
+lib.kvq_decode_step_graph_create.restype = _c.c_int
+lib.kvq_decode_step_graph_create.argtypes = ([_p, _p, _c.c_size_t, _p, _c.c_size_t]
+                                             + lib.kvq_decode_step.argtypes[:-1]
+                                             + [_c.POINTER(_p)])
+lib.kvq_decode_step_graph_launch.restype = _c.c_int
+lib.kvq_decode_step_graph_launch.argtypes = [_p, _p]
+lib.kvq_decode_step_graph_destroy.restype = None
+lib.kvq_decode_step_graph_destroy.argtypes = [_p]
 lib.kvq_decode_step_workspace_size.restype = _c.c_int
 lib.kvq_decode_step_workspace_size.argtypes = [
     _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.c_int, _c.POINTER(_c.c_size_t)]
@@ -388,6 +396,52 @@ def prepare_decode_step_host_io(host_in, dev_in, host_out, out_bytes: int, key, 
                                         sm_scale, window, soft_cap, k_scale, v_scale, out,
                                         workspace, kv_cache_dtype, heads_kv, alibi_slopes, sinks,
                                         stream, num_blocks), "kvq_decode_step_host_io")
+
+
+class DecodeStepGraph:
+    """A host-buffer decode step captured once in a CUDA graph
+    (kvq_decode_step_graph_create); calling it replays the step on the
+    stream it was made for and waits (kvq_decode_step_graph_launch).  The
+    buffers behind it must stay alive, in place, until close()."""
+
+    def __init__(self, handle, stream):
+        self._h = handle
+        self._stream = stream
+        self._launch = lib.kvq_decode_step_graph_launch
+
+    def __call__(self) -> None:
+        _check(self._launch(self._h, self._stream), "kvq_decode_step_graph_launch")
+
+    def close(self) -> None:
+        if self._h:
+            lib.kvq_decode_step_graph_destroy(self._h)
+            self._h = None
+
+    def __del__(self):
+        try:
+            self.close()
+        except Exception:
+            pass
+
+
+def decode_step_graph(host_in, dev_in, host_out, out_bytes: int, key, value, slot_mapping,
+                      key_cache, value_cache, q, query_start_loc, seq_lens, block_table,
+                      max_query_len: int, sm_scale: float, window: int, soft_cap: float,
+                      k_scale: float, v_scale: float, out, workspace, kv_cache_dtype,
+                      heads_kv: int, alibi_slopes=None, sinks=None, stream=None,
+                      num_blocks=None) -> DecodeStepGraph:
+    """kvq_decode_step_graph_create with the arguments of
+    prepare_decode_step_host_io; host_in must be pinned (the fused kernel
+    stages it).  Rewrite host_in between calls of the returned object."""
+    args = (_host_io_args(host_in, dev_in, host_out, out_bytes)
+            + _decode_step_args(key, value, slot_mapping, key_cache, value_cache, q,
+                                query_start_loc, seq_lens, block_table, max_query_len, sm_scale,
+                                window, soft_cap, k_scale, v_scale, out, workspace,
+                                kv_cache_dtype, heads_kv, alibi_slopes, sinks, stream,
+                                num_blocks))
+    h = _p()
+    _check(lib.kvq_decode_step_graph_create(*args[:-1], _c.byref(h)), "kvq_decode_step_graph_create")
+    return DecodeStepGraph(h, args[-1])
 
 
 def decode_step_check(workspace) -> None:

@@ -248,3 +248,154 @@ def test_fused_step_output_straight_to_host(cuda_device):
     assert torch.equal(h_out.view(torch.int16), want_out)
     assert torch.equal(g.kc.cpu(), ref_step.g.kc.cpu()) and torch.equal(g.vc.cpu(), ref_step.g.vc.cpu())
     kvq().decode_step_check(st.ws.t)
+
+
+def _packed_inputs(st, extra_tail, host):
+    """The step's inputs packed 256-byte aligned into one host buffer (plus
+    `extra_tail` bytes of noise at the end), and a garbage-filled device
+    buffer with views at the same offsets.  host: "pinned", "pinned+8" (a
+    pinned buffer starting 8 bytes past a 16-byte boundary) or "pageable"."""
+    g = st.g
+    parts = [g.q, st.nkey, st.nval, st.nslot, g.qsl, g.sl, g.bt]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    gen = torch.Generator().manual_seed(17)
+    h_in = torch.randint(0, 256, (o + extra_tail + 8,), dtype=torch.uint8, generator=gen)
+    if host != "pageable":
+        h_in = h_in.pin_memory()
+    h_in = h_in[8:] if host == "pinned+8" else h_in[:o + extra_tail]
+    for t, off, n in zip(parts, offs, sizes):
+        h_in[off:off + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+    d_in = torch.full((o + extra_tail,), 0xA5, dtype=torch.uint8, device=g.dev)
+    views = [d_in[off:off + n].view(t.dtype).view(t.shape) for t, off, n in zip(parts, offs, sizes)]
+    return h_in, d_in, views
+
+
+@pytest.mark.parametrize("host", ["pinned", "pinned+8", "pageable"])
+def test_fused_step_host_inputs_reach_the_device(cuda_device, host):
+    """kvq_decode_step_host_io's two ways in: pinned host_in on a 16-byte
+    boundary is read by the fused kernel through its device mapping and
+    copied to dev_in by the kernel's CTAs (a size with a 13-byte tail beyond
+    the last 16-byte word); host_in 8 bytes off that boundary goes through
+    one copy first; pageable host_in takes either way, depending on whether
+    the device addresses pageable memory.  Each time dev_in ends up equal to
+    host_in byte for byte, and the caches and the host output equal the
+    device-input step's."""
+    wl = W.custom("step-host-stage", [1, 1, 2, 1, 3, 1], [64, 1200, 480, 17, 3000, 256], 32, 8, 128,
+                  16, "fp8_e5m2", 913)
+    ref_step = Step(wl).run()
+    ref_step.check("device inputs")
+    want_out = ref_step.g.out.view(torch.int16).cpu()
+    want_kc, want_vc = ref_step.g.kc.cpu(), ref_step.g.vc.cpu()
+    st = Step(wl)
+    g = st.g
+    h_in, d_in, views = _packed_inputs(st, 13, host)
+    q, nkey, nval, nslot, qsl, sl, bt = views
+    h_out = torch.zeros(g.out.shape, dtype=torch.bfloat16).pin_memory()
+    call = kvq().prepare_decode_step_host_io(
+        h_in, d_in, h_out, 0, nkey, nval, nslot, g.kc, g.vc, q, qsl, sl, bt, st.mql,
+        wl.sm_scale, wl.window, wl.soft_cap, wl.k_scale, wl.v_scale, None, st.ws.t,
+        wl.kv_cache_dtype, wl.heads_kv)
+    call()
+    assert torch.equal(d_in.cpu(), h_in)
+    assert torch.equal(h_out.view(torch.int16), want_out)
+    assert torch.equal(g.kc.cpu(), want_kc) and torch.equal(g.vc.cpu(), want_vc)
+    kvq().decode_step_check(st.ws.t)
+
+
+def _pack_into(h_in, offs, tensors):
+    for t, off in zip(tensors, offs):
+        n = t.numel() * t.element_size()
+        h_in[off:off + n].copy_(t.cpu().contiguous().view(-1).view(torch.uint8))
+
+
+def test_fused_step_graph_from_host_buffers(cuda_device):
+    """kvq_decode_step_graph_create / _launch: the host-buffer step captured
+    once (inputs staged by the fused kernel from pinned host memory, output
+    stored straight into pinned host memory).  A launch equals the one-call
+    step bit for bit; after a second batch's rows, lengths, slots and table
+    are written into the same pinned buffer (same capacities) and the caches
+    are refilled with its context, a launch of the same graph matches the
+    oracle for that batch."""
+    hq, hkv, D = 32, 8, 128
+    # dynamic per-token-head scales: the captured step's per-tensor scales
+    # would be a's, not b's
+    a = W.custom("graph-io-a", [1, 2, 1, 1, 3, 1], [900, 40, 3200, 300, 7, 1500], hq, hkv, D, 16,
+                 "int8_per_token_head", 630, token_scale_range=(0.1, 10.0), extra_blocks=200)
+    ref_step = Step(a).run()
+    ref_step.check("graph io: device inputs")
+    want_out = ref_step.g.out.view(torch.int16).cpu()
+    st = Step(a)
+    g = st.g
+    parts = [g.q, st.nkey, st.nval, st.nslot, g.qsl, g.sl, g.bt]
+    sizes = [t.numel() * t.element_size() for t in parts]
+    offs, o = [], 0
+    for n in sizes:
+        offs.append(o)
+        o += (n + 255) // 256 * 256
+    h_in = torch.zeros(o, dtype=torch.uint8).pin_memory()
+    _pack_into(h_in, offs, parts)
+    d_in = torch.full((o,), 0xA5, dtype=torch.uint8, device=g.dev)
+    q, nkey, nval, nslot, qsl, sl, bt = [d_in[off:off + n].view(t.dtype).view(t.shape)
+                                         for t, off, n in zip(parts, offs, sizes)]
+    h_out = torch.full(g.out.shape, float("nan"), dtype=torch.bfloat16).pin_memory()
+    step = kvq().decode_step_graph(h_in, d_in, h_out, 0, nkey, nval, nslot, g.kc, g.vc, q, qsl,
+                                   sl, bt, st.mql, a.sm_scale, a.window, a.soft_cap, a.k_scale,
+                                   a.v_scale, None, st.ws.t, a.kv_cache_dtype, a.heads_kv)
+    try:
+        step()
+        assert torch.equal(h_out.view(torch.int16), want_out)
+        assert torch.equal(d_in.cpu(), h_in)
+        assert torch.equal(g.kc.cpu(), ref_step.g.kc.cpu())
+        assert torch.equal(g.vc.cpu(), ref_step.g.vc.cpu())
+        kvq().decode_step_check(st.ws.t)
+
+        # batch b: same request count and query lengths, other context lengths
+        b = W.custom("graph-io-b", [1, 2, 1, 1, 3, 1], [1700, 2, 600, 3100, 45, 900], hq, hkv, D,
+                     16, "int8_per_token_head", 631, token_scale_range=(0.1, 10.0),
+                     num_blocks=a.num_blocks)
+        assert b.block_table.shape[1] <= a.block_table.shape[1]
+        gb = GpuRun(b)
+        new = b.new_token_mask()
+        old_slots = b.slot_mapping.clone()
+        old_slots[new] = -1
+        g.kc.fill_(0xCD)
+        g.vc.fill_(0xCD)
+        kvq().reshape_and_cache(gb.key, gb.value, g.kc, g.vc, old_slots.to(g.dev),
+                                b.kv_cache_dtype, b.k_scale, b.v_scale)
+        torch.cuda.synchronize()
+        idx = torch.nonzero(new).flatten()
+        bt_b = torch.full(tuple(g.bt.shape), -1, dtype=torch.int32)
+        bt_b[:, :b.block_table.shape[1]] = b.block_table
+        _pack_into(h_in, offs, [b.q, b.key[idx], b.value[idx], b.slot_mapping[idx],
+                                b.query_start_loc, b.seq_lens_t, bt_b])
+        h_out.fill_(float("nan"))
+        step()
+        kvq().decode_step_check(st.ws.t)
+        kc, vc = oracle_cache(b)
+        assert np.array_equal(g.kc.cpu().numpy(), kc) and np.array_equal(g.vc.cpu().numpy(), vc)
+        ref, bnd = oracle_reference(b, kc, vc)
+        assert_attention_close(h_out.float().numpy(), ref, "graph replay with new host inputs", bnd)
+    finally:
+        step.close()
+
+
+def test_fused_step_graph_refuses_inputs_it_cannot_stage(cuda_device):
+    """A host_in the fused kernel cannot stage (here: 8 bytes off a 16-byte
+    boundary) would need a copy inside the graph: KVQ_E_UNSUPPORTED, and
+    nothing is created."""
+    wl = W.custom("graph-io-unaligned", [1, 1], [64, 200], 8, 2, 64, 16, "fp8_e4m3", 632)
+    st = Step(wl)
+    g = st.g
+    h_in = torch.zeros(4096 + 8, dtype=torch.uint8).pin_memory()[8:]
+    d_in = torch.zeros(4096, dtype=torch.uint8, device=g.dev)
+    h_out = torch.zeros(g.out.shape, dtype=torch.bfloat16).pin_memory()
+    with pytest.raises(kvq().KvqError) as e:
+        kvq().decode_step_graph(h_in, d_in, h_out, 0, st.nkey, st.nval, st.nslot, g.kc, g.vc, g.q,
+                                g.qsl, g.sl, g.bt, st.mql, wl.sm_scale, wl.window, wl.soft_cap,
+                                wl.k_scale, wl.v_scale, None, st.ws.t, wl.kv_cache_dtype,
+                                wl.heads_kv)
+    assert e.value.status == kvq().E_UNSUPPORTED
