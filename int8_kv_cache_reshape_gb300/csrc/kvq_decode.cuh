@@ -223,8 +223,10 @@ __device__ __forceinline__ bool grid_barrier(uint32_t* bar, int32_t* error_flag)
 }
 
 // DEV: the fused decode step -- the new tokens are written to the caches,
-// the plan is built from the device's lengths, and a grid barrier separates
-// both from the attention (which then reads the caches with coherent loads).
+// the plan is built from the device's lengths (and, when the inputs come
+// from a mapped host buffer, that buffer is copied to the device), and a
+// grid barrier separates all of it from the attention (which then reads the
+// caches with coherent loads).
 template <int DT, int D, int NT, bool AL, bool DEV>
 __global__ void __launch_bounds__(kDecodeThreads, decode_min_ctas(DT, D, NT))
 splitkv_decode_kernel(const AttnParams p, const StepParams sp) {
