@@ -223,3 +223,37 @@ def test_decode_step_shape_checks_come_first():
     assert f(4, 32, 8, 128, 9, 1, 0, ctypes.byref(out)) == kvq.E_INVALID_ARG   # dtype
     assert f(4, 32, 8, 128, 1, 1, 0, None) == kvq.E_INVALID_ARG
     assert kvq.lib.kvq_decode_step_check(None) == kvq.E_INVALID_ARG
+
+
+def _step_args():
+    """kvq_decode_step's arguments after the host-buffer ones, with NULL
+    pointers (never dereferenced: the calls below are refused first)."""
+    return [4, 32, 8, 128, 1, None, None, 0, 1024, 1024, None, None, None, 16, 16, None, None,
+            None, None, 1, 1, 0.088, 0, 0.0, None, None, 1.0, 1.0, None, None, 0]
+
+
+def test_host_io_checks_its_buffers_before_any_device_call():
+    """kvq_decode_step_host_io: a NULL buffer with a nonzero size is refused
+    on the host (no GPU needed)."""
+    f = kvq.lib.kvq_decode_step_host_io
+    h = ctypes.create_string_buffer(64)
+    assert f(None, ctypes.c_void_p(256), 64, None, 0, *_step_args(), None) == kvq.E_INVALID_ARG
+    assert f(h, None, 64, None, 0, *_step_args(), None) == kvq.E_INVALID_ARG
+    # out given, out_bytes > 0, host_out NULL
+    args = _step_args()
+    args[-3] = ctypes.c_void_p(256)
+    assert f(None, None, 0, None, 16, *args, None) == kvq.E_INVALID_ARG
+
+
+def test_step_graph_entry_points_refuse_null_handles():
+    """kvq_decode_step_graph_create needs somewhere to put the graph, and
+    refuses NULL buffers with sizes as host_io does; launch refuses a NULL
+    graph; destroy accepts NULL."""
+    create = kvq.lib.kvq_decode_step_graph_create
+    h = ctypes.c_void_p()
+    assert create(None, None, 0, None, 0, *_step_args(), None) == kvq.E_INVALID_ARG
+    assert create(None, ctypes.c_void_p(256), 64, None, 0, *_step_args(),
+                  ctypes.byref(h)) == kvq.E_INVALID_ARG
+    assert h.value is None
+    assert kvq.lib.kvq_decode_step_graph_launch(None, None) == kvq.E_INVALID_ARG
+    kvq.lib.kvq_decode_step_graph_destroy(None)
