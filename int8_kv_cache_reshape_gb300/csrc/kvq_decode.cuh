@@ -98,10 +98,18 @@ __device__ __forceinline__ void plan_step(const AttnParams& p, const StepParams&
   const int nt = sp.num_tiles;
   const int per = (nt + kDecodeThreads - 1) / kDecodeThreads;
   const int t0 = min(nt, tid * per), t1 = min(nt, t0 + per);
+  // A thread's tiles are consecutive, mostly the kv heads of one request:
+  // the last request's lengths stay in registers.
+  int last_r = -1, last_q = 0, last_l = 0;
   auto chunks_of = [&](int t, bool store) {
     const int r = t / p.heads_kv;
-    const int Q = sp.in_query_start_loc[r + 1] - sp.in_query_start_loc[r];
-    const int L = sp.in_seq_lens[r];
+    if (r != last_r) {
+      last_r = r;
+      last_q = sp.in_query_start_loc[r + 1] - sp.in_query_start_loc[r];
+      last_l = sp.in_seq_lens[r];
+    }
+    const int Q = last_q;
+    const int L = last_l;
     const int rows = Q * p.group;
     if (Q <= 0 || L < Q || rows > sp.max_rows) {
       if (store) {
