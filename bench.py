@@ -47,15 +47,15 @@ PROFILED_TRAFFIC = {
     # (workload, kv cache dtype, part of a mixed batch): DRAM bytes read +
     # written by that kernel in one launch, from the ncu capture in `profile`
     # (its "traffic" command; taken while the listed sources hashed to `sha1`).
-    (2, "fp8_e4m3", None): {"bytes": 361.341696e6 + 4.710144e6,
+    (2, "fp8_e4m3", None): {"bytes": 361.342976e6 + 4.596992e6,
                             "profile": "profiles/splitkv_decode_decode_batch.md",
-                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "38619d01a20302e3e2f48a2bcc3b13bc00517887"},
-    (5, "fp8_e5m2", None): {"bytes": 269.840896e6 + 4.427520e6,
+                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "635463d3cff41345045b05fa4f50b3d17c1b7c78"},
+    (5, "fp8_e5m2", None): {"bytes": 269.877760e6 + 4.454912e6,
                             "profile": "profiles/splitkv_decode_long_context.md",
-                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "38619d01a20302e3e2f48a2bcc3b13bc00517887"},
-    (4, "int8_per_token_head", "decode"): {"bytes": 484.947200e6 + 5.240064e6,
+                            "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "635463d3cff41345045b05fa4f50b3d17c1b7c78"},
+    (4, "int8_per_token_head", "decode"): {"bytes": 484.951296e6 + 5.326592e6,
                                            "profile": "profiles/mixed_batch_int8_per_token_head.md",
-                                           "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "38619d01a20302e3e2f48a2bcc3b13bc00517887"},
+                                           "sources": ['kvq_decode.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "635463d3cff41345045b05fa4f50b3d17c1b7c78"},
     (4, "int8_per_token_head", "prefill"): {"bytes": 379.163136e6 + 89.351680e6,
                                             "profile": "profiles/mixed_batch_int8_per_token_head.md",
                                             "sources": ['kvq_prefill.cuh', 'kvq_tcgen05.cuh', 'kvq_device.cuh', 'kvq_internal.h'], "sha1": "1960048207eeaf5dafb97e8a77909eb4819e45fe"},
