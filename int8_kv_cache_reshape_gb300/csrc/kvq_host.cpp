@@ -1096,14 +1096,16 @@ int host_io_enqueue(const HostIo& io, const void* host_in, void* dev_in, size_t 
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
-  void* const out_arg = out;
   {
+    // the step writes io.out_dev: `out` itself, or host_out's device mapping
+    // (the local name is the one KVQ_STEP_ARGS passes on)
     void* out = io.out_dev;
     const int rc = decode_step_impl(KVQ_STEP_ARGS, s, &io.stage);
     if (rc != KVQ_OK) return rc;
   }
+  // (a copy back only when `out` was given, so io.out_dev is `out`)
   if (io.out_bytes > 0 &&
-      cudaMemcpyAsync(host_out, out_arg, io.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
+      cudaMemcpyAsync(host_out, io.out_dev, io.out_bytes, cudaMemcpyDeviceToHost, s) != cudaSuccess) {
     cudaGetLastError();
     return KVQ_E_CUDA;
   }
