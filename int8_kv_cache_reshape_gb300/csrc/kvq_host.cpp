@@ -44,9 +44,12 @@ struct kvq_sched {
   int num_req, heads_q, heads_kv, head_dim, dtype, causal, window, group;
   int device;
   int64_t total_q;
-  std::vector<DecodePiece> pieces;
-  std::vector<WarpSeg> warp_seg;  // per launch, per warp: its segment and first piece
-  std::vector<MergeItem> merges;
+  // The plan lives in its host image (below): the pieces of both launches,
+  // then per launch and warp its segment and first piece, the merge items.
+  const DecodePiece* h_pieces;
+  const WarpSeg* h_warps;
+  const MergeItem* h_merges;
+  int64_t num_pieces, num_merges;
   std::vector<PrefillTile> prefill;
   DecodeLaunch launch[2];
   int64_t num_tiles, max_splits, partial_rows;
@@ -56,7 +59,7 @@ struct kvq_sched {
   size_t d_buf_bytes;
   size_t d_pieces_off, d_warps_off, d_merges_off, d_prefill_off, d_error_off;
   size_t image_bytes;       // bytes of the plan image (host and device copies)
-  void* h_image;            // pinned host image, uploaded by the first attention call
+  void* h_image;            // host image (pinned with a device), uploaded by the first attention call
   size_t h_image_bytes;
   bool h_image_pinned;
   std::atomic<bool> uploaded;
@@ -329,6 +332,11 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   s->h_image = nullptr;
   s->h_image_bytes = 0;
   s->h_image_pinned = false;
+  s->h_pieces = nullptr;
+  s->h_warps = nullptr;
+  s->h_merges = nullptr;
+  s->num_pieces = 0;
+  s->num_merges = 0;
   s->uploaded.store(false);
   // Without a usable CUDA device the plan is still built (host-only: its
   // attention calls return KVQ_E_CUDA), so that planning can be inspected
@@ -432,10 +440,8 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
                      });
   }
 
-  // 2) Work decomposition (stream-K): per class, lay the tiles' chunks end
-  //    to end and cut the sequence into equal contiguous segments, one per
-  //    warp.  A tile cut by a segment boundary becomes several pieces whose
-  //    partial rows are merged.  Tile order:
+  // 2) Per class of row tiles: the chunk count, the tile order and the warp
+  //    count.  Tile order:
   //    - request-major ((request, kv head) order) when a cache row is a whole
   //      number of 128-byte lines;
   //    - head lockstep otherwise (per-token-head rows of D + 16 bytes, 64-byte
@@ -456,49 +462,9 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   lockstep = lockstep && heads_kv > 1;
   s->partial_rows = 0;
   s->max_splits = 0;
-  struct Cut {
-    int64_t warp, lo, hi;
-  };
-  std::vector<int64_t> seg;
-  std::vector<Cut> cuts;
-  cuts.reserve(64);
-  s->pieces.reserve(tiles[0].size() + tiles[1].size() + 2 * 4096);
-  s->merges.reserve(tiles[0].size() + tiles[1].size());
-  auto add_piece = [&](const Tile& t, int64_t flat, int64_t chunk, int32_t part, int32_t merge) {
-    DecodePiece pc;
-    pc.req = t.req;
-    pc.kv_head = t.kv_head;
-    pc.row0 = t.row0;
-    pc.nrows = t.nrows;
-    pc.part = part;
-    pc.merge = merge;
-    pc.any_lo = (int32_t)t.any_lo;
-    pc.any_hi = (int32_t)t.any_hi;
-    pc.flat0 = (int32_t)flat;
-    pc.chunk0 = (int32_t)chunk;
-    pc.pad0 = pc.pad1 = 0;
-    s->pieces.push_back(pc);
-  };
-  // A merge item for a tile cut into np pieces; its partial rows follow the
-  // ones handed out so far.
-  auto add_merge = [&](const Tile& t, int64_t np) {
-    MergeItem m;
-    m.req = t.req;
-    m.kv_head = t.kv_head;
-    m.row0 = t.row0;
-    m.nrows = t.nrows;
-    m.part = (int32_t)s->partial_rows;
-    m.nsplits = (int32_t)np;
-    m.pad0 = m.pad1 = 0;
-    s->merges.push_back(m);
-    s->partial_rows += np * t.nrows;
-    s->max_splits = std::max(s->max_splits, np);
-    return (int32_t)(s->merges.size() - 1);
-  };
+  int64_t max_pieces = 0, max_merges = 0, num_warps = 0;
   for (int cls = 0; cls < 2; ++cls) {
     DecodeLaunch& dl = s->launch[cls];
-    dl.piece_off = (int64_t)s->pieces.size();
-    dl.warp_off = (int64_t)s->warp_seg.size();
     int64_t T = 0;
     for (const Tile& t : tiles[cls]) T += t.c_hi - t.c_lo;
     dl.num_chunks = T;
@@ -523,17 +489,76 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
       const int64_t unit = (int64_t)heads_kv * kvq::kDecodeWarps / std::gcd<int64_t>(heads_kv, kvq::kDecodeWarps);
       if (W >= unit) W = W / unit * unit;
     }
-
-    // Stream-K: segment w is [floor(w T / W), floor((w + 1) T / W)).
     dl.num_warps = (int)W;
-    s->warp_seg.resize((size_t)(dl.warp_off + W), WarpSeg{0, 0, 0, 0});
-    // Segment starts floor(w T / W), incrementally (no divides in the loop).
+    // a tile is cut at most at every segment boundary inside it
+    max_pieces += (int64_t)tiles[cls].size() + W - 1;
+    max_merges += (int64_t)tiles[cls].size();
+    num_warps += W;
+  }
+
+  // 3) The plan image, laid out for the largest plan these tiles can give:
+  //    pieces, per-launch warp table, merge items, prefill tiles, the error
+  //    word.  With a device it is pinned host memory, and a pooled device
+  //    buffer is reserved for it; the first attention call uploads it on its
+  //    own stream (no synchronisation here).  The decomposition below writes
+  //    the image directly.
+  s->d_pieces_off = 0;
+  s->d_warps_off = kvq::align256((size_t)max_pieces * sizeof(DecodePiece));
+  s->d_merges_off = s->d_warps_off + kvq::align256((size_t)num_warps * sizeof(WarpSeg));
+  s->d_prefill_off = s->d_merges_off + kvq::align256((size_t)max_merges * sizeof(MergeItem));
+  s->d_error_off = s->d_prefill_off + kvq::align256(s->prefill.size() * sizeof(PrefillTile));
+  const size_t total = s->d_error_off + sizeof(int32_t);
+  s->image_bytes = total;
+  if (have_device) {
+    s->d_buf = pool_get(s->device, total, &s->d_buf_bytes);
+    if (!s->d_buf) {
+      delete s;
+      return KVQ_E_NO_MEMORY;
+    }
+    s->h_image = pinned_get(total, &s->h_image_bytes, &s->h_image_pinned);
+  } else {
+    s->h_image = std::malloc(total);
+    s->h_image_bytes = total;
+    s->h_image_pinned = false;
+  }
+  if (!s->h_image) {
+    kvq_sched_destroy(s);
+    return KVQ_E_NO_MEMORY;
+  }
+  char* image = static_cast<char*>(s->h_image);
+  DecodePiece* const P = reinterpret_cast<DecodePiece*>(image + s->d_pieces_off);
+  WarpSeg* const WS = reinterpret_cast<WarpSeg*>(image + s->d_warps_off);
+  MergeItem* const M = reinterpret_cast<MergeItem*>(image + s->d_merges_off);
+  s->h_pieces = P;
+  s->h_warps = WS;
+  s->h_merges = M;
+  if (!s->prefill.empty())
+    std::memcpy(image + s->d_prefill_off, s->prefill.data(), s->prefill.size() * sizeof(PrefillTile));
+  std::memset(image + s->d_error_off, 0, sizeof(int32_t));  // the error word starts at zero
+
+  // 4) Work decomposition (stream-K): per class, lay the tiles' chunks end
+  //    to end and cut the sequence into equal contiguous segments, one per
+  //    warp.  A tile cut by a segment boundary becomes several pieces whose
+  //    partial rows are merged.  (Counters in locals and stores through plain
+  //    pointers into the image: this runs once per planned step.)
+  int64_t npieces = 0, nmerges = 0, nwarps = 0, partial_rows = 0, max_splits = 0;
+  std::vector<int64_t> seg;
+  for (int cls = 0; cls < 2; ++cls) {
+    DecodeLaunch& dl = s->launch[cls];
+    dl.piece_off = npieces;
+    dl.warp_off = nwarps;
+    const int64_t T = dl.num_chunks;
+    if (T == 0) continue;
+    const int64_t W = dl.num_warps;
+    // Stream-K: segment w is [floor(w T / W), floor((w + 1) T / W)),
+    // incrementally (no divides in the loop).
     seg.resize((size_t)W + 1);
+    int64_t* const sg = seg.data();
     {
       const int64_t qt = T / W, rt = T % W;
       int64_t q = 0, r = 0;
       for (int64_t w = 0; w <= W; ++w) {
-        seg[(size_t)w] = q;
+        sg[w] = q;
         q += qt;
         r += rt;
         if (r >= W) {
@@ -544,78 +569,73 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     }
     // Segment w goes to warp phys(w).  Head lockstep with W = Hkv * Wh: the
     // v-th segments of all kv heads go to neighbouring warps.
-    const bool interleave = ls && W % heads_kv == 0;
+    const bool interleave = dl.lockstep && W % heads_kv == 0;
     const int64_t Wh = W / heads_kv;
     auto phys = [&](int64_t w) { return interleave ? (w % Wh) * heads_kv + w / Wh : w; };
+    WarpSeg* const ws = WS + nwarps;
     for (int64_t w = 0; w < W; ++w) {
-      WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + phys(w))];
-      ws.seg0 = (int32_t)seg[(size_t)w];
-      ws.n = (int32_t)(seg[(size_t)w + 1] - seg[(size_t)w]);
+      WarpSeg& e = ws[phys(w)];
+      e.piece = 0;
+      e.seg0 = (int32_t)sg[w];
+      e.n = (int32_t)(sg[w + 1] - sg[w]);
+      e.pad = 0;
     }
-    // Tiles and warps in one pass: w is the warp whose segment holds F.
-    int64_t F = 0;  // flat position of the current tile's first chunk
+    // Tiles and warps in one pass: w is the warp whose segment holds F; the
+    // warps [w, we) hold the tile's chunks [F, Fe).
+    int64_t F = 0;
     int64_t w = 0;
     for (const Tile& t : tiles[cls]) {
-      const int64_t nt = t.c_hi - t.c_lo;
-      while (w + 1 < W && seg[(size_t)w + 1] <= F) ++w;
-      cuts.clear();  // (warp, [lo, hi)) per piece
-      for (int64_t ww = w; ww < W && seg[(size_t)ww] < F + nt; ++ww) {
-        const int64_t lo = std::max<int64_t>(F, seg[(size_t)ww]);
-        const int64_t hi = std::min<int64_t>(F + nt, seg[(size_t)ww + 1]);
-        if (hi > lo) cuts.push_back(Cut{ww, lo, hi});
+      const int64_t Fe = F + (t.c_hi - t.c_lo);
+      while (w + 1 < W && sg[w + 1] <= F) ++w;
+      int64_t np = 0, we = w;
+      for (; we < W && sg[we] < Fe; ++we) np += std::min(Fe, sg[we + 1]) > std::max(F, sg[we]);
+      // a tile cut into np > 1 pieces: a merge item, and partial rows after
+      // the ones handed out so far
+      int32_t merge = -1;
+      int64_t part = -1;
+      if (np > 1) {
+        MergeItem& m = M[nmerges];
+        m.req = t.req;
+        m.kv_head = t.kv_head;
+        m.row0 = t.row0;
+        m.nrows = t.nrows;
+        m.part = (int32_t)partial_rows;
+        m.nsplits = (int32_t)np;
+        m.pad0 = m.pad1 = 0;
+        merge = (int32_t)nmerges++;
+        part = partial_rows;
+        partial_rows += np * t.nrows;
       }
-      const int64_t np = (int64_t)cuts.size();
-      const int32_t merge = np > 1 ? add_merge(t, np) : -1;
-      const int64_t part0 = np > 1 ? s->partial_rows - np * t.nrows : -1;
-      for (int64_t k = 0; k < np; ++k) {
-        const Cut& cu = cuts[(size_t)k];
-        // A warp whose segment starts inside this tile starts with this piece.
-        if (seg[(size_t)cu.warp] >= F)
-          s->warp_seg[(size_t)(dl.warp_off + phys(cu.warp))].piece =
-              (int32_t)((int64_t)s->pieces.size() - dl.piece_off);
-        add_piece(t, cu.lo, t.c_lo + (cu.lo - F), np > 1 ? (int32_t)(part0 + k * t.nrows) : -1,
-                  merge);
+      for (int64_t ww = w; ww < we; ++ww) {
+        const int64_t lo = std::max(F, sg[ww]), hi = std::min(Fe, sg[ww + 1]);
+        if (hi <= lo) continue;
+        // a warp whose segment starts inside this tile starts with this piece
+        if (sg[ww] >= F) ws[phys(ww)].piece = (int32_t)(npieces - dl.piece_off);
+        DecodePiece& pc = P[npieces++];
+        pc.req = t.req;
+        pc.kv_head = t.kv_head;
+        pc.row0 = t.row0;
+        pc.nrows = t.nrows;
+        pc.part = (int32_t)part;
+        pc.merge = merge;
+        pc.any_lo = (int32_t)t.any_lo;
+        pc.any_hi = (int32_t)t.any_hi;
+        pc.flat0 = (int32_t)lo;
+        pc.chunk0 = (int32_t)(t.c_lo + (lo - F));
+        pc.pad0 = pc.pad1 = 0;
+        if (part >= 0) part += t.nrows;
       }
-      s->max_splits = std::max(s->max_splits, np);
-      F += nt;
+      max_splits = std::max(max_splits, np);
+      F = Fe;
     }
-    dl.num_pieces = (int64_t)s->pieces.size() - dl.piece_off;
+    dl.num_pieces = npieces - dl.piece_off;
+    nwarps += W;
   }
+  s->num_pieces = npieces;
+  s->num_merges = nmerges;
+  s->partial_rows = partial_rows;
+  s->max_splits = max_splits;
   s->workspace_bytes = kvq::workspace_bytes(s->partial_rows, head_dim);
-
-  // 3) The plan image (pieces, per-warp first pieces, merge items, prefill
-  //    tiles, zeroed error word) in pinned host
-  //    memory, and a pooled device buffer for it.  The first attention call
-  //    uploads it on its own stream (no synchronisation here).
-  const size_t pieces_bytes = s->pieces.size() * sizeof(DecodePiece);
-  const size_t warps_bytes = s->warp_seg.size() * sizeof(WarpSeg);
-  const size_t merges_bytes = s->merges.size() * sizeof(MergeItem);
-  const size_t prefill_bytes = s->prefill.size() * sizeof(PrefillTile);
-  s->d_pieces_off = 0;
-  s->d_warps_off = kvq::align256(pieces_bytes);
-  s->d_merges_off = s->d_warps_off + kvq::align256(warps_bytes);
-  s->d_prefill_off = s->d_merges_off + kvq::align256(merges_bytes);
-  s->d_error_off = s->d_prefill_off + kvq::align256(prefill_bytes);
-  const size_t total = s->d_error_off + sizeof(int32_t);
-  s->image_bytes = total;
-  if (have_device) {
-    s->d_buf = pool_get(s->device, total, &s->d_buf_bytes);
-    if (!s->d_buf) {
-      delete s;
-      return KVQ_E_NO_MEMORY;
-    }
-    s->h_image = pinned_get(total, &s->h_image_bytes, &s->h_image_pinned);
-    if (!s->h_image) {
-      kvq_sched_destroy(s);
-      return KVQ_E_NO_MEMORY;
-    }
-    char* image = static_cast<char*>(s->h_image);
-    std::memset(image, 0, total);  // the error word starts at zero
-    if (pieces_bytes) std::memcpy(image + s->d_pieces_off, s->pieces.data(), pieces_bytes);
-    if (warps_bytes) std::memcpy(image + s->d_warps_off, s->warp_seg.data(), warps_bytes);
-    if (merges_bytes) std::memcpy(image + s->d_merges_off, s->merges.data(), merges_bytes);
-    if (prefill_bytes) std::memcpy(image + s->d_prefill_off, s->prefill.data(), prefill_bytes);
-  }
   *workspace_bytes = s->workspace_bytes;
   *out = s;
   return KVQ_OK;
@@ -624,8 +644,8 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
 int kvq_sched_get_plan_sizes(const kvq_sched_t* s, kvq_plan_sizes_t* out) {
   if (!s || !out) return KVQ_E_INVALID_ARG;
   std::memset(out, 0, sizeof(*out));
-  out->num_pieces = (int64_t)s->pieces.size();
-  out->num_merges = (int64_t)s->merges.size();
+  out->num_pieces = s->num_pieces;
+  out->num_merges = s->num_merges;
   out->num_prefill_tiles = (int64_t)s->prefill.size();
   for (int c = 0; c < 2; ++c) {
     out->num_chunks[c] = s->launch[c].num_chunks;
@@ -640,16 +660,16 @@ int kvq_sched_export_plan(const kvq_sched_t* s, kvq_plan_piece_t* pieces, int64_
                           int64_t merges_cap, kvq_plan_prefill_tile_t* tiles, int64_t tiles_cap) {
   if (!s) return KVQ_E_INVALID_ARG;
   const int64_t nw = (int64_t)s->launch[0].num_warps + s->launch[1].num_warps;
-  if ((pieces && pieces_cap < (int64_t)s->pieces.size()) || (warp_first_piece && warps_cap < nw) ||
-      (merges && merges_cap < (int64_t)s->merges.size()) ||
+  if ((pieces && pieces_cap < s->num_pieces) || (warp_first_piece && warps_cap < nw) ||
+      (merges && merges_cap < s->num_merges) ||
       (tiles && tiles_cap < (int64_t)s->prefill.size()))
     return KVQ_E_INVALID_ARG;
   for (int c = 0; c < 2; ++c) {
     const DecodeLaunch& dl = s->launch[c];
     if (pieces) {
       for (int64_t i = 0; i < dl.num_pieces; ++i) {
-        const DecodePiece& pc = s->pieces[(size_t)(dl.piece_off + i)];
-        const int64_t end = i + 1 < dl.num_pieces ? s->pieces[(size_t)(dl.piece_off + i + 1)].flat0
+        const DecodePiece& pc = s->h_pieces[dl.piece_off + i];
+        const int64_t end = i + 1 < dl.num_pieces ? s->h_pieces[dl.piece_off + i + 1].flat0
                                                   : dl.num_chunks;
         kvq_plan_piece_t& o = pieces[dl.piece_off + i];
         o.launch = c;
@@ -669,14 +689,14 @@ int kvq_sched_export_plan(const kvq_sched_t* s, kvq_plan_piece_t* pieces, int64_
     if (warp_first_piece) {
       const int64_t base = c == 0 ? 0 : s->launch[0].num_warps;
       for (int w = 0; w < dl.num_warps; ++w) {
-        const WarpSeg& ws = s->warp_seg[(size_t)(dl.warp_off + w)];
+        const WarpSeg& ws = s->h_warps[dl.warp_off + w];
         warp_first_piece[base + w] = ws.n > 0 ? (int32_t)(dl.piece_off + ws.piece) : -1;
       }
     }
   }
   if (merges) {
-    for (size_t i = 0; i < s->merges.size(); ++i) {
-      const MergeItem& m = s->merges[i];
+    for (int64_t i = 0; i < s->num_merges; ++i) {
+      const MergeItem& m = s->h_merges[i];
       merges[i] = kvq_plan_merge_t{m.req, m.kv_head, m.row0, m.nrows, m.part, m.nsplits};
     }
   }
@@ -702,8 +722,8 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->causal = s->causal;
   out->window = s->window;
   out->num_tiles = s->num_tiles;
-  out->num_pieces = (int64_t)s->pieces.size();
-  out->num_merge_items = (int64_t)s->merges.size();
+  out->num_pieces = s->num_pieces;
+  out->num_merge_items = s->num_merges;
   out->num_chunks = s->launch[0].num_chunks + s->launch[1].num_chunks;
   out->num_decode_warps = (int64_t)s->launch[0].num_warps + s->launch[1].num_warps;
   out->max_splits = s->max_splits;
@@ -715,7 +735,7 @@ int kvq_sched_get_info(const kvq_sched_t* s, kvq_sched_info_t* out) {
   out->prefill_smem_bytes =
       kvq::prefill_smem_bytes(s->head_dim, kvq::prefill_cta_group(s->dtype, s->head_dim));
   out->num_kernel_launches = (s->launch[0].num_chunks > 0) + (s->launch[1].num_chunks > 0) +
-                             (!s->merges.empty()) + (!s->prefill.empty());
+                             (s->num_merges > 0) + (!s->prefill.empty());
   out->prefill_cta_group = kvq::prefill_cta_group(s->dtype, s->head_dim);
   return KVQ_OK;
 }
@@ -856,7 +876,7 @@ int kvq_attention_with_kv_cache(const kvq_sched_t* s, int heads_q, int heads_kv,
     const int rc = kvq::launch_decode(p, s->dtype, head_dim, cls + 1, stream);
     if (rc != KVQ_OK) return rc;
   }
-  return kvq::launch_merge(p, head_dim, (int64_t)s->merges.size(), stream);
+  return kvq::launch_merge(p, head_dim, s->num_merges, stream);
 }
 
 // ---- the fused decode step ------------------------------------------------
