@@ -213,6 +213,44 @@ int sm_count() {
 
 int64_t ceil_div(int64_t a, int64_t b) { return (a + b - 1) / b; }
 
+// Prefill tiles in order of key range, longest first, equal ranges in their
+// given order: a stable LSD radix sort of (longest range - range), 11 bits a
+// pass (a mixed batch has thousands of tiles).
+void sort_longest_first(std::vector<PrefillTile>& v) {
+  const size_t n = v.size();
+  if (n < 2) return;
+  uint32_t longest = 0;
+  for (const PrefillTile& t : v) longest = std::max(longest, (uint32_t)std::max(0, t.kv_hi - t.kv_lo));
+  std::vector<uint32_t> key(n), idx(n), key2(n), idx2(n);
+  for (size_t i = 0; i < n; ++i) {
+    key[i] = longest - (uint32_t)std::max(0, v[i].kv_hi - v[i].kv_lo);
+    idx[i] = (uint32_t)i;
+  }
+  constexpr int kBits = 11;
+  constexpr uint32_t kMask = (1u << kBits) - 1;
+  uint32_t count[1u << kBits];
+  for (int shift = 0; shift < 32 && (longest >> shift) != 0; shift += kBits) {
+    std::memset(count, 0, sizeof(count));
+    for (size_t i = 0; i < n; ++i) ++count[(key[i] >> shift) & kMask];
+    uint32_t run = 0;
+    for (uint32_t d = 0; d <= kMask; ++d) {
+      const uint32_t c = count[d];
+      count[d] = run;
+      run += c;
+    }
+    for (size_t i = 0; i < n; ++i) {
+      const uint32_t pos = count[(key[i] >> shift) & kMask]++;
+      key2[pos] = key[i];
+      idx2[pos] = idx[i];
+    }
+    key.swap(key2);
+    idx.swap(idx2);
+  }
+  std::vector<PrefillTile> sorted(n);
+  for (size_t i = 0; i < n; ++i) sorted[i] = v[idx[i]];
+  v.swap(sorted);
+}
+
 // SM count assumed when planning without a device (GB300: 152 SMs).
 constexpr int kDefaultSmCount = 152;
 
@@ -355,6 +393,26 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
   //    n-tile (class 0), larger ones two (class 1).
   std::vector<Tile> tiles[2];
   s->max_chunk = 0;
+  {
+    // capacities first (a prefill of many requests has thousands of tiles)
+    size_t n_prefill = 0, n_tiles[2] = {0, 0};
+    for (int r = 0; r < num_req; ++r) {
+      const int64_t rows = ((int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r]) * G;
+      if (rows == 0) continue;
+      if (rows > kvq::kTileMaxRows) {
+        n_prefill += (size_t)heads_kv * (size_t)ceil_div(rows, kvq::kPrefillRows);
+      } else {
+        n_tiles[rows > 8 ? 1 : 0] += (size_t)heads_kv;
+      }
+    }
+    s->prefill.reserve(n_prefill);
+    tiles[0].reserve(n_tiles[0]);
+    tiles[1].reserve(n_tiles[1]);
+  }
+  // A request's row tiles: their key ranges do not depend on the kv head, so
+  // each is worked out once and copied for every head (heads outermost).
+  std::vector<PrefillTile> row_prefill;
+  std::vector<Tile> row_tiles;
   for (int r = 0; r < num_req; ++r) {
     const int64_t L = seq_lens_host[r];
     const int64_t Q = (int64_t)query_start_loc_host[r + 1] - query_start_loc_host[r];
@@ -362,44 +420,53 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
     const int64_t rows = Q * G;
     if (rows > kvq::kTileMaxRows) {
       // Prefill: 128-row tiles on the tensor cores.
-      for (int h = 0; h < heads_kv; ++h) {
-        for (int64_t row0 = 0; row0 < rows; row0 += kvq::kPrefillRows) {
-          const int64_t nrows = std::min<int64_t>(kvq::kPrefillRows, rows - row0);
-          const int64_t p_min = L - Q + row0 / G;
-          const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
-          PrefillTile pt;
-          pt.req = r;
-          pt.kv_head = h;
-          pt.row0 = (int32_t)row0;
-          pt.nrows = (int32_t)nrows;
-          pt.kv_hi = (int32_t)(s->causal ? p_max + 1 : L);
-          pt.kv_lo = (int32_t)(s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0);
-          pt.q0 = query_start_loc_host[r];
-          pt.pos0 = (int32_t)(L - Q);
-          s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)((pt.kv_hi - 1) / kvq::kChunkTokens));
-          s->prefill.push_back(pt);
-        }
-      }
-      continue;
-    }
-    for (int h = 0; h < heads_kv; ++h) {
-      for (int64_t row0 = 0; row0 < rows; row0 += kvq::kTileMaxRows) {
-        const int64_t nrows = std::min<int64_t>(kvq::kTileMaxRows, rows - row0);
+      row_prefill.clear();
+      for (int64_t row0 = 0; row0 < rows; row0 += kvq::kPrefillRows) {
+        const int64_t nrows = std::min<int64_t>(kvq::kPrefillRows, rows - row0);
         const int64_t p_min = L - Q + row0 / G;
         const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
-        Tile t;
-        t.req = r;
-        t.kv_head = h;
-        t.row0 = (int)row0;
-        t.nrows = (int)nrows;
-        t.any_hi = s->causal ? p_max + 1 : L;
-        t.any_lo = s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0;
-        t.c_lo = t.any_lo / kvq::kChunkTokens;
-        t.c_hi = ceil_div(t.any_hi, kvq::kChunkTokens);
-        s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)(t.c_hi - 1));
-        tiles[nrows > 8 ? 1 : 0].push_back(t);
+        PrefillTile pt;
+        pt.req = r;
+        pt.kv_head = 0;
+        pt.row0 = (int32_t)row0;
+        pt.nrows = (int32_t)nrows;
+        pt.kv_hi = (int32_t)(s->causal ? p_max + 1 : L);
+        pt.kv_lo = (int32_t)(s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0);
+        pt.q0 = query_start_loc_host[r];
+        pt.pos0 = (int32_t)(L - Q);
+        s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)((pt.kv_hi - 1) / kvq::kChunkTokens));
+        row_prefill.push_back(pt);
       }
+      for (int h = 0; h < heads_kv; ++h)
+        for (const PrefillTile& pt : row_prefill) {
+          s->prefill.push_back(pt);
+          s->prefill.back().kv_head = h;
+        }
+      continue;
     }
+    row_tiles.clear();
+    for (int64_t row0 = 0; row0 < rows; row0 += kvq::kTileMaxRows) {
+      const int64_t nrows = std::min<int64_t>(kvq::kTileMaxRows, rows - row0);
+      const int64_t p_min = L - Q + row0 / G;
+      const int64_t p_max = L - Q + (row0 + nrows - 1) / G;
+      Tile t;
+      t.req = r;
+      t.kv_head = 0;
+      t.row0 = (int)row0;
+      t.nrows = (int)nrows;
+      t.any_hi = s->causal ? p_max + 1 : L;
+      t.any_lo = s->window > 0 ? std::max<int64_t>(0, p_min - s->window + 1) : 0;
+      t.c_lo = t.any_lo / kvq::kChunkTokens;
+      t.c_hi = ceil_div(t.any_hi, kvq::kChunkTokens);
+      s->max_chunk = std::max<int32_t>(s->max_chunk, (int32_t)(t.c_hi - 1));
+      row_tiles.push_back(t);
+    }
+    for (int h = 0; h < heads_kv; ++h)
+      for (const Tile& t : row_tiles) {
+        std::vector<Tile>& v = tiles[t.nrows > 8 ? 1 : 0];
+        v.push_back(t);
+        v.back().kv_head = h;
+      }
   }
   s->num_tiles = (int64_t)(tiles[0].size() + tiles[1].size());
   // Longest prefill tiles first, so the tail of the grid is short tiles.
@@ -434,10 +501,7 @@ int kvq_get_scheduler_metadata(int num_req, int heads_q, int heads_kv, int head_
       s->prefill.push_back(q.second);
     }
   } else {
-    std::stable_sort(s->prefill.begin(), s->prefill.end(),
-                     [](const PrefillTile& a, const PrefillTile& b) {
-                       return (a.kv_hi - a.kv_lo) > (b.kv_hi - b.kv_lo);
-                     });
+    sort_longest_first(s->prefill);
   }
 
   // 2) Per class of row tiles: the chunk count, the tile order and the warp
