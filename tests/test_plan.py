@@ -81,6 +81,11 @@ def check_plan(seq_lens, query_lens, hq=32, hkv=8, D=128, causal=True, window=0,
     else:
         assert len(allt) == len(got)
         spans = [t[5] - t[4] for t in got]
+        # equal key ranges keep (request, kv head, first row) order: the deal
+        # is deterministic
+        for a, b in zip(got, got[1:]):
+            if a[5] - a[4] == b[5] - b[4]:
+                assert a[:3] < b[:3]
     assert all(a >= b for a, b in zip(spans, spans[1:]))
 
     # decode tiles: the derived set, each in its launch class
