@@ -371,8 +371,8 @@ KVQ_API int kvq_decode_step_host_io(const void* host_in, void* dev_in, size_t in
  * KVQ_E_UNSUPPORTED.  host_out must be pinned.
  * Every buffer must stay allocated, in place, until the graph is destroyed.
  * Errors: those of kvq_decode_step_host_io (nothing is created then),
- * KVQ_E_CUDA for a failed capture.  Allocates the graph, its executable
- * form and a private capture stream; *graph NULL on error. */
+ * KVQ_E_NO_MEMORY, KVQ_E_CUDA for a failed capture.  Allocates the graph,
+ * its executable form and a private capture stream; *graph NULL on error. */
 typedef struct kvq_step_graph kvq_step_graph_t;
 KVQ_API int kvq_decode_step_graph_create(const void* host_in, void* dev_in, size_t in_bytes,
                                          void* host_out, size_t out_bytes, int num_req,

@@ -1235,8 +1235,14 @@ int kvq_decode_step_graph_create(const void* host_in, void* dev_in, size_t in_by
   HostIo io;
   int rc = host_io_resolve(host_in, dev_in, in_bytes, host_out, out_bytes, out, true, &io);
   if (rc != KVQ_OK) return rc;
+  // the launch configuration is looked up (and kept) before the capture, so
+  // the capture holds stream work only
+  size_t need = 0;
+  rc = kvq_decode_step_workspace_size(num_req, heads_q, heads_kv, head_dim, dtype, max_query_len,
+                                      alibi_slopes != nullptr, &need);
+  if (rc != KVQ_OK) return rc;
   kvq_step_graph_t* g = new (std::nothrow) kvq_step_graph_t();
-  if (!g) return KVQ_E_CUDA;
+  if (!g) return KVQ_E_NO_MEMORY;
   if (cudaStreamCreateWithFlags(&g->capture, cudaStreamNonBlocking) != cudaSuccess ||
       cudaStreamBeginCapture(g->capture, cudaStreamCaptureModeThreadLocal) != cudaSuccess) {
     cudaGetLastError();
